@@ -1,0 +1,270 @@
+"""Plain CPU oracle of the PPO learner step (fp64), driven through ctypes.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
+(``policy_rl_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``ppo_oracle.c``; this module only compiles it (gcc,
+``-ffp-contract=off`` so that no fused multiply-add changes the rounding of the
+plain C expressions) and marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ppo_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "libppo_oracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libppo_oracle.so``."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    hdr = os.path.join(_HERE, "ppo_oracle.h")
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(hdr))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(
+            ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-Wall", "-shared", "-fPIC",
+             _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Net(ctypes.Structure):
+    _fields_ = [("obs_dim", ctypes.c_int32), ("h1", ctypes.c_int32), ("h2", ctypes.c_int32),
+                ("act", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("head_n", ctypes.c_int32 * 8), ("n_gauss", ctypes.c_int32)]
+
+
+class _LossCfg(ctypes.Structure):
+    _fields_ = [("clip", ctypes.c_double), ("vf_coef", ctypes.c_double),
+                ("ent_coef", ctypes.c_double)]
+
+
+class _Hyper(ctypes.Structure):
+    _fields_ = [("gamma", ctypes.c_double), ("lambda_", ctypes.c_double),
+                ("clip", ctypes.c_double), ("vf_coef", ctypes.c_double),
+                ("ent_coef", ctypes.c_double), ("lr", ctypes.c_double),
+                ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("adam_eps", ctypes.c_double), ("max_grad_norm", ctypes.c_double),
+                ("seed", ctypes.c_uint32)]
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_D = ctypes.c_double
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        L = _lib
+        L.orc_mulberry32_next.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        L.orc_mulberry32_next.restype = ctypes.c_uint32
+        L.orc_gae.argtypes = [_I64, _I64, _P, _P, _P, _P, _D, _D, _P, _P]
+        L.orc_moments.argtypes = [_I64, _P, ctypes.POINTER(_D), ctypes.POINTER(_D)]
+        L.orc_normalize.argtypes = [_I64, _P, _D, _D, _P]
+        L.orc_perm.argtypes = [ctypes.c_uint32, _I64, _I64, _P]
+        L.orc_out_cols.argtypes = [ctypes.POINTER(_Net)]
+        L.orc_out_cols.restype = _I64
+        L.orc_num_params.argtypes = [ctypes.POINTER(_Net)]
+        L.orc_num_params.restype = _I64
+        L.orc_forward.argtypes = [ctypes.POINTER(_Net), _P, _P, _P]
+        L.orc_loss_grad.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_LossCfg), _P, _I64, _P,
+                                    _P, _P, _P, _P, _P, _P, ctypes.c_int, _D, _D, _P, _P, _P]
+        L.orc_loss_grad.restype = _D
+        L.orc_clip_grad_norm.argtypes = [_I64, _P, _D]
+        L.orc_clip_grad_norm.restype = _D
+        L.orc_adam.argtypes = [_I64, _P, _P, _P, _P, _I64, _D, _D, _D, _D]
+        L.orc_update.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_Hyper), _I64, _I64, _I64, _I64,
+                                 _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                 ctypes.POINTER(_I64), _P, _P, _P]
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _as(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+@dataclass
+class Net:
+    """MLP actor-critic shape.  act: 0 tanh, 1 ReLU."""
+    obs_dim: int
+    h1: int
+    h2: int
+    act: int = 0
+    heads: tuple = (3, 2, 2)
+    n_gauss: int = 0
+
+    def c(self) -> _Net:
+        hn = (ctypes.c_int32 * 8)(*(list(self.heads) + [0] * (8 - len(self.heads))))
+        return _Net(self.obs_dim, self.h1, self.h2, self.act, len(self.heads), hn, self.n_gauss)
+
+    @property
+    def out_cols(self) -> int:
+        return int(sum(self.heads)) + self.n_gauss + 1
+
+    @property
+    def num_params(self) -> int:
+        D, H1, H2, C = self.obs_dim, self.h1, self.h2, self.out_cols
+        return H1 * D + H1 + H2 * H1 + H2 + C * H2 + C + self.n_gauss
+
+
+@dataclass
+class Hyper:
+    gamma: float = 0.99
+    lam: float = 0.95
+    clip: float = 0.2
+    vf_coef: float = 0.5
+    ent_coef: float = 0.01
+    lr: float = 2.5e-4
+    beta1: float = 0.9
+    beta2: float = 0.999
+    adam_eps: float = 1e-8
+    max_grad_norm: float = 0.5
+    seed: int = 0
+
+    def c(self) -> _Hyper:
+        return _Hyper(self.gamma, self.lam, self.clip, self.vf_coef, self.ent_coef, self.lr,
+                      self.beta1, self.beta2, self.adam_eps, self.max_grad_norm, self.seed)
+
+
+def mulberry32_stream(seed: int, count: int) -> np.ndarray:
+    """First ``count`` raw uint32 draws of the stream seeded with ``seed``."""
+    L = lib()
+    st = ctypes.c_uint32(seed & 0xFFFFFFFF)
+    return np.array([L.orc_mulberry32_next(ctypes.byref(st)) for _ in range(count)],
+                    dtype=np.uint32)
+
+
+def gae(rew, val, done, boot, gamma, lam):
+    rew, val, done = (_as(x, np.float32) for x in (rew, val, done))
+    boot = _as(boot, np.float32)
+    T, N = rew.shape
+    adv = np.empty((T, N), np.float64)
+    ret = np.empty((T, N), np.float64)
+    lib().orc_gae(T, N, _ptr(rew), _ptr(val), _ptr(done), _ptr(boot), gamma, lam,
+                  _ptr(adv), _ptr(ret))
+    return adv, ret
+
+
+def moments(x):
+    x = _as(x, np.float64).ravel()
+    m, s = _D(), _D()
+    lib().orc_moments(x.size, _ptr(x), ctypes.byref(m), ctypes.byref(s))
+    return m.value, s.value
+
+
+def normalize(x, mean, std):
+    x = _as(x, np.float64)
+    out = np.empty_like(x)
+    lib().orc_normalize(x.size, _ptr(x), mean, std, _ptr(out))
+    return out
+
+
+def perm(seed: int, epoch: int, B: int) -> np.ndarray:
+    out = np.empty(B, np.int32)
+    lib().orc_perm(seed & 0xFFFFFFFF, epoch, B, _ptr(out))
+    return out
+
+
+def forward(net: Net, params, x):
+    params = _as(params, np.float64)
+    x = _as(x, np.float32)
+    rows = x.reshape(-1, net.obs_dim)
+    out = np.empty((rows.shape[0], net.out_cols), np.float64)
+    cn = net.c()
+    for i in range(rows.shape[0]):
+        r = np.ascontiguousarray(rows[i])
+        o = np.empty(net.out_cols, np.float64)
+        lib().orc_forward(ctypes.byref(cn), _ptr(params), _ptr(r), _ptr(o))
+        out[i] = o
+    return out
+
+
+def loss_grad(net: Net, params, idx, obs, act_disc, act_cont, logp_old, adv, ret,
+              clip=0.2, vf_coef=0.5, ent_coef=0.01, normalize=False, adv_mean=0.0,
+              adv_std=1.0):
+    """Returns (loss, grad[P], stats6[6], scale6[6])."""
+    params = _as(params, np.float64)
+    idx = _as(idx, np.int32)
+    obs = _as(obs, np.float32)
+    act_disc = _as(act_disc, np.int32)
+    act_cont = _as(act_cont if act_cont is not None else np.zeros((1,), np.float32), np.float32)
+    logp_old = _as(logp_old, np.float32)
+    adv = _as(adv, np.float64)
+    ret = _as(ret, np.float64)
+    grad = np.empty(net.num_params, np.float64)
+    st = np.empty(6, np.float64)
+    sc = np.empty(6, np.float64)
+    cfg = _LossCfg(clip, vf_coef, ent_coef)
+    cn = net.c()
+    loss = lib().orc_loss_grad(ctypes.byref(cn), ctypes.byref(cfg), _ptr(params), idx.size,
+                               _ptr(idx), _ptr(obs), _ptr(act_disc), _ptr(act_cont),
+                               _ptr(logp_old), _ptr(adv), _ptr(ret), int(bool(normalize)),
+                               adv_mean, adv_std, _ptr(grad), _ptr(st), _ptr(sc))
+    return loss, grad, st, sc
+
+
+def clip_grad_norm(g, max_norm):
+    g = _as(g, np.float64).copy()
+    n = lib().orc_clip_grad_norm(g.size, _ptr(g), max_norm)
+    return n, g
+
+
+def adam(p, g, m, v, step, lr, beta1=0.9, beta2=0.999, eps=1e-8):
+    p = _as(p, np.float64).copy()
+    m = _as(m, np.float64).copy()
+    v = _as(v, np.float64).copy()
+    g = _as(g, np.float64)
+    lib().orc_adam(p.size, _ptr(p), _ptr(g), _ptr(m), _ptr(v), step, lr, beta1, beta2, eps)
+    return p, m, v
+
+
+@dataclass
+class UpdateResult:
+    params: np.ndarray
+    m: np.ndarray
+    v: np.ndarray
+    step: int
+    stats: np.ndarray
+    adv: np.ndarray
+    ret: np.ndarray
+
+
+def update(net: Net, hp: Hyper, T, N, epochs, minibatches, obs, act_disc, act_cont, logp_old,
+           val, rew, done, boot, params, m=None, v=None, step=0) -> UpdateResult:
+    P = net.num_params
+    params = _as(params, np.float64).copy()
+    m = np.zeros(P) if m is None else _as(m, np.float64).copy()
+    v = np.zeros(P) if v is None else _as(v, np.float64).copy()
+    stats = np.empty((epochs * minibatches, 6), np.float64)
+    adv = np.empty(T * N, np.float64)
+    ret = np.empty(T * N, np.float64)
+    st = _I64(step)
+    arrs = [_as(obs, np.float32), _as(act_disc, np.int32),
+            _as(act_cont if act_cont is not None else np.zeros(1), np.float32),
+            _as(logp_old, np.float32), _as(val, np.float32), _as(rew, np.float32),
+            _as(done, np.float32), _as(boot, np.float32)]
+    cn, ch = net.c(), hp.c()
+    lib().orc_update(ctypes.byref(cn), ctypes.byref(ch), T, N, epochs, minibatches,
+                     *[_ptr(a) for a in arrs], _ptr(params), _ptr(m), _ptr(v),
+                     ctypes.byref(st), _ptr(stats), _ptr(adv), _ptr(ret))
+    return UpdateResult(params, m, v, st.value, stats, adv.reshape(T, N), ret.reshape(T, N))

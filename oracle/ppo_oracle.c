@@ -1,0 +1,413 @@
+/*
+ * ppo_oracle.c -- plain CPU reference of the PPO learner step (fp64).
+ *
+ * TEST INFRASTRUCTURE ONLY: used by tests/, the package smoke check and the
+ * bench's CPU-baseline leg.  Shares no code with the CUDA library.
+ * Every function follows the passage cited above it, in the pages' order;
+ * sums run in the plain order of their definition, in double precision.
+ */
+#include "ppo_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* "PlayTrain", Appendix F.2 listing "seeded RNG" (mulberry32).
+ * The state is a counter advanced by 0x6D2B79F5 per draw; the output is a
+ * xor-shift / multiply mix of it.  The listing's Math.imul and >>> are 32-bit
+ * wrapping multiply and logical shift, i.e. uint32_t arithmetic here. */
+uint32_t orc_mulberry32_next(uint32_t *state)
+{
+    uint32_t t = *state + 0x6D2B79F5u;
+    *state = t;
+    uint32_t n = (t ^ (t >> 15)) * (t | 1u);
+    n ^= n + (n ^ (n >> 7)) * (n | 61u);
+    return n ^ (n >> 14);
+}
+
+/* ------------------------------------------------------------------------ */
+/* "Teaching Mario to speedrun", sec. 6 "Better advantages":
+ *   delta_t = r_t + gamma V(s_{t+1}) - V(s_t)
+ *   A_t     = delta_t + (gamma lambda) delta_{t+1} + (gamma lambda)^2 delta_{t+2} + ...
+ * written as the backward recursion A_t = delta_t + gamma lambda A_{t+1}.
+ * Sec. 7: terminals are 1 where an episode just ended, so a done at step t
+ * stops both the bootstrap V(s_{t+1}) and the propagation of A_{t+1}.
+ * The return used by the value loss is the lambda-return A_t + V(s_t). */
+void orc_gae(int64_t T, int64_t N, const float *rew, const float *val,
+             const float *done, const float *boot, double gamma, double lambda,
+             double *adv, double *ret)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        double next_value = (double)boot[n];
+        double next_adv = 0.0;
+        for (int64_t t = T - 1; t >= 0; --t) {
+            int64_t i = t * N + n;
+            double alive = (done[i] != 0.0f) ? 0.0 : 1.0;
+            double v = (double)val[i];
+            double delta = (double)rew[i] + gamma * alive * next_value - v;
+            double a = delta + gamma * lambda * alive * next_adv;
+            adv[i] = a;
+            ret[i] = a + v;
+            next_value = v;
+            next_adv = a;
+        }
+    }
+}
+
+/* Global advantage statistics: mean and the unbiased standard deviation. */
+void orc_moments(int64_t n, const double *x, double *mean, double *std_unbiased)
+{
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s += x[i];
+    double mu = (n > 0) ? s / (double)n : 0.0;
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; ++i) ss += (x[i] - mu) * (x[i] - mu);
+    *mean = mu;
+    *std_unbiased = (n > 1) ? sqrt(ss / (double)(n - 1)) : 0.0;
+}
+
+void orc_normalize(int64_t n, const double *x, double mean, double std_, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = (x[i] - mean) / (std_ + 1e-8);
+}
+
+/* ------------------------------------------------------------------------ */
+/* "Teaching Mario to speedrun", sec. 6: "for minibatch in shuffle(batch)".
+ * The shuffle of epoch e sorts the indices by mulberry32 keys, key i being
+ * draw number e*B + i of the stream seeded with `seed`; equal keys keep index
+ * order.  Skipping e*B draws is adding e*B*0x6D2B79F5 to the counter. */
+typedef struct { uint32_t key; int32_t idx; } orc_kv;
+
+static int orc_kv_cmp(const void *a, const void *b)
+{
+    const orc_kv *x = (const orc_kv *)a, *y = (const orc_kv *)b;
+    if (x->key != y->key) return x->key < y->key ? -1 : 1;
+    return (x->idx > y->idx) - (x->idx < y->idx);
+}
+
+void orc_perm(uint32_t seed, int64_t epoch, int64_t B, int32_t *perm)
+{
+    orc_kv *kv = (orc_kv *)malloc((size_t)B * sizeof(orc_kv));
+    uint32_t state = seed + (uint32_t)((uint64_t)epoch * (uint64_t)B) * 0x6D2B79F5u;
+    for (int64_t i = 0; i < B; ++i) {
+        kv[i].key = orc_mulberry32_next(&state);
+        kv[i].idx = (int32_t)i;
+    }
+    qsort(kv, (size_t)B, sizeof(orc_kv), orc_kv_cmp);
+    for (int64_t i = 0; i < B; ++i) perm[i] = kv[i].idx;
+    free(kv);
+}
+
+/* ------------------------------------------------------------------------ */
+/* "Teaching Mario to speedrun", sec. 6 "The policy and the value are one
+ * network": observation in, one group of logits per action head plus one
+ * value out.  The MLP is h1 = act(W1 x + b1), h2 = act(W2 h1 + b2),
+ * z = W3 h2 + b3.  Hybrid action spaces ("boesch.dev DDNet RL", "What the
+ * agent sees and does") add diagonal-Gaussian means before the value. */
+int64_t orc_out_cols(const orc_net *net)
+{
+    int64_t c = 0;
+    for (int h = 0; h < net->n_heads; ++h) c += net->head_n[h];
+    return c + net->n_gauss + 1;
+}
+
+int64_t orc_num_params(const orc_net *net)
+{
+    int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
+    return H1 * D + H1 + H2 * H1 + H2 + C * H2 + C + net->n_gauss;
+}
+
+typedef struct {
+    const double *W1, *b1, *W2, *b2, *W3, *b3, *logstd;
+} orc_views;
+
+static orc_views orc_split(const orc_net *net, const double *p)
+{
+    int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
+    orc_views v;
+    v.W1 = p;
+    v.b1 = v.W1 + H1 * D;
+    v.W2 = v.b1 + H1;
+    v.b2 = v.W2 + H2 * H1;
+    v.W3 = v.b2 + H2;
+    v.b3 = v.W3 + C * H2;
+    v.logstd = v.b3 + C;
+    return v;
+}
+
+static double orc_act(int act, double pre)
+{
+    return act == 0 ? tanh(pre) : (pre > 0.0 ? pre : 0.0);
+}
+
+/* derivative of the activation, from its input and output:
+ * tanh' = 1 - tanh^2, ReLU' = 1[pre > 0] (0 at pre == 0). */
+static double orc_act_grad(int act, double pre, double post)
+{
+    return act == 0 ? 1.0 - post * post : (pre > 0.0 ? 1.0 : 0.0);
+}
+
+static void orc_forward_full(const orc_net *net, const orc_views *w, const float *x,
+                             double *pre1, double *h1, double *pre2, double *h2, double *z)
+{
+    int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
+    for (int64_t j = 0; j < H1; ++j) {
+        double s = w->b1[j];
+        for (int64_t k = 0; k < D; ++k) s += w->W1[j * D + k] * (double)x[k];
+        pre1[j] = s;
+        h1[j] = orc_act(net->act, s);
+    }
+    for (int64_t j = 0; j < H2; ++j) {
+        double s = w->b2[j];
+        for (int64_t k = 0; k < H1; ++k) s += w->W2[j * H1 + k] * h1[k];
+        pre2[j] = s;
+        h2[j] = orc_act(net->act, s);
+    }
+    for (int64_t c = 0; c < C; ++c) {
+        double s = w->b3[c];
+        for (int64_t k = 0; k < H2; ++k) s += w->W3[c * H2 + k] * h2[k];
+        z[c] = s;
+    }
+}
+
+void orc_forward(const orc_net *net, const double *params, const float *x, double *z)
+{
+    orc_views w = orc_split(net, params);
+    double *buf = (double *)malloc(sizeof(double) * 2 * (size_t)(net->h1 + net->h2));
+    orc_forward_full(net, &w, x, buf, buf + net->h1, buf + 2 * net->h1,
+                     buf + 2 * net->h1 + net->h2, z);
+    free(buf);
+}
+
+/* ------------------------------------------------------------------------ */
+/* "Teaching Mario to speedrun", sec. 6 "Don't move too far at once":
+ *   ratio  = new_prob(action) / old_prob(action)
+ *   loss_pi = -min(ratio A, clip(ratio, 1 - eps, 1 + eps) A)
+ *   loss_V  = (value - return)^2
+ *   loss    = loss_pi + c_v loss_V - c_e entropy
+ * averaged over the minibatch.  A multi-discrete action's probability is the
+ * product of its heads' softmax probabilities (sec. 6: each head sampled
+ * separately), so log-probabilities and entropies add over heads.  A Gaussian
+ * dimension g with mean mu_g and learned log-std s_g adds
+ *   log N(a; mu, e^s) = -(a-mu)^2 / (2 e^{2s}) - s - ln(2 pi)/2
+ * and entropy 1/2 + ln(2 pi)/2 + s.
+ * Gradient of the log-probability w.r.t. head logits: 1[k == a] - p_k
+ * (sec. 5, "the gradient of log probs[action]").  The clipped branch, where
+ * min() picks the clipped term, has zero gradient w.r.t. the ratio. */
+double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *params,
+                     int64_t mb, const int32_t *idx,
+                     const float *obs, const int32_t *act_disc, const float *act_cont,
+                     const float *logp_old, const double *adv, const double *ret,
+                     int normalize, double adv_mean, double adv_std,
+                     double *grad, double *stats6, double *scale6)
+{
+    const int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
+    const int64_t NH = net->n_heads, G = net->n_gauss;
+    const int64_t P = orc_num_params(net);
+    const double LOG_2PI = log(2.0 * acos(-1.0));
+    orc_views w = orc_split(net, params);
+
+    memset(grad, 0, sizeof(double) * (size_t)P);
+    double *gW1 = grad, *gb1 = gW1 + H1 * D, *gW2 = gb1 + H1, *gb2 = gW2 + H2 * H1;
+    double *gW3 = gb2 + H2, *gb3 = gW3 + C * H2, *glogstd = gb3 + C;
+
+    double *pre1 = (double *)malloc(sizeof(double) * (size_t)H1);
+    double *h1 = (double *)malloc(sizeof(double) * (size_t)H1);
+    double *pre2 = (double *)malloc(sizeof(double) * (size_t)H2);
+    double *h2 = (double *)malloc(sizeof(double) * (size_t)H2);
+    double *z = (double *)malloc(sizeof(double) * (size_t)C);
+    double *logprob = (double *)malloc(sizeof(double) * (size_t)C);
+    double *dz = (double *)malloc(sizeof(double) * (size_t)C);
+    double *dh2 = (double *)malloc(sizeof(double) * (size_t)H2);
+    double *dh1 = (double *)malloc(sizeof(double) * (size_t)H1);
+
+    double sum[6] = {0, 0, 0, 0, 0, 0}, asum[6] = {0, 0, 0, 0, 0, 0};
+    const double inv_mb = 1.0 / (double)mb;
+
+    for (int64_t r = 0; r < mb; ++r) {
+        const int64_t row = idx[r];
+        const float *x = obs + row * D;
+        orc_forward_full(net, &w, x, pre1, h1, pre2, h2, z);
+
+        /* log-probability and entropy of the taken action */
+        double logp = 0.0, ent = 0.0;
+        int64_t off = 0;
+        double head_ent[8];
+        for (int64_t h = 0; h < NH; ++h) {
+            int64_t n = net->head_n[h];
+            double zmax = z[off];
+            for (int64_t k = 1; k < n; ++k) if (z[off + k] > zmax) zmax = z[off + k];
+            double se = 0.0;
+            for (int64_t k = 0; k < n; ++k) se += exp(z[off + k] - zmax);
+            double lse = zmax + log(se);
+            double eh = 0.0;
+            for (int64_t k = 0; k < n; ++k) {
+                logprob[off + k] = z[off + k] - lse;
+                eh -= exp(logprob[off + k]) * logprob[off + k];
+            }
+            head_ent[h] = eh;
+            ent += eh;
+            logp += logprob[off + act_disc[row * NH + h]];
+            off += n;
+        }
+        for (int64_t g = 0; g < G; ++g) {
+            double mu = z[off + g], s = w.logstd[g];
+            double a = (double)act_cont[row * G + g];
+            double var = exp(2.0 * s);
+            logp += -(a - mu) * (a - mu) / (2.0 * var) - s - 0.5 * LOG_2PI;
+            ent += 0.5 + 0.5 * LOG_2PI + s;
+        }
+        const double value = z[C - 1];
+
+        double A = adv[row];
+        if (normalize) A = (A - adv_mean) / (adv_std + 1e-8);
+        const double R = ret[row];
+        const double log_ratio = logp - (double)logp_old[row];
+        const double ratio = exp(log_ratio);
+        const double lo = 1.0 - cfg->clip, hi = 1.0 + cfg->clip;
+        const double clipped = ratio < lo ? lo : (ratio > hi ? hi : ratio);
+        const double s1 = ratio * A, s2 = clipped * A;
+        const double pg = -(s1 < s2 ? s1 : s2);
+        const double vl = (value - R) * (value - R);
+        const double total = pg + cfg->vf_coef * vl - cfg->ent_coef * ent;
+        const double clipfrac = fabs(ratio - 1.0) > cfg->clip ? 1.0 : 0.0;
+        const double kl = (ratio - 1.0) - log_ratio;
+        const double terms[6] = {total, pg, vl, ent, clipfrac, kl};
+        for (int q = 0; q < 6; ++q) { sum[q] += terms[q]; asum[q] += fabs(terms[q]); }
+
+        /* dL/dlogp: the unclipped term is active when s1 <= s2 */
+        const double g_logp = (s1 <= s2) ? -A * ratio * inv_mb : 0.0;
+        const double g_ent = -cfg->ent_coef * inv_mb;
+
+        off = 0;
+        for (int64_t h = 0; h < NH; ++h) {
+            int64_t n = net->head_n[h];
+            int64_t a = act_disc[row * NH + h];
+            for (int64_t k = 0; k < n; ++k) {
+                double p = exp(logprob[off + k]);
+                double dlogp_dz = (k == a ? 1.0 : 0.0) - p;
+                double dent_dz = -p * (logprob[off + k] + head_ent[h]);
+                dz[off + k] = g_logp * dlogp_dz + g_ent * dent_dz;
+            }
+            off += n;
+        }
+        for (int64_t g = 0; g < G; ++g) {
+            double mu = z[off + g], s = w.logstd[g];
+            double a = (double)act_cont[row * G + g];
+            double var = exp(2.0 * s);
+            dz[off + g] = g_logp * (a - mu) / var;
+            glogstd[g] += g_logp * ((a - mu) * (a - mu) / var - 1.0) + g_ent * 1.0;
+        }
+        dz[C - 1] = cfg->vf_coef * 2.0 * (value - R) * inv_mb;
+
+        /* backward through z = W3 h2 + b3 */
+        for (int64_t j = 0; j < H2; ++j) dh2[j] = 0.0;
+        for (int64_t c = 0; c < C; ++c) {
+            gb3[c] += dz[c];
+            for (int64_t j = 0; j < H2; ++j) {
+                gW3[c * H2 + j] += dz[c] * h2[j];
+                dh2[j] += dz[c] * w.W3[c * H2 + j];
+            }
+        }
+        /* through h2 = act(W2 h1 + b2) */
+        for (int64_t k = 0; k < H1; ++k) dh1[k] = 0.0;
+        for (int64_t j = 0; j < H2; ++j) {
+            double dpre = dh2[j] * orc_act_grad(net->act, pre2[j], h2[j]);
+            gb2[j] += dpre;
+            for (int64_t k = 0; k < H1; ++k) {
+                gW2[j * H1 + k] += dpre * h1[k];
+                dh1[k] += dpre * w.W2[j * H1 + k];
+            }
+        }
+        /* through h1 = act(W1 x + b1) */
+        for (int64_t j = 0; j < H1; ++j) {
+            double dpre = dh1[j] * orc_act_grad(net->act, pre1[j], h1[j]);
+            gb1[j] += dpre;
+            for (int64_t k = 0; k < D; ++k) gW1[j * D + k] += dpre * (double)x[k];
+        }
+    }
+
+    for (int q = 0; q < 6; ++q) {
+        if (stats6) stats6[q] = sum[q] * inv_mb;
+        if (scale6) scale6[q] = asum[q] * inv_mb;
+    }
+    free(pre1); free(h1); free(pre2); free(h2); free(z); free(logprob);
+    free(dz); free(dh2); free(dh1);
+    return sum[0] * inv_mb;
+}
+
+/* ------------------------------------------------------------------------ */
+/* "PlayTrain", Table 8 (PPO column): gradient-norm clip 0.5.  The global L2
+ * norm over all parameters; if above max_norm, scale by max_norm/(norm+1e-6). */
+double orc_clip_grad_norm(int64_t P, double *g, double max_norm)
+{
+    double ss = 0.0;
+    for (int64_t i = 0; i < P; ++i) ss += g[i] * g[i];
+    double norm = sqrt(ss);
+    if (max_norm > 0.0) {
+        double coef = max_norm / (norm + 1e-6);
+        if (coef < 1.0)
+            for (int64_t i = 0; i < P; ++i) g[i] *= coef;
+    }
+    return norm;
+}
+
+/* "PlayTrain", Table 8 (PPO column): optimizer Adam (Kingma & Ba), with the
+ * usual bias correction:
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2
+ *   p -= lr * (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)            */
+void orc_adam(int64_t P, double *p, const double *g, double *m, double *v, int64_t step,
+              double lr, double beta1, double beta2, double eps)
+{
+    double bc1 = 1.0 - pow(beta1, (double)step);
+    double bc2 = 1.0 - pow(beta2, (double)step);
+    for (int64_t i = 0; i < P; ++i) {
+        m[i] = beta1 * m[i] + (1.0 - beta1) * g[i];
+        v[i] = beta2 * v[i] + (1.0 - beta2) * g[i] * g[i];
+        double mhat = m[i] / bc1;
+        double vhat = v[i] / bc2;
+        p[i] -= lr * mhat / (sqrt(vhat) + eps);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* "Teaching Mario to speedrun", sec. 6 "The whole algorithm": judge with GAE,
+ * then learn for a few epochs over shuffled minibatches, one backward pass
+ * and one optimizer step per minibatch.  The advantages are normalised with
+ * the statistics of the whole batch. */
+void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
+                int64_t epochs, int64_t minibatches,
+                const float *obs, const int32_t *act_disc, const float *act_cont,
+                const float *logp_old, const float *val, const float *rew,
+                const float *done, const float *boot,
+                double *params, double *m, double *v, int64_t *step,
+                double *stats, double *adv_out, double *ret_out)
+{
+    const int64_t B = T * N, mb = B / minibatches, P = orc_num_params(net);
+    double *adv = (double *)malloc(sizeof(double) * (size_t)B);
+    double *ret = (double *)malloc(sizeof(double) * (size_t)B);
+    int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * (size_t)B);
+    double *grad = (double *)malloc(sizeof(double) * (size_t)P);
+
+    orc_gae(T, N, rew, val, done, boot, hp->gamma, hp->lambda, adv, ret);
+    double mean, sd;
+    orc_moments(B, adv, &mean, &sd);
+
+    orc_loss_cfg lc = {hp->clip, hp->vf_coef, hp->ent_coef};
+    for (int64_t e = 0; e < epochs; ++e) {
+        orc_perm(hp->seed, e, B, perm);
+        for (int64_t k = 0; k < minibatches; ++k) {
+            double *st = stats ? stats + (e * minibatches + k) * 6 : NULL;
+            double tmp[6];
+            orc_loss_grad(net, &lc, params, mb, perm + k * mb, obs, act_disc, act_cont,
+                          logp_old, adv, ret, 1, mean, sd, grad, st ? st : tmp, NULL);
+            orc_clip_grad_norm(P, grad, hp->max_grad_norm);
+            *step += 1;
+            orc_adam(P, params, grad, m, v, *step, hp->lr, hp->beta1, hp->beta2, hp->adam_eps);
+        }
+    }
+    if (adv_out) memcpy(adv_out, adv, sizeof(double) * (size_t)B);
+    if (ret_out) memcpy(ret_out, ret, sizeof(double) * (size_t)B);
+    free(adv); free(ret); free(perm); free(grad);
+}

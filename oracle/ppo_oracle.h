@@ -1,0 +1,124 @@
+/*
+ * ppo_oracle.h -- plain CPU reference of the PPO learner step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the slow, obviously-correct restatement
+ * of what the learner step computes, written from the pages' text in fp64.
+ * It exists so that tests, the package smoke check and the bench's CPU
+ * baseline leg can compare against it.  The CUDA library never includes,
+ * links or calls anything here, and this code includes nothing of the CUDA
+ * library: the two share no code.
+ *
+ * Sources (page title, section):
+ *   "Teaching Mario to speedrun" (bigmah.com rl_blog) sec. 4  -- discounted return
+ *   same page, sec. 5  -- gradient of a log-softmax: (a == action) - probs[a]
+ *   same page, sec. 6 "Better advantages" -- delta_t and the GAE sum
+ *   same page, sec. 6 "Don't move too far at once" -- clipped ratio, value and
+ *                     entropy terms and their weights
+ *   same page, sec. 6 "The whole algorithm" -- epochs x shuffled minibatches,
+ *                     backward, optimizer step
+ *   same page, sec. 7 -- terminals are 1 where an episode just ended
+ *   "PlayTrain" (arXiv 2609.09059) Table 8 -- Adam, grad-norm clip 0.5, PPO
+ *                     hyper-parameters
+ *   "PlayTrain" Appendix F.2 listing "seeded RNG" -- mulberry32 definition
+ *   "boesch.dev DDNet RL" sec. "What the agent sees and does" -- hybrid
+ *                     discrete + continuous action space (diagonal Gaussian)
+ */
+#ifndef PPO_ORACLE_H
+#define PPO_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* One draw of mulberry32; *state is the generator's 32-bit counter. */
+uint32_t orc_mulberry32_next(uint32_t *state);
+
+/* GAE over a [T,N] rollout (time-major, env fastest).  done[t,n] != 0 means
+ * the episode ended during step t: rew[t,n] is its last reward, nothing is
+ * bootstrapped across it.  boot[n] is V(s_T).  Outputs adv, ret [T,N]. */
+void orc_gae(int64_t T, int64_t N, const float *rew, const float *val,
+             const float *done, const float *boot, double gamma, double lambda,
+             double *adv, double *ret);
+
+/* Mean and unbiased (n-1) standard deviation, two passes. */
+void orc_moments(int64_t n, const double *x, double *mean, double *std_unbiased);
+
+/* out[i] = (x[i] - mean) / (std + 1e-8) */
+void orc_normalize(int64_t n, const double *x, double mean, double std_, double *out);
+
+/* Minibatch permutation of epoch `epoch`: key i = mulberry32 draw number
+ * epoch*B + i of the stream seeded with `seed`; perm lists 0..B-1 sorted by
+ * (key, index). */
+void orc_perm(uint32_t seed, int64_t epoch, int64_t B, int32_t *perm);
+
+/* MLP actor-critic.  Output columns: head logits in head order, then the
+ * Gaussian means, then the value.  act: 0 = tanh, 1 = ReLU. */
+typedef struct {
+    int32_t obs_dim, h1, h2, act;
+    int32_t n_heads;
+    int32_t head_n[8];
+    int32_t n_gauss;
+} orc_net;
+
+/* Number of output columns C = sum(head_n) + n_gauss + 1. */
+int64_t orc_out_cols(const orc_net *net);
+/* Flat parameter count.  Layout: W1[h1][D], b1[h1], W2[h2][h1], b2[h2],
+ * W3[C][h2], b3[C], logstd[n_gauss]. */
+int64_t orc_num_params(const orc_net *net);
+
+/* Forward pass of one observation; z has C entries. */
+void orc_forward(const orc_net *net, const double *params, const float *x, double *z);
+
+typedef struct {
+    double clip, vf_coef, ent_coef;
+} orc_loss_cfg;
+
+/* Loss and gradient of one minibatch.
+ * rows idx[0..mb) select from the full-batch arrays obs [B][D],
+ * act_disc [B][n_heads], act_cont [B][n_gauss], logp_old [B], adv [B], ret [B].
+ * If normalize != 0 the advantage used is (adv - adv_mean)/(adv_std + 1e-8).
+ * grad (length num_params) is OVERWRITTEN with dL/dparams.
+ * stats6 = {loss, pg_loss, v_loss, entropy, clipfrac, approx_kl} (means).
+ * scale6 = mean |per-row term| of the same six quantities (may be NULL);
+ *          used by tests to form absolute tolerances for near-zero means.
+ * Returns the loss. */
+double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *params,
+                     int64_t mb, const int32_t *idx,
+                     const float *obs, const int32_t *act_disc, const float *act_cont,
+                     const float *logp_old, const double *adv, const double *ret,
+                     int normalize, double adv_mean, double adv_std,
+                     double *grad, double *stats6, double *scale6);
+
+/* L2 norm of g; if max_norm > 0, g *= min(1, max_norm/(norm + 1e-6)).
+ * Returns the norm before clipping. */
+double orc_clip_grad_norm(int64_t P, double *g, double max_norm);
+
+/* One Adam step (bias-corrected); `step` is the 1-based step number. */
+void orc_adam(int64_t P, double *p, const double *g, double *m, double *v, int64_t step,
+              double lr, double beta1, double beta2, double eps);
+
+typedef struct {
+    double gamma, lambda, clip, vf_coef, ent_coef;
+    double lr, beta1, beta2, adam_eps, max_grad_norm;
+    uint32_t seed;
+} orc_hyper;
+
+/* One whole PPO update: GAE, global advantage statistics, then for each epoch
+ * a fresh permutation and M minibatch steps (loss+grad, norm clip, Adam).
+ * params, m, v are updated in place; *step is incremented per minibatch.
+ * stats (E*M*6) receives the per-minibatch stats6.  adv_out/ret_out [T*N]
+ * may be NULL. */
+void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
+                int64_t epochs, int64_t minibatches,
+                const float *obs, const int32_t *act_disc, const float *act_cont,
+                const float *logp_old, const float *val, const float *rew,
+                const float *done, const float *boot,
+                double *params, double *m, double *v, int64_t *step,
+                double *stats, double *adv_out, double *ret_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
