@@ -1,0 +1,209 @@
+/*
+ * ppo.h -- C ABI of the GB300 (sm_103a) PPO learner step.
+ *
+ * The library computes, on one GPU, the learner half of PPO over a rollout
+ * buffer of T steps x N environments ("Teaching Mario to speedrun",
+ * sec. 6 "The whole algorithm", steps 2 "judge" and 3 "learn"):
+ *   GAE -> advantage normalisation -> for each epoch, a shuffled set of
+ *   minibatches -> MLP actor-critic forward, clipped surrogate + value +
+ *   entropy loss, backward -> gradient-norm clip -> Adam.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named d_* are DEVICE pointers on the current CUDA device;
+ *    pointers named h_* are HOST pointers.  The caller owns every buffer it
+ *    passes; the library never frees or retains a caller pointer beyond the
+ *    call, except that ppo_update may cache a CUDA graph that refers to the
+ *    pointers of its last call (re-captured whenever any argument changes).
+ *  - Rollout arrays are time-major: element (t, n) of a [T, N] array is at
+ *    t*N + n (environment index fastest).  Flat batch row b = t*N + n.
+ *  - Every device pointer must be 16-byte aligned (PPO_ERR_ALIGN otherwise).
+ *  - All work is enqueued asynchronously on `stream`; no call synchronises
+ *    the device except ppo_create, ppo_destroy, ppo_sync_status and
+ *    ppo_update_host.  Argument errors are detected on the host before any
+ *    launch and nothing is enqueued.  Errors found on the device (a bounded
+ *    wait that timed out) are latched in the context and returned by the next
+ *    ppo_sync_status.
+ *  - Results are deterministic: the same inputs give bit-identical outputs
+ *    (fixed-order reductions, no floating-point atomics).
+ *  - There is no CPU fallback: without a usable sm_103a device every call that
+ *    launches work returns PPO_ERR_CUDA or PPO_ERR_UNSUPPORTED.
+ */
+#ifndef PPO_H
+#define PPO_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PPO_OK = 0,
+    PPO_ERR_INVALID = 1,      /* bad size, null pointer, inconsistent shapes */
+    PPO_ERR_ALIGN = 2,        /* a device pointer is not 16-byte aligned      */
+    PPO_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed            */
+    PPO_ERR_UNSUPPORTED = 4,  /* shape outside what the kernels implement    */
+    PPO_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up           */
+    PPO_ERR_NOMEM = 6         /* device allocation failed                     */
+} ppo_status;
+
+#define PPO_MAX_HEADS 8
+
+/* Network and loss configuration (fixed for the life of a context).
+ * The MLP is h1 = act(W1 x + b1), h2 = act(W2 h1 + b2), z = W3 h2 + b3
+ * ("Teaching Mario to speedrun", sec. 6 "The policy and the value are one
+ * network").  The C = sum(head_n) + n_gauss + 1 output columns are, in order:
+ * the logits of each discrete head, the means of the diagonal-Gaussian
+ * dimensions ("boesch.dev DDNet RL", "What the agent sees and does"), the
+ * value.  Flat parameter layout (fp32):
+ *   W1[h1][obs_dim], b1[h1], W2[h2][h1], b2[h2], W3[C][h2], b3[C],
+ *   logstd[n_gauss]   (state-independent learned log-std per Gaussian dim). */
+typedef struct {
+    int32_t obs_dim;             /* D                                        */
+    int32_t h1, h2;              /* hidden widths                            */
+    int32_t act;                 /* 0 = tanh, 1 = ReLU                       */
+    int32_t n_heads;             /* discrete heads, 0..PPO_MAX_HEADS          */
+    int32_t head_n[PPO_MAX_HEADS];
+    int32_t n_gauss;             /* Gaussian action dims, 0..4               */
+    int32_t precision;           /* 0 = fp32 (CUDA-core FFMA GEMMs),
+                                    1 = bf16 tensor-core GEMMs (tcgen05), fp32
+                                        accumulate, fp32 master weights       */
+    float clip;                  /* epsilon of clip(ratio, 1-eps, 1+eps)     */
+    float vf_coef, ent_coef;     /* loss = pg + vf_coef*V - ent_coef*H       */
+    float beta1, beta2, adam_eps;
+    float max_grad_norm;         /* <= 0 disables the clip                   */
+    int64_t max_batch;           /* largest T*N given to ppo_update          */
+    int64_t max_minibatch;       /* largest minibatch row count              */
+    int32_t max_epochs;          /* largest epoch count given to ppo_update  */
+} ppo_config;
+
+typedef struct ppo_ctx ppo_ctx;
+
+/* Human-readable name of a status code (static string). */
+const char *ppo_status_string(ppo_status s);
+
+/* Creates a context on the current device: parameters (initialised from
+ * h_init_params, a HOST array of ppo_param_count() floats, or zero if NULL),
+ * gradient, Adam moments (zero), step counter (zero), the bf16 weight shadows
+ * and every workspace sized from max_batch / max_minibatch / max_epochs.
+ * Synchronous.  C <= 32; bf16 mode requires h1 and h2 to be multiples of 128
+ * and at most 512 (PPO_ERR_UNSUPPORTED otherwise); requires an sm_103 device. */
+ppo_status ppo_create(const ppo_config *cfg, const float *h_init_params, ppo_ctx **out);
+ppo_status ppo_destroy(ppo_ctx *ctx);
+
+/* Number of fp32 parameters for cfg (layout above).  No device needed. */
+ppo_status ppo_param_count(const ppo_config *cfg, int64_t *n);
+
+/* Device pointers owned by the context (valid until ppo_destroy): params,
+ * gradient (written by ppo_minibatch_loss_grad), Adam first and second
+ * moments.  Any may be NULL.  Writing d_params directly requires a following
+ * ppo_params_changed so that the bf16 shadows are refreshed. */
+ppo_status ppo_buffers(ppo_ctx *ctx, float **d_params, float **d_grad, float **d_adam_m,
+                       float **d_adam_v);
+ppo_status ppo_params_changed(ppo_ctx *ctx, cudaStream_t stream);
+/* Adam step counter (number of ppo_adam_step calls so far); synchronous. */
+ppo_status ppo_get_step(ppo_ctx *ctx, int64_t *step);
+
+/* ---- GAE ------------------------------------------------------------------
+ * "Teaching Mario to speedrun", sec. 6 "Better advantages":
+ *   delta_t = r_t + gamma V(s_{t+1}) - V(s_t),  A_t = sum_l (gamma lambda)^l delta_{t+l}
+ * computed per environment as a reverse-time scan.  d_done[t,n] != 0 means
+ * the episode ended during step t (sec. 7: terminals are 1 where an episode
+ * just ended): r[t,n] is its last reward and neither V(s_{t+1}) nor A_{t+1}
+ * crosses it.  d_boot[n] = V(s_T) bootstraps the last step.
+ * Inputs  d_rew, d_val, d_done: fp32 [T,N];  d_boot: fp32 [N].
+ * Outputs d_adv: fp32 [T,N] advantages; d_ret: fp32 [T,N] lambda-returns
+ *         A + V;  d_adv_norm (nullable): (A - mean)/(std + 1e-8);
+ *         d_stats (nullable): fp32 [2] = {mean, unbiased std} of A over all
+ *         T*N entries.
+ * d_work: device scratch of ppo_gae_workspace_bytes(T, N) bytes (may be NULL
+ * when both d_adv_norm and d_stats are NULL).  Outputs may not alias inputs.
+ * T, N >= 1; T*N < 2^31. */
+ppo_status ppo_gae_workspace_bytes(int64_t T, int64_t N, size_t *bytes);
+ppo_status ppo_gae(const float *d_rew, const float *d_val, const float *d_done,
+                   const float *d_boot, int64_t T, int64_t N, float gamma, float lambda,
+                   float *d_adv, float *d_ret, float *d_adv_norm, float *d_stats,
+                   void *d_work, size_t work_bytes, cudaStream_t stream);
+
+/* ---- Minibatch permutation -------------------------------------------------
+ * "Teaching Mario to speedrun", sec. 6: "for minibatch in shuffle(batch)".
+ * Key i = mulberry32 draw number epoch*B + i of the stream seeded with `seed`
+ * ("PlayTrain", Appendix F.2 "seeded RNG"); d_perm (int32 [B]) receives
+ * 0..B-1 sorted by (key, index).  Minibatch m of an epoch is
+ * d_perm[m*mb .. (m+1)*mb).  Bit-exact.  1 <= B < 2^31.
+ * d_work: ppo_perm_workspace_bytes(B) bytes of device scratch. */
+ppo_status ppo_perm_workspace_bytes(int64_t B, size_t *bytes);
+ppo_status ppo_minibatch_perm(uint32_t seed, int64_t epoch, int64_t B, int32_t *d_perm,
+                              void *d_work, size_t work_bytes, cudaStream_t stream);
+
+/* ---- Loss and gradient of one minibatch --------------------------------------
+ * "Teaching Mario to speedrun", sec. 6 "Don't move too far at once":
+ *   ratio = exp(logp - logp_old),  loss_pi = -min(ratio A, clip(ratio, 1-eps, 1+eps) A),
+ *   loss_V = (V - R)^2,  loss = mean(loss_pi) + vf_coef mean(loss_V) - ent_coef mean(H)
+ * with logp and H summed over the discrete heads (log-softmax) and the
+ * Gaussian dimensions.  Rows d_idx[0..mb) (int32, each in [0, B)) are
+ * gathered from the full-batch arrays
+ *   d_obs      fp32 [B][obs_dim]
+ *   d_act_disc int32 [B][n_heads]   (each in [0, head_n[h]))
+ *   d_act_cont fp32 [B][n_gauss]    (may be NULL if n_gauss == 0)
+ *   d_logp_old fp32 [B], d_adv fp32 [B], d_ret fp32 [B].
+ * If d_adv_stats (fp32 [2] = {mean, std}, device) is non-NULL the advantage
+ * used is (adv - mean)/(std + 1e-8).  The gradient dloss/dparams (fp32, flat
+ * layout) OVERWRITES the context's gradient buffer.  d_stats6 (nullable,
+ * fp32 [6]) receives the minibatch means {loss, pg_loss, v_loss, entropy,
+ * clipfrac, approx_kl}, with approx_kl = mean((r - 1) - log r).
+ * 1 <= mb <= max_minibatch.  An index outside [0, B) or an action outside
+ * [0, head_n) is clamped into range on the device (it never faults). */
+ppo_status ppo_minibatch_loss_grad(ppo_ctx *ctx, const float *d_obs, const int32_t *d_act_disc,
+                                   const float *d_act_cont, const float *d_logp_old,
+                                   const float *d_adv, const float *d_ret, const int32_t *d_idx,
+                                   int64_t B, int64_t mb, const float *d_adv_stats,
+                                   float *d_stats6, cudaStream_t stream);
+
+/* ---- Optimizer step ---------------------------------------------------------
+ * "PlayTrain", Table 8 (PPO column): Adam with gradient-norm clip.
+ * Scales the context gradient by min(1, max_grad_norm/(||g||_2 + 1e-6)) when
+ * max_grad_norm > 0, then one bias-corrected Adam step with learning rate
+ * lr; increments the step counter and refreshes the bf16 weight shadows.
+ * d_grad_norm (nullable, fp32 [1]) receives ||g||_2 before clipping. */
+ppo_status ppo_adam_step(ppo_ctx *ctx, float lr, float *d_grad_norm, cudaStream_t stream);
+
+/* ---- Whole update -------------------------------------------------------------
+ * "Teaching Mario to speedrun", sec. 6 "The whole algorithm", steps 2-3:
+ * GAE (gamma, lambda) over the [T,N] rollout, advantage statistics over all
+ * T*N entries, then for e in [0, epochs): permutation of epoch e (seed), and
+ * for m in [0, minibatches): loss+gradient of minibatch m, clip, Adam(lr).
+ * d_obs..d_boot as above (d_val, d_rew, d_done [T,N]; d_boot [N]).
+ * d_stats (nullable): fp32 [epochs*minibatches][6] minibatch stats.
+ * T*N must be divisible by minibatches; T*N <= max_batch; epochs <=
+ * max_epochs; T*N/minibatches <= max_minibatch.  Launched as one CUDA graph
+ * (captured on `stream` on the first call with a given argument set; the
+ * stream must not be the legacy default stream). */
+ppo_status ppo_update(ppo_ctx *ctx, const float *d_obs, const int32_t *d_act_disc,
+                      const float *d_act_cont, const float *d_logp_old, const float *d_val,
+                      const float *d_rew, const float *d_done, const float *d_boot,
+                      int64_t T, int64_t N, int32_t epochs, int32_t minibatches,
+                      float gamma, float lambda, float lr, uint32_t seed, float *d_stats,
+                      cudaStream_t stream);
+
+/* Same update, from HOST arrays (ideally pinned): copies the rollout into
+ * context-owned device buffers, runs ppo_update, copies the stats back into
+ * h_stats (nullable, fp32 [epochs*minibatches][6]) and synchronises
+ * `stream`.  h_act_cont may be NULL if n_gauss == 0. */
+ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_act_disc,
+                           const float *h_act_cont, const float *h_logp_old, const float *h_val,
+                           const float *h_rew, const float *h_done, const float *h_boot,
+                           int64_t T, int64_t N, int32_t epochs, int32_t minibatches,
+                           float gamma, float lambda, float lr, uint32_t seed, float *h_stats,
+                           cudaStream_t stream);
+
+/* Synchronises `stream` and returns any error latched on the device since
+ * the last call (PPO_ERR_TIMEOUT if a bounded wait gave up), clearing it. */
+ppo_status ppo_sync_status(ppo_ctx *ctx, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PPO_H */

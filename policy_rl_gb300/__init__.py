@@ -1,0 +1,221 @@
+"""GB300 (sm_103a) PPO learner step: Python binding of ``include/ppo.h``.
+
+The functions here carry the C ABI's names and only marshal arguments: torch
+tensors supply device memory (``data_ptr()``) and the current CUDA stream;
+every step of the computation runs in the library's CUDA kernels.  There is
+no CPU fallback -- without the built library (``policy_rl_gb300.build``) or
+an sm_103a device every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+from . import _abi
+from ._abi import PpoConfig, PpoError
+
+__all__ = [
+    "PpoConfig", "PpoError", "Context", "make_config", "ppo_param_count", "ppo_gae",
+    "ppo_gae_workspace_bytes", "ppo_minibatch_perm", "ppo_perm_workspace_bytes",
+    "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
+    "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
+    "ppo_sync_status", "library_path",
+]
+
+
+def library_path() -> str:
+    return _abi.LIB_PATH
+
+
+def _lib():
+    return _abi.load()
+
+
+def _ptr(t):
+    """Device (or host) address of a tensor / numpy array, None for None."""
+    if t is None:
+        return None
+    if hasattr(t, "data_ptr"):
+        if not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return ctypes.c_void_p(t.data_ptr())
+    if hasattr(t, "ctypes"):
+        return ctypes.c_void_p(t.ctypes.data)
+    return ctypes.c_void_p(int(t))
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_config(obs_dim, h1, h2, act=0, heads=(3, 2, 2), n_gauss=0, precision=1, clip=0.2,
+                vf_coef=0.5, ent_coef=0.01, beta1=0.9, beta2=0.999, adam_eps=1e-8,
+                max_grad_norm=0.5, max_batch=1, max_minibatch=1, max_epochs=1) -> PpoConfig:
+    hn = (ctypes.c_int32 * _abi.MAX_HEADS)(*(list(heads) + [0] * (_abi.MAX_HEADS - len(heads))))
+    return PpoConfig(obs_dim, h1, h2, act, len(heads), hn, n_gauss, precision, clip, vf_coef,
+                     ent_coef, beta1, beta2, adam_eps, max_grad_norm, max_batch, max_minibatch,
+                     max_epochs)
+
+
+def config_from_workload(w, max_batch=None, max_minibatch=None, max_epochs=None) -> PpoConfig:
+    B = w.T * w.N
+    return make_config(w.obs_dim, w.h1, w.h2, w.act, tuple(w.heads), w.n_gauss,
+                       1 if w.precision == "bf16" else 0, w.clip, w.vf_coef, w.ent_coef,
+                       max_grad_norm=w.max_grad_norm, max_batch=max_batch or B,
+                       max_minibatch=max_minibatch or B // w.minibatches,
+                       max_epochs=max_epochs or w.epochs)
+
+
+# ---- free functions -----------------------------------------------------------
+def ppo_param_count(cfg: PpoConfig) -> int:
+    n = ctypes.c_int64()
+    _abi.check(_lib().ppo_param_count(ctypes.byref(cfg), ctypes.byref(n)), "ppo_param_count")
+    return n.value
+
+
+def ppo_gae_workspace_bytes(T: int, N: int) -> int:
+    n = ctypes.c_size_t()
+    _abi.check(_lib().ppo_gae_workspace_bytes(T, N, ctypes.byref(n)), "ppo_gae_workspace_bytes")
+    return n.value
+
+
+def ppo_gae(rew, val, done, boot, gamma, lam, adv, ret, adv_norm=None, stats=None, work=None,
+            stream=None) -> None:
+    T, N = rew.shape
+    wb = work.numel() * work.element_size() if work is not None else 0
+    _abi.check(_lib().ppo_gae(_ptr(rew), _ptr(val), _ptr(done), _ptr(boot), T, N, gamma, lam,
+                              _ptr(adv), _ptr(ret), _ptr(adv_norm), _ptr(stats), _ptr(work), wb,
+                              _stream(stream)), "ppo_gae")
+
+
+def ppo_perm_workspace_bytes(B: int) -> int:
+    n = ctypes.c_size_t()
+    _abi.check(_lib().ppo_perm_workspace_bytes(B, ctypes.byref(n)), "ppo_perm_workspace_bytes")
+    return n.value
+
+
+def ppo_minibatch_perm(seed, epoch, B, perm, work, stream=None) -> None:
+    wb = work.numel() * work.element_size()
+    _abi.check(_lib().ppo_minibatch_perm(seed & 0xFFFFFFFF, epoch, B, _ptr(perm), _ptr(work), wb,
+                                         _stream(stream)), "ppo_minibatch_perm")
+
+
+# ---- context ------------------------------------------------------------------
+def ppo_create(cfg: PpoConfig, init_params=None):
+    h = ctypes.c_void_p()
+    if init_params is not None:
+        import numpy as np
+        init_params = np.ascontiguousarray(init_params, dtype=np.float32)
+    _abi.check(_lib().ppo_create(ctypes.byref(cfg), _ptr(init_params), ctypes.byref(h)),
+               "ppo_create")
+    return h
+
+
+def ppo_destroy(ctx) -> None:
+    _abi.check(_lib().ppo_destroy(ctx), "ppo_destroy")
+
+
+class _DevArray:
+    """Zero-copy view of library-owned device memory (CUDA array interface)."""
+
+    def __init__(self, ptr: int, n: int, typestr: str = "<f4"):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr,
+                                         "data": (ptr, False), "version": 3, "strides": None}
+
+
+def ppo_buffers(ctx, n_params: int):
+    """Torch views (params, grad, adam_m, adam_v) of the context's buffers."""
+    import torch
+    ps = [ctypes.c_void_p() for _ in range(4)]
+    _abi.check(_lib().ppo_buffers(ctx, *[ctypes.byref(p) for p in ps]), "ppo_buffers")
+    return tuple(torch.as_tensor(_DevArray(p.value, n_params), device="cuda") for p in ps)
+
+
+def ppo_params_changed(ctx, stream=None) -> None:
+    _abi.check(_lib().ppo_params_changed(ctx, _stream(stream)), "ppo_params_changed")
+
+
+def ppo_get_step(ctx) -> int:
+    n = ctypes.c_int64()
+    _abi.check(_lib().ppo_get_step(ctx, ctypes.byref(n)), "ppo_get_step")
+    return n.value
+
+
+def ppo_minibatch_loss_grad(ctx, obs, act_disc, act_cont, logp_old, adv, ret, idx,
+                            adv_stats=None, stats6=None, stream=None) -> None:
+    B = obs.shape[0]
+    _abi.check(_lib().ppo_minibatch_loss_grad(
+        ctx, _ptr(obs), _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(adv), _ptr(ret),
+        _ptr(idx), B, idx.numel(), _ptr(adv_stats), _ptr(stats6), _stream(stream)),
+        "ppo_minibatch_loss_grad")
+
+
+def ppo_adam_step(ctx, lr, grad_norm=None, stream=None) -> None:
+    _abi.check(_lib().ppo_adam_step(ctx, lr, _ptr(grad_norm), _stream(stream)), "ppo_adam_step")
+
+
+def ppo_update(ctx, obs, act_disc, act_cont, logp_old, val, rew, done, boot, epochs,
+               minibatches, gamma, lam, lr, seed, stats=None, stream=None) -> None:
+    T, N = val.shape
+    _abi.check(_lib().ppo_update(
+        ctx, _ptr(obs), _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(val), _ptr(rew),
+        _ptr(done), _ptr(boot), T, N, epochs, minibatches, gamma, lam, lr, seed & 0xFFFFFFFF,
+        _ptr(stats), _stream(stream)), "ppo_update")
+
+
+def ppo_update_host(ctx, obs, act_disc, act_cont, logp_old, val, rew, done, boot, epochs,
+                    minibatches, gamma, lam, lr, seed, stats=None, stream=None) -> None:
+    T, N = val.shape
+    _abi.check(_lib().ppo_update_host(
+        ctx, _ptr(obs), _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(val), _ptr(rew),
+        _ptr(done), _ptr(boot), T, N, epochs, minibatches, gamma, lam, lr, seed & 0xFFFFFFFF,
+        _ptr(stats), _stream(stream)), "ppo_update_host")
+
+
+def ppo_sync_status(ctx, stream=None) -> None:
+    _abi.check(_lib().ppo_sync_status(ctx, _stream(stream)), "ppo_sync_status")
+
+
+class Context:
+    """Owns one ppo_ctx (parameters, gradient, Adam state, workspaces)."""
+
+    def __init__(self, cfg: PpoConfig, init_params=None):
+        self.cfg = cfg
+        self.n_params = ppo_param_count(cfg)
+        self.handle = ppo_create(cfg, init_params)
+        self.params, self.grad, self.adam_m, self.adam_v = ppo_buffers(self.handle, self.n_params)
+
+    def close(self):
+        if self.handle is not None:
+            ppo_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def minibatch_loss_grad(self, *a, **k):
+        return ppo_minibatch_loss_grad(self.handle, *a, **k)
+
+    def adam_step(self, *a, **k):
+        return ppo_adam_step(self.handle, *a, **k)
+
+    def update(self, *a, **k):
+        return ppo_update(self.handle, *a, **k)
+
+    def update_host(self, *a, **k):
+        return ppo_update_host(self.handle, *a, **k)
+
+    def sync_status(self, stream=None):
+        return ppo_sync_status(self.handle, stream)
+
+    def params_changed(self, stream=None):
+        return ppo_params_changed(self.handle, stream)
+
+    def step(self) -> int:
+        return ppo_get_step(self.handle)

@@ -1,0 +1,152 @@
+// gemm.h -- internal interface of the MLP GEMM kernels (tensor-core bf16 and
+// CUDA-core fp32) used by the learner-step orchestration in api.cu.
+#pragma once
+
+#include "common.cuh"
+
+namespace ppo {
+
+// ---- bf16 tensor-core path --------------------------------------------------
+// D[M][N] = A[M][K] * B[N][K]^T; A and B row-major bf16 with row pitches
+// lda/ldb (elements, multiples of 8); N a multiple of 64 (or 16/32 for the
+// loss head); K <= lda, K <= ldb, columns of A/B between K and the next
+// multiple of 64 must be zero or lie beyond lda/ldb.
+struct GemmOperands {
+  const __nv_bfloat16* A;
+  int lda;
+  const __nv_bfloat16* B;
+  int ldb;
+  int M, N, K;
+};
+
+struct TcParams {
+  int M, N, K;
+  int tiles_m, tiles_n, k_tiles, last_k_steps;
+  int epi_n;
+  const float* bias;
+  __nv_bfloat16* out;
+  int ldo;
+  const __nv_bfloat16* aux;
+  int ldaux;
+  int act;
+  float* colsum_part;
+  NetShape shape;
+  LossCoef lc;
+  LossRows rows;
+  float inv_mb;
+  const float* logstd;
+  float* loss_part;
+  __nv_bfloat16* dz;
+  int lddz;
+  int* err;
+  uint64_t timeout_ns;
+};
+
+struct WRegion {
+  int M, N, bn, tiles_m, tiles_n, splits, kt_per_split, k_tiles, unit_begin;
+  float* part;  // [splits][M][N]
+};
+
+struct WParams {
+  WRegion r[3];
+  int nreg, total_units;
+  uint32_t mn_lbo, mn_sbo;
+  int* err;
+  uint64_t timeout_ns;
+};
+
+// One weight-gradient product P[M][N] = sum_r U[r][0..M) (x) V[r][0..N),
+// U, V bf16 row-major [rows][ldu/ldv]; M a multiple of 128, N of 64.
+struct WGradRegion {
+  const __nv_bfloat16* U;
+  int ldu, M;
+  const __nv_bfloat16* V;
+  int ldv, N;
+  int kt_per_split;   // 64-row k-tiles per split
+  float* part;        // [splits][M][N] fp32
+};
+
+cudaError_t tc_prepare();
+int tc_pick_bn(int N);
+int tc_wgrad_splits(int rows, int kt_per_split);
+
+cudaError_t tc_gemm_bias_act(const GemmOperands& g, const float* bias, int act,
+                             __nv_bfloat16* out, int ldo, int* err, uint64_t timeout_ns,
+                             int num_sms, cudaStream_t st);
+cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ldaux, int act,
+                         __nv_bfloat16* out, int ldo, float* colsum_part, int* err,
+                         uint64_t timeout_ns, int num_sms, cudaStream_t st, int* grid_out);
+cudaError_t tc_gemm_loss(const GemmOperands& g, const NetShape& s, LossCoef lc, LossRows rows,
+                         float inv_mb, const float* b3, const float* logstd, __nv_bfloat16* dz,
+                         int lddz, float* colsum_part, float* loss_part, int* err,
+                         uint64_t timeout_ns, int num_sms, cudaStream_t st, int* grid_out);
+cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lbo,
+                     uint32_t mn_sbo, int* err, uint64_t timeout_ns, int num_sms,
+                     cudaStream_t st);
+
+// ---- fp32 CUDA-core path ----------------------------------------------------
+// Generic-stride GEMM: C(m,n) = sum_k A(m,k) B(n,k) with
+// A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk].
+struct SimtOperands {
+  const float* A;
+  int64_t sam, sak;
+  const float* B;
+  int64_t sbn, sbk;
+  int M, N, K;
+};
+int simt_tiles_m(int M);
+cudaError_t simt_bias_act(const SimtOperands& g, const float* bias, int act, float* out, int ldo,
+                          cudaStream_t st);
+cudaError_t simt_dact(const SimtOperands& g, const float* aux, int ldaux, int act, float* out,
+                      int ldo, float* colsum_part, cudaStream_t st);
+// split-K partial products: part[split][M][N], split covers k_per_split rows
+cudaError_t simt_wgrad(const SimtOperands& g, int k_per_split, float* part, cudaStream_t st);
+// head + loss: z = H2 W3^T + b3 per row, per-row loss, dz (fp32 [mb][CP]),
+// per-block column sums of dz and loss partials; returns the block count.
+cudaError_t simt_head_loss(const NetShape& s, LossCoef lc, LossRows rows, float inv_mb,
+                           const float* H2, const float* W3, const float* b3,
+                           const float* logstd, int mb, float* dz, float* colsum_part,
+                           float* loss_part, cudaStream_t st, int* blocks_out);
+int simt_head_blocks(int mb);
+
+// ---- reduction and optimizer --------------------------------------------------
+struct ReduceArgs {
+  NetShape s;
+  const float* pW1; int s1; int ld1;    // [s1][H1][ld1]
+  const float* pW2; int s2;             // [s2][H2][H1]
+  const float* pW3t; int s3; int ld3;   // [s3][H2][ld3]  (dW3 transposed)
+  const float* pb1; int nb1;            // [nb1][H1]
+  const float* pb2; int nb2;            // [nb2][H2]
+  const float* pb3; int nb3; int ldb3;  // [nb3][ldb3]
+  const float* ploss; int nl;           // [nl][kLossPartials]
+  float inv_mb;
+  float* grad;                          // [P]
+  double* sq_part;                      // [reduce_blocks]
+  float* stats6;                        // nullable
+};
+int reduce_blocks(int64_t P);
+cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st);
+
+struct Shadows {
+  __nv_bfloat16 *W1s, *W2s, *W2Ts, *W3s, *W3Ts;  // nullptr in fp32 mode
+  int ld3t;                                       // row pitch of W3Ts
+};
+struct AdamArgs {
+  float* p;
+  const float* g;
+  float* m;
+  float* v;
+  int64_t P;
+  const double* sq_part;
+  int nsq;
+  float max_norm, lr, b1, b2, eps;
+  int64_t* step;
+  unsigned* done_ctr;
+  float* grad_norm_out;
+  NetShape s;
+  Shadows sh;
+};
+cudaError_t launch_adam(const AdamArgs& a, cudaStream_t st);
+cudaError_t launch_shadows(const float* p, const NetShape& s, const Shadows& sh, cudaStream_t st);
+
+}  // namespace ppo

@@ -1,0 +1,727 @@
+// gemm_tc.cu -- tcgen05 / TMA tensor-core GEMMs of the MLP actor-critic.
+//
+// The only dense contraction on the learner path is the MLP ("Teaching Mario
+// to speedrun", sec. 6 "The policy and the value are one network"; its
+// backward is sec. 6's loss.backward()).  Two persistent, warp-specialised
+// kernels cover all of it:
+//
+//  * tc_gemm_kernel<BN, EPI>:  D[M,N] = A[M,K] * B[N,K]^T with both operands
+//    K-major in global memory (activations [rows][features], weights
+//    [out][in]).  Warp 0 issues TMA loads (128B swizzle) into an S-stage
+//    shared-memory ring, warp 1 issues tcgen05.mma (128 x BN x 16 per
+//    instruction) into a double-buffered TMEM accumulator, warps 2-5 drain
+//    TMEM with tcgen05.ld and run the fused epilogue while the next tile's
+//    MMAs proceed:
+//      EPI_BIAS_ACT  h = act(acc + b)                      (forward layers)
+//      EPI_DACT      dpre = acc * act'(h), column sums     (backward data)
+//      EPI_LOSS      z = acc + b3 -> per-row PPO loss, dz  (head + loss)
+//  * tc_wgrad_kernel: weight gradients dW = dPre^T X with K = minibatch rows.
+//    Both operands are read MN-major straight from the row-major activation
+//    buffers; K is split across CTAs and every split writes its own fp32
+//    partial tile, reduced later in a fixed order (deterministic, no atomics).
+//
+// Every wait on an mbarrier is bounded (globaltimer); on expiry the kernel
+// latches kDevTimeout, stops issuing work, drains what it has in flight and
+// releases its TMEM before returning.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "tc_ptx.cuh"
+
+namespace ppo {
+
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle atom row
+constexpr int kThreads = 192;
+constexpr int kColsumCap = 512;
+
+enum Epi { EPI_BIAS_ACT = 0, EPI_DACT = 1, EPI_LOSS = 2 };
+
+template <int BN>
+struct Cfg {
+  static constexpr int S = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+  static constexpr int CTRL = 512;
+  static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + CTRL + 4 * kColsumCap * 4 +
+                                 4 * kLossPartials * 4;
+};
+
+struct Guard {
+  volatile int* abort;
+  int* err;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Guard& g) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*g.abort) return false;
+    if (globaltimer() - t0 > g.limit_ns) {
+      *g.abort = 1;
+      atomicOr(g.err, kDevTimeout);
+      return false;
+    }
+  }
+}
+
+// wait used while draining after an abort: never sets the abort flag again
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > limit_ns) return;
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&y)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_bf16x2(y[8 * i + 0], y[8 * i + 1]);
+    u.y = pack_bf16x2(y[8 * i + 2], y[8 * i + 3]);
+    u.z = pack_bf16x2(y[8 * i + 4], y[8 * i + 5]);
+    u.w = pack_bf16x2(y[8 * i + 6], y[8 * i + 7]);
+    d[i] = u;
+  }
+}
+
+struct Ctrl {
+  uint64_t* bars;
+  int S;
+  __device__ uint32_t full(int s) const { return smem_u32(&bars[s]); }
+  __device__ uint32_t empty(int s) const { return smem_u32(&bars[S + s]); }
+  __device__ uint32_t tfull(int a) const { return smem_u32(&bars[2 * S + a]); }
+  __device__ uint32_t tempty(int a) const { return smem_u32(&bars[2 * S + 2 + a]); }
+  __device__ uint32_t drain() const { return smem_u32(&bars[2 * S + 4]); }
+};
+
+// ---------------------------------------------------------------------------
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const TcParams p) {
+  using C = Cfg<BN>;
+  constexpr int S = C::S;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  uint8_t* ctrl = gbase + (size_t)S * C::STAGE;
+  Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), S};
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * S + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);  // issued, consumed
+  float* cs = reinterpret_cast<float*>(ctrl + C::CTRL);                      // [4][kColsumCap]
+  float* lp = cs + 4 * kColsumCap;                                           // [4][kLossPartials]
+
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  auto sA = [&](int s) { return base + (uint32_t)(s * C::STAGE); };
+  auto sB = [&](int s) { return base + (uint32_t)(s * C::STAGE + C::A_BYTES); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(cb.full(s), 1);
+      mbar_init(cb.empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(cb.tfull(a), 1);
+      mbar_init(cb.tempty(a), 128);
+    }
+    mbar_init(cb.drain(), 1);
+    *abort_flag = 0;
+    cnt[0] = 0;
+    cnt[1] = 0;
+    fence_mbar_init();
+  }
+  if (EPI != EPI_BIAS_ACT)
+    for (int i = threadIdx.x; i < 4 * kColsumCap + 4 * kLossPartials; i += kThreads) cs[i] = 0.f;
+  if (warp == 1) tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const Guard g{abort_flag, p.err, p.timeout_ns};
+  const int total = p.tiles_m * p.tiles_n;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          const int s = it % S;
+          const uint32_t r = it / S;
+          if (!wait_bar(cb.empty(s), (r & 1) ^ 1, g)) { ok = false; break; }
+          mbar_arrive_expect_tx(cb.full(s), C::STAGE);
+          tma_load_2d(sA(s), &tmA, kt * BK, tm * BM, cb.full(s));
+          tma_load_2d(sB(s), &tmB, kt * BK, tn * BN, cb.full(s));
+          ++it;
+          cnt[0] = it;
+        }
+      }
+      // tail: wait until the MMA warp has released every stage, so that no
+      // tcgen05.commit arrival is still pending when the CTA exits
+      if (ok)
+        for (int j = 0; j < S; ++j, ++it) {
+          const int s = it % S;
+          const uint32_t r = it / S;
+          if (!wait_bar(cb.empty(s), (r & 1) ^ 1, g)) break;
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int acc = tc & 1;
+        const uint32_t use = tc >> 1;
+        if (!wait_bar(cb.tempty(acc), (use & 1) ^ 1, g)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * BN);
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          const int s = it % S;
+          const uint32_t r = it / S;
+          if (!wait_bar(cb.full(s), r & 1, g)) { ok = false; break; }
+          tc_fence_after();
+          const int nk = (kt == p.k_tiles - 1) ? p.last_k_steps : BK / 16;
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint64_t da = sdesc_sw128(sA(s) + kk * 32, 16, 1024);
+            const uint64_t db = sdesc_sw128(sB(s) + kk * 32, 16, 1024);
+            tc_mma_bf16(d, da, db, idesc, (kt | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(cb.empty(s));
+          ++it;
+          cnt[1] = it;
+        }
+        if (!ok) break;
+        tc_commit(cb.tfull(acc));
+        ++tc;
+      }
+    }
+  } else {
+    // epilogue warps 2..5: TMEM lane quarter q = warp % 4
+    const int q = warp & 3;
+    const int et = (warp - 2) * kWarp + lane;  // 0..127
+    (void)et;
+    uint32_t tc = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const int acc = tc & 1;
+      const uint32_t use = tc >> 1;
+      if (!wait_bar(cb.tfull(acc), use & 1, g)) break;
+      tc_fence_after();
+      const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
+      const int row = tm * BM + q * 32 + lane;
+      const bool rok = row < p.M;
+      const uint32_t taddr = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      if constexpr (EPI == EPI_LOSS) {
+        float v[32];
+        if constexpr (BN == 16) tmem_ld16(taddr, v);
+        else tmem_ld32(taddr, v);
+        float z[32], dz[32], t6[6], dls[4];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          z[j] = (j < p.shape.C) ? v[j] + p.bias[j] : 0.f;
+          dz[j] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 6; ++k) t6[k] = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dls[k] = 0.f;
+        if (rok)
+          row_loss(p.shape, p.lc, p.inv_mb, z, p.rows.act + (int64_t)row * p.shape.NH,
+                   p.rows.actc + (int64_t)row * p.shape.G, p.logstd, p.rows.logp_old[row],
+                   p.rows.adv[row], p.rows.ret[row], dz, t6, dls);
+        if (rok) {
+          uint4* d = reinterpret_cast<uint4*>(p.dz + (int64_t)row * p.lddz);
+#pragma unroll
+          for (int i = 0; i < BN / 8; ++i) {
+            uint4 u;
+            u.x = pack_bf16x2(dz[8 * i + 0], dz[8 * i + 1]);
+            u.y = pack_bf16x2(dz[8 * i + 2], dz[8 * i + 3]);
+            u.z = pack_bf16x2(dz[8 * i + 4], dz[8 * i + 5]);
+            u.w = pack_bf16x2(dz[8 * i + 6], dz[8 * i + 7]);
+            d[i] = u;
+          }
+        }
+        const float colsum = warp_reduce_scatter32(dz);
+        cs[q * kColsumCap + lane] += colsum;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+          const float s6 = warp_sum(t6[k]);
+          if (lane == 0) lp[q * kLossPartials + k] += s6;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float s4 = warp_sum(dls[k]);
+          if (lane == 0) lp[q * kLossPartials + 6 + k] += s4;
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tmem_ld32(taddr + (uint32_t)c0, v);
+          const int col0 = tn * BN + c0;
+          if constexpr (EPI == EPI_BIAS_ACT) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float x = v[j] + __ldg(p.bias + col0 + j);
+              v[j] = p.act == 0 ? tanh_fast(x) : fmaxf(x, 0.f);
+            }
+            if (rok) store_bf16x32(p.out + (int64_t)row * p.ldo + col0, v);
+          } else {  // EPI_DACT
+            uint4 au[4] = {};
+            if (rok) {
+              const uint4* ap = reinterpret_cast<const uint4*>(p.aux + (int64_t)row * p.ldaux + col0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) au[i] = __ldg(ap + i);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t w4[4] = {au[i].x, au[i].y, au[i].z, au[i].w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float2 hv = unpack_bf16x2(w4[h]);
+                const int j = 8 * i + 2 * h;
+                const float d0 = p.act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
+                const float d1 = p.act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
+                v[j] = rok ? v[j] * d0 : 0.f;
+                v[j + 1] = rok ? v[j + 1] * d1 : 0.f;
+              }
+            }
+            if (rok) store_bf16x32(p.out + (int64_t)row * p.ldo + col0, v);
+            const float colsum = warp_reduce_scatter32(v);
+            cs[q * kColsumCap + col0 + lane] += colsum;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(cb.tempty(acc));
+      ++tc;
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // drain: TMA loads issued but never consumed, and outstanding MMAs
+    if (threadIdx.x == 0) {
+      const uint32_t issued = cnt[0], consumed = cnt[1];
+      for (uint32_t it = consumed; it < issued; ++it)
+        drain_wait(cb.full(it % S), (it / S) & 1, p.timeout_ns);
+    }
+    if (warp == 1 && lane == 0) {
+      tc_commit(cb.drain());
+      drain_wait(cb.drain(), 0, p.timeout_ns);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if constexpr (EPI != EPI_BIAS_ACT) {
+    if (warp >= 2) {
+      const int et = threadIdx.x - 2 * kWarp;
+      for (int c = et; c < p.epi_n; c += 128)
+        p.colsum_part[(int64_t)blockIdx.x * p.epi_n + c] =
+            ((cs[c] + cs[kColsumCap + c]) + cs[2 * kColsumCap + c]) + cs[3 * kColsumCap + c];
+      if constexpr (EPI == EPI_LOSS) {
+        if (et < kLossPartials)
+          p.loss_part[(int64_t)blockIdx.x * kLossPartials + et] =
+              ((lp[et] + lp[kLossPartials + et]) + lp[2 * kLossPartials + et]) +
+              lp[3 * kLossPartials + et];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Weight-gradient kernel: P[M][N] = sum_rows U[row][m] * V[row][n] over a
+// K-split of the minibatch rows; both operands MN-major in shared memory.
+constexpr int WBN = 128;
+constexpr int WS = 6;
+constexpr int W_A_BYTES = BM * BK * 2;   // 2 boxes of 64 features x 64 rows
+constexpr int W_B_BYTES = WBN * BK * 2;  // up to 2 boxes
+constexpr int W_STAGE = W_A_BYTES + W_B_BYTES;
+constexpr size_t W_SMEM = 1024 + (size_t)WS * W_STAGE + 512;
+constexpr int W_TMEM_COLS = 256;
+
+__device__ __forceinline__ void decode_unit(const WParams& p, int u, int& reg, int& tm, int& tn,
+                                            int& kt0, int& kt1, int& split) {
+  reg = 0;
+  while (reg + 1 < p.nreg && u >= p.r[reg + 1].unit_begin) ++reg;
+  const WRegion& R = p.r[reg];
+  const int local = u - R.unit_begin;
+  const int per = R.tiles_m * R.tiles_n;
+  split = local / per;
+  const int rem = local % per;
+  tm = rem / R.tiles_n;
+  tn = rem % R.tiles_n;
+  kt0 = split * R.kt_per_split;
+  kt1 = min(R.k_tiles, kt0 + R.kt_per_split);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant__ CUtensorMap tmV0,
+                const __grid_constant__ CUtensorMap tmU1, const __grid_constant__ CUtensorMap tmV1,
+                const __grid_constant__ CUtensorMap tmU2, const __grid_constant__ CUtensorMap tmV2,
+                const WParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  uint8_t* ctrl = gbase + (size_t)WS * W_STAGE;
+  Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), WS};
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * WS + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  auto sA = [&](int s) { return base + (uint32_t)(s * W_STAGE); };
+  auto sB = [&](int s) { return base + (uint32_t)(s * W_STAGE + W_A_BYTES); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WS; ++s) {
+      mbar_init(cb.full(s), 1);
+      mbar_init(cb.empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(cb.tfull(a), 1);
+      mbar_init(cb.tempty(a), 128);
+    }
+    mbar_init(cb.drain(), 1);
+    *abort_flag = 0;
+    cnt[0] = 0;
+    cnt[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tslot), W_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const Guard g{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+        int reg, tm, tn, kt0, kt1, split;
+        decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
+        const int bn = p.r[reg].bn;
+        const CUtensorMap* tu = reg == 0 ? &tmU0 : (reg == 1 ? &tmU1 : &tmU2);
+        const CUtensorMap* tv = reg == 0 ? &tmV0 : (reg == 1 ? &tmV1 : &tmV2);
+        const uint32_t bytes = (uint32_t)(BM + bn) * BK * 2;
+        for (int kt = kt0; kt < kt1; ++kt) {
+          const int s = it % WS;
+          const uint32_t r = it / WS;
+          if (!wait_bar(cb.empty(s), (r & 1) ^ 1, g)) { ok = false; break; }
+          mbar_arrive_expect_tx(cb.full(s), bytes);
+          tma_load_2d(sA(s), tu, tm * BM, kt * BK, cb.full(s));
+          tma_load_2d(sA(s) + 8192, tu, tm * BM + 64, kt * BK, cb.full(s));
+          for (int j = 0; j < bn / 64; ++j)
+            tma_load_2d(sB(s) + 8192 * j, tv, tn * bn + 64 * j, kt * BK, cb.full(s));
+          ++it;
+          cnt[0] = it;
+        }
+      }
+      if (ok)
+        for (int j = 0; j < WS; ++j, ++it) {
+          const int s = it % WS;
+          const uint32_t r = it / WS;
+          if (!wait_bar(cb.empty(s), (r & 1) ^ 1, g)) break;
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+        int reg, tm, tn, kt0, kt1, split;
+        decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
+        const uint32_t idesc = idesc_bf16(BM, p.r[reg].bn, true, true);
+        const int acc = tc & 1;
+        const uint32_t use = tc >> 1;
+        if (!wait_bar(cb.tempty(acc), (use & 1) ^ 1, g)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * WBN);
+        for (int kt = kt0; kt < kt1; ++kt) {
+          const int s = it % WS;
+          const uint32_t r = it / WS;
+          if (!wait_bar(cb.full(s), r & 1, g)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t da = sdesc_sw128(sA(s) + kk * 2048, p.mn_lbo, p.mn_sbo);
+            const uint64_t db = sdesc_sw128(sB(s) + kk * 2048, p.mn_lbo, p.mn_sbo);
+            tc_mma_bf16(d, da, db, idesc, (kt != kt0 || kk != 0) ? 1u : 0u);
+          }
+          tc_commit(cb.empty(s));
+          ++it;
+          cnt[1] = it;
+        }
+        if (!ok) break;
+        tc_commit(cb.tfull(acc));
+        ++tc;
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    uint32_t tc = 0;
+    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+      int reg, tm, tn, kt0, kt1, split;
+      decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
+      const WRegion& R = p.r[reg];
+      const int acc = tc & 1;
+      const uint32_t use = tc >> 1;
+      if (!wait_bar(cb.tfull(acc), use & 1, g)) break;
+      tc_fence_after();
+      const int row = tm * BM + q * 32 + lane;
+      const uint32_t taddr = tmem + (uint32_t)(acc * WBN) + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < R.bn; c0 += 32) {
+        float v[32];
+        tmem_ld32(taddr + (uint32_t)c0, v);
+        const int col0 = tn * R.bn + c0;
+        if (row < R.M && col0 < R.N) {
+          float4* dst = reinterpret_cast<float4*>(R.part + ((int64_t)split * R.M + row) * R.N + col0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(cb.tempty(acc));
+      ++tc;
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      const uint32_t issued = cnt[0], consumed = cnt[1];
+      for (uint32_t it = consumed; it < issued; ++it)
+        drain_wait(cb.full(it % WS), (it / WS) & 1, p.timeout_ns);
+    }
+    if (warp == 1 && lane == 0) {
+      tc_commit(cb.drain());
+      drain_wait(cb.drain(), 0, p.timeout_ns);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, W_TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encode() {
+  if (g_encode) return cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess) return e;
+  if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return cudaSuccess;
+}
+
+// bf16 row-major [rows][cols] (row pitch ld elements), box = box_cols x box_rows
+cudaError_t make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
+                      int box_cols, int box_rows) {
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream_t st,
+                      int* grid_out) {
+  CUtensorMap ta, tb;
+  cudaError_t e = make_tmap(&ta, g.A, g.lda, g.M, g.lda, BK, BM);
+  if (e != cudaSuccess) return e;
+  e = make_tmap(&tb, g.B, g.ldb, g.N, g.ldb, BK, BN);
+  if (e != cudaSuccess) return e;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.tiles_m = (g.M + BM - 1) / BM;
+  p.tiles_n = g.N / BN;
+  p.k_tiles = (g.K + BK - 1) / BK;
+  const int rem = g.K - (p.k_tiles - 1) * BK;
+  p.last_k_steps = (rem + 15) / 16;
+  const int total = p.tiles_m * p.tiles_n;
+  const int grid = total < num_sms ? total : num_sms;
+  tc_gemm_kernel<BN, EPI><<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, p);
+  if (grid_out) *grid_out = grid;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+template <int BN, int EPI>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Cfg<BN>::SMEM);
+}
+
+// Driver entry point and the shared-memory opt-in of every kernel instance;
+// called once per context, outside any stream capture.
+cudaError_t tc_prepare() {
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  const cudaError_t errs[] = {
+      set_smem_attr<256, EPI_BIAS_ACT>(), set_smem_attr<128, EPI_BIAS_ACT>(),
+      set_smem_attr<64, EPI_BIAS_ACT>(),  set_smem_attr<256, EPI_DACT>(),
+      set_smem_attr<128, EPI_DACT>(),     set_smem_attr<64, EPI_DACT>(),
+      set_smem_attr<16, EPI_LOSS>(),      set_smem_attr<32, EPI_LOSS>(),
+      cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)W_SMEM)};
+  for (cudaError_t x : errs)
+    if (x != cudaSuccess) return x;
+  return cudaSuccess;
+}
+
+int tc_pick_bn(int N) {
+  if (N % 256 == 0) return 256;
+  if (N % 128 == 0) return 128;
+  if (N % 64 == 0) return 64;
+  return 0;
+}
+
+cudaError_t tc_gemm_bias_act(const GemmOperands& g, const float* bias, int act,
+                             __nv_bfloat16* out, int ldo, int* err, uint64_t timeout_ns,
+                             int num_sms, cudaStream_t st) {
+  TcParams p{};
+  p.bias = bias;
+  p.act = act;
+  p.out = out;
+  p.ldo = ldo;
+  p.err = err;
+  p.timeout_ns = timeout_ns;
+  switch (tc_pick_bn(g.N)) {
+    case 256: return launch_tc<256, EPI_BIAS_ACT>(g, p, num_sms, st, nullptr);
+    case 128: return launch_tc<128, EPI_BIAS_ACT>(g, p, num_sms, st, nullptr);
+    case 64: return launch_tc<64, EPI_BIAS_ACT>(g, p, num_sms, st, nullptr);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ldaux, int act,
+                         __nv_bfloat16* out, int ldo, float* colsum_part, int* err,
+                         uint64_t timeout_ns, int num_sms, cudaStream_t st, int* grid_out) {
+  if (g.N > kColsumCap) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.aux = aux;
+  p.ldaux = ldaux;
+  p.act = act;
+  p.out = out;
+  p.ldo = ldo;
+  p.colsum_part = colsum_part;
+  p.epi_n = g.N;
+  p.err = err;
+  p.timeout_ns = timeout_ns;
+  switch (tc_pick_bn(g.N)) {
+    case 256: return launch_tc<256, EPI_DACT>(g, p, num_sms, st, grid_out);
+    case 128: return launch_tc<128, EPI_DACT>(g, p, num_sms, st, grid_out);
+    case 64: return launch_tc<64, EPI_DACT>(g, p, num_sms, st, grid_out);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_gemm_loss(const GemmOperands& g, const NetShape& s, LossCoef lc, LossRows rows,
+                         float inv_mb, const float* b3, const float* logstd, __nv_bfloat16* dz,
+                         int lddz, float* colsum_part, float* loss_part, int* err,
+                         uint64_t timeout_ns, int num_sms, cudaStream_t st, int* grid_out) {
+  TcParams p{};
+  p.bias = b3;
+  p.shape = s;
+  p.lc = lc;
+  p.rows = rows;
+  p.inv_mb = inv_mb;
+  p.logstd = logstd;
+  p.dz = dz;
+  p.lddz = lddz;
+  p.colsum_part = colsum_part;
+  p.loss_part = loss_part;
+  p.epi_n = g.N;
+  p.err = err;
+  p.timeout_ns = timeout_ns;
+  if (g.N == 16) return launch_tc<16, EPI_LOSS>(g, p, num_sms, st, grid_out);
+  if (g.N == 32) return launch_tc<32, EPI_LOSS>(g, p, num_sms, st, grid_out);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lbo,
+                     uint32_t mn_sbo, int* err, uint64_t timeout_ns, int num_sms,
+                     cudaStream_t st) {
+  if (nreg < 1 || nreg > 3) return cudaErrorInvalidValue;
+  CUtensorMap tu[3], tv[3];
+  WParams p{};
+  p.nreg = nreg;
+  p.err = err;
+  p.timeout_ns = timeout_ns;
+  p.mn_lbo = mn_lbo;
+  p.mn_sbo = mn_sbo;
+  int unit = 0;
+  for (int r = 0; r < nreg; ++r) {
+    const WGradRegion& G = regs[r];
+    cudaError_t e = make_tmap(&tu[r], G.U, G.M, rows, G.ldu, 64, BK);
+    if (e != cudaSuccess) return e;
+    e = make_tmap(&tv[r], G.V, G.N, rows, G.ldv, 64, BK);
+    if (e != cudaSuccess) return e;
+    WRegion& R = p.r[r];
+    R.M = G.M;
+    R.N = G.N;
+    R.bn = G.N % 128 == 0 ? 128 : 64;
+    R.tiles_m = G.M / BM;
+    R.tiles_n = G.N / R.bn;
+    R.k_tiles = (rows + BK - 1) / BK;
+    R.kt_per_split = G.kt_per_split;
+    R.splits = (R.k_tiles + R.kt_per_split - 1) / R.kt_per_split;
+    R.unit_begin = unit;
+    R.part = G.part;
+    unit += R.tiles_m * R.tiles_n * R.splits;
+  }
+  for (int r = nreg; r < 3; ++r) {
+    tu[r] = tu[0];
+    tv[r] = tv[0];
+  }
+  p.total_units = unit;
+  const int grid = unit < num_sms ? unit : num_sms;
+  tc_wgrad_kernel<<<grid, kThreads, W_SMEM, st>>>(tu[0], tv[0], tu[1], tv[1], tu[2], tv[2], p);
+  return cudaGetLastError();
+}
+
+int tc_wgrad_splits(int rows, int kt_per_split) {
+  const int k_tiles = (rows + BK - 1) / BK;
+  return (k_tiles + kt_per_split - 1) / kt_per_split;
+}
+
+}  // namespace ppo

@@ -1,0 +1,44 @@
+"""Shared helpers of the GPU parity tests (marshalling only)."""
+import numpy as np
+
+
+def dev(x):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def normwise(x, ref):
+    """||x - ref||_2 / ||ref||_2 (0 when both vanish)."""
+    x = np.asarray(x, np.float64).ravel()
+    ref = np.asarray(ref, np.float64).ravel()
+    d = np.linalg.norm(x - ref)
+    n = np.linalg.norm(ref)
+    return 0.0 if d == 0 else d / max(n, 1e-300)
+
+
+def assert_elementwise(x, ref, rtol):
+    """|x - ref| <= rtol * (|ref| + rms(ref)) element by element."""
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    bad = np.abs(x - ref) > rtol * (np.abs(ref) + rms)
+    if bad.any():
+        i = np.flatnonzero(bad.ravel())[0]
+        raise AssertionError(f"{bad.sum()} of {bad.size} elements differ; first at {i}: "
+                             f"{x.ravel()[i]!r} vs {ref.ravel()[i]!r} (rms {rms:.3g})")
+
+
+def param_slices(w):
+    """name -> slice of the flat parameter vector."""
+    D, H1, H2, C, G = w.obs_dim, w.h1, w.h2, w.out_cols, w.n_gauss
+    sizes = [("W1", H1 * D), ("b1", H1), ("W2", H2 * H1), ("b2", H2), ("W3", C * H2),
+             ("b3", C), ("logstd", G)]
+    out, o = {}, 0
+    for n, s in sizes:
+        out[n] = slice(o, o + s)
+        o += s
+    return out
