@@ -199,6 +199,28 @@ ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_ac
                            float gamma, float lambda, float lr, uint32_t seed, float *h_stats,
                            cudaStream_t stream);
 
+/* ---- Profiling -----------------------------------------------------------------
+ * The library's kernels, by stage; one stage entry is one kernel launch. */
+#define PPO_NUM_STAGES 18
+/* Name of a stage (static string; "unknown" outside [0, PPO_NUM_STAGES)). */
+const char *ppo_stage_name(int32_t stage);
+
+/* Runs one whole update exactly as ppo_update would (same arguments, same
+ * effect on parameters, Adam state and step counter), from a CUDA graph in
+ * which a CUDA event is recorded after every kernel, then returns per stage
+ * the summed device time in milliseconds (h_stage_ms[PPO_NUM_STAGES], HOST)
+ * and the number of launches (h_stage_launches[PPO_NUM_STAGES], HOST).  A
+ * launch's time is the interval since the previous kernel's event, so it
+ * includes its own launch gap.  Synchronous; `stream` must not be the legacy
+ * default stream. */
+ppo_status ppo_update_profile(ppo_ctx *ctx, const float *d_obs, const int32_t *d_act_disc,
+                              const float *d_act_cont, const float *d_logp_old,
+                              const float *d_val, const float *d_rew, const float *d_done,
+                              const float *d_boot, int64_t T, int64_t N, int32_t epochs,
+                              int32_t minibatches, float gamma, float lambda, float lr,
+                              uint32_t seed, float *d_stats, float *h_stage_ms,
+                              int32_t *h_stage_launches, cudaStream_t stream);
+
 /* Synchronises `stream` and returns any error latched on the device since
  * the last call (PPO_ERR_TIMEOUT if a bounded wait gave up), clearing it. */
 ppo_status ppo_sync_status(ppo_ctx *ctx, cudaStream_t stream);

@@ -80,6 +80,7 @@ def lib():
         L.orc_num_params.argtypes = [ctypes.POINTER(_Net)]
         L.orc_num_params.restype = _I64
         L.orc_forward.argtypes = [ctypes.POINTER(_Net), _P, _P, _P]
+        L.orc_policy_logp.argtypes = [ctypes.POINTER(_Net), _P, _I64, _P, _P, _P, _P, _P]
         L.orc_loss_grad.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_LossCfg), _P, _I64, _P,
                                     _P, _P, _P, _P, _P, _P, ctypes.c_int, _D, _D, _P, _P, _P]
         L.orc_loss_grad.restype = _D
@@ -197,6 +198,21 @@ def forward(net: Net, params, x):
         lib().orc_forward(ctypes.byref(cn), _ptr(params), _ptr(r), _ptr(o))
         out[i] = o
     return out
+
+
+def policy_logp(net: Net, params, obs, act_disc, act_cont=None):
+    """Per-row (log-probability of the action, entropy) under params."""
+    params = _as(params, np.float64)
+    obs = _as(obs, np.float32).reshape(-1, net.obs_dim)
+    n = obs.shape[0]
+    act_disc = _as(act_disc, np.int32)
+    act_cont = _as(act_cont if act_cont is not None and net.n_gauss else np.zeros(1), np.float32)
+    lp = np.empty(n, np.float64)
+    ent = np.empty(n, np.float64)
+    cn = net.c()
+    lib().orc_policy_logp(ctypes.byref(cn), _ptr(params), n, _ptr(obs), _ptr(act_disc),
+                          _ptr(act_cont), _ptr(lp), _ptr(ent))
+    return lp, ent
 
 
 def loss_grad(net: Net, params, idx, obs, act_disc, act_cont, logp_old, adv, ret,

@@ -180,6 +180,63 @@ void orc_forward(const orc_net *net, const double *params, const float *x, doubl
     free(buf);
 }
 
+/* Log-probability of one row's action and the policy entropy, from the
+ * row's output columns z: log-softmax per discrete head (probabilities
+ * multiply over heads, so log-probabilities and entropies add), then the
+ * diagonal-Gaussian dimensions.  logprob[] receives each head logit's
+ * log-softmax, head_ent[] each head's entropy. */
+static void orc_row_policy(const orc_net *net, const double *logstd, const double *z,
+                           const int32_t *act, const float *actc, double *logprob,
+                           double *head_ent, double *logp_out, double *ent_out)
+{
+    const double LOG_2PI = log(2.0 * acos(-1.0));
+    double logp = 0.0, ent = 0.0;
+    int64_t off = 0;
+    for (int64_t h = 0; h < net->n_heads; ++h) {
+        int64_t n = net->head_n[h];
+        double zmax = z[off];
+        for (int64_t k = 1; k < n; ++k) if (z[off + k] > zmax) zmax = z[off + k];
+        double se = 0.0;
+        for (int64_t k = 0; k < n; ++k) se += exp(z[off + k] - zmax);
+        double lse = zmax + log(se);
+        double eh = 0.0;
+        for (int64_t k = 0; k < n; ++k) {
+            logprob[off + k] = z[off + k] - lse;
+            eh -= exp(logprob[off + k]) * logprob[off + k];
+        }
+        head_ent[h] = eh;
+        ent += eh;
+        logp += logprob[off + act[h]];
+        off += n;
+    }
+    for (int64_t g = 0; g < net->n_gauss; ++g) {
+        double mu = z[off + g], s = logstd[g];
+        double a = (double)actc[g];
+        double var = exp(2.0 * s);
+        logp += -(a - mu) * (a - mu) / (2.0 * var) - s - 0.5 * LOG_2PI;
+        ent += 0.5 + 0.5 * LOG_2PI + s;
+    }
+    *logp_out = logp;
+    *ent_out = ent;
+}
+
+void orc_policy_logp(const orc_net *net, const double *params, int64_t n, const float *obs,
+                     const int32_t *act_disc, const float *act_cont, double *logp, double *ent)
+{
+    const int64_t C = orc_out_cols(net);
+    orc_views w = orc_split(net, params);
+    double *z = (double *)malloc(sizeof(double) * (size_t)C);
+    double *logprob = (double *)malloc(sizeof(double) * (size_t)C);
+    double head_ent[8];
+    for (int64_t r = 0; r < n; ++r) {
+        orc_forward(net, params, obs + r * net->obs_dim, z);
+        orc_row_policy(net, w.logstd, z, act_disc + r * net->n_heads,
+                       act_cont + r * net->n_gauss, logprob, head_ent, &logp[r], &ent[r]);
+    }
+    free(z);
+    free(logprob);
+}
+
 /* ------------------------------------------------------------------------ */
 /* "Teaching Mario to speedrun", sec. 6 "Don't move too far at once":
  *   ratio  = new_prob(action) / old_prob(action)
@@ -205,7 +262,6 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
     const int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
     const int64_t NH = net->n_heads, G = net->n_gauss;
     const int64_t P = orc_num_params(net);
-    const double LOG_2PI = log(2.0 * acos(-1.0));
     orc_views w = orc_split(net, params);
 
     memset(grad, 0, sizeof(double) * (size_t)P);
@@ -231,33 +287,9 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
         orc_forward_full(net, &w, x, pre1, h1, pre2, h2, z);
 
         /* log-probability and entropy of the taken action */
-        double logp = 0.0, ent = 0.0;
-        int64_t off = 0;
-        double head_ent[8];
-        for (int64_t h = 0; h < NH; ++h) {
-            int64_t n = net->head_n[h];
-            double zmax = z[off];
-            for (int64_t k = 1; k < n; ++k) if (z[off + k] > zmax) zmax = z[off + k];
-            double se = 0.0;
-            for (int64_t k = 0; k < n; ++k) se += exp(z[off + k] - zmax);
-            double lse = zmax + log(se);
-            double eh = 0.0;
-            for (int64_t k = 0; k < n; ++k) {
-                logprob[off + k] = z[off + k] - lse;
-                eh -= exp(logprob[off + k]) * logprob[off + k];
-            }
-            head_ent[h] = eh;
-            ent += eh;
-            logp += logprob[off + act_disc[row * NH + h]];
-            off += n;
-        }
-        for (int64_t g = 0; g < G; ++g) {
-            double mu = z[off + g], s = w.logstd[g];
-            double a = (double)act_cont[row * G + g];
-            double var = exp(2.0 * s);
-            logp += -(a - mu) * (a - mu) / (2.0 * var) - s - 0.5 * LOG_2PI;
-            ent += 0.5 + 0.5 * LOG_2PI + s;
-        }
+        double logp, ent, head_ent[8];
+        orc_row_policy(net, w.logstd, z, act_disc + row * NH, act_cont + row * G, logprob,
+                       head_ent, &logp, &ent);
         const double value = z[C - 1];
 
         double A = adv[row];
@@ -280,7 +312,7 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
         const double g_logp = (s1 <= s2) ? -A * ratio * inv_mb : 0.0;
         const double g_ent = -cfg->ent_coef * inv_mb;
 
-        off = 0;
+        int64_t off = 0;
         for (int64_t h = 0; h < NH; ++h) {
             int64_t n = net->head_n[h];
             int64_t a = act_disc[row * NH + h];

@@ -71,6 +71,11 @@ int64_t orc_num_params(const orc_net *net);
 /* Forward pass of one observation; z has C entries. */
 void orc_forward(const orc_net *net, const double *params, const float *x, double *z);
 
+/* Per-row log-probability of the given action and policy entropy at params
+ * (rows 0..n of obs [n][D], act_disc [n][n_heads], act_cont [n][n_gauss]). */
+void orc_policy_logp(const orc_net *net, const double *params, int64_t n, const float *obs,
+                     const int32_t *act_disc, const float *act_cont, double *logp, double *ent);
+
 typedef struct {
     double clip, vf_coef, ent_coef;
 } orc_loss_cfg;

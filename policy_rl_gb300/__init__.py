@@ -19,7 +19,7 @@ __all__ = [
     "ppo_gae_workspace_bytes", "ppo_minibatch_perm", "ppo_perm_workspace_bytes",
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
-    "ppo_sync_status", "library_path",
+    "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "library_path",
 ]
 
 
@@ -175,6 +175,23 @@ def ppo_update_host(ctx, obs, act_disc, act_cont, logp_old, val, rew, done, boot
         _ptr(stats), _stream(stream)), "ppo_update_host")
 
 
+def ppo_stage_name(stage: int) -> str:
+    return _lib().ppo_stage_name(stage).decode()
+
+
+def ppo_update_profile(ctx, obs, act_disc, act_cont, logp_old, val, rew, done, boot, epochs,
+                       minibatches, gamma, lam, lr, seed, stats=None, stream=None):
+    """One profiled update; returns {stage name: (total ms, launches)}."""
+    T, N = val.shape
+    ms = (ctypes.c_float * _abi.NUM_STAGES)()
+    cnt = (ctypes.c_int32 * _abi.NUM_STAGES)()
+    _abi.check(_lib().ppo_update_profile(
+        ctx, _ptr(obs), _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(val), _ptr(rew),
+        _ptr(done), _ptr(boot), T, N, epochs, minibatches, gamma, lam, lr, seed & 0xFFFFFFFF,
+        _ptr(stats), ms, cnt, _stream(stream)), "ppo_update_profile")
+    return {ppo_stage_name(i): (ms[i], cnt[i]) for i in range(_abi.NUM_STAGES) if cnt[i]}
+
+
 def ppo_sync_status(ctx, stream=None) -> None:
     _abi.check(_lib().ppo_sync_status(ctx, _stream(stream)), "ppo_sync_status")
 
@@ -210,6 +227,9 @@ class Context:
 
     def update_host(self, *a, **k):
         return ppo_update_host(self.handle, *a, **k)
+
+    def update_profile(self, *a, **k):
+        return ppo_update_profile(self.handle, *a, **k)
 
     def sync_status(self, stream=None):
         return ppo_sync_status(self.handle, stream)

@@ -18,8 +18,10 @@ SYMBOLS = (
     "ppo_status_string", "ppo_create", "ppo_destroy", "ppo_param_count", "ppo_buffers",
     "ppo_params_changed", "ppo_get_step", "ppo_gae_workspace_bytes", "ppo_gae",
     "ppo_perm_workspace_bytes", "ppo_minibatch_perm", "ppo_minibatch_loss_grad",
-    "ppo_adam_step", "ppo_update", "ppo_update_host", "ppo_sync_status",
+    "ppo_adam_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
+    "ppo_sync_status",
 )
+NUM_STAGES = 18
 
 STATUS = {0: "PPO_OK", 1: "PPO_ERR_INVALID", 2: "PPO_ERR_ALIGN", 3: "PPO_ERR_CUDA",
           4: "PPO_ERR_UNSUPPORTED", 5: "PPO_ERR_TIMEOUT", 6: "PPO_ERR_NOMEM"}
@@ -84,6 +86,9 @@ def load(path: str = LIB_PATH):
                         u32, _P, _P], ctypes.c_int),
         "ppo_update_host": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F,
                              _F, u32, _P, _P], ctypes.c_int),
+        "ppo_stage_name": ([i32], ctypes.c_char_p),
+        "ppo_update_profile": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F,
+                                _F, _F, u32, _P, _P, _P, _P], ctypes.c_int),
         "ppo_sync_status": ([_P, _P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():

@@ -80,6 +80,11 @@ struct ppo_ctx {
   int32_t* st_act = nullptr;
   int64_t st_stats_cap = 0;
 
+  // kernel-boundary trace hook (profiling) and its events
+  Trace tr;
+  std::vector<cudaEvent_t> prof_events;
+  std::vector<int> prof_stages;
+
   // graph cache of the last ppo_update
   cudaGraphExec_t gexec = nullptr;
   UpdateKey gkey{};
@@ -106,6 +111,7 @@ struct ppo_ctx {
   }
   ~ppo_ctx() {
     if (gexec) cudaGraphExecDestroy(gexec);
+    for (cudaEvent_t e : prof_events) cudaEventDestroy(e);
     for (void* p : allocs) cudaFree(p);
   }
 };
@@ -210,6 +216,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
   ga.adv_mb = c->adv_mb;
   ga.ret_mb = c->ret_mb;
   PPO_CUDA(launch_gather(s, ga, st));
+  c->tr.mark(ST_GATHER, st);
 
   LossRows rows{c->act_mb, c->actc_mb, c->logp_mb, c->adv_mb, c->ret_mb};
   LossCoef lc{c->cfg.clip, c->cfg.vf_coef, c->cfg.ent_coef};
@@ -234,18 +241,23 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     // forward: H1 = act(X W1^T + b1), H2 = act(H1 W2^T + b2)
     GemmOperands g1{X, s.Dp, c->sh.W1s, s.Dp, M, s.H1, s.Dp};
     PPO_CUDA(tc_gemm_bias_act(g1, P + s.ob1, s.act, H1, s.H1, c->err, kTimeoutNs, ns, st));
+    c->tr.mark(ST_FWD1, st);
     GemmOperands g2{H1, s.H1, c->sh.W2s, s.H1, M, s.H2, s.H1};
     PPO_CUDA(tc_gemm_bias_act(g2, P + s.ob2, s.act, H2, s.H2, c->err, kTimeoutNs, ns, st));
+    c->tr.mark(ST_FWD2, st);
     // head + loss: z = H2 W3^T + b3 -> dz
     int n3 = 0, n2 = 0, n1 = 0;
     GemmOperands g3{H2, s.H2, c->sh.W3s, s.H2, M, s.CP, s.H2};
     PPO_CUDA(tc_gemm_loss(g3, s, lc, rows, inv_mb, P + s.ob3, P + s.ologstd, dZ, c->lddz, c->cs3,
                           c->lossp, c->err, kTimeoutNs, ns, st, &n3));
+    c->tr.mark(ST_LOSS, st);
     // backward data: dP2 = (dz W3) * act'(H2);  dP1 = (dP2 W2) * act'(H1)
     GemmOperands g4{dZ, c->lddz, c->sh.W3Ts, c->sh.ld3t, M, s.H2, s.CP};
     PPO_CUDA(tc_gemm_dact(g4, H2, s.H2, s.act, dP2, s.H2, c->cs2, c->err, kTimeoutNs, ns, st, &n2));
+    c->tr.mark(ST_DACT2, st);
     GemmOperands g5{dP2, s.H2, c->sh.W2Ts, s.H2, M, s.H1, s.H2};
     PPO_CUDA(tc_gemm_dact(g5, H1, s.H1, s.act, dP1, s.H1, c->cs1, c->err, kTimeoutNs, ns, st, &n1));
+    c->tr.mark(ST_DACT1, st);
     // weight gradients, split over the minibatch rows
     const int per = wgrad_kt_per_split(s, mb, ns);
     WGradRegion regs[3] = {
@@ -256,6 +268,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
       if (tc_wgrad_splits(M, r.kt_per_split) > kMaxSplit)
         r.kt_per_split = (int)(((mb + 63) / 64 + kMaxSplit - 1) / kMaxSplit);
     PPO_CUDA(tc_wgrad(regs, 3, M, 8192, 1024, c->err, kTimeoutNs, ns, st));
+    c->tr.mark(ST_WGRAD, st);
     ra.pW1 = c->pW1; ra.s1 = tc_wgrad_splits(M, regs[1].kt_per_split); ra.ld1 = s.Dp;
     ra.pW2 = c->pW2; ra.s2 = tc_wgrad_splits(M, regs[0].kt_per_split);
     ra.pW3t = c->pW3; ra.s3 = tc_wgrad_splits(M, regs[2].kt_per_split); ra.ld3 = 64;
@@ -272,16 +285,21 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     auto* dP1 = static_cast<float*>(c->dP1);
     SimtOperands g1{X, s.D, 1, P + s.oW1, s.D, 1, M, s.H1, s.D};
     PPO_CUDA(simt_bias_act(g1, P + s.ob1, s.act, H1, s.H1, st));
+    c->tr.mark(ST_FWD1, st);
     SimtOperands g2{H1, s.H1, 1, P + s.oW2, s.H1, 1, M, s.H2, s.H1};
     PPO_CUDA(simt_bias_act(g2, P + s.ob2, s.act, H2, s.H2, st));
+    c->tr.mark(ST_FWD2, st);
     int n3 = 0;
     PPO_CUDA(simt_head_loss(s, lc, rows, inv_mb, H2, P + s.oW3, P + s.ob3, P + s.ologstd, M, dZ,
                             c->cs3, c->lossp, st, &n3));
+    c->tr.mark(ST_LOSS, st);
     // dP2(m, n) = sum_c dz(m, c) W3[c][n] * act'(H2)
     SimtOperands g4{dZ, s.CP, 1, P + s.oW3, 1, s.H2, M, s.H2, s.C};
     PPO_CUDA(simt_dact(g4, H2, s.H2, s.act, dP2, s.H2, c->cs2, st));
+    c->tr.mark(ST_DACT2, st);
     SimtOperands g5{dP2, s.H2, 1, P + s.oW2, 1, s.H1, M, s.H1, s.H2};
     PPO_CUDA(simt_dact(g5, H1, s.H1, s.act, dP1, s.H1, c->cs1, st));
+    c->tr.mark(ST_DACT1, st);
     // split-K weight gradients (transposed dW3 like the tensor-core path)
     auto kps = [&](int Mo, int No) {
       const int tiles = ((Mo + 63) / 64) * ((No + 63) / 64);
@@ -295,10 +313,13 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     const int k2 = kps(s.H2, s.H1), k1 = kps(s.H1, s.D), k3 = kps(s.H2, s.CP);
     SimtOperands w2{dP2, 1, s.H2, H1, 1, s.H1, s.H2, s.H1, M};
     PPO_CUDA(simt_wgrad(w2, k2, c->pW2, st));
+    c->tr.mark(ST_WGRAD, st);
     SimtOperands w1{dP1, 1, s.H1, X, 1, s.D, s.H1, s.D, M};
     PPO_CUDA(simt_wgrad(w1, k1, c->pW1, st));
+    c->tr.mark(ST_WGRAD, st);
     SimtOperands w3{H2, 1, s.H2, dZ, 1, s.CP, s.H2, s.CP, M};
     PPO_CUDA(simt_wgrad(w3, k3, c->pW3, st));
+    c->tr.mark(ST_WGRAD, st);
     ra.pW1 = c->pW1; ra.s1 = (int)((mb + k1 - 1) / k1); ra.ld1 = s.D;
     ra.pW2 = c->pW2; ra.s2 = (int)((mb + k2 - 1) / k2);
     ra.pW3t = c->pW3; ra.s3 = (int)((mb + k3 - 1) / k3); ra.ld3 = s.CP;
@@ -308,6 +329,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     ra.ploss = c->lossp; ra.nl = n3;
   }
   PPO_CUDA(launch_reduce(ra, st));
+  c->tr.mark(ST_REDUCE, st);
   return PPO_OK;
 }
 
@@ -329,7 +351,7 @@ ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t
   a.grad_norm_out = grad_norm_out;
   a.s = c->s;
   a.sh = c->sh;
-  PPO_CUDA(launch_adam(a, st));
+  PPO_CUDA(launch_adam(a, st, &c->tr));
   return PPO_OK;
 }
 
@@ -342,12 +364,15 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
   const __nv_bfloat16* packed = nullptr;
   if (c->bf16) {
     PPO_CUDA(launch_pack_obs(obs, B, c->s.D, c->s.Dp, c->obs_packed, st));
+    c->tr.mark(ST_PACK, st);
     packed = c->obs_packed;
   }
   PPO_CUDA(launch_gae(rew, val, done, boot, (int)T, (int)N, gamma, lambda, c->adv, c->ret,
                       c->gae_part, gae_num_blocks((int)N), st));
+  c->tr.mark(ST_GAE, st);
   PPO_CUDA(launch_gae_finalize(c->gae_part, gae_num_blocks((int)N), c->advstats, st));
-  PPO_CUDA(launch_perm(seed, 0, epochs, B, c->perm, c->perm_work, st));
+  c->tr.mark(ST_GAE_FINALIZE, st);
+  PPO_CUDA(launch_perm(seed, 0, epochs, B, c->perm, c->perm_work, st, &c->tr));
   for (int e = 0; e < epochs; ++e)
     for (int k = 0; k < minibatches; ++k) {
       const int32_t* idx = c->perm + (int64_t)e * B + (int64_t)k * mb;
@@ -590,11 +615,11 @@ ppo_status ppo_adam_step(ppo_ctx* c, float lr, float* grad_norm, cudaStream_t st
   return enqueue_adam(c, lr, grad_norm, st);
 }
 
-ppo_status ppo_update(ppo_ctx* c, const float* obs, const int32_t* act, const float* actc,
-                      const float* logp_old, const float* val, const float* rew,
-                      const float* done, const float* boot, int64_t T, int64_t N,
-                      int32_t epochs, int32_t minibatches, float gamma, float lambda, float lr,
-                      uint32_t seed, float* stats, cudaStream_t st) {
+static ppo_status check_update_args(ppo_ctx* c, const float* obs, const int32_t* act,
+                                    const float* actc, const float* logp_old, const float* val,
+                                    const float* rew, const float* done, const float* boot,
+                                    int64_t T, int64_t N, int32_t epochs, int32_t minibatches,
+                                    const float* stats) {
   if (!c || !val || !rew || !done || !boot) return PPO_ERR_INVALID;
   if (T < 1 || N < 1 || epochs < 1 || minibatches < 1) return PPO_ERR_INVALID;
   const int64_t B = T * N;
@@ -605,7 +630,16 @@ ppo_status ppo_update(ppo_ctx* c, const float* obs, const int32_t* act, const fl
   const void* ps[] = {obs, act, actc, logp_old, val, rew, done, boot, stats};
   for (const void* p : ps)
     if (p && !al16(p)) return PPO_ERR_ALIGN;
+  return PPO_OK;
+}
 
+ppo_status ppo_update(ppo_ctx* c, const float* obs, const int32_t* act, const float* actc,
+                      const float* logp_old, const float* val, const float* rew,
+                      const float* done, const float* boot, int64_t T, int64_t N,
+                      int32_t epochs, int32_t minibatches, float gamma, float lambda, float lr,
+                      uint32_t seed, float* stats, cudaStream_t st) {
+  TRY(check_update_args(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
+                        minibatches, stats));
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   PPO_CUDA(cudaStreamIsCapturing(st, &cs));
   if (st == nullptr || cs != cudaStreamCaptureStatusNone) {
@@ -649,6 +683,76 @@ ppo_status ppo_update(ppo_ctx* c, const float* obs, const int32_t* act, const fl
     c->gvalid = true;
   }
   PPO_CUDA(cudaGraphLaunch(c->gexec, st));
+  return PPO_OK;
+}
+
+const char* ppo_stage_name(int32_t stage) {
+  static const char* names[ST_COUNT] = {
+      "pack_obs", "gae_scan", "gae_finalize", "gae_normalize", "perm_hist", "perm_scan",
+      "perm_scatter", "gather", "fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm",
+      "dact1_gemm", "wgrad_gemm", "grad_reduce", "grad_sqnorm", "adam", "weight_shadows"};
+  if (stage < 0 || stage >= ST_COUNT) return "unknown";
+  return names[stage];
+}
+
+static void prof_mark(void* user, int stage, cudaStream_t st) {
+  ppo_ctx* c = static_cast<ppo_ctx*>(user);
+  const size_t i = c->prof_stages.size();
+  if (i + 1 < c->prof_events.size()) {
+    cudaEventRecord(c->prof_events[i + 1], st);
+    c->prof_stages.push_back(stage);
+  }
+}
+
+ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
+                              const float* actc, const float* logp_old, const float* val,
+                              const float* rew, const float* done, const float* boot, int64_t T,
+                              int64_t N, int32_t epochs, int32_t minibatches, float gamma,
+                              float lambda, float lr, uint32_t seed, float* stats,
+                              float* h_stage_ms, int32_t* h_stage_launches, cudaStream_t st) {
+  TRY(check_update_args(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
+                        minibatches, stats));
+  if (!h_stage_ms || !h_stage_launches || st == nullptr) return PPO_ERR_INVALID;
+  const size_t need = 8 + 3 * 4 * (size_t)epochs + 20 * (size_t)epochs * minibatches;
+  while (c->prof_events.size() < need) {
+    cudaEvent_t e;
+    PPO_CUDA(cudaEventCreate(&e));
+    c->prof_events.push_back(e);
+  }
+  c->prof_stages.clear();
+  PPO_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+  cudaEventRecord(c->prof_events[0], st);
+  c->tr.fn = prof_mark;
+  c->tr.user = c;
+  ppo_status r = enqueue_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
+                                minibatches, gamma, lambda, lr, seed, stats, st);
+  c->tr = Trace{};
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(st, &graph);
+  if (r != PPO_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return r;
+  }
+  if (e != cudaSuccess) return PPO_ERR_CUDA;
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return PPO_ERR_CUDA;
+  e = cudaGraphUpload(exec, st);
+  if (e == cudaSuccess) e = cudaGraphLaunch(exec, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaGraphExecDestroy(exec);
+  if (e != cudaSuccess) return PPO_ERR_CUDA;
+  for (int k = 0; k < ST_COUNT; ++k) {
+    h_stage_ms[k] = 0.f;
+    h_stage_launches[k] = 0;
+  }
+  for (size_t i = 0; i < c->prof_stages.size(); ++i) {
+    float ms = 0.f;
+    PPO_CUDA(cudaEventElapsedTime(&ms, c->prof_events[i], c->prof_events[i + 1]));
+    h_stage_ms[c->prof_stages[i]] += ms;
+    h_stage_launches[c->prof_stages[i]] += 1;
+  }
   return PPO_OK;
 }
 

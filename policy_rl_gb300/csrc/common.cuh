@@ -178,6 +178,24 @@ __device__ __forceinline__ void row_loss(const NetShape& s, const LossCoef& lc, 
 }
 
 // ---------------------------------------------------------------------------
+// Kernel stages of one update; every stage is exactly one kernel launch.  A
+// Trace hook, when set, is called on the launching stream after each launch
+// (the profiler records a CUDA event there).
+enum Stage : int {
+  ST_PACK = 0, ST_GAE, ST_GAE_FINALIZE, ST_GAE_NORMALIZE, ST_PERM_HIST, ST_PERM_SCAN,
+  ST_PERM_SCATTER, ST_GATHER, ST_FWD1, ST_FWD2, ST_LOSS, ST_DACT2, ST_DACT1, ST_WGRAD,
+  ST_REDUCE, ST_SQNORM, ST_ADAM, ST_SHADOW, ST_COUNT
+};
+
+struct Trace {
+  void (*fn)(void* user, int stage, cudaStream_t st) = nullptr;
+  void* user = nullptr;
+  void mark(int stage, cudaStream_t st) const {
+    if (fn) fn(user, stage, st);
+  }
+};
+
+// ---------------------------------------------------------------------------
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_gae(const float* rew, const float* val, const float* done, const float* boot,
                        int T, int N, float gamma, float lambda, float* adv, float* ret,
@@ -190,7 +208,7 @@ cudaError_t launch_normalize(const float* adv, const float* stats, float* out, i
 
 size_t perm_workspace_bytes(int64_t B, int epochs);
 cudaError_t launch_perm(uint32_t seed, int64_t epoch0, int epochs, int64_t B, int32_t* perm,
-                        void* work, cudaStream_t st);
+                        void* work, cudaStream_t st, const Trace* tr = nullptr);
 
 cudaError_t launch_pack_obs(const float* obs, int64_t B, int D, int Dp, __nv_bfloat16* out,
                             cudaStream_t st);

@@ -146,7 +146,7 @@ struct AdamArgs {
   NetShape s;
   Shadows sh;
 };
-cudaError_t launch_adam(const AdamArgs& a, cudaStream_t st);
+cudaError_t launch_adam(const AdamArgs& a, cudaStream_t st, const Trace* tr = nullptr);
 cudaError_t launch_shadows(const float* p, const NetShape& s, const Shadows& sh, cudaStream_t st);
 
 }  // namespace ppo

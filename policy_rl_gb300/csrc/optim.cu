@@ -172,11 +172,13 @@ cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_adam(const AdamArgs& a0, cudaStream_t st) {
+cudaError_t launch_adam(const AdamArgs& a0, cudaStream_t st, const Trace* tr) {
   AdamArgs a = a0;
   sqnorm_kernel<<<kNormBlocks, kNormThreads, 0, st>>>(a.g, a.P, const_cast<double*>(a.sq_part));
+  if (tr) tr->mark(ST_SQNORM, st);
   a.nsq = kNormBlocks;
   adam_kernel<<<blocks_for(a.P, kAdamThreads, 152 * 4), kAdamThreads, 0, st>>>(a);
+  if (tr) tr->mark(ST_ADAM, st);
   return cudaGetLastError();
 }
 

@@ -160,7 +160,7 @@ size_t perm_workspace_bytes(int64_t B, int /*epochs*/) {
 }
 
 cudaError_t launch_perm(uint32_t seed, int64_t epoch0, int epochs, int64_t B, int32_t* perm,
-                        void* work, cudaStream_t st) {
+                        void* work, cudaStream_t st, const Trace* tr) {
   const int64_t tiles64 = (B + kTile - 1) / kTile;
   const int tiles = (int)tiles64;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
@@ -194,8 +194,11 @@ cudaError_t launch_perm(uint32_t seed, int64_t epoch0, int epochs, int64_t B, in
         vo = va;
       }
       hist_kernel<<<tiles, kSortThreads, 0, st>>>(in, B, shift, ghist, tiles);
+      if (tr) tr->mark(ST_PERM_HIST, st);
       scan_kernel<<<1, kScanThreads, 0, st>>>(ghist, (int64_t)tiles * kRadix);
+      if (tr) tr->mark(ST_PERM_SCAN, st);
       scatter_kernel<<<tiles, kSortThreads, 0, st>>>(in, B, shift, ghist, tiles, ko, vo);
+      if (tr) tr->mark(ST_PERM_SCATTER, st);
       in = SortIn{ko, vo, seed, draw0};
     }
     cudaError_t err = cudaGetLastError();

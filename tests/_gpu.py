@@ -42,3 +42,21 @@ def param_slices(w):
         out[n] = slice(o, o + s)
         o += s
     return out
+
+
+# log-ratio offsets given to the rows in turn: both clipped branches (-0.5,
+# +0.5), both unclipped sides (-0.1, +0.1) and r = 1; every one lies at least
+# 0.08 in log space from the clip boundaries log(0.8) and log(1.2), far more
+# than the bf16 path's log-probability error (~1e-3), so the GPU and the
+# oracle take the same clip branch on every row.
+LOG_RATIO_OFFSETS = (-0.5, -0.1, 0.0, 0.1, 0.5)
+
+
+def conditioned_logp_old(w, ro, params):
+    """logp_old = (oracle log-probability at params) - offset, per row."""
+    import oracle
+    net = oracle.Net(w.obs_dim, w.h1, w.h2, w.act, w.heads, w.n_gauss)
+    lp, _ = oracle.policy_logp(net, np.asarray(params, np.float64), ro.obs, ro.act_disc,
+                               ro.act_cont)
+    off = np.array(LOG_RATIO_OFFSETS)[np.arange(lp.size) % len(LOG_RATIO_OFFSETS)]
+    return (lp - off).astype(np.float32)

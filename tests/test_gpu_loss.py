@@ -7,20 +7,24 @@ Tolerances (normwise per parameter tensor, ||g - g_ref|| / ||g_ref||):
 Loss statistics: |x - y| <= tol * max(|y|, mean |per-row term|) -- the
 policy term is a mean of signed terms that cancel, so a purely relative test
 is ill-posed there.
+The clip decision is discontinuous, so the inputs keep every ratio well away
+from 1 +- eps (tests/_gpu.py: LOG_RATIO_OFFSETS) -- both sides then take the
+same branch on every row, as the precision rule for decisions requires.
 """
 import numpy as np
 import pytest
 
 import oracle
 from policy_rl_gb300 import synth
-from tests._gpu import dev, host, normwise, param_slices
+from tests._gpu import conditioned_logp_old, dev, host, normwise, param_slices
 
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(w, seed=0, logp_from_policy=False):
+def _inputs(w, seed=0):
     ro = synth.rollout(w, seed=seed)
     p0 = synth.init_params(w, seed=seed)
+    ro.logp_old = conditioned_logp_old(w, ro, p0)
     adv, ret = oracle.gae(ro.rew, ro.val, ro.done, ro.boot, w.gamma, w.lam)
     adv = adv.ravel().astype(np.float32)
     ret = ret.ravel().astype(np.float32)

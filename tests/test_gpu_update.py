@@ -16,7 +16,7 @@ import pytest
 
 import oracle
 from policy_rl_gb300 import synth
-from tests._gpu import dev, host, normwise
+from tests._gpu import conditioned_logp_old, dev, host, normwise
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +54,7 @@ def _update(w, seed=0, host_api=False):
     import policy_rl_gb300 as P
     ro = synth.rollout(w, seed=seed)
     p0 = synth.init_params(w, seed=seed)
+    ro.logp_old = conditioned_logp_old(w, ro, p0)
     ctx = P.Context(P.config_from_workload(w), p0)
     E, M = w.epochs, w.minibatches
     if host_api:

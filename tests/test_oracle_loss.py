@@ -260,3 +260,19 @@ def test_matches_torch_autograd(net):
     tl, tg = _torch_loss(net, params, obs, act, actc, logp_old, adv, ret, idx, 0.2, 0.5, 0.01)
     assert abs(loss - tl) < 1e-12 * max(1.0, abs(tl))
     np.testing.assert_allclose(g, tg, rtol=1e-10, atol=1e-13)
+
+
+def test_policy_logp_matches_scipy_and_the_loss():
+    net = oracle.Net(3, 4, 4, act=1, heads=(3, 2), n_gauss=2)
+    params, obs, act, actc, _, _, _ = _setup(net, 6, 12, scale=1.0)
+    lp, ent = oracle.policy_logp(net, params, obs, act, actc)
+    z = oracle.forward(net, params, obs)
+    ls = params[-2:]
+    for r in range(6):
+        ref = (scipy.special.log_softmax(z[r, 0:3])[act[r, 0]]
+               + scipy.special.log_softmax(z[r, 3:5])[act[r, 1]]
+               + sum(scipy.stats.norm.logpdf(actc[r, g], z[r, 5 + g], math.exp(ls[g]))
+                     for g in range(2)))
+        assert abs(lp[r] - ref) < 1e-10
+        lp2, ent2 = _logp_ent(net, params, obs, act, actc, r)
+        assert abs(lp[r] - lp2) < 1e-12 and abs(ent[r] - ent2) < 1e-12
