@@ -72,8 +72,10 @@ typedef struct {
                                         accumulate, fp32 master weights       */
     float clip;                  /* epsilon of clip(ratio, 1-eps, 1+eps)     */
     float vf_coef, ent_coef;     /* loss = pg + vf_coef*V - ent_coef*H       */
-    float beta1, beta2, adam_eps;
     float max_grad_norm;         /* <= 0 disables the clip                   */
+    double beta1, beta2;         /* Adam moment decays (double: 1 - beta is
+                                    formed without fp32 cancellation)        */
+    double adam_eps;
     int64_t max_batch;           /* largest T*N given to ppo_update          */
     int64_t max_minibatch;       /* largest minibatch row count              */
     int32_t max_epochs;          /* largest epoch count given to ppo_update  */

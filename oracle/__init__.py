@@ -47,7 +47,7 @@ class _Net(ctypes.Structure):
 
 class _LossCfg(ctypes.Structure):
     _fields_ = [("clip", ctypes.c_double), ("vf_coef", ctypes.c_double),
-                ("ent_coef", ctypes.c_double)]
+                ("ent_coef", ctypes.c_double), ("bf16_operands", ctypes.c_int)]
 
 
 class _Hyper(ctypes.Structure):
@@ -56,7 +56,7 @@ class _Hyper(ctypes.Structure):
                 ("ent_coef", ctypes.c_double), ("lr", ctypes.c_double),
                 ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
                 ("adam_eps", ctypes.c_double), ("max_grad_norm", ctypes.c_double),
-                ("seed", ctypes.c_uint32)]
+                ("seed", ctypes.c_uint32), ("bf16_operands", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -80,6 +80,8 @@ def lib():
         L.orc_num_params.argtypes = [ctypes.POINTER(_Net)]
         L.orc_num_params.restype = _I64
         L.orc_forward.argtypes = [ctypes.POINTER(_Net), _P, _P, _P]
+        L.orc_round_bf16.argtypes = [_D]
+        L.orc_round_bf16.restype = _D
         L.orc_policy_logp.argtypes = [ctypes.POINTER(_Net), _P, _I64, _P, _P, _P, _P, _P]
         L.orc_loss_grad.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_LossCfg), _P, _I64, _P,
                                     _P, _P, _P, _P, _P, _P, ctypes.c_int, _D, _D, _P, _P, _P]
@@ -141,10 +143,12 @@ class Hyper:
     adam_eps: float = 1e-8
     max_grad_norm: float = 0.5
     seed: int = 0
+    bf16_operands: bool = False
 
     def c(self) -> _Hyper:
         return _Hyper(self.gamma, self.lam, self.clip, self.vf_coef, self.ent_coef, self.lr,
-                      self.beta1, self.beta2, self.adam_eps, self.max_grad_norm, self.seed)
+                      self.beta1, self.beta2, self.adam_eps, self.max_grad_norm, self.seed,
+                      int(self.bf16_operands))
 
 
 def mulberry32_stream(seed: int, count: int) -> np.ndarray:
@@ -200,6 +204,10 @@ def forward(net: Net, params, x):
     return out
 
 
+def round_bf16(x: float) -> float:
+    return lib().orc_round_bf16(float(x))
+
+
 def policy_logp(net: Net, params, obs, act_disc, act_cont=None):
     """Per-row (log-probability of the action, entropy) under params."""
     params = _as(params, np.float64)
@@ -217,7 +225,7 @@ def policy_logp(net: Net, params, obs, act_disc, act_cont=None):
 
 def loss_grad(net: Net, params, idx, obs, act_disc, act_cont, logp_old, adv, ret,
               clip=0.2, vf_coef=0.5, ent_coef=0.01, normalize=False, adv_mean=0.0,
-              adv_std=1.0):
+              adv_std=1.0, bf16_operands=False):
     """Returns (loss, grad[P], stats6[6], scale6[6])."""
     params = _as(params, np.float64)
     idx = _as(idx, np.int32)
@@ -230,7 +238,7 @@ def loss_grad(net: Net, params, idx, obs, act_disc, act_cont, logp_old, adv, ret
     grad = np.empty(net.num_params, np.float64)
     st = np.empty(6, np.float64)
     sc = np.empty(6, np.float64)
-    cfg = _LossCfg(clip, vf_coef, ent_coef)
+    cfg = _LossCfg(clip, vf_coef, ent_coef, int(bool(bf16_operands)))
     cn = net.c()
     loss = lib().orc_loss_grad(ctypes.byref(cn), ctypes.byref(cfg), _ptr(params), idx.size,
                                _ptr(idx), _ptr(obs), _ptr(act_disc), _ptr(act_cont),

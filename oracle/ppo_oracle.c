@@ -148,21 +148,43 @@ static double orc_act_grad(int act, double pre, double post)
     return act == 0 ? 1.0 - post * post : (pre > 0.0 ? 1.0 : 0.0);
 }
 
+/* bf16-operand mode: the value a bf16 tensor-core GEMM reads for operand x --
+ * x rounded to fp32, then to bfloat16 (8-bit significand), both to nearest
+ * even.  Identity when the mode is off. */
+static double orc_bf16(double x)
+{
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) != 0x7F800000u) u += 0x7FFFu + ((u >> 16) & 1u);
+    u &= 0xFFFF0000u;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double orc_rnd(int bf16, double x) { return bf16 ? orc_bf16(x) : x; }
+
+double orc_round_bf16(double x) { return orc_bf16(x); }
+
+/* Forward pass of one row.  In bf16-operand mode the observation and the
+ * stored activations are rounded to bf16 (the weights are rounded by the
+ * caller); the accumulation stays in double. */
 static void orc_forward_full(const orc_net *net, const orc_views *w, const float *x,
-                             double *pre1, double *h1, double *pre2, double *h2, double *z)
+                             double *pre1, double *h1, double *pre2, double *h2, double *z,
+                             int bf16)
 {
     int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
     for (int64_t j = 0; j < H1; ++j) {
         double s = w->b1[j];
-        for (int64_t k = 0; k < D; ++k) s += w->W1[j * D + k] * (double)x[k];
+        for (int64_t k = 0; k < D; ++k) s += w->W1[j * D + k] * orc_rnd(bf16, (double)x[k]);
         pre1[j] = s;
-        h1[j] = orc_act(net->act, s);
+        h1[j] = orc_rnd(bf16, orc_act(net->act, s));
     }
     for (int64_t j = 0; j < H2; ++j) {
         double s = w->b2[j];
         for (int64_t k = 0; k < H1; ++k) s += w->W2[j * H1 + k] * h1[k];
         pre2[j] = s;
-        h2[j] = orc_act(net->act, s);
+        h2[j] = orc_rnd(bf16, orc_act(net->act, s));
     }
     for (int64_t c = 0; c < C; ++c) {
         double s = w->b3[c];
@@ -176,7 +198,7 @@ void orc_forward(const orc_net *net, const double *params, const float *x, doubl
     orc_views w = orc_split(net, params);
     double *buf = (double *)malloc(sizeof(double) * 2 * (size_t)(net->h1 + net->h2));
     orc_forward_full(net, &w, x, buf, buf + net->h1, buf + 2 * net->h1,
-                     buf + 2 * net->h1 + net->h2, z);
+                     buf + 2 * net->h1 + net->h2, z, 0);
     free(buf);
 }
 
@@ -262,7 +284,20 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
     const int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
     const int64_t NH = net->n_heads, G = net->n_gauss;
     const int64_t P = orc_num_params(net);
-    orc_views w = orc_split(net, params);
+    const int bf16 = cfg->bf16_operands;
+    /* bf16-operand mode: the GEMMs read bf16-rounded weights; biases and
+     * log-std stay in full precision */
+    double *wr = NULL;
+    if (bf16) {
+        wr = (double *)malloc(sizeof(double) * (size_t)P);
+        memcpy(wr, params, sizeof(double) * (size_t)P);
+        orc_views v0 = orc_split(net, params);
+        const int64_t nW1 = H1 * D, nW2 = H2 * H1, nW3 = C * H2;
+        for (int64_t i = 0; i < nW1; ++i) wr[(v0.W1 - params) + i] = orc_bf16(v0.W1[i]);
+        for (int64_t i = 0; i < nW2; ++i) wr[(v0.W2 - params) + i] = orc_bf16(v0.W2[i]);
+        for (int64_t i = 0; i < nW3; ++i) wr[(v0.W3 - params) + i] = orc_bf16(v0.W3[i]);
+    }
+    orc_views w = orc_split(net, bf16 ? wr : params);
 
     memset(grad, 0, sizeof(double) * (size_t)P);
     double *gW1 = grad, *gb1 = gW1 + H1 * D, *gW2 = gb1 + H1, *gb2 = gW2 + H2 * H1;
@@ -284,7 +319,7 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
     for (int64_t r = 0; r < mb; ++r) {
         const int64_t row = idx[r];
         const float *x = obs + row * D;
-        orc_forward_full(net, &w, x, pre1, h1, pre2, h2, z);
+        orc_forward_full(net, &w, x, pre1, h1, pre2, h2, z, bf16);
 
         /* log-probability and entropy of the taken action */
         double logp, ent, head_ent[8];
@@ -333,13 +368,15 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
         }
         dz[C - 1] = cfg->vf_coef * 2.0 * (value - R) * inv_mb;
 
-        /* backward through z = W3 h2 + b3 */
+        /* backward through z = W3 h2 + b3 (bias gradients take the
+         * unrounded signal; GEMM operands are rounded in bf16-operand mode) */
         for (int64_t j = 0; j < H2; ++j) dh2[j] = 0.0;
         for (int64_t c = 0; c < C; ++c) {
             gb3[c] += dz[c];
+            const double dzc = orc_rnd(bf16, dz[c]);
             for (int64_t j = 0; j < H2; ++j) {
-                gW3[c * H2 + j] += dz[c] * h2[j];
-                dh2[j] += dz[c] * w.W3[c * H2 + j];
+                gW3[c * H2 + j] += dzc * h2[j];
+                dh2[j] += dzc * w.W3[c * H2 + j];
             }
         }
         /* through h2 = act(W2 h1 + b2) */
@@ -347,6 +384,7 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
         for (int64_t j = 0; j < H2; ++j) {
             double dpre = dh2[j] * orc_act_grad(net->act, pre2[j], h2[j]);
             gb2[j] += dpre;
+            dpre = orc_rnd(bf16, dpre);
             for (int64_t k = 0; k < H1; ++k) {
                 gW2[j * H1 + k] += dpre * h1[k];
                 dh1[k] += dpre * w.W2[j * H1 + k];
@@ -356,7 +394,8 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
         for (int64_t j = 0; j < H1; ++j) {
             double dpre = dh1[j] * orc_act_grad(net->act, pre1[j], h1[j]);
             gb1[j] += dpre;
-            for (int64_t k = 0; k < D; ++k) gW1[j * D + k] += dpre * (double)x[k];
+            dpre = orc_rnd(bf16, dpre);
+            for (int64_t k = 0; k < D; ++k) gW1[j * D + k] += dpre * orc_rnd(bf16, (double)x[k]);
         }
     }
 
@@ -366,6 +405,7 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
     }
     free(pre1); free(h1); free(pre2); free(h2); free(z); free(logprob);
     free(dz); free(dh2); free(dh1);
+    free(wr);
     return sum[0] * inv_mb;
 }
 
@@ -426,7 +466,7 @@ void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
     double mean, sd;
     orc_moments(B, adv, &mean, &sd);
 
-    orc_loss_cfg lc = {hp->clip, hp->vf_coef, hp->ent_coef};
+    orc_loss_cfg lc = {hp->clip, hp->vf_coef, hp->ent_coef, hp->bf16_operands};
     for (int64_t e = 0; e < epochs; ++e) {
         orc_perm(hp->seed, e, B, perm);
         for (int64_t k = 0; k < minibatches; ++k) {

@@ -68,6 +68,10 @@ int64_t orc_out_cols(const orc_net *net);
  * W3[C][h2], b3[C], logstd[n_gauss]. */
 int64_t orc_num_params(const orc_net *net);
 
+/* x rounded to fp32, then to bfloat16, both to nearest even (the rounding of
+ * the bf16-operand mode below). */
+double orc_round_bf16(double x);
+
 /* Forward pass of one observation; z has C entries. */
 void orc_forward(const orc_net *net, const double *params, const float *x, double *z);
 
@@ -78,6 +82,12 @@ void orc_policy_logp(const orc_net *net, const double *params, int64_t n, const 
 
 typedef struct {
     double clip, vf_coef, ent_coef;
+    /* 0: every product in fp64.  1: bf16-operand mode -- the operands of
+     * every GEMM (observation, weights W1..W3, stored activations, the
+     * backpropagated signals dz, dpre2, dpre1) are rounded to bfloat16 where
+     * a bf16 tensor-core implementation stores them; sums stay in fp64 and
+     * bias gradients use the unrounded signals. */
+    int bf16_operands;
 } orc_loss_cfg;
 
 /* Loss and gradient of one minibatch.
@@ -108,6 +118,7 @@ typedef struct {
     double gamma, lambda, clip, vf_coef, ent_coef;
     double lr, beta1, beta2, adam_eps, max_grad_norm;
     uint32_t seed;
+    int bf16_operands;   /* as in orc_loss_cfg */
 } orc_hyper;
 
 /* One whole PPO update: GAE, global advantage statistics, then for each epoch

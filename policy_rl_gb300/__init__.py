@@ -56,7 +56,7 @@ def make_config(obs_dim, h1, h2, act=0, heads=(3, 2, 2), n_gauss=0, precision=1,
                 max_grad_norm=0.5, max_batch=1, max_minibatch=1, max_epochs=1) -> PpoConfig:
     hn = (ctypes.c_int32 * _abi.MAX_HEADS)(*(list(heads) + [0] * (_abi.MAX_HEADS - len(heads))))
     return PpoConfig(obs_dim, h1, h2, act, len(heads), hn, n_gauss, precision, clip, vf_coef,
-                     ent_coef, beta1, beta2, adam_eps, max_grad_norm, max_batch, max_minibatch,
+                     ent_coef, max_grad_norm, beta1, beta2, adam_eps, max_batch, max_minibatch,
                      max_epochs)
 
 

@@ -39,8 +39,8 @@ class PpoConfig(ctypes.Structure):
         ("act", ctypes.c_int32), ("n_heads", ctypes.c_int32),
         ("head_n", ctypes.c_int32 * MAX_HEADS), ("n_gauss", ctypes.c_int32),
         ("precision", ctypes.c_int32), ("clip", ctypes.c_float), ("vf_coef", ctypes.c_float),
-        ("ent_coef", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
-        ("adam_eps", ctypes.c_float), ("max_grad_norm", ctypes.c_float),
+        ("ent_coef", ctypes.c_float), ("max_grad_norm", ctypes.c_float),
+        ("beta1", ctypes.c_double), ("beta2", ctypes.c_double), ("adam_eps", ctypes.c_double),
         ("max_batch", ctypes.c_int64), ("max_minibatch", ctypes.c_int64),
         ("max_epochs", ctypes.c_int32),
     ]

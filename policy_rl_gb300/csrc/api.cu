@@ -346,6 +346,8 @@ ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t
   a.b1 = c->cfg.beta1;
   a.b2 = c->cfg.beta2;
   a.eps = c->cfg.adam_eps;
+  a.omb1 = (float)(1.0 - c->cfg.beta1);   // 1 - beta in double: no cancellation in fp32
+  a.omb2 = (float)(1.0 - c->cfg.beta2);
   a.step = c->step;
   a.done_ctr = c->done_ctr;
   a.grad_norm_out = grad_norm_out;
@@ -699,7 +701,8 @@ static void prof_mark(void* user, int stage, cudaStream_t st) {
   ppo_ctx* c = static_cast<ppo_ctx*>(user);
   const size_t i = c->prof_stages.size();
   if (i + 1 < c->prof_events.size()) {
-    cudaEventRecord(c->prof_events[i + 1], st);
+    // External: inside stream capture this becomes an event-record node
+    cudaEventRecordWithFlags(c->prof_events[i + 1], st, cudaEventRecordExternal);
     c->prof_stages.push_back(stage);
   }
 }
@@ -721,7 +724,7 @@ ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
   }
   c->prof_stages.clear();
   PPO_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
-  cudaEventRecord(c->prof_events[0], st);
+  PPO_CUDA(cudaEventRecordWithFlags(c->prof_events[0], st, cudaEventRecordExternal));
   c->tr.fn = prof_mark;
   c->tr.user = c;
   ppo_status r = enqueue_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,

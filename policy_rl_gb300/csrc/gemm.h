@@ -139,7 +139,9 @@ struct AdamArgs {
   int64_t P;
   const double* sq_part;
   int nsq;
-  float max_norm, lr, b1, b2, eps;
+  float max_norm, lr, eps;
+  double b1, b2;      // for the bias corrections 1 - beta^t
+  float omb1, omb2;   // 1 - beta1, 1 - beta2 (rounded once from double)
   int64_t* step;
   unsigned* done_ctr;
   float* grad_norm_out;

@@ -117,15 +117,16 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
   __syncthreads();
   const float coef = s_coef;
   const double t = (double)s_t;
-  const float bc1 = (float)(1.0 - pow((double)a.b1, t));
-  const float bc2 = (float)(1.0 - pow((double)a.b2, t));
-  const float b1 = a.b1, b2 = a.b2, lr = a.lr, eps = a.eps;
+  const float bc1 = (float)(1.0 - pow(a.b1, t));
+  const float bc2 = (float)(1.0 - pow(a.b2, t));
+  const float b1 = (float)a.b1, b2 = (float)a.b2, omb1 = a.omb1, omb2 = a.omb2;
+  const float lr = a.lr, eps = a.eps;
   const bool shadows = a.sh.W1s != nullptr;
   const int64_t stride = (int64_t)gridDim.x * kAdamThreads;
   for (int64_t i = (int64_t)blockIdx.x * kAdamThreads + threadIdx.x; i < a.P; i += stride) {
     const float g = a.g[i] * coef;
-    const float m = b1 * a.m[i] + (1.f - b1) * g;
-    const float v = b2 * a.v[i] + (1.f - b2) * g * g;
+    const float m = b1 * a.m[i] + omb1 * g;
+    const float v = b2 * a.v[i] + omb2 * g * g;
     const float mhat = m / bc1;
     const float vhat = v / bc2;
     const float p = a.p[i] - lr * mhat / (sqrtf(vhat) + eps);

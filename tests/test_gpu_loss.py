@@ -9,7 +9,11 @@ policy term is a mean of signed terms that cancel, so a purely relative test
 is ill-posed there.
 The clip decision is discontinuous, so the inputs keep every ratio well away
 from 1 +- eps (tests/_gpu.py: LOG_RATIO_OFFSETS) -- both sides then take the
-same branch on every row, as the precision rule for decisions requires.
+same branch on every row.  The ReLU derivative 1[pre > 0] is a decision too:
+bf16-mode results are compared with the oracle's bf16-operand mode, which
+rounds exactly the GEMM operands the bf16 path rounds, so pre-activations
+agree to fp32 accumulation error and every unit takes the same branch.  For
+tanh nets the bf16 path is also held to the plain fp64 oracle at 2e-2.
 """
 import numpy as np
 import pytest
@@ -50,11 +54,13 @@ def _gpu_grad(w, ro, p0, adv, ret, idx, adv_stats=None, repeat=1):
     return grads, s6
 
 
-def _oracle(w, ro, p0, adv, ret, idx, adv_stats=None):
+def _oracle(w, ro, p0, adv, ret, idx, adv_stats=None, bf16_operands=None):
     net = oracle.Net(w.obs_dim, w.h1, w.h2, w.act, w.heads, w.n_gauss)
-    kw = {}
+    if bf16_operands is None:
+        bf16_operands = w.precision == "bf16"
+    kw = dict(bf16_operands=bf16_operands)
     if adv_stats is not None:
-        kw = dict(normalize=True, adv_mean=float(adv_stats[0]), adv_std=float(adv_stats[1]))
+        kw.update(normalize=True, adv_mean=float(adv_stats[0]), adv_std=float(adv_stats[1]))
     return oracle.loss_grad(net, p0.astype(np.float64), idx, ro.obs, ro.act_disc, ro.act_cont,
                             ro.logp_old, adv, ret, clip=w.clip, vf_coef=w.vf_coef,
                             ent_coef=w.ent_coef, **kw)
@@ -105,6 +111,15 @@ def test_normalised_advantages(prec):
     (g,), s6 = _gpu_grad(w, ro, p0, adv, ret, idx, adv_stats=st)
     _check(w, g, s6, _oracle(w, ro, p0, adv, ret, idx, adv_stats=st),
            1e-4 if prec == "fp32" else 2e-2)
+
+
+@pytest.mark.parametrize("wname", ["mario", "large"])
+def test_bf16_close_to_fp64_definition(wname):
+    w = synth.WORKLOADS[wname].scaled(T=16, N=256)
+    ro, p0, adv, ret = _inputs(w, seed=3)
+    idx = oracle.perm(2, 0, w.B)[:2048]
+    (g,), s6 = _gpu_grad(w, ro, p0, adv, ret, idx)
+    _check(w, g, s6, _oracle(w, ro, p0, adv, ret, idx, bf16_operands=False), 2e-2)
 
 
 def test_gradient_is_deterministic():

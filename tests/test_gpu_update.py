@@ -73,7 +73,8 @@ def _update(w, seed=0, host_api=False):
     ctx.close()
     net = oracle.Net(w.obs_dim, w.h1, w.h2, w.act, w.heads, w.n_gauss)
     hp = oracle.Hyper(gamma=w.gamma, lam=w.lam, clip=w.clip, vf_coef=w.vf_coef,
-                      ent_coef=w.ent_coef, lr=w.lr, max_grad_norm=w.max_grad_norm, seed=11)
+                      ent_coef=w.ent_coef, lr=w.lr, max_grad_norm=w.max_grad_norm, seed=11,
+                      bf16_operands=w.precision == "bf16")
     ref = oracle.update(net, hp, w.T, w.N, E, M, ro.obs, ro.act_disc, ro.act_cont, ro.logp_old,
                         ro.val, ro.rew, ro.done, ro.boot, p0)
     return p0, params, stats, step, ref

@@ -276,3 +276,48 @@ def test_policy_logp_matches_scipy_and_the_loss():
         assert abs(lp[r] - ref) < 1e-10
         lp2, ent2 = _logp_ent(net, params, obs, act, actc, r)
         assert abs(lp[r] - lp2) < 1e-12 and abs(ent[r] - ent2) < 1e-12
+
+
+# ---- bf16-operand mode -------------------------------------------------------
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(3)
+    xs = np.concatenate([rng.normal(size=2000) * 10.0 ** rng.integers(-30, 30, 2000),
+                         [0.0, -0.0, 1.0, 1.00390625, 1.01171875, 1.0078125, -2.5, 3e-39,
+                          1e-45, 3.3895313892515355e38]])
+    ref = torch.tensor(xs, dtype=torch.float64).float().bfloat16().double().numpy()
+    got = np.array([oracle.round_bf16(x) for x in xs])
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_bf16_mode_is_exact_on_representable_operands():
+    """ReLU net whose weights, observations, activations and value signal are
+    all bf16-exact dyadics: bf16-operand mode must equal the fp64 mode bit
+    for bit (no rounding of anything that was not rounded, no lost term)."""
+    net = oracle.Net(4, 4, 4, act=1, heads=(2,), n_gauss=0)
+    rng = np.random.default_rng(4)
+    params = rng.integers(-4, 5, net.num_params) / 8.0
+    obs = rng.integers(-3, 4, (4, 4)).astype(np.float32)
+    act = np.zeros((4, 1), np.int32)
+    z = oracle.forward(net, params, obs)
+    ret = z[:, -1] - rng.integers(-2, 3, 4) / 4.0          # V - R dyadic
+    kw = dict(clip=0.2, vf_coef=0.5, ent_coef=0.0)
+    args = (net, params, np.arange(4, dtype=np.int32), obs, act, None, np.zeros(4, np.float32),
+            np.zeros(4), ret)
+    l0, g0, s0, _ = oracle.loss_grad(*args, **kw)
+    l1, g1, s1, _ = oracle.loss_grad(*args, bf16_operands=True, **kw)
+    assert l0 == l1
+    np.testing.assert_array_equal(g0, g1)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_bf16_mode_is_close_to_fp64_on_tanh_nets(seed):
+    net = oracle.Net(16, 32, 32, act=0, heads=(9, 2, 2, 2))
+    params, obs, act, actc, logp_old, adv, ret = _setup(net, 64, seed, scale=0.2)
+    idx = np.arange(64, dtype=np.int32)
+    _, g0, s0, _ = oracle.loss_grad(net, params, idx, obs, act, actc, logp_old, adv, ret,
+                                    clip=10.0)
+    _, g1, s1, _ = oracle.loss_grad(net, params, idx, obs, act, actc, logp_old, adv, ret,
+                                    clip=10.0, bf16_operands=True)
+    assert np.linalg.norm(g1 - g0) / np.linalg.norm(g0) < 2e-2
+    assert np.linalg.norm(g1 - g0) > 0          # the mode does round something
