@@ -3,6 +3,7 @@
 // sec. 6 "The whole algorithm", steps 2 "judge" and 3 "learn") as a sequence
 // of kernel launches on the caller's stream, captured once into a CUDA graph.
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -163,7 +164,7 @@ ppo_status shape_from(const ppo_config* c, NetShape* s) {
 
 // K-split length (64-row k-tiles) of the weight-gradient units, chosen so
 // that the units of all three products have roughly equal cost and number
-// about twice the SM count.
+// about the SM count (one unit per CTA), with at least 8 k-tiles per unit.
 int wgrad_kt_per_split(const NetShape& s, int64_t mb, int num_sms) {
   const int64_t kt = (mb + 63) / 64;
   auto tiles = [](int M, int N) {
@@ -171,8 +172,8 @@ int wgrad_kt_per_split(const NetShape& s, int64_t mb, int num_sms) {
     return (double)(M / 128) * (N / bn) * (bn / 128.0);
   };
   const double cost = (tiles(s.H2, s.H1) + tiles(s.H1, s.Dp) + tiles(s.H2, 64)) * (double)kt;
-  int per = (int)(cost / (2.0 * num_sms));
-  if (per < 4) per = 4;
+  int per = (int)std::ceil(cost / (double)num_sms);
+  if (per < 8) per = 8;
   if ((kt + per - 1) / per > kMaxSplit) per = (int)((kt + kMaxSplit - 1) / kMaxSplit);
   return per;
 }
@@ -194,7 +195,8 @@ ppo_status check_minibatch_args(ppo_ctx* c, const float* obs, const int32_t* act
 ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* obs_packed,
                              const int32_t* act, const float* actc, const float* logp_old,
                              const float* adv, const float* ret, const int32_t* idx, int64_t B,
-                             int64_t mb, const float* adv_stats, float* stats6, cudaStream_t st) {
+                             int64_t mb, const float* adv_stats, float* stats6, cudaStream_t st,
+                             int* nsq_out = nullptr) {
   const NetShape& s = c->s;
   GatherArgs ga{};
   ga.obs_f32 = obs;
@@ -229,6 +231,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
   ra.inv_mb = inv_mb;
   ra.grad = c->grad;
   ra.stats6 = stats6;
+  ra.sq_part = nsq_out ? c->sq : nullptr;   // fused squared-norm partials for Adam
 
   if (c->bf16) {
     auto* X = static_cast<__nv_bfloat16*>(c->X);
@@ -330,10 +333,12 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
   }
   PPO_CUDA(launch_reduce(ra, st));
   c->tr.mark(ST_REDUCE, st);
+  if (nsq_out) *nsq_out = reduce_blocks(s.P);
   return PPO_OK;
 }
 
-ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t st) {
+ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t st,
+                        int nsq = 0) {
   AdamArgs a{};
   a.p = c->params;
   a.g = c->grad;
@@ -341,6 +346,7 @@ ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t
   a.v = c->v;
   a.P = c->s.P;
   a.sq_part = c->sq;
+  a.nsq = nsq;
   a.max_norm = c->cfg.max_grad_norm;
   a.lr = lr;
   a.b1 = c->cfg.beta1;
@@ -379,9 +385,10 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
     for (int k = 0; k < minibatches; ++k) {
       const int32_t* idx = c->perm + (int64_t)e * B + (int64_t)k * mb;
       float* st6 = stats ? stats + ((int64_t)e * minibatches + k) * 6 : nullptr;
+      int nsq = 0;
       TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
-                            c->advstats, st6, st));
-      TRY(enqueue_adam(c, lr, nullptr, st));
+                            c->advstats, st6, st, &nsq));
+      TRY(enqueue_adam(c, lr, nullptr, st, nsq));
     }
   return PPO_OK;
 }

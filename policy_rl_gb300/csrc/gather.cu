@@ -37,48 +37,48 @@ pack_kernel(const float* __restrict__ obs, int64_t B, int D, int Dp,
 }
 
 constexpr int kGatherThreads = 256;
-constexpr int kRowsPerBlock = kGatherThreads / kWarp;
 
+// One thread per 8-element chunk of a row (bf16 output) or per element (fp32
+// output); the thread holding chunk 0 of a row also copies the row's side data.
 __global__ void __launch_bounds__(kGatherThreads)
-gather_kernel(NetShape s, GatherArgs a) {
-  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-  const int64_t r = (int64_t)blockIdx.x * kRowsPerBlock + warp;
+gather_kernel(NetShape s, GatherArgs a, int per_row) {
+  const int64_t t = (int64_t)blockIdx.x * kGatherThreads + threadIdx.x;
+  const int64_t r = t / per_row;
+  const int c = (int)(t - r * per_row);
   if (r >= a.mb) return;
   int64_t src = a.idx[r];
   src = src < 0 ? 0 : (src >= a.B ? a.B - 1 : src);   // never read outside the batch
   if (a.obs_bf16) {
     const uint4* in = reinterpret_cast<const uint4*>(a.obs_bf16 + src * s.Dp);
-    uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.X) + r * s.Dp);
-    for (int j = lane; j < s.Dp / 8; j += kWarp) out[j] = __ldg(in + j);
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.X) + r * s.Dp)[c] = __ldg(in + c);
   } else if (a.x_bf16) {
     const float* in = a.obs_f32 + src * s.D;
-    uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.X) + r * s.Dp);
-    for (int j = lane; j < s.Dp / 2; j += kWarp) {
-      const int c = 2 * j;
-      const float x0 = c < s.D ? __ldg(in + c) : 0.f;
-      const float x1 = c + 1 < s.D ? __ldg(in + c + 1) : 0.f;
-      out[j] = pack_bf16x2(x0, x1);
-    }
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = (8 * c + j < s.D) ? __ldg(in + 8 * c + j) : 0.f;
+    uint4 o;
+    o.x = pack_bf16x2(f[0], f[1]);
+    o.y = pack_bf16x2(f[2], f[3]);
+    o.z = pack_bf16x2(f[4], f[5]);
+    o.w = pack_bf16x2(f[6], f[7]);
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.X) + r * s.Dp)[c] = o;
   } else {
-    const float* in = a.obs_f32 + src * s.D;
-    float* out = static_cast<float*>(a.X) + r * s.D;
-    for (int j = lane; j < s.D; j += kWarp) out[j] = __ldg(in + j);
+    static_cast<float*>(a.X)[r * s.D + c] = __ldg(a.obs_f32 + src * s.D + c);
   }
-  if (lane < s.NH) {
+  if (c != 0) return;
+  for (int h = 0; h < s.NH; ++h) {
     // an out-of-range action is clamped into its head so the loss never
     // indexes outside the head's logits
-    int32_t x = a.act[src * s.NH + lane];
-    const int n = s.head_n[lane];
-    a.act_mb[r * s.NH + lane] = x < 0 ? 0 : (x >= n ? n - 1 : x);
+    const int32_t x = a.act[src * s.NH + h];
+    const int n = s.head_n[h];
+    a.act_mb[r * s.NH + h] = x < 0 ? 0 : (x >= n ? n - 1 : x);
   }
-  if (lane < s.G) a.actc_mb[r * s.G + lane] = a.actc[src * s.G + lane];
-  if (lane == 0) {
-    a.logp_mb[r] = a.logp_old[src];
-    float A = a.adv[src];
-    if (a.adv_stats) A = (A - a.adv_stats[0]) / (a.adv_stats[1] + 1e-8f);
-    a.adv_mb[r] = A;
-    a.ret_mb[r] = a.ret[src];
-  }
+  for (int g = 0; g < s.G; ++g) a.actc_mb[r * s.G + g] = a.actc[src * s.G + g];
+  a.logp_mb[r] = a.logp_old[src];
+  float A = a.adv[src];
+  if (a.adv_stats) A = (A - a.adv_stats[0]) / (a.adv_stats[1] + 1e-8f);
+  a.adv_mb[r] = A;
+  a.ret_mb[r] = a.ret[src];
 }
 
 }  // namespace
@@ -94,8 +94,10 @@ cudaError_t launch_pack_obs(const float* obs, int64_t B, int D, int Dp, __nv_bfl
 }
 
 cudaError_t launch_gather(const NetShape& s, const GatherArgs& a, cudaStream_t st) {
-  const int64_t blocks = (a.mb + kRowsPerBlock - 1) / kRowsPerBlock;
-  gather_kernel<<<(int)blocks, kGatherThreads, 0, st>>>(s, a);
+  const int per_row = (a.obs_bf16 || a.x_bf16) ? s.Dp / 8 : s.D;
+  const int64_t threads = a.mb * per_row;
+  const int64_t blocks = (threads + kGatherThreads - 1) / kGatherThreads;
+  gather_kernel<<<(int)blocks, kGatherThreads, 0, st>>>(s, a, per_row);
   return cudaGetLastError();
 }
 

@@ -121,7 +121,7 @@ struct ReduceArgs {
   const float* ploss; int nl;           // [nl][kLossPartials]
   float inv_mb;
   float* grad;                          // [P]
-  double* sq_part;                      // [reduce_blocks]
+  double* sq_part;                      // nullable: per-block sum of squares of grad
   float* stats6;                        // nullable
 };
 int reduce_blocks(int64_t P);
@@ -137,8 +137,8 @@ struct AdamArgs {
   float* m;
   float* v;
   int64_t P;
-  const double* sq_part;
-  int nsq;
+  const double* sq_part;   // per-block sums of squares of g (written by the caller's
+  int nsq;                 // reduce when nsq > 0; computed by launch_adam when nsq == 0)
   float max_norm, lr, eps;
   double b1, b2;      // for the bias corrections 1 - beta^t
   float omb1, omb2;   // 1 - beta1, 1 - beta2 (rounded once from double)

@@ -21,35 +21,61 @@ constexpr int kAdamThreads = 256;
 
 __global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a) {
   const NetShape& s = a.s;
-  const int64_t stride = (int64_t)gridDim.x * kRedThreads;
-  for (int64_t i = (int64_t)blockIdx.x * kRedThreads + threadIdx.x; i < s.P; i += stride) {
+  const int P = (int)s.P;
+  const int stride = gridDim.x * kRedThreads;
+  double sq = 0.0;
+  for (int i = blockIdx.x * kRedThreads + threadIdx.x; i < P; i += stride) {
     float v = 0.f;
     if (i < s.ob1) {
-      const int64_t r = i - s.oW1;
-      const int64_t j = r / s.D, k = r % s.D;
-      for (int sp = 0; sp < a.s1; ++sp) v += a.pW1[((int64_t)sp * s.H1 + j) * a.ld1 + k];
+      const int r = i - (int)s.oW1;
+      const int j = r / s.D, k = r - j * s.D;
+      const float* q = a.pW1 + (int64_t)j * a.ld1 + k;
+      const int64_t st = (int64_t)s.H1 * a.ld1;
+#pragma unroll 8
+      for (int sp = 0; sp < a.s1; ++sp) v += q[sp * st];
     } else if (i < s.oW2) {
-      const int64_t j = i - s.ob1;
+      const int j = i - (int)s.ob1;
+#pragma unroll 8
       for (int b = 0; b < a.nb1; ++b) v += a.pb1[(int64_t)b * s.H1 + j];
     } else if (i < s.ob2) {
-      const int64_t r = i - s.oW2;
-      const int64_t j = r / s.H1, k = r % s.H1;
-      for (int sp = 0; sp < a.s2; ++sp) v += a.pW2[((int64_t)sp * s.H2 + j) * s.H1 + k];
+      const int r = i - (int)s.oW2;
+      const float* q = a.pW2 + r;
+      const int64_t st = (int64_t)s.H2 * s.H1;
+#pragma unroll 8
+      for (int sp = 0; sp < a.s2; ++sp) v += q[sp * st];
     } else if (i < s.oW3) {
-      const int64_t j = i - s.ob2;
+      const int j = i - (int)s.ob2;
+#pragma unroll 8
       for (int b = 0; b < a.nb2; ++b) v += a.pb2[(int64_t)b * s.H2 + j];
     } else if (i < s.ob3) {
-      const int64_t r = i - s.oW3;
-      const int64_t c = r / s.H2, j = r % s.H2;
-      for (int sp = 0; sp < a.s3; ++sp) v += a.pW3t[((int64_t)sp * s.H2 + j) * a.ld3 + c];
+      const int r = i - (int)s.oW3;
+      const int c = r / s.H2, j = r - c * s.H2;
+      const float* q = a.pW3t + (int64_t)j * a.ld3 + c;
+      const int64_t st = (int64_t)s.H2 * a.ld3;
+#pragma unroll 8
+      for (int sp = 0; sp < a.s3; ++sp) v += q[sp * st];
     } else if (i < s.ologstd) {
-      const int64_t c = i - s.ob3;
+      const int c = i - (int)s.ob3;
+#pragma unroll 8
       for (int b = 0; b < a.nb3; ++b) v += a.pb3[(int64_t)b * a.ldb3 + c];
     } else {
-      const int64_t gi = i - s.ologstd;
+      const int gi = i - (int)s.ologstd;
       for (int b = 0; b < a.nl; ++b) v += a.ploss[(int64_t)b * kLossPartials + 6 + gi];
     }
     a.grad[i] = v;
+    sq += (double)v * (double)v;
+  }
+  if (a.sq_part != nullptr) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    __shared__ double ws[kRedThreads / kWarp];
+    if (threadIdx.x % kWarp == 0) ws[threadIdx.x / kWarp] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double t = 0.0;
+      for (int w = 0; w < kRedThreads / kWarp; ++w) t += ws[w];
+      a.sq_part[blockIdx.x] = t;
+    }
   }
   if (blockIdx.x == 0 && a.stats6 != nullptr && threadIdx.x < 6) {
     float v = 0.f;
@@ -78,28 +104,28 @@ sqnorm_kernel(const float* __restrict__ g, int64_t P, double* __restrict__ part)
   }
 }
 
-__device__ __forceinline__ void write_shadow(const NetShape& s, const Shadows& sh, int64_t i,
+__device__ __forceinline__ void write_shadow(const NetShape& s, const Shadows& sh, int i,
                                              float p) {
   const __nv_bfloat16 b = __float2bfloat16_rn(p);
-  if (i < s.ob1) {
-    const int64_t r = i - s.oW1;
-    const int64_t j = r / s.D, k = r % s.D;
+  if (i < (int)s.ob1) {
+    const int r = i - (int)s.oW1;
+    const int j = r / s.D, k = r - j * s.D;
     sh.W1s[j * s.Dp + k] = b;
-  } else if (i >= s.oW2 && i < s.ob2) {
-    const int64_t r = i - s.oW2;
-    const int64_t j = r / s.H1, k = r % s.H1;
-    sh.W2s[j * s.H1 + k] = b;
+  } else if (i >= (int)s.oW2 && i < (int)s.ob2) {
+    const int r = i - (int)s.oW2;
+    const int j = r / s.H1, k = r - j * s.H1;
+    sh.W2s[r] = b;
     sh.W2Ts[k * s.H2 + j] = b;
-  } else if (i >= s.oW3 && i < s.ob3) {
-    const int64_t r = i - s.oW3;
-    const int64_t c = r / s.H2, j = r % s.H2;
-    sh.W3s[c * s.H2 + j] = b;
+  } else if (i >= (int)s.oW3 && i < (int)s.ob3) {
+    const int r = i - (int)s.oW3;
+    const int c = r / s.H2, j = r - c * s.H2;
+    sh.W3s[r] = b;
     sh.W3Ts[j * sh.ld3t + c] = b;
   }
 }
 
 __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
-  __shared__ float s_coef, s_norm;
+  __shared__ float s_coef, s_norm, s_ibc1, s_ibc2;
   __shared__ long long s_t;
   if (threadIdx.x == 0) {
     double ss = 0.0;
@@ -110,26 +136,26 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
       const double c = (double)a.max_norm / (norm + 1e-6);
       coef = c < 1.0 ? c : 1.0;
     }
+    const long long t = (long long)(*a.step) + 1;
     s_coef = (float)coef;
     s_norm = (float)norm;
-    s_t = (long long)(*a.step) + 1;
+    s_t = t;
+    // bias corrections 1 - beta^t, in double, once per block
+    s_ibc1 = (float)(1.0 / (1.0 - pow(a.b1, (double)t)));
+    s_ibc2 = (float)(1.0 / (1.0 - pow(a.b2, (double)t)));
   }
   __syncthreads();
-  const float coef = s_coef;
-  const double t = (double)s_t;
-  const float bc1 = (float)(1.0 - pow(a.b1, t));
-  const float bc2 = (float)(1.0 - pow(a.b2, t));
+  const float coef = s_coef, ibc1 = s_ibc1, ibc2 = s_ibc2;
   const float b1 = (float)a.b1, b2 = (float)a.b2, omb1 = a.omb1, omb2 = a.omb2;
   const float lr = a.lr, eps = a.eps;
   const bool shadows = a.sh.W1s != nullptr;
-  const int64_t stride = (int64_t)gridDim.x * kAdamThreads;
-  for (int64_t i = (int64_t)blockIdx.x * kAdamThreads + threadIdx.x; i < a.P; i += stride) {
+  const int P = (int)a.P;
+  const int stride = gridDim.x * kAdamThreads;
+  for (int i = blockIdx.x * kAdamThreads + threadIdx.x; i < P; i += stride) {
     const float g = a.g[i] * coef;
     const float m = b1 * a.m[i] + omb1 * g;
     const float v = b2 * a.v[i] + omb2 * g * g;
-    const float mhat = m / bc1;
-    const float vhat = v / bc2;
-    const float p = a.p[i] - lr * mhat / (sqrtf(vhat) + eps);
+    const float p = a.p[i] - lr * (m * ibc1) / (sqrtf(v * ibc2) + eps);
     a.m[i] = m;
     a.v[i] = v;
     a.p[i] = p;
@@ -154,7 +180,7 @@ __global__ void __launch_bounds__(kAdamThreads)
 shadow_kernel(const float* __restrict__ p, NetShape s, Shadows sh) {
   const int64_t stride = (int64_t)gridDim.x * kAdamThreads;
   for (int64_t i = (int64_t)blockIdx.x * kAdamThreads + threadIdx.x; i < s.P; i += stride)
-    write_shadow(s, sh, i, p[i]);
+    write_shadow(s, sh, (int)i, p[i]);
 }
 
 int blocks_for(int64_t n, int threads, int cap) {
@@ -175,9 +201,11 @@ cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
 
 cudaError_t launch_adam(const AdamArgs& a0, cudaStream_t st, const Trace* tr) {
   AdamArgs a = a0;
-  sqnorm_kernel<<<kNormBlocks, kNormThreads, 0, st>>>(a.g, a.P, const_cast<double*>(a.sq_part));
-  if (tr) tr->mark(ST_SQNORM, st);
-  a.nsq = kNormBlocks;
+  if (a.nsq <= 0) {   // no squared-norm partials supplied: compute them
+    sqnorm_kernel<<<kNormBlocks, kNormThreads, 0, st>>>(a.g, a.P, const_cast<double*>(a.sq_part));
+    if (tr) tr->mark(ST_SQNORM, st);
+    a.nsq = kNormBlocks;
+  }
   adam_kernel<<<blocks_for(a.P, kAdamThreads, 152 * 4), kAdamThreads, 0, st>>>(a);
   if (tr) tr->mark(ST_ADAM, st);
   return cudaGetLastError();

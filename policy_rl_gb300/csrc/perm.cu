@@ -7,8 +7,9 @@
 // of seed + (k+1)*0x6D2B79F5 and every thread computes its own key.
 // The permutation is the index order sorted by (key, index), produced by a
 // stable least-significant-digit radix sort: 4 passes of 8 bits, each pass a
-// per-tile histogram, one digit-major exclusive scan, and a stable scatter in
-// which every warp ranks equal digits with __match_any_sync.
+// per-tile histogram, a per-digit exclusive scan over the tiles (one block per
+// digit), and a stable scatter in which every warp ranks equal digits with
+// __match_any_sync.
 #include "common.cuh"
 
 namespace ppo {
@@ -21,7 +22,6 @@ constexpr int kPerLane = 16;                         // elements per lane
 constexpr int kWarpSpan = kWarp * kPerLane;          // 512 elements per warp
 constexpr int kTile = kSortWarps * kWarpSpan;        // 4096 elements per block
 constexpr int kRadix = 256;
-constexpr int kScanThreads = 1024;
 
 __device__ __forceinline__ uint32_t mulberry32_draw(uint32_t seed, uint64_t k) {
   uint32_t t = seed + (uint32_t)(k + 1) * 0x6D2B79F5u;
@@ -56,9 +56,7 @@ hist_kernel(SortIn in, int64_t B, int shift, uint32_t* __restrict__ ghist, int n
   for (int j = 0; j < kTile / kSortThreads; ++j) {
     const int64_t i = base + j * kSortThreads + threadIdx.x;
     if (i < B) {
-      uint32_t k;
-      int32_t v;
-      load_kv(in, i, k, v);
+      const uint32_t k = in.keys ? in.keys[i] : mulberry32_draw(in.seed, in.draw0 + (uint64_t)i);
       atomicAdd(&h[(k >> shift) & 0xFF], 1u);
     }
   }
@@ -66,36 +64,78 @@ hist_kernel(SortIn in, int64_t B, int shift, uint32_t* __restrict__ ghist, int n
   ghist[(int64_t)threadIdx.x * num_tiles + blockIdx.x] = h[threadIdx.x];
 }
 
-// Exclusive scan of n counts in place (one block, fixed order).
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(uint32_t* __restrict__ a, int64_t n) {
-  __shared__ uint32_t part[kScanThreads];
-  const int64_t per = (n + kScanThreads - 1) / kScanThreads;
-  const int64_t lo = threadIdx.x * per;
-  const int64_t hi = lo + per < n ? lo + per : n;
-  uint32_t s = 0;
-  for (int64_t i = lo; i < hi; ++i) s += a[i];
-  part[threadIdx.x] = s;
+// Exclusive scan over 256 threads (fixed order); returns the exclusive prefix
+// of x and writes the block total to *total.
+__device__ __forceinline__ uint32_t block_excl_scan256(uint32_t x, uint32_t* wsum,
+                                                       uint32_t* total) {
+  const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+  uint32_t incl = x;
+#pragma unroll
+  for (int o = 1; o < kWarp; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == kWarp - 1) wsum[warp] = incl;
   __syncthreads();
-  // Hillis-Steele inclusive scan of the 1024 partial sums
-  for (int o = 1; o < kScanThreads; o <<= 1) {
-    uint32_t add = threadIdx.x >= o ? part[threadIdx.x - o] : 0u;
-    __syncthreads();
-    part[threadIdx.x] += add;
-    __syncthreads();
+  if (warp == 0) {
+    uint32_t v = lane < kSortWarps ? wsum[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < kSortWarps; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane < kSortWarps) wsum[lane] = v;
   }
-  uint32_t run = threadIdx.x > 0 ? part[threadIdx.x - 1] : 0u;
-  for (int64_t i = lo; i < hi; ++i) {
-    const uint32_t c = a[i];
-    a[i] = run;
-    run += c;
+  __syncthreads();
+  const uint32_t excl = incl - x + (warp > 0 ? wsum[warp - 1] : 0u);
+  *total = wsum[kSortWarps - 1];
+  __syncthreads();
+  return excl;
+}
+
+// One block per digit: exclusive scan of that digit's per-tile counts (in
+// place) and the digit's total count.
+constexpr int kScanPer = 8;
+__global__ void __launch_bounds__(kSortThreads)
+digit_scan_kernel(uint32_t* __restrict__ ghist, int num_tiles, uint32_t* __restrict__ dtotal) {
+  __shared__ uint32_t wsum[kSortWarps];
+  uint32_t* row = ghist + (int64_t)blockIdx.x * num_tiles;
+  uint32_t carry = 0;
+  for (int base = 0; base < num_tiles; base += kSortThreads * kScanPer) {
+    const int i0 = base + threadIdx.x * kScanPer;
+    uint32_t c[kScanPer];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < kScanPer; ++j) {
+      c[j] = (i0 + j < num_tiles) ? row[i0 + j] : 0u;
+      sum += c[j];
+    }
+    uint32_t chunk_total;
+    uint32_t run = carry + block_excl_scan256(sum, wsum, &chunk_total);
+#pragma unroll
+    for (int j = 0; j < kScanPer; ++j)
+      if (i0 + j < num_tiles) {
+        row[i0 + j] = run;
+        run += c[j];
+      }
+    carry += chunk_total;
   }
+  if (threadIdx.x == 0) dtotal[blockIdx.x] = carry;
 }
 
 __global__ void __launch_bounds__(kSortThreads)
 scatter_kernel(SortIn in, int64_t B, int shift, const uint32_t* __restrict__ gscan, int num_tiles,
-               uint32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out) {
+               const uint32_t* __restrict__ dtotal, uint32_t* __restrict__ keys_out,
+               int32_t* __restrict__ vals_out) {
   __shared__ uint32_t wofs[kSortWarps][kRadix];
+  __shared__ uint32_t dbase[kRadix];
+  __shared__ uint32_t wsum[kSortWarps];
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  {
+    // first output position of each digit: exclusive scan of the digit totals
+    uint32_t tot;
+    dbase[threadIdx.x] = block_excl_scan256(dtotal[threadIdx.x], wsum, &tot);
+  }
   for (int d = threadIdx.x; d < kSortWarps * kRadix; d += kSortThreads)
     (&wofs[0][0])[d] = 0;
   __syncthreads();
@@ -126,7 +166,7 @@ scatter_kernel(SortIn in, int64_t B, int shift, const uint32_t* __restrict__ gsc
   // warp w's first position for digit d: global tile offset + counts of warps < w
   {
     const int d = threadIdx.x;   // kSortThreads == kRadix
-    uint32_t run = gscan[(int64_t)d * num_tiles + blockIdx.x];
+    uint32_t run = dbase[d] + gscan[(int64_t)d * num_tiles + blockIdx.x];
     for (int w = 0; w < kSortWarps; ++w) {
       const uint32_t c = wofs[w][d];
       wofs[w][d] = run;
@@ -156,7 +196,7 @@ size_t perm_workspace_bytes(int64_t B, int /*epochs*/) {
   const int64_t tiles = (B + kTile - 1) / kTile;
   const size_t kv = (size_t)B * 4;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return 4 * al(kv) + al((size_t)tiles * kRadix * 4);
+  return 4 * al(kv) + al((size_t)tiles * kRadix * 4) + al(kRadix * 4);
 }
 
 cudaError_t launch_perm(uint32_t seed, int64_t epoch0, int epochs, int64_t B, int32_t* perm,
@@ -174,6 +214,8 @@ cudaError_t launch_perm(uint32_t seed, int64_t epoch0, int epochs, int64_t B, in
   int32_t* vb = reinterpret_cast<int32_t*>(w);
   w += al((size_t)B * 4);
   uint32_t* ghist = reinterpret_cast<uint32_t*>(w);
+  w += al((size_t)tiles * kRadix * 4);
+  uint32_t* dtotal = reinterpret_cast<uint32_t*>(w);
 
   for (int e = 0; e < epochs; ++e) {
     const uint64_t draw0 = (uint64_t)(epoch0 + e) * (uint64_t)B;
@@ -195,9 +237,9 @@ cudaError_t launch_perm(uint32_t seed, int64_t epoch0, int epochs, int64_t B, in
       }
       hist_kernel<<<tiles, kSortThreads, 0, st>>>(in, B, shift, ghist, tiles);
       if (tr) tr->mark(ST_PERM_HIST, st);
-      scan_kernel<<<1, kScanThreads, 0, st>>>(ghist, (int64_t)tiles * kRadix);
+      digit_scan_kernel<<<kRadix, kSortThreads, 0, st>>>(ghist, tiles, dtotal);
       if (tr) tr->mark(ST_PERM_SCAN, st);
-      scatter_kernel<<<tiles, kSortThreads, 0, st>>>(in, B, shift, ghist, tiles, ko, vo);
+      scatter_kernel<<<tiles, kSortThreads, 0, st>>>(in, B, shift, ghist, tiles, dtotal, ko, vo);
       if (tr) tr->mark(ST_PERM_SCATTER, st);
       in = SortIn{ko, vo, seed, draw0};
     }
