@@ -162,13 +162,25 @@ def run_ours(args, world, rank, local):
     w = synth.WORKLOADS[args.workload]
     B, E, M = w.B, w.epochs, w.minibatches
     mb = B // M
-    ro = synth.rollout(w, seed=rank)
+    # observations of the large workloads (> 2e8 values) are drawn on the device
+    # (torch's seeded N(0,1) / uniform tile ids); everything else comes from
+    # the host-side seeded generator
+    big = w.B * w.obs_dim > 2e8
+    ro = synth.rollout(w, seed=rank, with_obs=not big)
     p0 = synth.init_params(w)
     ctx = P.Context(P.config_from_workload(w), p0)
     stream = torch.cuda.Stream()
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
-    args_dev = [dev(x) for x in (ro.obs, ro.act_disc, ro.act_cont, ro.logp_old, ro.val, ro.rew,
-                                 ro.done, ro.boot)]
+    if big:
+        g = torch.Generator(device="cuda")
+        g.manual_seed(rank)
+        obs_d = torch.randn(B, w.obs_dim, device="cuda", generator=g)
+        if w.obs_kind == "ddnet":
+            obs_d[:, :1333] = torch.randint(0, 6, (B, 1333), device="cuda", generator=g).float()
+    else:
+        obs_d = dev(ro.obs)
+    args_dev = [obs_d] + [dev(x) for x in (ro.act_disc, ro.act_cont, ro.logp_old, ro.val,
+                                           ro.rew, ro.done, ro.boot)]
     stats = torch.zeros(E * M, 6, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     hp = (E, M, w.gamma, w.lam, w.lr, 1234)
@@ -231,8 +243,9 @@ def run_ours(args, world, rank, local):
 
     # end to end: host (pinned) buffers through the C ABI, copies inside the timed region
     pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
-    host_args = [pin(x) for x in (ro.obs, ro.act_disc, ro.act_cont, ro.logp_old, ro.val, ro.rew,
-                                  ro.done, ro.boot)]
+    host_obs = obs_d.cpu().pin_memory() if big else pin(ro.obs)
+    host_args = [host_obs] + [pin(x) for x in (ro.act_disc, ro.act_cont, ro.logp_old, ro.val,
+                                               ro.rew, ro.done, ro.boot)]
     host_stats = torch.zeros(E * M, 6).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_args)
     d2h = host_stats.numel() * 4
@@ -251,6 +264,10 @@ def run_ours(args, world, rank, local):
     gae = None
     if rank == 0 and not args.skip_gae_stress:
         gae = _gae_stress(stream, hbm_peak)
+
+    adam = None
+    if rank == 0 and not args.skip_adam_stress:
+        adam = _adam_stress(stream, hbm_peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -277,6 +294,7 @@ def run_ours(args, world, rank, local):
         "stages": stages,
         "profiled_update_ms": round(total_ms, 4),
         "gae_stress": gae,
+        "adam_stress": adam,
         "cpu_baseline": cpu,
         "clocks": clk,
     }
@@ -317,6 +335,34 @@ def _gae_stress(stream, hbm_peak):
             res[name] = {"ms": round(t * 1e3, 4), "GB_per_s": round(gbs, 1),
                          "frac_of_hbm": round(gbs / hbm_peak, 4), "bytes_per_elem": bpe}
     return {"workload": "gae_stress: T=1024 N=65536 fp32 (inputs > L2)", **res}
+
+
+def _adam_stress(stream, hbm_peak):
+    """Gradient-norm pass + Adam over 64M fp32 parameters (state 1 GB, far
+    larger than L2): 4 B (norm) + 16 B read + 12 B written per parameter."""
+    import torch
+    import policy_rl_gb300 as P
+    cfg = P.make_config(65536, 1024, 64, heads=(2,), precision=0, max_batch=1,
+                        max_minibatch=1, max_epochs=1)
+    ctx = P.Context(cfg)
+    n = ctx.n_params
+    with torch.cuda.stream(stream):
+        ctx.grad.normal_()
+        for _ in range(3):
+            ctx.adam_step(1e-4, stream=stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(10)]
+        for s0, e0 in evs:
+            s0.record(stream)
+            ctx.adam_step(1e-4, stream=stream)
+            e0.record(stream)
+        stream.synchronize()
+    t = float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
+    ctx.close()
+    gbs = 32 * n / t / 1e9
+    return {"params": n, "ms": round(t * 1e3, 4), "GB_per_s": round(gbs, 1),
+            "frac_of_hbm": round(gbs / hbm_peak, 4), "bytes_per_param": 32,
+            "note": "ppo_adam_step: squared-norm pass + fused clip/Adam pass, fp32 mode"}
 
 
 def _cpu_sample(w):
@@ -392,6 +438,7 @@ def main():
                     choices=["tiny", "mario", "ddnet", "large"])
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     ap.add_argument("--skip-gae-stress", action="store_true")
+    ap.add_argument("--skip-adam-stress", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = _dist()

@@ -333,7 +333,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
   }
   PPO_CUDA(launch_reduce(ra, st));
   c->tr.mark(ST_REDUCE, st);
-  if (nsq_out) *nsq_out = reduce_blocks(s.P);
+  if (nsq_out) *nsq_out = reduce_blocks(s);
   return PPO_OK;
 }
 
@@ -466,7 +466,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->step, 1);
   A(c->done_ctr, 1);
   A(c->err, 1);
-  A(c->sq, 1024);
+  A(c->sq, std::max(1024, reduce_blocks(s)));
   if (c->bf16) {
     c->sh.ld3t = 64;
     A(c->sh.W1s, (int64_t)s.H1 * s.Dp);
@@ -499,9 +499,12 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->adv_mb, mbm);
   A(c->ret_mb, mbm);
   const int ldW1 = c->bf16 ? s.Dp : s.D;
-  A(c->pW1, (int64_t)kMaxSplit * s.H1 * ldW1);
-  A(c->pW2, (int64_t)kMaxSplit * s.H2 * s.H1);
-  A(c->pW3, (int64_t)kMaxSplit * s.H2 * (c->bf16 ? 64 : s.CP));
+  // split-K partials: a split covers at least 16 rows (fp32) / 8 k-tiles (bf16)
+  const int64_t max_split = std::min<int64_t>(kMaxSplit, c->bf16 ? (mbm + 511) / 512 + 1
+                                                                   : (mbm + 15) / 16 + 1);
+  A(c->pW1, max_split * s.H1 * ldW1);
+  A(c->pW2, max_split * s.H2 * s.H1);
+  A(c->pW3, max_split * s.H2 * (c->bf16 ? 64 : s.CP));
   const int64_t part_rows = std::max<int64_t>(c->num_sms, (mbm + 63) / 64) + 1;
   A(c->cs1, part_rows * s.H1);
   A(c->cs2, part_rows * s.H2);

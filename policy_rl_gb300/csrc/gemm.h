@@ -124,7 +124,7 @@ struct ReduceArgs {
   double* sq_part;                      // nullable: per-block sum of squares of grad
   float* stats6;                        // nullable
 };
-int reduce_blocks(int64_t P);
+int reduce_blocks(const NetShape& s);
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st);
 
 struct Shadows {

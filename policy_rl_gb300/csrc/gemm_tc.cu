@@ -51,7 +51,7 @@ struct Cfg {
   static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   static constexpr int CTRL = 512;
   static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + CTRL + 4 * kColsumCap * 4 +
-                                 4 * kLossPartials * 4;
+                                 4 * kLossPartials * 4 + kColsumCap * 4;
 };
 
 struct Guard {
@@ -124,6 +124,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);  // issued, consumed
   float* cs = reinterpret_cast<float*>(ctrl + C::CTRL);                      // [4][kColsumCap]
   float* lp = cs + 4 * kColsumCap;                                           // [4][kLossPartials]
+  float* bias_s = lp + 4 * kLossPartials;                                    // [kColsumCap]
 
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   auto sA = [&](int s) { return base + (uint32_t)(s * C::STAGE); };
@@ -146,6 +147,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
   if (EPI != EPI_BIAS_ACT)
     for (int i = threadIdx.x; i < 4 * kColsumCap + 4 * kLossPartials; i += kThreads) cs[i] = 0.f;
+  if (EPI != EPI_DACT)   // the bias, read by every epilogue thread, staged once
+    for (int i = threadIdx.x; i < p.N; i += kThreads) bias_s[i] = p.bias[i];
   if (warp == 1) tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
@@ -237,7 +240,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         float z[32], dz[32], t6[6], dls[4];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          z[j] = (j < p.shape.C) ? v[j] + p.bias[j] : 0.f;
+          z[j] = (j < p.shape.C) ? v[j] + bias_s[j] : 0.f;
           dz[j] = 0.f;
         }
 #pragma unroll
@@ -273,28 +276,50 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (lane == 0) lp[q * kLossPartials + 6 + k] += s4;
         }
       } else {
-#pragma unroll 1
+        // software pipeline over 32-column chunks: the TMEM load (and the
+        // activation operand) of chunk c+1 are in flight while chunk c is
+        // processed and stored
+        // two register buffers, alternated by chunk parity (the loop is fully
+        // unrolled, so the index is a compile-time constant): the registers of
+        // an asynchronous TMEM load are read only after their own wait
+        uint32_t r[2][32];
+        uint4 ax[2][4];
+        const __nv_bfloat16* auxrow = p.aux + (int64_t)row * p.ldaux + tn * BN;
+        tmem_ld32_async(taddr, r[0]);
+        if constexpr (EPI == EPI_DACT) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            ax[0][i] = rok ? __ldg(reinterpret_cast<const uint4*>(auxrow) + i)
+                           : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
         for (int c0 = 0; c0 < BN; c0 += 32) {
+          const int cur = (c0 / 32) & 1, nxt = cur ^ 1;
+          tmem_wait_ld(r[cur]);
+          if (c0 + 32 < BN) {
+            tmem_ld32_async(taddr + (uint32_t)(c0 + 32), r[nxt]);
+            if constexpr (EPI == EPI_DACT) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                ax[nxt][i] = rok ? __ldg(reinterpret_cast<const uint4*>(auxrow + c0 + 32) + i)
+                                 : make_uint4(0, 0, 0, 0);
+            }
+          }
           float v[32];
-          tmem_ld32(taddr + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[cur][j]);
           const int col0 = tn * BN + c0;
           if constexpr (EPI == EPI_BIAS_ACT) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              const float x = v[j] + __ldg(p.bias + col0 + j);
+              const float x = v[j] + bias_s[col0 + j];
               v[j] = p.act == 0 ? tanh_fast(x) : fmaxf(x, 0.f);
             }
             if (rok) store_bf16x32(p.out + (int64_t)row * p.ldo + col0, v);
           } else {  // EPI_DACT
-            uint4 au[4] = {};
-            if (rok) {
-              const uint4* ap = reinterpret_cast<const uint4*>(p.aux + (int64_t)row * p.ldaux + col0);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) au[i] = __ldg(ap + i);
-            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint32_t w4[4] = {au[i].x, au[i].y, au[i].z, au[i].w};
+              const uint32_t w4[4] = {ax[cur][i].x, ax[cur][i].y, ax[cur][i].z, ax[cur][i].w};
 #pragma unroll
               for (int h = 0; h < 4; ++h) {
                 const float2 hv = unpack_bf16x2(w4[h]);

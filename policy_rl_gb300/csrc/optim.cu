@@ -19,68 +19,99 @@ constexpr int kNormThreads = 256;
 constexpr int kNormBlocks = 128;
 constexpr int kAdamThreads = 256;
 
-__global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a) {
+// Weight elements: one thread each, summing the split-K partials in split
+// order.  Bias / log-std elements and the six loss statistics: one warp each,
+// lanes striding over the per-CTA partial rows, then a fixed xor-shuffle tree.
+// Every block also writes the sum of squares of the gradient entries it
+// produced (fixed order), for the clip norm.
+constexpr int kRedWarps = kRedThreads / kWarp;
+
+__device__ __forceinline__ float warp_rows_sum(const float* base, int rows, int64_t stride) {
+  const int lane = threadIdx.x % kWarp;
+  float v = 0.f;
+  for (int b = lane; b < rows; b += kWarp) v += base[(int64_t)b * stride];
+  return warp_sum(v);
+}
+
+__global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int weight_blocks) {
   const NetShape& s = a.s;
-  const int P = (int)s.P;
-  const int stride = gridDim.x * kRedThreads;
+  const int nW1 = s.H1 * s.D, nW2 = s.H2 * s.H1, nW3 = s.C * s.H2;
   double sq = 0.0;
-  for (int i = blockIdx.x * kRedThreads + threadIdx.x; i < P; i += stride) {
+  if ((int)blockIdx.x < weight_blocks) {
+    const int e = blockIdx.x * kRedThreads + threadIdx.x;
     float v = 0.f;
-    if (i < s.ob1) {
-      const int r = i - (int)s.oW1;
-      const int j = r / s.D, k = r - j * s.D;
+    int i = -1;
+    if (e < nW1) {
+      i = (int)s.oW1 + e;
+      const int j = e / s.D, k = e - j * s.D;
       const float* q = a.pW1 + (int64_t)j * a.ld1 + k;
       const int64_t st = (int64_t)s.H1 * a.ld1;
 #pragma unroll 8
       for (int sp = 0; sp < a.s1; ++sp) v += q[sp * st];
-    } else if (i < s.oW2) {
-      const int j = i - (int)s.ob1;
-#pragma unroll 8
-      for (int b = 0; b < a.nb1; ++b) v += a.pb1[(int64_t)b * s.H1 + j];
-    } else if (i < s.ob2) {
-      const int r = i - (int)s.oW2;
+    } else if (e < nW1 + nW2) {
+      const int r = e - nW1;
+      i = (int)s.oW2 + r;
       const float* q = a.pW2 + r;
       const int64_t st = (int64_t)s.H2 * s.H1;
 #pragma unroll 8
       for (int sp = 0; sp < a.s2; ++sp) v += q[sp * st];
-    } else if (i < s.oW3) {
-      const int j = i - (int)s.ob2;
-#pragma unroll 8
-      for (int b = 0; b < a.nb2; ++b) v += a.pb2[(int64_t)b * s.H2 + j];
-    } else if (i < s.ob3) {
-      const int r = i - (int)s.oW3;
+    } else if (e < nW1 + nW2 + nW3) {
+      const int r = e - nW1 - nW2;
+      i = (int)s.oW3 + r;
       const int c = r / s.H2, j = r - c * s.H2;
       const float* q = a.pW3t + (int64_t)j * a.ld3 + c;
       const int64_t st = (int64_t)s.H2 * a.ld3;
 #pragma unroll 8
       for (int sp = 0; sp < a.s3; ++sp) v += q[sp * st];
-    } else if (i < s.ologstd) {
-      const int c = i - (int)s.ob3;
-#pragma unroll 8
-      for (int b = 0; b < a.nb3; ++b) v += a.pb3[(int64_t)b * a.ldb3 + c];
-    } else {
-      const int gi = i - (int)s.ologstd;
-      for (int b = 0; b < a.nl; ++b) v += a.ploss[(int64_t)b * kLossPartials + 6 + gi];
     }
-    a.grad[i] = v;
-    sq += (double)v * (double)v;
+    if (i >= 0) {
+      a.grad[i] = v;
+      sq = (double)v * (double)v;
+    }
+  } else {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int e = ((int)blockIdx.x - weight_blocks) * kRedWarps + warp;
+    const int nb = s.H1 + s.H2 + s.C + s.G;
+    if (e < nb) {
+      float v;
+      int i;
+      if (e < s.H1) {
+        i = (int)s.ob1 + e;
+        v = warp_rows_sum(a.pb1 + e, a.nb1, s.H1);
+      } else if (e < s.H1 + s.H2) {
+        const int j = e - s.H1;
+        i = (int)s.ob2 + j;
+        v = warp_rows_sum(a.pb2 + j, a.nb2, s.H2);
+      } else if (e < s.H1 + s.H2 + s.C) {
+        const int c = e - s.H1 - s.H2;
+        i = (int)s.ob3 + c;
+        v = warp_rows_sum(a.pb3 + c, a.nb3, a.ldb3);
+      } else {
+        const int g = e - s.H1 - s.H2 - s.C;
+        i = (int)s.ologstd + g;
+        v = warp_rows_sum(a.ploss + 6 + g, a.nl, kLossPartials);
+      }
+      if (lane == 0) {
+        a.grad[i] = v;
+        sq = (double)v * (double)v;
+      }
+    } else if (e < nb + 6) {
+      const int q = e - nb;
+      const float v = warp_rows_sum(a.ploss + q, a.nl, kLossPartials);
+      if (lane == 0 && a.stats6 != nullptr) a.stats6[q] = v * a.inv_mb;
+    }
   }
   if (a.sq_part != nullptr) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    __shared__ double ws[kRedThreads / kWarp];
+    __shared__ double ws[kRedWarps];
     if (threadIdx.x % kWarp == 0) ws[threadIdx.x / kWarp] = sq;
     __syncthreads();
     if (threadIdx.x == 0) {
       double t = 0.0;
-      for (int w = 0; w < kRedThreads / kWarp; ++w) t += ws[w];
+      for (int w = 0; w < kRedWarps; ++w) t += ws[w];
       a.sq_part[blockIdx.x] = t;
     }
-  }
-  if (blockIdx.x == 0 && a.stats6 != nullptr && threadIdx.x < 6) {
-    float v = 0.f;
-    for (int b = 0; b < a.nl; ++b) v += a.ploss[(int64_t)b * kLossPartials + threadIdx.x];
-    a.stats6[threadIdx.x] = v * a.inv_mb;
   }
 }
 
@@ -127,9 +158,19 @@ __device__ __forceinline__ void write_shadow(const NetShape& s, const Shadows& s
 __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
   __shared__ float s_coef, s_norm, s_ibc1, s_ibc2;
   __shared__ long long s_t;
+  __shared__ double s_ws[kAdamThreads / kWarp];
+  {
+    // every block sums the norm partials in the same fixed order
+    double ss = 0.0;
+    for (int b = threadIdx.x; b < a.nsq; b += kAdamThreads) ss += a.sq_part[b];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (threadIdx.x % kWarp == 0) s_ws[threadIdx.x / kWarp] = ss;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     double ss = 0.0;
-    for (int b = 0; b < a.nsq; ++b) ss += a.sq_part[b];
+    for (int w = 0; w < kAdamThreads / kWarp; ++w) ss += s_ws[w];
     const double norm = sqrt(ss);
     double coef = 1.0;
     if (a.max_norm > 0.f) {
@@ -192,10 +233,18 @@ int blocks_for(int64_t n, int threads, int cap) {
 
 }  // namespace
 
-int reduce_blocks(int64_t P) { return blocks_for(P, kRedThreads, 1024); }
+static int reduce_weight_blocks(const NetShape& s) {
+  const int64_t nW = (int64_t)s.H1 * s.D + (int64_t)s.H2 * s.H1 + (int64_t)s.C * s.H2;
+  return (int)((nW + kRedThreads - 1) / kRedThreads);
+}
+
+int reduce_blocks(const NetShape& s) {
+  const int nb = s.H1 + s.H2 + s.C + s.G + 6;
+  return reduce_weight_blocks(s) + (nb + kRedWarps - 1) / kRedWarps;
+}
 
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
-  reduce_kernel<<<reduce_blocks(a.s.P), kRedThreads, 0, st>>>(a);
+  reduce_kernel<<<reduce_blocks(a.s), kRedThreads, 0, st>>>(a, reduce_weight_blocks(a.s));
   return cudaGetLastError();
 }
 

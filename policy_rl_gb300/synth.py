@@ -161,7 +161,9 @@ class Rollout:
     boot: np.ndarray              # [N] float32
 
 
-def rollout(w: Workload, seed: int | None = None) -> Rollout:
+def rollout(w: Workload, seed: int | None = None, with_obs: bool = True) -> Rollout:
+    """Seeded rollout.  with_obs=False leaves obs None (a caller that fills a
+    very large observation buffer itself)."""
     s = w.seed if seed is None else seed
     T, N, B = w.T, w.N, w.B
     if w.reward == "sparse":
@@ -177,7 +179,9 @@ def rollout(w: Workload, seed: int | None = None) -> Rollout:
         return Rollout(None, None, None, None, val, rew, done, boot)
 
     D = w.obs_dim
-    if w.obs_kind == "ddnet":
+    if not with_obs:
+        obs = None
+    elif w.obs_kind == "ddnet":
         # 43x31 tile grid of integer ids 0..5, 15-d player state x 4 frames,
         # 4-d checkpoint navigation
         tiles = np.floor(6.0 * uniform(s, _ID["tiles"], B * 1333)).astype(np.float32)
@@ -198,8 +202,8 @@ def rollout(w: Workload, seed: int | None = None) -> Rollout:
     if w.n_gauss:
         lp += (-0.5 * act_cont.astype(np.float64) ** 2 - 0.5 * math.log(2 * math.pi)).sum(1)
     lp += 0.1 * normal(s, _ID["jitter"], B)
-    return Rollout(np.ascontiguousarray(obs), act_disc, act_cont, lp.astype(np.float32),
-                   val, rew, done, boot)
+    return Rollout(None if obs is None else np.ascontiguousarray(obs), act_disc, act_cont,
+                   lp.astype(np.float32), val, rew, done, boot)
 
 
 def init_params(w: Workload, seed: int | None = None) -> np.ndarray:
