@@ -129,6 +129,24 @@ ppo_status ppo_gae(const float *d_rew, const float *d_val, const float *d_done,
                    float *d_adv, float *d_ret, float *d_adv_norm, float *d_stats,
                    void *d_work, size_t work_bytes, cudaStream_t stream);
 
+/* ppo_gae without the workspace argument, for callers that cannot allocate
+ * device memory (a stream being captured into a CUDA graph where cudaMalloc is
+ * not allowed, latency-critical loops that must not enter the allocator,
+ * hosts whose device memory is all owned by their own pool).  The pages have
+ * no counterpart; the results are those of ppo_gae with the same arguments.
+ * The moment partials live in a fixed array in the library's device memory
+ * (about 193 KB, held on every GPU that loads the library until exit), so
+ * N must be at most 1,048,576 (PPO_ERR_UNSUPPORTED otherwise).  The first
+ * call on a device looks that array's address up (cudaGetSymbolAddress with
+ * the device current): make it before any stream capture.  All calls share
+ * the array: calls that may overlap on the GPU (unordered streams, several
+ * host threads) race and must be serialised by the caller.  Never calls
+ * cudaMalloc or cudaFree. */
+ppo_status ppo_gae_noalloc(const float *d_rew, const float *d_val, const float *d_done,
+                           const float *d_boot, int64_t T, int64_t N, float gamma, float lambda,
+                           float *d_adv, float *d_ret, float *d_adv_norm, float *d_stats,
+                           cudaStream_t stream);
+
 /* ---- Minibatch permutation -------------------------------------------------
  * "Teaching Mario to speedrun", sec. 6: "for minibatch in shuffle(batch)".
  * Key i = mulberry32 draw number epoch*B + i of the stream seeded with `seed`

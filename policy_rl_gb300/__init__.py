@@ -16,7 +16,7 @@ from ._abi import PpoConfig, PpoError
 
 __all__ = [
     "PpoConfig", "PpoError", "Context", "make_config", "ppo_param_count", "ppo_gae",
-    "ppo_gae_workspace_bytes", "ppo_minibatch_perm", "ppo_perm_workspace_bytes",
+    "ppo_gae_workspace_bytes", "ppo_gae_noalloc", "ppo_minibatch_perm", "ppo_perm_workspace_bytes",
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
     "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "library_path",
@@ -89,6 +89,15 @@ def ppo_gae(rew, val, done, boot, gamma, lam, adv, ret, adv_norm=None, stats=Non
     _abi.check(_lib().ppo_gae(_ptr(rew), _ptr(val), _ptr(done), _ptr(boot), T, N, gamma, lam,
                               _ptr(adv), _ptr(ret), _ptr(adv_norm), _ptr(stats), _ptr(work), wb,
                               _stream(stream)), "ppo_gae")
+
+
+def ppo_gae_noalloc(rew, val, done, boot, gamma, lam, adv, ret, adv_norm=None, stats=None,
+                    stream=None) -> None:
+    """ppo_gae for callers that cannot allocate device memory (see ppo.h)."""
+    T, N = rew.shape
+    _abi.check(_lib().ppo_gae_noalloc(_ptr(rew), _ptr(val), _ptr(done), _ptr(boot), T, N, gamma,
+                                      lam, _ptr(adv), _ptr(ret), _ptr(adv_norm), _ptr(stats),
+                                      _stream(stream)), "ppo_gae_noalloc")
 
 
 def ppo_perm_workspace_bytes(B: int) -> int:

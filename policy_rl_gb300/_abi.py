@@ -17,6 +17,7 @@ MAX_HEADS = 8
 SYMBOLS = (
     "ppo_status_string", "ppo_create", "ppo_destroy", "ppo_param_count", "ppo_buffers",
     "ppo_params_changed", "ppo_get_step", "ppo_gae_workspace_bytes", "ppo_gae",
+    "ppo_gae_noalloc",
     "ppo_perm_workspace_bytes", "ppo_minibatch_perm", "ppo_minibatch_loss_grad",
     "ppo_adam_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
     "ppo_sync_status",
@@ -77,6 +78,8 @@ def load(path: str = LIB_PATH):
         "ppo_gae_workspace_bytes": ([_I64, _I64, ctypes.POINTER(_SZ)], ctypes.c_int),
         "ppo_gae": ([_P, _P, _P, _P, _I64, _I64, _F, _F, _P, _P, _P, _P, _P, _SZ, _P],
                     ctypes.c_int),
+        "ppo_gae_noalloc": ([_P, _P, _P, _P, _I64, _I64, _F, _F, _P, _P, _P, _P, _P],
+                            ctypes.c_int),
         "ppo_perm_workspace_bytes": ([_I64, ctypes.POINTER(_SZ)], ctypes.c_int),
         "ppo_minibatch_perm": ([u32, _I64, _I64, _P, _P, _SZ, _P], ctypes.c_int),
         "ppo_minibatch_loss_grad": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P],
