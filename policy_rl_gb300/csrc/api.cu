@@ -466,7 +466,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->step, 1);
   A(c->done_ctr, 1);
   A(c->err, 1);
-  A(c->sq, std::max(1024, reduce_blocks(s)));
+  A(c->sq, std::max(4096, reduce_blocks(s)));
   if (c->bf16) {
     c->sh.ld3t = 64;
     A(c->sh.W1s, (int64_t)s.H1 * s.Dp);

@@ -42,6 +42,8 @@ constexpr int kGatherThreads = 256;
 // output); the thread holding chunk 0 of a row also copies the row's side data.
 __global__ void __launch_bounds__(kGatherThreads)
 gather_kernel(NetShape s, GatherArgs a, int per_row) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t t = (int64_t)blockIdx.x * kGatherThreads + threadIdx.x;
   const int64_t r = t / per_row;
   const int c = (int)(t - r * per_row);
@@ -97,8 +99,8 @@ cudaError_t launch_gather(const NetShape& s, const GatherArgs& a, cudaStream_t s
   const int per_row = (a.obs_bf16 || a.x_bf16) ? s.Dp / 8 : s.D;
   const int64_t threads = a.mb * per_row;
   const int64_t blocks = (threads + kGatherThreads - 1) / kGatherThreads;
-  gather_kernel<<<(int)blocks, kGatherThreads, 0, st>>>(s, a, per_row);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, dim3((unsigned)blocks), dim3(kGatherThreads), 0, st, s, a,
+                    per_row);
 }
 
 }  // namespace ppo

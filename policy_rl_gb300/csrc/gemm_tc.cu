@@ -147,8 +147,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
   if (EPI != EPI_BIAS_ACT)
     for (int i = threadIdx.x; i < 4 * kColsumCap + 4 * kLossPartials; i += kThreads) cs[i] = 0.f;
-  if (EPI != EPI_DACT)   // the bias, read by every epilogue thread, staged once
-    for (int i = threadIdx.x; i < p.N; i += kThreads) bias_s[i] = p.bias[i];
   if (warp == 1) tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
@@ -160,6 +158,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t tmem = *tslot;
   const Guard g{abort_flag, p.err, p.timeout_ns};
   const int total = p.tiles_m * p.tiles_n;
+  pdl_wait();      // inputs are written by the previous kernel of the chain
+  pdl_trigger();
+  if (EPI != EPI_DACT) {  // the bias, read by every epilogue thread, staged once
+    if (warp >= 2)
+      for (int i = threadIdx.x - 2 * kWarp; i < p.N; i += kThreads - 2 * kWarp)
+        bias_s[i] = p.bias[i];
+    asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 2 * kWarp));   // epilogue warps only
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -441,6 +447,8 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const Guard g{abort_flag, p.err, p.timeout_ns};
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -603,9 +611,9 @@ cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream
   p.last_k_steps = (rem + 15) / 16;
   const int total = p.tiles_m * p.tiles_n;
   const int grid = total < num_sms ? total : num_sms;
-  tc_gemm_kernel<BN, EPI><<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, p);
   if (grid_out) *grid_out = grid;
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(kThreads), Cfg<BN>::SMEM, st, ta,
+                    tb, p);
 }
 
 }  // namespace
@@ -740,8 +748,8 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
   }
   p.total_units = unit;
   const int grid = unit < num_sms ? unit : num_sms;
-  tc_wgrad_kernel<<<grid, kThreads, W_SMEM, st>>>(tu[0], tv[0], tu[1], tv[1], tu[2], tv[2], p);
-  return cudaGetLastError();
+  return launch_pdl(tc_wgrad_kernel, dim3(grid), dim3(kThreads), W_SMEM, st, tu[0], tv[0], tu[1],
+                    tv[1], tu[2], tv[2], p);
 }
 
 int tc_wgrad_splits(int rows, int kt_per_split) {

@@ -16,7 +16,7 @@ namespace {
 
 constexpr int kRedThreads = 256;
 constexpr int kNormThreads = 256;
-constexpr int kNormBlocks = 128;
+constexpr int kNormBlocks = 152 * 8;
 constexpr int kAdamThreads = 256;
 
 // Weight elements: one thread each, summing the split-K partials in split
@@ -34,6 +34,8 @@ __device__ __forceinline__ float warp_rows_sum(const float* base, int rows, int6
 }
 
 __global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int weight_blocks) {
+  pdl_wait();
+  pdl_trigger();
   const NetShape& s = a.s;
   const int nW1 = s.H1 * s.D, nW2 = s.H2 * s.H1, nW3 = s.C * s.H2;
   double sq = 0.0;
@@ -117,9 +119,16 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int w
 
 __global__ void __launch_bounds__(kNormThreads)
 sqnorm_kernel(const float* __restrict__ g, int64_t P, double* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   double s = 0.0;
-  for (int64_t i = (int64_t)blockIdx.x * kNormThreads + threadIdx.x; i < P;
-       i += (int64_t)gridDim.x * kNormThreads) {
+  const int64_t P4 = P / 4;
+  const int64_t stride = (int64_t)gridDim.x * kNormThreads;
+  for (int64_t i = (int64_t)blockIdx.x * kNormThreads + threadIdx.x; i < P4; i += stride) {
+    const float4 x = __ldcs(reinterpret_cast<const float4*>(g) + i);
+    s += (double)x.x * x.x + (double)x.y * x.y + (double)x.z * x.z + (double)x.w * x.w;
+  }
+  for (int64_t i = P4 * 4 + (int64_t)blockIdx.x * kNormThreads + threadIdx.x; i < P; i += stride) {
     const double x = g[i];
     s += x * x;
   }
@@ -159,6 +168,8 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
   __shared__ float s_coef, s_norm, s_ibc1, s_ibc2;
   __shared__ long long s_t;
   __shared__ double s_ws[kAdamThreads / kWarp];
+  pdl_wait();
+  pdl_trigger();
   {
     // every block sums the norm partials in the same fixed order
     double ss = 0.0;
@@ -191,12 +202,37 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
   const float lr = a.lr, eps = a.eps;
   const bool shadows = a.sh.W1s != nullptr;
   const int P = (int)a.P;
+  const int P4 = P / 4;
   const int stride = gridDim.x * kAdamThreads;
-  for (int i = blockIdx.x * kAdamThreads + threadIdx.x; i < P; i += stride) {
-    const float g = a.g[i] * coef;
-    const float m = b1 * a.m[i] + omb1 * g;
-    const float v = b2 * a.v[i] + omb2 * g * g;
-    const float p = a.p[i] - lr * (m * ibc1) / (sqrtf(v * ibc2) + eps);
+  auto step = [&](float g, float m0, float v0, float p0, float& m, float& v, float& p) {
+    g *= coef;
+    m = b1 * m0 + omb1 * g;
+    v = b2 * v0 + omb2 * g * g;
+    p = p0 - lr * (m * ibc1) / (sqrtf(v * ibc2) + eps);
+  };
+  for (int i = blockIdx.x * kAdamThreads + threadIdx.x; i < P4; i += stride) {
+    const float4 g4 = __ldcs(reinterpret_cast<const float4*>(a.g) + i);
+    const float4 m4 = reinterpret_cast<const float4*>(a.m)[i];
+    const float4 v4 = reinterpret_cast<const float4*>(a.v)[i];
+    const float4 p4 = reinterpret_cast<const float4*>(a.p)[i];
+    float4 mo, vo, po;
+    step(g4.x, m4.x, v4.x, p4.x, mo.x, vo.x, po.x);
+    step(g4.y, m4.y, v4.y, p4.y, mo.y, vo.y, po.y);
+    step(g4.z, m4.z, v4.z, p4.z, mo.z, vo.z, po.z);
+    step(g4.w, m4.w, v4.w, p4.w, mo.w, vo.w, po.w);
+    reinterpret_cast<float4*>(a.m)[i] = mo;
+    reinterpret_cast<float4*>(a.v)[i] = vo;
+    reinterpret_cast<float4*>(a.p)[i] = po;
+    if (shadows) {
+      write_shadow(a.s, a.sh, 4 * i + 0, po.x);
+      write_shadow(a.s, a.sh, 4 * i + 1, po.y);
+      write_shadow(a.s, a.sh, 4 * i + 2, po.z);
+      write_shadow(a.s, a.sh, 4 * i + 3, po.w);
+    }
+  }
+  for (int i = P4 * 4 + blockIdx.x * kAdamThreads + threadIdx.x; i < P; i += stride) {
+    float m, v, p;
+    step(a.g[i], a.m[i], a.v[i], a.p[i], m, v, p);
     a.m[i] = m;
     a.v[i] = v;
     a.p[i] = p;
@@ -244,20 +280,25 @@ int reduce_blocks(const NetShape& s) {
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
-  reduce_kernel<<<reduce_blocks(a.s), kRedThreads, 0, st>>>(a, reduce_weight_blocks(a.s));
-  return cudaGetLastError();
+  return launch_pdl(reduce_kernel, dim3(reduce_blocks(a.s)), dim3(kRedThreads), 0, st, a,
+                    reduce_weight_blocks(a.s));
 }
 
 cudaError_t launch_adam(const AdamArgs& a0, cudaStream_t st, const Trace* tr) {
   AdamArgs a = a0;
   if (a.nsq <= 0) {   // no squared-norm partials supplied: compute them
-    sqnorm_kernel<<<kNormBlocks, kNormThreads, 0, st>>>(a.g, a.P, const_cast<double*>(a.sq_part));
+    const int nb = blocks_for((a.P + 3) / 4, kNormThreads, kNormBlocks);
+    cudaError_t e = launch_pdl(sqnorm_kernel, dim3(nb), dim3(kNormThreads), 0, st, a.g, a.P,
+                               const_cast<double*>(a.sq_part));
+    if (e != cudaSuccess) return e;
     if (tr) tr->mark(ST_SQNORM, st);
-    a.nsq = kNormBlocks;
+    a.nsq = nb;
   }
-  adam_kernel<<<blocks_for(a.P, kAdamThreads, 152 * 4), kAdamThreads, 0, st>>>(a);
+  cudaError_t e = launch_pdl(adam_kernel, dim3(blocks_for((a.P + 3) / 4, kAdamThreads, 152 * 8)),
+                             dim3(kAdamThreads), 0, st, a);
+  if (e != cudaSuccess) return e;
   if (tr) tr->mark(ST_ADAM, st);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_shadows(const float* p, const NetShape& s, const Shadows& sh, cudaStream_t st) {
