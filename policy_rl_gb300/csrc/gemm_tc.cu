@@ -161,10 +161,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   pdl_wait();      // inputs are written by the previous kernel of the chain
   pdl_trigger();
   if (EPI != EPI_DACT) {  // the bias, read by every epilogue thread, staged once
-    if (warp >= 2)
-      for (int i = threadIdx.x - 2 * kWarp; i < p.N; i += kThreads - 2 * kWarp)
-        bias_s[i] = p.bias[i];
-    asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 2 * kWarp));   // epilogue warps only
+    for (int i = threadIdx.x; i < p.N; i += kThreads) bias_s[i] = p.bias[i];
+    __syncthreads();      // reached by every thread of the block (before the role split)
   }
 
   if (warp == 0) {
