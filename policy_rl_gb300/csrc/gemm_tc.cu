@@ -107,12 +107,21 @@ struct Ctrl {
 };
 
 // ---------------------------------------------------------------------------
+// Epilogue warps: 8 (two per TMEM lane quarter, splitting the tile's
+// columns) for the element-wise epilogues, 4 for the per-row loss epilogue.
+template <int EPI>
+__host__ __device__ constexpr int epi_warps() { return EPI == EPI_LOSS ? 4 : 8; }
+template <int EPI>
+__host__ __device__ constexpr int gemm_threads() { return 2 * kWarp + kWarp * epi_warps<EPI>(); }
+
 template <int BN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const TcParams p) {
   using C = Cfg<BN>;
   constexpr int S = C::S;
+  constexpr int EW = epi_warps<EPI>();
+  constexpr int NT = gemm_threads<EPI>();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -137,7 +146,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(cb.tfull(a), 1);
-      mbar_init(cb.tempty(a), 128);
+      mbar_init(cb.tempty(a), EW * kWarp);
     }
     mbar_init(cb.drain(), 1);
     *abort_flag = 0;
@@ -146,7 +155,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     fence_mbar_init();
   }
   if (EPI != EPI_BIAS_ACT)
-    for (int i = threadIdx.x; i < 4 * kColsumCap + 4 * kLossPartials; i += kThreads) cs[i] = 0.f;
+    for (int i = threadIdx.x; i < 4 * kColsumCap + 4 * kLossPartials; i += NT) cs[i] = 0.f;
   if (warp == 1) tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
@@ -161,7 +170,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   pdl_wait();      // inputs are written by the previous kernel of the chain
   pdl_trigger();
   if (EPI != EPI_DACT) {  // the bias, read by every epilogue thread, staged once
-    for (int i = threadIdx.x; i < p.N; i += kThreads) bias_s[i] = p.bias[i];
+    for (int i = threadIdx.x; i < p.N; i += NT) bias_s[i] = p.bias[i];
     __syncthreads();      // reached by every thread of the block (before the role split)
   }
 
@@ -223,10 +232,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
   } else {
-    // epilogue warps 2..5: TMEM lane quarter q = warp % 4
+    // epilogue warps 2..2+EW: TMEM lane quarter q = warp % 4, column part h
     const int q = warp & 3;
-    const int et = (warp - 2) * kWarp + lane;  // 0..127
-    (void)et;
+    const int h = (warp - 2) / 4;
     uint32_t tc = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const int acc = tc & 1;
@@ -286,10 +294,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // two register buffers, alternated by chunk parity (the loop is fully
         // unrolled, so the index is a compile-time constant): the registers of
         // an asynchronous TMEM load are read only after their own wait
+        constexpr int PART = BN / (EW / 4);   // columns per epilogue warp
+        constexpr int NCH = PART / 32;
+        const int cbase = h * PART;
         uint32_t r[2][32];
         uint4 ax[2][4];
-        const __nv_bfloat16* auxrow = p.aux + (int64_t)row * p.ldaux + tn * BN;
-        tmem_ld32_async(taddr, r[0]);
+        const __nv_bfloat16* auxrow = p.aux + (int64_t)row * p.ldaux + tn * BN + cbase;
+        tmem_ld32_async(taddr + (uint32_t)cbase, r[0]);
         if constexpr (EPI == EPI_DACT) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -297,15 +308,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                            : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          const int cur = (c0 / 32) & 1, nxt = cur ^ 1;
+        for (int k = 0; k < NCH; ++k) {
+          const int cur = k & 1, nxt = cur ^ 1;
+          const int c0 = cbase + 32 * k;
           tmem_wait_ld(r[cur]);
-          if (c0 + 32 < BN) {
+          if (k + 1 < NCH) {
             tmem_ld32_async(taddr + (uint32_t)(c0 + 32), r[nxt]);
             if constexpr (EPI == EPI_DACT) {
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                ax[nxt][i] = rok ? __ldg(reinterpret_cast<const uint4*>(auxrow + c0 + 32) + i)
+                ax[nxt][i] = rok ? __ldg(reinterpret_cast<const uint4*>(auxrow + 32 * (k + 1)) + i)
                                  : make_uint4(0, 0, 0, 0);
             }
           }
@@ -367,7 +379,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if constexpr (EPI != EPI_BIAS_ACT) {
     if (warp >= 2) {
       const int et = threadIdx.x - 2 * kWarp;
-      for (int c = et; c < p.epi_n; c += 128)
+      for (int c = et; c < p.epi_n; c += EW * kWarp)
         p.colsum_part[(int64_t)blockIdx.x * p.epi_n + c] =
             ((cs[c] + cs[kColsumCap + c]) + cs[2 * kColsumCap + c]) + cs[3 * kColsumCap + c];
       if constexpr (EPI == EPI_LOSS) {
@@ -610,8 +622,8 @@ cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream
   const int total = p.tiles_m * p.tiles_n;
   const int grid = total < num_sms ? total : num_sms;
   if (grid_out) *grid_out = grid;
-  return launch_pdl(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(kThreads), Cfg<BN>::SMEM, st, ta,
-                    tb, p);
+  return launch_pdl(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(gemm_threads<EPI>()), Cfg<BN>::SMEM,
+                    st, ta, tb, p);
 }
 
 }  // namespace

@@ -210,19 +210,24 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
     v = b2 * v0 + omb2 * g * g;
     p = p0 - lr * (m * ibc1) / (sqrtf(v * ibc2) + eps);
   };
+  const float4* __restrict__ G4 = reinterpret_cast<const float4*>(a.g);
+  float4* __restrict__ M4 = reinterpret_cast<float4*>(a.m);
+  float4* __restrict__ V4 = reinterpret_cast<float4*>(a.v);
+  float4* __restrict__ PP4 = reinterpret_cast<float4*>(a.p);
+#pragma unroll 2
   for (int i = blockIdx.x * kAdamThreads + threadIdx.x; i < P4; i += stride) {
-    const float4 g4 = __ldcs(reinterpret_cast<const float4*>(a.g) + i);
-    const float4 m4 = reinterpret_cast<const float4*>(a.m)[i];
-    const float4 v4 = reinterpret_cast<const float4*>(a.v)[i];
-    const float4 p4 = reinterpret_cast<const float4*>(a.p)[i];
+    const float4 g4 = __ldcs(G4 + i);
+    const float4 m4 = __ldcs(M4 + i);
+    const float4 v4 = __ldcs(V4 + i);
+    const float4 p4 = __ldcs(PP4 + i);
     float4 mo, vo, po;
     step(g4.x, m4.x, v4.x, p4.x, mo.x, vo.x, po.x);
     step(g4.y, m4.y, v4.y, p4.y, mo.y, vo.y, po.y);
     step(g4.z, m4.z, v4.z, p4.z, mo.z, vo.z, po.z);
     step(g4.w, m4.w, v4.w, p4.w, mo.w, vo.w, po.w);
-    reinterpret_cast<float4*>(a.m)[i] = mo;
-    reinterpret_cast<float4*>(a.v)[i] = vo;
-    reinterpret_cast<float4*>(a.p)[i] = po;
+    __stcs(M4 + i, mo);
+    __stcs(V4 + i, vo);
+    __stcs(PP4 + i, po);
     if (shadows) {
       write_shadow(a.s, a.sh, 4 * i + 0, po.x);
       write_shadow(a.s, a.sh, 4 * i + 1, po.y);
