@@ -51,6 +51,7 @@ struct ppo_ctx {
 
   float *params = nullptr, *grad = nullptr, *m = nullptr, *v = nullptr;
   int64_t* step = nullptr;
+  double* beta_pow = nullptr;
   unsigned* done_ctr = nullptr;
   int* err = nullptr;
   double* sq = nullptr;
@@ -355,6 +356,7 @@ ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t
   a.omb1 = (float)(1.0 - c->cfg.beta1);   // 1 - beta in double: no cancellation in fp32
   a.omb2 = (float)(1.0 - c->cfg.beta2);
   a.step = c->step;
+  a.beta_pow = c->beta_pow;
   a.done_ctr = c->done_ctr;
   a.grad_norm_out = grad_norm_out;
   a.s = c->s;
@@ -464,6 +466,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->m, P);
   A(c->v, P);
   A(c->step, 1);
+  A(c->beta_pow, 2);
   A(c->done_ctr, 1);
   A(c->err, 1);
   A(c->sq, std::max(4096, reduce_blocks(s)));
@@ -520,7 +523,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->perm, B * c->emax);
   {
     void* t;
-    if ((r = c->alloc(&t, perm_workspace_bytes(B, 1))) != PPO_OK) return fail(r);
+    if ((r = c->alloc(&t, perm_workspace_bytes(B, c->emax))) != PPO_OK) return fail(r);
     c->perm_work = t;
   }
 #undef A
@@ -528,6 +531,11 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   if (h_init_params) {
     if (cudaMemcpy(c->params, h_init_params, sizeof(float) * P, cudaMemcpyHostToDevice) !=
         cudaSuccess)
+      return fail(PPO_ERR_CUDA);
+  }
+  {
+    const double one[2] = {1.0, 1.0};   // beta^0
+    if (cudaMemcpy(c->beta_pow, one, sizeof one, cudaMemcpyHostToDevice) != cudaSuccess)
       return fail(PPO_ERR_CUDA);
   }
   if (launch_shadows(c->params, s, c->sh, 0) != cudaSuccess) return fail(PPO_ERR_CUDA);

@@ -35,6 +35,24 @@ __device__ __forceinline__ Moments merge(Moments a, Moments b) {
   return r;
 }
 
+// fp32 variant for the warp level (counts <= 32*T < 2^24 are exact in float)
+struct MomentsF {
+  float n, mean, m2;
+};
+
+__device__ __forceinline__ MomentsF merge_f(MomentsF a, MomentsF b) {
+  if (a.n == 0.f) return b;
+  if (b.n == 0.f) return a;
+  const float n = a.n + b.n;
+  const float d = b.mean - a.mean;
+  const float fb = b.n / n;
+  MomentsF r;
+  r.n = n;
+  r.mean = a.mean + d * fb;
+  r.m2 = a.m2 + b.m2 + d * d * a.n * fb;
+  return r;
+}
+
 __device__ __forceinline__ Moments shfl_moments(Moments m, int o) {
   Moments r;
   r.n = __shfl_xor_sync(0xffffffffu, m.n, o);
@@ -66,7 +84,7 @@ gae_kernel(const float* __restrict__ rew, const float* __restrict__ val,
            float gamma, float gl, float* __restrict__ adv, float* __restrict__ ret,
            double* __restrict__ partials) {
   const int n = blockIdx.x * kGaeThreads + threadIdx.x;
-  Moments mom{0.0, 0.0, 0.0};
+  MomentsF momf{0.f, 0.f, 0.f};
   if (n < N) {
     float next_v = boot[n];
     float next_a = 0.f;
@@ -115,15 +133,22 @@ gae_kernel(const float* __restrict__ rew, const float* __restrict__ val,
         }
       }
     }
-    const double cnt = (double)T;
-    mom.n = cnt;
-    mom.mean = (double)shift + (double)s1 / cnt;
-    mom.m2 = fmax((double)s2 - (double)s1 * (double)s1 / cnt, 0.0);
+    const float cnt = (float)T;
+    momf.n = cnt;
+    momf.mean = shift + s1 / cnt;
+    momf.m2 = fmaxf(s2 - s1 * (s1 / cnt), 0.f);
   }
   if (partials == nullptr) return;
-  // fixed-order tree: warp xor-merges, then warp 0 merges the warps' results
+  // fixed-order tree: fp32 warp xor-merges, then fp64 over the warps
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mom = merge(mom, shfl_moments(mom, o));
+  for (int o = 16; o > 0; o >>= 1) {
+    MomentsF other;
+    other.n = __shfl_xor_sync(0xffffffffu, momf.n, o);
+    other.mean = __shfl_xor_sync(0xffffffffu, momf.mean, o);
+    other.m2 = __shfl_xor_sync(0xffffffffu, momf.m2, o);
+    momf = merge_f(momf, other);
+  }
+  Moments mom{(double)momf.n, (double)momf.mean, (double)momf.m2};
   __shared__ Moments wm[kGaeThreads / kWarp];
   const int w = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   if (lane == 0) wm[w] = mom;

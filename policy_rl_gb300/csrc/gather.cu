@@ -48,7 +48,7 @@ gather_kernel(NetShape s, GatherArgs a, int per_row) {
   const int64_t r = t / per_row;
   const int c = (int)(t - r * per_row);
   if (r >= a.mb) return;
-  int64_t src = a.idx[r];
+  int64_t src = __ldg(a.idx + r);
   src = src < 0 ? 0 : (src >= a.B ? a.B - 1 : src);   // never read outside the batch
   if (a.obs_bf16) {
     const uint4* in = reinterpret_cast<const uint4*>(a.obs_bf16 + src * s.Dp);
@@ -68,19 +68,25 @@ gather_kernel(NetShape s, GatherArgs a, int per_row) {
     static_cast<float*>(a.X)[r * s.D + c] = __ldg(a.obs_f32 + src * s.D + c);
   }
   if (c != 0) return;
+  // side data: every load is issued before any store
+  int32_t act[PPO_MAX_HEADS];
+  float actc[4];
+  for (int h = 0; h < s.NH; ++h) act[h] = __ldg(a.act + src * s.NH + h);
+  for (int g = 0; g < s.G; ++g) actc[g] = __ldg(a.actc + src * s.G + g);
+  const float lp = __ldg(a.logp_old + src);
+  float A = __ldg(a.adv + src);
+  const float R = __ldg(a.ret + src);
+  if (a.adv_stats) A = (A - __ldg(a.adv_stats)) / (__ldg(a.adv_stats + 1) + 1e-8f);
   for (int h = 0; h < s.NH; ++h) {
     // an out-of-range action is clamped into its head so the loss never
     // indexes outside the head's logits
-    const int32_t x = a.act[src * s.NH + h];
     const int n = s.head_n[h];
-    a.act_mb[r * s.NH + h] = x < 0 ? 0 : (x >= n ? n - 1 : x);
+    a.act_mb[r * s.NH + h] = act[h] < 0 ? 0 : (act[h] >= n ? n - 1 : act[h]);
   }
-  for (int g = 0; g < s.G; ++g) a.actc_mb[r * s.G + g] = a.actc[src * s.G + g];
-  a.logp_mb[r] = a.logp_old[src];
-  float A = a.adv[src];
-  if (a.adv_stats) A = (A - a.adv_stats[0]) / (a.adv_stats[1] + 1e-8f);
+  for (int g = 0; g < s.G; ++g) a.actc_mb[r * s.G + g] = actc[g];
+  a.logp_mb[r] = lp;
   a.adv_mb[r] = A;
-  a.ret_mb[r] = a.ret[src];
+  a.ret_mb[r] = R;
 }
 
 }  // namespace

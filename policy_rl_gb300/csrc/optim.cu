@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int w
     }
     if (i >= 0) {
       a.grad[i] = v;
-      sq = (double)v * (double)v;
+      sq = (double)(v * v);
     }
   } else {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int w
       }
       if (lane == 0) {
         a.grad[i] = v;
-        sq = (double)v * (double)v;
+        sq = (double)(v * v);
       }
     } else if (e < nb + 6) {
       const int q = e - nb;
@@ -121,17 +121,18 @@ __global__ void __launch_bounds__(kNormThreads)
 sqnorm_kernel(const float* __restrict__ g, int64_t P, double* __restrict__ part) {
   pdl_wait();
   pdl_trigger();
-  double s = 0.0;
+  // fp32 within a thread (a few hundred terms at most), fp64 across threads
+  float sf = 0.f;
   const int64_t P4 = P / 4;
   const int64_t stride = (int64_t)gridDim.x * kNormThreads;
+#pragma unroll 4
   for (int64_t i = (int64_t)blockIdx.x * kNormThreads + threadIdx.x; i < P4; i += stride) {
     const float4 x = __ldcs(reinterpret_cast<const float4*>(g) + i);
-    s += (double)x.x * x.x + (double)x.y * x.y + (double)x.z * x.z + (double)x.w * x.w;
+    sf = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, sf))));
   }
-  for (int64_t i = P4 * 4 + (int64_t)blockIdx.x * kNormThreads + threadIdx.x; i < P; i += stride) {
-    const double x = g[i];
-    s += x * x;
-  }
+  for (int64_t i = P4 * 4 + (int64_t)blockIdx.x * kNormThreads + threadIdx.x; i < P; i += stride)
+    sf = fmaf(g[i], g[i], sf);
+  double s = (double)sf;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   __shared__ double ws[kNormThreads / kWarp];
@@ -182,19 +183,16 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
   if (threadIdx.x == 0) {
     double ss = 0.0;
     for (int w = 0; w < kAdamThreads / kWarp; ++w) ss += s_ws[w];
-    const double norm = sqrt(ss);
-    double coef = 1.0;
-    if (a.max_norm > 0.f) {
-      const double c = (double)a.max_norm / (norm + 1e-6);
-      coef = c < 1.0 ? c : 1.0;
-    }
-    const long long t = (long long)(*a.step) + 1;
-    s_coef = (float)coef;
-    s_norm = (float)norm;
-    s_t = t;
-    // bias corrections 1 - beta^t, in double, once per block
-    s_ibc1 = (float)(1.0 / (1.0 - pow(a.b1, (double)t)));
-    s_ibc2 = (float)(1.0 / (1.0 - pow(a.b2, (double)t)));
+    const float norm = sqrtf((float)ss);
+    float coef = 1.f;
+    if (a.max_norm > 0.f) coef = fminf(1.f, a.max_norm / (norm + 1e-6f));
+    s_coef = coef;
+    s_norm = norm;
+    s_t = (long long)(*a.step) + 1;
+    // bias corrections 1 - beta^t from the running powers beta^(t-1) (device
+    // state, advanced by the last block), one multiply each -- no pow()
+    s_ibc1 = (float)(1.0 / (1.0 - a.beta_pow[0] * a.b1));
+    s_ibc2 = (float)(1.0 / (1.0 - a.beta_pow[1] * a.b2));
   }
   __syncthreads();
   const float coef = s_coef, ibc1 = s_ibc1, ibc2 = s_ibc2;
@@ -251,6 +249,8 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
     const unsigned prev = atomicAdd(a.done_ctr, 1u);
     if (prev == gridDim.x - 1) {
       *a.step = (int64_t)s_t;
+      a.beta_pow[0] *= a.b1;
+      a.beta_pow[1] *= a.b2;
       if (a.grad_norm_out) *a.grad_norm_out = s_norm;
       *a.done_ctr = 0u;
       __threadfence();

@@ -30,19 +30,23 @@ __device__ __forceinline__ uint32_t mulberry32_draw(uint32_t seed, uint64_t k) {
   return n ^ (n >> 14);
 }
 
+// Input of one radix pass for all epochs at once: epoch e = blockIdx.y reads
+// keys/vals at offset e*B (or generates draw e*B + i of the stream).
 struct SortIn {
-  const uint32_t* keys;   // nullptr: generate from (seed, draw0 + i)
+  const uint32_t* keys;   // nullptr: generate from (seed, draw0 + e*B + i)
   const int32_t* vals;    // nullptr: value = i
   uint32_t seed;
   uint64_t draw0;
 };
 
-__device__ __forceinline__ void load_kv(const SortIn& in, int64_t i, uint32_t& k, int32_t& v) {
+__device__ __forceinline__ void load_kv(const SortIn& in, int64_t B, int64_t i, uint32_t& k,
+                                        int32_t& v) {
+  const int64_t e = blockIdx.y;
   if (in.keys) {
-    k = in.keys[i];
-    v = in.vals[i];
+    k = in.keys[e * B + i];
+    v = in.vals[e * B + i];
   } else {
-    k = mulberry32_draw(in.seed, in.draw0 + (uint64_t)i);
+    k = mulberry32_draw(in.seed, in.draw0 + (uint64_t)(e * B + i));
     v = (int32_t)i;
   }
 }
@@ -50,13 +54,16 @@ __device__ __forceinline__ void load_kv(const SortIn& in, int64_t i, uint32_t& k
 __global__ void __launch_bounds__(kSortThreads)
 hist_kernel(SortIn in, int64_t B, int shift, uint32_t* __restrict__ ghist, int num_tiles) {
   __shared__ uint32_t h[kRadix];
+  const int64_t e = blockIdx.y;
+  ghist += e * (int64_t)kRadix * num_tiles;
   h[threadIdx.x] = 0;
   __syncthreads();
   const int64_t base = (int64_t)blockIdx.x * kTile;
   for (int j = 0; j < kTile / kSortThreads; ++j) {
     const int64_t i = base + j * kSortThreads + threadIdx.x;
     if (i < B) {
-      const uint32_t k = in.keys ? in.keys[i] : mulberry32_draw(in.seed, in.draw0 + (uint64_t)i);
+      const uint32_t k = in.keys ? in.keys[e * B + i]
+                                 : mulberry32_draw(in.seed, in.draw0 + (uint64_t)(e * B + i));
       atomicAdd(&h[(k >> shift) & 0xFF], 1u);
     }
   }
@@ -99,6 +106,8 @@ constexpr int kScanPer = 8;
 __global__ void __launch_bounds__(kSortThreads)
 digit_scan_kernel(uint32_t* __restrict__ ghist, int num_tiles, uint32_t* __restrict__ dtotal) {
   __shared__ uint32_t wsum[kSortWarps];
+  ghist += (int64_t)blockIdx.y * kRadix * num_tiles;
+  dtotal += (int64_t)blockIdx.y * kRadix;
   uint32_t* row = ghist + (int64_t)blockIdx.x * num_tiles;
   uint32_t carry = 0;
   for (int base = 0; base < num_tiles; base += kSortThreads * kScanPer) {
@@ -132,6 +141,13 @@ scatter_kernel(SortIn in, int64_t B, int shift, const uint32_t* __restrict__ gsc
   __shared__ uint32_t wsum[kSortWarps];
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   {
+    const int64_t e = blockIdx.y;
+    gscan += e * (int64_t)kRadix * num_tiles;
+    dtotal += e * kRadix;
+    if (keys_out) keys_out += e * B;
+    vals_out += e * B;
+  }
+  {
     // first output position of each digit: exclusive scan of the digit totals
     uint32_t tot;
     dbase[threadIdx.x] = block_excl_scan256(dtotal[threadIdx.x], wsum, &tot);
@@ -148,7 +164,7 @@ scatter_kernel(SortIn in, int64_t B, int shift, const uint32_t* __restrict__ gsc
   for (int r = 0; r < kPerLane; ++r) {
     const int64_t i = base + r * kWarp + lane;
     if (i < B) {
-      load_kv(in, i, k[r], v[r]);
+      load_kv(in, B, i, k[r], v[r]);
       dig[r] = (k[r] >> shift) & 0xFF;
     } else {
       dig[r] = kRadix;   // sentinel: not counted, not written
@@ -192,61 +208,58 @@ scatter_kernel(SortIn in, int64_t B, int shift, const uint32_t* __restrict__ gsc
 
 }  // namespace
 
-size_t perm_workspace_bytes(int64_t B, int /*epochs*/) {
+size_t perm_workspace_bytes(int64_t B, int epochs) {
   const int64_t tiles = (B + kTile - 1) / kTile;
-  const size_t kv = (size_t)B * 4;
+  const size_t kv = (size_t)B * 4 * epochs;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return 4 * al(kv) + al((size_t)tiles * kRadix * 4) + al(kRadix * 4);
+  return 4 * al(kv) + al((size_t)tiles * kRadix * 4 * epochs) + al((size_t)kRadix * 4 * epochs);
 }
 
 cudaError_t launch_perm(uint32_t seed, int64_t epoch0, int epochs, int64_t B, int32_t* perm,
                         void* work, cudaStream_t st, const Trace* tr) {
-  const int64_t tiles64 = (B + kTile - 1) / kTile;
-  const int tiles = (int)tiles64;
+  const int tiles = (int)((B + kTile - 1) / kTile);
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t kv = (size_t)B * 4 * epochs;
   char* w = static_cast<char*>(work);
   uint32_t* ka = reinterpret_cast<uint32_t*>(w);
-  w += al((size_t)B * 4);
+  w += al(kv);
   int32_t* va = reinterpret_cast<int32_t*>(w);
-  w += al((size_t)B * 4);
+  w += al(kv);
   uint32_t* kb = reinterpret_cast<uint32_t*>(w);
-  w += al((size_t)B * 4);
+  w += al(kv);
   int32_t* vb = reinterpret_cast<int32_t*>(w);
-  w += al((size_t)B * 4);
+  w += al(kv);
   uint32_t* ghist = reinterpret_cast<uint32_t*>(w);
-  w += al((size_t)tiles * kRadix * 4);
+  w += al((size_t)tiles * kRadix * 4 * epochs);
   uint32_t* dtotal = reinterpret_cast<uint32_t*>(w);
 
-  for (int e = 0; e < epochs; ++e) {
-    const uint64_t draw0 = (uint64_t)(epoch0 + e) * (uint64_t)B;
-    int32_t* out = perm + (int64_t)e * B;
-    SortIn in{nullptr, nullptr, seed, draw0};
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 8 * pass;
-      uint32_t* ko;
-      int32_t* vo;
-      if (pass == 3) {
-        ko = nullptr;
-        vo = out;
-      } else if (pass % 2 == 0) {
-        ko = kb;
-        vo = vb;
-      } else {
-        ko = ka;
-        vo = va;
-      }
-      hist_kernel<<<tiles, kSortThreads, 0, st>>>(in, B, shift, ghist, tiles);
-      if (tr) tr->mark(ST_PERM_HIST, st);
-      digit_scan_kernel<<<kRadix, kSortThreads, 0, st>>>(ghist, tiles, dtotal);
-      if (tr) tr->mark(ST_PERM_SCAN, st);
-      scatter_kernel<<<tiles, kSortThreads, 0, st>>>(in, B, shift, ghist, tiles, dtotal, ko, vo);
-      if (tr) tr->mark(ST_PERM_SCATTER, st);
-      in = SortIn{ko, vo, seed, draw0};
+  // all epochs sorted together: epoch e = blockIdx.y, output perm + e*B
+  const uint64_t draw0 = (uint64_t)epoch0 * (uint64_t)B;
+  SortIn in{nullptr, nullptr, seed, draw0};
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 8 * pass;
+    uint32_t* ko;
+    int32_t* vo;
+    if (pass == 3) {
+      ko = nullptr;
+      vo = perm;
+    } else if (pass % 2 == 0) {
+      ko = kb;
+      vo = vb;
+    } else {
+      ko = ka;
+      vo = va;
     }
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    hist_kernel<<<dim3(tiles, epochs), kSortThreads, 0, st>>>(in, B, shift, ghist, tiles);
+    if (tr) tr->mark(ST_PERM_HIST, st);
+    digit_scan_kernel<<<dim3(kRadix, epochs), kSortThreads, 0, st>>>(ghist, tiles, dtotal);
+    if (tr) tr->mark(ST_PERM_SCAN, st);
+    scatter_kernel<<<dim3(tiles, epochs), kSortThreads, 0, st>>>(in, B, shift, ghist, tiles,
+                                                                  dtotal, ko, vo);
+    if (tr) tr->mark(ST_PERM_SCATTER, st);
+    in = SortIn{ko, vo, seed, draw0};
   }
-  return cudaSuccess;
+  return cudaGetLastError();
 }
 
 }  // namespace ppo
