@@ -79,6 +79,11 @@ typedef struct {
     int64_t max_batch;           /* largest T*N given to ppo_update          */
     int64_t max_minibatch;       /* largest minibatch row count              */
     int32_t max_epochs;          /* largest epoch count given to ppo_update  */
+    int32_t per_stage_kernels;   /* bf16 mode: 0 (default) runs a minibatch
+                                    step as one persistent cooperative kernel
+                                    (stages separated by grid barriers); 1
+                                    launches one kernel per stage.  Same
+                                    results up to fp32 summation order.      */
 } ppo_config;
 
 typedef struct ppo_ctx ppo_ctx;
@@ -221,7 +226,7 @@ ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_ac
 
 /* ---- Profiling -----------------------------------------------------------------
  * The library's kernels, by stage; one stage entry is one kernel launch. */
-#define PPO_NUM_STAGES 18
+#define PPO_NUM_STAGES 19
 /* Name of a stage (static string; "unknown" outside [0, PPO_NUM_STAGES)). */
 const char *ppo_stage_name(int32_t stage);
 

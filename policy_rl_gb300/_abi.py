@@ -22,7 +22,7 @@ SYMBOLS = (
     "ppo_adam_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
     "ppo_sync_status",
 )
-NUM_STAGES = 18
+NUM_STAGES = 19
 
 STATUS = {0: "PPO_OK", 1: "PPO_ERR_INVALID", 2: "PPO_ERR_ALIGN", 3: "PPO_ERR_CUDA",
           4: "PPO_ERR_UNSUPPORTED", 5: "PPO_ERR_TIMEOUT", 6: "PPO_ERR_NOMEM"}
@@ -43,7 +43,7 @@ class PpoConfig(ctypes.Structure):
         ("ent_coef", ctypes.c_float), ("max_grad_norm", ctypes.c_float),
         ("beta1", ctypes.c_double), ("beta2", ctypes.c_double), ("adam_eps", ctypes.c_double),
         ("max_batch", ctypes.c_int64), ("max_minibatch", ctypes.c_int64),
-        ("max_epochs", ctypes.c_int32),
+        ("max_epochs", ctypes.c_int32), ("per_stage_kernels", ctypes.c_int32),
     ]
 
 

@@ -46,7 +46,9 @@ struct ppo_ctx {
   ppo_config cfg;
   NetShape s;
   int bf16 = 0;
+  int use_mk = 0;        // bf16: one persistent kernel per minibatch
   int num_sms = 1;
+  unsigned* gbar = nullptr;
   std::vector<void*> allocs;
 
   float *params = nullptr, *grad = nullptr, *m = nullptr, *v = nullptr;
@@ -365,6 +367,113 @@ ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t
   return PPO_OK;
 }
 
+// One bf16 minibatch (gather .. gradient assembly, and Adam when do_adam) as
+// one persistent cooperative kernel.
+ppo_status enqueue_minibatch_mk(ppo_ctx* c, const float* obs, const __nv_bfloat16* obs_packed,
+                                const int32_t* act, const float* actc, const float* logp_old,
+                                const float* adv, const float* ret, const int32_t* idx, int64_t B,
+                                int64_t mb, const float* adv_stats, float* stats6, int do_adam,
+                                float lr, cudaStream_t st) {
+  const NetShape& s = c->s;
+  const float* P = c->params;
+  const int M = (int)mb;
+  const int grid = mk_grid(c->num_sms);
+  auto* X = static_cast<__nv_bfloat16*>(c->X);
+  auto* H1 = static_cast<__nv_bfloat16*>(c->H1);
+  auto* H2 = static_cast<__nv_bfloat16*>(c->H2);
+  auto* dZ = static_cast<__nv_bfloat16*>(c->dZ);
+  auto* dP2 = static_cast<__nv_bfloat16*>(c->dP2);
+  auto* dP1 = static_cast<__nv_bfloat16*>(c->dP1);
+  MkLaunch L{};
+  L.s = s;
+  L.ga.obs_f32 = obs;
+  L.ga.obs_bf16 = obs_packed;
+  L.ga.act = act;
+  L.ga.actc = actc;
+  L.ga.logp_old = logp_old;
+  L.ga.adv = adv;
+  L.ga.ret = ret;
+  L.ga.adv_stats = adv_stats;
+  L.ga.idx = idx;
+  L.ga.mb = mb;
+  L.ga.B = B;
+  L.ga.X = X;
+  L.ga.x_bf16 = 1;
+  L.ga.act_mb = c->act_mb;
+  L.ga.actc_mb = c->actc_mb;
+  L.ga.logp_mb = c->logp_mb;
+  L.ga.adv_mb = c->adv_mb;
+  L.ga.ret_mb = c->ret_mb;
+  L.fwd1 = GemmOperands{X, s.Dp, c->sh.W1s, s.Dp, M, s.H1, s.Dp};
+  L.fwd2 = GemmOperands{H1, s.H1, c->sh.W2s, s.H1, M, s.H2, s.H1};
+  L.loss = GemmOperands{H2, s.H2, c->sh.W3s, s.H2, M, s.CP, s.H2};
+  L.dact2 = GemmOperands{dZ, c->lddz, c->sh.W3Ts, c->sh.ld3t, M, s.H2, s.CP};
+  L.dact1 = GemmOperands{dP2, s.H2, c->sh.W2Ts, s.H2, M, s.H1, s.H2};
+  L.b1 = P + s.ob1;
+  L.b2 = P + s.ob2;
+  L.b3 = P + s.ob3;
+  L.logstd = P + s.ologstd;
+  L.H1 = H1;
+  L.H2 = H2;
+  L.dP2 = dP2;
+  L.dP1 = dP1;
+  L.dz = dZ;
+  L.lddz = c->lddz;
+  L.cs1 = c->cs1;
+  L.cs2 = c->cs2;
+  L.cs3 = c->cs3;
+  L.loss_part = c->lossp;
+  const int per = wgrad_kt_per_split(s, mb, grid);
+  L.wg[0] = {dP2, s.H2, s.H2, H1, s.H1, s.H1, per, c->pW2};
+  L.wg[1] = {dP1, s.H1, s.H1, X, s.Dp, s.Dp, s.Dp % 128 == 0 ? per : 2 * per, c->pW1};
+  L.wg[2] = {H2, s.H2, s.H2, dZ, c->lddz, 64, 2 * per, c->pW3};
+  for (auto& r : L.wg)
+    if (tc_wgrad_splits(M, r.kt_per_split) > kMaxSplit)
+      r.kt_per_split = (int)(((mb + 63) / 64 + kMaxSplit - 1) / kMaxSplit);
+  L.rows = M;
+  ReduceArgs& ra = L.ra;
+  ra.s = s;
+  ra.inv_mb = 1.0f / (float)mb;
+  ra.grad = c->grad;
+  ra.stats6 = stats6;
+  ra.pW1 = c->pW1; ra.s1 = tc_wgrad_splits(M, L.wg[1].kt_per_split); ra.ld1 = s.Dp;
+  ra.pW2 = c->pW2; ra.s2 = tc_wgrad_splits(M, L.wg[0].kt_per_split);
+  ra.pW3t = c->pW3; ra.s3 = tc_wgrad_splits(M, L.wg[2].kt_per_split); ra.ld3 = 64;
+  ra.pb1 = c->cs1; ra.nb1 = grid;
+  ra.pb2 = c->cs2; ra.nb2 = grid;
+  ra.pb3 = c->cs3; ra.nb3 = grid; ra.ldb3 = s.CP;
+  ra.ploss = c->lossp; ra.nl = grid;
+  L.do_adam = do_adam;
+  AdamArgs& a = L.aa;
+  a.p = c->params;
+  a.g = c->grad;
+  a.m = c->m;
+  a.v = c->v;
+  a.P = s.P;
+  a.max_norm = c->cfg.max_grad_norm;
+  a.lr = lr;
+  a.b1 = c->cfg.beta1;
+  a.b2 = c->cfg.beta2;
+  a.eps = (float)c->cfg.adam_eps;
+  a.omb1 = (float)(1.0 - c->cfg.beta1);
+  a.omb2 = (float)(1.0 - c->cfg.beta2);
+  a.step = c->step;
+  a.beta_pow = c->beta_pow;
+  a.s = s;
+  a.sh = c->sh;
+  L.lc = LossCoef{c->cfg.clip, c->cfg.vf_coef, c->cfg.ent_coef};
+  L.rows_in = LossRows{c->act_mb, c->actc_mb, c->logp_mb, c->adv_mb, c->ret_mb};
+  L.inv_mb = 1.0f / (float)mb;
+  L.gbar = c->gbar;
+  L.sq_part = c->sq;
+  L.err = c->err;
+  L.timeout_ns = kTimeoutNs;
+  L.grid = grid;
+  PPO_CUDA(mk_launch(L, st));
+  c->tr.mark(ST_MINIBATCH, st);
+  return PPO_OK;
+}
+
 ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, const float* actc,
                           const float* logp_old, const float* val, const float* rew,
                           const float* done, const float* boot, int64_t T, int64_t N,
@@ -372,6 +481,8 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
                           float lr, uint32_t seed, float* stats, cudaStream_t st) {
   const int64_t B = T * N, mb = B / minibatches;
   const __nv_bfloat16* packed = nullptr;
+  if (c->use_mk)   // grid-barrier counters start at zero (also after an aborted launch)
+    PPO_CUDA(cudaMemsetAsync(c->gbar, 0, 2 * sizeof(unsigned), st));
   if (c->bf16) {
     PPO_CUDA(launch_pack_obs(obs, B, c->s.D, c->s.Dp, c->obs_packed, st));
     c->tr.mark(ST_PACK, st);
@@ -387,10 +498,15 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
     for (int k = 0; k < minibatches; ++k) {
       const int32_t* idx = c->perm + (int64_t)e * B + (int64_t)k * mb;
       float* st6 = stats ? stats + ((int64_t)e * minibatches + k) * 6 : nullptr;
-      int nsq = 0;
-      TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
-                            c->advstats, st6, st, &nsq));
-      TRY(enqueue_adam(c, lr, nullptr, st, nsq));
+      if (c->use_mk) {
+        TRY(enqueue_minibatch_mk(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
+                                 c->advstats, st6, 1, lr, st));
+      } else {
+        int nsq = 0;
+        TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
+                              c->advstats, st6, st, &nsq));
+        TRY(enqueue_adam(c, lr, nullptr, st, nsq));
+      }
     }
   return PPO_OK;
 }
@@ -446,6 +562,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   c->cfg = *cfg;
   c->s = s;
   c->bf16 = cfg->precision == 1;
+  c->use_mk = c->bf16 && cfg->per_stage_kernels == 0;
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (c->num_sms < 1) c->num_sms = 1;
   c->mbmax = cfg->max_minibatch;
@@ -467,6 +584,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->v, P);
   A(c->step, 1);
   A(c->beta_pow, 2);
+  A(c->gbar, 2);
   A(c->done_ctr, 1);
   A(c->err, 1);
   A(c->sq, std::max(4096, reduce_blocks(s)));
@@ -528,6 +646,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   }
 #undef A
   if (c->bf16 && tc_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
+  if (c->use_mk && mk_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (h_init_params) {
     if (cudaMemcpy(c->params, h_init_params, sizeof(float) * P, cudaMemcpyHostToDevice) !=
         cudaSuccess)
@@ -625,6 +744,11 @@ ppo_status ppo_minibatch_loss_grad(ppo_ctx* c, const float* obs, const int32_t* 
                                    const float* adv_stats, float* stats6, cudaStream_t st) {
   TRY(check_minibatch_args(c, obs, act, actc, logp_old, adv, ret, idx, B, mb));
   if ((adv_stats && !al16(adv_stats)) || (stats6 && !al16(stats6))) return PPO_ERR_ALIGN;
+  if (c->use_mk) {
+    PPO_CUDA(cudaMemsetAsync(c->gbar, 0, 2 * sizeof(unsigned), st));
+    return enqueue_minibatch_mk(c, obs, nullptr, act, actc, logp_old, adv, ret, idx, B, mb,
+                                adv_stats, stats6, 0, 0.f, st);
+  }
   return enqueue_minibatch(c, obs, nullptr, act, actc, logp_old, adv, ret, idx, B, mb, adv_stats,
                            stats6, st);
 }
@@ -710,7 +834,8 @@ const char* ppo_stage_name(int32_t stage) {
   static const char* names[ST_COUNT] = {
       "pack_obs", "gae_scan", "gae_finalize", "gae_normalize", "perm_hist", "perm_scan",
       "perm_scatter", "gather", "fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm",
-      "dact1_gemm", "wgrad_gemm", "grad_reduce", "grad_sqnorm", "adam", "weight_shadows"};
+      "dact1_gemm", "wgrad_gemm", "grad_reduce", "grad_sqnorm", "adam", "weight_shadows",
+      "minibatch_persistent"};
   if (stage < 0 || stage >= ST_COUNT) return "unknown";
   return names[stage];
 }
@@ -734,7 +859,7 @@ ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
   TRY(check_update_args(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
                         minibatches, stats));
   if (!h_stage_ms || !h_stage_launches || st == nullptr) return PPO_ERR_INVALID;
-  const size_t need = 8 + 3 * 4 * (size_t)epochs + 20 * (size_t)epochs * minibatches;
+  const size_t need = 8 + 3 * 4 + 20 * (size_t)epochs * minibatches;
   while (c->prof_events.size() < need) {
     cudaEvent_t e;
     PPO_CUDA(cudaEventCreate(&e));

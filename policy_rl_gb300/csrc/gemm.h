@@ -150,6 +150,38 @@ struct AdamArgs {
   Shadows sh;
 };
 cudaError_t launch_adam(const AdamArgs& a, cudaStream_t st, const Trace* tr = nullptr);
+
+// ---- persistent minibatch kernel (mk.cu) ------------------------------------
+// Everything the fused bf16 minibatch step needs: the five K-major GEMMs, the
+// three weight-gradient regions, gradient assembly and (optionally) Adam.
+struct MkLaunch {
+  NetShape s;
+  GatherArgs ga;
+  GemmOperands fwd1, fwd2, loss, dact2, dact1;
+  const float *b1, *b2, *b3, *logstd;
+  __nv_bfloat16 *H1, *H2, *dP2, *dP1, *dz;
+  int lddz;
+  float *cs1, *cs2, *cs3, *loss_part;   // per-CTA partial rows [grid][...]
+  WGradRegion wg[3];
+  int rows;                             // minibatch rows
+  ReduceArgs ra;
+  int do_adam;
+  AdamArgs aa;
+  LossCoef lc;
+  LossRows rows_in;
+  float inv_mb;
+  unsigned* gbar;                       // [2] grid-barrier counters (zero between launches)
+  double* sq_part;                      // [grid]
+  int* err;
+  uint64_t timeout_ns;
+  int grid;
+};
+cudaError_t mk_prepare();
+int mk_grid(int num_sms);
+int mk_wgrad_bn(int N);
+cudaError_t mk_launch(const MkLaunch& L, cudaStream_t st);
+cudaError_t tc_make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
+                         int box_cols, int box_rows);
 cudaError_t launch_shadows(const float* p, const NetShape& s, const Shadows& sh, cudaStream_t st);
 
 }  // namespace ppo

@@ -28,19 +28,16 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "tc_ptx.cuh"
+#include "tc_tile.cuh"
 
 namespace ppo {
 
 namespace {
 
 using namespace ptx;
+using namespace tc;
 
-constexpr int BM = 128;
-constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle atom row
 constexpr int kThreads = 192;
-constexpr int kColsumCap = 512;
-
-enum Epi { EPI_BIAS_ACT = 0, EPI_DACT = 1, EPI_LOSS = 2 };
 
 template <int BN>
 struct Cfg {
@@ -54,57 +51,7 @@ struct Cfg {
                                  4 * kLossPartials * 4 + kColsumCap * 4;
 };
 
-struct Guard {
-  volatile int* abort;
-  int* err;
-  uint64_t limit_ns;
-};
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Guard& g) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*g.abort) return false;
-    if (globaltimer() - t0 > g.limit_ns) {
-      *g.abort = 1;
-      atomicOr(g.err, kDevTimeout);
-      return false;
-    }
-  }
-}
-
-// wait used while draining after an abort: never sets the abort flag again
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > limit_ns) return;
-}
-
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&y)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 u;
-    u.x = pack_bf16x2(y[8 * i + 0], y[8 * i + 1]);
-    u.y = pack_bf16x2(y[8 * i + 2], y[8 * i + 3]);
-    u.z = pack_bf16x2(y[8 * i + 4], y[8 * i + 5]);
-    u.w = pack_bf16x2(y[8 * i + 6], y[8 * i + 7]);
-    d[i] = u;
-  }
-}
-
-struct Ctrl {
-  uint64_t* bars;
-  int S;
-  __device__ uint32_t full(int s) const { return smem_u32(&bars[s]); }
-  __device__ uint32_t empty(int s) const { return smem_u32(&bars[S + s]); }
-  __device__ uint32_t tfull(int a) const { return smem_u32(&bars[2 * S + a]); }
-  __device__ uint32_t tempty(int a) const { return smem_u32(&bars[2 * S + 2 + a]); }
-  __device__ uint32_t drain() const { return smem_u32(&bars[2 * S + 4]); }
-};
 
 // ---------------------------------------------------------------------------
 // Epilogue warps: 8 (two per TMEM lane quarter, splitting the tile's
@@ -128,7 +75,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint8_t* gbase = smem_raw + (base - raw);
   uint8_t* ctrl = gbase + (size_t)S * C::STAGE;
   Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), S};
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * S + 5));
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * Ctrl::count(S));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);  // issued, consumed
   float* cs = reinterpret_cast<float*>(ctrl + C::CTRL);                      // [4][kColsumCap]
@@ -246,111 +193,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const bool rok = row < p.M;
       const uint32_t taddr = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       if constexpr (EPI == EPI_LOSS) {
-        float v[32];
-        if constexpr (BN == 16) tmem_ld16(taddr, v);
-        else tmem_ld32(taddr, v);
-        float z[32], dz[32], t6[6], dls[4];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          z[j] = (j < p.shape.C) ? v[j] + bias_s[j] : 0.f;
-          dz[j] = 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 6; ++k) t6[k] = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) dls[k] = 0.f;
-        if (rok)
-          row_loss(p.shape, p.lc, p.inv_mb, z, p.rows.act + (int64_t)row * p.shape.NH,
-                   p.rows.actc + (int64_t)row * p.shape.G, p.logstd, p.rows.logp_old[row],
-                   p.rows.adv[row], p.rows.ret[row], dz, t6, dls);
-        if (rok) {
-          uint4* d = reinterpret_cast<uint4*>(p.dz + (int64_t)row * p.lddz);
-#pragma unroll
-          for (int i = 0; i < BN / 8; ++i) {
-            uint4 u;
-            u.x = pack_bf16x2(dz[8 * i + 0], dz[8 * i + 1]);
-            u.y = pack_bf16x2(dz[8 * i + 2], dz[8 * i + 3]);
-            u.z = pack_bf16x2(dz[8 * i + 4], dz[8 * i + 5]);
-            u.w = pack_bf16x2(dz[8 * i + 6], dz[8 * i + 7]);
-            d[i] = u;
-          }
-        }
-        const float colsum = warp_reduce_scatter32(dz);
-        cs[q * kColsumCap + lane] += colsum;
-#pragma unroll
-        for (int k = 0; k < 6; ++k) {
-          const float s6 = warp_sum(t6[k]);
-          if (lane == 0) lp[q * kLossPartials + k] += s6;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float s4 = warp_sum(dls[k]);
-          if (lane == 0) lp[q * kLossPartials + 6 + k] += s4;
-        }
+        epi_loss_tile<BN>(taddr, row, rok, p.shape, p.lc, p.inv_mb, p.rows, p.logstd, bias_s,
+                          p.dz, p.lddz, cs + q * kColsumCap, lp + q * kLossPartials, lane);
       } else {
-        // software pipeline over 32-column chunks: the TMEM load (and the
-        // activation operand) of chunk c+1 are in flight while chunk c is
-        // processed and stored
-        // two register buffers, alternated by chunk parity (the loop is fully
-        // unrolled, so the index is a compile-time constant): the registers of
-        // an asynchronous TMEM load are read only after their own wait
-        constexpr int PART = BN / (EW / 4);   // columns per epilogue warp
-        constexpr int NCH = PART / 32;
-        const int cbase = h * PART;
-        uint32_t r[2][32];
-        uint4 ax[2][4];
-        const __nv_bfloat16* auxrow = p.aux + (int64_t)row * p.ldaux + tn * BN + cbase;
-        tmem_ld32_async(taddr + (uint32_t)cbase, r[0]);
-        if constexpr (EPI == EPI_DACT) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            ax[0][i] = rok ? __ldg(reinterpret_cast<const uint4*>(auxrow) + i)
-                           : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < NCH; ++k) {
-          const int cur = k & 1, nxt = cur ^ 1;
-          const int c0 = cbase + 32 * k;
-          tmem_wait_ld(r[cur]);
-          if (k + 1 < NCH) {
-            tmem_ld32_async(taddr + (uint32_t)(c0 + 32), r[nxt]);
-            if constexpr (EPI == EPI_DACT) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                ax[nxt][i] = rok ? __ldg(reinterpret_cast<const uint4*>(auxrow + 32 * (k + 1)) + i)
-                                 : make_uint4(0, 0, 0, 0);
-            }
-          }
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[cur][j]);
-          const int col0 = tn * BN + c0;
-          if constexpr (EPI == EPI_BIAS_ACT) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float x = v[j] + bias_s[col0 + j];
-              v[j] = p.act == 0 ? tanh_fast(x) : fmaxf(x, 0.f);
-            }
-            if (rok) store_bf16x32(p.out + (int64_t)row * p.ldo + col0, v);
-          } else {  // EPI_DACT
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t w4[4] = {ax[cur][i].x, ax[cur][i].y, ax[cur][i].z, ax[cur][i].w};
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const float2 hv = unpack_bf16x2(w4[h]);
-                const int j = 8 * i + 2 * h;
-                const float d0 = p.act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
-                const float d1 = p.act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
-                v[j] = rok ? v[j] * d0 : 0.f;
-                v[j + 1] = rok ? v[j + 1] * d1 : 0.f;
-              }
-            }
-            if (rok) store_bf16x32(p.out + (int64_t)row * p.ldo + col0, v);
-            const float colsum = warp_reduce_scatter32(v);
-            cs[q * kColsumCap + col0 + lane] += colsum;
-          }
-        }
+        epi_elem_tile<BN, EW, EPI == EPI_DACT>(taddr, row, rok, tn * BN, h, p.act, bias_s, p.aux,
+                                              p.ldaux, p.out, p.ldo, cs + q * kColsumCap, lane);
       }
       tc_fence_before();
       mbar_arrive(cb.tempty(acc));
@@ -429,7 +276,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
   uint8_t* gbase = smem_raw + (base - raw);
   uint8_t* ctrl = gbase + (size_t)WS * W_STAGE;
   Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), WS};
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * WS + 5));
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * Ctrl::count(WS));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -537,17 +384,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
       tc_fence_after();
       const int row = tm * BM + q * 32 + lane;
       const uint32_t taddr = tmem + (uint32_t)(acc * WBN) + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-      for (int c0 = 0; c0 < R.bn; c0 += 32) {
-        float v[32];
-        tmem_ld32(taddr + (uint32_t)c0, v);
-        const int col0 = tn * R.bn + c0;
-        if (row < R.M && col0 < R.N) {
-          float4* dst = reinterpret_cast<float4*>(R.part + ((int64_t)split * R.M + row) * R.N + col0);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        }
-      }
+      epi_wgrad_tile(taddr, row, R.bn, R.M, R.N, tn * R.bn, R.part + (int64_t)split * R.M * R.N);
       tc_fence_before();
       mbar_arrive(cb.tempty(acc));
       ++tc;
@@ -649,6 +486,11 @@ cudaError_t tc_prepare() {
   for (cudaError_t x : errs)
     if (x != cudaSuccess) return x;
   return cudaSuccess;
+}
+
+cudaError_t tc_make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
+                         int box_cols, int box_rows) {
+  return make_tmap(m, base, cols, rows, ld, box_cols, box_rows);
 }
 
 int tc_pick_bn(int N) {

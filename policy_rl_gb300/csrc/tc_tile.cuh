@@ -1,0 +1,222 @@
+// tc_tile.cuh -- pieces shared by the tensor-core kernels (the standalone
+// GEMM kernels and the persistent minibatch kernel): tile constants, bounded
+// mbarrier waits, the shared-memory barrier block, and the per-tile
+// epilogues that drain a TMEM accumulator.
+#pragma once
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace ppo {
+namespace tc {
+
+using namespace ptx;
+
+constexpr int BM = 128;
+constexpr int BK = 64;          // 64 bf16 = 128 bytes = one swizzle atom row
+constexpr int kColsumCap = 512;
+
+enum Epi { EPI_BIAS_ACT = 0, EPI_DACT = 1, EPI_LOSS = 2 };
+
+struct Guard {
+  volatile int* abort;
+  int* err;
+  uint64_t limit_ns;
+};
+
+// Bounded wait on an mbarrier phase: gives up after limit_ns (latching
+// kDevTimeout and the CTA's abort flag) or when another role aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Guard& g) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*g.abort) return false;
+    if (globaltimer() - t0 > g.limit_ns) {
+      *g.abort = 1;
+      atomicOr(g.err, kDevTimeout);
+      return false;
+    }
+  }
+}
+
+// wait used while draining after an abort: never sets the abort flag again
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > limit_ns) return;
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&y)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_bf16x2(y[8 * i + 0], y[8 * i + 1]);
+    u.y = pack_bf16x2(y[8 * i + 2], y[8 * i + 3]);
+    u.z = pack_bf16x2(y[8 * i + 4], y[8 * i + 5]);
+    u.w = pack_bf16x2(y[8 * i + 6], y[8 * i + 7]);
+    d[i] = u;
+  }
+}
+
+// mbarriers of a tensor-core CTA: S smem stages (full/empty), two TMEM
+// accumulators (full/empty), a drain barrier and (persistent kernel) an
+// epilogue-group barrier.
+struct Ctrl {
+  uint64_t* bars;
+  int S;
+  __device__ uint32_t full(int s) const { return smem_u32(&bars[s]); }
+  __device__ uint32_t empty(int s) const { return smem_u32(&bars[S + s]); }
+  __device__ uint32_t tfull(int a) const { return smem_u32(&bars[2 * S + a]); }
+  __device__ uint32_t tempty(int a) const { return smem_u32(&bars[2 * S + 2 + a]); }
+  __device__ uint32_t drain() const { return smem_u32(&bars[2 * S + 4]); }
+  __device__ uint32_t epi() const { return smem_u32(&bars[2 * S + 5]); }
+  __host__ __device__ static constexpr int count(int S) { return 2 * S + 6; }
+};
+
+// Element-wise epilogue of one 128 x BN tile for one epilogue warp: TMEM lane
+// quarter (the warp's rows), columns [h*PART, (h+1)*PART) of the tile.
+//   DACT = false: out = act(acc + bias)                          (forward)
+//   DACT = true : out = acc * act'(aux); per-warp column sums into cs_q
+// The TMEM load (and the aux operand) of chunk k+1 are in flight while chunk
+// k is processed; the two register buffers alternate by chunk parity (the
+// loop is fully unrolled, so the index is a compile-time constant) and each
+// buffer is read only after its own wait.
+template <int BN, int EW, bool DACT>
+__device__ __forceinline__ void epi_elem_tile(uint32_t taddr, int row, bool rok, int col_tile,
+                                              int h, int act, const float* bias_s,
+                                              const __nv_bfloat16* aux, int ldaux,
+                                              __nv_bfloat16* out, int ldo, float* cs_q,
+                                              int lane) {
+  constexpr int PART = BN / (EW / 4);   // columns per epilogue warp
+  constexpr int NCH = PART / 32;
+  const int cbase = h * PART;
+  uint32_t r[2][32];
+  uint4 ax[2][4];
+  const __nv_bfloat16* auxrow = DACT ? aux + (int64_t)row * ldaux + col_tile + cbase : nullptr;
+  tmem_ld32_async(taddr + (uint32_t)cbase, r[0]);
+  if constexpr (DACT) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      ax[0][i] = rok ? __ldg(reinterpret_cast<const uint4*>(auxrow) + i) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int k = 0; k < NCH; ++k) {
+    const int cur = k & 1, nxt = cur ^ 1;
+    const int c0 = cbase + 32 * k;
+    tmem_wait_ld(r[cur]);
+    if (k + 1 < NCH) {
+      tmem_ld32_async(taddr + (uint32_t)(c0 + 32), r[nxt]);
+      if constexpr (DACT) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          ax[nxt][i] = rok ? __ldg(reinterpret_cast<const uint4*>(auxrow + 32 * (k + 1)) + i)
+                           : make_uint4(0, 0, 0, 0);
+      }
+    }
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[cur][j]);
+    const int col0 = col_tile + c0;
+    if constexpr (!DACT) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float x = v[j] + bias_s[col0 + j];
+        v[j] = act == 0 ? tanh_fast(x) : fmaxf(x, 0.f);
+      }
+      if (rok) store_bf16x32(out + (int64_t)row * ldo + col0, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w4[4] = {ax[cur][i].x, ax[cur][i].y, ax[cur][i].z, ax[cur][i].w};
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          const float2 hv = unpack_bf16x2(w4[hh]);
+          const int j = 8 * i + 2 * hh;
+          const float d0 = act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
+          const float d1 = act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
+          v[j] = rok ? v[j] * d0 : 0.f;
+          v[j + 1] = rok ? v[j + 1] * d1 : 0.f;
+        }
+      }
+      if (rok) store_bf16x32(out + (int64_t)row * ldo + col0, v);
+      const float colsum = warp_reduce_scatter32(v);
+      cs_q[col0 + lane] += colsum;
+    }
+  }
+}
+
+// Loss epilogue of one 128 x BN (BN = CP = 16 or 32) head tile for one warp:
+// z = acc + b3 -> per-row PPO loss -> dz (bf16 row, CP columns), column sums
+// of dz into cs_q, loss terms and dlogstd into lp_q.
+template <int BN>
+__device__ __forceinline__ void epi_loss_tile(uint32_t taddr, int row, bool rok, const NetShape& s,
+                                              const LossCoef& lc, float inv_mb,
+                                              const LossRows& rows, const float* logstd,
+                                              const float* bias_s, __nv_bfloat16* dz, int lddz,
+                                              float* cs_q, float* lp_q, int lane) {
+  float v[32];
+  if constexpr (BN == 16) tmem_ld16(taddr, v);
+  else tmem_ld32(taddr, v);
+  float z[32], dzr[32], t6[6], dls[4];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    z[j] = (j < s.C) ? v[j] + bias_s[j] : 0.f;
+    dzr[j] = 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < 6; ++k) t6[k] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) dls[k] = 0.f;
+  if (rok)
+    row_loss(s, lc, inv_mb, z, rows.act + (int64_t)row * s.NH, rows.actc + (int64_t)row * s.G,
+             logstd, rows.logp_old[row], rows.adv[row], rows.ret[row], dzr, t6, dls);
+  if (rok) {
+    uint4* d = reinterpret_cast<uint4*>(dz + (int64_t)row * lddz);
+#pragma unroll
+    for (int i = 0; i < BN / 8; ++i) {
+      uint4 u;
+      u.x = pack_bf16x2(dzr[8 * i + 0], dzr[8 * i + 1]);
+      u.y = pack_bf16x2(dzr[8 * i + 2], dzr[8 * i + 3]);
+      u.z = pack_bf16x2(dzr[8 * i + 4], dzr[8 * i + 5]);
+      u.w = pack_bf16x2(dzr[8 * i + 6], dzr[8 * i + 7]);
+      d[i] = u;
+    }
+  }
+  const float colsum = warp_reduce_scatter32(dzr);
+  cs_q[lane] += colsum;
+#pragma unroll
+  for (int k = 0; k < 6; ++k) {
+    const float s6 = warp_sum(t6[k]);
+    if (lane == 0) lp_q[k] += s6;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float s4 = warp_sum(dls[k]);
+    if (lane == 0) lp_q[6 + k] += s4;
+  }
+}
+
+// Weight-gradient epilogue: the fp32 accumulator of one 128 x bn unit tile
+// goes to its split-K partial (rows < M, columns < N).
+__device__ __forceinline__ void epi_wgrad_tile(uint32_t taddr, int row, int bn, int M, int N,
+                                               int col_tile, float* part_split) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < bn; c0 += 32) {
+    float v[32];
+    tmem_ld32(taddr + (uint32_t)c0, v);
+    const int col0 = col_tile + c0;
+    if (row < M && col0 < N) {
+      float4* dst = reinterpret_cast<float4*>(part_split + (int64_t)row * N + col0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+  }
+}
+
+}  // namespace tc
+}  // namespace ppo

@@ -49,13 +49,13 @@ def test_adam_step_matches_oracle(prec, max_norm):
     ctx.close()
 
 
-def _update(w, seed=0, host_api=False):
+def _update(w, seed=0, host_api=False, per_stage=0):
     import torch
     import policy_rl_gb300 as P
     ro = synth.rollout(w, seed=seed)
     p0 = synth.init_params(w, seed=seed)
     ro.logp_old = conditioned_logp_old(w, ro, p0)
-    ctx = P.Context(P.config_from_workload(w), p0)
+    ctx = P.Context(P.config_from_workload(w, per_stage_kernels=per_stage), p0)
     E, M = w.epochs, w.minibatches
     if host_api:
         stats = np.zeros((E * M, 6), np.float32)
@@ -91,9 +91,10 @@ def test_tiny_update_fp32(host_api):
     np.testing.assert_allclose(stats[:, 2:4], ref.stats[:, 2:4], rtol=1e-4)
 
 
-def test_small_update_bf16():
+@pytest.mark.parametrize("per_stage", [0, 1])
+def test_small_update_bf16(per_stage):
     w = synth.WORKLOADS["mario"].scaled(T=16, N=256, epochs=2, minibatches=4)
-    p0, p, stats, step, ref = _update(w)
+    p0, p, stats, step, ref = _update(w, per_stage=per_stage)
     assert step == 8
     e = normwise(p - p0, ref.params - p0)
     assert e <= 0.1, e
