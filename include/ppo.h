@@ -225,8 +225,13 @@ ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_ac
                            cudaStream_t stream);
 
 /* ---- Profiling -----------------------------------------------------------------
- * The library's kernels, by stage; one stage entry is one kernel launch. */
-#define PPO_NUM_STAGES 19
+ * The library's kernels, by stage; one stage entry is one kernel launch.
+ * Entries PPO_NUM_KERNEL_STAGES .. PPO_NUM_STAGES-1 ("phase:*") are the
+ * phases inside the persistent minibatch kernel (time between the phase
+ * starts seen by its first CTA, summed over minibatches); they are not
+ * separate launches. */
+#define PPO_NUM_KERNEL_STAGES 19
+#define PPO_NUM_STAGES 28
 /* Name of a stage (static string; "unknown" outside [0, PPO_NUM_STAGES)). */
 const char *ppo_stage_name(int32_t stage);
 
@@ -236,7 +241,8 @@ const char *ppo_stage_name(int32_t stage);
  * the summed device time in milliseconds (h_stage_ms[PPO_NUM_STAGES], HOST)
  * and the number of launches (h_stage_launches[PPO_NUM_STAGES], HOST).  A
  * launch's time is the interval since the previous kernel's event, so it
- * includes its own launch gap.  Synchronous; `stream` must not be the legacy
+ * includes its own launch gap.  Phase entries hold times within the
+ * persistent kernel's launches.  Synchronous; `stream` must not be the legacy
  * default stream. */
 ppo_status ppo_update_profile(ppo_ctx *ctx, const float *d_obs, const int32_t *d_act_disc,
                               const float *d_act_cont, const float *d_logp_old,

@@ -22,7 +22,8 @@ SYMBOLS = (
     "ppo_adam_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
     "ppo_sync_status",
 )
-NUM_STAGES = 19
+NUM_STAGES = 28
+NUM_KERNEL_STAGES = 19
 
 STATUS = {0: "PPO_OK", 1: "PPO_ERR_INVALID", 2: "PPO_ERR_ALIGN", 3: "PPO_ERR_CUDA",
           4: "PPO_ERR_UNSUPPORTED", 5: "PPO_ERR_TIMEOUT", 6: "PPO_ERR_NOMEM"}

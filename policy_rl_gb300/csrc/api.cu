@@ -49,6 +49,8 @@ struct ppo_ctx {
   int use_mk = 0;        // bf16: one persistent kernel per minibatch
   int num_sms = 1;
   unsigned* gbar = nullptr;
+  unsigned long long* phase_ns = nullptr;   // persistent-kernel phase times (profiling)
+  bool profiling = false;
   std::vector<void*> allocs;
 
   float *params = nullptr, *grad = nullptr, *m = nullptr, *v = nullptr;
@@ -466,6 +468,7 @@ ppo_status enqueue_minibatch_mk(ppo_ctx* c, const float* obs, const __nv_bfloat1
   L.inv_mb = 1.0f / (float)mb;
   L.gbar = c->gbar;
   L.sq_part = c->sq;
+  L.phase_ns = c->profiling ? c->phase_ns : nullptr;
   L.err = c->err;
   L.timeout_ns = kTimeoutNs;
   L.grid = grid;
@@ -585,6 +588,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->step, 1);
   A(c->beta_pow, 2);
   A(c->gbar, 2);
+  A(c->phase_ns, kMkPhases);
   A(c->done_ctr, 1);
   A(c->err, 1);
   A(c->sq, std::max(4096, reduce_blocks(s)));
@@ -836,6 +840,10 @@ const char* ppo_stage_name(int32_t stage) {
       "perm_scatter", "gather", "fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm",
       "dact1_gemm", "wgrad_gemm", "grad_reduce", "grad_sqnorm", "adam", "weight_shadows",
       "minibatch_persistent"};
+  static const char* phases[kMkPhases] = {
+      "phase:gather", "phase:fwd1", "phase:fwd2", "phase:head_loss", "phase:dact2",
+      "phase:dact1", "phase:wgrad", "phase:grad_reduce", "phase:adam"};
+  if (stage >= ST_COUNT && stage < ST_COUNT + kMkPhases) return phases[stage - ST_COUNT];
   if (stage < 0 || stage >= ST_COUNT) return "unknown";
   return names[stage];
 }
@@ -866,6 +874,8 @@ ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
     c->prof_events.push_back(e);
   }
   c->prof_stages.clear();
+  PPO_CUDA(cudaMemsetAsync(c->phase_ns, 0, kMkPhases * sizeof(unsigned long long), st));
+  c->profiling = true;
   PPO_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
   PPO_CUDA(cudaEventRecordWithFlags(c->prof_events[0], st, cudaEventRecordExternal));
   c->tr.fn = prof_mark;
@@ -873,6 +883,7 @@ ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
   ppo_status r = enqueue_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
                                 minibatches, gamma, lambda, lr, seed, stats, st);
   c->tr = Trace{};
+  c->profiling = false;
   cudaGraph_t graph = nullptr;
   cudaError_t e = cudaStreamEndCapture(st, &graph);
   if (r != PPO_OK) {
@@ -889,7 +900,7 @@ ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   cudaGraphExecDestroy(exec);
   if (e != cudaSuccess) return PPO_ERR_CUDA;
-  for (int k = 0; k < ST_COUNT; ++k) {
+  for (int k = 0; k < ST_COUNT + kMkPhases; ++k) {
     h_stage_ms[k] = 0.f;
     h_stage_launches[k] = 0;
   }
@@ -898,6 +909,15 @@ ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
     PPO_CUDA(cudaEventElapsedTime(&ms, c->prof_events[i], c->prof_events[i + 1]));
     h_stage_ms[c->prof_stages[i]] += ms;
     h_stage_launches[c->prof_stages[i]] += 1;
+  }
+  if (c->use_mk) {   // phases of the persistent kernel, as seen by its first CTA
+    unsigned long long ns[kMkPhases];
+    PPO_CUDA(cudaMemcpy(ns, c->phase_ns, sizeof ns, cudaMemcpyDeviceToHost));
+    const int nmb = h_stage_launches[ST_MINIBATCH];
+    for (int k = 0; k < kMkPhases; ++k) {
+      h_stage_ms[ST_COUNT + k] = (float)(ns[k] * 1e-6);
+      h_stage_launches[ST_COUNT + k] = k == kMkPhases - 1 && c->cfg.max_grad_norm < -1.f ? 0 : nmb;
+    }
   }
   return PPO_OK;
 }

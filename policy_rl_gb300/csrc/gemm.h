@@ -172,10 +172,12 @@ struct MkLaunch {
   float inv_mb;
   unsigned* gbar;                       // [2] grid-barrier counters (zero between launches)
   double* sq_part;                      // [grid]
+  unsigned long long* phase_ns;         // nullable: per-phase time sums (profiling)
   int* err;
   uint64_t timeout_ns;
   int grid;
 };
+constexpr int kMkPhases = 9;   // gather, fwd1, fwd2, loss, dact2, dact1, wgrad, reduce, adam
 cudaError_t mk_prepare();
 int mk_grid(int num_sms);
 int mk_wgrad_bn(int N);

@@ -79,6 +79,7 @@ struct MkParams {
   int lddz;
   unsigned* gbar;           // [0] phase arrivals, [1] exits
   double* sq_part;          // [grid]
+  unsigned long long* phase_ns;   // nullable: per-phase time accumulators (profiling)
   int* err;
   uint64_t timeout_ns;
 };
@@ -288,7 +289,7 @@ __device__ __forceinline__ void decode_unit(const WParams& w, int u, int& reg, i
 }
 
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kMkThreads, 1)
+__global__ void __maxnreg__(200)
 mk_kernel(const __grid_constant__ MkMaps maps, const MkParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -468,8 +469,19 @@ mk_kernel(const __grid_constant__ MkMaps maps, const MkParams p) {
       }
       return true;
     };
+    // profiling: CTA 0 adds the time between consecutive phase starts
+    const bool timing = p.phase_ns != nullptr && blockIdx.x == 0 && et == 0;
+    uint64_t t_prev = timing ? globaltimer() : 0;
+    auto stamp = [&](int ph) {
+      if (timing) {
+        const uint64_t now = globaltimer();
+        p.phase_ns[ph] += now - t_prev;
+        t_prev = now;
+      }
+    };
     auto phase_begin = [&](int ph) -> bool {
       if (et == 0 && !grid_wait(gbar, (unsigned)ph * G, g)) return false;
+      stamp(ph - 1);
       return epi_sync();
     };
 
@@ -593,6 +605,7 @@ mk_kernel(const __grid_constant__ MkMaps maps, const MkParams p) {
         if (ok) phase_adam(p.aa, et, red[kEW + 0], red[kEW + 1], red[kEW + 2]);
         if (ok) ok = epi_sync();
         if (ok && et == 0) {
+          stamp(8);
           // the last CTA out advances the step, the beta powers, and resets
           // the barrier counters for the next launch
           __threadfence();
@@ -609,6 +622,7 @@ mk_kernel(const __grid_constant__ MkMaps maps, const MkParams p) {
         }
       }
     } else if (ok && et == 0) {
+      stamp(7);
       __threadfence();
       const unsigned prev = atomicAdd(gbar + 1, 1u);
       if (prev == G - 1) {
@@ -698,7 +712,7 @@ cudaError_t mk_launch(const MkLaunch& L, cudaStream_t st) {
     WRegion& R = p.w.r[r];
     R.M = G.M;
     R.N = G.N;
-    R.bn = G.N % 256 == 0 ? 256 : (G.N % 128 == 0 ? 128 : 64);
+    R.bn = G.N % 128 == 0 ? 128 : 64;
     R.tiles_m = G.M / BM;
     R.tiles_n = G.N / R.bn;
     R.k_tiles = (L.rows + BK - 1) / BK;
@@ -721,6 +735,7 @@ cudaError_t mk_launch(const MkLaunch& L, cudaStream_t st) {
   p.lddz = L.lddz;
   p.gbar = L.gbar;
   p.sq_part = L.sq_part;
+  p.phase_ns = L.phase_ns;
   p.err = L.err;
   p.timeout_ns = L.timeout_ns;
 
@@ -737,7 +752,6 @@ cudaError_t mk_launch(const MkLaunch& L, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, mk_kernel, maps, p);
 }
 
-// the weight-gradient split used by the persistent kernel: BN up to 256
-int mk_wgrad_bn(int N) { return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64); }
+int mk_wgrad_bn(int N) { return N % 128 == 0 ? 128 : 64; }
 
 }  // namespace ppo
