@@ -20,7 +20,8 @@
 // (async-proxy) reads see the epilogues' generic-proxy stores.  Every wait --
 // mbarrier or grid barrier -- is bounded (globaltimer); on expiry the kernel
 // latches kDevTimeout and unwinds.  The launch is cooperative, so all CTAs
-// are co-resident.
+// are co-resident.  Ten warps per CTA put three warps on two of the SM's four
+// 16K-register partitions, which caps a thread at 168 registers.
 #include "common.cuh"
 #include "gemm.h"
 #include "tc_ptx.cuh"
@@ -289,7 +290,7 @@ __device__ __forceinline__ void decode_unit(const WParams& w, int u, int& reg, i
 }
 
 // ---------------------------------------------------------------------------
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kMkThreads, 1)
 mk_kernel(const __grid_constant__ MkMaps maps, const MkParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
