@@ -79,10 +79,11 @@ typedef struct {
     int64_t max_batch;           /* largest T*N given to ppo_update          */
     int64_t max_minibatch;       /* largest minibatch row count              */
     int32_t max_epochs;          /* largest epoch count given to ppo_update  */
-    int32_t per_stage_kernels;   /* bf16 mode: 0 (default) runs a minibatch
-                                    step as one persistent cooperative kernel
-                                    (stages separated by grid barriers); 1
-                                    launches one kernel per stage.  Same
+    int32_t persistent_minibatch; /* bf16 mode: 0 (default) launches one kernel
+                                    per stage of a minibatch step; 1 runs the
+                                    whole step (gather .. Adam) as one
+                                    persistent cooperative kernel whose stages
+                                    are separated by grid barriers.  Same
                                     results up to fp32 summation order.      */
 } ppo_config;
 

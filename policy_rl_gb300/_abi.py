@@ -44,7 +44,7 @@ class PpoConfig(ctypes.Structure):
         ("ent_coef", ctypes.c_float), ("max_grad_norm", ctypes.c_float),
         ("beta1", ctypes.c_double), ("beta2", ctypes.c_double), ("adam_eps", ctypes.c_double),
         ("max_batch", ctypes.c_int64), ("max_minibatch", ctypes.c_int64),
-        ("max_epochs", ctypes.c_int32), ("per_stage_kernels", ctypes.c_int32),
+        ("max_epochs", ctypes.c_int32), ("persistent_minibatch", ctypes.c_int32),
     ]
 
 

@@ -565,7 +565,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   c->cfg = *cfg;
   c->s = s;
   c->bf16 = cfg->precision == 1;
-  c->use_mk = c->bf16 && cfg->per_stage_kernels == 0;
+  c->use_mk = c->bf16 && cfg->persistent_minibatch != 0;
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (c->num_sms < 1) c->num_sms = 1;
   c->mbmax = cfg->max_minibatch;

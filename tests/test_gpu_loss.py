@@ -38,7 +38,7 @@ def _inputs(w, seed=0):
 def _gpu_grad(w, ro, p0, adv, ret, idx, adv_stats=None, repeat=1, per_stage=0):
     import torch
     import policy_rl_gb300 as P
-    cfg = P.config_from_workload(w, max_minibatch=max(len(idx), 1), per_stage_kernels=per_stage)
+    cfg = P.config_from_workload(w, max_minibatch=max(len(idx), 1), persistent_minibatch=1 - per_stage)
     ctx = P.Context(cfg, p0)
     st6 = torch.zeros(8, device="cuda")
     args = [dev(ro.obs), dev(ro.act_disc), dev(ro.act_cont), dev(ro.logp_old), dev(adv),

@@ -55,7 +55,7 @@ def _update(w, seed=0, host_api=False, per_stage=0):
     ro = synth.rollout(w, seed=seed)
     p0 = synth.init_params(w, seed=seed)
     ro.logp_old = conditioned_logp_old(w, ro, p0)
-    ctx = P.Context(P.config_from_workload(w, per_stage_kernels=per_stage), p0)
+    ctx = P.Context(P.config_from_workload(w, persistent_minibatch=1 - per_stage), p0)
     E, M = w.epochs, w.minibatches
     if host_api:
         stats = np.zeros((E * M, 6), np.float32)
