@@ -167,20 +167,52 @@ ppo_status shape_from(const ppo_config* c, NetShape* s) {
   return PPO_OK;
 }
 
-// K-split length (64-row k-tiles) of the weight-gradient units, chosen so
-// that the units of all three products have roughly equal cost and number
-// about the SM count (one unit per CTA), with at least 8 k-tiles per unit.
+// K-split length (64-row k-tiles) of the persistent kernel's weight-gradient
+// units (at most 128 columns), chosen so that the units of all three products
+// have roughly equal cost and number about the SM count, with at least 8
+// k-tiles per unit.  In 128-column units: 64-column regions take twice as many.
 int wgrad_kt_per_split(const NetShape& s, int64_t mb, int num_sms) {
   const int64_t kt = (mb + 63) / 64;
-  auto tiles = [](int M, int N) {
-    const int bn = N % 128 == 0 ? 128 : 64;
-    return (double)(M / 128) * (N / bn) * (bn / 128.0);
-  };
+  auto tiles = [](int M, int N) { return (double)(M / 128) * (N / 128.0); };
   const double cost = (tiles(s.H2, s.H1) + tiles(s.H1, s.Dp) + tiles(s.H2, 64)) * (double)kt;
   int per = (int)std::ceil(cost / (double)num_sms);
   if (per < 8) per = 8;
   if ((kt + per - 1) / per > kMaxSplit) per = (int)((kt + kMaxSplit - 1) / kMaxSplit);
   return per;
+}
+
+// Split plan of the standalone weight-gradient kernel (256/128/64-column
+// tiles).  At large minibatches the kernel streams its operands (each unit
+// reads (128 + bn) features of every row in its k-range) and the tensor pipe
+// is not the limit, so units are balanced by the bytes they load: a region of
+// bn-column tiles gets q / (128 + bn) k-tiles per unit.  q is the smallest
+// budget whose units fit in one wave of num_sms CTAs (a second, partial wave
+// would double the kernel's time); every unit covers at least 4 k-tiles.
+struct WgradPlan {
+  int kt[3];   // k-tiles per unit: W2 (H2 x H1), W1 (H1 x Dp), W3 (H2 x 64)
+};
+
+WgradPlan wgrad_plan(const NetShape& s, int64_t mb, int num_sms) {
+  const int64_t kt = (mb + 63) / 64;
+  const int regs[3][2] = {{s.H2, s.H1}, {s.H1, s.Dp}, {s.H2, 64}};
+  double total = 0;
+  for (const auto& r : regs)
+    total += (double)(r[0] / 128) * (r[1] / tc_wgrad_bn(r[1])) * (128 + tc_wgrad_bn(r[1])) * kt;
+  int64_t q = (int64_t)std::ceil(total / num_sms);
+  WgradPlan P{};
+  for (;; q += (q + 15) / 16) {
+    int64_t units = 0;
+    for (int i = 0; i < 3; ++i) {
+      const int bn = tc_wgrad_bn(regs[i][1]);
+      int64_t kp = q / (128 + bn);
+      if (kp < 4) kp = 4;
+      if ((kt + kp - 1) / kp > kMaxSplit) kp = (kt + kMaxSplit - 1) / kMaxSplit;
+      if (kp > kt) kp = kt;
+      P.kt[i] = (int)kp;
+      units += (int64_t)(regs[i][0] / 128) * (regs[i][1] / bn) * ((kt + kp - 1) / kp);
+    }
+    if (units <= num_sms || q >= 1024 * kt) return P;
+  }
 }
 
 ppo_status check_minibatch_args(ppo_ctx* c, const float* obs, const int32_t* act,
@@ -267,14 +299,10 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     PPO_CUDA(tc_gemm_dact(g5, H1, s.H1, s.act, dP1, s.H1, c->cs1, c->err, kTimeoutNs, ns, st, &n1));
     c->tr.mark(ST_DACT1, st);
     // weight gradients, split over the minibatch rows
-    const int per = wgrad_kt_per_split(s, mb, ns);
-    WGradRegion regs[3] = {
-        {dP2, s.H2, s.H2, H1, s.H1, s.H1, s.H1 % 128 == 0 ? per : 2 * per, c->pW2},
-        {dP1, s.H1, s.H1, X, s.Dp, s.Dp, s.Dp % 128 == 0 ? per : 2 * per, c->pW1},
-        {H2, s.H2, s.H2, dZ, c->lddz, 64, 2 * per, c->pW3}};
-    for (auto& r : regs)
-      if (tc_wgrad_splits(M, r.kt_per_split) > kMaxSplit)
-        r.kt_per_split = (int)(((mb + 63) / 64 + kMaxSplit - 1) / kMaxSplit);
+    const WgradPlan wp = wgrad_plan(s, mb, ns);
+    WGradRegion regs[3] = {{dP2, s.H2, s.H2, H1, s.H1, s.H1, wp.kt[0], c->pW2},
+                           {dP1, s.H1, s.H1, X, s.Dp, s.Dp, wp.kt[1], c->pW1},
+                           {H2, s.H2, s.H2, dZ, c->lddz, 64, wp.kt[2], c->pW3}};
     PPO_CUDA(tc_wgrad(regs, 3, M, 8192, 1024, c->err, kTimeoutNs, ns, st));
     c->tr.mark(ST_WGRAD, st);
     ra.pW1 = c->pW1; ra.s1 = tc_wgrad_splits(M, regs[1].kt_per_split); ra.ld1 = s.Dp;
@@ -624,8 +652,8 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->adv_mb, mbm);
   A(c->ret_mb, mbm);
   const int ldW1 = c->bf16 ? s.Dp : s.D;
-  // split-K partials: a split covers at least 16 rows (fp32) / 8 k-tiles (bf16)
-  const int64_t max_split = std::min<int64_t>(kMaxSplit, c->bf16 ? (mbm + 511) / 512 + 1
+  // split-K partials: a split covers at least 16 rows (fp32) / 4 k-tiles (bf16)
+  const int64_t max_split = std::min<int64_t>(kMaxSplit, c->bf16 ? (mbm + 255) / 256 + 1
                                                                    : (mbm + 15) / 16 + 1);
   A(c->pW1, max_split * s.H1 * ldW1);
   A(c->pW2, max_split * s.H2 * s.H1);

@@ -69,6 +69,7 @@ struct WGradRegion {
 cudaError_t tc_prepare();
 int tc_pick_bn(int N);
 int tc_wgrad_splits(int rows, int kt_per_split);
+int tc_wgrad_bn(int N);   // column width of the weight-gradient tiles of an N-column product
 
 cudaError_t tc_gemm_bias_act(const GemmOperands& g, const float* bias, int act,
                              __nv_bfloat16* out, int ldo, int* err, uint64_t timeout_ns,

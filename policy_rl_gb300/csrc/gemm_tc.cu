@@ -39,16 +39,19 @@ using namespace tc;
 
 constexpr int kThreads = 192;
 
-template <int BN>
+template <int BN, int EPI>
 struct Cfg {
-  static constexpr int S = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  // backward-data kernels keep two TMA-loaded activation tiles (aux) too
+  static constexpr int AUX_SLOT = EPI == EPI_DACT ? BM * BN * 2 : 0;
+  static constexpr int S = EPI == EPI_DACT ? (BN >= 128 ? 4 : 6)
+                                          : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   static constexpr int CTRL = 512;
-  static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + CTRL + 4 * kColsumCap * 4 +
-                                 4 * kLossPartials * 4 + kColsumCap * 4;
+  static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + 2 * (size_t)AUX_SLOT + CTRL +
+                                 4 * kColsumCap * 4 + 4 * kLossPartials * 4 + kColsumCap * 4;
 };
 
 
@@ -64,8 +67,8 @@ __host__ __device__ constexpr int gemm_threads() { return 2 * kWarp + kWarp * ep
 template <int BN, int EPI>
 __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const TcParams p) {
-  using C = Cfg<BN>;
+               const __grid_constant__ CUtensorMap tmX, const TcParams p) {
+  using C = Cfg<BN, EPI>;
   constexpr int S = C::S;
   constexpr int EW = epi_warps<EPI>();
   constexpr int NT = gemm_threads<EPI>();
@@ -73,11 +76,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  uint8_t* ctrl = gbase + (size_t)S * C::STAGE;
+  uint8_t* auxs = gbase + (size_t)S * C::STAGE;          // [2][BM x BN] (DACT only)
+  uint8_t* ctrl = auxs + 2 * (size_t)C::AUX_SLOT;
   Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), S};
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * Ctrl::count(S));
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(ctrl) + Ctrl::count(S);  // aux full[2], empty[2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-  volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);  // issued, consumed
+  volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);  // issued, consumed, aux issued
   float* cs = reinterpret_cast<float*>(ctrl + C::CTRL);                      // [4][kColsumCap]
   float* lp = cs + 4 * kColsumCap;                                           // [4][kLossPartials]
   float* bias_s = lp + 4 * kLossPartials;                                    // [kColsumCap]
@@ -96,9 +101,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(cb.tempty(a), EW * kWarp);
     }
     mbar_init(cb.drain(), 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&xbar[a]), 1);
+      mbar_init(smem_u32(&xbar[2 + a]), EW * kWarp);
+    }
     *abort_flag = 0;
     cnt[0] = 0;
     cnt[1] = 0;
+    cnt[2] = 0;
     fence_mbar_init();
   }
   if (EPI != EPI_BIAS_ACT)
@@ -107,6 +117,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (EPI == EPI_DACT) prefetch_tmap(&tmX);
   }
   tc_fence_before();
   __syncthreads();
@@ -125,8 +136,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      uint32_t lt = 0;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++lt) {
         const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
+        if constexpr (EPI == EPI_DACT) {
+          // this tile's activation operand, one slot of two, ahead of its k-loop
+          const int xs = lt & 1;
+          const uint32_t xu = lt >> 1;
+          if (!wait_bar(smem_u32(&xbar[2 + xs]), (xu & 1) ^ 1, g)) { ok = false; break; }
+          mbar_arrive_expect_tx(smem_u32(&xbar[xs]), C::AUX_SLOT);
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(smem_u32(auxs) + (uint32_t)(xs * C::AUX_SLOT + j * 16384), &tmX,
+                        tn * BN + 64 * j, tm * BM, smem_u32(&xbar[xs]));
+          cnt[2] = lt + 1;
+        }
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           const int s = it % S;
           const uint32_t r = it / S;
@@ -192,12 +215,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int row = tm * BM + q * 32 + lane;
       const bool rok = row < p.M;
       const uint32_t taddr = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      if constexpr (EPI == EPI_LOSS) {
+      if constexpr (EPI == EPI_DACT) {
+        // tile tc uses aux slot tc & 1 (same tile order as the producer)
+        const int xs = tc & 1;
+        if (!wait_bar(smem_u32(&xbar[xs]), (tc >> 1) & 1, g)) break;
+        epi_dact_smem_tile<BN, EW>(taddr, q * 32 + lane, row, rok, tn * BN, h, p.act,
+                                   auxs + xs * C::AUX_SLOT, p.out, p.ldo, cs + q * kColsumCap,
+                                   lane);
+        mbar_arrive(smem_u32(&xbar[2 + xs]));
+      } else if constexpr (EPI == EPI_LOSS) {
         epi_loss_tile<BN>(taddr, row, rok, p.shape, p.lc, p.inv_mb, p.rows, p.logstd, bias_s,
                           p.dz, p.lddz, cs + q * kColsumCap, lp + q * kLossPartials, lane);
       } else {
-        epi_elem_tile<BN, EW, EPI == EPI_DACT>(taddr, row, rok, tn * BN, h, p.act, bias_s, p.aux,
-                                              p.ldaux, p.out, p.ldo, cs + q * kColsumCap, lane);
+        epi_elem_tile<BN, EW, false>(taddr, row, rok, tn * BN, h, p.act, bias_s, nullptr, 0,
+                                     p.out, p.ldo, cs + q * kColsumCap, lane);
       }
       tc_fence_before();
       mbar_arrive(cb.tempty(acc));
@@ -212,6 +243,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t issued = cnt[0], consumed = cnt[1];
       for (uint32_t it = consumed; it < issued; ++it)
         drain_wait(cb.full(it % S), (it / S) & 1, p.timeout_ns);
+      const uint32_t xi = cnt[2];   // the last two activation-tile loads
+      for (uint32_t l = xi >= 2 ? xi - 2 : 0; l < xi; ++l)
+        drain_wait(smem_u32(&xbar[l & 1]), (l >> 1) & 1, p.timeout_ns);
     }
     if (warp == 1 && lane == 0) {
       tc_commit(cb.drain());
@@ -242,13 +276,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // ---------------------------------------------------------------------------
 // Weight-gradient kernel: P[M][N] = sum_rows U[row][m] * V[row][n] over a
 // K-split of the minibatch rows; both operands MN-major in shared memory.
-constexpr int WBN = 128;
-constexpr int WS = 6;
-constexpr int W_A_BYTES = BM * BK * 2;   // 2 boxes of 64 features x 64 rows
-constexpr int W_B_BYTES = WBN * BK * 2;  // up to 2 boxes
+constexpr int WBN = 256;
+constexpr int WS = 4;
+constexpr int W_A_BYTES = BM * BK * 2;   // 2 blocks of 64 features x 64 rows
+constexpr int W_B_BYTES = WBN * BK * 2;  // up to 4 blocks
 constexpr int W_STAGE = W_A_BYTES + W_B_BYTES;
 constexpr size_t W_SMEM = 1024 + (size_t)WS * W_STAGE + 512;
-constexpr int W_TMEM_COLS = 256;
+constexpr int W_TMEM_COLS = 512;
 
 __device__ __forceinline__ void decode_unit(const WParams& p, int u, int& reg, int& tm, int& tn,
                                             int& kt0, int& kt1, int& split) {
@@ -323,10 +357,9 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
           const uint32_t r = it / WS;
           if (!wait_bar(cb.empty(s), (r & 1) ^ 1, g)) { ok = false; break; }
           mbar_arrive_expect_tx(cb.full(s), bytes);
-          tma_load_2d(sA(s), tu, tm * BM, kt * BK, cb.full(s));
-          tma_load_2d(sA(s) + 8192, tu, tm * BM + 64, kt * BK, cb.full(s));
-          for (int j = 0; j < bn / 64; ++j)
-            tma_load_2d(sB(s) + 8192 * j, tv, tn * bn + 64 * j, kt * BK, cb.full(s));
+          // one 3-D box per operand: 64 rows x {2, bn/64} blocks of 64 features
+          tma_load_3d(sA(s), tu, 0, kt * BK, tm * (BM / 64), cb.full(s));
+          tma_load_3d(sB(s), tv, 0, kt * BK, tn * (bn / 64), cb.full(s));
           ++it;
           cnt[0] = it;
         }
@@ -440,14 +473,37 @@ cudaError_t make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t ro
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// bf16 row-major [rows][ld] read as 64-feature blocks: x = feature within the
+// block, y = row, z = block (of nblk); box = 64 x box_rows x box_blk.  The
+// box lands in shared memory as box_blk consecutive [box_rows][64] atoms.
+cudaError_t make_tmap_blocks(CUtensorMap* m, const void* base, int64_t rows, int64_t ld, int nblk,
+                             int box_rows, int box_blk) {
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)nblk};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_blk};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int BN, int EPI>
 cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream_t st,
                       int* grid_out) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tx;
   cudaError_t e = make_tmap(&ta, g.A, g.lda, g.M, g.lda, BK, BM);
   if (e != cudaSuccess) return e;
   e = make_tmap(&tb, g.B, g.ldb, g.N, g.ldb, BK, BN);
   if (e != cudaSuccess) return e;
+  tx = ta;
+  if (EPI == EPI_DACT) {   // activation operand [M][N], 128-row x 64-column boxes
+    e = make_tmap(&tx, p.aux, g.N, g.M, p.ldaux, 64, BM);
+    if (e != cudaSuccess) return e;
+  }
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
@@ -459,8 +515,8 @@ cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream
   const int total = p.tiles_m * p.tiles_n;
   const int grid = total < num_sms ? total : num_sms;
   if (grid_out) *grid_out = grid;
-  return launch_pdl(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(gemm_threads<EPI>()), Cfg<BN>::SMEM,
-                    st, ta, tb, p);
+  return launch_pdl(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(gemm_threads<EPI>()),
+                    Cfg<BN, EPI>::SMEM, st, ta, tb, tx, p);
 }
 
 }  // namespace
@@ -468,7 +524,7 @@ cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream
 template <int BN, int EPI>
 cudaError_t set_smem_attr() {
   return cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Cfg<BN>::SMEM);
+                              (int)Cfg<BN, EPI>::SMEM);
 }
 
 // Driver entry point and the shared-memory opt-in of every kernel instance;
@@ -478,8 +534,8 @@ cudaError_t tc_prepare() {
   if (e != cudaSuccess) return e;
   const cudaError_t errs[] = {
       set_smem_attr<256, EPI_BIAS_ACT>(), set_smem_attr<128, EPI_BIAS_ACT>(),
-      set_smem_attr<64, EPI_BIAS_ACT>(),  set_smem_attr<256, EPI_DACT>(),
-      set_smem_attr<128, EPI_DACT>(),     set_smem_attr<64, EPI_DACT>(),
+      set_smem_attr<64, EPI_BIAS_ACT>(),  set_smem_attr<128, EPI_DACT>(),
+      set_smem_attr<64, EPI_DACT>(),
       set_smem_attr<16, EPI_LOSS>(),      set_smem_attr<32, EPI_LOSS>(),
       cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)W_SMEM)};
@@ -532,11 +588,9 @@ cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ld
   p.epi_n = g.N;
   p.err = err;
   p.timeout_ns = timeout_ns;
-  switch (tc_pick_bn(g.N)) {
-    case 256: return launch_tc<256, EPI_DACT>(g, p, num_sms, st, grid_out);
-    case 128: return launch_tc<128, EPI_DACT>(g, p, num_sms, st, grid_out);
-    case 64: return launch_tc<64, EPI_DACT>(g, p, num_sms, st, grid_out);
-  }
+  // at most 128 columns, so that 4 stages and two activation tiles fit
+  if (g.N % 128 == 0) return launch_tc<128, EPI_DACT>(g, p, num_sms, st, grid_out);
+  if (g.N % 64 == 0) return launch_tc<64, EPI_DACT>(g, p, num_sms, st, grid_out);
   return cudaErrorInvalidValue;
 }
 
@@ -577,14 +631,15 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
   int unit = 0;
   for (int r = 0; r < nreg; ++r) {
     const WGradRegion& G = regs[r];
-    cudaError_t e = make_tmap(&tu[r], G.U, G.M, rows, G.ldu, 64, BK);
-    if (e != cudaSuccess) return e;
-    e = make_tmap(&tv[r], G.V, G.N, rows, G.ldv, 64, BK);
-    if (e != cudaSuccess) return e;
+    if (G.M % BM != 0 || G.N % 64 != 0 || G.M > G.ldu || G.N > G.ldv) return cudaErrorInvalidValue;
     WRegion& R = p.r[r];
+    R.bn = tc_wgrad_bn(G.N);
+    cudaError_t e = make_tmap_blocks(&tu[r], G.U, rows, G.ldu, G.M / 64, BK, BM / 64);
+    if (e != cudaSuccess) return e;
+    e = make_tmap_blocks(&tv[r], G.V, rows, G.ldv, G.N / 64, BK, R.bn / 64);
+    if (e != cudaSuccess) return e;
     R.M = G.M;
     R.N = G.N;
-    R.bn = G.N % 128 == 0 ? 128 : 64;
     R.tiles_m = G.M / BM;
     R.tiles_n = G.N / R.bn;
     R.k_tiles = (rows + BK - 1) / BK;
@@ -603,6 +658,8 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
   return launch_pdl(tc_wgrad_kernel, dim3(grid), dim3(kThreads), W_SMEM, st, tu[0], tv[0], tu[1],
                     tv[1], tu[2], tv[2], p);
 }
+
+int tc_wgrad_bn(int N) { return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64); }
 
 int tc_wgrad_splits(int rows, int kt_per_split) {
   const int k_tiles = (rows + BK - 1) / BK;

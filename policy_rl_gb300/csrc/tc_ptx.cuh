@@ -52,6 +52,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// 3-D tiled TMA load (x innermost), completing on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const void* p) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)p) : "memory");
 }

@@ -149,6 +149,52 @@ __device__ __forceinline__ void epi_elem_tile(uint32_t taddr, int row, bool rok,
   }
 }
 
+// Backward-data epilogue with the activation operand already in shared
+// memory: `aux` is a 128 x BN bf16 tile loaded by TMA with the 128-byte
+// swizzle (BN/64 blocks of 128 rows x 128 bytes, 16-byte chunk c of row r at
+// r*128 + ((c ^ (r & 7)) * 16)).  out = acc * act'(aux); per-warp column sums.
+template <int BN, int EW>
+__device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, int row, bool rok,
+                                                   int col_tile, int h, int act,
+                                                   const uint8_t* aux, __nv_bfloat16* out,
+                                                   int ldo, float* cs_q, int lane) {
+  constexpr int PART = BN / (EW / 4);
+  constexpr int NCH = PART / 32;
+  const int cbase = h * PART;
+  uint32_t r[2][32];
+  tmem_ld32_async(taddr + (uint32_t)cbase, r[0]);
+#pragma unroll
+  for (int k = 0; k < NCH; ++k) {
+    const int cur = k & 1, nxt = cur ^ 1;
+    const int c0 = cbase + 32 * k;
+    tmem_wait_ld(r[cur]);
+    if (k + 1 < NCH) tmem_ld32_async(taddr + (uint32_t)(c0 + 32), r[nxt]);
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[cur][j]);
+    const uint8_t* blk = aux + (c0 / 64) * 16384 + rl * 128;
+    const int c16 = (c0 % 64) / 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a4 = *reinterpret_cast<const uint4*>(blk + (((c16 + i) ^ (rl & 7)) << 4));
+      const uint32_t w4[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        const float2 hv = unpack_bf16x2(w4[hh]);
+        const int j = 8 * i + 2 * hh;
+        const float d0 = act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
+        const float d1 = act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
+        v[j] = rok ? v[j] * d0 : 0.f;
+        v[j + 1] = rok ? v[j + 1] * d1 : 0.f;
+      }
+    }
+    const int col0 = col_tile + c0;
+    if (rok) store_bf16x32(out + (int64_t)row * ldo + col0, v);
+    const float colsum = warp_reduce_scatter32(v);
+    cs_q[col0 + lane] += colsum;
+  }
+}
+
 // Loss epilogue of one 128 x BN (BN = CP = 16 or 32) head tile for one warp:
 // z = acc + b3 -> per-row PPO loss -> dz (bf16 row, CP columns), column sums
 // of dz into cs_q, loss terms and dlogstd into lp_q.
