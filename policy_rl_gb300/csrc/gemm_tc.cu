@@ -41,33 +41,39 @@ constexpr int kThreads = 192;
 
 template <int BN, int EPI>
 struct Cfg {
-  // backward-data kernels keep two TMA-loaded activation tiles (aux) too
+  // backward-data kernels keep two TMA-loaded activation tiles (aux), which
+  // also stage their output; forward kernels stage their output per warp
   static constexpr int AUX_SLOT = EPI == EPI_DACT ? BM * BN * 2 : 0;
-  static constexpr int S = EPI == EPI_DACT ? (BN >= 128 ? 4 : 6)
-                                          : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
+  static constexpr int STG_WARP = EPI == EPI_BIAS_ACT ? (BN / 2 / 64) * 4096 : 0;
+  static constexpr int S = EPI == EPI_DACT ? 4
+                         : EPI == EPI_BIAS_ACT ? (BN >= 256 ? 3 : 5)
+                                               : (BN >= 128 ? 6 : 8);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   static constexpr int CTRL = 512;
-  static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + 2 * (size_t)AUX_SLOT + CTRL +
-                                 4 * kColsumCap * 4 + 4 * kLossPartials * 4 + kColsumCap * 4;
+  static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + 2 * (size_t)AUX_SLOT +
+                                 8 * (size_t)STG_WARP + CTRL + 4 * kColsumCap * 4 +
+                                 8 * kLossPartials * 4 + kColsumCap * 4;
 };
 
 
 
 // ---------------------------------------------------------------------------
-// Epilogue warps: 8 (two per TMEM lane quarter, splitting the tile's
-// columns) for the element-wise epilogues, 4 for the per-row loss epilogue.
+// Epilogue warps: 8, two per TMEM lane quarter.  The element-wise epilogues
+// split each tile's columns between the two; the per-row loss epilogue gives
+// the two groups of four warps alternate tiles (one accumulator each).
 template <int EPI>
-__host__ __device__ constexpr int epi_warps() { return EPI == EPI_LOSS ? 4 : 8; }
+__host__ __device__ constexpr int epi_warps() { return 8; }
 template <int EPI>
 __host__ __device__ constexpr int gemm_threads() { return 2 * kWarp + kWarp * epi_warps<EPI>(); }
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmX, const TcParams p) {
+               const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
+               const TcParams p) {
   using C = Cfg<BN, EPI>;
   constexpr int S = C::S;
   constexpr int EW = epi_warps<EPI>();
@@ -77,15 +83,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   uint8_t* auxs = gbase + (size_t)S * C::STAGE;          // [2][BM x BN] (DACT only)
-  uint8_t* ctrl = auxs + 2 * (size_t)C::AUX_SLOT;
+  uint8_t* stgs = auxs + 2 * (size_t)C::AUX_SLOT;        // [8 warps][STG_WARP] (BIAS_ACT only)
+  uint8_t* ctrl = stgs + 8 * (size_t)C::STG_WARP;
   Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), S};
   uint64_t* xbar = reinterpret_cast<uint64_t*>(ctrl) + Ctrl::count(S);  // aux full[2], empty[2]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);  // issued, consumed, aux issued
   float* cs = reinterpret_cast<float*>(ctrl + C::CTRL);                      // [4][kColsumCap]
-  float* lp = cs + 4 * kColsumCap;                                           // [4][kLossPartials]
-  float* bias_s = lp + 4 * kLossPartials;                                    // [kColsumCap]
+  float* lp = cs + 4 * kColsumCap;                                           // [8][kLossPartials]
+  float* bias_s = lp + 8 * kLossPartials;                                    // [kColsumCap]
 
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   auto sA = [&](int s) { return base + (uint32_t)(s * C::STAGE); };
@@ -98,7 +105,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(cb.tfull(a), 1);
-      mbar_init(cb.tempty(a), EW * kWarp);
+      mbar_init(cb.tempty(a), (EPI == EPI_LOSS ? 4 : EW) * kWarp);
     }
     mbar_init(cb.drain(), 1);
     for (int a = 0; a < 2; ++a) {
@@ -112,12 +119,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     fence_mbar_init();
   }
   if (EPI != EPI_BIAS_ACT)
-    for (int i = threadIdx.x; i < 4 * kColsumCap + 4 * kLossPartials; i += NT) cs[i] = 0.f;
+    for (int i = threadIdx.x; i < 4 * kColsumCap + 8 * kLossPartials; i += NT) cs[i] = 0.f;
   if (warp == 1) tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (EPI == EPI_DACT) prefetch_tmap(&tmX);
+    if (EPI != EPI_LOSS) prefetch_tmap(&tmO);
   }
   tc_fence_before();
   __syncthreads();
@@ -201,6 +209,26 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ++tc;
       }
     }
+  } else if constexpr (EPI == EPI_LOSS) {
+    // two groups of four warps (lane quarter q = warp % 4) take alternate
+    // tiles, i.e. the tiles of accumulator grp; column sums of group 1 sit
+    // 256 floats after group 0's in each quarter's slot
+    const int q = warp & 3;
+    const int grp = (warp - 2) / 4;
+    const HeadMasks hm = head_masks(p.shape);
+    uint32_t i = 0;
+    for (int tile = blockIdx.x + grp * gridDim.x; tile < total; tile += 2 * gridDim.x, ++i) {
+      if (!wait_bar(cb.tfull(grp), i & 1, g)) break;
+      tc_fence_after();
+      const int tm = tile / p.tiles_n;
+      const int row = tm * BM + q * 32 + lane;
+      const uint32_t taddr = tmem + (uint32_t)(grp * BN) + ((uint32_t)(q * 32) << 16);
+      epi_loss_tile<BN>(taddr, row, row < p.M, p.shape, hm, p.lc, p.inv_mb, p.rows, p.logstd,
+                        bias_s, p.dz, p.lddz, cs + q * kColsumCap + grp * 256,
+                        lp + (grp * 4 + q) * kLossPartials, lane);
+      tc_fence_before();
+      mbar_arrive(cb.tempty(grp));
+    }
   } else {
     // epilogue warps 2..2+EW: TMEM lane quarter q = warp % 4, column part h
     const int q = warp & 3;
@@ -215,25 +243,51 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int row = tm * BM + q * 32 + lane;
       const bool rok = row < p.M;
       const uint32_t taddr = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      constexpr int PART = BN / (EW / 4);   // columns of this warp: [h*PART, (h+1)*PART)
       if constexpr (EPI == EPI_DACT) {
-        // tile tc uses aux slot tc & 1 (same tile order as the producer)
+        // tile tc uses aux slot tc & 1 (same tile order as the producer); the
+        // result overwrites the warp's rows of the slot and leaves by TMA
         const int xs = tc & 1;
         if (!wait_bar(smem_u32(&xbar[xs]), (tc >> 1) & 1, g)) break;
-        epi_dact_smem_tile<BN, EW>(taddr, q * 32 + lane, row, rok, tn * BN, h, p.act,
-                                   auxs + xs * C::AUX_SLOT, p.out, p.ldo, cs + q * kColsumCap,
-                                   lane);
+        uint8_t* slot = auxs + xs * C::AUX_SLOT;
+        epi_dact_smem_tile<BN, EW>(taddr, q * 32 + lane, rok, tn * BN, h, p.act, slot,
+                                   cs + q * kColsumCap, lane);
+        tc_fence_before();
+        mbar_arrive(cb.tempty(acc));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int b = 0; b < PART / 64; ++b) {
+            const int cb64 = (h * PART) / 64 + b;
+            tma_store_2d(&tmO, smem_u32(slot + cb64 * 16384 + q * 4096), tn * BN + cb64 * 64,
+                         tm * BM + q * 32);
+          }
+          bulk_commit();
+          bulk_wait_read0();   // the slot is refilled by the producer after this
+        }
+        __syncwarp();
         mbar_arrive(smem_u32(&xbar[2 + xs]));
-      } else if constexpr (EPI == EPI_LOSS) {
-        epi_loss_tile<BN>(taddr, row, rok, p.shape, p.lc, p.inv_mb, p.rows, p.logstd, bias_s,
-                          p.dz, p.lddz, cs + q * kColsumCap, lp + q * kLossPartials, lane);
       } else {
-        epi_elem_tile<BN, EW, false>(taddr, row, rok, tn * BN, h, p.act, bias_s, nullptr, 0,
-                                     p.out, p.ldo, cs + q * kColsumCap, lane);
+        uint8_t* stg = stgs + (warp - 2) * C::STG_WARP;
+        if (lane == 0) bulk_wait_read0();   // the previous tile's stores have left stg
+        __syncwarp();
+        epi_act_stage_tile<BN, EW>(taddr, tn * BN, h, p.act, bias_s, stg, lane);
+        tc_fence_before();
+        mbar_arrive(cb.tempty(acc));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int b = 0; b < PART / 64; ++b)
+            tma_store_2d(&tmO, smem_u32(stg + b * 4096), tn * BN + h * PART + b * 64,
+                         tm * BM + q * 32);
+          bulk_commit();
+        }
       }
-      tc_fence_before();
-      mbar_arrive(cb.tempty(acc));
       ++tc;
     }
+    if (lane == 0) bulk_wait0();   // this warp's stores are complete before the CTA exits
   }
 
   __syncthreads();
@@ -260,14 +314,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if constexpr (EPI != EPI_BIAS_ACT) {
     if (warp >= 2) {
       const int et = threadIdx.x - 2 * kWarp;
+      auto quad = [&](const float* b, int c) {
+        return ((b[c] + b[kColsumCap + c]) + b[2 * kColsumCap + c]) + b[3 * kColsumCap + c];
+      };
       for (int c = et; c < p.epi_n; c += EW * kWarp)
         p.colsum_part[(int64_t)blockIdx.x * p.epi_n + c] =
-            ((cs[c] + cs[kColsumCap + c]) + cs[2 * kColsumCap + c]) + cs[3 * kColsumCap + c];
+            EPI == EPI_LOSS ? quad(cs, c) + quad(cs + 256, c) : quad(cs, c);
       if constexpr (EPI == EPI_LOSS) {
-        if (et < kLossPartials)
-          p.loss_part[(int64_t)blockIdx.x * kLossPartials + et] =
-              ((lp[et] + lp[kLossPartials + et]) + lp[2 * kLossPartials + et]) +
-              lp[3 * kLossPartials + et];
+        if (et < kLossPartials) {
+          float t = 0.f;
+          for (int k = 0; k < 8; ++k) t += lp[k * kLossPartials + et];
+          p.loss_part[(int64_t)blockIdx.x * kLossPartials + et] = t;
+        }
       }
     }
   }
@@ -494,14 +552,19 @@ cudaError_t make_tmap_blocks(CUtensorMap* m, const void* base, int64_t rows, int
 template <int BN, int EPI>
 cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream_t st,
                       int* grid_out) {
-  CUtensorMap ta, tb, tx;
+  CUtensorMap ta, tb, tx, to;
   cudaError_t e = make_tmap(&ta, g.A, g.lda, g.M, g.lda, BK, BM);
   if (e != cudaSuccess) return e;
   e = make_tmap(&tb, g.B, g.ldb, g.N, g.ldb, BK, BN);
   if (e != cudaSuccess) return e;
   tx = ta;
+  to = ta;
   if (EPI == EPI_DACT) {   // activation operand [M][N], 128-row x 64-column boxes
     e = make_tmap(&tx, p.aux, g.N, g.M, p.ldaux, 64, BM);
+    if (e != cudaSuccess) return e;
+  }
+  if (EPI != EPI_LOSS) {   // output [M][N] (row pitch ldo), 32-row x 64-column boxes
+    e = make_tmap(&to, p.out, g.N, g.M, p.ldo, 64, 32);
     if (e != cudaSuccess) return e;
   }
   p.M = g.M;
@@ -516,7 +579,7 @@ cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream
   const int grid = total < num_sms ? total : num_sms;
   if (grid_out) *grid_out = grid;
   return launch_pdl(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(gemm_threads<EPI>()),
-                    Cfg<BN, EPI>::SMEM, st, ta, tb, tx, p);
+                    Cfg<BN, EPI>::SMEM, st, ta, tb, tx, to, p);
 }
 
 }  // namespace
@@ -534,8 +597,7 @@ cudaError_t tc_prepare() {
   if (e != cudaSuccess) return e;
   const cudaError_t errs[] = {
       set_smem_attr<256, EPI_BIAS_ACT>(), set_smem_attr<128, EPI_BIAS_ACT>(),
-      set_smem_attr<64, EPI_BIAS_ACT>(),  set_smem_attr<128, EPI_DACT>(),
-      set_smem_attr<64, EPI_DACT>(),
+      set_smem_attr<128, EPI_DACT>(),
       set_smem_attr<16, EPI_LOSS>(),      set_smem_attr<32, EPI_LOSS>(),
       cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)W_SMEM)};
@@ -566,11 +628,9 @@ cudaError_t tc_gemm_bias_act(const GemmOperands& g, const float* bias, int act,
   p.ldo = ldo;
   p.err = err;
   p.timeout_ns = timeout_ns;
-  switch (tc_pick_bn(g.N)) {
-    case 256: return launch_tc<256, EPI_BIAS_ACT>(g, p, num_sms, st, nullptr);
-    case 128: return launch_tc<128, EPI_BIAS_ACT>(g, p, num_sms, st, nullptr);
-    case 64: return launch_tc<64, EPI_BIAS_ACT>(g, p, num_sms, st, nullptr);
-  }
+  // output widths are multiples of 128 (64-column TMA-store blocks per warp)
+  if (g.N % 256 == 0) return launch_tc<256, EPI_BIAS_ACT>(g, p, num_sms, st, nullptr);
+  if (g.N % 128 == 0) return launch_tc<128, EPI_BIAS_ACT>(g, p, num_sms, st, nullptr);
   return cudaErrorInvalidValue;
 }
 
@@ -588,9 +648,8 @@ cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ld
   p.epi_n = g.N;
   p.err = err;
   p.timeout_ns = timeout_ns;
-  // at most 128 columns, so that 4 stages and two activation tiles fit
+  // 128 columns, so that 4 stages and two activation tiles fit
   if (g.N % 128 == 0) return launch_tc<128, EPI_DACT>(g, p, num_sms, st, grid_out);
-  if (g.N % 64 == 0) return launch_tc<64, EPI_DACT>(g, p, num_sms, st, grid_out);
   return cudaErrorInvalidValue;
 }
 

@@ -520,10 +520,10 @@ mk_kernel(const __grid_constant__ MkMaps maps, const MkParams p) {
           if (m->epi == EPI_LOSS) {
             if (h == 0) {
               if (m->BN == 16)
-                epi_loss_tile<16>(taddr, row, rok, p.s, p.lc, p.inv_mb, p.rows, p.logstd, bias_s,
+                epi_loss_tile<16>(taddr, row, rok, p.s, head_masks(p.s), p.lc, p.inv_mb, p.rows, p.logstd, bias_s,
                                   p.dz, p.lddz, cs_q, lp + q * kLossPartials, lane);
               else
-                epi_loss_tile<32>(taddr, row, rok, p.s, p.lc, p.inv_mb, p.rows, p.logstd, bias_s,
+                epi_loss_tile<32>(taddr, row, rok, p.s, head_masks(p.s), p.lc, p.inv_mb, p.rows, p.logstd, bias_s,
                                   p.dz, p.lddz, cs_q, lp + q * kLossPartials, lane);
             }
           } else if (m->epi == EPI_BIAS_ACT) {

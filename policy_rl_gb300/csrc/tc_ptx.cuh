@@ -61,6 +61,29 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
       "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
+// 2-D tiled TMA store from shared memory (bulk-group completion).  Elements
+// of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   (uint64_t)tmap),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the shared-memory sources of this thread's committed bulk stores may be reused
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// this thread's committed bulk stores are complete
+__device__ __forceinline__ void bulk_wait0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// generic-proxy shared-memory writes become visible to the async proxy (TMA)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const void* p) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)p) : "memory");
 }

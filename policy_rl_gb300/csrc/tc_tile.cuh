@@ -152,12 +152,13 @@ __device__ __forceinline__ void epi_elem_tile(uint32_t taddr, int row, bool rok,
 // Backward-data epilogue with the activation operand already in shared
 // memory: `aux` is a 128 x BN bf16 tile loaded by TMA with the 128-byte
 // swizzle (BN/64 blocks of 128 rows x 128 bytes, 16-byte chunk c of row r at
-// r*128 + ((c ^ (r & 7)) * 16)).  out = acc * act'(aux); per-warp column sums.
+// r*128 + ((c ^ (r & 7)) * 16)).  out = acc * act'(aux) is written back in
+// place (same thread, same bytes) for a TMA store of the tile; per-warp column
+// sums of out go to cs_q (rows >= M count as zero).
 template <int BN, int EW>
-__device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, int row, bool rok,
-                                                   int col_tile, int h, int act,
-                                                   const uint8_t* aux, __nv_bfloat16* out,
-                                                   int ldo, float* cs_q, int lane) {
+__device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool rok, int col_tile,
+                                                   int h, int act, uint8_t* aux, float* cs_q,
+                                                   int lane) {
   constexpr int PART = BN / (EW / 4);
   constexpr int NCH = PART / 32;
   const int cbase = h * PART;
@@ -172,11 +173,12 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, int r
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[cur][j]);
-    const uint8_t* blk = aux + (c0 / 64) * 16384 + rl * 128;
+    uint8_t* blk = aux + (c0 / 64) * 16384 + rl * 128;
     const int c16 = (c0 % 64) / 8;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 a4 = *reinterpret_cast<const uint4*>(blk + (((c16 + i) ^ (rl & 7)) << 4));
+      uint4* slot = reinterpret_cast<uint4*>(blk + (((c16 + i) ^ (rl & 7)) << 4));
+      const uint4 a4 = *slot;
       const uint32_t w4[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {
@@ -187,40 +189,218 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, int r
         v[j] = rok ? v[j] * d0 : 0.f;
         v[j + 1] = rok ? v[j + 1] * d1 : 0.f;
       }
+      uint4 o;
+      o.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+      o.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+      o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+      o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+      *slot = o;
     }
-    const int col0 = col_tile + c0;
-    if (rok) store_bf16x32(out + (int64_t)row * ldo + col0, v);
     const float colsum = warp_reduce_scatter32(v);
-    cs_q[col0 + lane] += colsum;
+    cs_q[col_tile + c0 + lane] += colsum;
   }
 }
 
-// Loss epilogue of one 128 x BN (BN = CP = 16 or 32) head tile for one warp:
-// z = acc + b3 -> per-row PPO loss -> dz (bf16 row, CP columns), column sums
-// of dz into cs_q, loss terms and dlogstd into lp_q.
+// Forward epilogue, out = act(acc + bias), for one epilogue warp: its 32 rows
+// (lane = row) and columns [h*PART, (h+1)*PART) of the tile go to the warp's
+// staging buffer stg as PART/64 blocks of 32 rows x 128 bytes in the 128-byte
+// swizzled layout, ready for one TMA store per block.
+template <int BN, int EW>
+__device__ __forceinline__ void epi_act_stage_tile(uint32_t taddr, int col_tile, int h, int act,
+                                                   const float* bias_s, uint8_t* stg, int lane) {
+  constexpr int PART = BN / (EW / 4);
+  constexpr int NCH = PART / 32;
+  const int cbase = h * PART;
+  uint32_t r[2][32];
+  tmem_ld32_async(taddr + (uint32_t)cbase, r[0]);
+#pragma unroll
+  for (int k = 0; k < NCH; ++k) {
+    const int cur = k & 1, nxt = cur ^ 1;
+    const int c0 = cbase + 32 * k;
+    tmem_wait_ld(r[cur]);
+    if (k + 1 < NCH) tmem_ld32_async(taddr + (uint32_t)(c0 + 32), r[nxt]);
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float x = __uint_as_float(r[cur][j]) + bias_s[col_tile + c0 + j];
+      v[j] = act == 0 ? tanh_fast(x) : fmaxf(x, 0.f);
+    }
+    uint8_t* blk = stg + ((32 * k) / 64) * 4096 + lane * 128;
+    const int c16 = ((32 * k) % 64) / 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 o;
+      o.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+      o.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+      o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+      o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+      *reinterpret_cast<uint4*>(blk + (((c16 + i) ^ (lane & 7)) << 4)) = o;
+    }
+  }
+}
+
+// Column masks of the head layout (bit k = column k): first / last column of
+// each discrete head, all discrete columns, Gaussian means (column g0 + g).
+struct HeadMasks {
+  uint32_t hs, he, hd, gm;
+  int g0, vcol;
+};
+
+__device__ __forceinline__ HeadMasks head_masks(const NetShape& s) {
+  HeadMasks m{0u, 0u, 0u, 0u, 0, s.C - 1};
+  int off = 0;
+  for (int h = 0; h < s.NH; ++h) {
+    const int n = s.head_n[h];
+    m.hs |= 1u << off;
+    m.he |= 1u << (off + n - 1);
+    m.hd |= ((1u << n) - 1u) << off;
+    off += n;
+  }
+  m.g0 = off;
+  m.gm = s.G > 0 ? ((1u << s.G) - 1u) << off : 0u;
+  return m;
+}
+
+// Per-row PPO loss and d(loss)/dz for one row of head outputs z (CP columns),
+// the same quantities as row_loss: log-softmax per discrete head, Gaussian
+// log-density, entropy, clipped surrogate, value loss, and their gradients
+// ("Proximal Policy Optimization Algorithms", sec. 3 and 5).  Heads are
+// contiguous column segments, so every per-head reduction is a segmented scan
+// over the compile-time-indexed columns and all state stays in registers.
+// amask has one bit per head: the column of the taken action.
+template <int CP>
+__device__ __forceinline__ void row_loss_seg(const HeadMasks& hm, const LossCoef& lc, float inv_mb,
+                                             const float (&z)[32], uint32_t amask,
+                                             const float* actc, const float* logstd,
+                                             float logp_old, float A, float R, float (&dz)[32],
+                                             float (&t6)[6], float (&dls)[4]) {
+  const float LOG_2PI = 1.8378770664093453f;
+  float u[CP], w[CP];
+  // head max: running max from each head's first column, broadcast back from its last
+  float run = 0.f;
+#pragma unroll
+  for (int k = 0; k < CP; ++k) {
+    run = ((hm.hs >> k) & 1u) ? z[k] : fmaxf(run, z[k]);
+    u[k] = run;
+  }
+#pragma unroll
+  for (int k = CP - 2; k >= 0; --k)
+    if (!((hm.he >> k) & 1u)) u[k] = u[k + 1];
+  // sum of exp(z - max) per head, then log-sum-exp broadcast back
+  float srun = 0.f;
+#pragma unroll
+  for (int k = 0; k < CP; ++k) {
+    const float e = ((hm.hd >> k) & 1u) ? expf(z[k] - u[k]) : 0.f;
+    srun = ((hm.hs >> k) & 1u) ? e : srun + e;
+    w[k] = srun;
+  }
+#pragma unroll
+  for (int k = CP - 1; k >= 0; --k) {
+    if ((hm.he >> k) & 1u) u[k] = u[k] + logf(w[k]);
+    else if (k + 1 < CP) u[k] = u[k + 1];
+  }
+  // log-probabilities, probabilities, per-head entropy (kept in dz for now)
+  float logp = 0.f, ent = 0.f, erun = 0.f;
+#pragma unroll
+  for (int k = 0; k < CP; ++k) {
+    const bool d = (hm.hd >> k) & 1u;
+    const float lp = z[k] - u[k];
+    const float pk = d ? expf(lp) : 0.f;
+    u[k] = lp;
+    w[k] = pk;
+    const float hk = d ? -(pk * lp) : 0.f;
+    erun = ((hm.hs >> k) & 1u) ? hk : erun + hk;
+    dz[k] = erun;
+    if ((hm.he >> k) & 1u) ent += erun;
+    if ((amask >> k) & 1u) logp += lp;
+  }
+#pragma unroll
+  for (int k = CP - 2; k >= 0; --k)
+    if (!((hm.he >> k) & 1u)) dz[k] = dz[k + 1];
+  float value = 0.f;
+#pragma unroll
+  for (int k = 0; k < CP; ++k) {
+    if ((hm.gm >> k) & 1u) {
+      const int g = k - hm.g0;
+      const float mu = z[k], ls = logstd[g], a = actc[g];
+      const float inv_var = expf(-2.f * ls);
+      logp += -0.5f * (a - mu) * (a - mu) * inv_var - ls - 0.5f * LOG_2PI;
+      ent += 0.5f + 0.5f * LOG_2PI + ls;
+    }
+    if (k == hm.vcol) value = z[k];
+  }
+  const float log_ratio = logp - logp_old;
+  const float ratio = expf(log_ratio);
+  const float lo = 1.f - lc.clip, hi = 1.f + lc.clip;
+  const float clipped = fminf(fmaxf(ratio, lo), hi);
+  const float s1 = ratio * A, s2 = clipped * A;
+  const float pg = -fminf(s1, s2);
+  const float vdiff = value - R;
+  const float vl = vdiff * vdiff;
+  t6[0] = pg + lc.vf * vl - lc.ent * ent;
+  t6[1] = pg;
+  t6[2] = vl;
+  t6[3] = ent;
+  t6[4] = fabsf(ratio - 1.f) > lc.clip ? 1.f : 0.f;
+  t6[5] = (ratio - 1.f) - log_ratio;
+  const float g_logp = (s1 <= s2) ? -A * ratio * inv_mb : 0.f;
+  const float g_ent = -lc.ent * inv_mb;
+#pragma unroll
+  for (int k = 0; k < CP; ++k) {
+    if ((hm.hd >> k) & 1u) {
+      const float dlogp = (((amask >> k) & 1u) ? 1.f : 0.f) - w[k];
+      const float dent = -w[k] * (u[k] + dz[k]);
+      dz[k] = g_logp * dlogp + g_ent * dent;
+    } else if ((hm.gm >> k) & 1u) {
+      const int g = k - hm.g0;
+      const float mu = z[k], ls = logstd[g], a = actc[g];
+      const float inv_var = expf(-2.f * ls);
+      dz[k] = g_logp * (a - mu) * inv_var;
+      const float dl = g_logp * ((a - mu) * (a - mu) * inv_var - 1.f) + g_ent;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (g == j) dls[j] = dl;
+    } else if (k == hm.vcol) {
+      dz[k] = lc.vf * 2.f * vdiff * inv_mb;
+    } else {
+      dz[k] = 0.f;
+    }
+  }
+}
+
+// Loss epilogue of one 128 x BN head tile (BN = CP columns): thread = row.
+// Writes dz (bf16) and accumulates the per-warp column sums of dz into cs_q,
+// the loss terms and dlogstd into lp_q.
 template <int BN>
 __device__ __forceinline__ void epi_loss_tile(uint32_t taddr, int row, bool rok, const NetShape& s,
-                                              const LossCoef& lc, float inv_mb,
-                                              const LossRows& rows, const float* logstd,
-                                              const float* bias_s, __nv_bfloat16* dz, int lddz,
-                                              float* cs_q, float* lp_q, int lane) {
+                                              const HeadMasks& hm, const LossCoef& lc,
+                                              float inv_mb, const LossRows& rows,
+                                              const float* logstd, const float* bias_s,
+                                              __nv_bfloat16* dz, int lddz, float* cs_q,
+                                              float* lp_q, int lane) {
   float v[32];
   if constexpr (BN == 16) tmem_ld16(taddr, v);
   else tmem_ld32(taddr, v);
   float z[32], dzr[32], t6[6], dls[4];
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    z[j] = (j < s.C) ? v[j] + bias_s[j] : 0.f;
+    z[j] = (j < BN && j < s.C) ? v[j] + bias_s[j] : 0.f;
     dzr[j] = 0.f;
   }
 #pragma unroll
   for (int k = 0; k < 6; ++k) t6[k] = 0.f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) dls[k] = 0.f;
-  if (rok)
-    row_loss(s, lc, inv_mb, z, rows.act + (int64_t)row * s.NH, rows.actc + (int64_t)row * s.G,
-             logstd, rows.logp_old[row], rows.adv[row], rows.ret[row], dzr, t6, dls);
   if (rok) {
+    uint32_t amask = 0u;
+    int off = 0;
+    const int32_t* a = rows.act + (int64_t)row * s.NH;
+    for (int h = 0; h < s.NH; ++h) {
+      amask |= 1u << (off + a[h]);
+      off += s.head_n[h];
+    }
+    row_loss_seg<BN>(hm, lc, inv_mb, z, amask, rows.actc + (int64_t)row * s.G, logstd,
+                     rows.logp_old[row], rows.adv[row], rows.ret[row], dzr, t6, dls);
     uint4* d = reinterpret_cast<uint4*>(dz + (int64_t)row * lddz);
 #pragma unroll
     for (int i = 0; i < BN / 8; ++i) {
