@@ -130,17 +130,27 @@ def _barrier(world):
 
 # ---- algorithmic work per kernel stage (for the roofline) ----------------------
 def _stage_work(stage: str, w, mb: int):
-    """(bound, algorithmic units per launch, unit) for one launch of a stage."""
+    """(FLOPs, HBM bytes) of one launch of a kernel stage, or None.
+
+    GEMM bytes are the bf16 activations each kernel must read and write once
+    (weights and per-CTA partials are small and L2-resident): X [mb, Dp],
+    H1/H2/dP1/dP2 [mb, H], dZ [mb, CP] (CP = head columns padded to 16/32;
+    the weight-gradient kernel reads dZ through 64-column boxes)."""
     D, H1, H2, C = w.obs_dim, w.h1, w.h2, w.out_cols
     B = w.B
+    Dp = -(-D // 64) * 64
+    CP = 16 if C <= 16 else 32
+    a = 2 * mb   # bytes per activation column of a minibatch (bf16)
     gemm = {
-        "fwd1_gemm": 2 * mb * H1 * D, "fwd2_gemm": 2 * mb * H2 * H1,
-        "head_loss_gemm": 2 * mb * C * H2, "dact2_gemm": 2 * mb * H2 * C,
-        "dact1_gemm": 2 * mb * H1 * H2, "wgrad_gemm": 2 * mb * (H2 * H1 + H1 * D + C * H2),
+        "fwd1_gemm": (2 * mb * H1 * D, a * (Dp + H1)),
+        "fwd2_gemm": (2 * mb * H2 * H1, a * (H1 + H2)),
+        "head_loss_gemm": (2 * mb * C * H2, a * (H2 + CP) + mb * (4 * len(w.heads) + 12)),
+        "dact2_gemm": (2 * mb * H2 * C, a * (CP + 2 * H2)),
+        "dact1_gemm": (2 * mb * H1 * H2, a * (H2 + 2 * H1)),
+        "wgrad_gemm": (2 * mb * (H2 * H1 + H1 * D + C * H2), a * (H2 + H1 + H1 + Dp + H2 + 64)),
     }
     if stage in gemm:
-        return "tensor", gemm[stage], "flop"
-    Dp = -(-D // 64) * 64
+        return gemm[stage]
     P = w.num_params
     hbm = {
         "gae_scan": 20 * B,                       # read r, v, d; write adv, ret
@@ -148,11 +158,36 @@ def _stage_work(stage: str, w, mb: int):
         "gather": mb * (2 * Dp * 2 + 4 * len(w.heads) * 2 + 4 * 3 * 2),
         "adam": 30 * P, "grad_sqnorm": 4 * P,
         "grad_reduce": 4 * P,
-        "gather_phase": 0,
     }
     if stage in hbm:
-        return "hbm", hbm[stage], "byte"
+        return 0, hbm[stage]
     return None
+
+
+def _roofline(stage, w, mb, ms_total, launches, hbm_peak, tf_peak, peak_src):
+    """Roofline entry of one stage: bound = the larger of its tensor-time and
+    HBM-time floors at the measured peaks; achieved = algorithmic work per
+    launch / mean launch duration."""
+    work = _stage_work(stage, w, mb)
+    if work is None:
+        return None
+    flops, nbytes = work
+    per_launch_s = ms_total / launches / 1e3
+    t_tc = flops / (tf_peak * 1e12)
+    t_hbm = nbytes / (hbm_peak * 1e9)
+    if t_tc >= t_hbm:
+        achieved = flops / per_launch_s / 1e12
+        return {"bound": "tensor", "kernel": stage, "achieved": round(achieved, 2),
+                "peak": tf_peak, "unit": "TFLOP/s", "frac": round(achieved / tf_peak, 4),
+                "traffic": None, "peak_kind": f"bf16 sustained ({peak_src})",
+                "per_launch_us": round(per_launch_s * 1e6, 2),
+                "algorithmic_per_launch": {"flop": flops, "bytes": nbytes}}
+    achieved = nbytes / per_launch_s / 1e9
+    return {"bound": "hbm", "kernel": stage, "achieved": round(achieved, 1), "peak": hbm_peak,
+            "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+            "peak_kind": f"HBM copy ({peak_src})", "per_launch_us": round(per_launch_s * 1e6, 2),
+            "algorithmic_per_launch": {"flop": flops, "bytes": nbytes},
+            "tensor_TFLOPs": round(flops / per_launch_s / 1e12, 2) if flops else None}
 
 
 def run_ours(args, world, rank, local):
@@ -235,24 +270,18 @@ def run_ours(args, world, rank, local):
     dom = max(cand, key=lambda k: cand[k][0])
     prof_all = prof
     prof = cand
-    work = _stage_work(dom, w, mb)
-    roof = None
-    if work is not None:
-        bound, units, unit = work
-        per_launch_s = prof[dom][0] / prof[dom][1] / 1e3
-        if bound == "tensor":
-            achieved = units / per_launch_s / 1e12
-            peak = tf_sust
-            roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2),
-                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                    "traffic": None, "peak_kind": f"bf16 sustained ({peak_src})"}
-        else:
-            achieved = units / per_launch_s / 1e9
-            roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                    "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                    "traffic": None, "peak_kind": f"HBM copy ({peak_src})"}
+    roof = _roofline(dom, w, mb, prof[dom][0], prof[dom][1], hbm_peak, tf_sust, peak_src)
+    if roof is not None:
         roof["share"] = round(prof[dom][0] / total_ms, 4)
-        roof["per_launch_us"] = round(per_launch_s * 1e6, 2)
+    # all tensor-core GEMM stages together: FLOPs / their summed device time
+    gemm_names = ("fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm", "dact1_gemm",
+                  "wgrad_gemm")
+    g_ms = sum(prof[k][0] for k in gemm_names if k in prof)
+    g_flop = sum(_stage_work(k, w, mb)[0] * prof[k][1] for k in gemm_names if k in prof)
+    gemm_all = ({"ms_per_update": round(g_ms, 4),
+                 "TFLOPs": round(g_flop / (g_ms / 1e3) / 1e12, 2),
+                 "frac_of_bf16_sustained": round(g_flop / (g_ms / 1e3) / 1e12 / tf_sust, 4)}
+                if g_ms > 0 else None)
     stages = {k: {"ms": round(t, 4), "launches": c, "share": round(t / total_ms, 4)}
               for k, (t, c) in sorted(prof_all.items(), key=lambda kv: -kv[1][0])}
 
@@ -306,6 +335,7 @@ def run_ours(args, world, rank, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "ppo_update_host (pinned host rollout -> device, stats -> host)"},
         "roofline": roof,
+        "gemm_all": gemm_all,
         "stages": stages,
         "profiled_update_ms": round(total_ms, 4),
         "gae_stress": gae,

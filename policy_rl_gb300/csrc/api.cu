@@ -64,6 +64,10 @@ struct ppo_ctx {
   // minibatch workspace
   int64_t mbmax = 0;
   void* X = nullptr;
+  // one epoch of minibatch rows gathered in permutation order (ppo_update)
+  void* X_ep = nullptr;
+  int32_t* act_ep = nullptr;
+  float *actc_ep = nullptr, *logp_ep = nullptr, *adv_ep = nullptr, *ret_ep = nullptr;
   int32_t* act_mb = nullptr;
   float *actc_mb = nullptr, *logp_mb = nullptr, *adv_mb = nullptr, *ret_mb = nullptr;
   void *H1 = nullptr, *H2 = nullptr, *dZ = nullptr, *dP2 = nullptr, *dP1 = nullptr;
@@ -228,13 +232,19 @@ ppo_status check_minibatch_args(ppo_ctx* c, const float* obs, const int32_t* act
   return PPO_OK;
 }
 
-// One minibatch: gather, forward, loss, backward, gradient assembly.
-ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* obs_packed,
-                             const int32_t* act, const float* actc, const float* logp_old,
-                             const float* adv, const float* ret, const int32_t* idx, int64_t B,
-                             int64_t mb, const float* adv_stats, float* stats6, cudaStream_t st,
-                             int* nsq_out = nullptr) {
-  const NetShape& s = c->s;
+// Rows of one minibatch in minibatch order: X (bf16 [mb][Dp] or fp32 [mb][D]),
+// actions, logp_old, normalised advantages, returns.
+struct MbRows {
+  void* X;
+  int32_t* act;
+  float *actc, *logp, *adv, *ret;
+};
+
+// Gathers rows idx[0..n) of the rollout into r (advantages normalised).
+cudaError_t enqueue_gather(ppo_ctx* c, const float* obs, const __nv_bfloat16* obs_packed,
+                           const int32_t* act, const float* actc, const float* logp_old,
+                           const float* adv, const float* ret, const int32_t* idx, int64_t B,
+                           int64_t n, const float* adv_stats, const MbRows& r, cudaStream_t st) {
   GatherArgs ga{};
   ga.obs_f32 = obs;
   ga.obs_bf16 = obs_packed;
@@ -245,19 +255,36 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
   ga.ret = ret;
   ga.adv_stats = adv_stats;
   ga.idx = idx;
-  ga.mb = mb;
+  ga.mb = n;
   ga.B = B;
-  ga.X = c->X;
+  ga.X = r.X;
   ga.x_bf16 = c->bf16;
-  ga.act_mb = c->act_mb;
-  ga.actc_mb = c->actc_mb;
-  ga.logp_mb = c->logp_mb;
-  ga.adv_mb = c->adv_mb;
-  ga.ret_mb = c->ret_mb;
-  PPO_CUDA(launch_gather(s, ga, st));
-  c->tr.mark(ST_GATHER, st);
+  ga.act_mb = r.act;
+  ga.actc_mb = r.actc;
+  ga.logp_mb = r.logp;
+  ga.adv_mb = r.adv;
+  ga.ret_mb = r.ret;
+  return launch_gather(c->s, ga, st);
+}
 
-  LossRows rows{c->act_mb, c->actc_mb, c->logp_mb, c->adv_mb, c->ret_mb};
+// One minibatch: gather (unless its rows are given, already gathered),
+// forward, loss, backward, gradient assembly.
+ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* obs_packed,
+                             const int32_t* act, const float* actc, const float* logp_old,
+                             const float* adv, const float* ret, const int32_t* idx, int64_t B,
+                             int64_t mb, const float* adv_stats, float* stats6, cudaStream_t st,
+                             int* nsq_out = nullptr, const MbRows* pre = nullptr) {
+  const NetShape& s = c->s;
+  MbRows mr{c->X, c->act_mb, c->actc_mb, c->logp_mb, c->adv_mb, c->ret_mb};
+  if (pre) {
+    mr = *pre;
+  } else {
+    PPO_CUDA(enqueue_gather(c, obs, obs_packed, act, actc, logp_old, adv, ret, idx, B, mb,
+                            adv_stats, mr, st));
+    c->tr.mark(ST_GATHER, st);
+  }
+
+  LossRows rows{mr.act, mr.actc, mr.logp, mr.adv, mr.ret};
   LossCoef lc{c->cfg.clip, c->cfg.vf_coef, c->cfg.ent_coef};
   const float inv_mb = 1.0f / (float)mb;
   const float* P = c->params;
@@ -271,7 +298,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
   ra.sq_part = nsq_out ? c->sq : nullptr;   // fused squared-norm partials for Adam
 
   if (c->bf16) {
-    auto* X = static_cast<__nv_bfloat16*>(c->X);
+    auto* X = static_cast<__nv_bfloat16*>(mr.X);
     auto* H1 = static_cast<__nv_bfloat16*>(c->H1);
     auto* H2 = static_cast<__nv_bfloat16*>(c->H2);
     auto* dZ = static_cast<__nv_bfloat16*>(c->dZ);
@@ -313,7 +340,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     ra.pb3 = c->cs3; ra.nb3 = n3; ra.ldb3 = s.CP;
     ra.ploss = c->lossp; ra.nl = n3;
   } else {
-    auto* X = static_cast<float*>(c->X);
+    auto* X = static_cast<float*>(mr.X);
     auto* H1 = static_cast<float*>(c->H1);
     auto* H2 = static_cast<float*>(c->H2);
     auto* dZ = static_cast<float*>(c->dZ);
@@ -525,20 +552,34 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
   PPO_CUDA(launch_gae_finalize(c->gae_part, gae_num_blocks((int)N), c->advstats, st));
   c->tr.mark(ST_GAE_FINALIZE, st);
   PPO_CUDA(launch_perm(seed, 0, epochs, B, c->perm, c->perm_work, st, &c->tr));
-  for (int e = 0; e < epochs; ++e)
+  const MbRows ep{c->X_ep, c->act_ep, c->actc_ep, c->logp_ep, c->adv_ep, c->ret_ep};
+  const int64_t xrow = c->bf16 ? (int64_t)c->s.Dp * 2 : (int64_t)c->s.D * 4;
+  const int NH = c->s.NH > 0 ? c->s.NH : 1, G = c->s.G > 0 ? c->s.G : 1;
+  for (int e = 0; e < epochs; ++e) {
+    const int32_t* perm_e = c->perm + (int64_t)e * B;
+    if (!c->use_mk) {
+      // the epoch's rows in permutation order: one gather for all its minibatches
+      PPO_CUDA(enqueue_gather(c, obs, packed, act, actc, logp_old, c->adv, c->ret, perm_e, B, B,
+                              c->advstats, ep, st));
+      c->tr.mark(ST_GATHER, st);
+    }
     for (int k = 0; k < minibatches; ++k) {
-      const int32_t* idx = c->perm + (int64_t)e * B + (int64_t)k * mb;
+      const int32_t* idx = perm_e + (int64_t)k * mb;
       float* st6 = stats ? stats + ((int64_t)e * minibatches + k) * 6 : nullptr;
       if (c->use_mk) {
         TRY(enqueue_minibatch_mk(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
                                  c->advstats, st6, 1, lr, st));
       } else {
+        const int64_t r0 = (int64_t)k * mb;
+        const MbRows mr{static_cast<uint8_t*>(ep.X) + r0 * xrow, ep.act + r0 * NH,
+                        ep.actc + r0 * G, ep.logp + r0, ep.adv + r0, ep.ret + r0};
         int nsq = 0;
         TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
-                              c->advstats, st6, st, &nsq));
+                              c->advstats, st6, st, &nsq, &mr));
         TRY(enqueue_adam(c, lr, nullptr, st, nsq));
       }
     }
+  }
   return PPO_OK;
 }
 
@@ -646,6 +687,17 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
     if ((r = c->alloc(&t, (size_t)mbm * s.H1 * esz)) != PPO_OK) return fail(r);
     c->dP1 = t;
   }
+  {
+    void* t;
+    if ((r = c->alloc(&t, (size_t)c->bmax * (c->bf16 ? s.Dp : s.D) * esz)) != PPO_OK)
+      return fail(r);
+    c->X_ep = t;
+  }
+  A(c->act_ep, c->bmax * (s.NH > 0 ? s.NH : 1));
+  A(c->actc_ep, c->bmax * (s.G > 0 ? s.G : 1));
+  A(c->logp_ep, c->bmax);
+  A(c->adv_ep, c->bmax);
+  A(c->ret_ep, c->bmax);
   A(c->act_mb, mbm * (s.NH > 0 ? s.NH : 1));
   A(c->actc_mb, mbm * (s.G > 0 ? s.G : 1));
   A(c->logp_mb, mbm);
