@@ -85,6 +85,15 @@ typedef struct {
                                     persistent cooperative kernel whose stages
                                     are separated by grid barriers.  Same
                                     results up to fp32 summation order.      */
+    int32_t fused_mlp;           /* bf16 mode, persistent_minibatch == 0: 0
+                                    (default) launches one kernel per GEMM
+                                    stage; 1 runs forward, loss and
+                                    backward-data of a minibatch as one fused
+                                    kernel when the network fits its shared
+                                    memory tiles (padded obs width 64, hidden
+                                    widths 128 or 256, <= 32 head columns,
+                                    <= 4 Gaussian dims), else per stage.  Same
+                                    results up to fp32 summation order.      */
 } ppo_config;
 
 typedef struct ppo_ctx ppo_ctx;
@@ -231,8 +240,8 @@ ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_ac
  * phases inside the persistent minibatch kernel (time between the phase
  * starts seen by its first CTA, summed over minibatches); they are not
  * separate launches. */
-#define PPO_NUM_KERNEL_STAGES 19
-#define PPO_NUM_STAGES 28
+#define PPO_NUM_KERNEL_STAGES 20
+#define PPO_NUM_STAGES 29
 /* Name of a stage (static string; "unknown" outside [0, PPO_NUM_STAGES)). */
 const char *ppo_stage_name(int32_t stage);
 

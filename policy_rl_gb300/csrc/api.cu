@@ -63,6 +63,7 @@ struct ppo_ctx {
 
   // minibatch workspace
   int64_t mbmax = 0;
+  bool use_fmlp = false;   // fused forward + loss + backward-data kernel
   void* X = nullptr;
   // one epoch of minibatch rows gathered in permutation order (ppo_update)
   void* X_ep = nullptr;
@@ -305,6 +306,42 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     auto* dP2 = static_cast<__nv_bfloat16*>(c->dP2);
     auto* dP1 = static_cast<__nv_bfloat16*>(c->dP1);
     const int ns = c->num_sms;
+    int n3 = 0, n2 = 0, n1 = 0;
+    if (c->use_fmlp) {
+      // forward, loss and backward-data in one kernel (activations stay on chip)
+      FusedMlp f{};
+      f.s = s;
+      f.M = M;
+      f.X = X;
+      f.W1s = c->sh.W1s;
+      f.W2s = c->sh.W2s;
+      f.W3s = c->sh.W3s;
+      f.W3Ts = c->sh.W3Ts;
+      f.W2Ts = c->sh.W2Ts;
+      f.ld3t = c->sh.ld3t;
+      f.b1 = P + s.ob1;
+      f.b2 = P + s.ob2;
+      f.b3 = P + s.ob3;
+      f.logstd = P + s.ologstd;
+      f.H1 = H1;
+      f.H2 = H2;
+      f.dZ = dZ;
+      f.dP2 = dP2;
+      f.dP1 = dP1;
+      f.lddz = c->lddz;
+      f.lc = lc;
+      f.rows = rows;
+      f.inv_mb = inv_mb;
+      f.cs1 = c->cs1;
+      f.cs2 = c->cs2;
+      f.cs3 = c->cs3;
+      f.lossp = c->lossp;
+      f.err = c->err;
+      f.timeout_ns = kTimeoutNs;
+      PPO_CUDA(fmlp_launch(f, ns, st, &n1));
+      n2 = n3 = n1;
+      c->tr.mark(ST_FUSED_MLP, st);
+    } else {
     // forward: H1 = act(X W1^T + b1), H2 = act(H1 W2^T + b2)
     GemmOperands g1{X, s.Dp, c->sh.W1s, s.Dp, M, s.H1, s.Dp};
     PPO_CUDA(tc_gemm_bias_act(g1, P + s.ob1, s.act, H1, s.H1, c->err, kTimeoutNs, ns, st));
@@ -313,7 +350,6 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     PPO_CUDA(tc_gemm_bias_act(g2, P + s.ob2, s.act, H2, s.H2, c->err, kTimeoutNs, ns, st));
     c->tr.mark(ST_FWD2, st);
     // head + loss: z = H2 W3^T + b3 -> dz
-    int n3 = 0, n2 = 0, n1 = 0;
     GemmOperands g3{H2, s.H2, c->sh.W3s, s.H2, M, s.CP, s.H2};
     PPO_CUDA(tc_gemm_loss(g3, s, lc, rows, inv_mb, P + s.ob3, P + s.ologstd, dZ, c->lddz, c->cs3,
                           c->lossp, c->err, kTimeoutNs, ns, st, &n3));
@@ -325,6 +361,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     GemmOperands g5{dP2, s.H2, c->sh.W2Ts, s.H2, M, s.H1, s.H2};
     PPO_CUDA(tc_gemm_dact(g5, H1, s.H1, s.act, dP1, s.H1, c->cs1, c->err, kTimeoutNs, ns, st, &n1));
     c->tr.mark(ST_DACT1, st);
+    }
     // weight gradients, split over the minibatch rows
     const WgradPlan wp = wgrad_plan(s, mb, ns);
     WGradRegion regs[3] = {{dP2, s.H2, s.H2, H1, s.H1, s.H1, wp.kt[0], c->pW2},
@@ -635,6 +672,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   c->s = s;
   c->bf16 = cfg->precision == 1;
   c->use_mk = c->bf16 && cfg->persistent_minibatch != 0;
+  c->use_fmlp = c->bf16 && !c->use_mk && cfg->fused_mlp != 0 && fmlp_supported(s);
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (c->num_sms < 1) c->num_sms = 1;
   c->mbmax = cfg->max_minibatch;
@@ -730,6 +768,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   }
 #undef A
   if (c->bf16 && tc_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
+  if (c->use_fmlp && fmlp_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (c->use_mk && mk_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (h_init_params) {
     if (cudaMemcpy(c->params, h_init_params, sizeof(float) * P, cudaMemcpyHostToDevice) !=
@@ -919,7 +958,7 @@ const char* ppo_stage_name(int32_t stage) {
       "pack_obs", "gae_scan", "gae_finalize", "gae_normalize", "perm_hist", "perm_scan",
       "perm_scatter", "gather", "fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm",
       "dact1_gemm", "wgrad_gemm", "grad_reduce", "grad_sqnorm", "adam", "weight_shadows",
-      "minibatch_persistent"};
+      "minibatch_persistent", "fused_mlp"};
   static const char* phases[kMkPhases] = {
       "phase:gather", "phase:fwd1", "phase:fwd2", "phase:head_loss", "phase:dact2",
       "phase:dact1", "phase:wgrad", "phase:grad_reduce", "phase:adam"};

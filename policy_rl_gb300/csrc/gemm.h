@@ -185,6 +185,31 @@ int mk_wgrad_bn(int N);
 cudaError_t mk_launch(const MkLaunch& L, cudaStream_t st);
 cudaError_t tc_make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
                          int box_cols, int box_rows);
+// [rows][ld] bf16 viewed as 64-column blocks: box = 64 x box_rows x box_blk,
+// landing as box_blk consecutive [box_rows][64] swizzled blocks
+cudaError_t tc_make_tmap_blocks(CUtensorMap* m, const void* base, int64_t rows, int64_t ld,
+                                int nblk, int box_rows, int box_blk);
 cudaError_t launch_shadows(const float* p, const NetShape& s, const Shadows& sh, cudaStream_t st);
+
+// Fused forward + loss + backward-data pass of one minibatch (fmlp.cu): all
+// activations bf16 row-major [M][width]; dZ with row pitch lddz (64).
+struct FusedMlp {
+  NetShape s;
+  int M;
+  const __nv_bfloat16 *X, *W1s, *W2s, *W3s, *W3Ts, *W2Ts;
+  int ld3t;
+  const float *b1, *b2, *b3, *logstd;
+  __nv_bfloat16 *H1, *H2, *dZ, *dP2, *dP1;
+  int lddz;
+  LossCoef lc;
+  LossRows rows;
+  float inv_mb;
+  float *cs1, *cs2, *cs3, *lossp;   // per-CTA partial rows (grid of them)
+  int* err;
+  uint64_t timeout_ns;
+};
+bool fmlp_supported(const NetShape& s);
+cudaError_t fmlp_prepare();
+cudaError_t fmlp_launch(const FusedMlp& f, int num_sms, cudaStream_t st, int* grid_out);
 
 }  // namespace ppo

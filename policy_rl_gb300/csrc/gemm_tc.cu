@@ -256,7 +256,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         mbar_arrive(cb.tempty(acc));
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && tm * BM + q * 32 < p.M) {   // rows of the box exist
 #pragma unroll
           for (int b = 0; b < PART / 64; ++b) {
             const int cb64 = (h * PART) / 64 + b;
@@ -277,7 +277,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         mbar_arrive(cb.tempty(acc));
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && tm * BM + q * 32 < p.M) {   // rows of the box exist
 #pragma unroll
           for (int b = 0; b < PART / 64; ++b)
             tma_store_2d(&tmO, smem_u32(stg + b * 4096), tn * BN + h * PART + b * 64,
@@ -609,6 +609,11 @@ cudaError_t tc_prepare() {
 cudaError_t tc_make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
                          int box_cols, int box_rows) {
   return make_tmap(m, base, cols, rows, ld, box_cols, box_rows);
+}
+
+cudaError_t tc_make_tmap_blocks(CUtensorMap* m, const void* base, int64_t rows, int64_t ld,
+                                int nblk, int box_rows, int box_blk) {
+  return make_tmap_blocks(m, base, rows, ld, nblk, box_rows, box_blk);
 }
 
 int tc_pick_bn(int N) {

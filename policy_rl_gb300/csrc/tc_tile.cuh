@@ -149,6 +149,65 @@ __device__ __forceinline__ void epi_elem_tile(uint32_t taddr, int row, bool rok,
   }
 }
 
+// Walks the NCH 32-column chunks [cbase + 32k, cbase + 32k + 32) of a TMEM
+// accumulator (this warp's lane quarter), calling body(regs, c0) per chunk.
+// The load of chunk k+1 is in flight while chunk k is processed.  The loop is
+// rolled two chunks at a time (two register buffers with compile-time names),
+// so the body's code appears twice rather than NCH times: the epilogues run
+// once or twice per CTA and kernel at small minibatches, where instruction-
+// cache misses on long unrolled code cost more than the loop.
+template <int NCH, class Body>
+__device__ __forceinline__ void tmem_chunks(uint32_t taddr, int cbase, Body&& body) {
+  uint32_t r0[32], r1[32];
+  tmem_ld32_async(taddr + (uint32_t)cbase, r0);
+  if constexpr (NCH == 1) {
+    tmem_wait_ld(r0);
+    body(r0, cbase);
+  } else {
+    static_assert(NCH % 2 == 0, "chunk pairs");
+#pragma unroll 1
+    for (int k = 0; k < NCH; k += 2) {
+      const int c0 = cbase + 32 * k;
+      tmem_wait_ld(r0);
+      tmem_ld32_async(taddr + (uint32_t)(c0 + 32), r1);
+      body(r0, c0);
+      tmem_wait_ld(r1);
+      if (k + 2 < NCH) tmem_ld32_async(taddr + (uint32_t)(c0 + 64), r0);
+      body(r1, c0 + 32);
+    }
+  }
+}
+
+// 32 values -> four 16-byte bf16 chunks of a 128-byte-swizzled row at `row`
+// (chunk c of row r at (c ^ (r & 7)) * 16), starting at chunk c16.
+__device__ __forceinline__ void put_row_chunks(uint8_t* row, int r, int c16, const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 o;
+    o.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    o.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    *reinterpret_cast<uint4*>(row + (((c16 + i) ^ (r & 7)) << 4)) = o;
+  }
+}
+
+// act(acc + bias) for one 32-column chunk (bias read as float4 from shared memory)
+__device__ __forceinline__ void act_bias_chunk(const uint32_t (&r)[32], const float* bias, int act,
+                                               float (&v)[32]) {
+  const float4* b4 = reinterpret_cast<const float4*>(bias);   // 16-byte aligned
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) {
+    const float4 b = b4[j4];
+    const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = __uint_as_float(r[4 * j4 + e]) + bb[e];
+      v[4 * j4 + e] = act == 0 ? tanh_fast(x) : fmaxf(x, 0.f);
+    }
+  }
+}
+
 // Backward-data epilogue with the activation operand already in shared
 // memory: `aux` is a 128 x BN bf16 tile loaded by TMA with the 128-byte
 // swizzle (BN/64 blocks of 128 rows x 128 bytes, 16-byte chunk c of row r at
@@ -160,25 +219,15 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool 
                                                    int h, int act, uint8_t* aux, float* cs_q,
                                                    int lane) {
   constexpr int PART = BN / (EW / 4);
-  constexpr int NCH = PART / 32;
-  const int cbase = h * PART;
-  uint32_t r[2][32];
-  tmem_ld32_async(taddr + (uint32_t)cbase, r[0]);
-#pragma unroll
-  for (int k = 0; k < NCH; ++k) {
-    const int cur = k & 1, nxt = cur ^ 1;
-    const int c0 = cbase + 32 * k;
-    tmem_wait_ld(r[cur]);
-    if (k + 1 < NCH) tmem_ld32_async(taddr + (uint32_t)(c0 + 32), r[nxt]);
+  tmem_chunks<PART / 32>(taddr, h * PART, [&](const uint32_t (&r)[32], int c0) {
     float v[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[cur][j]);
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
     uint8_t* blk = aux + (c0 / 64) * 16384 + rl * 128;
     const int c16 = (c0 % 64) / 8;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      uint4* slot = reinterpret_cast<uint4*>(blk + (((c16 + i) ^ (rl & 7)) << 4));
-      const uint4 a4 = *slot;
+      const uint4 a4 = *reinterpret_cast<const uint4*>(blk + (((c16 + i) ^ (rl & 7)) << 4));
       const uint32_t w4[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {
@@ -189,16 +238,11 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool 
         v[j] = rok ? v[j] * d0 : 0.f;
         v[j + 1] = rok ? v[j + 1] * d1 : 0.f;
       }
-      uint4 o;
-      o.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-      o.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-      o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-      o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-      *slot = o;
     }
+    put_row_chunks(blk, rl, c16, v);
     const float colsum = warp_reduce_scatter32(v);
     cs_q[col_tile + c0 + lane] += colsum;
-  }
+  });
 }
 
 // Forward epilogue, out = act(acc + bias), for one epilogue warp: its 32 rows
@@ -209,45 +253,40 @@ template <int BN, int EW>
 __device__ __forceinline__ void epi_act_stage_tile(uint32_t taddr, int col_tile, int h, int act,
                                                    const float* bias_s, uint8_t* stg, int lane) {
   constexpr int PART = BN / (EW / 4);
-  constexpr int NCH = PART / 32;
   const int cbase = h * PART;
-  uint32_t r[2][32];
-  tmem_ld32_async(taddr + (uint32_t)cbase, r[0]);
-#pragma unroll
-  for (int k = 0; k < NCH; ++k) {
-    const int cur = k & 1, nxt = cur ^ 1;
-    const int c0 = cbase + 32 * k;
-    tmem_wait_ld(r[cur]);
-    if (k + 1 < NCH) tmem_ld32_async(taddr + (uint32_t)(c0 + 32), r[nxt]);
+  tmem_chunks<PART / 32>(taddr, cbase, [&](const uint32_t (&r)[32], int c0) {
     float v[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float x = __uint_as_float(r[cur][j]) + bias_s[col_tile + c0 + j];
-      v[j] = act == 0 ? tanh_fast(x) : fmaxf(x, 0.f);
-    }
-    uint8_t* blk = stg + ((32 * k) / 64) * 4096 + lane * 128;
-    const int c16 = ((32 * k) % 64) / 8;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 o;
-      o.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-      o.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-      o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-      o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-      *reinterpret_cast<uint4*>(blk + (((c16 + i) ^ (lane & 7)) << 4)) = o;
-    }
-  }
+    act_bias_chunk(r, bias_s + col_tile + c0, act, v);
+    const int lc = c0 - cbase;   // column within the warp's part
+    put_row_chunks(stg + (lc / 64) * 4096 + lane * 128, lane, (lc % 64) / 8, v);
+  });
+}
+
+// Forward epilogue into a 128-row operand tile: out = act(acc + bias) for the
+// warp's row rl (thread = row) and columns [h*PART, (h+1)*PART) of an N-column
+// accumulator, written as bf16 into 128-row x 64-column blocks (16 KB each,
+// 128-byte swizzle) at dst + (column / 64) * 16384 -- the K-major layout of a
+// tensor-core A operand, and the layout of 32-row TMA store boxes.
+template <int N, int EW>
+__device__ __forceinline__ void epi_act_to_blocks(uint32_t taddr, int h, int act,
+                                                  const float* bias_s, uint8_t* dst, int rl) {
+  constexpr int PART = N / (EW / 4);
+  tmem_chunks<PART / 32>(taddr, h * PART, [&](const uint32_t (&r)[32], int c0) {
+    float v[32];
+    act_bias_chunk(r, bias_s + c0, act, v);
+    put_row_chunks(dst + (c0 / 64) * 16384 + rl * 128, rl, (c0 % 64) / 8, v);
+  });
 }
 
 // Column masks of the head layout (bit k = column k): first / last column of
 // each discrete head, all discrete columns, Gaussian means (column g0 + g).
 struct HeadMasks {
   uint32_t hs, he, hd, gm;
-  int g0, vcol;
+  int g0, vcol, G;
 };
 
 __device__ __forceinline__ HeadMasks head_masks(const NetShape& s) {
-  HeadMasks m{0u, 0u, 0u, 0u, 0, s.C - 1};
+  HeadMasks m{0u, 0u, 0u, 0u, 0, s.C - 1, s.G};
   int off = 0;
   for (int h = 0; h < s.NH; ++h) {
     const int n = s.head_n[h];
@@ -267,7 +306,9 @@ __device__ __forceinline__ HeadMasks head_masks(const NetShape& s) {
 // ("Proximal Policy Optimization Algorithms", sec. 3 and 5).  Heads are
 // contiguous column segments, so every per-head reduction is a segmented scan
 // over the compile-time-indexed columns and all state stays in registers.
-// amask has one bit per head: the column of the taken action.
+// exp and log are the hardware approximations (__expf/__logf, relative error
+// about 1e-6, far inside the bf16 path's tolerance).  amask has one bit per
+// head: the column of the taken action.
 template <int CP>
 __device__ __forceinline__ void row_loss_seg(const HeadMasks& hm, const LossCoef& lc, float inv_mb,
                                              const float (&z)[32], uint32_t amask,
@@ -290,13 +331,13 @@ __device__ __forceinline__ void row_loss_seg(const HeadMasks& hm, const LossCoef
   float srun = 0.f;
 #pragma unroll
   for (int k = 0; k < CP; ++k) {
-    const float e = ((hm.hd >> k) & 1u) ? expf(z[k] - u[k]) : 0.f;
+    const float e = ((hm.hd >> k) & 1u) ? __expf(z[k] - u[k]) : 0.f;
     srun = ((hm.hs >> k) & 1u) ? e : srun + e;
     w[k] = srun;
   }
 #pragma unroll
   for (int k = CP - 1; k >= 0; --k) {
-    if ((hm.he >> k) & 1u) u[k] = u[k] + logf(w[k]);
+    if ((hm.he >> k) & 1u) u[k] = u[k] + __logf(w[k]);
     else if (k + 1 < CP) u[k] = u[k + 1];
   }
   // log-probabilities, probabilities, per-head entropy (kept in dz for now)
@@ -305,7 +346,7 @@ __device__ __forceinline__ void row_loss_seg(const HeadMasks& hm, const LossCoef
   for (int k = 0; k < CP; ++k) {
     const bool d = (hm.hd >> k) & 1u;
     const float lp = z[k] - u[k];
-    const float pk = d ? expf(lp) : 0.f;
+    const float pk = d ? __expf(lp) : 0.f;
     u[k] = lp;
     w[k] = pk;
     const float hk = d ? -(pk * lp) : 0.f;
@@ -317,20 +358,31 @@ __device__ __forceinline__ void row_loss_seg(const HeadMasks& hm, const LossCoef
 #pragma unroll
   for (int k = CP - 2; k >= 0; --k)
     if (!((hm.he >> k) & 1u)) dz[k] = dz[k + 1];
-  float value = 0.f;
+  // the value and the Gaussian means, picked out of the row with selects (the
+  // Gaussian terms are computed once per dimension, not once per column)
+  float value = 0.f, mu[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int k = 0; k < CP; ++k) {
-    if ((hm.gm >> k) & 1u) {
-      const int g = k - hm.g0;
-      const float mu = z[k], ls = logstd[g], a = actc[g];
-      const float inv_var = expf(-2.f * ls);
-      logp += -0.5f * (a - mu) * (a - mu) * inv_var - ls - 0.5f * LOG_2PI;
-      ent += 0.5f + 0.5f * LOG_2PI + ls;
+    value = (k == hm.vcol) ? z[k] : value;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) mu[g] = (k == hm.g0 + g) ? z[k] : mu[g];
+  }
+  float ag[4], lsg[4], ivg[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    ag[g] = 0.f;
+    lsg[g] = 0.f;
+    ivg[g] = 0.f;
+    if (g < hm.G) {
+      ag[g] = actc[g];
+      lsg[g] = logstd[g];
+      ivg[g] = __expf(-2.f * lsg[g]);
+      logp += -0.5f * (ag[g] - mu[g]) * (ag[g] - mu[g]) * ivg[g] - lsg[g] - 0.5f * LOG_2PI;
+      ent += 0.5f + 0.5f * LOG_2PI + lsg[g];
     }
-    if (k == hm.vcol) value = z[k];
   }
   const float log_ratio = logp - logp_old;
-  const float ratio = expf(log_ratio);
+  const float ratio = __expf(log_ratio);
   const float lo = 1.f - lc.clip, hi = 1.f + lc.clip;
   const float clipped = fminf(fmaxf(ratio, lo), hi);
   const float s1 = ratio * A, s2 = clipped * A;
@@ -345,43 +397,41 @@ __device__ __forceinline__ void row_loss_seg(const HeadMasks& hm, const LossCoef
   t6[5] = (ratio - 1.f) - log_ratio;
   const float g_logp = (s1 <= s2) ? -A * ratio * inv_mb : 0.f;
   const float g_ent = -lc.ent * inv_mb;
+  const float dz_value = lc.vf * 2.f * vdiff * inv_mb;
 #pragma unroll
   for (int k = 0; k < CP; ++k) {
-    if ((hm.hd >> k) & 1u) {
-      const float dlogp = (((amask >> k) & 1u) ? 1.f : 0.f) - w[k];
-      const float dent = -w[k] * (u[k] + dz[k]);
-      dz[k] = g_logp * dlogp + g_ent * dent;
-    } else if ((hm.gm >> k) & 1u) {
-      const int g = k - hm.g0;
-      const float mu = z[k], ls = logstd[g], a = actc[g];
-      const float inv_var = expf(-2.f * ls);
-      dz[k] = g_logp * (a - mu) * inv_var;
-      const float dl = g_logp * ((a - mu) * (a - mu) * inv_var - 1.f) + g_ent;
+    const float dlogp = (((amask >> k) & 1u) ? 1.f : 0.f) - w[k];
+    const float dent = -w[k] * (u[k] + dz[k]);
+    const float dd = g_logp * dlogp + g_ent * dent;
+    dz[k] = ((hm.hd >> k) & 1u) ? dd : 0.f;
+    dz[k] = (k == hm.vcol) ? dz_value : dz[k];
+  }
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (g == j) dls[j] = dl;
-    } else if (k == hm.vcol) {
-      dz[k] = lc.vf * 2.f * vdiff * inv_mb;
-    } else {
-      dz[k] = 0.f;
+  for (int g = 0; g < 4; ++g) {
+    if (g < hm.G) {
+      const float d = ag[g] - mu[g];
+      const float dzg = g_logp * d * ivg[g];
+      dls[g] = g_logp * (d * d * ivg[g] - 1.f) + g_ent;
+#pragma unroll
+      for (int k = 0; k < CP; ++k) dz[k] = (k == hm.g0 + g) ? dzg : dz[k];
     }
   }
 }
 
-// Loss epilogue of one 128 x BN head tile (BN = CP columns): thread = row.
-// Writes dz (bf16) and accumulates the per-warp column sums of dz into cs_q,
-// the loss terms and dlogstd into lp_q.
+// Per-row loss of one 128 x BN head tile (BN = CP columns), thread = row:
+// z = TMEM accumulator + b3, then d(loss)/dz, the loss terms and dlogstd in
+// registers (all zero for rows >= M).
 template <int BN>
-__device__ __forceinline__ void epi_loss_tile(uint32_t taddr, int row, bool rok, const NetShape& s,
-                                              const HeadMasks& hm, const LossCoef& lc,
-                                              float inv_mb, const LossRows& rows,
-                                              const float* logstd, const float* bias_s,
-                                              __nv_bfloat16* dz, int lddz, float* cs_q,
-                                              float* lp_q, int lane) {
+__device__ __forceinline__ void loss_row_regs(uint32_t taddr, int row, bool rok,
+                                              const NetShape& s, const HeadMasks& hm,
+                                              const LossCoef& lc, float inv_mb,
+                                              const LossRows& rows, const float* logstd,
+                                              const float* bias_s, float (&dzr)[32],
+                                              float (&t6)[6], float (&dls)[4]) {
   float v[32];
   if constexpr (BN == 16) tmem_ld16(taddr, v);
   else tmem_ld32(taddr, v);
-  float z[32], dzr[32], t6[6], dls[4];
+  float z[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     z[j] = (j < BN && j < s.C) ? v[j] + bias_s[j] : 0.f;
@@ -395,23 +445,24 @@ __device__ __forceinline__ void epi_loss_tile(uint32_t taddr, int row, bool rok,
     uint32_t amask = 0u;
     int off = 0;
     const int32_t* a = rows.act + (int64_t)row * s.NH;
-    for (int h = 0; h < s.NH; ++h) {
-      amask |= 1u << (off + a[h]);
-      off += s.head_n[h];
+    int av[PPO_MAX_HEADS];
+#pragma unroll
+    for (int h = 0; h < PPO_MAX_HEADS; ++h) av[h] = h < s.NH ? a[h] : 0;   // loads in flight together
+#pragma unroll
+    for (int h = 0; h < PPO_MAX_HEADS; ++h) {
+      if (h < s.NH) amask |= 1u << (off + av[h]);
+      off += h < s.NH ? s.head_n[h] : 0;
     }
     row_loss_seg<BN>(hm, lc, inv_mb, z, amask, rows.actc + (int64_t)row * s.G, logstd,
                      rows.logp_old[row], rows.adv[row], rows.ret[row], dzr, t6, dls);
-    uint4* d = reinterpret_cast<uint4*>(dz + (int64_t)row * lddz);
-#pragma unroll
-    for (int i = 0; i < BN / 8; ++i) {
-      uint4 u;
-      u.x = pack_bf16x2(dzr[8 * i + 0], dzr[8 * i + 1]);
-      u.y = pack_bf16x2(dzr[8 * i + 2], dzr[8 * i + 3]);
-      u.z = pack_bf16x2(dzr[8 * i + 4], dzr[8 * i + 5]);
-      u.w = pack_bf16x2(dzr[8 * i + 6], dzr[8 * i + 7]);
-      d[i] = u;
-    }
   }
+}
+
+// Warp-level reductions of the loss epilogue: column sums of dz into cs_q,
+// the six loss terms and dlogstd into lp_q (fixed order).
+__device__ __forceinline__ void loss_warp_reduce(float (&dzr)[32], const float (&t6)[6],
+                                                 const float (&dls)[4], float* cs_q, float* lp_q,
+                                                 int lane) {
   const float colsum = warp_reduce_scatter32(dzr);
   cs_q[lane] += colsum;
 #pragma unroll
@@ -424,6 +475,32 @@ __device__ __forceinline__ void epi_loss_tile(uint32_t taddr, int row, bool rok,
     const float s4 = warp_sum(dls[k]);
     if (lane == 0) lp_q[6 + k] += s4;
   }
+}
+
+// Loss epilogue of one 128 x BN head tile: dz (bf16) to global row by row,
+// per-warp reductions into cs_q / lp_q.
+template <int BN>
+__device__ __forceinline__ void epi_loss_tile(uint32_t taddr, int row, bool rok, const NetShape& s,
+                                              const HeadMasks& hm, const LossCoef& lc,
+                                              float inv_mb, const LossRows& rows,
+                                              const float* logstd, const float* bias_s,
+                                              __nv_bfloat16* dz, int lddz, float* cs_q,
+                                              float* lp_q, int lane) {
+  float dzr[32], t6[6], dls[4];
+  loss_row_regs<BN>(taddr, row, rok, s, hm, lc, inv_mb, rows, logstd, bias_s, dzr, t6, dls);
+  if (rok) {
+    uint4* d = reinterpret_cast<uint4*>(dz + (int64_t)row * lddz);
+#pragma unroll
+    for (int i = 0; i < BN / 8; ++i) {
+      uint4 u;
+      u.x = pack_bf16x2(dzr[8 * i + 0], dzr[8 * i + 1]);
+      u.y = pack_bf16x2(dzr[8 * i + 2], dzr[8 * i + 3]);
+      u.z = pack_bf16x2(dzr[8 * i + 4], dzr[8 * i + 5]);
+      u.w = pack_bf16x2(dzr[8 * i + 6], dzr[8 * i + 7]);
+      d[i] = u;
+    }
+  }
+  loss_warp_reduce(dzr, t6, dls, cs_q, lp_q, lane);
 }
 
 // Weight-gradient epilogue: the fp32 accumulator of one 128 x bn unit tile

@@ -60,3 +60,20 @@ def conditioned_logp_old(w, ro, params):
                                ro.act_cont)
     off = np.array(LOG_RATIO_OFFSETS)[np.arange(lp.size) % len(LOG_RATIO_OFFSETS)]
     return (lp - off).astype(np.float32)
+
+
+MODES = ("fused", "per_stage", "persistent")
+
+
+def mode_kwargs(mode):
+    """Context options of the three bf16 minibatch paths: forward, loss and
+    backward-data fused in one kernel (where the network fits it), one kernel
+    per GEMM stage (the default), and the persistent cooperative kernel."""
+    return {"fused": {"fused_mlp": 1}, "per_stage": {},
+            "persistent": {"persistent_minibatch": 1}}[mode]
+
+
+def fused_applies(w):
+    Dp = -(-w.obs_dim // 64) * 64
+    return (w.precision == "bf16" and Dp == 64 and w.h1 in (128, 256) and w.h2 in (128, 256)
+            and w.out_cols <= 32 and w.n_gauss <= 4)

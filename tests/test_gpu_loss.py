@@ -20,7 +20,8 @@ import pytest
 
 import oracle
 from policy_rl_gb300 import synth
-from tests._gpu import conditioned_logp_old, dev, host, normwise, param_slices
+from tests._gpu import (MODES, conditioned_logp_old, dev, fused_applies, host, mode_kwargs,
+                        normwise, param_slices)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,10 +36,10 @@ def _inputs(w, seed=0):
     return ro, p0, adv, ret
 
 
-def _gpu_grad(w, ro, p0, adv, ret, idx, adv_stats=None, repeat=1, per_stage=0):
+def _gpu_grad(w, ro, p0, adv, ret, idx, adv_stats=None, repeat=1, mode="per_stage"):
     import torch
     import policy_rl_gb300 as P
-    cfg = P.config_from_workload(w, max_minibatch=max(len(idx), 1), persistent_minibatch=1 - per_stage)
+    cfg = P.config_from_workload(w, max_minibatch=max(len(idx), 1), **mode_kwargs(mode))
     ctx = P.Context(cfg, p0)
     st6 = torch.zeros(8, device="cuda")
     args = [dev(ro.obs), dev(ro.act_disc), dev(ro.act_cont), dev(ro.logp_old), dev(adv),
@@ -89,28 +90,34 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("per_stage", [0, 1], ids=["persistent", "per_stage"])
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name,w,mb,tol", CASES, ids=[c[0] for c in CASES])
-def test_minibatch_grad_matches_oracle(name, w, mb, tol, per_stage):
-    """bf16 cases run both the persistent minibatch kernel and the
-    one-kernel-per-stage path (fp32 mode has a single path)."""
+def test_minibatch_grad_matches_oracle(name, w, mb, tol, mode):
+    """bf16 cases run every minibatch path: the fused forward/loss/backward-data
+    kernel (where the network fits it), one kernel per GEMM stage, and the
+    persistent minibatch kernel (fp32 mode has a single path)."""
     if name == "mario_fp32":
         import dataclasses
         w = dataclasses.replace(w, precision="fp32")
-    if w.precision == "fp32" and per_stage:
+    if w.precision == "fp32" and mode != "per_stage":
         pytest.skip("fp32 mode has one path")
+    if w.precision == "bf16" and mode == "fused" and not fused_applies(w):
+        pytest.skip("the fused kernel does not take this network (per-stage path)")
     ro, p0, adv, ret = _inputs(w)
     idx = oracle.perm(5, 0, w.B)[:mb]
-    (g,), s6 = _gpu_grad(w, ro, p0, adv, ret, idx, per_stage=per_stage)
+    (g,), s6 = _gpu_grad(w, ro, p0, adv, ret, idx, mode=mode)
     _check(w, g, s6, _oracle(w, ro, p0, adv, ret, idx), tol)
 
 
-def test_persistent_and_per_stage_paths_agree():
-    w = synth.WORKLOADS["large"].scaled(T=8, N=512)
+@pytest.mark.parametrize("wname,other", [("large", "persistent"), ("mario", "persistent"),
+                                         ("mario", "fused")])
+def test_minibatch_paths_agree(wname, other):
+    """Every path computes the same gradient up to fp32 summation order."""
+    w = synth.WORKLOADS[wname].scaled(T=8, N=512)
     ro, p0, adv, ret = _inputs(w, seed=4)
     idx = oracle.perm(6, 0, w.B)[:4096]
-    (g0,), s0 = _gpu_grad(w, ro, p0, adv, ret, idx, per_stage=0)
-    (g1,), s1 = _gpu_grad(w, ro, p0, adv, ret, idx, per_stage=1)
+    (g0,), s0 = _gpu_grad(w, ro, p0, adv, ret, idx, mode="per_stage")
+    (g1,), s1 = _gpu_grad(w, ro, p0, adv, ret, idx, mode=other)
     for name, sl in param_slices(w).items():
         if sl.stop > sl.start:
             assert normwise(g0[sl], g1[sl]) < 1e-5, name
@@ -139,12 +146,12 @@ def test_bf16_close_to_fp64_definition(wname):
     _check(w, g, s6, _oracle(w, ro, p0, adv, ret, idx, bf16_operands=False), 2e-2)
 
 
-@pytest.mark.parametrize("per_stage", [0, 1])
-def test_gradient_is_deterministic(per_stage):
+@pytest.mark.parametrize("mode", MODES)
+def test_gradient_is_deterministic(mode):
     w = synth.WORKLOADS["mario"].scaled(T=32, N=256)
     ro, p0, adv, ret = _inputs(w)
     idx = oracle.perm(5, 0, w.B)[:4096]
-    grads, _ = _gpu_grad(w, ro, p0, adv, ret, idx, repeat=3, per_stage=per_stage)
+    grads, _ = _gpu_grad(w, ro, p0, adv, ret, idx, repeat=3, mode=mode)
     assert np.array_equal(grads[0], grads[1]) and np.array_equal(grads[0], grads[2])
 
 

@@ -16,7 +16,7 @@ import pytest
 
 import oracle
 from policy_rl_gb300 import synth
-from tests._gpu import conditioned_logp_old, dev, host, normwise
+from tests._gpu import MODES, conditioned_logp_old, dev, host, mode_kwargs, normwise
 
 pytestmark = pytest.mark.gpu
 
@@ -49,13 +49,13 @@ def test_adam_step_matches_oracle(prec, max_norm):
     ctx.close()
 
 
-def _update(w, seed=0, host_api=False, per_stage=0):
+def _update(w, seed=0, host_api=False, mode="per_stage"):
     import torch
     import policy_rl_gb300 as P
     ro = synth.rollout(w, seed=seed)
     p0 = synth.init_params(w, seed=seed)
     ro.logp_old = conditioned_logp_old(w, ro, p0)
-    ctx = P.Context(P.config_from_workload(w, persistent_minibatch=1 - per_stage), p0)
+    ctx = P.Context(P.config_from_workload(w, **mode_kwargs(mode)), p0)
     E, M = w.epochs, w.minibatches
     if host_api:
         stats = np.zeros((E * M, 6), np.float32)
@@ -91,10 +91,10 @@ def test_tiny_update_fp32(host_api):
     np.testing.assert_allclose(stats[:, 2:4], ref.stats[:, 2:4], rtol=1e-4)
 
 
-@pytest.mark.parametrize("per_stage", [0, 1])
-def test_small_update_bf16(per_stage):
+@pytest.mark.parametrize("mode", MODES)
+def test_small_update_bf16(mode):
     w = synth.WORKLOADS["mario"].scaled(T=16, N=256, epochs=2, minibatches=4)
-    p0, p, stats, step, ref = _update(w, per_stage=per_stage)
+    p0, p, stats, step, ref = _update(w, mode=mode)
     assert step == 8
     e = normwise(p - p0, ref.params - p0)
     assert e <= 0.1, e
