@@ -164,6 +164,19 @@ def _stage_work(stage: str, w, mb: int):
     return None
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the current kernels, cold caches (profiles/gemm_minibatch_*.md);
+# stages without such a capture report null.
+NCU_TRAFFIC = {
+    ("mario", "fwd1_gemm"): 4.255e6, ("mario", "fwd2_gemm"): 16.936e6,
+    ("mario", "head_loss_gemm"): 17.769e6, ("mario", "dact2_gemm"): 21.046e6,
+    ("mario", "dact1_gemm"): 33.724e6, ("mario", "wgrad_gemm"): 77.718e6,
+    ("large", "fwd1_gemm"): 274.635e6, ("large", "fwd2_gemm"): 488.671e6,
+    ("large", "head_loss_gemm"): 284.184e6, ("large", "dact2_gemm"): 526.086e6,
+    ("large", "dact1_gemm"): 773.370e6, ("large", "wgrad_gemm"): 1191.720e6,
+}
+
+
 def _roofline(stage, w, mb, ms_total, launches, hbm_peak, tf_peak, peak_src):
     """Roofline entry of one stage: bound = the larger of its tensor-time and
     HBM-time floors at the measured peaks; achieved = algorithmic work per
@@ -175,16 +188,17 @@ def _roofline(stage, w, mb, ms_total, launches, hbm_peak, tf_peak, peak_src):
     per_launch_s = ms_total / launches / 1e3
     t_tc = flops / (tf_peak * 1e12)
     t_hbm = nbytes / (hbm_peak * 1e9)
+    traffic = NCU_TRAFFIC.get((w.name, stage))
     if t_tc >= t_hbm:
         achieved = flops / per_launch_s / 1e12
         return {"bound": "tensor", "kernel": stage, "achieved": round(achieved, 2),
                 "peak": tf_peak, "unit": "TFLOP/s", "frac": round(achieved / tf_peak, 4),
-                "traffic": None, "peak_kind": f"bf16 sustained ({peak_src})",
+                "traffic": traffic, "peak_kind": f"bf16 sustained ({peak_src})",
                 "per_launch_us": round(per_launch_s * 1e6, 2),
                 "algorithmic_per_launch": {"flop": flops, "bytes": nbytes}}
     achieved = nbytes / per_launch_s / 1e9
     return {"bound": "hbm", "kernel": stage, "achieved": round(achieved, 1), "peak": hbm_peak,
-            "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+            "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
             "peak_kind": f"HBM copy ({peak_src})", "per_launch_us": round(per_launch_s * 1e6, 2),
             "algorithmic_per_launch": {"flop": flops, "bytes": nbytes},
             "tensor_TFLOPs": round(flops / per_launch_s / 1e12, 2) if flops else None}
