@@ -148,6 +148,10 @@ def _stage_work(stage: str, w, mb: int):
         "dact2_gemm": (2 * mb * H2 * C, a * (CP + 2 * H2)),
         "dact1_gemm": (2 * mb * H1 * H2, a * (H2 + 2 * H1)),
         "wgrad_gemm": (2 * mb * (H2 * H1 + H1 * D + C * H2), a * (H2 + H1 + H1 + Dp + H2 + 64)),
+        # fused variants: head + loss + dP2 (H2 read once); the whole fwd / loss / bwd-data
+        "head_loss_dact2": (4 * mb * C * H2, a * (2 * H2 + 64) + mb * (4 * len(w.heads) + 12)),
+        "fused_mlp": (2 * mb * (H1 * D + H2 * H1 + 2 * C * H2 + H1 * H2),
+                      a * (Dp + 2 * H1 + 2 * H2 + 64) + mb * (4 * len(w.heads) + 12)),
     }
     if stage in gemm:
         return gemm[stage]
@@ -158,6 +162,7 @@ def _stage_work(stage: str, w, mb: int):
         "gather": mb * (2 * Dp * 2 + 4 * len(w.heads) * 2 + 4 * 3 * 2),
         "adam": 30 * P, "grad_sqnorm": 4 * P,
         "grad_reduce": 4 * P,
+        "grad_reduce_adam": 34 * P,               # gradient write + norm + Adam + shadow
     }
     if stage in hbm:
         return 0, hbm[stage]
@@ -289,7 +294,7 @@ def run_ours(args, world, rank, local):
         roof["share"] = round(prof[dom][0] / total_ms, 4)
     # all tensor-core GEMM stages together: FLOPs / their summed device time
     gemm_names = ("fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm", "dact1_gemm",
-                  "wgrad_gemm")
+                  "wgrad_gemm", "head_loss_dact2", "fused_mlp")
     g_ms = sum(prof[k][0] for k in gemm_names if k in prof)
     g_flop = sum(_stage_work(k, w, mb)[0] * prof[k][1] for k in gemm_names if k in prof)
     gemm_all = ({"ms_per_update": round(g_ms, 4),

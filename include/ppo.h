@@ -94,6 +94,12 @@ typedef struct {
                                     widths 128 or 256, <= 32 head columns,
                                     <= 4 Gaussian dims), else per stage.  Same
                                     results up to fp32 summation order.      */
+    int32_t fused_loss;          /* bf16 mode: 0 (default) runs head + loss and
+                                    dP2 = (dz W3) * act'(H2) as two kernels;
+                                    1 as one kernel that keeps each tile's H2
+                                    in shared memory and reads it once (H2 in
+                                    {128, 256, 512}).  Same results up to fp32
+                                    summation order.                         */
 } ppo_config;
 
 typedef struct ppo_ctx ppo_ctx;
@@ -240,8 +246,8 @@ ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_ac
  * phases inside the persistent minibatch kernel (time between the phase
  * starts seen by its first CTA, summed over minibatches); they are not
  * separate launches. */
-#define PPO_NUM_KERNEL_STAGES 20
-#define PPO_NUM_STAGES 29
+#define PPO_NUM_KERNEL_STAGES 22
+#define PPO_NUM_STAGES 31
 /* Name of a stage (static string; "unknown" outside [0, PPO_NUM_STAGES)). */
 const char *ppo_stage_name(int32_t stage);
 

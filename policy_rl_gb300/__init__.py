@@ -54,15 +54,15 @@ def _stream(stream):
 def make_config(obs_dim, h1, h2, act=0, heads=(3, 2, 2), n_gauss=0, precision=1, clip=0.2,
                 vf_coef=0.5, ent_coef=0.01, beta1=0.9, beta2=0.999, adam_eps=1e-8,
                 max_grad_norm=0.5, max_batch=1, max_minibatch=1, max_epochs=1,
-                persistent_minibatch=0, fused_mlp=0) -> PpoConfig:
+                persistent_minibatch=0, fused_mlp=0, fused_loss=0) -> PpoConfig:
     hn = (ctypes.c_int32 * _abi.MAX_HEADS)(*(list(heads) + [0] * (_abi.MAX_HEADS - len(heads))))
     return PpoConfig(obs_dim, h1, h2, act, len(heads), hn, n_gauss, precision, clip, vf_coef,
                      ent_coef, max_grad_norm, beta1, beta2, adam_eps, max_batch, max_minibatch,
-                     max_epochs, persistent_minibatch, fused_mlp)
+                     max_epochs, persistent_minibatch, fused_mlp, fused_loss)
 
 
 def config_from_workload(w, max_batch=None, max_minibatch=None, max_epochs=None,
-                         persistent_minibatch=0, fused_mlp=0) -> PpoConfig:
+                         persistent_minibatch=0, fused_mlp=0, fused_loss=0) -> PpoConfig:
     B = w.T * w.N
     return make_config(w.obs_dim, w.h1, w.h2, w.act, tuple(w.heads), w.n_gauss,
                        1 if w.precision == "bf16" else 0, w.clip, w.vf_coef, w.ent_coef,
@@ -70,7 +70,7 @@ def config_from_workload(w, max_batch=None, max_minibatch=None, max_epochs=None,
                        max_minibatch=max_minibatch or B // w.minibatches,
                        max_epochs=max_epochs or w.epochs,
                        persistent_minibatch=persistent_minibatch,
-                       fused_mlp=fused_mlp)
+                       fused_mlp=fused_mlp, fused_loss=fused_loss)
 
 
 # ---- free functions -----------------------------------------------------------

@@ -22,8 +22,8 @@ SYMBOLS = (
     "ppo_adam_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
     "ppo_sync_status",
 )
-NUM_STAGES = 29
-NUM_KERNEL_STAGES = 20
+NUM_STAGES = 31
+NUM_KERNEL_STAGES = 22
 
 STATUS = {0: "PPO_OK", 1: "PPO_ERR_INVALID", 2: "PPO_ERR_ALIGN", 3: "PPO_ERR_CUDA",
           4: "PPO_ERR_UNSUPPORTED", 5: "PPO_ERR_TIMEOUT", 6: "PPO_ERR_NOMEM"}
@@ -45,7 +45,7 @@ class PpoConfig(ctypes.Structure):
         ("beta1", ctypes.c_double), ("beta2", ctypes.c_double), ("adam_eps", ctypes.c_double),
         ("max_batch", ctypes.c_int64), ("max_minibatch", ctypes.c_int64),
         ("max_epochs", ctypes.c_int32), ("persistent_minibatch", ctypes.c_int32),
-        ("fused_mlp", ctypes.c_int32),
+        ("fused_mlp", ctypes.c_int32), ("fused_loss", ctypes.c_int32),
     ]
 
 

@@ -64,6 +64,8 @@ struct ppo_ctx {
   // minibatch workspace
   int64_t mbmax = 0;
   bool use_fmlp = false;   // fused forward + loss + backward-data kernel
+  bool use_hl2 = false;    // head + loss + layer-2 backward-data kernel
+  unsigned* rbar = nullptr; // grid-barrier counter of the reduce + Adam kernel
   void* X = nullptr;
   // one epoch of minibatch rows gathered in permutation order (ppo_update)
   void* X_ep = nullptr;
@@ -274,7 +276,8 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
                              const int32_t* act, const float* actc, const float* logp_old,
                              const float* adv, const float* ret, const int32_t* idx, int64_t B,
                              int64_t mb, const float* adv_stats, float* stats6, cudaStream_t st,
-                             int* nsq_out = nullptr, const MbRows* pre = nullptr) {
+                             int* nsq_out = nullptr, const MbRows* pre = nullptr,
+                             const AdamArgs* adam = nullptr) {
   const NetShape& s = c->s;
   MbRows mr{c->X, c->act_mb, c->actc_mb, c->logp_mb, c->adv_mb, c->ret_mb};
   if (pre) {
@@ -349,15 +352,44 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     GemmOperands g2{H1, s.H1, c->sh.W2s, s.H1, M, s.H2, s.H1};
     PPO_CUDA(tc_gemm_bias_act(g2, P + s.ob2, s.act, H2, s.H2, c->err, kTimeoutNs, ns, st));
     c->tr.mark(ST_FWD2, st);
-    // head + loss: z = H2 W3^T + b3 -> dz
-    GemmOperands g3{H2, s.H2, c->sh.W3s, s.H2, M, s.CP, s.H2};
-    PPO_CUDA(tc_gemm_loss(g3, s, lc, rows, inv_mb, P + s.ob3, P + s.ologstd, dZ, c->lddz, c->cs3,
-                          c->lossp, c->err, kTimeoutNs, ns, st, &n3));
-    c->tr.mark(ST_LOSS, st);
-    // backward data: dP2 = (dz W3) * act'(H2);  dP1 = (dP2 W2) * act'(H1)
-    GemmOperands g4{dZ, c->lddz, c->sh.W3Ts, c->sh.ld3t, M, s.H2, s.CP};
-    PPO_CUDA(tc_gemm_dact(g4, H2, s.H2, s.act, dP2, s.H2, c->cs2, c->err, kTimeoutNs, ns, st, &n2));
-    c->tr.mark(ST_DACT2, st);
+    if (c->use_hl2) {
+      // head + loss + dP2 = (dz W3) * act'(H2) in one kernel (H2 read once)
+      HeadLossDact f{};
+      f.s = s;
+      f.M = M;
+      f.H2 = H2;
+      f.W3s = c->sh.W3s;
+      f.W3Ts = c->sh.W3Ts;
+      f.ld3t = c->sh.ld3t;
+      f.b3 = P + s.ob3;
+      f.logstd = P + s.ologstd;
+      f.dZ = dZ;
+      f.dP2 = dP2;
+      f.lddz = c->lddz;
+      f.lc = lc;
+      f.rows = rows;
+      f.inv_mb = inv_mb;
+      f.cs2 = c->cs2;
+      f.cs3 = c->cs3;
+      f.lossp = c->lossp;
+      f.err = c->err;
+      f.timeout_ns = kTimeoutNs;
+      PPO_CUDA(hl2_launch(f, ns, st, &n3));
+      n2 = n3;
+      c->tr.mark(ST_LOSS_DACT2, st);
+    } else {
+      // head + loss: z = H2 W3^T + b3 -> dz
+      GemmOperands g3{H2, s.H2, c->sh.W3s, s.H2, M, s.CP, s.H2};
+      PPO_CUDA(tc_gemm_loss(g3, s, lc, rows, inv_mb, P + s.ob3, P + s.ologstd, dZ, c->lddz,
+                            c->cs3, c->lossp, c->err, kTimeoutNs, ns, st, &n3));
+      c->tr.mark(ST_LOSS, st);
+      // backward data: dP2 = (dz W3) * act'(H2)
+      GemmOperands g4{dZ, c->lddz, c->sh.W3Ts, c->sh.ld3t, M, s.H2, s.CP};
+      PPO_CUDA(tc_gemm_dact(g4, H2, s.H2, s.act, dP2, s.H2, c->cs2, c->err, kTimeoutNs, ns, st,
+                            &n2));
+      c->tr.mark(ST_DACT2, st);
+    }
+    // backward data: dP1 = (dP2 W2) * act'(H1)
     GemmOperands g5{dP2, s.H2, c->sh.W2Ts, s.H2, M, s.H1, s.H2};
     PPO_CUDA(tc_gemm_dact(g5, H1, s.H1, s.act, dP1, s.H1, c->cs1, c->err, kTimeoutNs, ns, st, &n1));
     c->tr.mark(ST_DACT1, st);
@@ -428,14 +460,19 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     ra.pb3 = c->cs3; ra.nb3 = n3; ra.ldb3 = s.CP;
     ra.ploss = c->lossp; ra.nl = n3;
   }
+  if (adam) {   // gradient assembly, clip and Adam in one cooperative launch
+    ra.sq_part = c->sq;
+    PPO_CUDA(launch_reduce_adam(ra, *adam, c->rbar, c->err, kTimeoutNs, c->num_sms, st));
+    c->tr.mark(ST_REDUCE_ADAM, st);
+    return PPO_OK;
+  }
   PPO_CUDA(launch_reduce(ra, st));
   c->tr.mark(ST_REDUCE, st);
   if (nsq_out) *nsq_out = reduce_blocks(s);
   return PPO_OK;
 }
 
-ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t st,
-                        int nsq = 0) {
+AdamArgs make_adam_args(ppo_ctx* c, float lr, float* grad_norm_out, int nsq) {
   AdamArgs a{};
   a.p = c->params;
   a.g = c->grad;
@@ -457,6 +494,12 @@ ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t
   a.grad_norm_out = grad_norm_out;
   a.s = c->s;
   a.sh = c->sh;
+  return a;
+}
+
+ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t st,
+                        int nsq = 0) {
+  const AdamArgs a = make_adam_args(c, lr, grad_norm_out, nsq);
   PPO_CUDA(launch_adam(a, st, &c->tr));
   return PPO_OK;
 }
@@ -578,6 +621,8 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
   const __nv_bfloat16* packed = nullptr;
   if (c->use_mk)   // grid-barrier counters start at zero (also after an aborted launch)
     PPO_CUDA(cudaMemsetAsync(c->gbar, 0, 2 * sizeof(unsigned), st));
+  else
+    PPO_CUDA(cudaMemsetAsync(c->rbar, 0, sizeof(unsigned), st));
   if (c->bf16) {
     PPO_CUDA(launch_pack_obs(obs, B, c->s.D, c->s.Dp, c->obs_packed, st));
     c->tr.mark(ST_PACK, st);
@@ -610,10 +655,9 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
         const int64_t r0 = (int64_t)k * mb;
         const MbRows mr{static_cast<uint8_t*>(ep.X) + r0 * xrow, ep.act + r0 * NH,
                         ep.actc + r0 * G, ep.logp + r0, ep.adv + r0, ep.ret + r0};
-        int nsq = 0;
+        const AdamArgs aa = make_adam_args(c, lr, nullptr, 0);
         TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
-                              c->advstats, st6, st, &nsq, &mr));
-        TRY(enqueue_adam(c, lr, nullptr, st, nsq));
+                              c->advstats, st6, st, nullptr, &mr, &aa));
       }
     }
   }
@@ -673,6 +717,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   c->bf16 = cfg->precision == 1;
   c->use_mk = c->bf16 && cfg->persistent_minibatch != 0;
   c->use_fmlp = c->bf16 && !c->use_mk && cfg->fused_mlp != 0 && fmlp_supported(s);
+  c->use_hl2 = c->bf16 && !c->use_mk && cfg->fused_loss != 0 && hl2_supported(s);
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (c->num_sms < 1) c->num_sms = 1;
   c->mbmax = cfg->max_minibatch;
@@ -699,6 +744,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->done_ctr, 1);
   A(c->err, 1);
   A(c->sq, std::max(4096, reduce_blocks(s)));
+  A(c->rbar, 1);
   if (c->bf16) {
     c->sh.ld3t = 64;
     A(c->sh.W1s, (int64_t)s.H1 * s.Dp);
@@ -769,6 +815,8 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
 #undef A
   if (c->bf16 && tc_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (c->use_fmlp && fmlp_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
+  if (c->use_hl2 && hl2_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
+  if (reduce_adam_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (c->use_mk && mk_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (h_init_params) {
     if (cudaMemcpy(c->params, h_init_params, sizeof(float) * P, cudaMemcpyHostToDevice) !=
@@ -958,7 +1006,7 @@ const char* ppo_stage_name(int32_t stage) {
       "pack_obs", "gae_scan", "gae_finalize", "gae_normalize", "perm_hist", "perm_scan",
       "perm_scatter", "gather", "fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm",
       "dact1_gemm", "wgrad_gemm", "grad_reduce", "grad_sqnorm", "adam", "weight_shadows",
-      "minibatch_persistent", "fused_mlp"};
+      "minibatch_persistent", "fused_mlp", "grad_reduce_adam", "head_loss_dact2"};
   static const char* phases[kMkPhases] = {
       "phase:gather", "phase:fwd1", "phase:fwd2", "phase:head_loss", "phase:dact2",
       "phase:dact1", "phase:wgrad", "phase:grad_reduce", "phase:adam"};

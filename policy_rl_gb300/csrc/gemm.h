@@ -151,6 +151,11 @@ struct AdamArgs {
   Shadows sh;
 };
 cudaError_t launch_adam(const AdamArgs& a, cudaStream_t st, const Trace* tr = nullptr);
+// Gradient assembly + clip + Adam in one cooperative launch (optim.cu); *bar
+// is a zeroed grid-barrier counter (cleared again by the kernel).
+cudaError_t reduce_adam_prepare();
+cudaError_t launch_reduce_adam(const ReduceArgs& ra, const AdamArgs& aa, unsigned* bar, int* err,
+                               uint64_t limit_ns, int num_sms, cudaStream_t st);
 
 // ---- persistent minibatch kernel (mk.cu) ------------------------------------
 // Everything the fused bf16 minibatch step needs: the five K-major GEMMs, the
@@ -208,6 +213,27 @@ struct FusedMlp {
   int* err;
   uint64_t timeout_ns;
 };
+// Head + loss + backward-data through the last hidden layer (hl2.cu):
+// dz [M][lddz] and dP2 [M][H2] from H2 [M][H2], all bf16.
+struct HeadLossDact {
+  NetShape s;
+  int M;
+  const __nv_bfloat16 *H2, *W3s, *W3Ts;
+  int ld3t;
+  const float *b3, *logstd;
+  __nv_bfloat16 *dZ, *dP2;
+  int lddz;
+  LossCoef lc;
+  LossRows rows;
+  float inv_mb;
+  float *cs2, *cs3, *lossp;   // per-CTA partial rows (grid of them)
+  int* err;
+  uint64_t timeout_ns;
+};
+bool hl2_supported(const NetShape& s);
+cudaError_t hl2_prepare();
+cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int* grid_out);
+
 bool fmlp_supported(const NetShape& s);
 cudaError_t fmlp_prepare();
 cudaError_t fmlp_launch(const FusedMlp& f, int num_sms, cudaStream_t st, int* grid_out);

@@ -9,6 +9,7 @@
 // one coalesced grid-stride pass.
 #include "common.cuh"
 #include "gemm.h"
+#include "tc_ptx.cuh"
 
 namespace ppo {
 
@@ -33,14 +34,28 @@ __device__ __forceinline__ float warp_rows_sum(const float* base, int rows, int6
   return warp_sum(v);
 }
 
-__global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int weight_blocks) {
-  pdl_wait();
-  pdl_trigger();
+// Sum of n <= kMaxSplits split-K partials q[0], q[st], ... in split order, with
+// every load issued before the first add (one memory latency, not n).
+constexpr int kMaxSplits = 64;
+__device__ __forceinline__ float split_sum(const float* q, int64_t st, int n) {
+  float x[kMaxSplits];
+#pragma unroll
+  for (int sp = 0; sp < kMaxSplits; ++sp) x[sp] = sp < n ? q[sp * st] : 0.f;
+  float v = 0.f;
+#pragma unroll
+  for (int sp = 0; sp < kMaxSplits; ++sp)
+    if (sp < n) v += x[sp];
+  return v;
+}
+
+// The reduce work of virtual block vb (weight elements for vb < weight_blocks,
+// bias / log-std / loss-statistic warps above); writes sq_part[vb].
+__device__ __forceinline__ void reduce_block(const ReduceArgs& a, int vb, int weight_blocks) {
   const NetShape& s = a.s;
   const int nW1 = s.H1 * s.D, nW2 = s.H2 * s.H1, nW3 = s.C * s.H2;
   double sq = 0.0;
-  if ((int)blockIdx.x < weight_blocks) {
-    const int e = blockIdx.x * kRedThreads + threadIdx.x;
+  if (vb < weight_blocks) {
+    const int e = vb * kRedThreads + threadIdx.x;
     float v = 0.f;
     int i = -1;
     if (e < nW1) {
@@ -48,23 +63,20 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int w
       const int j = e / s.D, k = e - j * s.D;
       const float* q = a.pW1 + (int64_t)j * a.ld1 + k;
       const int64_t st = (int64_t)s.H1 * a.ld1;
-#pragma unroll 8
-      for (int sp = 0; sp < a.s1; ++sp) v += q[sp * st];
+      v = split_sum(q, st, a.s1);
     } else if (e < nW1 + nW2) {
       const int r = e - nW1;
       i = (int)s.oW2 + r;
       const float* q = a.pW2 + r;
       const int64_t st = (int64_t)s.H2 * s.H1;
-#pragma unroll 8
-      for (int sp = 0; sp < a.s2; ++sp) v += q[sp * st];
+      v = split_sum(q, st, a.s2);
     } else if (e < nW1 + nW2 + nW3) {
       const int r = e - nW1 - nW2;
       i = (int)s.oW3 + r;
       const int c = r / s.H2, j = r - c * s.H2;
       const float* q = a.pW3t + (int64_t)j * a.ld3 + c;
       const int64_t st = (int64_t)s.H2 * a.ld3;
-#pragma unroll 8
-      for (int sp = 0; sp < a.s3; ++sp) v += q[sp * st];
+      v = split_sum(q, st, a.s3);
     }
     if (i >= 0) {
       a.grad[i] = v;
@@ -72,7 +84,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int w
     }
   } else {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int e = ((int)blockIdx.x - weight_blocks) * kRedWarps + warp;
+    const int e = (vb - weight_blocks) * kRedWarps + warp;
     const int nb = s.H1 + s.H2 + s.C + s.G;
     if (e < nb) {
       float v;
@@ -112,9 +124,15 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int w
     if (threadIdx.x == 0) {
       double t = 0.0;
       for (int w = 0; w < kRedWarps; ++w) t += ws[w];
-      a.sq_part[blockIdx.x] = t;
+      a.sq_part[vb] = t;
     }
   }
+}
+
+__global__ void __launch_bounds__(kRedThreads) reduce_kernel(ReduceArgs a, int weight_blocks) {
+  pdl_wait();
+  pdl_trigger();
+  reduce_block(a, blockIdx.x, weight_blocks);
 }
 
 __global__ void __launch_bounds__(kNormThreads)
@@ -165,12 +183,14 @@ __device__ __forceinline__ void write_shadow(const NetShape& s, const Shadows& s
   }
 }
 
-__global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
+// Clip + Adam over the grid-stride share of block `block` of `nblocks`; the
+// last block to finish publishes the step count and the beta powers (and
+// clears *extra_ctr when given).
+__device__ __forceinline__ void adam_body(const AdamArgs& a, int block, int nblocks,
+                                          unsigned* extra_ctr) {
   __shared__ float s_coef, s_norm, s_ibc1, s_ibc2;
   __shared__ long long s_t;
   __shared__ double s_ws[kAdamThreads / kWarp];
-  pdl_wait();
-  pdl_trigger();
   {
     // every block sums the norm partials in the same fixed order
     double ss = 0.0;
@@ -201,7 +221,7 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
   const bool shadows = a.sh.W1s != nullptr;
   const int P = (int)a.P;
   const int P4 = P / 4;
-  const int stride = gridDim.x * kAdamThreads;
+  const int stride = nblocks * kAdamThreads;
   auto step = [&](float g, float m0, float v0, float p0, float& m, float& v, float& p) {
     g *= coef;
     m = b1 * m0 + omb1 * g;
@@ -213,7 +233,7 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
   float4* __restrict__ V4 = reinterpret_cast<float4*>(a.v);
   float4* __restrict__ PP4 = reinterpret_cast<float4*>(a.p);
 #pragma unroll 2
-  for (int i = blockIdx.x * kAdamThreads + threadIdx.x; i < P4; i += stride) {
+  for (int i = block * kAdamThreads + threadIdx.x; i < P4; i += stride) {
     const float4 g4 = __ldcs(G4 + i);
     const float4 m4 = __ldcs(M4 + i);
     const float4 v4 = __ldcs(V4 + i);
@@ -233,7 +253,7 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
       write_shadow(a.s, a.sh, 4 * i + 3, po.w);
     }
   }
-  for (int i = P4 * 4 + blockIdx.x * kAdamThreads + threadIdx.x; i < P; i += stride) {
+  for (int i = P4 * 4 + block * kAdamThreads + threadIdx.x; i < P; i += stride) {
     float m, v, p;
     step(a.g[i], a.m[i], a.v[i], a.p[i], m, v, p);
     a.m[i] = m;
@@ -247,15 +267,63 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
   if (threadIdx.x == 0) {
     __threadfence();
     const unsigned prev = atomicAdd(a.done_ctr, 1u);
-    if (prev == gridDim.x - 1) {
+    if (prev == (unsigned)nblocks - 1) {
       *a.step = (int64_t)s_t;
       a.beta_pow[0] *= a.b1;
       a.beta_pow[1] *= a.b2;
       if (a.grad_norm_out) *a.grad_norm_out = s_norm;
       *a.done_ctr = 0u;
+      if (extra_ctr) *extra_ctr = 0u;
       __threadfence();
     }
   }
+}
+
+__global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  adam_body(a, blockIdx.x, gridDim.x, nullptr);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Gradient assembly, then clip + Adam, in one cooperative launch: the grid
+// reduces the split-K / per-CTA partials (virtual blocks 0..nvb), meets at a
+// grid barrier (bounded: on expiry it latches kDevTimeout and skips Adam), then
+// runs Adam with the norm of all nvb partial sums.  Same arithmetic and order
+// as reduce_kernel followed by adam_kernel.
+__global__ void __launch_bounds__(kRedThreads)
+reduce_adam_kernel(ReduceArgs ra, AdamArgs aa, int weight_blocks, int nvb, unsigned* bar,
+                   int* err, uint64_t limit_ns) {
+  __shared__ int s_abort;
+  for (int vb = blockIdx.x; vb < nvb; vb += gridDim.x) {
+    reduce_block(ra, vb, weight_blocks);
+    __syncthreads();   // the block's shared partials are reused by the next virtual block
+  }
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    __threadfence();
+    atomicAdd(bar, 1u);
+    if (ld_acquire_u32(bar) < gridDim.x) {
+      const uint64_t t0 = ptx::globaltimer();
+      while (ld_acquire_u32(bar) < gridDim.x) {
+        if (ptx::globaltimer() - t0 > limit_ns) {
+          atomicOr(err, kDevTimeout);
+          s_abort = 1;
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  if (s_abort) return;
+  aa.nsq = nvb;
+  adam_body(aa, blockIdx.x, gridDim.x, bar);
 }
 
 __global__ void __launch_bounds__(kAdamThreads)
@@ -287,6 +355,37 @@ int reduce_blocks(const NetShape& s) {
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
   return launch_pdl(reduce_kernel, dim3(reduce_blocks(a.s)), dim3(kRedThreads), 0, st, a,
                     reduce_weight_blocks(a.s));
+}
+
+int g_reduce_adam_blocks_per_sm = 0;
+
+cudaError_t reduce_adam_prepare() {
+  if (g_reduce_adam_blocks_per_sm > 0) return cudaSuccess;
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reduce_adam_kernel, kRedThreads, 0);
+  if (e != cudaSuccess) return e;
+  g_reduce_adam_blocks_per_sm = n < 1 ? 1 : n;
+  return cudaSuccess;
+}
+
+cudaError_t launch_reduce_adam(const ReduceArgs& ra, const AdamArgs& aa, unsigned* bar, int* err,
+                               uint64_t limit_ns, int num_sms, cudaStream_t st) {
+  if (g_reduce_adam_blocks_per_sm <= 0) return cudaErrorInitializationError;
+  const int nvb = reduce_blocks(ra.s);
+  int grid = num_sms * (g_reduce_adam_blocks_per_sm < 4 ? g_reduce_adam_blocks_per_sm : 4);
+  if (grid > nvb) grid = nvb;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRedThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;   // all blocks resident: they meet at a barrier
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, reduce_adam_kernel, ra, aa, reduce_weight_blocks(ra.s), nvb, bar,
+                            err, limit_ns);
 }
 
 cudaError_t launch_adam(const AdamArgs& a0, cudaStream_t st, const Trace* tr) {

@@ -110,7 +110,8 @@ def test_minibatch_grad_matches_oracle(name, w, mb, tol, mode):
 
 
 @pytest.mark.parametrize("wname,other", [("large", "persistent"), ("mario", "persistent"),
-                                         ("mario", "fused")])
+                                         ("mario", "fused"), ("large", "fused_loss"),
+                                         ("mario", "fused_loss")])
 def test_minibatch_paths_agree(wname, other):
     """Every path computes the same gradient up to fp32 summation order."""
     w = synth.WORKLOADS[wname].scaled(T=8, N=512)
