@@ -738,7 +738,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->m, P);
   A(c->v, P);
   A(c->step, 1);
-  A(c->beta_pow, 2);
+  A(c->beta_pow, 4);
   A(c->gbar, 2);
   A(c->phase_ns, kMkPhases);
   A(c->done_ctr, 1);
@@ -824,7 +824,8 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
       return fail(PPO_ERR_CUDA);
   }
   {
-    const double one[2] = {1.0, 1.0};   // beta^0
+    // beta^0 and the first step's bias corrections 1 / (1 - beta^1)
+    const double one[4] = {1.0, 1.0, 1.0 / (1.0 - cfg->beta1), 1.0 / (1.0 - cfg->beta2)};
     if (cudaMemcpy(c->beta_pow, one, sizeof one, cudaMemcpyHostToDevice) != cudaSuccess)
       return fail(PPO_ERR_CUDA);
   }

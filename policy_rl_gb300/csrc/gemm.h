@@ -144,7 +144,8 @@ struct AdamArgs {
   double b1, b2;      // for the bias corrections 1 - beta^t
   float omb1, omb2;   // 1 - beta1, 1 - beta2 (rounded once from double)
   int64_t* step;
-  double* beta_pow;        // {beta1^step, beta2^step}, advanced by the last block
+  double* beta_pow;        // {beta1^step, beta2^step, 1/(1-beta1^(step+1)), 1/(1-beta2^(step+1))},
+                           // advanced by the last block
   unsigned* done_ctr;
   float* grad_norm_out;
   NetShape s;

@@ -44,8 +44,15 @@ struct Cfg {
   // backward-data kernels keep two TMA-loaded activation tiles (aux), which
   // also stage their output; forward kernels stage their output per warp
   static constexpr int AUX_SLOT = EPI == EPI_DACT ? BM * BN * 2 : 0;
+#ifndef PPO_DACT_AUX_SLOTS
+#define PPO_DACT_AUX_SLOTS 2
+#endif
+#ifndef PPO_DACT_STAGES
+#define PPO_DACT_STAGES 4
+#endif
+  static constexpr int NAUX = EPI == EPI_DACT ? PPO_DACT_AUX_SLOTS : 2;
   static constexpr int STG_WARP = EPI == EPI_BIAS_ACT ? (BN / 2 / 64) * 4096 : 0;
-  static constexpr int S = EPI == EPI_DACT ? 4
+  static constexpr int S = EPI == EPI_DACT ? PPO_DACT_STAGES
                          : EPI == EPI_BIAS_ACT ? (BN >= 256 ? 3 : 5)
                                                : (BN >= 128 ? 6 : 8);
   static constexpr int A_BYTES = BM * BK * 2;
@@ -53,7 +60,7 @@ struct Cfg {
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   static constexpr int CTRL = 512;
-  static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + 2 * (size_t)AUX_SLOT +
+  static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + NAUX * (size_t)AUX_SLOT +
                                  8 * (size_t)STG_WARP + CTRL + 4 * kColsumCap * 4 +
                                  8 * kLossPartials * 4 + kColsumCap * 4;
 };
@@ -83,7 +90,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   uint8_t* auxs = gbase + (size_t)S * C::STAGE;          // [2][BM x BN] (DACT only)
-  uint8_t* stgs = auxs + 2 * (size_t)C::AUX_SLOT;        // [8 warps][STG_WARP] (BIAS_ACT only)
+  uint8_t* stgs = auxs + C::NAUX * (size_t)C::AUX_SLOT;  // [8 warps][STG_WARP] (BIAS_ACT only)
   uint8_t* ctrl = stgs + 8 * (size_t)C::STG_WARP;
   Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), S};
   uint64_t* xbar = reinterpret_cast<uint64_t*>(ctrl) + Ctrl::count(S);  // aux full[2], empty[2]
@@ -149,8 +156,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
         if constexpr (EPI == EPI_DACT) {
           // this tile's activation operand, one slot of two, ahead of its k-loop
-          const int xs = lt & 1;
-          const uint32_t xu = lt >> 1;
+          const int xs = lt % C::NAUX;
+          const uint32_t xu = lt / C::NAUX;
           if (!wait_bar(smem_u32(&xbar[2 + xs]), (xu & 1) ^ 1, g)) { ok = false; break; }
           mbar_arrive_expect_tx(smem_u32(&xbar[xs]), C::AUX_SLOT);
           for (int j = 0; j < BN / 64; ++j)
@@ -247,8 +254,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if constexpr (EPI == EPI_DACT) {
         // tile tc uses aux slot tc & 1 (same tile order as the producer); the
         // result overwrites the warp's rows of the slot and leaves by TMA
-        const int xs = tc & 1;
-        if (!wait_bar(smem_u32(&xbar[xs]), (tc >> 1) & 1, g)) break;
+        const int xs = tc % C::NAUX;
+        if (!wait_bar(smem_u32(&xbar[xs]), (tc / C::NAUX) & 1, g)) break;
         uint8_t* slot = auxs + xs * C::AUX_SLOT;
         epi_dact_smem_tile<BN, EW>(taddr, q * 32 + lane, rok, tn * BN, h, p.act, slot,
                                    cs + q * kColsumCap, lane);
@@ -298,8 +305,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (uint32_t it = consumed; it < issued; ++it)
         drain_wait(cb.full(it % S), (it / S) & 1, p.timeout_ns);
       const uint32_t xi = cnt[2];   // the last two activation-tile loads
-      for (uint32_t l = xi >= 2 ? xi - 2 : 0; l < xi; ++l)
-        drain_wait(smem_u32(&xbar[l & 1]), (l >> 1) & 1, p.timeout_ns);
+      for (uint32_t l = xi >= (uint32_t)C::NAUX ? xi - C::NAUX : 0; l < xi; ++l)
+        drain_wait(smem_u32(&xbar[l % C::NAUX]), (l / C::NAUX) & 1, p.timeout_ns);
     }
     if (warp == 1 && lane == 0) {
       tc_commit(cb.drain());

@@ -616,6 +616,8 @@ mk_kernel(const __grid_constant__ MkMaps maps, const MkParams p) {
             *a.step += 1;
             a.beta_pow[0] *= a.b1;
             a.beta_pow[1] *= a.b2;
+            a.beta_pow[2] = 1.0 / (1.0 - a.beta_pow[0] * a.b1);   // next step's corrections
+            a.beta_pow[3] = 1.0 / (1.0 - a.beta_pow[1] * a.b2);
             gbar[0] = 0u;
             gbar[1] = 0u;
             __threadfence();

@@ -183,6 +183,42 @@ __device__ __forceinline__ void write_shadow(const NetShape& s, const Shadows& s
   }
 }
 
+// write_shadow for the four consecutive parameters i0..i0+3 (region starts are
+// multiples of 4 in bf16 mode): one row/column division, then increments.
+__device__ __forceinline__ void write_shadow4(const NetShape& s, const Shadows& sh, int i0,
+                                              float4 p4) {
+  const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+  if (i0 < (int)s.ob1) {
+    const int r = i0 - (int)s.oW1;
+    int j = r / s.D, k = r - j * s.D;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (i0 + e < (int)s.ob1) sh.W1s[j * s.Dp + k] = __float2bfloat16_rn(pv[e]);
+      if (++k == s.D) { k = 0; ++j; }
+    }
+  } else if (i0 >= (int)s.oW2 && i0 < (int)s.ob2) {
+    const int r = i0 - (int)s.oW2;
+    int j = r / s.H1, k = r - j * s.H1;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(pv[e]);
+      sh.W2s[r + e] = b;
+      sh.W2Ts[k * s.H2 + j] = b;
+      if (++k == s.H1) { k = 0; ++j; }
+    }
+  } else if (i0 >= (int)s.oW3 && i0 < (int)s.ob3) {
+    const int r = i0 - (int)s.oW3;
+    int c = r / s.H2, j = r - c * s.H2;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(pv[e]);
+      sh.W3s[r + e] = b;
+      sh.W3Ts[j * sh.ld3t + c] = b;
+      if (++j == s.H2) { j = 0; ++c; }
+    }
+  }
+}
+
 // Clip + Adam over the grid-stride share of block `block` of `nblocks`; the
 // last block to finish publishes the step count and the beta powers (and
 // clears *extra_ctr when given).
@@ -209,10 +245,10 @@ __device__ __forceinline__ void adam_body(const AdamArgs& a, int block, int nblo
     s_coef = coef;
     s_norm = norm;
     s_t = (long long)(*a.step) + 1;
-    // bias corrections 1 - beta^t from the running powers beta^(t-1) (device
-    // state, advanced by the last block), one multiply each -- no pow()
-    s_ibc1 = (float)(1.0 / (1.0 - a.beta_pow[0] * a.b1));
-    s_ibc2 = (float)(1.0 / (1.0 - a.beta_pow[1] * a.b2));
+    // bias corrections 1 / (1 - beta^t), computed in double by the block that
+    // finished the previous step (no pow(), no division on this path)
+    s_ibc1 = (float)a.beta_pow[2];
+    s_ibc2 = (float)a.beta_pow[3];
   }
   __syncthreads();
   const float coef = s_coef, ibc1 = s_ibc1, ibc2 = s_ibc2;
@@ -246,12 +282,7 @@ __device__ __forceinline__ void adam_body(const AdamArgs& a, int block, int nblo
     __stcs(M4 + i, mo);
     __stcs(V4 + i, vo);
     __stcs(PP4 + i, po);
-    if (shadows) {
-      write_shadow(a.s, a.sh, 4 * i + 0, po.x);
-      write_shadow(a.s, a.sh, 4 * i + 1, po.y);
-      write_shadow(a.s, a.sh, 4 * i + 2, po.z);
-      write_shadow(a.s, a.sh, 4 * i + 3, po.w);
-    }
+    if (shadows) write_shadow4(a.s, a.sh, 4 * i, po);
   }
   for (int i = P4 * 4 + block * kAdamThreads + threadIdx.x; i < P; i += stride) {
     float m, v, p;
@@ -271,6 +302,8 @@ __device__ __forceinline__ void adam_body(const AdamArgs& a, int block, int nblo
       *a.step = (int64_t)s_t;
       a.beta_pow[0] *= a.b1;
       a.beta_pow[1] *= a.b2;
+      a.beta_pow[2] = 1.0 / (1.0 - a.beta_pow[0] * a.b1);   // next step's corrections
+      a.beta_pow[3] = 1.0 / (1.0 - a.beta_pow[1] * a.b2);
       if (a.grad_norm_out) *a.grad_norm_out = s_norm;
       *a.done_ctr = 0u;
       if (extra_ctr) *extra_ctr = 0u;
@@ -372,6 +405,8 @@ cudaError_t launch_reduce_adam(const ReduceArgs& ra, const AdamArgs& aa, unsigne
                                uint64_t limit_ns, int num_sms, cudaStream_t st) {
   if (g_reduce_adam_blocks_per_sm <= 0) return cudaErrorInitializationError;
   const int nvb = reduce_blocks(ra.s);
+  // up to 4 resident blocks per SM: one virtual block of reduce work each at
+  // the usual sizes (one block per SM measured slower: serial reduce work)
   int grid = num_sms * (g_reduce_adam_blocks_per_sm < 4 ? g_reduce_adam_blocks_per_sm : 4);
   if (grid > nvb) grid = nvb;
   cudaLaunchConfig_t cfg = {};
