@@ -414,8 +414,10 @@ cudaError_t launch_reduce_adam(const ReduceArgs& ra, const AdamArgs& aa, unsigne
   cfg.blockDim = dim3(kRedThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
+  // cooperative: all blocks resident, they meet at a barrier.  (Adding
+  // programmatic serialization to this launch measured 3 % slower per update.)
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;   // all blocks resident: they meet at a barrier
+  attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
