@@ -27,10 +27,22 @@ constexpr int kAdamThreads = 256;
 // produced (fixed order), for the clip norm.
 constexpr int kRedWarps = kRedThreads / kWarp;
 
+// Lane l sums rows l, l+32, ... in order (eight loads in flight per lane), then
+// a fixed xor-shuffle tree.
 __device__ __forceinline__ float warp_rows_sum(const float* base, int rows, int64_t stride) {
   const int lane = threadIdx.x % kWarp;
   float v = 0.f;
-  for (int b = lane; b < rows; b += kWarp) v += base[(int64_t)b * stride];
+  for (int b0 = lane; b0 < rows; b0 += 8 * kWarp) {
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int b = b0 + u * kWarp;
+      x[u] = b < rows ? base[(int64_t)b * stride] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (b0 + u * kWarp < rows) v += x[u];
+  }
   return warp_sum(v);
 }
 
