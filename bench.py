@@ -170,7 +170,8 @@ def _stage_work(stage: str, w, mb: int):
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of the current kernels, cold caches (profiles/gemm_minibatch_*.md);
+# ncu capture of the current kernels, cold caches (profiles/gemm_minibatch_*.md,
+# profiles/reduce_adam_mario.md);
 # stages without such a capture report null.
 NCU_TRAFFIC = {
     ("mario", "fwd1_gemm"): 4.255e6, ("mario", "fwd2_gemm"): 16.936e6,
@@ -179,6 +180,7 @@ NCU_TRAFFIC = {
     ("large", "fwd1_gemm"): 274.635e6, ("large", "fwd2_gemm"): 488.671e6,
     ("large", "head_loss_gemm"): 284.184e6, ("large", "dact2_gemm"): 526.086e6,
     ("large", "dact1_gemm"): 773.370e6, ("large", "wgrad_gemm"): 1191.720e6,
+    ("mario", "grad_reduce_adam"): 13.008e6,
 }
 
 
