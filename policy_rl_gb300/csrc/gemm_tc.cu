@@ -39,6 +39,16 @@ using namespace tc;
 
 constexpr int kThreads = 192;
 
+// Epilogue warps: 16 for the element-wise epilogues of 256-column tiles (four
+// per TMEM lane quarter, each taking 64 of the tile's columns -- one TMA store
+// block; measured faster than 8), 8 otherwise (two per lane quarter).  The
+// per-row loss epilogue runs two groups of four warps on alternate tiles (one
+// accumulator each; its 168 registers per thread leave no room for more).
+template <int BN, int EPI>
+__host__ __device__ constexpr int epi_warps() { return (EPI != EPI_LOSS && BN >= 256) ? 16 : 8; }
+template <int BN, int EPI>
+__host__ __device__ constexpr int gemm_threads() { return 2 * kWarp + kWarp * epi_warps<BN, EPI>(); }
+
 template <int BN, int EPI>
 struct Cfg {
   // backward-data kernels keep two TMA-loaded activation tiles (aux), which
@@ -51,7 +61,9 @@ struct Cfg {
 #define PPO_DACT_STAGES 4
 #endif
   static constexpr int NAUX = EPI == EPI_DACT ? PPO_DACT_AUX_SLOTS : 2;
-  static constexpr int STG_WARP = EPI == EPI_BIAS_ACT ? (BN / 2 / 64) * 4096 : 0;
+  // per-warp output staging: 64-column blocks of 32 rows (4 KB); a warp takes
+  // 64 columns of a 256-column tile (16 epilogue warps) or half a 128-column one
+  static constexpr int STG_WARP = EPI == EPI_BIAS_ACT ? 4096 : 0;
   static constexpr int S = EPI == EPI_DACT ? PPO_DACT_STAGES
                          : EPI == EPI_BIAS_ACT ? (BN >= 256 ? 3 : 5)
                                                : (BN >= 128 ? 6 : 8);
@@ -61,37 +73,29 @@ struct Cfg {
   static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   static constexpr int CTRL = 512;
   static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + NAUX * (size_t)AUX_SLOT +
-                                 8 * (size_t)STG_WARP + CTRL + 4 * kColsumCap * 4 +
+                                 epi_warps<BN, EPI>() * (size_t)STG_WARP + CTRL + 4 * kColsumCap * 4 +
                                  8 * kLossPartials * 4 + kColsumCap * 4;
 };
 
 
 
 // ---------------------------------------------------------------------------
-// Epilogue warps: 8, two per TMEM lane quarter.  The element-wise epilogues
-// split each tile's columns between the two; the per-row loss epilogue gives
-// the two groups of four warps alternate tiles (one accumulator each).
-template <int EPI>
-__host__ __device__ constexpr int epi_warps() { return 8; }
-template <int EPI>
-__host__ __device__ constexpr int gemm_threads() { return 2 * kWarp + kWarp * epi_warps<EPI>(); }
-
 template <int BN, int EPI>
-__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
+__global__ void __launch_bounds__(gemm_threads<BN, EPI>(), 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
                const TcParams p) {
   using C = Cfg<BN, EPI>;
   constexpr int S = C::S;
-  constexpr int EW = epi_warps<EPI>();
-  constexpr int NT = gemm_threads<EPI>();
+  constexpr int EW = epi_warps<BN, EPI>();
+  constexpr int NT = gemm_threads<BN, EPI>();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   uint8_t* auxs = gbase + (size_t)S * C::STAGE;          // [2][BM x BN] (DACT only)
-  uint8_t* stgs = auxs + C::NAUX * (size_t)C::AUX_SLOT;  // [8 warps][STG_WARP] (BIAS_ACT only)
-  uint8_t* ctrl = stgs + 8 * (size_t)C::STG_WARP;
+  uint8_t* stgs = auxs + C::NAUX * (size_t)C::AUX_SLOT;  // [EW warps][STG_WARP] (BIAS_ACT only)
+  uint8_t* ctrl = stgs + EW * (size_t)C::STG_WARP;
   Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), S};
   uint64_t* xbar = reinterpret_cast<uint64_t*>(ctrl) + Ctrl::count(S);  // aux full[2], empty[2]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 4);
@@ -251,6 +255,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const bool rok = row < p.M;
       const uint32_t taddr = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       constexpr int PART = BN / (EW / 4);   // columns of this warp: [h*PART, (h+1)*PART)
+      static_assert(PART == 64, "one 64-column TMA store block per epilogue warp");
       if constexpr (EPI == EPI_DACT) {
         // tile tc uses aux slot tc & 1 (same tile order as the producer); the
         // result overwrites the warp's rows of the slot and leaves by TMA
@@ -585,7 +590,7 @@ cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream
   const int total = p.tiles_m * p.tiles_n;
   const int grid = total < num_sms ? total : num_sms;
   if (grid_out) *grid_out = grid;
-  return launch_pdl(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(gemm_threads<EPI>()),
+  return launch_pdl(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(gemm_threads<BN, EPI>()),
                     Cfg<BN, EPI>::SMEM, st, ta, tb, tx, to, p);
 }
 
