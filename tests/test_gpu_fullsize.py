@@ -6,7 +6,7 @@ configuration the benchmark times.
 - Large batch: one full minibatch of 262,144 rows.  The oracle would take
   minutes here, so the check is a property that holds at any size: the loss
   is a mean over rows, so |S| g(S) is additive over a split of the rows,
-  g(A u B) = (|A| g(A) + |B| g(B)) / (|A| + |B|), up to fp32 summation order.
+  g(A u B) = (|A| g(A) + |B| g(B)) / (|A| + |B|), up to rounding.
   The oracle comparison of the same network runs at 2,048 rows in
   test_gpu_loss.py.
 """
@@ -60,7 +60,14 @@ def test_mario_full_minibatch_matches_oracle():
         assert abs(s6[k] - sref[k]) <= 2e-2 * max(abs(sref[k]), scale[k]) + 1e-7, (k, s6, sref)
 
 
-def test_large_full_minibatch_is_additive_over_rows():
+@pytest.mark.parametrize("na,tol", [(131_072, 1e-4), (100_003, 4e-3)])
+def test_large_full_minibatch_is_additive_over_rows(na, tol):
+    """Two splits of the 262,144 rows.  Halves: dz = dloss/dz / |S| differs
+    between the runs by an exact factor of 2, so every bf16 rounding of dz, dP2
+    and dP1 scales exactly and only the fp32 summation order differs (1e-4).
+    Ragged split (100,003 rows, not a whole number of tiles): the 1/|S| scales
+    are not powers of two, so the bf16 roundings of the backpropagated values
+    differ by up to 2^-9 relative per element (4e-3)."""
     import policy_rl_gb300 as P
     w = synth.WORKLOADS["large"].scaled(T=4, N=65536, minibatches=1)   # 262,144 rows
     mb = w.B
@@ -72,7 +79,6 @@ def test_large_full_minibatch_is_additive_over_rows():
     idx = oracle.perm(21, 0, mb)
     ctx = P.Context(P.config_from_workload(w, max_minibatch=mb), p0)
     g_all, s_all = _grad(ctx, ro, adv, ret, idx)
-    na = 100_003                      # ragged split: neither part is a whole number of tiles
     g_a, s_a = _grad(ctx, ro, adv, ret, idx[:na])
     g_b, s_b = _grad(ctx, ro, adv, ret, idx[na:])
     ctx.close()
@@ -80,8 +86,8 @@ def test_large_full_minibatch_is_additive_over_rows():
     for name, sl in param_slices(w).items():
         if sl.stop > sl.start:
             e = normwise(g_all[sl], comb[sl])
-            assert e <= 1e-4, f"{name}: normwise error {e:.3e}"
-    # the loss statistics are means over rows too
+            assert e <= tol, f"{name}: normwise error {e:.3e}"
+    # the loss statistics are means over rows too (fp32 terms, no bf16 step)
     s_comb = (na * s_a.astype(np.float64) + (mb - na) * s_b.astype(np.float64)) / mb
     np.testing.assert_allclose(s_all, s_comb, rtol=1e-4, atol=1e-6)
     assert np.all(np.isfinite(g_all))
