@@ -99,7 +99,10 @@ struct ppo_ctx {
   std::vector<int> prof_stages;
 
   // graph cache of the last ppo_update
-  cudaGraphExec_t gexec = nullptr;
+  cudaGraphExec_t gexec = nullptr;        // the update after GAE and the permutation
+  cudaGraphExec_t gexec_pre = nullptr;    // GAE, advantage moments, permutations
+  cudaStream_t cst = nullptr;             // ppo_update_host: rollout copies that GAE does not read
+  cudaEvent_t cev = nullptr;
   UpdateKey gkey{};
   bool gvalid = false;
 
@@ -124,6 +127,9 @@ struct ppo_ctx {
   }
   ~ppo_ctx() {
     if (gexec) cudaGraphExecDestroy(gexec);
+    if (gexec_pre) cudaGraphExecDestroy(gexec_pre);
+    if (cev) cudaEventDestroy(cev);
+    if (cst) cudaStreamDestroy(cst);
     for (cudaEvent_t e : prof_events) cudaEventDestroy(e);
     for (void* p : allocs) cudaFree(p);
   }
@@ -616,24 +622,28 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
                           const float* logp_old, const float* val, const float* rew,
                           const float* done, const float* boot, int64_t T, int64_t N,
                           int32_t epochs, int32_t minibatches, float gamma, float lambda,
-                          float lr, uint32_t seed, float* stats, cudaStream_t st) {
+                          float lr, uint32_t seed, float* stats, cudaStream_t st,
+                          int parts = 3) {
   const int64_t B = T * N, mb = B / minibatches;
-  const __nv_bfloat16* packed = nullptr;
-  if (c->use_mk)   // grid-barrier counters start at zero (also after an aborted launch)
-    PPO_CUDA(cudaMemsetAsync(c->gbar, 0, 2 * sizeof(unsigned), st));
-  else
-    PPO_CUDA(cudaMemsetAsync(c->rbar, 0, sizeof(unsigned), st));
+  const __nv_bfloat16* packed = c->bf16 ? c->obs_packed : nullptr;
+  if (parts & 1) {
+    // part 1 reads only rewards, values, dones and bootstrap values
+    if (c->use_mk)   // grid-barrier counters start at zero (also after an aborted launch)
+      PPO_CUDA(cudaMemsetAsync(c->gbar, 0, 2 * sizeof(unsigned), st));
+    else
+      PPO_CUDA(cudaMemsetAsync(c->rbar, 0, sizeof(unsigned), st));
+    PPO_CUDA(launch_gae(rew, val, done, boot, (int)T, (int)N, gamma, lambda, c->adv, c->ret,
+                        c->gae_part, gae_num_blocks((int)N), st));
+    c->tr.mark(ST_GAE, st);
+    PPO_CUDA(launch_gae_finalize(c->gae_part, gae_num_blocks((int)N), c->advstats, st));
+    c->tr.mark(ST_GAE_FINALIZE, st);
+    PPO_CUDA(launch_perm(seed, 0, epochs, B, c->perm, c->perm_work, st, &c->tr));
+  }
+  if (!(parts & 2)) return PPO_OK;
   if (c->bf16) {
     PPO_CUDA(launch_pack_obs(obs, B, c->s.D, c->s.Dp, c->obs_packed, st));
     c->tr.mark(ST_PACK, st);
-    packed = c->obs_packed;
   }
-  PPO_CUDA(launch_gae(rew, val, done, boot, (int)T, (int)N, gamma, lambda, c->adv, c->ret,
-                      c->gae_part, gae_num_blocks((int)N), st));
-  c->tr.mark(ST_GAE, st);
-  PPO_CUDA(launch_gae_finalize(c->gae_part, gae_num_blocks((int)N), c->advstats, st));
-  c->tr.mark(ST_GAE_FINALIZE, st);
-  PPO_CUDA(launch_perm(seed, 0, epochs, B, c->perm, c->perm_work, st, &c->tr));
   const MbRows ep{c->X_ep, c->act_ep, c->actc_ep, c->logp_ep, c->adv_ep, c->ret_ep};
   const int64_t xrow = c->bf16 ? (int64_t)c->s.Dp * 2 : (int64_t)c->s.D * 4;
   const int NH = c->s.NH > 0 ? c->s.NH : 1, G = c->s.G > 0 ? c->s.G : 1;
@@ -949,19 +959,27 @@ static ppo_status check_update_args(ppo_ctx* c, const float* obs, const int32_t*
   return PPO_OK;
 }
 
-ppo_status ppo_update(ppo_ctx* c, const float* obs, const int32_t* act, const float* actc,
+}  // extern "C"
+
+namespace {
+// ppo_update with an optional event that part 2 waits for (ppo_update_host)
+ppo_status run_update(ppo_ctx* c, const float* obs, const int32_t* act, const float* actc,
                       const float* logp_old, const float* val, const float* rew,
                       const float* done, const float* boot, int64_t T, int64_t N,
                       int32_t epochs, int32_t minibatches, float gamma, float lambda, float lr,
-                      uint32_t seed, float* stats, cudaStream_t st) {
+                      uint32_t seed, float* stats, cudaStream_t st,
+                      cudaEvent_t wait_before_part2) {
   TRY(check_update_args(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
                         minibatches, stats));
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   PPO_CUDA(cudaStreamIsCapturing(st, &cs));
   if (st == nullptr || cs != cudaStreamCaptureStatusNone) {
     // legacy stream cannot be captured; inside a caller's capture, just enqueue
+    TRY(enqueue_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
+                       minibatches, gamma, lambda, lr, seed, stats, st, 1));
+    if (wait_before_part2) PPO_CUDA(cudaStreamWaitEvent(st, wait_before_part2, 0));
     return enqueue_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
-                          minibatches, gamma, lambda, lr, seed, stats, st);
+                          minibatches, gamma, lambda, lr, seed, stats, st, 2);
   }
   UpdateKey key{};
   const void* kp[9] = {obs, act, actc, logp_old, val, rew, done, boot, c};
@@ -977,29 +995,48 @@ ppo_status ppo_update(ppo_ctx* c, const float* obs, const int32_t* act, const fl
   key.stats = stats;
   key.stream = st;
   if (!c->gvalid || !(key == c->gkey)) {
-    if (c->gexec) {
-      cudaGraphExecDestroy(c->gexec);
-      c->gexec = nullptr;
-      c->gvalid = false;
+    for (cudaGraphExec_t* g : {&c->gexec_pre, &c->gexec})
+      if (*g) {
+        cudaGraphExecDestroy(*g);
+        *g = nullptr;
+      }
+    c->gvalid = false;
+    // two graphs: part 1 (GAE, moments, permutations) and part 2 (the rest),
+    // so that ppo_update_host can wait for the observation copy in between
+    for (int part = 1; part <= 2; ++part) {
+      PPO_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+      ppo_status r = enqueue_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N,
+                                    epochs, minibatches, gamma, lambda, lr, seed, stats, st, part);
+      cudaGraph_t graph = nullptr;
+      cudaError_t e = cudaStreamEndCapture(st, &graph);
+      if (r != PPO_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return r;
+      }
+      if (e != cudaSuccess) return PPO_ERR_CUDA;
+      e = cudaGraphInstantiate(part == 1 ? &c->gexec_pre : &c->gexec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) return PPO_ERR_CUDA;
     }
-    PPO_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
-    ppo_status r = enqueue_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
-                                  minibatches, gamma, lambda, lr, seed, stats, st);
-    cudaGraph_t graph = nullptr;
-    cudaError_t e = cudaStreamEndCapture(st, &graph);
-    if (r != PPO_OK) {
-      if (graph) cudaGraphDestroy(graph);
-      return r;
-    }
-    if (e != cudaSuccess) return PPO_ERR_CUDA;
-    e = cudaGraphInstantiate(&c->gexec, graph, 0);
-    cudaGraphDestroy(graph);
-    if (e != cudaSuccess) return PPO_ERR_CUDA;
     c->gkey = key;
     c->gvalid = true;
   }
+  PPO_CUDA(cudaGraphLaunch(c->gexec_pre, st));
+  if (wait_before_part2) PPO_CUDA(cudaStreamWaitEvent(st, wait_before_part2, 0));
   PPO_CUDA(cudaGraphLaunch(c->gexec, st));
   return PPO_OK;
+}
+}  // namespace
+
+extern "C" {
+
+ppo_status ppo_update(ppo_ctx* c, const float* obs, const int32_t* act, const float* actc,
+                      const float* logp_old, const float* val, const float* rew,
+                      const float* done, const float* boot, int64_t T, int64_t N,
+                      int32_t epochs, int32_t minibatches, float gamma, float lambda, float lr,
+                      uint32_t seed, float* stats, cudaStream_t st) {
+  return run_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
+                    minibatches, gamma, lambda, lr, seed, stats, st, nullptr);
 }
 
 const char* ppo_stage_name(int32_t stage) {
@@ -1120,20 +1157,28 @@ ppo_status ppo_update_host(ppo_ctx* c, const float* h_obs, const int32_t* h_act,
     if ((r = c->alloc_n(&c->st_stats, nstats)) != PPO_OK) return r;
     c->st_stats_cap = nstats;
   }
-  auto h2d = [&](void* d, const void* h, size_t bytes) {
-    return cudaMemcpyAsync(d, h, bytes, cudaMemcpyHostToDevice, st);
+  if (!c->cst) {
+    PPO_CUDA(cudaStreamCreateWithFlags(&c->cst, cudaStreamNonBlocking));
+    PPO_CUDA(cudaEventCreateWithFlags(&c->cev, cudaEventDisableTiming));
+  }
+  auto h2d = [&](void* d, const void* h, size_t bytes, cudaStream_t s2) {
+    return cudaMemcpyAsync(d, h, bytes, cudaMemcpyHostToDevice, s2);
   };
-  PPO_CUDA(h2d(c->st_obs, h_obs, sizeof(float) * B * s.D));
-  if (s.NH > 0) PPO_CUDA(h2d(c->st_act, h_act, sizeof(int32_t) * B * s.NH));
-  if (s.G > 0) PPO_CUDA(h2d(c->st_actc, h_actc, sizeof(float) * B * s.G));
-  PPO_CUDA(h2d(c->st_logp, h_logp_old, sizeof(float) * B));
-  PPO_CUDA(h2d(c->st_val, h_val, sizeof(float) * B));
-  PPO_CUDA(h2d(c->st_rew, h_rew, sizeof(float) * B));
-  PPO_CUDA(h2d(c->st_done, h_done, sizeof(float) * B));
-  PPO_CUDA(h2d(c->st_boot, h_boot, sizeof(float) * N));
-  TRY(ppo_update(c, c->st_obs, c->st_act, c->st_actc, c->st_logp, c->st_val, c->st_rew,
+  // GAE's inputs on `stream`; observations, actions and logp_old on a second
+  // stream, copied while GAE and the permutation run (the previous call ended
+  // with a stream synchronisation, so nothing still reads these buffers)
+  PPO_CUDA(h2d(c->st_val, h_val, sizeof(float) * B, st));
+  PPO_CUDA(h2d(c->st_rew, h_rew, sizeof(float) * B, st));
+  PPO_CUDA(h2d(c->st_done, h_done, sizeof(float) * B, st));
+  PPO_CUDA(h2d(c->st_boot, h_boot, sizeof(float) * N, st));
+  PPO_CUDA(h2d(c->st_obs, h_obs, sizeof(float) * B * s.D, c->cst));
+  if (s.NH > 0) PPO_CUDA(h2d(c->st_act, h_act, sizeof(int32_t) * B * s.NH, c->cst));
+  if (s.G > 0) PPO_CUDA(h2d(c->st_actc, h_actc, sizeof(float) * B * s.G, c->cst));
+  PPO_CUDA(h2d(c->st_logp, h_logp_old, sizeof(float) * B, c->cst));
+  PPO_CUDA(cudaEventRecord(c->cev, c->cst));
+  TRY(run_update(c, c->st_obs, c->st_act, c->st_actc, c->st_logp, c->st_val, c->st_rew,
                  c->st_done, c->st_boot, T, N, epochs, minibatches, gamma, lambda, lr, seed,
-                 h_stats ? c->st_stats : nullptr, st));
+                 h_stats ? c->st_stats : nullptr, st, c->cev));
   if (h_stats)
     PPO_CUDA(cudaMemcpyAsync(h_stats, c->st_stats, sizeof(float) * nstats,
                              cudaMemcpyDeviceToHost, st));
