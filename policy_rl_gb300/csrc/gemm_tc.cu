@@ -351,7 +351,8 @@ constexpr int WS = 4;
 constexpr int W_A_BYTES = BM * BK * 2;   // 2 blocks of 64 features x 64 rows
 constexpr int W_B_BYTES = WBN * BK * 2;  // up to 4 blocks
 constexpr int W_STAGE = W_A_BYTES + W_B_BYTES;
-constexpr size_t W_SMEM = 1024 + (size_t)WS * W_STAGE + 512;
+constexpr int W_STG = 2 * 4096;   // per epilogue warp: two 32 x 32 fp32 store boxes
+constexpr size_t W_SMEM = 1024 + (size_t)WS * W_STAGE + 4 * W_STG + 512;
 constexpr int W_TMEM_COLS = 512;
 
 __device__ __forceinline__ void decode_unit(const WParams& p, int u, int& reg, int& tm, int& tn,
@@ -373,12 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant__ CUtensorMap tmV0,
                 const __grid_constant__ CUtensorMap tmU1, const __grid_constant__ CUtensorMap tmV1,
                 const __grid_constant__ CUtensorMap tmU2, const __grid_constant__ CUtensorMap tmV2,
-                const WParams p) {
+                const __grid_constant__ CUtensorMap tmP0, const __grid_constant__ CUtensorMap tmP1,
+                const __grid_constant__ CUtensorMap tmP2, const WParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  uint8_t* ctrl = gbase + (size_t)WS * W_STAGE;
+  uint8_t* wstg = gbase + (size_t)WS * W_STAGE;   // [4 warps][2][32 rows x 128 B]
+  uint8_t* ctrl = wstg + 4 * W_STG;
   Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), WS};
   uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * Ctrl::count(WS));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
@@ -476,7 +479,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
     }
   } else {
     const int q = warp & 3;
-    uint32_t tc = 0;
+    uint32_t tc = 0, sc = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
       int reg, tm, tn, kt0, kt1, split;
       decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
@@ -485,13 +488,35 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
       const uint32_t use = tc >> 1;
       if (!wait_bar(cb.tfull(acc), use & 1, g)) break;
       tc_fence_after();
-      const int row = tm * BM + q * 32 + lane;
+      // fp32 partial tile -> this split's slice of the partial buffer, 32
+      // columns at a time through two 32 x 32 staging boxes per warp (128-byte
+      // swizzle: float4 c of row r at ((c ^ (r & 7)) * 16)) and TMA stores
+      const CUtensorMap* tp = reg == 0 ? &tmP0 : (reg == 1 ? &tmP1 : &tmP2);
       const uint32_t taddr = tmem + (uint32_t)(acc * WBN) + ((uint32_t)(q * 32) << 16);
-      epi_wgrad_tile(taddr, row, R.bn, R.M, R.N, tn * R.bn, R.part + (int64_t)split * R.M * R.N);
+      uint8_t* mystg = wstg + (warp - 2) * W_STG;
+#pragma unroll 1
+      for (int c0 = 0; c0 < R.bn; c0 += 32, ++sc) {
+        float v[32];
+        tmem_ld32(taddr + (uint32_t)c0, v);
+        uint8_t* buf = mystg + (sc & 1) * 4096;
+        if (lane == 0) bulk_wait_read1();   // the store that used buf last has read it
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+              make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(tp, smem_u32(buf), tn * R.bn + c0, tm * BM + q * 32, split);
+          bulk_commit();
+        }
+      }
       tc_fence_before();
       mbar_arrive(cb.tempty(acc));
       ++tc;
     }
+    if (lane == 0) bulk_wait0();   // this warp's stores are complete before the CTA exits
   }
   __syncthreads();
   if (*abort_flag) {
@@ -546,6 +571,22 @@ cudaError_t make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t ro
 // bf16 row-major [rows][ld] read as 64-feature blocks: x = feature within the
 // block, y = row, z = block (of nblk); box = 64 x box_rows x box_blk.  The
 // box lands in shared memory as box_blk consecutive [box_rows][64] atoms.
+// fp32 split-K partials [splits][rows][cols] as 32-column x 32-row x 1-split boxes
+cudaError_t make_tmap_partials(CUtensorMap* m, const float* base, int64_t cols, int64_t rows,
+                               int64_t splits) {
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)splits};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)(cols * rows * 4)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_tmap_blocks(CUtensorMap* m, const void* base, int64_t rows, int64_t ld, int nblk,
                              int box_rows, int box_blk) {
   cudaError_t e = get_encode();
@@ -697,7 +738,7 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
                      uint32_t mn_sbo, int* err, uint64_t timeout_ns, int num_sms,
                      cudaStream_t st) {
   if (nreg < 1 || nreg > 3) return cudaErrorInvalidValue;
-  CUtensorMap tu[3], tv[3];
+  CUtensorMap tu[3], tv[3], tp[3];
   WParams p{};
   p.nreg = nreg;
   p.err = err;
@@ -721,6 +762,8 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
     R.k_tiles = (rows + BK - 1) / BK;
     R.kt_per_split = G.kt_per_split;
     R.splits = (R.k_tiles + R.kt_per_split - 1) / R.kt_per_split;
+    e = make_tmap_partials(&tp[r], G.part, G.N, G.M, R.splits);
+    if (e != cudaSuccess) return e;
     R.unit_begin = unit;
     R.part = G.part;
     unit += R.tiles_m * R.tiles_n * R.splits;
@@ -728,11 +771,12 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
   for (int r = nreg; r < 3; ++r) {
     tu[r] = tu[0];
     tv[r] = tv[0];
+    tp[r] = tp[0];
   }
   p.total_units = unit;
   const int grid = unit < num_sms ? unit : num_sms;
   return launch_pdl(tc_wgrad_kernel, dim3(grid), dim3(kThreads), W_SMEM, st, tu[0], tv[0], tu[1],
-                    tv[1], tu[2], tv[2], p);
+                    tv[1], tu[2], tv[2], tp[0], tp[1], tp[2], p);
 }
 
 int tc_wgrad_bn(int N) { return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64); }
