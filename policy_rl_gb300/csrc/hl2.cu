@@ -16,8 +16,9 @@
 // followed by a separate backward-data kernel this reads H2 once instead of
 // twice and drops the dz round trip and one launch.
 //
-// Roles: warp 0 TMA, warp 1 MMA, warps 2..9 epilogues (TMEM lane quarter
-// q = warp % 4, column half h).  TMEM: R_A = columns [0, 256) holds Z (first
+// Roles: warp 0 TMA, warp 1 MMA, warps 2..5 the loss and warps 6..9 the dP2
+// epilogue (TMEM lane quarter q = warp % 4 in each group), so that the loss of
+// one tile overlaps the dP2 epilogue of the previous one.  TMEM: R_A = columns [0, 256) holds Z (first
 // CP columns) and then the second 256-column half of dP2 (H2 = 512); R_B =
 // [256, 512) holds the first half of dP2.  Every wait is bounded.
 #include <cuda.h>
@@ -37,6 +38,7 @@ using namespace tc;
 constexpr int kHWarps = 10;
 constexpr int kHThreads = kHWarps * kWarp;
 constexpr int kHEpi = 8 * kWarp;
+constexpr int kHGrp = 4 * kWarp;   // one epilogue group
 constexpr int kBlk = 128 * 128;   // 128 rows x 64 bf16 columns (16 KB)
 constexpr int kH2Max = 512;
 
@@ -101,17 +103,17 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_HS_FULL + b), 1);
-      mbar_init(bar(B_HS_EMPTY + b), kHEpi);
+      mbar_init(bar(B_HS_EMPTY + b), kHGrp);
     }
     mbar_init(bar(B_W3_FULL), 1);
     mbar_init(bar(B_W3T_FULL), 1);
     mbar_init(bar(B_W3T_EMPTY), 1);
     mbar_init(bar(B_ZFULL), 1);
-    mbar_init(bar(B_DZ_RDY), kHEpi);
+    mbar_init(bar(B_DZ_RDY), kHGrp);
     mbar_init(bar(B_P0), 1);
     mbar_init(bar(B_P1), 1);
-    mbar_init(bar(B_RA_FREE), kHEpi);
-    mbar_init(bar(B_RB_FREE), kHEpi);
+    mbar_init(bar(B_RA_FREE), kHGrp);
+    mbar_init(bar(B_RB_FREE), kHGrp);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     cnt[0] = 0;
@@ -199,8 +201,10 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
       }
     }
   } else {
+    // two epilogue groups of four warps (TMEM lane quarter q = warp % 4 each):
+    // warps 2..5 run the loss of tile t+1 while warps 6..9 finish dP2 of tile t
     const int q = warp & 3;
-    const int h = (warp - 2) / 4;
+    const bool loss_grp = warp < 6;
     const int rl = q * 32 + lane;
     const HeadMasks hm = head_masks(p.shape);
     const uint32_t lanes = (uint32_t)(q * 32) << 16;
@@ -228,10 +232,11 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
       const int row0 = tile * 128;
       const int row = row0 + rl;
       const bool rok = row < p.M;
-      // loss on Z (warps of column half 0; one row per thread) -> dz tile
-      if (!wait_bar(bar(B_ZFULL), ph, g)) break;
-      tc_fence_after();
-      if (h == 0) {
+      if (loss_grp) {
+        // loss on Z (one row per thread) -> dz tile.  ZFULL(t) is committed after
+        // the dP2 products of tile t-1, which read the dz tile: it is free.
+        if (!wait_bar(bar(B_ZFULL), ph, g)) break;
+        tc_fence_after();
         float dzr[32], t6[6], dls[4];
         loss_row_regs<CP>(RA, row, rok, p.shape, hm, p.lc, p.inv_mb, p.rows, p.logstd, b3s, dzr,
                           t6, dls);
@@ -250,24 +255,25 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
         loss_warp_reduce(dzr, t6, dls, cs3 + q * 32, lp + q * kLossPartials, lane);
         tc_fence_before();
         store_rows(&maps.dz, DZ, 0, 1, row0);
-        stores_read();   // the dz tile is rewritten by the next tile
+        stores_read();   // the dz tile is rewritten with the next tile
+        mbar_arrive(bar(B_DZ_RDY));
+        if (NH == 1) mbar_arrive(bar(B_RA_FREE));   // RA held only Z
       } else {
-        tc_fence_before();
+        // dP2 halves, in place in HS, stored (one warp per quarter: all columns)
+        bool ok = true;
+        for (int hf = 0; hf < NH; ++hf) {
+          if (!wait_bar(bar(hf == 0 ? B_P0 : B_P1), ph, g)) { ok = false; break; }
+          tc_fence_after();
+          epi_dact_smem_tile<HN, 4>(hf == 0 ? RB : RA, rl, rok, hf * 256, 0, p.act,
+                                    hs + hf * 4 * kBlk, cs2 + q * kH2Max, lane);
+          tc_fence_before();
+          store_rows(&maps.dp2, hs, hf * 4, HN / 64, row0);
+          mbar_arrive(bar(hf == 0 ? B_RB_FREE : B_RA_FREE));
+        }
+        if (!ok) break;
+        stores_read();   // this buffer is reloaded after this
+        mbar_arrive(bar(B_HS_EMPTY + hb));
       }
-      mbar_arrive(bar(B_DZ_RDY));
-      if (NH == 1) mbar_arrive(bar(B_RA_FREE));   // RA held only Z
-      // dP2 halves, in place in HS, stored
-      for (int hf = 0; hf < NH; ++hf) {
-        if (!wait_bar(bar(hf == 0 ? B_P0 : B_P1), ph, g)) break;
-        tc_fence_after();
-        epi_dact_smem_tile<HN, 8>(hf == 0 ? RB : RA, rl, rok, hf * 256, h, p.act,
-                                  hs + hf * 4 * kBlk, cs2 + q * kH2Max, lane);
-        tc_fence_before();
-        store_rows(&maps.dp2, hs, hf * 4 + h * (HN / 128), HN / 128, row0);
-        mbar_arrive(bar(hf == 0 ? B_RB_FREE : B_RA_FREE));
-      }
-      stores_read();   // this buffer is reloaded after this
-      mbar_arrive(bar(B_HS_EMPTY + hb));
     }
     if (lane == 0) bulk_wait0();
   }
