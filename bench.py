@@ -174,13 +174,13 @@ def _stage_work(stage: str, w, mb: int):
 # profiles/reduce_adam_mario.md);
 # stages without such a capture report null.
 NCU_TRAFFIC = {
-    ("mario", "fwd1_gemm"): 4.255e6, ("mario", "fwd2_gemm"): 16.936e6,
-    ("mario", "head_loss_gemm"): 17.769e6, ("mario", "dact2_gemm"): 21.046e6,
-    ("mario", "dact1_gemm"): 33.724e6, ("mario", "wgrad_gemm"): 77.718e6,
-    ("large", "fwd1_gemm"): 274.635e6, ("large", "fwd2_gemm"): 488.671e6,
-    ("large", "head_loss_gemm"): 284.184e6, ("large", "dact2_gemm"): 526.086e6,
-    ("large", "dact1_gemm"): 773.370e6, ("large", "wgrad_gemm"): 1191.720e6,
+    ("mario", "fwd1_gemm"): 4.254e6, ("mario", "fwd2_gemm"): 16.936e6,
+    ("mario", "head_loss_gemm"): 17.769e6, ("mario", "dact2_gemm"): 21.041e6,
+    ("mario", "dact1_gemm"): 33.731e6, ("mario", "wgrad_gemm"): 77.725e6,
     ("mario", "grad_reduce_adam"): 13.008e6,
+    ("large", "fwd1_gemm"): 274.744e6, ("large", "fwd2_gemm"): 489.007e6,
+    ("large", "head_loss_gemm"): 284.109e6, ("large", "dact2_gemm"): 526.100e6,
+    ("large", "dact1_gemm"): 773.235e6, ("large", "wgrad_gemm"): 1191.282e6,
 }
 
 
