@@ -344,9 +344,7 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded mulberry32 rollout with the workload's shapes and value "
                 "distributions; random-init weights)",
-        "config": {"workload": f"{w.name}: T={w.T} N={w.N} obs={w.obs_dim} "
-                               f"MLP {w.obs_dim}-{w.h1}-{w.h2} {'tanh' if w.act == 0 else 'relu'} "
-                               f"heads {list(w.heads)}+V epochs={E} minibatches={M} mb={mb}",
+        "config": {"workload": _workload_str(w),
                    "global_batch": world * B, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (256 MB write)",
                    "timing": "CUDA events per update on the launching stream, mean over steps"},
@@ -458,6 +456,13 @@ def _cpu_baseline(w):
                       f"plain C fp64, single thread ({t:.2f} s)"}
 
 
+def _workload_str(w) -> str:
+    mb = w.B // w.minibatches
+    return (f"{w.name}: T={w.T} N={w.N} obs={w.obs_dim} MLP {w.obs_dim}-{w.h1}-{w.h2} "
+            f"{'tanh' if w.act == 0 else 'relu'} heads {list(w.heads)}+V epochs={w.epochs} "
+            f"minibatches={w.minibatches} mb={mb}")
+
+
 def run_reference(args, world, rank):
     """The oracle timed on the host cores, one bounded sample per step.  The
     sample (a T=16 x N slice of the workload) is sized so that the whole
@@ -485,7 +490,9 @@ def run_reference(args, world, rank):
         "value": round(v, 2), "unit": "samples/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name} (oracle sample per step: {ws.B} samples)"},
+        "config": {"workload": _workload_str(w), "global_batch": world * w.B,
+                   "parallelism": "host cores (rank 0)",
+                   "sample": f"oracle on a {ws.B}-sample slice per step (T={ws.T} x N={ws.N})"},
         "cpu_baseline": {"value": round(v, 2), "unit": "samples/s", "cores": 1,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 2), "unit": "samples/s", "h2d_bytes_per_step": 0,
