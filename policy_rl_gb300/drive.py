@@ -5,6 +5,9 @@
       of the named synthetic workload (random advantages/returns/indices).
   python -m policy_rl_gb300.drive gae <T> <N> [reps]
       ppo_gae with moments and normalisation on seeded N(0,1) inputs.
+  python -m policy_rl_gb300.drive adam [reps]
+      ppo_adam_step (squared-norm pass + clip/Adam) over the 67.2 M fp32
+      parameters of a 65536-1024-64 network (1 GB of optimiser state).
 """
 from __future__ import annotations
 
@@ -54,11 +57,28 @@ def gae(T: int, N: int, reps: int = 3) -> None:
     torch.cuda.synchronize()
 
 
+def adam(reps: int = 3) -> None:
+    import torch
+    import policy_rl_gb300 as P
+    cfg = P.make_config(65536, 1024, 64, heads=(2,), precision=0, max_batch=1, max_minibatch=1,
+                        max_epochs=1)
+    ctx = P.Context(cfg)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    ctx.grad.normal_(generator=g)
+    for _ in range(reps):
+        ctx.adam_step(1e-4)
+    ctx.sync_status()
+    ctx.close()
+
+
 if __name__ == "__main__":
     if sys.argv[1] == "minibatch":
         minibatch(sys.argv[2] if len(sys.argv) > 2 else "mario",
                   int(sys.argv[3]) if len(sys.argv) > 3 else 3)
     elif sys.argv[1] == "gae":
         gae(int(sys.argv[2]), int(sys.argv[3]), int(sys.argv[4]) if len(sys.argv) > 4 else 3)
+    elif sys.argv[1] == "adam":
+        adam(int(sys.argv[2]) if len(sys.argv) > 2 else 3)
     else:
         raise SystemExit(__doc__)
