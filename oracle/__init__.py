@@ -56,7 +56,9 @@ class _Hyper(ctypes.Structure):
                 ("ent_coef", ctypes.c_double), ("lr", ctypes.c_double),
                 ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
                 ("adam_eps", ctypes.c_double), ("max_grad_norm", ctypes.c_double),
-                ("seed", ctypes.c_uint32), ("bf16_operands", ctypes.c_int)]
+                ("seed", ctypes.c_uint32), ("bf16_operands", ctypes.c_int),
+                ("adv_mode", ctypes.c_int), ("rho_clip", ctypes.c_double),
+                ("c_clip", ctypes.c_double)]
 
 
 _P = ctypes.c_void_p
@@ -89,6 +91,14 @@ def lib():
         L.orc_clip_grad_norm.argtypes = [_I64, _P, _D]
         L.orc_clip_grad_norm.restype = _D
         L.orc_adam.argtypes = [_I64, _P, _P, _P, _P, _I64, _D, _D, _D, _D]
+        L.orc_segment_advantage.argtypes = [_I64, _I64, _P, _P, _P, _I64, _P, _P, _P, _D, _D,
+                                            _D, _D, _P, _P]
+        L.orc_fresh_values.argtypes = [ctypes.POINTER(_Net), ctypes.c_int, _P, _I64, _P, _P, _P,
+                                       _P, _P, _P, _P]
+        L.orc_loss_grad_fresh.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_LossCfg), _P,
+                                          _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          ctypes.c_int, _D, _D, _D, _D, _P, _P, _P, _P, _P]
+        L.orc_loss_grad_fresh.restype = _D
         L.orc_update.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_Hyper), _I64, _I64, _I64, _I64,
                                  _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                  ctypes.POINTER(_I64), _P, _P, _P]
@@ -144,11 +154,14 @@ class Hyper:
     max_grad_norm: float = 0.5
     seed: int = 0
     bf16_operands: bool = False
+    adv_mode: int = 0          # 0 once per update, 1 fresh GAE, 2 fresh V-trace
+    rho_clip: float = 1.0
+    c_clip: float = 1.0
 
     def c(self) -> _Hyper:
         return _Hyper(self.gamma, self.lam, self.clip, self.vf_coef, self.ent_coef, self.lr,
                       self.beta1, self.beta2, self.adam_eps, self.max_grad_norm, self.seed,
-                      int(self.bf16_operands))
+                      int(self.bf16_operands), int(self.adv_mode), self.rho_clip, self.c_clip)
 
 
 def mulberry32_stream(seed: int, count: int) -> np.ndarray:
@@ -168,6 +181,73 @@ def gae(rew, val, done, boot, gamma, lam):
     lib().orc_gae(T, N, _ptr(rew), _ptr(val), _ptr(done), _ptr(boot), gamma, lam,
                   _ptr(adv), _ptr(ret))
     return adv, ret
+
+
+def segment_advantage(rew, done, boot, envs, val, ratio, gamma, lam, rho_clip=1.0, c_clip=1.0):
+    """Advantages and value targets of the environment segments ``envs`` from
+    the given values ``val`` [T][ns] (and ratios, V-trace; None = GAE).
+    Returns (adv, ret), each float64 [T][ns]."""
+    rew, done = _as(rew, np.float32), _as(done, np.float32)
+    boot = _as(boot, np.float32)
+    envs = _as(envs, np.int32)
+    T, N = rew.shape
+    ns = envs.size
+    val = _as(val, np.float64).reshape(T, ns)
+    ratio = None if ratio is None else _as(ratio, np.float64).reshape(T, ns)
+    adv = np.empty((T, ns), np.float64)
+    ret = np.empty((T, ns), np.float64)
+    lib().orc_segment_advantage(T, N, _ptr(rew), _ptr(done), _ptr(boot), ns, _ptr(envs),
+                                _ptr(val), _ptr(ratio), gamma, lam, rho_clip, c_clip,
+                                _ptr(adv), _ptr(ret))
+    return adv, ret
+
+
+def segment_rows(T: int, N: int, envs) -> np.ndarray:
+    """Flat batch rows of a segment minibatch, in minibatch order t*ns + j."""
+    envs = np.asarray(envs, np.int64)
+    return (np.arange(T, dtype=np.int64)[:, None] * N + envs[None, :]).ravel().astype(np.int32)
+
+
+def fresh_values(net: Net, params, idx, obs, act_disc, act_cont, logp_old, bf16_operands=False,
+                 with_ratio=True):
+    """(value, ratio) of rows idx at params (ratio None unless with_ratio)."""
+    params = _as(params, np.float64)
+    idx = _as(idx, np.int32)
+    n = idx.size
+    val = np.empty(n, np.float64)
+    ratio = np.empty(n, np.float64) if with_ratio else None
+    act_cont = _as(act_cont if act_cont is not None else np.zeros(1), np.float32)
+    cn = net.c()
+    lib().orc_fresh_values(ctypes.byref(cn), int(bool(bf16_operands)), _ptr(params), n, _ptr(idx),
+                           _ptr(_as(obs, np.float32)), _ptr(_as(act_disc, np.int32)),
+                           _ptr(act_cont), _ptr(_as(logp_old, np.float32)), _ptr(val),
+                           _ptr(ratio))
+    return val, ratio
+
+
+def loss_grad_fresh(net: Net, params, T, N, envs, obs, act_disc, act_cont, logp_old, rew, done,
+                    boot, vtrace=False, gamma=0.99, lam=0.95, rho_clip=1.0, c_clip=1.0,
+                    clip=0.2, vf_coef=0.5, ent_coef=0.01, bf16_operands=False):
+    """Segment minibatch with fresh advantages.  Returns
+    (loss, grad[P], stats6, scale6, adv_norm[T*ns], ret[T*ns])."""
+    params = _as(params, np.float64)
+    envs = _as(envs, np.int32)
+    ns = envs.size
+    grad = np.empty(net.num_params, np.float64)
+    st = np.empty(6, np.float64)
+    sc = np.empty(6, np.float64)
+    an = np.empty(T * ns, np.float64)
+    rt = np.empty(T * ns, np.float64)
+    act_cont = _as(act_cont if act_cont is not None else np.zeros(1), np.float32)
+    cfg = _LossCfg(clip, vf_coef, ent_coef, int(bool(bf16_operands)))
+    cn = net.c()
+    loss = lib().orc_loss_grad_fresh(
+        ctypes.byref(cn), ctypes.byref(cfg), _ptr(params), T, N, ns, _ptr(envs),
+        _ptr(_as(obs, np.float32)), _ptr(_as(act_disc, np.int32)), _ptr(act_cont),
+        _ptr(_as(logp_old, np.float32)), _ptr(_as(rew, np.float32)), _ptr(_as(done, np.float32)),
+        _ptr(_as(boot, np.float32)), int(bool(vtrace)), gamma, lam, rho_clip, c_clip,
+        _ptr(grad), _ptr(st), _ptr(sc), _ptr(an), _ptr(rt))
+    return loss, grad, st, sc, an, rt
 
 
 def moments(x):
@@ -280,8 +360,8 @@ def update(net: Net, hp: Hyper, T, N, epochs, minibatches, obs, act_disc, act_co
     m = np.zeros(P) if m is None else _as(m, np.float64).copy()
     v = np.zeros(P) if v is None else _as(v, np.float64).copy()
     stats = np.empty((epochs * minibatches, 6), np.float64)
-    adv = np.empty(T * N, np.float64)
-    ret = np.empty(T * N, np.float64)
+    adv = np.zeros(T * N, np.float64)   # not written in the fresh-advantage modes
+    ret = np.zeros(T * N, np.float64)
     st = _I64(step)
     arrs = [_as(obs, np.float32), _as(act_disc, np.int32),
             _as(act_cont if act_cont is not None else np.zeros(1), np.float32),

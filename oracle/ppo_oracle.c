@@ -55,6 +55,52 @@ void orc_gae(int64_t T, int64_t N, const float *rew, const float *val,
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* "Teaching Mario to speedrun", sec. 8 "The Puffer net, and the trainer":
+ * PufferLib 5.0 computes the advantages of each minibatch from fresh values,
+ * by GAE or by V-trace.  The pages give V-trace no formula; it is taken from
+ * its published definition (Espeholt et al. 2018, "IMPALA", sec. 4.1, eq. 1
+ * and Remarks 1-2): with truncated importance weights
+ * rho_t = min(rho_bar, pi/mu) and lambda-weighted traces
+ * c_t = lambda min(c_bar, pi/mu), the value target is
+ *   v_s = V(x_s) + sum_{t >= s} gamma^{t-s} (c_s ... c_{t-1}) rho_t delta_t,
+ *   delta_t = r_t + gamma V(x_{t+1}) - V(x_t),
+ * computed here by its backward recursion
+ *   v_s - V(x_s) = rho_s delta_s + gamma c_s (v_{s+1} - V(x_{s+1})).
+ * Terminals cut the bootstrap and the trace exactly as in orc_gae.  The
+ * advantage is v_s - V(x_s) and the value target v_s, so that, as for GAE,
+ * ret = adv + V.  ratio == NULL is on-policy GAE: rho = 1, c = lambda.
+ * Segment j is environment envs[j] over the whole horizon; val, ratio, adv
+ * and ret are [T][ns] (element t*ns + j); rew, done [T][N]; boot [N]. */
+void orc_segment_advantage(int64_t T, int64_t N, const float *rew, const float *done,
+                           const float *boot, int64_t ns, const int32_t *envs,
+                           const double *val, const double *ratio, double gamma,
+                           double lambda, double rho_clip, double c_clip, double *adv,
+                           double *ret)
+{
+    for (int64_t j = 0; j < ns; ++j) {
+        const int64_t n = envs[j];
+        double next_value = (double)boot[n];
+        double next_corr = 0.0;   /* v_{t+1} - V(x_{t+1}) */
+        for (int64_t t = T - 1; t >= 0; --t) {
+            const int64_t i = t * N + n, k = t * ns + j;
+            const double alive = (done[i] != 0.0f) ? 0.0 : 1.0;
+            double rho = 1.0, c = lambda;
+            if (ratio) {
+                rho = ratio[k] < rho_clip ? ratio[k] : rho_clip;
+                c = lambda * (ratio[k] < c_clip ? ratio[k] : c_clip);
+            }
+            const double v = val[k];
+            const double delta = (double)rew[i] + gamma * alive * next_value - v;
+            const double corr = rho * delta + gamma * alive * c * next_corr;
+            adv[k] = corr;
+            ret[k] = v + corr;
+            next_value = v;
+            next_corr = corr;
+        }
+    }
+}
+
 /* Global advantage statistics: mean and the unbiased standard deviation. */
 void orc_moments(int64_t n, const double *x, double *mean, double *std_unbiased)
 {
@@ -165,6 +211,24 @@ static double orc_bf16(double x)
 static double orc_rnd(int bf16, double x) { return bf16 ? orc_bf16(x) : x; }
 
 double orc_round_bf16(double x) { return orc_bf16(x); }
+
+/* bf16-operand mode: the GEMMs read bf16-rounded weights; biases and
+ * log-std stay in full precision.  Returns a rounded copy of params (caller
+ * frees), or NULL when the mode is off. */
+static double *orc_gemm_weights(const orc_net *net, const double *params, int bf16)
+{
+    if (!bf16) return NULL;
+    const int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
+    const int64_t P = orc_num_params(net);
+    double *wr = (double *)malloc(sizeof(double) * (size_t)P);
+    memcpy(wr, params, sizeof(double) * (size_t)P);
+    orc_views v0 = orc_split(net, params);
+    const int64_t nW1 = H1 * D, nW2 = H2 * H1, nW3 = C * H2;
+    for (int64_t i = 0; i < nW1; ++i) wr[(v0.W1 - params) + i] = orc_bf16(v0.W1[i]);
+    for (int64_t i = 0; i < nW2; ++i) wr[(v0.W2 - params) + i] = orc_bf16(v0.W2[i]);
+    for (int64_t i = 0; i < nW3; ++i) wr[(v0.W3 - params) + i] = orc_bf16(v0.W3[i]);
+    return wr;
+}
 
 /* Forward pass of one row.  In bf16-operand mode the observation and the
  * stored activations are rounded to bf16 (the weights are rounded by the
@@ -285,18 +349,7 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
     const int64_t NH = net->n_heads, G = net->n_gauss;
     const int64_t P = orc_num_params(net);
     const int bf16 = cfg->bf16_operands;
-    /* bf16-operand mode: the GEMMs read bf16-rounded weights; biases and
-     * log-std stay in full precision */
-    double *wr = NULL;
-    if (bf16) {
-        wr = (double *)malloc(sizeof(double) * (size_t)P);
-        memcpy(wr, params, sizeof(double) * (size_t)P);
-        orc_views v0 = orc_split(net, params);
-        const int64_t nW1 = H1 * D, nW2 = H2 * H1, nW3 = C * H2;
-        for (int64_t i = 0; i < nW1; ++i) wr[(v0.W1 - params) + i] = orc_bf16(v0.W1[i]);
-        for (int64_t i = 0; i < nW2; ++i) wr[(v0.W2 - params) + i] = orc_bf16(v0.W2[i]);
-        for (int64_t i = 0; i < nW3; ++i) wr[(v0.W3 - params) + i] = orc_bf16(v0.W3[i]);
-    }
+    double *wr = orc_gemm_weights(net, params, bf16);
     orc_views w = orc_split(net, bf16 ? wr : params);
 
     memset(grad, 0, sizeof(double) * (size_t)P);
@@ -410,6 +463,84 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
 }
 
 /* ------------------------------------------------------------------------ */
+/* "Teaching Mario to speedrun", sec. 8 "The Puffer net, and the trainer":
+ * fresh values for the advantages of a minibatch.  For rows idx[0..n): the
+ * value column of the forward pass at params, and the importance ratio
+ * pi/mu = exp(logp - logp_old) of the taken action (sec. 6 "Don't move too
+ * far at once").  bf16: the operand rounding of orc_loss_cfg.  ratio may be
+ * NULL. */
+void orc_fresh_values(const orc_net *net, int bf16, const double *params, int64_t n,
+                      const int32_t *idx, const float *obs, const int32_t *act_disc,
+                      const float *act_cont, const float *logp_old, double *val, double *ratio)
+{
+    const int64_t H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
+    double *wr = orc_gemm_weights(net, params, bf16);
+    orc_views w = orc_split(net, bf16 ? wr : params);
+    double *buf = (double *)malloc(sizeof(double) * (size_t)(2 * H1 + 2 * H2 + 2 * C));
+    double *pre1 = buf, *h1 = pre1 + H1, *pre2 = h1 + H1, *h2 = pre2 + H2, *z = h2 + H2;
+    double *logprob = z + C;
+    double head_ent[8];
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t row = idx[r];
+        orc_forward_full(net, &w, obs + row * net->obs_dim, pre1, h1, pre2, h2, z, bf16);
+        val[r] = z[C - 1];
+        if (ratio) {
+            double logp, ent;
+            orc_row_policy(net, w.logstd, z, act_disc + row * net->n_heads,
+                           act_cont + row * net->n_gauss, logprob, head_ent, &logp, &ent);
+            ratio[r] = exp(logp - (double)logp_old[row]);
+        }
+    }
+    free(buf);
+    free(wr);
+}
+
+/* One minibatch made of whole environment segments, with advantages computed
+ * from fresh values ("Teaching Mario to speedrun", sec. 8: per minibatch,
+ * GAE or V-trace).  The rows are (t, envs[j]) for t < T, j < ns, in the order
+ * t*ns + j, i.e. flat batch rows t*N + envs[j].  Steps: fresh values (and,
+ * for V-trace, ratios) at params; orc_segment_advantage; the minibatch's own
+ * mean and unbiased std; orc_loss_grad with the normalised advantages and the
+ * targets ret.  vtrace: 0 GAE, 1 V-trace.  adv_norm_out / ret_out (nullable,
+ * [T*ns]) receive the normalised advantages and the value targets. */
+double orc_loss_grad_fresh(const orc_net *net, const orc_loss_cfg *cfg, const double *params,
+                           int64_t T, int64_t N, int64_t ns, const int32_t *envs,
+                           const float *obs, const int32_t *act_disc, const float *act_cont,
+                           const float *logp_old, const float *rew, const float *done,
+                           const float *boot, int vtrace, double gamma, double lambda,
+                           double rho_clip, double c_clip, double *grad, double *stats6,
+                           double *scale6, double *adv_norm_out, double *ret_out)
+{
+    const int64_t mb = T * ns, B = T * N;
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)mb);
+    double *val = (double *)malloc(sizeof(double) * (size_t)mb);
+    double *ratio = vtrace ? (double *)malloc(sizeof(double) * (size_t)mb) : NULL;
+    double *adv = (double *)malloc(sizeof(double) * (size_t)mb);
+    double *ret = (double *)malloc(sizeof(double) * (size_t)mb);
+    double *adv_full = (double *)calloc((size_t)B, sizeof(double));
+    double *ret_full = (double *)calloc((size_t)B, sizeof(double));
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t j = 0; j < ns; ++j) idx[t * ns + j] = (int32_t)(t * N + envs[j]);
+    orc_fresh_values(net, cfg->bf16_operands, params, mb, idx, obs, act_disc, act_cont,
+                     logp_old, val, ratio);
+    orc_segment_advantage(T, N, rew, done, boot, ns, envs, val, ratio, gamma, lambda, rho_clip,
+                          c_clip, adv, ret);
+    double mean, sd;
+    orc_moments(mb, adv, &mean, &sd);
+    for (int64_t r = 0; r < mb; ++r) {
+        adv_full[idx[r]] = adv[r];
+        ret_full[idx[r]] = ret[r];
+        if (adv_norm_out) adv_norm_out[r] = (adv[r] - mean) / (sd + 1e-8);
+        if (ret_out) ret_out[r] = ret[r];
+    }
+    const double loss = orc_loss_grad(net, cfg, params, mb, idx, obs, act_disc, act_cont,
+                                      logp_old, adv_full, ret_full, 1, mean, sd, grad, stats6,
+                                      scale6);
+    free(idx); free(val); free(ratio); free(adv); free(ret); free(adv_full); free(ret_full);
+    return loss;
+}
+
+/* ------------------------------------------------------------------------ */
 /* "PlayTrain", Table 8 (PPO column): gradient-norm clip 0.5.  The global L2
  * norm over all parameters; if above max_norm, scale by max_norm/(norm+1e-6). */
 double orc_clip_grad_norm(int64_t P, double *g, double max_norm)
@@ -462,11 +593,35 @@ void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
     int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * (size_t)B);
     double *grad = (double *)malloc(sizeof(double) * (size_t)P);
 
+    orc_loss_cfg lc = {hp->clip, hp->vf_coef, hp->ent_coef, hp->bf16_operands};
+    if (hp->adv_mode != 0) {
+        /* sec. 8: minibatches of whole environment segments, advantages
+         * recomputed per minibatch from fresh values (GAE or V-trace); epoch
+         * e shuffles the N environments with the rule of orc_perm */
+        const int64_t ns = N / minibatches;
+        for (int64_t e = 0; e < epochs; ++e) {
+            orc_perm(hp->seed, e, N, perm);
+            for (int64_t k = 0; k < minibatches; ++k) {
+                double *st = stats ? stats + (e * minibatches + k) * 6 : NULL;
+                double tmp[6];
+                orc_loss_grad_fresh(net, &lc, params, T, N, ns, perm + k * ns, obs, act_disc,
+                                    act_cont, logp_old, rew, done, boot, hp->adv_mode == 2,
+                                    hp->gamma, hp->lambda, hp->rho_clip, hp->c_clip, grad,
+                                    st ? st : tmp, NULL, NULL, NULL);
+                orc_clip_grad_norm(P, grad, hp->max_grad_norm);
+                *step += 1;
+                orc_adam(P, params, grad, m, v, *step, hp->lr, hp->beta1, hp->beta2,
+                         hp->adam_eps);
+            }
+        }
+        free(adv); free(ret); free(perm); free(grad);
+        return;
+    }
+
     orc_gae(T, N, rew, val, done, boot, hp->gamma, hp->lambda, adv, ret);
     double mean, sd;
     orc_moments(B, adv, &mean, &sd);
 
-    orc_loss_cfg lc = {hp->clip, hp->vf_coef, hp->ent_coef, hp->bf16_operands};
     for (int64_t e = 0; e < epochs; ++e) {
         orc_perm(hp->seed, e, B, perm);
         for (int64_t k = 0; k < minibatches; ++k) {

@@ -42,6 +42,17 @@ void orc_gae(int64_t T, int64_t N, const float *rew, const float *val,
              const float *done, const float *boot, double gamma, double lambda,
              double *adv, double *ret);
 
+/* Advantages of whole environment segments from given values: V-trace
+ * (Espeholt et al. 2018, sec. 4.1) with rho = min(rho_clip, ratio) and
+ * c = lambda min(c_clip, ratio); ratio == NULL gives GAE (rho = 1, c = lambda).
+ * Segment j is environment envs[j]; val, ratio, adv, ret are [T][ns]
+ * (element t*ns + j); rew, done [T][N]; boot [N].  adv = v - V, ret = v. */
+void orc_segment_advantage(int64_t T, int64_t N, const float *rew, const float *done,
+                           const float *boot, int64_t ns, const int32_t *envs,
+                           const double *val, const double *ratio, double gamma,
+                           double lambda, double rho_clip, double c_clip, double *adv,
+                           double *ret);
+
 /* Mean and unbiased (n-1) standard deviation, two passes. */
 void orc_moments(int64_t n, const double *x, double *mean, double *std_unbiased);
 
@@ -106,6 +117,24 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
                      int normalize, double adv_mean, double adv_std,
                      double *grad, double *stats6, double *scale6);
 
+/* Fresh values (value column at params) and ratios exp(logp - logp_old) of
+ * rows idx[0..n).  bf16: operand rounding as in orc_loss_cfg.  ratio nullable. */
+void orc_fresh_values(const orc_net *net, int bf16, const double *params, int64_t n,
+                      const int32_t *idx, const float *obs, const int32_t *act_disc,
+                      const float *act_cont, const float *logp_old, double *val, double *ratio);
+
+/* Loss and gradient of the minibatch of environment segments envs[0..ns)
+ * (rows t*N + envs[j], in the order t*ns + j) with advantages from fresh
+ * values: GAE (vtrace 0) or V-trace (vtrace 1), normalised over the
+ * minibatch.  adv_norm_out / ret_out nullable [T*ns].  Returns the loss. */
+double orc_loss_grad_fresh(const orc_net *net, const orc_loss_cfg *cfg, const double *params,
+                           int64_t T, int64_t N, int64_t ns, const int32_t *envs,
+                           const float *obs, const int32_t *act_disc, const float *act_cont,
+                           const float *logp_old, const float *rew, const float *done,
+                           const float *boot, int vtrace, double gamma, double lambda,
+                           double rho_clip, double c_clip, double *grad, double *stats6,
+                           double *scale6, double *adv_norm_out, double *ret_out);
+
 /* L2 norm of g; if max_norm > 0, g *= min(1, max_norm/(norm + 1e-6)).
  * Returns the norm before clipping. */
 double orc_clip_grad_norm(int64_t P, double *g, double max_norm);
@@ -119,10 +148,17 @@ typedef struct {
     double lr, beta1, beta2, adam_eps, max_grad_norm;
     uint32_t seed;
     int bf16_operands;   /* as in orc_loss_cfg */
+    int adv_mode;        /* 0: GAE once per update over the whole rollout;
+                            1: per minibatch of env segments, GAE from fresh values;
+                            2: the same with V-trace */
+    double rho_clip, c_clip;   /* V-trace truncation levels (adv_mode 2) */
 } orc_hyper;
 
 /* One whole PPO update: GAE, global advantage statistics, then for each epoch
  * a fresh permutation and M minibatch steps (loss+grad, norm clip, Adam).
+ * adv_mode 1/2: each epoch permutes the N environments instead, minibatch k
+ * is the segments of envs perm[k*N/M .. (k+1)*N/M) with orc_loss_grad_fresh,
+ * and adv_out/ret_out are not written.
  * params, m, v are updated in place; *step is incremented per minibatch.
  * stats (E*M*6) receives the per-minibatch stats6.  adv_out/ret_out [T*N]
  * may be NULL. */
