@@ -100,6 +100,26 @@ typedef struct {
                                     in shared memory and reads it once (H2 in
                                     {128, 256, 512}).  Same results up to fp32
                                     summation order.                         */
+    int32_t adv_mode;            /* advantages of ppo_update:
+                                    0 (default) GAE once per update over the
+                                      whole rollout, normalised over all T*N;
+                                    1 per minibatch from fresh values ("Teaching
+                                      Mario to speedrun", sec. 8): minibatches
+                                      are whole environment segments (epoch e
+                                      shuffles the N environments with the rule
+                                      of ppo_minibatch_perm, minibatch k takes
+                                      N/minibatches of them), and before each
+                                      loss the advantages are recomputed by GAE
+                                      from the current network's values and
+                                      normalised over the minibatch;
+                                    2 as 1 with V-trace (see
+                                      ppo_segment_advantage) using the current
+                                      network's importance ratios.
+                                    Modes 1 and 2 run the per-stage kernels
+                                    (persistent_minibatch and fused_mlp are
+                                    ignored) and need N % minibatches == 0.   */
+    float vtrace_rho_clip;       /* V-trace rho_bar (adv_mode 2; IMPALA: 1)    */
+    float vtrace_c_clip;         /* V-trace c_bar   (adv_mode 2; IMPALA: 1)    */
 } ppo_config;
 
 typedef struct ppo_ctx ppo_ctx;
@@ -168,6 +188,36 @@ ppo_status ppo_gae_noalloc(const float *d_rew, const float *d_val, const float *
                            float *d_adv, float *d_ret, float *d_adv_norm, float *d_stats,
                            cudaStream_t stream);
 
+/* ---- Advantages of environment segments (per-minibatch recompute) ----------
+ * "Teaching Mario to speedrun", sec. 8 "The Puffer net, and the trainer":
+ * advantages computed per minibatch from fresh values, by GAE or V-trace.
+ * V-trace is defined by Espeholt et al. 2018 ("IMPALA", sec. 4.1, eq. 1 with
+ * lambda-weighted traces): with rho_t = min(rho_clip, ratio_t) and
+ * c_t = lambda min(c_clip, ratio_t),
+ *   A_t = rho_t delta_t + gamma c_t (1 - d_t) A_{t+1},  A_T = 0,
+ *   delta_t = r_t + gamma (1 - d_t) V_{t+1} - V_t,      V_T = boot,
+ * ret_t = A_t + V_t (the V-trace target v_t).  d_ratio == NULL is GAE
+ * (rho = 1, c = lambda; the clips are ignored).  Terminals as in ppo_gae.
+ * Segment j is environment d_envs[j] (int32 [ns], each in [0, N); clamped
+ * on the device) over the whole horizon; the segment arrays are [T][ns]
+ * (element t*ns + j):
+ *   d_val    fp32 [T][ns]  values V(s_t) of the segments' steps
+ *   d_ratio  fp32 [T][ns]  importance ratios pi/mu, or NULL
+ *   d_rew, d_done fp32 [T][N]; d_boot fp32 [N]  (the whole rollout)
+ * Outputs d_adv, d_ret fp32 [T][ns]; d_adv_norm (nullable, may equal d_adv)
+ * = (A - mean)/(std + 1e-8); d_stats (nullable) fp32 [2] = {mean, unbiased
+ * std} of A over the T*ns entries.  d_work: ppo_segment_advantage_workspace_bytes()
+ * bytes of device scratch; its int32 at byte offset 4 is set nonzero if a
+ * bounded device wait of the call gave up (outputs then unspecified).
+ * T, ns >= 1; T*ns < 2^31.  Deterministic. */
+ppo_status ppo_segment_advantage_workspace_bytes(size_t *bytes);
+ppo_status ppo_segment_advantage(const float *d_rew, const float *d_done, const float *d_boot,
+                                 int64_t T, int64_t N, const int32_t *d_envs, int64_t ns,
+                                 const float *d_val, const float *d_ratio, float gamma,
+                                 float lambda, float rho_clip, float c_clip, float *d_adv,
+                                 float *d_ret, float *d_adv_norm, float *d_stats, void *d_work,
+                                 size_t work_bytes, cudaStream_t stream);
+
 /* ---- Minibatch permutation -------------------------------------------------
  * "Teaching Mario to speedrun", sec. 6: "for minibatch in shuffle(batch)".
  * Key i = mulberry32 draw number epoch*B + i of the stream seeded with `seed`
@@ -202,6 +252,27 @@ ppo_status ppo_minibatch_loss_grad(ppo_ctx *ctx, const float *d_obs, const int32
                                    const float *d_adv, const float *d_ret, const int32_t *d_idx,
                                    int64_t B, int64_t mb, const float *d_adv_stats,
                                    float *d_stats6, cudaStream_t stream);
+
+/* Loss and gradient of a minibatch of environment segments with advantages
+ * from fresh values ("Teaching Mario to speedrun", sec. 8): the rows are
+ * (t, d_envs[j]) for t < T, j < ns (batch row t*N + d_envs[j]), in the order
+ * t*ns + j.  After the forward pass, the value of every row (adv_mode 1: GAE)
+ * and, for V-trace (adv_mode 2), the ratio exp(logp - logp_old) of its action
+ * feed ppo_segment_advantage's recursion (clips from the config); the
+ * advantages are normalised over the minibatch and the loss uses ret = A + V
+ * as the value target.  d_rew, d_done [T][N], d_boot [N]; other inputs as in
+ * ppo_minibatch_loss_grad (B = T*N).  The gradient overwrites the context's
+ * gradient buffer; d_stats6 as there.  d_adv_out / d_ret_out (nullable, fp32
+ * [T*ns]) receive the normalised advantages and the value targets.
+ * 1 <= T*ns <= max_minibatch; adv_mode 1 or 2. */
+ppo_status ppo_minibatch_loss_grad_fresh(ppo_ctx *ctx, const float *d_obs,
+                                         const int32_t *d_act_disc, const float *d_act_cont,
+                                         const float *d_logp_old, const float *d_rew,
+                                         const float *d_done, const float *d_boot, int64_t T,
+                                         int64_t N, const int32_t *d_envs, int64_t ns,
+                                         int32_t adv_mode, float gamma, float lambda,
+                                         float *d_stats6, float *d_adv_out, float *d_ret_out,
+                                         cudaStream_t stream);
 
 /* ---- Optimizer step ---------------------------------------------------------
  * "PlayTrain", Table 8 (PPO column): Adam with gradient-norm clip.
@@ -246,8 +317,8 @@ ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_ac
  * phases inside the persistent minibatch kernel (time between the phase
  * starts seen by its first CTA, summed over minibatches); they are not
  * separate launches. */
-#define PPO_NUM_KERNEL_STAGES 22
-#define PPO_NUM_STAGES 31
+#define PPO_NUM_KERNEL_STAGES 23
+#define PPO_NUM_STAGES 32
 /* Name of a stage (static string; "unknown" outside [0, PPO_NUM_STAGES)). */
 const char *ppo_stage_name(int32_t stage);
 

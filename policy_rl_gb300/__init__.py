@@ -17,6 +17,8 @@ from ._abi import PpoConfig, PpoError
 __all__ = [
     "PpoConfig", "PpoError", "Context", "make_config", "ppo_param_count", "ppo_gae",
     "ppo_gae_workspace_bytes", "ppo_gae_noalloc", "ppo_minibatch_perm", "ppo_perm_workspace_bytes",
+    "ppo_segment_advantage", "ppo_segment_advantage_workspace_bytes",
+    "ppo_minibatch_loss_grad_fresh",
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
     "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "library_path",
@@ -54,15 +56,18 @@ def _stream(stream):
 def make_config(obs_dim, h1, h2, act=0, heads=(3, 2, 2), n_gauss=0, precision=1, clip=0.2,
                 vf_coef=0.5, ent_coef=0.01, beta1=0.9, beta2=0.999, adam_eps=1e-8,
                 max_grad_norm=0.5, max_batch=1, max_minibatch=1, max_epochs=1,
-                persistent_minibatch=0, fused_mlp=0, fused_loss=0) -> PpoConfig:
+                persistent_minibatch=0, fused_mlp=0, fused_loss=0, adv_mode=0,
+                vtrace_rho_clip=1.0, vtrace_c_clip=1.0) -> PpoConfig:
     hn = (ctypes.c_int32 * _abi.MAX_HEADS)(*(list(heads) + [0] * (_abi.MAX_HEADS - len(heads))))
     return PpoConfig(obs_dim, h1, h2, act, len(heads), hn, n_gauss, precision, clip, vf_coef,
                      ent_coef, max_grad_norm, beta1, beta2, adam_eps, max_batch, max_minibatch,
-                     max_epochs, persistent_minibatch, fused_mlp, fused_loss)
+                     max_epochs, persistent_minibatch, fused_mlp, fused_loss, adv_mode,
+                     vtrace_rho_clip, vtrace_c_clip)
 
 
 def config_from_workload(w, max_batch=None, max_minibatch=None, max_epochs=None,
-                         persistent_minibatch=0, fused_mlp=0, fused_loss=0) -> PpoConfig:
+                         persistent_minibatch=0, fused_mlp=0, fused_loss=0, adv_mode=0,
+                         vtrace_rho_clip=1.0, vtrace_c_clip=1.0) -> PpoConfig:
     B = w.T * w.N
     return make_config(w.obs_dim, w.h1, w.h2, w.act, tuple(w.heads), w.n_gauss,
                        1 if w.precision == "bf16" else 0, w.clip, w.vf_coef, w.ent_coef,
@@ -70,7 +75,8 @@ def config_from_workload(w, max_batch=None, max_minibatch=None, max_epochs=None,
                        max_minibatch=max_minibatch or B // w.minibatches,
                        max_epochs=max_epochs or w.epochs,
                        persistent_minibatch=persistent_minibatch,
-                       fused_mlp=fused_mlp, fused_loss=fused_loss)
+                       fused_mlp=fused_mlp, fused_loss=fused_loss, adv_mode=adv_mode,
+                       vtrace_rho_clip=vtrace_rho_clip, vtrace_c_clip=vtrace_c_clip)
 
 
 # ---- free functions -----------------------------------------------------------
@@ -102,6 +108,26 @@ def ppo_gae_noalloc(rew, val, done, boot, gamma, lam, adv, ret, adv_norm=None, s
     _abi.check(_lib().ppo_gae_noalloc(_ptr(rew), _ptr(val), _ptr(done), _ptr(boot), T, N, gamma,
                                       lam, _ptr(adv), _ptr(ret), _ptr(adv_norm), _ptr(stats),
                                       _stream(stream)), "ppo_gae_noalloc")
+
+
+def ppo_segment_advantage_workspace_bytes() -> int:
+    n = ctypes.c_size_t()
+    _abi.check(_lib().ppo_segment_advantage_workspace_bytes(ctypes.byref(n)),
+               "ppo_segment_advantage_workspace_bytes")
+    return n.value
+
+
+def ppo_segment_advantage(rew, done, boot, envs, val, ratio, gamma, lam, adv, ret,
+                          rho_clip=1.0, c_clip=1.0, adv_norm=None, stats=None, work=None,
+                          stream=None) -> None:
+    """GAE / V-trace advantages of the environment segments ``envs`` (see ppo.h)."""
+    T, N = rew.shape
+    ns = envs.numel()
+    wb = work.numel() * work.element_size() if work is not None else 0
+    _abi.check(_lib().ppo_segment_advantage(
+        _ptr(rew), _ptr(done), _ptr(boot), T, N, _ptr(envs), ns, _ptr(val), _ptr(ratio), gamma,
+        lam, rho_clip, c_clip, _ptr(adv), _ptr(ret), _ptr(adv_norm), _ptr(stats), _ptr(work), wb,
+        _stream(stream)), "ppo_segment_advantage")
 
 
 def ppo_perm_workspace_bytes(B: int) -> int:
@@ -164,6 +190,16 @@ def ppo_minibatch_loss_grad(ctx, obs, act_disc, act_cont, logp_old, adv, ret, id
         ctx, _ptr(obs), _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(adv), _ptr(ret),
         _ptr(idx), B, idx.numel(), _ptr(adv_stats), _ptr(stats6), _stream(stream)),
         "ppo_minibatch_loss_grad")
+
+
+def ppo_minibatch_loss_grad_fresh(ctx, obs, act_disc, act_cont, logp_old, rew, done, boot, envs,
+                                  adv_mode, gamma, lam, stats6=None, adv_out=None, ret_out=None,
+                                  stream=None) -> None:
+    T, N = rew.shape
+    _abi.check(_lib().ppo_minibatch_loss_grad_fresh(
+        ctx, _ptr(obs), _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(rew), _ptr(done),
+        _ptr(boot), T, N, _ptr(envs), envs.numel(), adv_mode, gamma, lam, _ptr(stats6),
+        _ptr(adv_out), _ptr(ret_out), _stream(stream)), "ppo_minibatch_loss_grad_fresh")
 
 
 def ppo_adam_step(ctx, lr, grad_norm=None, stream=None) -> None:
@@ -231,6 +267,9 @@ class Context:
 
     def minibatch_loss_grad(self, *a, **k):
         return ppo_minibatch_loss_grad(self.handle, *a, **k)
+
+    def minibatch_loss_grad_fresh(self, *a, **k):
+        return ppo_minibatch_loss_grad_fresh(self.handle, *a, **k)
 
     def adam_step(self, *a, **k):
         return ppo_adam_step(self.handle, *a, **k)

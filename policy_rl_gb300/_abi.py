@@ -17,13 +17,13 @@ MAX_HEADS = 8
 SYMBOLS = (
     "ppo_status_string", "ppo_create", "ppo_destroy", "ppo_param_count", "ppo_buffers",
     "ppo_params_changed", "ppo_get_step", "ppo_gae_workspace_bytes", "ppo_gae",
-    "ppo_gae_noalloc",
+    "ppo_gae_noalloc", "ppo_segment_advantage_workspace_bytes", "ppo_segment_advantage",
     "ppo_perm_workspace_bytes", "ppo_minibatch_perm", "ppo_minibatch_loss_grad",
-    "ppo_adam_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
+    "ppo_minibatch_loss_grad_fresh", "ppo_adam_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
     "ppo_sync_status",
 )
-NUM_STAGES = 31
-NUM_KERNEL_STAGES = 22
+NUM_STAGES = 32
+NUM_KERNEL_STAGES = 23
 
 STATUS = {0: "PPO_OK", 1: "PPO_ERR_INVALID", 2: "PPO_ERR_ALIGN", 3: "PPO_ERR_CUDA",
           4: "PPO_ERR_UNSUPPORTED", 5: "PPO_ERR_TIMEOUT", 6: "PPO_ERR_NOMEM"}
@@ -46,6 +46,8 @@ class PpoConfig(ctypes.Structure):
         ("max_batch", ctypes.c_int64), ("max_minibatch", ctypes.c_int64),
         ("max_epochs", ctypes.c_int32), ("persistent_minibatch", ctypes.c_int32),
         ("fused_mlp", ctypes.c_int32), ("fused_loss", ctypes.c_int32),
+        ("adv_mode", ctypes.c_int32), ("vtrace_rho_clip", ctypes.c_float),
+        ("vtrace_c_clip", ctypes.c_float),
     ]
 
 
@@ -82,10 +84,15 @@ def load(path: str = LIB_PATH):
                     ctypes.c_int),
         "ppo_gae_noalloc": ([_P, _P, _P, _P, _I64, _I64, _F, _F, _P, _P, _P, _P, _P],
                             ctypes.c_int),
+        "ppo_segment_advantage_workspace_bytes": ([ctypes.POINTER(_SZ)], ctypes.c_int),
+        "ppo_segment_advantage": ([_P, _P, _P, _I64, _I64, _P, _I64, _P, _P, _F, _F, _F, _F,
+                                   _P, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
         "ppo_perm_workspace_bytes": ([_I64, ctypes.POINTER(_SZ)], ctypes.c_int),
         "ppo_minibatch_perm": ([u32, _I64, _I64, _P, _P, _SZ, _P], ctypes.c_int),
         "ppo_minibatch_loss_grad": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P],
                                     ctypes.c_int),
+        "ppo_minibatch_loss_grad_fresh": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _I64,
+                                           i32, _F, _F, _P, _P, _P, _P], ctypes.c_int),
         "ppo_adam_step": ([_P, _F, _P, _P], ctypes.c_int),
         "ppo_update": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F, _F,
                         u32, _P, _P], ctypes.c_int),

@@ -66,6 +66,10 @@ struct ppo_ctx {
   bool use_fmlp = false;   // fused forward + loss + backward-data kernel
   bool use_hl2 = false;    // head + loss + layer-2 backward-data kernel
   unsigned* rbar = nullptr; // grid-barrier counter of the reduce + Adam kernel
+  // per-minibatch advantages from fresh values (adv_mode 1, 2)
+  float *vfresh = nullptr, *rfresh = nullptr;   // [mbmax] fresh values / ratios
+  double* fpart = nullptr;                      // [kFreshMaxGrid][3] moment partials
+  unsigned* fbar = nullptr;                     // grid-barrier counter of that kernel
   void* X = nullptr;
   // one epoch of minibatch rows gathered in permutation order (ppo_update)
   void* X_ep = nullptr;
@@ -150,6 +154,7 @@ ppo_status shape_from(const ppo_config* c, NetShape* s) {
   if (c->n_heads < 0 || c->n_heads > PPO_MAX_HEADS) return PPO_ERR_INVALID;
   if (c->n_gauss < 0 || c->n_gauss > 4) return PPO_ERR_INVALID;
   if (c->precision != 0 && c->precision != 1) return PPO_ERR_INVALID;
+  if (c->adv_mode < 0 || c->adv_mode > 2) return PPO_ERR_INVALID;
   std::memset(s, 0, sizeof(*s));
   s->D = c->obs_dim;
   s->H1 = c->h1;
@@ -276,14 +281,52 @@ cudaError_t enqueue_gather(ppo_ctx* c, const float* obs, const __nv_bfloat16* ob
   return launch_gather(c->s, ga, st);
 }
 
+// Gathers the rows of minibatches of environment segments: n rows, minibatch m
+// being envs[m*ns .. (m+1)*ns) over the horizon T, rows ordered t*ns + j.
+// Advantages and returns are left to the fresh-advantage kernel.
+cudaError_t enqueue_gather_seg(ppo_ctx* c, const float* obs, const __nv_bfloat16* obs_packed,
+                               const int32_t* act, const float* actc, const float* logp_old,
+                               const int32_t* envs, int T, int ns, int64_t N, int64_t n,
+                               const MbRows& r, cudaStream_t st) {
+  GatherArgs ga{};
+  ga.obs_f32 = obs;
+  ga.obs_bf16 = obs_packed;
+  ga.act = act;
+  ga.actc = actc;
+  ga.logp_old = logp_old;
+  ga.mb = n;
+  ga.B = (int64_t)T * N;
+  ga.seg_envs = envs;
+  ga.seg_T = T;
+  ga.seg_ns = ns;
+  ga.seg_N = N;
+  ga.X = r.X;
+  ga.x_bf16 = c->bf16;
+  ga.act_mb = r.act;
+  ga.actc_mb = r.actc;
+  ga.logp_mb = r.logp;
+  return launch_gather(c->s, ga, st);
+}
+
+// Advantages of one minibatch from fresh values: the rollout's rewards, dones
+// and bootstrap values, the minibatch's environments, and the scan's settings.
+struct FreshSpec {
+  const float *rew, *done, *boot;
+  const int32_t* envs;   // [ns]
+  int T, ns;
+  int64_t N;
+  float gamma, lambda;
+  int vtrace;
+};
+
 // One minibatch: gather (unless its rows are given, already gathered),
-// forward, loss, backward, gradient assembly.
+// forward, [advantages from fresh values], loss, backward, gradient assembly.
 ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* obs_packed,
                              const int32_t* act, const float* actc, const float* logp_old,
                              const float* adv, const float* ret, const int32_t* idx, int64_t B,
                              int64_t mb, const float* adv_stats, float* stats6, cudaStream_t st,
                              int* nsq_out = nullptr, const MbRows* pre = nullptr,
-                             const AdamArgs* adam = nullptr) {
+                             const AdamArgs* adam = nullptr, const FreshSpec* fr = nullptr) {
   const NetShape& s = c->s;
   MbRows mr{c->X, c->act_mb, c->actc_mb, c->logp_mb, c->adv_mb, c->ret_mb};
   if (pre) {
@@ -299,6 +342,44 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
   const float inv_mb = 1.0f / (float)mb;
   const float* P = c->params;
   const int M = (int)mb;
+  // advantages from the values (and ratios) of the forward pass just run;
+  // they overwrite the minibatch rows' advantages (normalised) and returns
+  auto fresh_adv = [&](const void* H2) -> cudaError_t {
+    FreshAdvArgs f{};
+    f.head = 1;
+    f.s = s;
+    f.H2 = H2;
+    f.h2_bf16 = c->bf16;
+    f.W3 = c->bf16 ? static_cast<const void*>(c->sh.W3s) : static_cast<const void*>(P + s.oW3);
+    f.b3 = P + s.ob3;
+    f.logstd = P + s.ologstd;
+    f.act = mr.act;
+    f.actc = mr.actc;
+    f.logp_old = mr.logp;
+    f.rew = fr->rew;
+    f.done = fr->done;
+    f.boot = fr->boot;
+    f.envs = fr->envs;
+    f.T = fr->T;
+    f.ns = fr->ns;
+    f.N = fr->N;
+    f.val = c->vfresh;
+    f.ratio = fr->vtrace ? c->rfresh : nullptr;
+    f.gamma = fr->gamma;
+    f.lambda = fr->lambda;
+    f.rho_clip = c->cfg.vtrace_rho_clip;
+    f.c_clip = c->cfg.vtrace_c_clip;
+    f.adv = mr.adv;
+    f.ret = mr.ret;
+    f.adv_norm = mr.adv;
+    f.part = c->fpart;
+    f.bar = c->fbar;
+    f.err = c->err;
+    f.timeout_ns = kTimeoutNs;
+    cudaError_t e = launch_fresh_adv(f, c->num_sms, st);
+    if (e == cudaSuccess) c->tr.mark(ST_FRESH_ADV, st);
+    return e;
+  };
 
   ReduceArgs ra{};
   ra.s = s;
@@ -316,7 +397,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     auto* dP1 = static_cast<__nv_bfloat16*>(c->dP1);
     const int ns = c->num_sms;
     int n3 = 0, n2 = 0, n1 = 0;
-    if (c->use_fmlp) {
+    if (c->use_fmlp && !fr) {
       // forward, loss and backward-data in one kernel (activations stay on chip)
       FusedMlp f{};
       f.s = s;
@@ -358,6 +439,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     GemmOperands g2{H1, s.H1, c->sh.W2s, s.H1, M, s.H2, s.H1};
     PPO_CUDA(tc_gemm_bias_act(g2, P + s.ob2, s.act, H2, s.H2, c->err, kTimeoutNs, ns, st));
     c->tr.mark(ST_FWD2, st);
+    if (fr) PPO_CUDA(fresh_adv(H2));
     if (c->use_hl2) {
       // head + loss + dP2 = (dz W3) * act'(H2) in one kernel (H2 read once)
       HeadLossDact f{};
@@ -427,6 +509,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     SimtOperands g2{H1, s.H1, 1, P + s.oW2, s.H1, 1, M, s.H2, s.H1};
     PPO_CUDA(simt_bias_act(g2, P + s.ob2, s.act, H2, s.H2, st));
     c->tr.mark(ST_FWD2, st);
+    if (fr) PPO_CUDA(fresh_adv(H2));
     int n3 = 0;
     PPO_CUDA(simt_head_loss(s, lc, rows, inv_mb, H2, P + s.oW3, P + s.ob3, P + s.ologstd, M, dZ,
                             c->cs3, c->lossp, st, &n3));
@@ -626,6 +709,43 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
                           int parts = 3) {
   const int64_t B = T * N, mb = B / minibatches;
   const __nv_bfloat16* packed = c->bf16 ? c->obs_packed : nullptr;
+  if (c->cfg.adv_mode != 0) {
+    // advantages per minibatch of environment segments, from fresh values
+    // ("Teaching Mario to speedrun", sec. 8); epoch e shuffles the N
+    // environments with the mulberry32 rule, minibatch k takes N/M of them
+    const int ns = (int)(N / minibatches);
+    if (parts & 1) {
+      PPO_CUDA(cudaMemsetAsync(c->rbar, 0, sizeof(unsigned), st));
+      PPO_CUDA(cudaMemsetAsync(c->fbar, 0, sizeof(unsigned), st));
+      PPO_CUDA(launch_perm(seed, 0, epochs, N, c->perm, c->perm_work, st, &c->tr));
+    }
+    if (!(parts & 2)) return PPO_OK;
+    if (c->bf16) {
+      PPO_CUDA(launch_pack_obs(obs, B, c->s.D, c->s.Dp, c->obs_packed, st));
+      c->tr.mark(ST_PACK, st);
+    }
+    const MbRows ep{c->X_ep, c->act_ep, c->actc_ep, c->logp_ep, c->adv_ep, c->ret_ep};
+    const int64_t xrow = c->bf16 ? (int64_t)c->s.Dp * 2 : (int64_t)c->s.D * 4;
+    const int NH = c->s.NH > 0 ? c->s.NH : 1, G = c->s.G > 0 ? c->s.G : 1;
+    for (int e = 0; e < epochs; ++e) {
+      const int32_t* perm_e = c->perm + (int64_t)e * N;
+      PPO_CUDA(enqueue_gather_seg(c, obs, packed, act, actc, logp_old, perm_e, (int)T, ns, N, B,
+                                  ep, st));
+      c->tr.mark(ST_GATHER, st);
+      for (int k = 0; k < minibatches; ++k) {
+        float* st6 = stats ? stats + ((int64_t)e * minibatches + k) * 6 : nullptr;
+        const int64_t r0 = (int64_t)k * mb;
+        const MbRows mr{static_cast<uint8_t*>(ep.X) + r0 * xrow, ep.act + r0 * NH,
+                        ep.actc + r0 * G, ep.logp + r0, ep.adv + r0, ep.ret + r0};
+        const AdamArgs aa = make_adam_args(c, lr, nullptr, 0);
+        const FreshSpec fs{rew, done, boot, perm_e + (int64_t)k * ns, (int)T, ns, N, gamma,
+                           lambda, c->cfg.adv_mode == 2};
+        TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, nullptr, nullptr, nullptr, B,
+                              mb, nullptr, st6, st, nullptr, &mr, &aa, &fs));
+      }
+    }
+    return PPO_OK;
+  }
   if (parts & 1) {
     // part 1 reads only rewards, values, dones and bootstrap values
     if (c->use_mk)   // grid-barrier counters start at zero (also after an aborted launch)
@@ -725,8 +845,11 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   c->cfg = *cfg;
   c->s = s;
   c->bf16 = cfg->precision == 1;
-  c->use_mk = c->bf16 && cfg->persistent_minibatch != 0;
-  c->use_fmlp = c->bf16 && !c->use_mk && cfg->fused_mlp != 0 && fmlp_supported(s);
+  // the persistent and fused-MLP kernels have no step between the forward
+  // pass and the loss, where per-minibatch advantages are computed
+  c->use_mk = c->bf16 && cfg->persistent_minibatch != 0 && cfg->adv_mode == 0;
+  c->use_fmlp = c->bf16 && !c->use_mk && cfg->fused_mlp != 0 && cfg->adv_mode == 0 &&
+                fmlp_supported(s);
   c->use_hl2 = c->bf16 && !c->use_mk && cfg->fused_loss != 0 && hl2_supported(s);
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (c->num_sms < 1) c->num_sms = 1;
@@ -755,6 +878,10 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->err, 1);
   A(c->sq, std::max(4096, reduce_blocks(s)));
   A(c->rbar, 1);
+  A(c->fbar, 1);
+  A(c->fpart, 3 * (int64_t)kFreshMaxGrid);
+  A(c->vfresh, cfg->max_minibatch);
+  A(c->rfresh, cfg->max_minibatch);
   if (c->bf16) {
     c->sh.ld3t = 64;
     A(c->sh.W1s, (int64_t)s.H1 * s.Dp);
@@ -827,6 +954,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   if (c->use_fmlp && fmlp_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (c->use_hl2 && hl2_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (reduce_adam_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
+  if (fresh_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (c->use_mk && mk_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (h_init_params) {
     if (cudaMemcpy(c->params, h_init_params, sizeof(float) * P, cudaMemcpyHostToDevice) !=
@@ -935,6 +1063,93 @@ ppo_status ppo_minibatch_loss_grad(ppo_ctx* c, const float* obs, const int32_t* 
                            stats6, st);
 }
 
+ppo_status ppo_minibatch_loss_grad_fresh(ppo_ctx* c, const float* obs, const int32_t* act,
+                                         const float* actc, const float* logp_old,
+                                         const float* rew, const float* done, const float* boot,
+                                         int64_t T, int64_t N, const int32_t* envs, int64_t ns,
+                                         int32_t adv_mode, float gamma, float lambda,
+                                         float* stats6, float* adv_out, float* ret_out,
+                                         cudaStream_t st) {
+  if (!c || !obs || !logp_old || !rew || !done || !boot || !envs) return PPO_ERR_INVALID;
+  if (c->s.NH > 0 && !act) return PPO_ERR_INVALID;
+  if (c->s.G > 0 && !actc) return PPO_ERR_INVALID;
+  if (adv_mode != 1 && adv_mode != 2) return PPO_ERR_INVALID;
+  if (T < 1 || N < 1 || ns < 1 || T * N >= (1ll << 31) || T * ns > c->mbmax)
+    return PPO_ERR_INVALID;
+  const void* ps[] = {obs, act, actc, logp_old, rew, done, boot, envs, stats6, adv_out, ret_out};
+  for (const void* p : ps)
+    if (p && !al16(p)) return PPO_ERR_ALIGN;
+  const int64_t mb = T * ns;
+  const MbRows mr{c->X, c->act_mb, c->actc_mb, c->logp_mb, c->adv_mb, c->ret_mb};
+  PPO_CUDA(cudaMemsetAsync(c->fbar, 0, sizeof(unsigned), st));
+  PPO_CUDA(enqueue_gather_seg(c, obs, nullptr, act, actc, logp_old, envs, (int)T, (int)ns, N, mb,
+                              mr, st));
+  c->tr.mark(ST_GATHER, st);
+  const FreshSpec fs{rew, done, boot, envs, (int)T, (int)ns, N, gamma, lambda, adv_mode == 2};
+  TRY(enqueue_minibatch(c, obs, nullptr, act, actc, logp_old, nullptr, nullptr, nullptr, T * N,
+                        mb, nullptr, stats6, st, nullptr, &mr, nullptr, &fs));
+  if (adv_out)
+    PPO_CUDA(cudaMemcpyAsync(adv_out, c->adv_mb, sizeof(float) * mb, cudaMemcpyDeviceToDevice, st));
+  if (ret_out)
+    PPO_CUDA(cudaMemcpyAsync(ret_out, c->ret_mb, sizeof(float) * mb, cudaMemcpyDeviceToDevice, st));
+  return PPO_OK;
+}
+
+ppo_status ppo_segment_advantage_workspace_bytes(size_t* bytes) {
+  if (!bytes) return PPO_ERR_INVALID;
+  *bytes = 16 + sizeof(double) * 3 * (size_t)kFreshMaxGrid;
+  return PPO_OK;
+}
+
+ppo_status ppo_segment_advantage(const float* rew, const float* done, const float* boot,
+                                 int64_t T, int64_t N, const int32_t* envs, int64_t ns,
+                                 const float* val, const float* ratio, float gamma, float lambda,
+                                 float rho_clip, float c_clip, float* adv, float* ret,
+                                 float* adv_norm, float* stats, void* work, size_t work_bytes,
+                                 cudaStream_t st) {
+  if (!rew || !done || !boot || !envs || !val || !adv || !ret || !work) return PPO_ERR_INVALID;
+  if (T < 1 || N < 1 || ns < 1 || T * N >= (1ll << 31) || T * ns >= (1ll << 31))
+    return PPO_ERR_INVALID;
+  size_t need = 0;
+  ppo_segment_advantage_workspace_bytes(&need);
+  if (work_bytes < need) return PPO_ERR_INVALID;
+  const void* ps[] = {rew, done, boot, envs, val, ratio, adv, ret, adv_norm, stats, work};
+  for (const void* p : ps)
+    if (p && !al16(p)) return PPO_ERR_ALIGN;
+  PPO_CUDA(fresh_prepare());
+  int dev = 0, nsm = 1;
+  PPO_CUDA(cudaGetDevice(&dev));
+  PPO_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+  unsigned* bar = static_cast<unsigned*>(work);
+  int* err = reinterpret_cast<int*>(static_cast<uint8_t*>(work) + 4);
+  PPO_CUDA(cudaMemsetAsync(work, 0, 16, st));
+  FreshAdvArgs f{};
+  f.head = 0;
+  f.rew = rew;
+  f.done = done;
+  f.boot = boot;
+  f.envs = envs;
+  f.T = (int)T;
+  f.ns = (int)ns;
+  f.N = N;
+  f.val = const_cast<float*>(val);
+  f.ratio = const_cast<float*>(ratio);
+  f.gamma = gamma;
+  f.lambda = lambda;
+  f.rho_clip = rho_clip;
+  f.c_clip = c_clip;
+  f.adv = adv;
+  f.ret = ret;
+  f.adv_norm = adv_norm;
+  f.stats = stats;
+  f.part = reinterpret_cast<double*>(static_cast<uint8_t*>(work) + 16);
+  f.bar = bar;
+  f.err = err;
+  f.timeout_ns = kTimeoutNs;
+  PPO_CUDA(launch_fresh_adv(f, nsm, st));
+  return PPO_OK;
+}
+
 ppo_status ppo_adam_step(ppo_ctx* c, float lr, float* grad_norm, cudaStream_t st) {
   if (!c) return PPO_ERR_INVALID;
   if (grad_norm && !al16(grad_norm)) return PPO_ERR_ALIGN;
@@ -950,6 +1165,7 @@ static ppo_status check_update_args(ppo_ctx* c, const float* obs, const int32_t*
   if (T < 1 || N < 1 || epochs < 1 || minibatches < 1) return PPO_ERR_INVALID;
   const int64_t B = T * N;
   if (B > c->bmax || epochs > c->emax || B % minibatches != 0) return PPO_ERR_INVALID;
+  if (c->cfg.adv_mode != 0 && N % minibatches != 0) return PPO_ERR_INVALID;
   const int64_t mb = B / minibatches;
   if (mb > c->mbmax || !obs || !logp_old || (c->s.NH > 0 && !act) || (c->s.G > 0 && !actc))
     return PPO_ERR_INVALID;
@@ -1044,7 +1260,8 @@ const char* ppo_stage_name(int32_t stage) {
       "pack_obs", "gae_scan", "gae_finalize", "gae_normalize", "perm_hist", "perm_scan",
       "perm_scatter", "gather", "fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm",
       "dact1_gemm", "wgrad_gemm", "grad_reduce", "grad_sqnorm", "adam", "weight_shadows",
-      "minibatch_persistent", "fused_mlp", "grad_reduce_adam", "head_loss_dact2"};
+      "minibatch_persistent", "fused_mlp", "grad_reduce_adam", "head_loss_dact2",
+      "fresh_advantages"};
   static const char* phases[kMkPhases] = {
       "phase:gather", "phase:fwd1", "phase:fwd2", "phase:head_loss", "phase:dact2",
       "phase:dact1", "phase:wgrad", "phase:grad_reduce", "phase:adam"};

@@ -215,7 +215,7 @@ enum Stage : int {
   ST_PACK = 0, ST_GAE, ST_GAE_FINALIZE, ST_GAE_NORMALIZE, ST_PERM_HIST, ST_PERM_SCAN,
   ST_PERM_SCATTER, ST_GATHER, ST_FWD1, ST_FWD2, ST_LOSS, ST_DACT2, ST_DACT1, ST_WGRAD,
   ST_REDUCE, ST_SQNORM, ST_ADAM, ST_SHADOW, ST_MINIBATCH, ST_FUSED_MLP, ST_REDUCE_ADAM,
-  ST_LOSS_DACT2, ST_COUNT
+  ST_LOSS_DACT2, ST_FRESH_ADV, ST_COUNT
 };
 
 struct Trace {
@@ -254,9 +254,14 @@ struct GatherArgs {
   const float* adv;                // [B]
   const float* ret;                // [B]
   const float* adv_stats;          // [2] mean, std or nullptr
-  const int32_t* idx;              // [mb], entries clamped to [0, B)
+  const int32_t* idx;              // [mb], entries clamped to [0, B); unused with seg_envs
   int64_t mb;
   int64_t B;
+  // segment rows instead of idx: row r = (m, t, j) with r = (m*T + t)*ns + j
+  // gathers batch row t*seg_N + seg_envs[m*ns + j] (entries clamped to [0, seg_N))
+  const int32_t* seg_envs;
+  int seg_T, seg_ns;
+  int64_t seg_N;
   // outputs
   void* X;                         // bf16 [mb][Dp] or fp32 [mb][D]
   int x_bf16;
@@ -267,5 +272,43 @@ struct GatherArgs {
   float* ret_mb;
 };
 cudaError_t launch_gather(const NetShape& s, const GatherArgs& a, cudaStream_t st);
+
+// Advantages of a minibatch of environment segments from fresh values
+// (fresh.cu).  Rows are ordered t*ns + j (segment j = environment envs[j]).
+constexpr int kFreshMaxGrid = 1024;
+struct FreshAdvArgs {
+  // phase A (head != 0): value, and with ratio != nullptr the importance
+  // ratio, of every row from the last hidden layer
+  int head;
+  NetShape s;
+  const void* H2;          // [rows][H2], bf16 (h2_bf16) or fp32
+  int h2_bf16;
+  const void* W3;          // bf16 shadow [CP][H2] or fp32 [C][H2]
+  const float* b3;
+  const float* logstd;
+  const int32_t* act;      // [rows][NH]
+  const float* actc;       // [rows][G]
+  const float* logp_old;   // [rows]
+  // phase B
+  const float* rew;        // [T][N]
+  const float* done;       // [T][N]
+  const float* boot;       // [N]
+  const int32_t* envs;     // [ns]
+  int T, ns;
+  int64_t N;
+  float* val;              // [rows] (written by phase A, else given)
+  float* ratio;            // [rows] or nullptr (GAE)
+  float gamma, lambda, rho_clip, c_clip;
+  float* adv;              // [rows] advantages
+  float* ret;              // [rows] value targets
+  float* adv_norm;         // [rows] normalised advantages (may equal adv), or nullptr
+  float* stats;            // [2] {mean, unbiased std} of adv, or nullptr
+  double* part;            // [kFreshMaxGrid][3]
+  unsigned* bar;           // zero on entry; reset to zero by the launch
+  int* err;
+  uint64_t timeout_ns;
+};
+cudaError_t fresh_prepare();
+cudaError_t launch_fresh_adv(const FreshAdvArgs& a, int num_sms, cudaStream_t st);
 
 }  // namespace ppo

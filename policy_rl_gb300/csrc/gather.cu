@@ -5,7 +5,8 @@
 // element.  Gather: rows idx[0..mb) of the batch ("Teaching Mario to
 // speedrun", sec. 6: "for minibatch in shuffle(batch)") into contiguous
 // minibatch buffers that the GEMMs' TMA loads can tile; the advantage is
-// normalised on the way, (A - mean)/(std + 1e-8).
+// normalised on the way, (A - mean)/(std + 1e-8).  Segment mode gathers whole
+// environment segments (sec. 8, advantages per minibatch from fresh values).
 #include "common.cuh"
 
 namespace ppo {
@@ -48,7 +49,19 @@ gather_kernel(NetShape s, GatherArgs a, int per_row) {
   const int64_t r = t / per_row;
   const int c = (int)(t - r * per_row);
   if (r >= a.mb) return;
-  int64_t src = __ldg(a.idx + r);
+  int64_t src;
+  if (a.seg_envs) {
+    const int64_t per = (int64_t)a.seg_T * a.seg_ns;
+    const int64_t m = r / per;
+    const int64_t rr = r - m * per;
+    const int64_t t = rr / a.seg_ns;
+    const int64_t j = rr - t * a.seg_ns;
+    int64_t e = __ldg(a.seg_envs + m * a.seg_ns + j);
+    e = e < 0 ? 0 : (e >= a.seg_N ? a.seg_N - 1 : e);
+    src = t * a.seg_N + e;
+  } else {
+    src = __ldg(a.idx + r);
+  }
   src = src < 0 ? 0 : (src >= a.B ? a.B - 1 : src);   // never read outside the batch
   if (a.obs_bf16) {
     const uint4* in = reinterpret_cast<const uint4*>(a.obs_bf16 + src * s.Dp);
@@ -74,9 +87,12 @@ gather_kernel(NetShape s, GatherArgs a, int per_row) {
   for (int h = 0; h < s.NH; ++h) act[h] = __ldg(a.act + src * s.NH + h);
   for (int g = 0; g < s.G; ++g) actc[g] = __ldg(a.actc + src * s.G + g);
   const float lp = __ldg(a.logp_old + src);
-  float A = __ldg(a.adv + src);
-  const float R = __ldg(a.ret + src);
-  if (a.adv_stats) A = (A - __ldg(a.adv_stats)) / (__ldg(a.adv_stats + 1) + 1e-8f);
+  float A = 0.f, R = 0.f;
+  if (a.adv) {   // no advantages when they are computed per minibatch later
+    A = __ldg(a.adv + src);
+    R = __ldg(a.ret + src);
+    if (a.adv_stats) A = (A - __ldg(a.adv_stats)) / (__ldg(a.adv_stats + 1) + 1e-8f);
+  }
   for (int h = 0; h < s.NH; ++h) {
     // an out-of-range action is clamped into its head so the loss never
     // indexes outside the head's logits
@@ -85,8 +101,10 @@ gather_kernel(NetShape s, GatherArgs a, int per_row) {
   }
   for (int g = 0; g < s.G; ++g) a.actc_mb[r * s.G + g] = actc[g];
   a.logp_mb[r] = lp;
-  a.adv_mb[r] = A;
-  a.ret_mb[r] = R;
+  if (a.adv) {
+    a.adv_mb[r] = A;
+    a.ret_mb[r] = R;
+  }
 }
 
 }  // namespace
