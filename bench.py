@@ -163,10 +163,18 @@ def _stage_work(stage: str, w, mb: int):
         "adam": 30 * P, "grad_sqnorm": 4 * P,
         "grad_reduce": 4 * P,
         "grad_reduce_adam": 34 * P,               # gradient write + norm + Adam + shadow
+        # per-minibatch advantages: read H2 once (bf16), values (+ ratios) written and
+        # re-read, rewards/dones read, advantages/returns written, normalised in place
+        "fresh_advantages": mb * (2 * H2 + 40),
     }
     if stage in hbm:
         return 0, hbm[stage]
     return None
+
+
+# --advantages: 0 GAE once per update over the rollout; 1 per minibatch of
+# environment segments from fresh values (GAE); 2 the same with V-trace
+ADV_MODES = {"global": 0, "fresh_gae": 1, "vtrace": 2}
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
@@ -227,7 +235,7 @@ def run_ours(args, world, rank, local):
     big = w.B * w.obs_dim > 2e8
     ro = synth.rollout(w, seed=rank, with_obs=not big)
     p0 = synth.init_params(w)
-    ctx = P.Context(P.config_from_workload(w), p0)
+    ctx = P.Context(P.config_from_workload(w, adv_mode=ADV_MODES[args.advantages]), p0)
     stream = torch.cuda.Stream()
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
     if big:
@@ -335,7 +343,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
-        cpu = _cpu_baseline(w)
+        cpu = _cpu_baseline(w, ADV_MODES[args.advantages])
 
     out = {
         "metric": "PPO update samples/s (GAE+clipped loss fwd/bwd+Adam); GAE GB/s vs HBM peak",
@@ -344,7 +352,7 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded mulberry32 rollout with the workload's shapes and value "
                 "distributions; random-init weights)",
-        "config": {"workload": _workload_str(w),
+        "config": {"workload": _workload_str(w, args.advantages),
                    "global_batch": world * B, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (256 MB write)",
                    "timing": "CUDA events per update on the launching stream, mean over steps"},
@@ -429,38 +437,44 @@ def _adam_stress(stream, hbm_peak):
 
 
 def _cpu_sample(w):
-    from policy_rl_gb300 import synth
-    return w.scaled(T=w.T, N=max(1, 8192 // w.T), minibatches=w.minibatches, epochs=w.epochs)
+    n = max(1, 8192 // w.T)
+    n = max(n - n % w.minibatches, w.minibatches)   # whole segments per minibatch
+    return w.scaled(T=w.T, N=n, minibatches=w.minibatches, epochs=w.epochs)
 
 
-def _oracle_update(ws, seed=0):
+def _oracle_update(ws, seed=0, adv_mode=0):
     import oracle
     from policy_rl_gb300 import synth
     ro = synth.rollout(ws, seed=seed)
     p0 = synth.init_params(ws).astype(np.float64)
     net = oracle.Net(ws.obs_dim, ws.h1, ws.h2, ws.act, ws.heads, ws.n_gauss)
     hp = oracle.Hyper(gamma=ws.gamma, lam=ws.lam, clip=ws.clip, vf_coef=ws.vf_coef,
-                      ent_coef=ws.ent_coef, lr=ws.lr, max_grad_norm=ws.max_grad_norm, seed=1234)
+                      ent_coef=ws.ent_coef, lr=ws.lr, max_grad_norm=ws.max_grad_norm, seed=1234,
+                      adv_mode=adv_mode)
     t0 = time.perf_counter()
     oracle.update(net, hp, ws.T, ws.N, ws.epochs, ws.minibatches, ro.obs, ro.act_disc,
                   ro.act_cont, ro.logp_old, ro.val, ro.rew, ro.done, ro.boot, p0)
     return time.perf_counter() - t0
 
 
-def _cpu_baseline(w):
+def _cpu_baseline(w, adv_mode=0):
     ws = _cpu_sample(w)
-    t = _oracle_update(ws)
+    t = _oracle_update(ws, adv_mode=adv_mode)
     return {"value": round(ws.B / t, 1), "unit": "samples/s", "cores": 1, "kind": "oracle",
             "sample": f"whole update of a T={ws.T} x N={ws.N} slice ({ws.B} samples) of the "
                       f"{w.name} workload, {ws.epochs} epochs x {ws.minibatches} minibatches; "
                       f"plain C fp64, single thread ({t:.2f} s)"}
 
 
-def _workload_str(w) -> str:
+def _workload_str(w, advantages="global") -> str:
     mb = w.B // w.minibatches
-    return (f"{w.name}: T={w.T} N={w.N} obs={w.obs_dim} MLP {w.obs_dim}-{w.h1}-{w.h2} "
-            f"{'tanh' if w.act == 0 else 'relu'} heads {list(w.heads)}+V epochs={w.epochs} "
-            f"minibatches={w.minibatches} mb={mb}")
+    s = (f"{w.name}: T={w.T} N={w.N} obs={w.obs_dim} MLP {w.obs_dim}-{w.h1}-{w.h2} "
+         f"{'tanh' if w.act == 0 else 'relu'} heads {list(w.heads)}+V epochs={w.epochs} "
+         f"minibatches={w.minibatches} mb={mb}")
+    if advantages != "global":
+        s += (f" advantages={advantages} (per minibatch of {w.N // w.minibatches} env segments, "
+              f"from fresh values)")
+    return s
 
 
 def run_reference(args, world, rank):
@@ -469,16 +483,17 @@ def run_reference(args, world, rank):
     run (warm-up + timed steps) takes about two minutes."""
     from policy_rl_gb300 import synth
     w = synth.WORKLOADS[args.workload]
-    probe = w.scaled(T=16, N=8, minibatches=w.minibatches, epochs=w.epochs)
-    per_sample = _oracle_update(probe) / probe.B
+    am = ADV_MODES[args.advantages]
+    n = max(8, w.minibatches)    # powers of two: whole env segments per minibatch
+    probe = w.scaled(T=16, N=n, minibatches=w.minibatches, epochs=w.epochs)
+    per_sample = _oracle_update(probe, adv_mode=am) / probe.B
     budget = 120.0 / (args.steps + args.warmup)
-    n = 8
     while n < 1024 and 16 * (2 * n) * per_sample <= budget:
         n *= 2
     ws = w.scaled(T=16, N=n, minibatches=w.minibatches, epochs=w.epochs)
     for i in range(args.warmup):
-        _oracle_update(ws, seed=i)
-    times = [_oracle_update(ws, seed=args.warmup + i) for i in range(args.steps)]
+        _oracle_update(ws, seed=i, adv_mode=am)
+    times = [_oracle_update(ws, seed=args.warmup + i, adv_mode=am) for i in range(args.steps)]
     t = float(np.mean(times))
     v = ws.B / t
     sample = (f"whole update of a T={ws.T} x N={ws.N} slice ({ws.B} samples) of the {w.name} "
@@ -490,7 +505,7 @@ def run_reference(args, world, rank):
         "value": round(v, 2), "unit": "samples/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": _workload_str(w), "global_batch": world * w.B,
+        "config": {"workload": _workload_str(w, args.advantages), "global_batch": world * w.B,
                    "parallelism": "host cores (rank 0)",
                    "sample": f"oracle on a {ws.B}-sample slice per step (T={ws.T} x N={ws.N})"},
         "cpu_baseline": {"value": round(v, 2), "unit": "samples/s", "cores": 1,
@@ -508,6 +523,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mario",
                     choices=["tiny", "mario", "ddnet", "large"])
+    ap.add_argument("--advantages", default="global", choices=sorted(ADV_MODES),
+                    help="global: GAE once per update (default); fresh_gae / vtrace: per "
+                         "minibatch of env segments from fresh values")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     ap.add_argument("--skip-gae-stress", action="store_true")
     ap.add_argument("--skip-adam-stress", action="store_true")

@@ -68,7 +68,7 @@ struct ppo_ctx {
   unsigned* rbar = nullptr; // grid-barrier counter of the reduce + Adam kernel
   // per-minibatch advantages from fresh values (adv_mode 1, 2)
   float *vfresh = nullptr, *rfresh = nullptr;   // [mbmax] fresh values / ratios
-  double* fpart = nullptr;                      // [kFreshMaxGrid][3] moment partials
+  float* fpart = nullptr;                       // [kFreshMaxGrid][3] moment partials
   unsigned* fbar = nullptr;                     // grid-barrier counter of that kernel
   void* X = nullptr;
   // one epoch of minibatch rows gathered in permutation order (ppo_update)
@@ -1097,7 +1097,7 @@ ppo_status ppo_minibatch_loss_grad_fresh(ppo_ctx* c, const float* obs, const int
 
 ppo_status ppo_segment_advantage_workspace_bytes(size_t* bytes) {
   if (!bytes) return PPO_ERR_INVALID;
-  *bytes = 16 + sizeof(double) * 3 * (size_t)kFreshMaxGrid;
+  *bytes = 16 + sizeof(float) * 3 * (size_t)kFreshMaxGrid;
   return PPO_OK;
 }
 
@@ -1142,7 +1142,7 @@ ppo_status ppo_segment_advantage(const float* rew, const float* done, const floa
   f.ret = ret;
   f.adv_norm = adv_norm;
   f.stats = stats;
-  f.part = reinterpret_cast<double*>(static_cast<uint8_t*>(work) + 16);
+  f.part = reinterpret_cast<float*>(static_cast<uint8_t*>(work) + 16);
   f.bar = bar;
   f.err = err;
   f.timeout_ns = kTimeoutNs;

@@ -303,7 +303,7 @@ struct FreshAdvArgs {
   float* ret;              // [rows] value targets
   float* adv_norm;         // [rows] normalised advantages (may equal adv), or nullptr
   float* stats;            // [2] {mean, unbiased std} of adv, or nullptr
-  double* part;            // [kFreshMaxGrid][3]
+  float* part;             // [kFreshMaxGrid][3] per-block (count, mean, M2)
   unsigned* bar;           // zero on entry; reset to zero by the launch
   int* err;
   uint64_t timeout_ns;

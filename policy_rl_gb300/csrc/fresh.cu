@@ -11,18 +11,23 @@
 // and GAE is the on-policy case (rho = 1, c = lambda).
 //
 // One cooperative launch, three phases separated by bounded grid barriers:
-//  A (optional) fresh values: one warp per row, V = w_V . h2 + b_V from the
-//    last hidden layer the forward pass just wrote (and, for V-trace, all
-//    head columns -> log-probability of the taken action -> the ratio);
+//  A (optional) fresh values: a quad of lanes per row computes the row's
+//    head outputs from the last hidden layer the forward pass just wrote,
+//    with the head weights staged in shared memory (fp32, [H2][NCOL], read
+//    as broadcasts, chunks skewed across banks).  GAE needs only the value column (NCOL = 1); V-trace needs
+//    every column to form the log-probability of the taken action and the
+//    ratio pi/mu = exp(logp - logp_old).
 //  B the segment scan: one warp per segment; the recursion is affine in
 //    A_{t+1} (A_t = b_t + a_t A_{t+1}), so each lane composes the maps of a
-//    run of K steps, a suffix scan over the lanes composes the runs, and each
-//    lane then replays its K steps from the exact incoming value.  Windows of
-//    32 K steps are chained from the end of the horizon.  Each lane keeps
-//    (n, mean, M2) of its advantages in fp64 (Welford; Chan merges upward);
-//  C every block merges all blocks' moments in the same fixed order, and the
-//    advantages are normalised in place: (A - mean) / (std + 1e-8), std the
-//    unbiased estimate.
+//    run of kRun steps, a suffix scan over the lanes composes the runs, and
+//    each lane then replays its steps from the exact incoming value.  Windows
+//    of 32 kRun steps are chained from the end of the horizon.
+//  C moments: each lane keeps shifted fp32 sums of its advantages, merged by
+//    Chan's formula up the warp and the block into per-block partials; after
+//    the barrier every block merges all partials in the same fixed order and
+//    normalises its share of the advantages: (A - mean) / (std + 1e-8), std
+//    the unbiased estimate.  (fp32 throughout: GB300's fp64 rate is a small
+//    fraction of its fp32 rate.)
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -34,41 +39,57 @@ constexpr int kFreshThreads = 256;
 constexpr int kFreshWarps = kFreshThreads / 32;
 constexpr int kRun = 4;   // steps per lane per window
 
-struct Mom {
-  double n, mean, m2;
+struct MomF {
+  float n, mean, m2;
 };
 
-__device__ __forceinline__ Mom mom_merge(Mom a, Mom b) {
-  if (a.n == 0.0) return b;
-  if (b.n == 0.0) return a;
-  const double n = a.n + b.n;
-  const double d = b.mean - a.mean;
-  Mom r;
+// Chan et al. pairwise merge of (count, mean, M2).
+__device__ __forceinline__ MomF mom_merge(MomF a, MomF b) {
+  if (a.n == 0.f) return b;
+  if (b.n == 0.f) return a;
+  const float n = a.n + b.n;
+  const float d = b.mean - a.mean;
+  const float fb = b.n / n;
+  MomF r;
   r.n = n;
-  r.mean = a.mean + d * (b.n / n);
-  r.m2 = a.m2 + b.m2 + d * d * (a.n * b.n / n);
+  r.mean = a.mean + d * fb;
+  r.m2 = a.m2 + b.m2 + d * d * a.n * fb;
   return r;
 }
 
-__device__ __forceinline__ Mom mom_shfl(Mom m, int o) {
-  Mom r;
+__device__ __forceinline__ MomF mom_shfl(MomF m, int o) {
+  MomF r;
   r.n = __shfl_xor_sync(0xffffffffu, m.n, o);
   r.mean = __shfl_xor_sync(0xffffffffu, m.mean, o);
   r.m2 = __shfl_xor_sync(0xffffffffu, m.m2, o);
   return r;
 }
 
-__device__ __forceinline__ Mom mom_warp(Mom m) {
+// Butterfly merge; lane 0's result is the one used (the merge is not
+// symmetric in rounding, so lanes may differ in the last bits).
+__device__ __forceinline__ MomF mom_warp(MomF m) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) m = mom_merge(m, mom_shfl(m, o));
   return m;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
+// Shifted sums of one lane: values x are accumulated as e = x - shift with
+// shift = the lane's first value, so that constant inputs give M2 = 0 exactly.
+struct LaneSums {
+  float n, shift, s1, s2;
+  __device__ __forceinline__ void add(float x) {
+    if (n == 0.f) shift = x;
+    const float e = x - shift;
+    n += 1.f;
+    s1 += e;
+    s2 += e * e;
+  }
+  __device__ __forceinline__ MomF moments() const {
+    if (n == 0.f) return MomF{0.f, 0.f, 0.f};
+    const float q = s1 / n;
+    return MomF{n, shift + q, fmaxf(s2 - s1 * q, 0.f)};
+  }
+};
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
@@ -105,113 +126,242 @@ __device__ bool grid_barrier(unsigned* bar, unsigned k, int* err, uint64_t limit
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-__device__ __forceinline__ float dot8(uint4 h, uint4 w) {
-  float s = bf_lo(h.x) * bf_lo(w.x);
-  s = fmaf(bf_hi(h.x), bf_hi(w.x), s);
-  s = fmaf(bf_lo(h.y), bf_lo(w.y), s);
-  s = fmaf(bf_hi(h.y), bf_hi(w.y), s);
-  s = fmaf(bf_lo(h.z), bf_lo(w.z), s);
-  s = fmaf(bf_hi(h.z), bf_hi(w.z), s);
-  s = fmaf(bf_lo(h.w), bf_lo(w.w), s);
-  s = fmaf(bf_hi(h.w), bf_hi(w.w), s);
-  return s;
+// Phase A splits every row over a quad of lanes: lane q of the quad reads the
+// row's 8-unit chunks q, q + 4, q + 8, ... (the quad reads 64 contiguous
+// bytes at a time) and the quad sums its partial head outputs with two
+// butterfly steps.
+constexpr int kSplit = 4;
+
+// Head weights staged in shared memory as fp32: unit k's NCOL columns start
+// at w3_off(k).  H2 is rounded up to whole chunks (zero padding).  With
+// several columns, 8-unit chunk b starts 16 b bytes later than packed, so
+// that the four lanes of a quad, which read the same unit of four
+// consecutive chunks, hit different banks.
+__host__ __device__ __forceinline__ int w3_rows(int H2) { return (H2 + 7) / 8 * 8; }
+template <int NCOL>
+__host__ __device__ __forceinline__ int w3_off(int k) {
+  return k * NCOL + (NCOL > 1 ? (k >> 3) * 4 : 0);
+}
+__host__ __device__ __forceinline__ int w3_floats(int ncol, int H2) {
+  return w3_rows(H2) * ncol + (ncol > 1 ? w3_rows(H2) / 2 : 0);
 }
 
-// This lane's share of the last hidden layer of a row, bf16 mode: the
-// 8-element chunks at lane*8 and lane*8 + 256 (hidden width <= 512).
-struct HRow {
-  uint4 h[2];
-};
-
-__device__ __forceinline__ HRow load_hrow(const FreshAdvArgs& a, int64_t row, int lane) {
-  const int H = a.s.H2;
-  const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(a.H2) + row * H;
-  HRow r;
-  const uint4 z{0u, 0u, 0u, 0u};
-  r.h[0] = lane * 8 < H ? *reinterpret_cast<const uint4*>(h + lane * 8) : z;
-  r.h[1] = lane * 8 + 256 < H ? *reinterpret_cast<const uint4*>(h + lane * 8 + 256) : z;
-  return r;
-}
-
-// Partial (over this lane's share of the hidden width) of output column c.
-__device__ __forceinline__ float col_partial(const FreshAdvArgs& a, const HRow& hr, int64_t row,
-                                             int c, int lane) {
-  const int H = a.s.H2;
-  if (a.h2_bf16) {
-    const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(a.W3) + (int64_t)c * H;
-    float acc = 0.f;
-    if (lane * 8 < H) acc = dot8(hr.h[0], __ldg(reinterpret_cast<const uint4*>(w + lane * 8)));
-    if (lane * 8 + 256 < H)
-      acc += dot8(hr.h[1], __ldg(reinterpret_cast<const uint4*>(w + lane * 8 + 256)));
-    return acc;
+// Phase A setup.  NCOL == 1 stages the value column only.  Work item i is
+// 8 consecutive hidden units of one column (one 16-byte load in bf16 mode);
+// the loads of up to 4 items per thread are issued before their stores.
+template <int NCOL>
+__device__ __forceinline__ void stage_w3(const FreshAdvArgs& a, float* w3t) {
+  const int H = a.s.H2, C = a.s.C, Hp = w3_rows(H);
+  const int chunks = Hp / 8, items = NCOL * chunks;
+  constexpr int kU = 4;
+  for (int i0 = threadIdx.x; i0 < items; i0 += kU * kFreshThreads) {
+    float w[kU][8];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * kFreshThreads;
+      const int c = i / chunks, k0 = (i - c * chunks) * 8;
+      const int col = NCOL == 1 ? C - 1 : c;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[u][j] = 0.f;
+      if (i < items && col < C) {
+        const int64_t o = (int64_t)col * H + k0;
+        if (a.h2_bf16) {   // H2 is a multiple of 128: whole chunks
+          const uint4 q = *reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(a.W3) + o);
+          w[u][0] = bf_lo(q.x); w[u][1] = bf_hi(q.x); w[u][2] = bf_lo(q.y); w[u][3] = bf_hi(q.y);
+          w[u][4] = bf_lo(q.z); w[u][5] = bf_hi(q.z); w[u][6] = bf_lo(q.w); w[u][7] = bf_hi(q.w);
+        } else {
+          const float* src = static_cast<const float*>(a.W3) + o;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w[u][j] = k0 + j < H ? src[j] : 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * kFreshThreads;
+      if (i < items) {
+        const int c = i / chunks, k0 = (i - c * chunks) * 8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w3t[w3_off<NCOL>(k0 + j) + c] = w[u][j];
+      }
+    }
   }
-  const float* h = static_cast<const float*>(a.H2) + row * H;
-  const float* w = static_cast<const float*>(a.W3) + (int64_t)c * H;
-  float acc = 0.f;
-  for (int k = lane; k < H; k += 32) acc = fmaf(h[k], __ldg(w + k), acc);
-  return acc;
+  __syncthreads();
 }
 
-// Phase A for one row: fresh value, and for V-trace the ratio of the taken
-// action's probability to the behaviour policy's.
-__device__ __forceinline__ void fresh_row(const FreshAdvArgs& a, int64_t row, int lane) {
+// z[c] += h * w3t[unit k][c].
+template <int NCOL>
+__device__ __forceinline__ void fma_unit(float h, const float* w3t, int k, float (&z)[NCOL]) {
+  const float* w = w3t + w3_off<NCOL>(k);
+  if constexpr (NCOL == 1) {
+    z[0] = fmaf(h, w[0], z[0]);
+  } else {
+#pragma unroll
+    for (int c4 = 0; c4 < NCOL; c4 += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(w + c4);
+      z[c4 + 0] = fmaf(h, q.x, z[c4 + 0]);
+      z[c4 + 1] = fmaf(h, q.y, z[c4 + 1]);
+      z[c4 + 2] = fmaf(h, q.z, z[c4 + 2]);
+      z[c4 + 3] = fmaf(h, q.w, z[c4 + 3]);
+    }
+  }
+}
+
+// Log-probability of the taken action from a row of head outputs z (thread
+// = row): log-softmax per discrete head by segmented running max / sum over
+// the compile-time-indexed columns, then the diagonal-Gaussian dimensions.
+template <int NCOL>
+__device__ __forceinline__ float row_logp(const FreshAdvArgs& a, int64_t row,
+                                          const float (&z)[NCOL]) {
   const NetShape& s = a.s;
-  const int C = s.C;
-  HRow hr;
-  if (a.h2_bf16) hr = load_hrow(a, row, lane);
-  if (a.ratio == nullptr) {
-    const float v = warp_sum(col_partial(a, hr, row, C - 1, lane)) + __ldg(a.b3 + C - 1);
-    if (lane == 0) a.val[row] = v;
-    return;
-  }
-  // lane c ends with column c (one butterfly sum per column keeps the
-  // register footprint small)
-  float z = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < C; ++c) {
-    const float col = warp_sum(col_partial(a, hr, row, c, lane));
-    if (lane == c) z = col;
-  }
-  if (lane < C) z += __ldg(a.b3 + lane);
-  // log-probability of the action: log-softmax per discrete head, then the
-  // diagonal-Gaussian dimensions
-  const float neg_inf = -__int_as_float(0x7f800000);
-  float contrib = 0.f;
+  uint32_t hs = 0u, he = 0u, hd = 0u, amask = 0u;
   int off = 0;
   for (int h = 0; h < s.NH; ++h) {
     const int n = s.head_n[h];
-    const bool in = lane >= off && lane < off + n;
-    const float m = warp_max(in ? z : neg_inf);
-    const float se = warp_sum(in ? expf(z - m) : 0.f);
     int act = __ldg(a.act + row * s.NH + h);
     act = act < 0 ? 0 : (act >= n ? n - 1 : act);
-    if (lane == off + act) contrib += z - (m + logf(se));
+    hs |= 1u << off;
+    he |= 1u << (off + n - 1);
+    hd |= ((1u << n) - 1u) << off;
+    amask |= 1u << (off + act);
     off += n;
   }
-  if (lane >= off && lane < off + s.G) {
-    const int g = lane - off;
-    const float ls = __ldg(a.logstd + g);
-    const float d = __ldg(a.actc + row * s.G + g) - z;
-    contrib += -d * d * 0.5f * expf(-2.f * ls) - ls - 0.91893853320467274f;   // ln(2 pi) / 2
+  float mx[NCOL], se[NCOL];
+  float run = 0.f;
+#pragma unroll
+  for (int k = 0; k < NCOL; ++k) {
+    run = ((hs >> k) & 1u) ? z[k] : fmaxf(run, z[k]);
+    mx[k] = run;
   }
-  const float logp = warp_sum(contrib);
-  const float v = __shfl_sync(0xffffffffu, z, C - 1);
-  if (lane == 0) {
+#pragma unroll
+  for (int k = NCOL - 2; k >= 0; --k)
+    if (!((he >> k) & 1u)) mx[k] = mx[k + 1];
+  float srun = 0.f;
+#pragma unroll
+  for (int k = 0; k < NCOL; ++k) {
+    const float e = ((hd >> k) & 1u) ? __expf(z[k] - mx[k]) : 0.f;
+    srun = ((hs >> k) & 1u) ? e : srun + e;
+    se[k] = srun;
+  }
+#pragma unroll
+  for (int k = NCOL - 1; k >= 0; --k) {
+    if ((he >> k) & 1u) mx[k] = mx[k] + __logf(se[k]);   // the head's log-sum-exp
+    else if (k + 1 < NCOL) mx[k] = mx[k + 1];
+  }
+  float logp = 0.f;
+#pragma unroll
+  for (int k = 0; k < NCOL; ++k)
+    if ((amask >> k) & 1u) logp += z[k] - mx[k];
+  for (int g = 0; g < s.G; ++g) {
+    float mu = 0.f;
+#pragma unroll
+    for (int k = 0; k < NCOL; ++k) mu = (k == off + g) ? z[k] : mu;
+    const float ls = __ldg(a.logstd + g);
+    const float d = __ldg(a.actc + row * s.G + g) - mu;
+    logp += -0.5f * d * d * __expf(-2.f * ls) - ls - 0.91893853320467274f;   // ln(2 pi) / 2
+  }
+  return logp;
+}
+
+// Phase A for one row, lane q of its quad (every lane of the warp calls this
+// together; `valid` is false past the last row).
+template <int NCOL>
+__device__ __forceinline__ void eval_row(const FreshAdvArgs& a, const float* w3t, int64_t row,
+                                         bool valid, int q) {
+  const int H = a.s.H2, C = a.s.C;
+  float z[NCOL];
+#pragma unroll
+  for (int c = 0; c < NCOL; ++c) z[c] = 0.f;
+  if (valid) {
+    if (a.h2_bf16) {   // H2 is a multiple of 128 in bf16 mode
+      const uint4* hp =
+          reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.H2) + row * H);
+      // up to kBatch chunks of the row in flight per lane before any arithmetic
+      constexpr int kBatch = 8;
+      for (int kb = 8 * q; kb < H; kb += 8 * kSplit * kBatch) {
+        uint4 u[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int k0 = kb + 8 * kSplit * i;
+          u[i] = k0 < H ? hp[k0 / 8] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int k0 = kb + 8 * kSplit * i;
+          if (k0 < H) {
+            const float h[8] = {bf_lo(u[i].x), bf_hi(u[i].x), bf_lo(u[i].y), bf_hi(u[i].y),
+                                bf_lo(u[i].z), bf_hi(u[i].z), bf_lo(u[i].w), bf_hi(u[i].w)};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) fma_unit<NCOL>(h[j], w3t, k0 + j, z);
+          }
+        }
+      }
+    } else {
+      const float* hp = static_cast<const float*>(a.H2) + row * H;
+      for (int k0 = 8 * q; k0 < H; k0 += 8 * kSplit) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)   // staged units below w3_rows(H) are zero past H
+          fma_unit<NCOL>(k0 + j < H ? hp[k0 + j] : 0.f, w3t, k0 + j, z);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < NCOL; ++c) {
+    z[c] += __shfl_xor_sync(0xffffffffu, z[c], 1);
+    z[c] += __shfl_xor_sync(0xffffffffu, z[c], 2);
+  }
+  if (!valid || q != 0) return;
+  if constexpr (NCOL == 1) {
+    a.val[row] = z[0] + __ldg(a.b3 + C - 1);
+  } else {
+    float v = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCOL; ++c) {
+      z[c] += c < C ? __ldg(a.b3 + c) : 0.f;
+      v = (c == C - 1) ? z[c] : v;
+    }
     a.val[row] = v;
-    a.ratio[row] = expf(logp - __ldg(a.logp_old + row));
+    a.ratio[row] = __expf(row_logp<NCOL>(a, row, z) - __ldg(a.logp_old + row));
   }
 }
 
-// Phase B for segment j: the scan over the horizon; returns this lane's
-// moments of the advantages it wrote.
-__device__ __forceinline__ Mom fresh_segment(const FreshAdvArgs& a, int j, int lane, Mom mom) {
+// The rollout inputs of a segment's last window (rewards, dones, bootstrap
+// value): they do not depend on phase A, so they are loaded before its barrier.
+struct SegPre {
+  int64_t e;
+  float boot;
+  float r[kRun], d[kRun];
+};
+
+__device__ __forceinline__ void seg_prefetch(const FreshAdvArgs& a, int64_t e, int lane,
+                                             SegPre& p) {
+  const int64_t N = a.N;
+  p.e = e < 0 ? 0 : (e >= N ? N - 1 : e);
+  p.boot = __ldg(a.boot + p.e);
+  const int t_lo = a.T - 32 * kRun > 0 ? a.T - 32 * kRun : 0;
+  const int start = t_lo + lane * kRun;
+#pragma unroll
+  for (int q = 0; q < kRun; ++q) {
+    p.r[q] = p.d[q] = 0.f;
+    if (start + q < a.T) {
+      const int64_t i = (int64_t)(start + q) * N + p.e;
+      p.r[q] = __ldg(a.rew + i);
+      p.d[q] = __ldg(a.done + i);
+    }
+  }
+}
+
+// Phase B for segment j: the scan over the horizon, accumulating this lane's
+// advantages into its sums.  pre: the segment's prefetched last window.
+__device__ __forceinline__ void fresh_segment(const FreshAdvArgs& a, int j, int lane,
+                                              const SegPre& pre, LaneSums& acc) {
   const int T = a.T, ns = a.ns;
   const int64_t N = a.N;
-  int e = __ldg(a.envs + j);
-  e = e < 0 ? 0 : (e >= N ? (int)(N - 1) : e);
+  const int64_t e = pre.e;
   const bool vtrace = a.ratio != nullptr;
-  float A_in = 0.f;            // advantage at t_hi
-  float v_in = __ldg(a.boot + e);   // value at t_hi
+  float A_in = 0.f;       // advantage at t_hi
+  float v_in = pre.boot;  // value at t_hi
   for (int t_hi = T; t_hi > 0; t_hi -= 32 * kRun) {
     const int t_lo = t_hi - 32 * kRun > 0 ? t_hi - 32 * kRun : 0;
     const int start = t_lo + lane * kRun;
@@ -220,21 +370,25 @@ __device__ __forceinline__ Mom fresh_segment(const FreshAdvArgs& a, int j, int l
     float r[kRun], d[kRun], v[kRun], rho[kRun];
 #pragma unroll
     for (int q = 0; q < kRun; ++q) {
-      r[q] = d[q] = v[q] = 0.f;
+      r[q] = pre.r[q];
+      d[q] = pre.d[q];
+      v[q] = 0.f;
       rho[q] = 1.f;
       if (q < cnt) {
-        const int t = start + q;
-        const int64_t i = (int64_t)t * N + e;
-        const int64_t k = (int64_t)t * ns + j;
-        r[q] = __ldg(a.rew + i);
-        d[q] = __ldg(a.done + i);
-        v[q] = a.val[k];          // written by phase A of this launch: plain load
+        const int64_t t = start + q;
+        const int64_t k = t * ns + j;
+        if (t_hi != T) {
+          r[q] = __ldg(a.rew + t * N + e);
+          d[q] = __ldg(a.done + t * N + e);
+        }
+        v[q] = a.val[k];          // may have been written by phase A: plain loads
         if (vtrace) rho[q] = a.ratio[k];
       }
     }
     // value after this lane's run: the next lane's first value, or v_in
     const float v_next_lane = __shfl_down_sync(0xffffffffu, v[0], 1);
-    const float v_after = (start + cnt == t_hi || lane == 31) ? v_in : v_next_lane;
+    const bool last_run = (start + cnt == t_hi) || lane == 31;
+    const float v_after = last_run ? v_in : v_next_lane;
     float bq[kRun], aq[kRun];
     float alpha = 1.f, beta = 0.f;
 #pragma unroll
@@ -266,9 +420,8 @@ __device__ __forceinline__ Mom fresh_segment(const FreshAdvArgs& a, int j, int l
         alpha = alpha * a2;
       }
     }
-    const float y = beta + alpha * A_in;
-    const float y_next = __shfl_down_sync(0xffffffffu, y, 1);
-    float A = (start + cnt == t_hi || lane == 31) ? A_in : y_next;
+    const float y_next = __shfl_down_sync(0xffffffffu, beta + alpha * A_in, 1);
+    float A = last_run ? A_in : y_next;
 #pragma unroll
     for (int q = kRun - 1; q >= 0; --q) {
       if (q < cnt) {
@@ -276,64 +429,88 @@ __device__ __forceinline__ Mom fresh_segment(const FreshAdvArgs& a, int j, int l
         const int64_t k = (int64_t)(start + q) * ns + j;
         a.adv[k] = A;
         a.ret[k] = A + v[q];
-        // Welford update of this lane's moments
-        mom.n += 1.0;
-        const double dx = (double)A - mom.mean;
-        mom.mean += dx / mom.n;
-        mom.m2 += dx * ((double)A - mom.mean);
+        acc.add(A);
       }
     }
     A_in = __shfl_sync(0xffffffffu, A, 0);
     v_in = __shfl_sync(0xffffffffu, v[0], 0);
   }
-  return mom;
 }
 
+template <int NCOL>
 __global__ void __launch_bounds__(kFreshThreads, 2)
 fresh_adv_kernel(FreshAdvArgs a) {
+  extern __shared__ float4 smem_dyn[];
+  float* w3t = reinterpret_cast<float*>(smem_dyn);
   __shared__ int s_abort;
-  __shared__ Mom s_mom[kFreshWarps];
+  __shared__ MomF s_mom[kFreshWarps];
   __shared__ float s_stats[2];
   pdl_wait();
   if (threadIdx.x == 0) s_abort = 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int gwarp = blockIdx.x * kFreshWarps + warp;
-  const int nwarps = gridDim.x * kFreshWarps;
   const int64_t rows = (int64_t)a.T * a.ns;
   unsigned k = 0;
+  const int nwarps = gridDim.x * kFreshWarps;
+  const int j0 = blockIdx.x * kFreshWarps + warp;
+  // the first segment's rollout inputs: its environment index now, the rest
+  // after phase A, so that their latency hides behind phase A and the barrier
+  const int64_t e0 = j0 < a.ns ? (int64_t)__ldg(a.envs + j0) : 0;
+  SegPre pre;
   if (a.head) {
-    for (int64_t row = gwarp; row < rows; row += nwarps) fresh_row(a, row, lane);
+    stage_w3<NCOL>(a, w3t);
+    // warp-uniform loop (the quads shuffle): t0 = the warp's first thread
+    const int64_t stride = (int64_t)gridDim.x * kFreshThreads;
+    for (int64_t t0 = (int64_t)blockIdx.x * kFreshThreads + warp * 32; t0 / kSplit < rows;
+         t0 += stride) {
+      const int64_t row = (t0 + lane) / kSplit;
+      eval_row<NCOL>(a, w3t, row, row < rows, lane & (kSplit - 1));
+    }
+    if (j0 < a.ns) seg_prefetch(a, e0, lane, pre);
     if (!grid_barrier(a.bar, ++k, a.err, a.timeout_ns, &s_abort)) return;
+  } else if (j0 < a.ns) {
+    seg_prefetch(a, e0, lane, pre);
   }
-  Mom mom{0.0, 0.0, 0.0};
-  for (int j = gwarp; j < a.ns; j += nwarps) mom = fresh_segment(a, j, lane, mom);
-  mom = mom_warp(mom);
-  if (lane == 0) s_mom[warp] = mom;
+  LaneSums acc{0.f, 0.f, 0.f, 0.f};
+  for (int j = j0; j < a.ns; j += nwarps) {
+    if (j != j0) seg_prefetch(a, __ldg(a.envs + j), lane, pre);
+    fresh_segment(a, j, lane, pre, acc);
+  }
+  const MomF wm = mom_warp(acc.moments());
+  if (lane == 0) s_mom[warp] = wm;
   __syncthreads();
   if (threadIdx.x == 0) {
-    Mom b = s_mom[0];
+    MomF b = s_mom[0];
     for (int w = 1; w < kFreshWarps; ++w) b = mom_merge(b, s_mom[w]);
-    a.part[3 * blockIdx.x + 0] = b.n;
-    a.part[3 * blockIdx.x + 1] = b.mean;
-    a.part[3 * blockIdx.x + 2] = b.m2;
+    float* part = a.part + 3 * blockIdx.x;
+    part[0] = b.n;
+    part[1] = b.mean;
+    part[2] = b.m2;
   }
   if (!grid_barrier(a.bar, ++k, a.err, a.timeout_ns, &s_abort)) return;
   if (warp == 0) {
     // the same fixed merge order in every block: lane l takes blocks
-    // l, l + 32, ... in turn, then the xor tree
-    Mom m{0.0, 0.0, 0.0};
-    for (int b = lane; b < (int)gridDim.x; b += 32) {
-      const Mom p{a.part[3 * b], a.part[3 * b + 1], a.part[3 * b + 2]};
-      m = mom_merge(m, p);
+    // l, l + 32, ... in turn, then the butterfly
+    const float* part = a.part;
+    MomF m{0.f, 0.f, 0.f};
+    for (int b0 = lane; b0 < (int)gridDim.x; b0 += 32 * 8) {
+      MomF p[8];   // every load of the batch in flight before the merges
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int b = b0 + 32 * u;
+        p[u] = b < (int)gridDim.x ? MomF{part[3 * b], part[3 * b + 1], part[3 * b + 2]}
+                                  : MomF{0.f, 0.f, 0.f};
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m = mom_merge(m, p[u]);
     }
     m = mom_warp(m);
     if (lane == 0) {
-      const double sd = m.n > 1.0 ? sqrt(m.m2 / (m.n - 1.0)) : 0.0;
-      s_stats[0] = (float)m.mean;
-      s_stats[1] = (float)sd;
+      const float sd = m.n > 1.f ? sqrtf(m.m2 / (m.n - 1.f)) : 0.f;
+      s_stats[0] = m.mean;
+      s_stats[1] = sd;
       if (blockIdx.x == 0 && a.stats) {
-        a.stats[0] = (float)m.mean;
-        a.stats[1] = (float)sd;
+        a.stats[0] = m.mean;
+        a.stats[1] = sd;
       }
     }
   }
@@ -352,39 +529,58 @@ fresh_adv_kernel(FreshAdvArgs a) {
   }
 }
 
-int g_fresh_blocks_per_sm = 0;
+// Variants by the number of head columns phase A computes, their shared
+// memory at the largest hidden width (512) and resident blocks per SM.
+constexpr int kVariants = 3;
+constexpr int kVarCols[kVariants] = {1, 16, 32};
+int g_blocks_per_sm[kVariants] = {0, 0, 0};
+
+size_t smem_bytes(int ncol, int H2) { return (size_t)w3_floats(ncol, H2) * sizeof(float); }
+
+template <int NCOL>
+cudaError_t prepare_one(int v) {
+  const size_t smem = smem_bytes(NCOL, 512);
+  cudaError_t e = cudaFuncSetAttribute(fresh_adv_kernel<NCOL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fresh_adv_kernel<NCOL>, kFreshThreads,
+                                                    smem);
+  if (e != cudaSuccess) return e;
+  g_blocks_per_sm[v] = n < 1 ? 1 : n;
+  return cudaSuccess;
+}
 
 }  // namespace
 
 cudaError_t fresh_prepare() {
-  if (g_fresh_blocks_per_sm > 0) return cudaSuccess;
-  int n = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fresh_adv_kernel,
-                                                                kFreshThreads, 0);
-  if (e != cudaSuccess) return e;
-  g_fresh_blocks_per_sm = n < 1 ? 1 : n;
-  return cudaSuccess;
-}
-
-int fresh_grid(int64_t rows, int ns, int head, int num_sms) {
-  const int bps = g_fresh_blocks_per_sm < 4 ? g_fresh_blocks_per_sm : 4;
-  int64_t cap = (int64_t)num_sms * (bps > 0 ? bps : 1);
-  if (cap > kFreshMaxGrid) cap = kFreshMaxGrid;
-  int64_t want = (ns + kFreshWarps - 1) / kFreshWarps;
-  const int64_t per_rows = head ? (rows + 4 * kFreshWarps - 1) / (4 * kFreshWarps)
-                                : (rows + 8 * kFreshThreads - 1) / (8 * kFreshThreads);
-  if (per_rows > want) want = per_rows;
-  if (want > cap) want = cap;
-  return want < 1 ? 1 : (int)want;
+  if (g_blocks_per_sm[0] > 0) return cudaSuccess;
+  cudaError_t e = prepare_one<1>(0);
+  if (e == cudaSuccess) e = prepare_one<16>(1);
+  if (e == cudaSuccess) e = prepare_one<32>(2);
+  return e;
 }
 
 cudaError_t launch_fresh_adv(const FreshAdvArgs& a, int num_sms, cudaStream_t st) {
-  if (g_fresh_blocks_per_sm <= 0) return cudaErrorInitializationError;
-  const int grid = fresh_grid((int64_t)a.T * a.ns, a.ns, a.head, num_sms);
+  if (g_blocks_per_sm[0] <= 0) return cudaErrorInitializationError;
+  // GAE needs the value column only; V-trace every head column
+  const int v = (!a.head || a.ratio == nullptr) ? 0 : (a.s.C <= 16 ? 1 : 2);
+  if (a.head && a.s.H2 > 512) return cudaErrorInvalidValue;
+  const int bps = g_blocks_per_sm[v] < 4 ? g_blocks_per_sm[v] : 4;
+  int64_t cap = (int64_t)num_sms * bps;
+  if (cap > kFreshMaxGrid) cap = kFreshMaxGrid;
+  const int64_t rows = (int64_t)a.T * a.ns;
+  // enough blocks for one row per thread in phase A (or for the normalisation)
+  // and one warp per segment in phase B
+  int64_t want = (a.ns + kFreshWarps - 1) / kFreshWarps;
+  const int64_t per_rows = a.head ? (rows * kSplit + kFreshThreads - 1) / kFreshThreads
+                                  : (rows + 8 * kFreshThreads - 1) / (8 * kFreshThreads);
+  if (per_rows > want) want = per_rows;
+  const int grid = (int)(want > cap ? cap : (want < 1 ? 1 : want));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kFreshThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = a.head ? smem_bytes(kVarCols[v], a.s.H2) : 0;
   cfg.stream = st;
   // cooperative: all blocks are resident and meet at the grid barriers
   cudaLaunchAttribute attr[1];
@@ -392,7 +588,11 @@ cudaError_t launch_fresh_adv(const FreshAdvArgs& a, int num_sms, cudaStream_t st
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fresh_adv_kernel, a);
+  switch (v) {
+    case 0: return cudaLaunchKernelEx(&cfg, fresh_adv_kernel<1>, a);
+    case 1: return cudaLaunchKernelEx(&cfg, fresh_adv_kernel<16>, a);
+    default: return cudaLaunchKernelEx(&cfg, fresh_adv_kernel<32>, a);
+  }
 }
 
 }  // namespace ppo
