@@ -11,7 +11,7 @@
 // and GAE is the on-policy case (rho = 1, c = lambda).
 //
 // One cooperative launch, three phases separated by bounded grid barriers:
-//  A (optional) fresh values: a quad of lanes per row computes the row's
+//  A (optional) fresh values: one thread per row computes the row's
 //    head outputs from the last hidden layer the forward pass just wrote,
 //    with the head weights staged in shared memory (fp32, [H2][NCOL], read
 //    as broadcasts, chunks skewed across banks).  GAE needs only the value column (NCOL = 1); V-trace needs
@@ -126,16 +126,18 @@ __device__ bool grid_barrier(unsigned* bar, unsigned k, int* err, uint64_t limit
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-// Phase A splits every row over a quad of lanes: lane q of the quad reads the
-// row's 8-unit chunks q, q + 4, q + 8, ... (the quad reads 64 contiguous
-// bytes at a time) and the quad sums its partial head outputs with two
-// butterfly steps.
-constexpr int kSplit = 4;
+// Phase A gives each row kSplit consecutive lanes: lane q reads the row's
+// 8-unit chunks q, q + kSplit, ... and the lanes sum their partial head
+// outputs by butterfly.  One lane per row measured fastest (Mario-like
+// minibatch: 22.5 us per launch against 22.8 with 2 lanes and 26.6 with 4;
+// more lanes per row mean more blocks, and the grid barriers and the final
+// merge grow with the block count).
+constexpr int kSplit = 1;
 
 // Head weights staged in shared memory as fp32: unit k's NCOL columns start
 // at w3_off(k).  H2 is rounded up to whole chunks (zero padding).  With
 // several columns, 8-unit chunk b starts 16 b bytes later than packed, so
-// that the four lanes of a quad, which read the same unit of four
+// that lanes of one row (kSplit > 1), which read the same unit of
 // consecutive chunks, hit different banks.
 __host__ __device__ __forceinline__ int w3_rows(int H2) { return (H2 + 7) / 8 * 8; }
 template <int NCOL>
@@ -264,8 +266,8 @@ __device__ __forceinline__ float row_logp(const FreshAdvArgs& a, int64_t row,
   return logp;
 }
 
-// Phase A for one row, lane q of its quad (every lane of the warp calls this
-// together; `valid` is false past the last row).
+// Phase A for one row, lane q of its kSplit lanes (every lane of the warp
+// calls this together; `valid` is false past the last row).
 template <int NCOL>
 __device__ __forceinline__ void eval_row(const FreshAdvArgs& a, const float* w3t, int64_t row,
                                          bool valid, int q) {
@@ -307,10 +309,9 @@ __device__ __forceinline__ void eval_row(const FreshAdvArgs& a, const float* w3t
     }
   }
 #pragma unroll
-  for (int c = 0; c < NCOL; ++c) {
-    z[c] += __shfl_xor_sync(0xffffffffu, z[c], 1);
-    z[c] += __shfl_xor_sync(0xffffffffu, z[c], 2);
-  }
+  for (int c = 0; c < NCOL; ++c)
+#pragma unroll
+    for (int o = 1; o < kSplit; o <<= 1) z[c] += __shfl_xor_sync(0xffffffffu, z[c], o);
   if (!valid || q != 0) return;
   if constexpr (NCOL == 1) {
     a.val[row] = z[0] + __ldg(a.b3 + C - 1);
@@ -458,7 +459,7 @@ fresh_adv_kernel(FreshAdvArgs a) {
   SegPre pre;
   if (a.head) {
     stage_w3<NCOL>(a, w3t);
-    // warp-uniform loop (the quads shuffle): t0 = the warp's first thread
+    // warp-uniform loop (the lanes of a row shuffle): t0 = the warp's first thread
     const int64_t stride = (int64_t)gridDim.x * kFreshThreads;
     for (int64_t t0 = (int64_t)blockIdx.x * kFreshThreads + warp * 32; t0 / kSplit < rows;
          t0 += stride) {
