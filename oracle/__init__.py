@@ -99,6 +99,16 @@ def lib():
                                           _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P,
                                           ctypes.c_int, _D, _D, _D, _D, _P, _P, _P, _P, _P]
         L.orc_loss_grad_fresh.restype = _D
+        L.orc_uniform24.argtypes = [ctypes.c_uint32]
+        L.orc_uniform24.restype = _D
+        L.orc_mulberry32_at.argtypes = [ctypes.c_uint32, ctypes.c_uint64]
+        L.orc_mulberry32_at.restype = ctypes.c_uint32
+        L.orc_sample_categorical.argtypes = [_P, ctypes.c_int, _D]
+        L.orc_sample_categorical.restype = ctypes.c_int
+        L.orc_box_muller.argtypes = [_D, _D]
+        L.orc_box_muller.restype = _D
+        L.orc_policy_act.argtypes = [ctypes.POINTER(_Net), ctypes.c_int, _P, _I64, _P, ctypes.c_uint32,
+                                     ctypes.c_uint64, _P, _P, _P, _P]
         L.orc_update.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_Hyper), _I64, _I64, _I64, _I64,
                                  _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                  ctypes.POINTER(_I64), _P, _P, _P]
@@ -248,6 +258,41 @@ def loss_grad_fresh(net: Net, params, T, N, envs, obs, act_disc, act_cont, logp_
         _ptr(_as(boot, np.float32)), int(bool(vtrace)), gamma, lam, rho_clip, c_clip,
         _ptr(grad), _ptr(st), _ptr(sc), _ptr(an), _ptr(rt))
     return loss, grad, st, sc, an, rt
+
+
+def uniform24(x: int) -> float:
+    return lib().orc_uniform24(int(x) & 0xFFFFFFFF)
+
+
+def mulberry32_at(seed: int, draw: int) -> int:
+    """Draw number ``draw`` (0-based) of the mulberry32 stream seeded with ``seed``."""
+    return lib().orc_mulberry32_at(seed & 0xFFFFFFFF, int(draw))
+
+
+def sample_categorical(z, u: float) -> int:
+    z = _as(z, np.float64)
+    return lib().orc_sample_categorical(_ptr(z), z.size, float(u))
+
+
+def box_muller(u1: float, u2: float) -> float:
+    return lib().orc_box_muller(float(u1), float(u2))
+
+
+def policy_act(net: Net, params, obs, seed: int, draw0: int = 0, bf16_operands=False):
+    """Sampled (act_disc [n][NH] int32, act_cont [n][G], logp [n], value [n])."""
+    params = _as(params, np.float64)
+    obs = _as(obs, np.float32).reshape(-1, net.obs_dim)
+    n = obs.shape[0]
+    NH, G = len(net.heads), net.n_gauss
+    act = np.empty((n, max(NH, 1)), np.int32)
+    actc = np.empty((n, max(G, 1)), np.float64)
+    logp = np.empty(n, np.float64)
+    val = np.empty(n, np.float64)
+    cn = net.c()
+    lib().orc_policy_act(ctypes.byref(cn), int(bool(bf16_operands)), _ptr(params), n, _ptr(obs),
+                         seed & 0xFFFFFFFF, int(draw0), _ptr(act), _ptr(actc), _ptr(logp),
+                         _ptr(val))
+    return act[:, :NH], actc[:, :G], logp, val
 
 
 def moments(x):

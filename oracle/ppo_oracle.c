@@ -541,6 +541,88 @@ double orc_loss_grad_fresh(const orc_net *net, const orc_loss_cfg *cfg, const do
 }
 
 /* ------------------------------------------------------------------------ */
+/* Rollout side: "Teaching Mario to speedrun", sec. 6 "The whole algorithm",
+ * step 1, and sec. 7 (the trainer's side of a horizon): for every agent,
+ * logits and value from the policy, an action sampled from the logits, and
+ * its probability kept as old_prob.  The pages do not define sample(); the
+ * plainest reading is used: per discrete head, inverse-CDF sampling of the
+ * softmax with one uniform u (the first category whose cumulative
+ * probability exceeds u); per Gaussian dimension, mu + e^s n with n from the
+ * Box-Muller transform of two uniforms.  Uniforms come from mulberry32
+ * ("PlayTrain", Appendix F.2) used as a counter: for agent i, slot k (head h
+ * is slot h, Gaussian dim g uses slots NH + 2g and NH + 2g + 1, K = NH + 2G
+ * slots per agent) the draw number is draw0 + i K + k of the stream seeded
+ * with `seed`, and u = (draw >> 8) / 2^24, a 24-bit uniform in [0, 1). */
+double orc_uniform24(uint32_t x) { return (double)(x >> 8) / 16777216.0; }
+
+uint32_t orc_mulberry32_at(uint32_t seed, uint64_t draw)
+{
+    uint32_t state = seed + (uint32_t)draw * 0x6D2B79F5u;   /* skip `draw` draws */
+    return orc_mulberry32_next(&state);
+}
+
+/* Inverse CDF of softmax(z[0..n)): the smallest k with u < sum_{i<=k} p_i,
+ * compared as u * sum_i e^{z_i - max} < sum_{i<=k} e^{z_i - max}; n - 1 if
+ * rounding leaves no such k. */
+int orc_sample_categorical(const double *z, int n, double u)
+{
+    double zmax = z[0];
+    for (int k = 1; k < n; ++k) if (z[k] > zmax) zmax = z[k];
+    double total = 0.0;
+    for (int k = 0; k < n; ++k) total += exp(z[k] - zmax);
+    double cum = 0.0;
+    for (int k = 0; k < n; ++k) {
+        cum += exp(z[k] - zmax);
+        if (u * total < cum) return k;
+    }
+    return n - 1;
+}
+
+/* Box-Muller: n = sqrt(-2 ln(1 - u1)) cos(2 pi u2) (1 - u1 lies in (0, 1]). */
+double orc_box_muller(double u1, double u2)
+{
+    return sqrt(-2.0 * log(1.0 - u1)) * cos(2.0 * acos(-1.0) * u2);
+}
+
+void orc_policy_act(const orc_net *net, int bf16, const double *params, int64_t n,
+                    const float *obs, uint32_t seed, uint64_t draw0, int32_t *act,
+                    double *actc, double *logp, double *value)
+{
+    const int64_t H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
+    const int64_t NH = net->n_heads, G = net->n_gauss, K = NH + 2 * G;
+    double *wr = orc_gemm_weights(net, params, bf16);
+    orc_views w = orc_split(net, bf16 ? wr : params);
+    double *buf = (double *)malloc(sizeof(double) * (size_t)(2 * H1 + 2 * H2 + 2 * C));
+    double *pre1 = buf, *h1 = pre1 + H1, *pre2 = h1 + H1, *h2 = pre2 + H2, *z = h2 + H2;
+    double *logprob = z + C;
+    double head_ent[8];
+    float actc_f[4];
+    for (int64_t i = 0; i < n; ++i) {
+        orc_forward_full(net, &w, obs + i * net->obs_dim, pre1, h1, pre2, h2, z, bf16);
+        const uint64_t d0 = draw0 + (uint64_t)i * (uint64_t)K;
+        int64_t off = 0;
+        for (int64_t h = 0; h < NH; ++h) {
+            const double u = orc_uniform24(orc_mulberry32_at(seed, d0 + (uint64_t)h));
+            act[i * NH + h] = orc_sample_categorical(z + off, net->head_n[h], u);
+            off += net->head_n[h];
+        }
+        for (int64_t g = 0; g < G; ++g) {
+            const double u1 = orc_uniform24(orc_mulberry32_at(seed, d0 + (uint64_t)(NH + 2 * g)));
+            const double u2 = orc_uniform24(orc_mulberry32_at(seed, d0 + (uint64_t)(NH + 2 * g + 1)));
+            const double a = z[off + g] + exp(w.logstd[g]) * orc_box_muller(u1, u2);
+            actc[i * G + g] = a;
+            actc_f[g] = (float)a;
+        }
+        /* the kept log-probability: of the action as stored (fp32) */
+        double ent;
+        orc_row_policy(net, w.logstd, z, act + i * NH, actc_f, logprob, head_ent, &logp[i], &ent);
+        value[i] = z[C - 1];
+    }
+    free(buf);
+    free(wr);
+}
+
+/* ------------------------------------------------------------------------ */
 /* "PlayTrain", Table 8 (PPO column): gradient-norm clip 0.5.  The global L2
  * norm over all parameters; if above max_norm, scale by max_norm/(norm+1e-6). */
 double orc_clip_grad_norm(int64_t P, double *g, double max_norm)

@@ -135,6 +135,18 @@ double orc_loss_grad_fresh(const orc_net *net, const orc_loss_cfg *cfg, const do
                            double rho_clip, double c_clip, double *grad, double *stats6,
                            double *scale6, double *adv_norm_out, double *ret_out);
 
+/* Rollout-side policy step (sample actions for n agents at params): see
+ * ppo_oracle.c.  act [n][n_heads] int32, actc [n][n_gauss], logp [n] (of the
+ * sampled action, Gaussian part at the fp32-rounded action), value [n].
+ * bf16: operand rounding as in orc_loss_cfg. */
+double orc_uniform24(uint32_t x);
+uint32_t orc_mulberry32_at(uint32_t seed, uint64_t draw);
+int orc_sample_categorical(const double *z, int n, double u);
+double orc_box_muller(double u1, double u2);
+void orc_policy_act(const orc_net *net, int bf16, const double *params, int64_t n,
+                    const float *obs, uint32_t seed, uint64_t draw0, int32_t *act,
+                    double *actc, double *logp, double *value);
+
 /* L2 norm of g; if max_norm > 0, g *= min(1, max_norm/(norm + 1e-6)).
  * Returns the norm before clipping. */
 double orc_clip_grad_norm(int64_t P, double *g, double max_norm);
