@@ -274,6 +274,32 @@ ppo_status ppo_minibatch_loss_grad_fresh(ppo_ctx *ctx, const float *d_obs,
                                          float *d_stats6, float *d_adv_out, float *d_ret_out,
                                          cudaStream_t stream);
 
+/* ---- Rollout-side policy step -------------------------------------------------
+ * "Teaching Mario to speedrun", sec. 6 "The whole algorithm", step 1, and
+ * sec. 7 (the trainer's side of a horizon): for the N agents of one
+ * environment step, logits and value from the context's current policy, an
+ * action sampled from the logits, and the log-probability of that action
+ * (the learner's logp_old).  The forward pass is the learner's (bf16 tensor
+ * cores in bf16 mode).  Sampling (the pages leave it open; the plainest
+ * reading): per discrete head, the first category whose cumulative softmax
+ * probability exceeds a uniform u; per Gaussian dimension
+ * mu + exp(logstd) sqrt(-2 ln(1 - u1)) cos(2 pi u2).  The uniforms are
+ * u = (x >> 8) / 2^24 for x = draw number draw0 + i*K + k of the mulberry32
+ * stream seeded with `seed` ("PlayTrain", Appendix F.2), agent i, slot k
+ * (head h: slot h; Gaussian dim g: slots n_heads + 2g and n_heads + 2g + 1),
+ * K = n_heads + 2 n_gauss; a horizon advances draw0 by N*K per step.
+ * Inputs  d_obs fp32 [N][obs_dim].
+ * Outputs d_act_disc int32 [N][n_heads]; d_act_cont fp32 [N][n_gauss] (may
+ *         be NULL if n_gauss == 0); d_logp fp32 [N] (nullable) the
+ *         log-probability of the stored action; d_value fp32 [N] (nullable).
+ * 1 <= N <= max_minibatch (the minibatch workspace holds the activations, so
+ * calls on one context are ordered by its stream); h2 <= 512
+ * (PPO_ERR_UNSUPPORTED otherwise).  Deterministic: a function of the
+ * parameters, the observations, seed and draw0. */
+ppo_status ppo_policy_act(ppo_ctx *ctx, const float *d_obs, int64_t N, uint32_t seed,
+                          uint64_t draw0, int32_t *d_act_disc, float *d_act_cont, float *d_logp,
+                          float *d_value, cudaStream_t stream);
+
 /* ---- Optimizer step ---------------------------------------------------------
  * "PlayTrain", Table 8 (PPO column): Adam with gradient-norm clip.
  * Scales the context gradient by min(1, max_grad_norm/(||g||_2 + 1e-6)) when
@@ -317,8 +343,8 @@ ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_ac
  * phases inside the persistent minibatch kernel (time between the phase
  * starts seen by its first CTA, summed over minibatches); they are not
  * separate launches. */
-#define PPO_NUM_KERNEL_STAGES 23
-#define PPO_NUM_STAGES 32
+#define PPO_NUM_KERNEL_STAGES 24
+#define PPO_NUM_STAGES 33
 /* Name of a stage (static string; "unknown" outside [0, PPO_NUM_STAGES)). */
 const char *ppo_stage_name(int32_t stage);
 

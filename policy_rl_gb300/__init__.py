@@ -18,7 +18,7 @@ __all__ = [
     "PpoConfig", "PpoError", "Context", "make_config", "ppo_param_count", "ppo_gae",
     "ppo_gae_workspace_bytes", "ppo_gae_noalloc", "ppo_minibatch_perm", "ppo_perm_workspace_bytes",
     "ppo_segment_advantage", "ppo_segment_advantage_workspace_bytes",
-    "ppo_minibatch_loss_grad_fresh",
+    "ppo_minibatch_loss_grad_fresh", "ppo_policy_act",
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
     "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "library_path",
@@ -202,6 +202,14 @@ def ppo_minibatch_loss_grad_fresh(ctx, obs, act_disc, act_cont, logp_old, rew, d
         _ptr(adv_out), _ptr(ret_out), _stream(stream)), "ppo_minibatch_loss_grad_fresh")
 
 
+def ppo_policy_act(ctx, obs, seed, draw0, act_disc, act_cont=None, logp=None, value=None,
+                   stream=None) -> None:
+    """Sampled actions, their log-probability and the value for the rows of obs."""
+    _abi.check(_lib().ppo_policy_act(
+        ctx, _ptr(obs), obs.shape[0], seed & 0xFFFFFFFF, int(draw0), _ptr(act_disc),
+        _ptr(act_cont), _ptr(logp), _ptr(value), _stream(stream)), "ppo_policy_act")
+
+
 def ppo_adam_step(ctx, lr, grad_norm=None, stream=None) -> None:
     _abi.check(_lib().ppo_adam_step(ctx, lr, _ptr(grad_norm), _stream(stream)), "ppo_adam_step")
 
@@ -270,6 +278,9 @@ class Context:
 
     def minibatch_loss_grad_fresh(self, *a, **k):
         return ppo_minibatch_loss_grad_fresh(self.handle, *a, **k)
+
+    def policy_act(self, *a, **k):
+        return ppo_policy_act(self.handle, *a, **k)
 
     def adam_step(self, *a, **k):
         return ppo_adam_step(self.handle, *a, **k)

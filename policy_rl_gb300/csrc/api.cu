@@ -955,6 +955,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   if (c->use_hl2 && hl2_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (reduce_adam_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (fresh_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
+  if (policy_act_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (c->use_mk && mk_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
   if (h_init_params) {
     if (cudaMemcpy(c->params, h_init_params, sizeof(float) * P, cudaMemcpyHostToDevice) !=
@@ -1074,6 +1075,7 @@ ppo_status ppo_minibatch_loss_grad_fresh(ppo_ctx* c, const float* obs, const int
   if (c->s.NH > 0 && !act) return PPO_ERR_INVALID;
   if (c->s.G > 0 && !actc) return PPO_ERR_INVALID;
   if (adv_mode != 1 && adv_mode != 2) return PPO_ERR_INVALID;
+  if (c->s.H2 > 512) return PPO_ERR_UNSUPPORTED;
   if (T < 1 || N < 1 || ns < 1 || T * N >= (1ll << 31) || T * ns > c->mbmax)
     return PPO_ERR_INVALID;
   const void* ps[] = {obs, act, actc, logp_old, rew, done, boot, envs, stats6, adv_out, ret_out};
@@ -1092,6 +1094,59 @@ ppo_status ppo_minibatch_loss_grad_fresh(ppo_ctx* c, const float* obs, const int
     PPO_CUDA(cudaMemcpyAsync(adv_out, c->adv_mb, sizeof(float) * mb, cudaMemcpyDeviceToDevice, st));
   if (ret_out)
     PPO_CUDA(cudaMemcpyAsync(ret_out, c->ret_mb, sizeof(float) * mb, cudaMemcpyDeviceToDevice, st));
+  return PPO_OK;
+}
+
+ppo_status ppo_policy_act(ppo_ctx* c, const float* obs, int64_t N, uint32_t seed, uint64_t draw0,
+                          int32_t* act, float* actc, float* logp, float* value, cudaStream_t st) {
+  if (!c || !obs) return PPO_ERR_INVALID;
+  const NetShape& s = c->s;
+  if ((s.NH > 0 && !act) || (s.G > 0 && !actc)) return PPO_ERR_INVALID;
+  if (N < 1 || N > c->mbmax) return PPO_ERR_INVALID;
+  if (s.H2 > 512) return PPO_ERR_UNSUPPORTED;
+  const void* ps[] = {obs, act, actc, logp, value};
+  for (const void* p : ps)
+    if (p && !al16(p)) return PPO_ERR_ALIGN;
+  const float* P = c->params;
+  const int M = (int)N;
+  if (c->bf16) {
+    auto* X = static_cast<__nv_bfloat16*>(c->X);
+    auto* H1 = static_cast<__nv_bfloat16*>(c->H1);
+    auto* H2 = static_cast<__nv_bfloat16*>(c->H2);
+    PPO_CUDA(launch_pack_obs(obs, N, s.D, s.Dp, X, st));
+    c->tr.mark(ST_PACK, st);
+    GemmOperands g1{X, s.Dp, c->sh.W1s, s.Dp, M, s.H1, s.Dp};
+    PPO_CUDA(tc_gemm_bias_act(g1, P + s.ob1, s.act, H1, s.H1, c->err, kTimeoutNs, c->num_sms, st));
+    c->tr.mark(ST_FWD1, st);
+    GemmOperands g2{H1, s.H1, c->sh.W2s, s.H1, M, s.H2, s.H1};
+    PPO_CUDA(tc_gemm_bias_act(g2, P + s.ob2, s.act, H2, s.H2, c->err, kTimeoutNs, c->num_sms, st));
+    c->tr.mark(ST_FWD2, st);
+  } else {
+    auto* H1 = static_cast<float*>(c->H1);
+    auto* H2 = static_cast<float*>(c->H2);
+    SimtOperands g1{obs, s.D, 1, P + s.oW1, s.D, 1, M, s.H1, s.D};
+    PPO_CUDA(simt_bias_act(g1, P + s.ob1, s.act, H1, s.H1, st));
+    c->tr.mark(ST_FWD1, st);
+    SimtOperands g2{H1, s.H1, 1, P + s.oW2, s.H1, 1, M, s.H2, s.H1};
+    PPO_CUDA(simt_bias_act(g2, P + s.ob2, s.act, H2, s.H2, st));
+    c->tr.mark(ST_FWD2, st);
+  }
+  PolicyActArgs a{};
+  a.s = s;
+  a.h = c->H2;
+  a.h_bf16 = c->bf16;
+  a.W3 = c->bf16 ? static_cast<const void*>(c->sh.W3s) : static_cast<const void*>(P + s.oW3);
+  a.b3 = P + s.ob3;
+  a.logstd = P + s.ologstd;
+  a.n = N;
+  a.seed = seed;
+  a.draw0 = draw0;
+  a.act = act;
+  a.actc = actc;
+  a.logp = logp;
+  a.value = value;
+  PPO_CUDA(launch_policy_act(a, st));
+  c->tr.mark(ST_POLICY_ACT, st);
   return PPO_OK;
 }
 
@@ -1166,6 +1221,7 @@ static ppo_status check_update_args(ppo_ctx* c, const float* obs, const int32_t*
   const int64_t B = T * N;
   if (B > c->bmax || epochs > c->emax || B % minibatches != 0) return PPO_ERR_INVALID;
   if (c->cfg.adv_mode != 0 && N % minibatches != 0) return PPO_ERR_INVALID;
+  if (c->cfg.adv_mode != 0 && c->s.H2 > 512) return PPO_ERR_UNSUPPORTED;
   const int64_t mb = B / minibatches;
   if (mb > c->mbmax || !obs || !logp_old || (c->s.NH > 0 && !act) || (c->s.G > 0 && !actc))
     return PPO_ERR_INVALID;
@@ -1261,7 +1317,7 @@ const char* ppo_stage_name(int32_t stage) {
       "perm_scatter", "gather", "fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm",
       "dact1_gemm", "wgrad_gemm", "grad_reduce", "grad_sqnorm", "adam", "weight_shadows",
       "minibatch_persistent", "fused_mlp", "grad_reduce_adam", "head_loss_dact2",
-      "fresh_advantages"};
+      "fresh_advantages", "policy_act"};
   static const char* phases[kMkPhases] = {
       "phase:gather", "phase:fwd1", "phase:fwd2", "phase:head_loss", "phase:dact2",
       "phase:dact1", "phase:wgrad", "phase:grad_reduce", "phase:adam"};

@@ -215,7 +215,7 @@ enum Stage : int {
   ST_PACK = 0, ST_GAE, ST_GAE_FINALIZE, ST_GAE_NORMALIZE, ST_PERM_HIST, ST_PERM_SCAN,
   ST_PERM_SCATTER, ST_GATHER, ST_FWD1, ST_FWD2, ST_LOSS, ST_DACT2, ST_DACT1, ST_WGRAD,
   ST_REDUCE, ST_SQNORM, ST_ADAM, ST_SHADOW, ST_MINIBATCH, ST_FUSED_MLP, ST_REDUCE_ADAM,
-  ST_LOSS_DACT2, ST_FRESH_ADV, ST_COUNT
+  ST_LOSS_DACT2, ST_FRESH_ADV, ST_POLICY_ACT, ST_COUNT
 };
 
 struct Trace {
@@ -310,5 +310,25 @@ struct FreshAdvArgs {
 };
 cudaError_t fresh_prepare();
 cudaError_t launch_fresh_adv(const FreshAdvArgs& a, int num_sms, cudaStream_t st);
+
+// Rollout-side policy step (act.cu): sampled actions, log-probability of the
+// stored action and value for n agents, from the last hidden layer.
+struct PolicyActArgs {
+  NetShape s;
+  const void* h;           // [n][H2], bf16 (h_bf16) or fp32
+  int h_bf16;
+  const void* W3;          // bf16 shadow [CP][H2] or fp32 [C][H2]
+  const float* b3;
+  const float* logstd;
+  int64_t n;
+  uint32_t seed;
+  uint64_t draw0;
+  int32_t* act;            // [n][NH]
+  float* actc;             // [n][G]
+  float* logp;             // [n] or nullptr
+  float* value;            // [n] or nullptr
+};
+cudaError_t policy_act_prepare();
+cudaError_t launch_policy_act(const PolicyActArgs& a, cudaStream_t st);
 
 }  // namespace ppo

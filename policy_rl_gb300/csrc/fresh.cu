@@ -12,9 +12,11 @@
 //
 // One cooperative launch, three phases separated by bounded grid barriers:
 //  A (optional) fresh values: one thread per row computes the row's
-//    head outputs from the last hidden layer the forward pass just wrote,
-//    with the head weights staged in shared memory (fp32, [H2][NCOL], read
-//    as broadcasts, chunks skewed across banks).  GAE needs only the value column (NCOL = 1); V-trace needs
+//    head outputs from the last hidden layer the forward pass just wrote
+//    (head_rows.cuh; one thread per row measured faster than 2 or 4 lanes
+//    per row -- 22.5 against 22.8 / 26.6 us per Mario-like minibatch --
+//    because more lanes need more blocks, and the grid barriers and the
+//    final merge grow with the block count).  GAE needs only the value column (NCOL = 1); V-trace needs
 //    every column to form the log-probability of the taken action and the
 //    ratio pi/mu = exp(logp - logp_old).
 //  B the segment scan: one warp per segment; the recursion is affine in
@@ -29,6 +31,7 @@
 //    the unbiased estimate.  (fp32 throughout: GB300's fp64 rate is a small
 //    fraction of its fp32 rate.)
 #include "common.cuh"
+#include "head_rows.cuh"
 #include "tc_ptx.cuh"
 
 namespace ppo {
@@ -123,93 +126,6 @@ __device__ bool grid_barrier(unsigned* bar, unsigned k, int* err, uint64_t limit
   return *s_abort == 0;
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
-
-// Phase A gives each row kSplit consecutive lanes: lane q reads the row's
-// 8-unit chunks q, q + kSplit, ... and the lanes sum their partial head
-// outputs by butterfly.  One lane per row measured fastest (Mario-like
-// minibatch: 22.5 us per launch against 22.8 with 2 lanes and 26.6 with 4;
-// more lanes per row mean more blocks, and the grid barriers and the final
-// merge grow with the block count).
-constexpr int kSplit = 1;
-
-// Head weights staged in shared memory as fp32: unit k's NCOL columns start
-// at w3_off(k).  H2 is rounded up to whole chunks (zero padding).  With
-// several columns, 8-unit chunk b starts 16 b bytes later than packed, so
-// that lanes of one row (kSplit > 1), which read the same unit of
-// consecutive chunks, hit different banks.
-__host__ __device__ __forceinline__ int w3_rows(int H2) { return (H2 + 7) / 8 * 8; }
-template <int NCOL>
-__host__ __device__ __forceinline__ int w3_off(int k) {
-  return k * NCOL + (NCOL > 1 ? (k >> 3) * 4 : 0);
-}
-__host__ __device__ __forceinline__ int w3_floats(int ncol, int H2) {
-  return w3_rows(H2) * ncol + (ncol > 1 ? w3_rows(H2) / 2 : 0);
-}
-
-// Phase A setup.  NCOL == 1 stages the value column only.  Work item i is
-// 8 consecutive hidden units of one column (one 16-byte load in bf16 mode);
-// the loads of up to 4 items per thread are issued before their stores.
-template <int NCOL>
-__device__ __forceinline__ void stage_w3(const FreshAdvArgs& a, float* w3t) {
-  const int H = a.s.H2, C = a.s.C, Hp = w3_rows(H);
-  const int chunks = Hp / 8, items = NCOL * chunks;
-  constexpr int kU = 4;
-  for (int i0 = threadIdx.x; i0 < items; i0 += kU * kFreshThreads) {
-    float w[kU][8];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i = i0 + u * kFreshThreads;
-      const int c = i / chunks, k0 = (i - c * chunks) * 8;
-      const int col = NCOL == 1 ? C - 1 : c;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) w[u][j] = 0.f;
-      if (i < items && col < C) {
-        const int64_t o = (int64_t)col * H + k0;
-        if (a.h2_bf16) {   // H2 is a multiple of 128: whole chunks
-          const uint4 q = *reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(a.W3) + o);
-          w[u][0] = bf_lo(q.x); w[u][1] = bf_hi(q.x); w[u][2] = bf_lo(q.y); w[u][3] = bf_hi(q.y);
-          w[u][4] = bf_lo(q.z); w[u][5] = bf_hi(q.z); w[u][6] = bf_lo(q.w); w[u][7] = bf_hi(q.w);
-        } else {
-          const float* src = static_cast<const float*>(a.W3) + o;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) w[u][j] = k0 + j < H ? src[j] : 0.f;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i = i0 + u * kFreshThreads;
-      if (i < items) {
-        const int c = i / chunks, k0 = (i - c * chunks) * 8;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w3t[w3_off<NCOL>(k0 + j) + c] = w[u][j];
-      }
-    }
-  }
-  __syncthreads();
-}
-
-// z[c] += h * w3t[unit k][c].
-template <int NCOL>
-__device__ __forceinline__ void fma_unit(float h, const float* w3t, int k, float (&z)[NCOL]) {
-  const float* w = w3t + w3_off<NCOL>(k);
-  if constexpr (NCOL == 1) {
-    z[0] = fmaf(h, w[0], z[0]);
-  } else {
-#pragma unroll
-    for (int c4 = 0; c4 < NCOL; c4 += 4) {
-      const float4 q = *reinterpret_cast<const float4*>(w + c4);
-      z[c4 + 0] = fmaf(h, q.x, z[c4 + 0]);
-      z[c4 + 1] = fmaf(h, q.y, z[c4 + 1]);
-      z[c4 + 2] = fmaf(h, q.z, z[c4 + 2]);
-      z[c4 + 3] = fmaf(h, q.w, z[c4 + 3]);
-    }
-  }
-}
-
 // Log-probability of the taken action from a row of head outputs z (thread
 // = row): log-softmax per discrete head by segmented running max / sum over
 // the compile-time-indexed columns, then the diagonal-Gaussian dimensions.
@@ -266,62 +182,18 @@ __device__ __forceinline__ float row_logp(const FreshAdvArgs& a, int64_t row,
   return logp;
 }
 
-// Phase A for one row, lane q of its kSplit lanes (every lane of the warp
-// calls this together; `valid` is false past the last row).
+// Phase A for one row (thread = row).
 template <int NCOL>
-__device__ __forceinline__ void eval_row(const FreshAdvArgs& a, const float* w3t, int64_t row,
-                                         bool valid, int q) {
-  const int H = a.s.H2, C = a.s.C;
+__device__ __forceinline__ void eval_row(const FreshAdvArgs& a, const HeadSrc& hs,
+                                         const float* w3t, int64_t row) {
   float z[NCOL];
-#pragma unroll
-  for (int c = 0; c < NCOL; ++c) z[c] = 0.f;
-  if (valid) {
-    if (a.h2_bf16) {   // H2 is a multiple of 128 in bf16 mode
-      const uint4* hp =
-          reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.H2) + row * H);
-      // up to kBatch chunks of the row in flight per lane before any arithmetic
-      constexpr int kBatch = 8;
-      for (int kb = 8 * q; kb < H; kb += 8 * kSplit * kBatch) {
-        uint4 u[kBatch];
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-          const int k0 = kb + 8 * kSplit * i;
-          u[i] = k0 < H ? hp[k0 / 8] : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-          const int k0 = kb + 8 * kSplit * i;
-          if (k0 < H) {
-            const float h[8] = {bf_lo(u[i].x), bf_hi(u[i].x), bf_lo(u[i].y), bf_hi(u[i].y),
-                                bf_lo(u[i].z), bf_hi(u[i].z), bf_lo(u[i].w), bf_hi(u[i].w)};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) fma_unit<NCOL>(h[j], w3t, k0 + j, z);
-          }
-        }
-      }
-    } else {
-      const float* hp = static_cast<const float*>(a.H2) + row * H;
-      for (int k0 = 8 * q; k0 < H; k0 += 8 * kSplit) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)   // staged units below w3_rows(H) are zero past H
-          fma_unit<NCOL>(k0 + j < H ? hp[k0 + j] : 0.f, w3t, k0 + j, z);
-      }
-    }
-  }
-#pragma unroll
-  for (int c = 0; c < NCOL; ++c)
-#pragma unroll
-    for (int o = 1; o < kSplit; o <<= 1) z[c] += __shfl_xor_sync(0xffffffffu, z[c], o);
-  if (!valid || q != 0) return;
+  head_row<NCOL>(hs, w3t, row, z);
   if constexpr (NCOL == 1) {
-    a.val[row] = z[0] + __ldg(a.b3 + C - 1);
+    a.val[row] = z[0];
   } else {
     float v = 0.f;
 #pragma unroll
-    for (int c = 0; c < NCOL; ++c) {
-      z[c] += c < C ? __ldg(a.b3 + c) : 0.f;
-      v = (c == C - 1) ? z[c] : v;
-    }
+    for (int c = 0; c < NCOL; ++c) v = (c == a.s.C - 1) ? z[c] : v;
     a.val[row] = v;
     a.ratio[row] = __expf(row_logp<NCOL>(a, row, z) - __ldg(a.logp_old + row));
   }
@@ -458,14 +330,12 @@ fresh_adv_kernel(FreshAdvArgs a) {
   const int64_t e0 = j0 < a.ns ? (int64_t)__ldg(a.envs + j0) : 0;
   SegPre pre;
   if (a.head) {
-    stage_w3<NCOL>(a, w3t);
-    // warp-uniform loop (the lanes of a row shuffle): t0 = the warp's first thread
+    const HeadSrc hs{a.H2, a.h2_bf16, a.W3, a.b3, a.s.H2, a.s.C};
+    stage_w3<NCOL>(hs, w3t, kFreshThreads);
     const int64_t stride = (int64_t)gridDim.x * kFreshThreads;
-    for (int64_t t0 = (int64_t)blockIdx.x * kFreshThreads + warp * 32; t0 / kSplit < rows;
-         t0 += stride) {
-      const int64_t row = (t0 + lane) / kSplit;
-      eval_row<NCOL>(a, w3t, row, row < rows, lane & (kSplit - 1));
-    }
+    for (int64_t row = (int64_t)blockIdx.x * kFreshThreads + threadIdx.x; row < rows;
+         row += stride)
+      eval_row<NCOL>(a, hs, w3t, row);
     if (j0 < a.ns) seg_prefetch(a, e0, lane, pre);
     if (!grid_barrier(a.bar, ++k, a.err, a.timeout_ns, &s_abort)) return;
   } else if (j0 < a.ns) {
@@ -574,7 +444,7 @@ cudaError_t launch_fresh_adv(const FreshAdvArgs& a, int num_sms, cudaStream_t st
   // enough blocks for one row per thread in phase A (or for the normalisation)
   // and one warp per segment in phase B
   int64_t want = (a.ns + kFreshWarps - 1) / kFreshWarps;
-  const int64_t per_rows = a.head ? (rows * kSplit + kFreshThreads - 1) / kFreshThreads
+  const int64_t per_rows = a.head ? (rows + kFreshThreads - 1) / kFreshThreads
                                   : (rows + 8 * kFreshThreads - 1) / (8 * kFreshThreads);
   if (per_rows > want) want = per_rows;
   const int grid = (int)(want > cap ? cap : (want < 1 ? 1 : want));
