@@ -341,6 +341,11 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.skip_adam_stress:
         adam = _adam_stress(stream, hbm_peak)
 
+    # rollout side: one policy step (forward + sampling) of the workload's N agents
+    act_step = None
+    if rank == 0 and not args.skip_policy_act:
+        act_step = _policy_act_step(ctx, w, obs_d, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
         cpu = _cpu_baseline(w, ADV_MODES[args.advantages])
@@ -366,6 +371,7 @@ def run_ours(args, world, rank, local):
         "profiled_update_ms": round(total_ms, 4),
         "gae_stress": gae,
         "adam_stress": adam,
+        "policy_act": act_step,
         "cpu_baseline": cpu,
         "clocks": clk,
     }
@@ -434,6 +440,40 @@ def _adam_stress(stream, hbm_peak):
     return {"params": n, "ms": round(t * 1e3, 4), "GB_per_s": round(gbs, 1),
             "frac_of_hbm": round(gbs / hbm_peak, 4), "bytes_per_param": 32,
             "note": "ppo_adam_step: squared-norm pass + fused clip/Adam pass, fp32 mode"}
+
+
+def _policy_act_step(ctx, w, obs_d, stream, reps=50):
+    """ppo_policy_act on the first N rows of the rollout (one environment step
+    of all N agents): pack + two forward GEMMs + head/sampling kernel."""
+    import torch
+    import policy_rl_gb300 as P
+    N = w.N
+    obs = obs_d[:N].contiguous()
+    act = torch.empty(N, max(len(w.heads), 1), dtype=torch.int32, device="cuda")
+    actc = torch.empty(N, max(w.n_gauss, 1), device="cuda")
+    logp = torch.empty(N, device="cuda")
+    val = torch.empty(N, device="cuda")
+    K = len(w.heads) + 2 * w.n_gauss
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            P.ppo_policy_act(ctx.handle, obs, 1, i * N * K, act, actc if w.n_gauss else None,
+                             logp, val, stream=stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for i, (s0, e0) in enumerate(evs):
+            s0.record(stream)
+            P.ppo_policy_act(ctx.handle, obs, 1, (5 + i) * N * K, act,
+                             actc if w.n_gauss else None, logp, val, stream=stream)
+            e0.record(stream)
+        stream.synchronize()
+    P.ppo_sync_status(ctx.handle, stream)
+    t = float(np.median([a.elapsed_time(b) for a, b in evs])) / 1e3
+    bf16 = w.precision == "bf16"
+    return {"agents": N, "us_per_step": round(t * 1e6, 2), "agents_per_s": round(N / t, 1),
+            "launches": 4 if bf16 else 3,
+            "note": ("ppo_policy_act: pack obs, fwd1, fwd2 (tcgen05), head + sampling"
+                     if bf16 else "ppo_policy_act: fwd1, fwd2 (CUDA cores), head + sampling")
+                    + f"; median of {reps} steps, inputs resident, no L2 flush"}
 
 
 def _cpu_sample(w):
@@ -529,6 +569,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     ap.add_argument("--skip-gae-stress", action="store_true")
     ap.add_argument("--skip-adam-stress", action="store_true")
+    ap.add_argument("--skip-policy-act", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = _dist()

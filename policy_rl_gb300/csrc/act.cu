@@ -6,7 +6,8 @@
 // for all agents at once, actions sampled from the logits and written
 // straight into the action buffer, the probability of the taken action kept
 // for the ratio.  The forward GEMMs are the learner's (tensor cores in bf16
-// mode); this kernel takes the last hidden layer, one thread per agent:
+// mode); this kernel takes the last hidden layer, one thread per agent (8
+// lanes per agent for steps of fewer than 16,384 agents):
 //   head outputs z (head_rows.cuh), then per discrete head an inverse-CDF
 //   draw (the first category whose cumulative probability exceeds u,
 //   compared as u * sum e^(z - max) < running sum), per Gaussian dimension
@@ -36,7 +37,9 @@ __device__ __forceinline__ uint32_t mulberry32_at(uint32_t seed, uint64_t draw) 
 
 __device__ __forceinline__ float uniform24(uint32_t x) { return (float)(x >> 8) * 5.9604645e-8f; }
 
-template <int NCOL>
+// One agent per SPLIT consecutive lanes: SPLIT = 1 for large agent counts;
+// SPLIT = 8 spreads a small step (a few thousand agents) over more SMs.
+template <int NCOL, int SPLIT>
 __global__ void __launch_bounds__(kActThreads)
 policy_act_kernel(PolicyActArgs a) {
   extern __shared__ float4 smem_dyn[];
@@ -45,10 +48,20 @@ policy_act_kernel(PolicyActArgs a) {
   const HeadSrc hs{a.h, a.h_bf16, a.W3, a.b3, a.s.H2, a.s.C};
   stage_w3<NCOL>(hs, w3t, kActThreads);
   pdl_trigger();
-  const int64_t i = (int64_t)blockIdx.x * kActThreads + threadIdx.x;
-  if (i >= a.n) return;
+  const int64_t t = (int64_t)blockIdx.x * kActThreads + threadIdx.x;
+  const int64_t i = t / SPLIT;
+  const int q = (int)(t % SPLIT);
+  const bool valid = i < a.n;
+  if (SPLIT == 1 && !valid) return;
   float zr[NCOL];
-  head_row<NCOL>(hs, w3t, i, zr);
+  if (valid) {
+    head_row<NCOL, SPLIT>(hs, w3t, i, zr, q);
+  } else {
+#pragma unroll
+    for (int c = 0; c < NCOL; ++c) zr[c] = 0.f;
+  }
+  if constexpr (SPLIT > 1) split_sum<NCOL, SPLIT>(zr);   // every lane of the warp
+  if (!valid || q != 0) return;
   float z[NCOL];   // dynamically indexed below (local memory)
 #pragma unroll
   for (int c = 0; c < NCOL; ++c) z[c] = zr[c];
@@ -91,11 +104,15 @@ policy_act_kernel(PolicyActArgs a) {
   if (a.value) a.value[i] = z[s.C - 1];
 }
 
+// Agent counts below this use 8 lanes per agent.
+constexpr int64_t kActSplitBelow = 16384;
+
 int g_act_ready = 0;
 
-template <int NCOL>
+template <int NCOL, int SPLIT>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(policy_act_kernel<NCOL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(policy_act_kernel<NCOL, SPLIT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)(w3_floats(NCOL, 512) * sizeof(float)));
 }
 
@@ -103,8 +120,10 @@ cudaError_t prepare_one() {
 
 cudaError_t policy_act_prepare() {
   if (g_act_ready) return cudaSuccess;
-  cudaError_t e = prepare_one<16>();
-  if (e == cudaSuccess) e = prepare_one<32>();
+  cudaError_t e = prepare_one<16, 1>();
+  if (e == cudaSuccess) e = prepare_one<32, 1>();
+  if (e == cudaSuccess) e = prepare_one<16, 8>();
+  if (e == cudaSuccess) e = prepare_one<32, 8>();
   if (e == cudaSuccess) g_act_ready = 1;
   return e;
 }
@@ -113,10 +132,15 @@ cudaError_t launch_policy_act(const PolicyActArgs& a, cudaStream_t st) {
   if (!g_act_ready) return cudaErrorInitializationError;
   if (a.s.H2 > 512) return cudaErrorInvalidValue;
   const int ncol = a.s.C <= 16 ? 16 : 32;
+  const bool split = a.n < kActSplitBelow;
   const size_t smem = (size_t)w3_floats(ncol, a.s.H2) * sizeof(float);
-  const dim3 grid((unsigned)((a.n + kActThreads - 1) / kActThreads));
-  if (ncol == 16) return launch_pdl(policy_act_kernel<16>, grid, dim3(kActThreads), smem, st, a);
-  return launch_pdl(policy_act_kernel<32>, grid, dim3(kActThreads), smem, st, a);
+  const int64_t threads = a.n * (split ? 8 : 1);
+  const dim3 grid((unsigned)((threads + kActThreads - 1) / kActThreads)), block(kActThreads);
+  if (ncol == 16)
+    return split ? launch_pdl(policy_act_kernel<16, 8>, grid, block, smem, st, a)
+                 : launch_pdl(policy_act_kernel<16, 1>, grid, block, smem, st, a);
+  return split ? launch_pdl(policy_act_kernel<32, 8>, grid, block, smem, st, a)
+               : launch_pdl(policy_act_kernel<32, 1>, grid, block, smem, st, a);
 }
 
 }  // namespace ppo

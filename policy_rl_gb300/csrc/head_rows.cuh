@@ -104,9 +104,12 @@ __device__ __forceinline__ void fma_unit(float h, const float* w3t, int k, float
 
 // Head outputs of one row: NCOL == 1 gives z[0] = the value (column C - 1);
 // otherwise z[c] = column c for c < C and 0 beyond.  Biases included.
-template <int NCOL>
+// SPLIT > 1: this thread is lane q of the SPLIT consecutive lanes that share
+// the row; it sums the row's 8-unit chunks q, q + SPLIT, ... only (bias on
+// lane 0), and the caller adds the lanes' partials (split_sum).
+template <int NCOL, int SPLIT = 1>
 __device__ __forceinline__ void head_row(const HeadSrc& hs, const float* w3t, int64_t row,
-                                         float (&z)[NCOL]) {
+                                         float (&z)[NCOL], int q = 0) {
   const int H = hs.H, C = hs.C;
 #pragma unroll
   for (int c = 0; c < NCOL; ++c) z[c] = 0.f;
@@ -114,14 +117,16 @@ __device__ __forceinline__ void head_row(const HeadSrc& hs, const float* w3t, in
     const uint4* hp =
         reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(hs.h) + row * H);
     constexpr int kBatch = 8;   // chunks in flight before any arithmetic
-    for (int kb = 0; kb < H; kb += 8 * kBatch) {
+    for (int kb = 8 * q; kb < H; kb += 8 * SPLIT * kBatch) {
       uint4 u[kBatch];
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i)
-        u[i] = kb + 8 * i < H ? hp[kb / 8 + i] : make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < kBatch; ++i) {
+        const int k0 = kb + 8 * SPLIT * i;
+        u[i] = k0 < H ? hp[k0 / 8] : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
-        const int k0 = kb + 8 * i;
+        const int k0 = kb + 8 * SPLIT * i;
         if (k0 < H) {
           const float h[8] = {bf_lo(u[i].x), bf_hi(u[i].x), bf_lo(u[i].y), bf_hi(u[i].y),
                               bf_lo(u[i].z), bf_hi(u[i].z), bf_lo(u[i].w), bf_hi(u[i].w)};
@@ -132,18 +137,29 @@ __device__ __forceinline__ void head_row(const HeadSrc& hs, const float* w3t, in
     }
   } else {
     const float* hp = static_cast<const float*>(hs.h) + row * H;
-    for (int k0 = 0; k0 < H; k0 += 8) {
+    for (int k0 = 8 * q; k0 < H; k0 += 8 * SPLIT) {
 #pragma unroll
       for (int j = 0; j < 8; ++j)   // staged units below w3_rows(H) are zero past H
         fma_unit<NCOL>(k0 + j < H ? hp[k0 + j] : 0.f, w3t, k0 + j, z);
     }
   }
+  if (q != 0) return;
   if constexpr (NCOL == 1) {
     z[0] += __ldg(hs.b3 + C - 1);
   } else {
 #pragma unroll
     for (int c = 0; c < NCOL; ++c) z[c] += c < C ? __ldg(hs.b3 + c) : 0.f;
   }
+}
+
+// Sums the partials of the SPLIT consecutive lanes of a row (all lanes of the
+// warp must call it); every lane of the group ends with the total.
+template <int NCOL, int SPLIT>
+__device__ __forceinline__ void split_sum(float (&z)[NCOL]) {
+#pragma unroll
+  for (int c = 0; c < NCOL; ++c)
+#pragma unroll
+    for (int o = 1; o < SPLIT; o <<= 1) z[c] += __shfl_xor_sync(0xffffffffu, z[c], o);
 }
 
 }  // namespace ppo
