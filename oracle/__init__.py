@@ -58,7 +58,8 @@ class _Hyper(ctypes.Structure):
                 ("adam_eps", ctypes.c_double), ("max_grad_norm", ctypes.c_double),
                 ("seed", ctypes.c_uint32), ("bf16_operands", ctypes.c_int),
                 ("adv_mode", ctypes.c_int), ("rho_clip", ctypes.c_double),
-                ("c_clip", ctypes.c_double)]
+                ("c_clip", ctypes.c_double), ("optimizer", ctypes.c_int),
+                ("muon_lr", ctypes.c_double), ("muon_beta", ctypes.c_double)]
 
 
 _P = ctypes.c_void_p
@@ -109,8 +110,11 @@ def lib():
         L.orc_box_muller.restype = _D
         L.orc_policy_act.argtypes = [ctypes.POINTER(_Net), ctypes.c_int, _P, _I64, _P, ctypes.c_uint32,
                                      ctypes.c_uint64, _P, _P, _P, _P]
+        L.orc_newton_schulz5.argtypes = [_I64, _I64, _P, ctypes.c_int, _P]
+        L.orc_muon.argtypes = [ctypes.POINTER(_Net), _P, _P, _P, _P, _P, _I64, _D, _D, _D, _D, _D,
+                               _D]
         L.orc_update.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_Hyper), _I64, _I64, _I64, _I64,
-                                 _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                 _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                  ctypes.POINTER(_I64), _P, _P, _P]
     return _lib
 
@@ -167,11 +171,15 @@ class Hyper:
     adv_mode: int = 0          # 0 once per update, 1 fresh GAE, 2 fresh V-trace
     rho_clip: float = 1.0
     c_clip: float = 1.0
+    optimizer: int = 0         # 0 Adam, 1 Muon (weight matrices) + Adam (vectors)
+    muon_lr: float = 0.02
+    muon_beta: float = 0.95
 
     def c(self) -> _Hyper:
         return _Hyper(self.gamma, self.lam, self.clip, self.vf_coef, self.ent_coef, self.lr,
                       self.beta1, self.beta2, self.adam_eps, self.max_grad_norm, self.seed,
-                      int(self.bf16_operands), int(self.adv_mode), self.rho_clip, self.c_clip)
+                      int(self.bf16_operands), int(self.adv_mode), self.rho_clip, self.c_clip,
+                      int(self.optimizer), self.muon_lr, self.muon_beta)
 
 
 def mulberry32_stream(seed: int, count: int) -> np.ndarray:
@@ -387,11 +395,32 @@ def adam(p, g, m, v, step, lr, beta1=0.9, beta2=0.999, eps=1e-8):
     return p, m, v
 
 
+def newton_schulz5(G, steps: int = 5):
+    """Muon's quintic Newton-Schulz orthogonalisation of a matrix (fp64)."""
+    G = _as(G, np.float64)
+    rows, cols = G.shape
+    out = np.empty_like(G)
+    lib().orc_newton_schulz5(rows, cols, _ptr(G), steps, _ptr(out))
+    return out
+
+
+def muon(net: Net, p, g, mom, m, v, step, muon_lr=0.02, muon_beta=0.95, lr=2.5e-4,
+         beta1=0.9, beta2=0.999, eps=1e-8):
+    """One Muon step (matrices) + Adam (vectors); returns (p, mom, m, v)."""
+    p, mom, m, v = (_as(x, np.float64).copy() for x in (p, mom, m, v))
+    g = _as(g, np.float64)
+    cn = net.c()
+    lib().orc_muon(ctypes.byref(cn), _ptr(p), _ptr(g), _ptr(mom), _ptr(m), _ptr(v), step, muon_lr,
+                   muon_beta, lr, beta1, beta2, eps)
+    return p, mom, m, v
+
+
 @dataclass
 class UpdateResult:
     params: np.ndarray
     m: np.ndarray
     v: np.ndarray
+    mom: np.ndarray
     step: int
     stats: np.ndarray
     adv: np.ndarray
@@ -399,11 +428,12 @@ class UpdateResult:
 
 
 def update(net: Net, hp: Hyper, T, N, epochs, minibatches, obs, act_disc, act_cont, logp_old,
-           val, rew, done, boot, params, m=None, v=None, step=0) -> UpdateResult:
+           val, rew, done, boot, params, m=None, v=None, step=0, mom=None) -> UpdateResult:
     P = net.num_params
     params = _as(params, np.float64).copy()
     m = np.zeros(P) if m is None else _as(m, np.float64).copy()
     v = np.zeros(P) if v is None else _as(v, np.float64).copy()
+    mom = np.zeros(P) if mom is None else _as(mom, np.float64).copy()
     stats = np.empty((epochs * minibatches, 6), np.float64)
     adv = np.zeros(T * N, np.float64)   # not written in the fresh-advantage modes
     ret = np.zeros(T * N, np.float64)
@@ -414,6 +444,6 @@ def update(net: Net, hp: Hyper, T, N, epochs, minibatches, obs, act_disc, act_co
             _as(done, np.float32), _as(boot, np.float32)]
     cn, ch = net.c(), hp.c()
     lib().orc_update(ctypes.byref(cn), ctypes.byref(ch), T, N, epochs, minibatches,
-                     *[_ptr(a) for a in arrs], _ptr(params), _ptr(m), _ptr(v),
+                     *[_ptr(a) for a in arrs], _ptr(params), _ptr(m), _ptr(v), _ptr(mom),
                      ctypes.byref(st), _ptr(stats), _ptr(adv), _ptr(ret))
-    return UpdateResult(params, m, v, st.value, stats, adv.reshape(T, N), ret.reshape(T, N))
+    return UpdateResult(params, m, v, mom, st.value, stats, adv.reshape(T, N), ret.reshape(T, N))

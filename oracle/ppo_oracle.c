@@ -657,16 +657,126 @@ void orc_adam(int64_t P, double *p, const double *g, double *m, double *v, int64
 }
 
 /* ------------------------------------------------------------------------ */
+/* "Teaching Mario to speedrun", sec. 8 "The Puffer net, and the trainer" and
+ * "puff-rs": the 5.0 optimizer is Muon, which orthogonalises each weight
+ * matrix's update, with five Newton-Schulz iterations.  The pages give no
+ * formula; the definition is Muon's published write-up (K. Jordan et al.,
+ * 2024, "Muon: An optimizer for hidden layers in neural networks"):
+ *   X = G / (||G||_F + 1e-7), as an r x k matrix with r <= k (transposed if
+ *   G has more rows than columns); five times
+ *     A = X X^T,  B = b A + c A A,  X = a X + B X,
+ *   with (a, b, c) = (3.4445, -4.7750, 2.0315); transposed back.
+ * The write-up runs the iteration in bf16; here it is fp64. */
+void orc_newton_schulz5(int64_t rows, int64_t cols, const double *G, int steps, double *out)
+{
+    const double ca = 3.4445, cb = -4.7750, cc = 2.0315;
+    const int tr = rows > cols;
+    const int64_t r = tr ? cols : rows, k = tr ? rows : cols;
+    double *X = (double *)malloc(sizeof(double) * (size_t)(r * k));
+    double *Xn = (double *)malloc(sizeof(double) * (size_t)(r * k));
+    double *A = (double *)malloc(sizeof(double) * (size_t)(r * r));
+    double *B = (double *)malloc(sizeof(double) * (size_t)(r * r));
+    double ss = 0.0;
+    for (int64_t i = 0; i < rows * cols; ++i) ss += G[i] * G[i];
+    const double inv = 1.0 / (sqrt(ss) + 1e-7);
+    for (int64_t i = 0; i < r; ++i)
+        for (int64_t j = 0; j < k; ++j)
+            X[i * k + j] = (tr ? G[j * cols + i] : G[i * cols + j]) * inv;
+    for (int s = 0; s < steps; ++s) {
+        for (int64_t i = 0; i < r; ++i)
+            for (int64_t j = 0; j < r; ++j) {
+                double t = 0.0;
+                for (int64_t q = 0; q < k; ++q) t += X[i * k + q] * X[j * k + q];
+                A[i * r + j] = t;
+            }
+        for (int64_t i = 0; i < r; ++i)
+            for (int64_t j = 0; j < r; ++j) {
+                double t = 0.0;
+                for (int64_t q = 0; q < r; ++q) t += A[i * r + q] * A[q * r + j];
+                B[i * r + j] = cb * A[i * r + j] + cc * t;
+            }
+        for (int64_t i = 0; i < r; ++i)
+            for (int64_t j = 0; j < k; ++j) {
+                double t = 0.0;
+                for (int64_t q = 0; q < r; ++q) t += B[i * r + q] * X[q * k + j];
+                Xn[i * k + j] = ca * X[i * k + j] + t;
+            }
+        memcpy(X, Xn, sizeof(double) * (size_t)(r * k));
+    }
+    for (int64_t i = 0; i < r; ++i)
+        for (int64_t j = 0; j < k; ++j) {
+            if (tr) out[j * cols + i] = X[i * k + j];
+            else out[i * cols + j] = X[i * k + j];
+        }
+    free(X); free(Xn); free(A); free(B);
+}
+
+/* One Muon step of the MLP's parameters (write-up's update with Nesterov
+ * momentum): for each weight matrix W1, W2, W3 (rows x cols)
+ *   mom = beta mom + g;  u = g + beta mom;
+ *   W -= muon_lr sqrt(max(1, rows / cols)) NS5(u),
+ * and, as the write-up prescribes for parameters that are not matrices, Adam
+ * for the biases and the log-std (orc_adam's update, this `step`).  mom
+ * covers the whole parameter vector (only the matrix entries are used);
+ * adam_m, adam_v likewise (only the vector entries). */
+void orc_muon(const orc_net *net, double *params, const double *g, double *mom,
+              double *adam_m, double *adam_v, int64_t step, double muon_lr, double muon_beta,
+              double lr, double beta1, double beta2, double eps)
+{
+    const int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
+    const int64_t P = orc_num_params(net);
+    orc_views v = orc_split(net, params);
+    const int64_t offs[3] = {v.W1 - params, v.W2 - params, v.W3 - params};
+    const int64_t rows[3] = {H1, H2, C}, cols[3] = {D, H1, H2};
+    char *is_mat = (char *)calloc((size_t)P, 1);
+    for (int mtx = 0; mtx < 3; ++mtx) {
+        const int64_t o = offs[mtx], n = rows[mtx] * cols[mtx];
+        double *u = (double *)malloc(sizeof(double) * (size_t)n);
+        double *x = (double *)malloc(sizeof(double) * (size_t)n);
+        for (int64_t i = 0; i < n; ++i) {
+            mom[o + i] = muon_beta * mom[o + i] + g[o + i];
+            u[i] = g[o + i] + muon_beta * mom[o + i];
+            is_mat[o + i] = 1;
+        }
+        orc_newton_schulz5(rows[mtx], cols[mtx], u, 5, x);
+        const double ratio = (double)rows[mtx] / (double)cols[mtx];
+        const double scale = sqrt(ratio > 1.0 ? ratio : 1.0);
+        for (int64_t i = 0; i < n; ++i) params[o + i] -= muon_lr * scale * x[i];
+        free(u); free(x);
+    }
+    const double bc1 = 1.0 - pow(beta1, (double)step);
+    const double bc2 = 1.0 - pow(beta2, (double)step);
+    for (int64_t i = 0; i < P; ++i) {
+        if (is_mat[i]) continue;
+        adam_m[i] = beta1 * adam_m[i] + (1.0 - beta1) * g[i];
+        adam_v[i] = beta2 * adam_v[i] + (1.0 - beta2) * g[i] * g[i];
+        params[i] -= lr * (adam_m[i] / bc1) / (sqrt(adam_v[i] / bc2) + eps);
+    }
+    free(is_mat);
+}
+
+/* ------------------------------------------------------------------------ */
 /* "Teaching Mario to speedrun", sec. 6 "The whole algorithm": judge with GAE,
  * then learn for a few epochs over shuffled minibatches, one backward pass
  * and one optimizer step per minibatch.  The advantages are normalised with
  * the statistics of the whole batch. */
+/* The optimizer step of orc_update: Adam (optimizer 0) or Muon (1). */
+static void orc_optimize(const orc_net *net, const orc_hyper *hp, int64_t P, double *params,
+                         const double *grad, double *m, double *v, double *mom, int64_t step)
+{
+    if (hp->optimizer == 1)
+        orc_muon(net, params, grad, mom, m, v, step, hp->muon_lr, hp->muon_beta, hp->lr,
+                 hp->beta1, hp->beta2, hp->adam_eps);
+    else
+        orc_adam(P, params, grad, m, v, step, hp->lr, hp->beta1, hp->beta2, hp->adam_eps);
+}
+
 void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
                 int64_t epochs, int64_t minibatches,
                 const float *obs, const int32_t *act_disc, const float *act_cont,
                 const float *logp_old, const float *val, const float *rew,
                 const float *done, const float *boot,
-                double *params, double *m, double *v, int64_t *step,
+                double *params, double *m, double *v, double *mom, int64_t *step,
                 double *stats, double *adv_out, double *ret_out)
 {
     const int64_t B = T * N, mb = B / minibatches, P = orc_num_params(net);
@@ -692,8 +802,7 @@ void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
                                     st ? st : tmp, NULL, NULL, NULL);
                 orc_clip_grad_norm(P, grad, hp->max_grad_norm);
                 *step += 1;
-                orc_adam(P, params, grad, m, v, *step, hp->lr, hp->beta1, hp->beta2,
-                         hp->adam_eps);
+                orc_optimize(net, hp, P, params, grad, m, v, mom, *step);
             }
         }
         free(adv); free(ret); free(perm); free(grad);
@@ -713,7 +822,7 @@ void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
                           logp_old, adv, ret, 1, mean, sd, grad, st ? st : tmp, NULL);
             orc_clip_grad_norm(P, grad, hp->max_grad_norm);
             *step += 1;
-            orc_adam(P, params, grad, m, v, *step, hp->lr, hp->beta1, hp->beta2, hp->adam_eps);
+            orc_optimize(net, hp, P, params, grad, m, v, mom, *step);
         }
     }
     if (adv_out) memcpy(adv_out, adv, sizeof(double) * (size_t)B);

@@ -155,6 +155,15 @@ double orc_clip_grad_norm(int64_t P, double *g, double max_norm);
 void orc_adam(int64_t P, double *p, const double *g, double *m, double *v, int64_t step,
               double lr, double beta1, double beta2, double eps);
 
+/* Muon ("Muon: An optimizer for hidden layers in neural networks"): the
+ * quintic Newton-Schulz orthogonalisation of a rows x cols matrix (steps
+ * iterations), and one Muon step of the MLP (matrices W1..W3 by Muon with
+ * Nesterov momentum mom, biases and log-std by Adam).  See ppo_oracle.c. */
+void orc_newton_schulz5(int64_t rows, int64_t cols, const double *G, int steps, double *out);
+void orc_muon(const orc_net *net, double *params, const double *g, double *mom,
+              double *adam_m, double *adam_v, int64_t step, double muon_lr, double muon_beta,
+              double lr, double beta1, double beta2, double eps);
+
 typedef struct {
     double gamma, lambda, clip, vf_coef, ent_coef;
     double lr, beta1, beta2, adam_eps, max_grad_norm;
@@ -164,6 +173,8 @@ typedef struct {
                             1: per minibatch of env segments, GAE from fresh values;
                             2: the same with V-trace */
     double rho_clip, c_clip;   /* V-trace truncation levels (adv_mode 2) */
+    int optimizer;             /* 0 Adam; 1 Muon for the weight matrices (orc_muon) */
+    double muon_lr, muon_beta;
 } orc_hyper;
 
 /* One whole PPO update: GAE, global advantage statistics, then for each epoch
@@ -179,7 +190,7 @@ void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
                 const float *obs, const int32_t *act_disc, const float *act_cont,
                 const float *logp_old, const float *val, const float *rew,
                 const float *done, const float *boot,
-                double *params, double *m, double *v, int64_t *step,
+                double *params, double *m, double *v, double *mom, int64_t *step,
                 double *stats, double *adv_out, double *ret_out);
 
 #ifdef __cplusplus
