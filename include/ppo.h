@@ -120,6 +120,15 @@ typedef struct {
                                     ignored) and need N % minibatches == 0.   */
     float vtrace_rho_clip;       /* V-trace rho_bar (adv_mode 2; IMPALA: 1)    */
     float vtrace_c_clip;         /* V-trace c_bar   (adv_mode 2; IMPALA: 1)    */
+    int32_t optimizer;           /* optimizer step of ppo_update:
+                                    0 (default) Adam on every parameter;
+                                    1 Muon ("Teaching Mario to speedrun",
+                                      sec. 8; see ppo_muon_step) on W1, W2,
+                                      W3 and Adam on the biases and log-std.
+                                    Muon needs persistent_minibatch == 0
+                                    (ignored otherwise).                      */
+    float muon_lr;               /* Muon learning rate (write-up: 0.02)        */
+    float muon_beta;             /* Muon momentum (write-up: 0.95)             */
 } ppo_config;
 
 typedef struct ppo_ctx ppo_ctx;
@@ -308,6 +317,22 @@ ppo_status ppo_policy_act(ppo_ctx *ctx, const float *d_obs, int64_t N, uint32_t 
  * d_grad_norm (nullable, fp32 [1]) receives ||g||_2 before clipping. */
 ppo_status ppo_adam_step(ppo_ctx *ctx, float lr, float *d_grad_norm, cudaStream_t stream);
 
+/* Muon step ("Teaching Mario to speedrun", sec. 8 and "puff-rs": the 5.0
+ * optimizer orthogonalises each weight matrix's update with five
+ * Newton-Schulz iterations).  Definition from Muon's published write-up:
+ * after the gradient-norm clip (as in ppo_adam_step), for each weight matrix
+ * W (rows x cols) with momentum buffer mom (context-owned, zero at creation):
+ *   mom = muon_beta mom + g;  u = g + muon_beta mom  (Nesterov);
+ *   X = u / (||u||_F + 1e-7) as an r x k matrix, r = min(rows, cols);
+ *   five times: A = X X^T, B = b A + c A A, X = a X + B X,
+ *     (a, b, c) = (3.4445, -4.7750, 2.0315);
+ *   W -= muon_lr sqrt(max(1, rows / cols)) X.
+ * The biases and log-std take the Adam step of ppo_adam_step with rate lr.
+ * The Newton-Schulz products run in fp32 (the write-up uses bf16).  Requires
+ * a context created with optimizer == 1 (PPO_ERR_INVALID otherwise);
+ * increments the step counter; d_grad_norm as in ppo_adam_step. */
+ppo_status ppo_muon_step(ppo_ctx *ctx, float lr, float *d_grad_norm, cudaStream_t stream);
+
 /* ---- Whole update -------------------------------------------------------------
  * "Teaching Mario to speedrun", sec. 6 "The whole algorithm", steps 2-3:
  * GAE (gamma, lambda) over the [T,N] rollout, advantage statistics over all
@@ -343,8 +368,8 @@ ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_ac
  * phases inside the persistent minibatch kernel (time between the phase
  * starts seen by its first CTA, summed over minibatches); they are not
  * separate launches. */
-#define PPO_NUM_KERNEL_STAGES 24
-#define PPO_NUM_STAGES 33
+#define PPO_NUM_KERNEL_STAGES 25
+#define PPO_NUM_STAGES 34
 /* Name of a stage (static string; "unknown" outside [0, PPO_NUM_STAGES)). */
 const char *ppo_stage_name(int32_t stage);
 

@@ -18,7 +18,7 @@ __all__ = [
     "PpoConfig", "PpoError", "Context", "make_config", "ppo_param_count", "ppo_gae",
     "ppo_gae_workspace_bytes", "ppo_gae_noalloc", "ppo_minibatch_perm", "ppo_perm_workspace_bytes",
     "ppo_segment_advantage", "ppo_segment_advantage_workspace_bytes",
-    "ppo_minibatch_loss_grad_fresh", "ppo_policy_act",
+    "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_muon_step",
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
     "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "library_path",
@@ -57,17 +57,19 @@ def make_config(obs_dim, h1, h2, act=0, heads=(3, 2, 2), n_gauss=0, precision=1,
                 vf_coef=0.5, ent_coef=0.01, beta1=0.9, beta2=0.999, adam_eps=1e-8,
                 max_grad_norm=0.5, max_batch=1, max_minibatch=1, max_epochs=1,
                 persistent_minibatch=0, fused_mlp=0, fused_loss=0, adv_mode=0,
-                vtrace_rho_clip=1.0, vtrace_c_clip=1.0) -> PpoConfig:
+                vtrace_rho_clip=1.0, vtrace_c_clip=1.0, optimizer=0, muon_lr=0.02,
+                muon_beta=0.95) -> PpoConfig:
     hn = (ctypes.c_int32 * _abi.MAX_HEADS)(*(list(heads) + [0] * (_abi.MAX_HEADS - len(heads))))
     return PpoConfig(obs_dim, h1, h2, act, len(heads), hn, n_gauss, precision, clip, vf_coef,
                      ent_coef, max_grad_norm, beta1, beta2, adam_eps, max_batch, max_minibatch,
                      max_epochs, persistent_minibatch, fused_mlp, fused_loss, adv_mode,
-                     vtrace_rho_clip, vtrace_c_clip)
+                     vtrace_rho_clip, vtrace_c_clip, optimizer, muon_lr, muon_beta)
 
 
 def config_from_workload(w, max_batch=None, max_minibatch=None, max_epochs=None,
                          persistent_minibatch=0, fused_mlp=0, fused_loss=0, adv_mode=0,
-                         vtrace_rho_clip=1.0, vtrace_c_clip=1.0) -> PpoConfig:
+                         vtrace_rho_clip=1.0, vtrace_c_clip=1.0, optimizer=0, muon_lr=0.02,
+                         muon_beta=0.95) -> PpoConfig:
     B = w.T * w.N
     return make_config(w.obs_dim, w.h1, w.h2, w.act, tuple(w.heads), w.n_gauss,
                        1 if w.precision == "bf16" else 0, w.clip, w.vf_coef, w.ent_coef,
@@ -76,7 +78,8 @@ def config_from_workload(w, max_batch=None, max_minibatch=None, max_epochs=None,
                        max_epochs=max_epochs or w.epochs,
                        persistent_minibatch=persistent_minibatch,
                        fused_mlp=fused_mlp, fused_loss=fused_loss, adv_mode=adv_mode,
-                       vtrace_rho_clip=vtrace_rho_clip, vtrace_c_clip=vtrace_c_clip)
+                       vtrace_rho_clip=vtrace_rho_clip, vtrace_c_clip=vtrace_c_clip,
+                       optimizer=optimizer, muon_lr=muon_lr, muon_beta=muon_beta)
 
 
 # ---- free functions -----------------------------------------------------------
@@ -210,6 +213,10 @@ def ppo_policy_act(ctx, obs, seed, draw0, act_disc, act_cont=None, logp=None, va
         _ptr(act_cont), _ptr(logp), _ptr(value), _stream(stream)), "ppo_policy_act")
 
 
+def ppo_muon_step(ctx, lr, grad_norm=None, stream=None) -> None:
+    _abi.check(_lib().ppo_muon_step(ctx, lr, _ptr(grad_norm), _stream(stream)), "ppo_muon_step")
+
+
 def ppo_adam_step(ctx, lr, grad_norm=None, stream=None) -> None:
     _abi.check(_lib().ppo_adam_step(ctx, lr, _ptr(grad_norm), _stream(stream)), "ppo_adam_step")
 
@@ -281,6 +288,9 @@ class Context:
 
     def policy_act(self, *a, **k):
         return ppo_policy_act(self.handle, *a, **k)
+
+    def muon_step(self, *a, **k):
+        return ppo_muon_step(self.handle, *a, **k)
 
     def adam_step(self, *a, **k):
         return ppo_adam_step(self.handle, *a, **k)

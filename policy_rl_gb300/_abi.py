@@ -19,11 +19,11 @@ SYMBOLS = (
     "ppo_params_changed", "ppo_get_step", "ppo_gae_workspace_bytes", "ppo_gae",
     "ppo_gae_noalloc", "ppo_segment_advantage_workspace_bytes", "ppo_segment_advantage",
     "ppo_perm_workspace_bytes", "ppo_minibatch_perm", "ppo_minibatch_loss_grad",
-    "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_adam_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
+    "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_adam_step", "ppo_muon_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
     "ppo_sync_status",
 )
-NUM_STAGES = 33
-NUM_KERNEL_STAGES = 24
+NUM_STAGES = 34
+NUM_KERNEL_STAGES = 25
 
 STATUS = {0: "PPO_OK", 1: "PPO_ERR_INVALID", 2: "PPO_ERR_ALIGN", 3: "PPO_ERR_CUDA",
           4: "PPO_ERR_UNSUPPORTED", 5: "PPO_ERR_TIMEOUT", 6: "PPO_ERR_NOMEM"}
@@ -47,7 +47,8 @@ class PpoConfig(ctypes.Structure):
         ("max_epochs", ctypes.c_int32), ("persistent_minibatch", ctypes.c_int32),
         ("fused_mlp", ctypes.c_int32), ("fused_loss", ctypes.c_int32),
         ("adv_mode", ctypes.c_int32), ("vtrace_rho_clip", ctypes.c_float),
-        ("vtrace_c_clip", ctypes.c_float),
+        ("vtrace_c_clip", ctypes.c_float), ("optimizer", ctypes.c_int32),
+        ("muon_lr", ctypes.c_float), ("muon_beta", ctypes.c_float),
     ]
 
 
@@ -95,6 +96,7 @@ def load(path: str = LIB_PATH):
                                            i32, _F, _F, _P, _P, _P, _P], ctypes.c_int),
         "ppo_policy_act": ([_P, _P, _I64, u32, ctypes.c_uint64, _P, _P, _P, _P, _P], ctypes.c_int),
         "ppo_adam_step": ([_P, _F, _P, _P], ctypes.c_int),
+        "ppo_muon_step": ([_P, _F, _P, _P], ctypes.c_int),
         "ppo_update": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F, _F,
                         u32, _P, _P], ctypes.c_int),
         "ppo_update_host": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F,

@@ -69,6 +69,10 @@ struct ppo_ctx {
   // per-minibatch advantages from fresh values (adv_mode 1, 2)
   float *vfresh = nullptr, *rfresh = nullptr;   // [mbmax] fresh values / ratios
   float* fpart = nullptr;                       // [kFreshMaxGrid][3] moment partials
+  // Muon (optimizer 1): momentum [P] and the Newton-Schulz workspaces
+  float* mom = nullptr;
+  float *ns_ws[3][4] = {};                      // per matrix: X0, X1 [r][k], A, B [r][r]
+  float *mpart = nullptr, *minv = nullptr;
   unsigned* fbar = nullptr;                     // grid-barrier counter of that kernel
   void* X = nullptr;
   // one epoch of minibatch rows gathered in permutation order (ppo_update)
@@ -155,6 +159,7 @@ ppo_status shape_from(const ppo_config* c, NetShape* s) {
   if (c->n_gauss < 0 || c->n_gauss > 4) return PPO_ERR_INVALID;
   if (c->precision != 0 && c->precision != 1) return PPO_ERR_INVALID;
   if (c->adv_mode < 0 || c->adv_mode > 2) return PPO_ERR_INVALID;
+  if (c->optimizer != 0 && c->optimizer != 1) return PPO_ERR_INVALID;
   std::memset(s, 0, sizeof(*s));
   s->D = c->obs_dim;
   s->H1 = c->h1;
@@ -586,6 +591,40 @@ AdamArgs make_adam_args(ppo_ctx* c, float lr, float* grad_norm_out, int nsq) {
   return a;
 }
 
+MuonArgs make_muon_args(ppo_ctx* c) {
+  const NetShape& s = c->s;
+  MuonArgs mu{};
+  const int64_t offs[3] = {s.oW1, s.oW2, s.oW3};
+  const int rows[3] = {s.H1, s.H2, s.C}, cols[3] = {s.D, s.H1, s.H2};
+  for (int m = 0; m < 3; ++m) {
+    MuonMat& w = mu.m[m];
+    w.p = c->params + offs[m];
+    w.g = c->grad + offs[m];
+    w.mom = c->mom + offs[m];
+    w.rows = rows[m];
+    w.cols = cols[m];
+    w.off = offs[m];
+    w.X0 = c->ns_ws[m][0];
+    w.X1 = c->ns_ws[m][1];
+    w.A = c->ns_ws[m][2];
+    w.B = c->ns_ws[m][3];
+  }
+  mu.beta = c->cfg.muon_beta;
+  mu.lr = c->cfg.muon_lr;
+  mu.mpart = c->mpart;
+  mu.inv = c->minv;
+  mu.s = s;
+  mu.sh = c->sh;
+  return mu;
+}
+
+ppo_status enqueue_muon(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t st, int nsq) {
+  if (!c->mom) return PPO_ERR_INVALID;   // context created with optimizer 0
+  const AdamArgs a = make_adam_args(c, lr, grad_norm_out, nsq);
+  PPO_CUDA(launch_muon(make_muon_args(c), a, st, &c->tr));
+  return PPO_OK;
+}
+
 ppo_status enqueue_adam(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t st,
                         int nsq = 0) {
   const AdamArgs a = make_adam_args(c, lr, grad_norm_out, nsq);
@@ -740,8 +779,15 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
         const AdamArgs aa = make_adam_args(c, lr, nullptr, 0);
         const FreshSpec fs{rew, done, boot, perm_e + (int64_t)k * ns, (int)T, ns, N, gamma,
                            lambda, c->cfg.adv_mode == 2};
-        TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, nullptr, nullptr, nullptr, B,
-                              mb, nullptr, st6, st, nullptr, &mr, &aa, &fs));
+        if (c->cfg.optimizer == 1) {
+          int nsq = 0;
+          TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, nullptr, nullptr, nullptr,
+                                B, mb, nullptr, st6, st, &nsq, &mr, nullptr, &fs));
+          TRY(enqueue_muon(c, lr, nullptr, st, nsq));
+        } else {
+          TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, nullptr, nullptr, nullptr,
+                                B, mb, nullptr, st6, st, nullptr, &mr, &aa, &fs));
+        }
       }
     }
     return PPO_OK;
@@ -786,8 +832,15 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
         const MbRows mr{static_cast<uint8_t*>(ep.X) + r0 * xrow, ep.act + r0 * NH,
                         ep.actc + r0 * G, ep.logp + r0, ep.adv + r0, ep.ret + r0};
         const AdamArgs aa = make_adam_args(c, lr, nullptr, 0);
-        TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
-                              c->advstats, st6, st, nullptr, &mr, &aa));
+        if (c->cfg.optimizer == 1) {
+          int nsq = 0;
+          TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
+                                c->advstats, st6, st, &nsq, &mr));
+          TRY(enqueue_muon(c, lr, nullptr, st, nsq));
+        } else {
+          TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
+                                c->advstats, st6, st, nullptr, &mr, &aa));
+        }
       }
     }
   }
@@ -847,7 +900,8 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   c->bf16 = cfg->precision == 1;
   // the persistent and fused-MLP kernels have no step between the forward
   // pass and the loss, where per-minibatch advantages are computed
-  c->use_mk = c->bf16 && cfg->persistent_minibatch != 0 && cfg->adv_mode == 0;
+  c->use_mk = c->bf16 && cfg->persistent_minibatch != 0 && cfg->adv_mode == 0 &&
+              cfg->optimizer == 0;   // the persistent kernel runs Adam itself
   c->use_fmlp = c->bf16 && !c->use_mk && cfg->fused_mlp != 0 && cfg->adv_mode == 0 &&
                 fmlp_supported(s);
   c->use_hl2 = c->bf16 && !c->use_mk && cfg->fused_loss != 0 && hl2_supported(s);
@@ -882,6 +936,19 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->fpart, 3 * (int64_t)kFreshMaxGrid);
   A(c->vfresh, cfg->max_minibatch);
   A(c->rfresh, cfg->max_minibatch);
+  if (cfg->optimizer == 1) {
+    A(c->mom, P);
+    A(c->mpart, 3 * kMuonPrepBlocks);
+    A(c->minv, 4);
+    const int64_t rows[3] = {s.H1, s.H2, s.C}, cols[3] = {s.D, s.H1, s.H2};
+    for (int m = 0; m < 3; ++m) {
+      const int64_t nr = std::min(rows[m], cols[m]), nk = std::max(rows[m], cols[m]);
+      A(c->ns_ws[m][0], nr * nk);
+      A(c->ns_ws[m][1], nr * nk);
+      A(c->ns_ws[m][2], nr * nr);
+      A(c->ns_ws[m][3], nr * nr);
+    }
+  }
   if (c->bf16) {
     c->sh.ld3t = 64;
     A(c->sh.W1s, (int64_t)s.H1 * s.Dp);
@@ -1205,6 +1272,13 @@ ppo_status ppo_segment_advantage(const float* rew, const float* done, const floa
   return PPO_OK;
 }
 
+ppo_status ppo_muon_step(ppo_ctx* c, float lr, float* grad_norm, cudaStream_t st) {
+  if (!c) return PPO_ERR_INVALID;
+  if (c->cfg.optimizer != 1) return PPO_ERR_INVALID;
+  if (grad_norm && !al16(grad_norm)) return PPO_ERR_ALIGN;
+  return enqueue_muon(c, lr, grad_norm, st, 0);
+}
+
 ppo_status ppo_adam_step(ppo_ctx* c, float lr, float* grad_norm, cudaStream_t st) {
   if (!c) return PPO_ERR_INVALID;
   if (grad_norm && !al16(grad_norm)) return PPO_ERR_ALIGN;
@@ -1317,7 +1391,7 @@ const char* ppo_stage_name(int32_t stage) {
       "perm_scatter", "gather", "fwd1_gemm", "fwd2_gemm", "head_loss_gemm", "dact2_gemm",
       "dact1_gemm", "wgrad_gemm", "grad_reduce", "grad_sqnorm", "adam", "weight_shadows",
       "minibatch_persistent", "fused_mlp", "grad_reduce_adam", "head_loss_dact2",
-      "fresh_advantages", "policy_act"};
+      "fresh_advantages", "policy_act", "muon"};
   static const char* phases[kMkPhases] = {
       "phase:gather", "phase:fwd1", "phase:fwd2", "phase:head_loss", "phase:dact2",
       "phase:dact1", "phase:wgrad", "phase:grad_reduce", "phase:adam"};

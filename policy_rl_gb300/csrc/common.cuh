@@ -215,7 +215,7 @@ enum Stage : int {
   ST_PACK = 0, ST_GAE, ST_GAE_FINALIZE, ST_GAE_NORMALIZE, ST_PERM_HIST, ST_PERM_SCAN,
   ST_PERM_SCATTER, ST_GATHER, ST_FWD1, ST_FWD2, ST_LOSS, ST_DACT2, ST_DACT1, ST_WGRAD,
   ST_REDUCE, ST_SQNORM, ST_ADAM, ST_SHADOW, ST_MINIBATCH, ST_FUSED_MLP, ST_REDUCE_ADAM,
-  ST_LOSS_DACT2, ST_FRESH_ADV, ST_POLICY_ACT, ST_COUNT
+  ST_LOSS_DACT2, ST_FRESH_ADV, ST_POLICY_ACT, ST_MUON, ST_COUNT
 };
 
 struct Trace {

@@ -150,8 +150,37 @@ struct AdamArgs {
   float* grad_norm_out;
   NetShape s;
   Shadows sh;
+  int vectors_only;        // 1: update only the biases and log-std (the weight
+                           // matrices take Muon's update instead)
 };
 cudaError_t launch_adam(const AdamArgs& a, cudaStream_t st, const Trace* tr = nullptr);
+
+// ---- Muon (optim.cu) ---------------------------------------------------------
+// One weight matrix p [rows][cols] of the flat parameter vector, its gradient
+// and momentum, and the Newton-Schulz workspaces (r = min(rows, cols),
+// k = max): X0, X1 [r][k] (ping-pong), A, B [r][r].
+struct MuonMat {
+  float* p;
+  const float* g;
+  float* mom;
+  int rows, cols;
+  int64_t off;         // flat index of p[0][0]
+  float *X0, *X1, *A, *B;
+};
+constexpr int kMuonPrepBlocks = 64;
+struct MuonArgs {
+  MuonMat m[3];        // W1, W2, W3
+  float beta, lr;      // momentum and Muon learning rate
+  float* mpart;        // [3][kMuonPrepBlocks] per-block sums of squares of u
+  float* inv;          // [3] 1 / (||u||_F + 1e-7)
+  NetShape s;
+  Shadows sh;
+};
+// Clip (coefficient from a's squared-norm partials, computed by launch_muon
+// when a.nsq == 0), Muon on the three weight matrices, Adam (a) on the
+// biases and log-std, bf16 shadows refreshed.
+cudaError_t launch_muon(const MuonArgs& mu, const AdamArgs& a, cudaStream_t st,
+                        const Trace* tr = nullptr);
 // Gradient assembly + clip + Adam in one cooperative launch (optim.cu); *bar
 // is a zeroed grid-barrier counter (cleared again by the kernel).
 cudaError_t reduce_adam_prepare();

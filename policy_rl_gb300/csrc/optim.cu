@@ -1,4 +1,4 @@
-// optim.cu -- gradient assembly, gradient-norm clip and fused Adam.
+// optim.cu -- gradient assembly, gradient-norm clip, fused Adam and Muon.
 //
 // reduce: sums the split-K weight-gradient partials and the per-CTA bias /
 // loss partials in a fixed order into the flat fp32 gradient (deterministic).
@@ -7,6 +7,8 @@
 // order by every Adam block; Adam then streams p, g, m, v once and
 // writes p, m, v and the bf16 weight shadows the tensor-core GEMMs read,
 // one coalesced grid-stride pass.
+#include <algorithm>
+
 #include "common.cuh"
 #include "gemm.h"
 #include "tc_ptx.cuh"
@@ -276,6 +278,19 @@ __device__ __forceinline__ void adam_body(const AdamArgs& a, int block, int nblo
     v = b2 * v0 + omb2 * g * g;
     p = p0 - lr * (m * ibc1) / (sqrtf(v * ibc2) + eps);
   };
+  if (a.vectors_only) {
+    // biases and log-std only: b1 [H1], b2 [H2], b3 [C] + log-std [G]
+    const int n1 = a.s.H1, n2 = a.s.H2, n3 = a.s.C + a.s.G;
+    for (int j = block * kAdamThreads + threadIdx.x; j < n1 + n2 + n3; j += stride) {
+      const int i = j < n1 ? (int)a.s.ob1 + j
+                           : (j < n1 + n2 ? (int)a.s.ob2 + (j - n1) : (int)a.s.ob3 + (j - n1 - n2));
+      float m, v, p;
+      step(a.g[i], a.m[i], a.v[i], a.p[i], m, v, p);
+      a.m[i] = m;
+      a.v[i] = v;
+      a.p[i] = p;
+    }
+  } else {
   const float4* __restrict__ G4 = reinterpret_cast<const float4*>(a.g);
   float4* __restrict__ M4 = reinterpret_cast<float4*>(a.m);
   float4* __restrict__ V4 = reinterpret_cast<float4*>(a.v);
@@ -304,6 +319,7 @@ __device__ __forceinline__ void adam_body(const AdamArgs& a, int block, int nblo
     a.p[i] = p;
     if (shadows) write_shadow(a.s, a.sh, i, p);
   }
+  }
   // the last block to finish publishes the new step count (every block has
   // read the old one before its arrival)
   __syncthreads();
@@ -328,6 +344,177 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
   pdl_wait();
   pdl_trigger();
   adam_body(a, blockIdx.x, gridDim.x, nullptr);
+}
+
+// ---- Muon ("Muon: An optimizer for hidden layers in neural networks") -------
+// Newton-Schulz on X (r x k, r <= k): five times A = X X^T, B = b A + c A A,
+// X = a X + B X.  Each product is one launch over the tiles of all three
+// matrices (fp32 CUDA cores: the matrices are at most 512 x 1408 and the
+// products are latency-bound).
+constexpr float kNsA = 3.4445f, kNsB = -4.7750f, kNsC = 2.0315f;
+constexpr int kNsTile = 32;
+constexpr int kNsThreads = 256;
+
+// Momentum update of the matrices and the Frobenius partials of u:
+//   g' = coef g (clip), mom = beta mom + g', u = g' + beta mom,
+// u stored as X0 [r][k] (transposed when the matrix has more rows than columns).
+__global__ void __launch_bounds__(kAdamThreads) muon_prep_kernel(MuonArgs mu, AdamArgs a) {
+  pdl_wait();
+  __shared__ float s_coef;
+  __shared__ double s_ws[kAdamThreads / kWarp];
+  {
+    double ss = 0.0;
+    for (int b = threadIdx.x; b < a.nsq; b += kAdamThreads) ss += a.sq_part[b];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (threadIdx.x % kWarp == 0) s_ws[threadIdx.x / kWarp] = ss;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {   // the same coefficient adam_body computes
+    double ss = 0.0;
+    for (int w = 0; w < kAdamThreads / kWarp; ++w) ss += s_ws[w];
+    const float norm = sqrtf((float)ss);
+    s_coef = a.max_norm > 0.f ? fminf(1.f, a.max_norm / (norm + 1e-6f)) : 1.f;
+  }
+  __syncthreads();
+  pdl_trigger();
+  const float coef = s_coef;
+  __shared__ float s_red[3][kAdamThreads / kWarp];
+  for (int mtx = 0; mtx < 3; ++mtx) {
+    const MuonMat& m = mu.m[mtx];
+    const int n = m.rows * m.cols;
+    const bool tr = m.rows > m.cols;
+    const int k = tr ? m.rows : m.cols;
+    float acc = 0.f;
+    for (int i = blockIdx.x * kAdamThreads + threadIdx.x; i < n; i += gridDim.x * kAdamThreads) {
+      const float g = m.g[i] * coef;
+      const float mo = mu.beta * m.mom[i] + g;
+      m.mom[i] = mo;
+      const float u = g + mu.beta * mo;
+      const int row = i / m.cols, col = i - row * m.cols;
+      m.X0[tr ? (int64_t)col * k + row : (int64_t)row * k + col] = u;
+      acc = fmaf(u, u, acc);
+    }
+    acc = warp_sum(acc);
+    if (threadIdx.x % kWarp == 0) s_red[mtx][threadIdx.x / kWarp] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x < 3) {
+    float t = 0.f;
+    for (int w = 0; w < kAdamThreads / kWarp; ++w) t += s_red[threadIdx.x][w];
+    mu.mpart[threadIdx.x * kMuonPrepBlocks + blockIdx.x] = t;
+  }
+}
+
+// inv[m] = 1 / (||u_m||_F + 1e-7), partials summed in block order.
+__global__ void muon_norm_kernel(MuonArgs mu) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x < 3) {
+    float t = 0.f;
+    for (int b = 0; b < kMuonPrepBlocks; ++b) t += mu.mpart[threadIdx.x * kMuonPrepBlocks + b];
+    mu.inv[threadIdx.x] = 1.f / (sqrtf(t) + 1e-7f);
+  }
+}
+
+// One Newton-Schulz product over the tiles of all three matrices:
+//   stage 0: A = s^2 X X^T;  stage 1: B = b A + c A A;  stage 2: Xo = a s X + B (s X),
+// with s = inv[m] on the first iteration (X = X0 unnormalised) and 1 after.
+struct NsStage {
+  int stage;
+  int first;                 // first iteration: scale X by inv[m]
+  const float* src[3];       // X of this iteration per matrix
+  float* dst[3];             // Xo (stage 2)
+  int tiles[4];              // prefix sums of the tile counts over the matrices
+};
+
+__global__ void __launch_bounds__(kNsThreads) ns_stage_kernel(MuonArgs mu, NsStage st) {
+  pdl_wait();
+  __shared__ float Ps[kNsTile][kNsTile + 1], Qs[kNsTile][kNsTile + 1];
+  const int b = blockIdx.x;
+  const int mtx = b < st.tiles[1] ? 0 : (b < st.tiles[2] ? 1 : 2);
+  const MuonMat& m = mu.m[mtx];
+  const int r = m.rows < m.cols ? m.rows : m.cols;
+  const int kk = m.rows < m.cols ? m.cols : m.rows;
+  const float* X = st.src[mtx];
+  const float s = st.first ? mu.inv[mtx] : 1.f;
+  // output [Mo][No], reduction length K, operands P(i, q) and Q(j, q)
+  int No, K;
+  const float *P, *Q, *D = nullptr;
+  int64_t pi, pq, qj, qq;
+  float alpha = 0.f, beta;
+  float* out;
+  if (st.stage == 0) {          // A[i][j] = sum_q X[i][q] X[j][q]
+    No = r; K = kk; P = X; Q = X; pi = kk; pq = 1; qj = kk; qq = 1; beta = s * s; out = m.A;
+  } else if (st.stage == 1) {   // B[i][j] = b A[i][j] + c sum_q A[i][q] A[q][j] (A symmetric)
+    No = r; K = r; P = m.A; Q = m.A; pi = r; pq = 1; qj = r; qq = 1;
+    D = m.A; alpha = kNsB; beta = kNsC; out = m.B;
+  } else {                      // Xo[i][j] = a s X[i][j] + s sum_q B[i][q] X[q][j]
+    No = kk; K = r; P = m.B; Q = X; pi = r; pq = 1; qj = 1; qq = kk;
+    D = X; alpha = kNsA * s; beta = s; out = st.dst[mtx];
+  }
+  const int tn = (No + kNsTile - 1) / kNsTile;
+  const int t = b - st.tiles[mtx];
+  const int i0 = (t / tn) * kNsTile, j0 = (t % tn) * kNsTile;
+  const int Mo = r;
+  // each thread: a 2 x 2 block of the 32 x 32 tile
+  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  for (int q0 = 0; q0 < K; q0 += kNsTile) {
+    for (int e = threadIdx.x; e < kNsTile * kNsTile; e += kNsThreads) {
+      const int rr = e / kNsTile, qc = e % kNsTile;
+      const int q = q0 + qc;
+      Ps[rr][qc] = (i0 + rr < Mo && q < K) ? P[(int64_t)(i0 + rr) * pi + (int64_t)q * pq] : 0.f;
+      Qs[rr][qc] = (j0 + rr < No && q < K) ? Q[(int64_t)(j0 + rr) * qj + (int64_t)q * qq] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int qc = 0; qc < kNsTile; ++qc) {
+      const float p0 = Ps[2 * ty][qc], p1 = Ps[2 * ty + 1][qc];
+      const float q0v = Qs[2 * tx][qc], q1v = Qs[2 * tx + 1][qc];
+      acc[0][0] = fmaf(p0, q0v, acc[0][0]);
+      acc[0][1] = fmaf(p0, q1v, acc[0][1]);
+      acc[1][0] = fmaf(p1, q0v, acc[1][0]);
+      acc[1][1] = fmaf(p1, q1v, acc[1][1]);
+    }
+    __syncthreads();
+  }
+  pdl_trigger();
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+      const int i = i0 + 2 * ty + u, j = j0 + 2 * tx + v;
+      if (i < Mo && j < No) {
+        float y = beta * acc[u][v];
+        if (D) y = fmaf(alpha, D[(int64_t)i * No + j], y);
+        out[(int64_t)i * No + j] = y;
+      }
+    }
+}
+
+// W -= lr sqrt(max(1, rows/cols)) X (transposed back), bf16 shadows refreshed.
+// Five iterations ping-pong X0 -> X1 -> X0 -> X1 -> X0 -> X1: the result is X1.
+__global__ void __launch_bounds__(kAdamThreads) muon_apply_kernel(MuonArgs mu) {
+  pdl_wait();
+  pdl_trigger();
+  const bool shadows = mu.sh.W1s != nullptr;
+  for (int mtx = 0; mtx < 3; ++mtx) {
+    const MuonMat& m = mu.m[mtx];
+    const int n = m.rows * m.cols;
+    const bool tr = m.rows > m.cols;
+    const int k = tr ? m.rows : m.cols;
+    const float ratio = (float)m.rows / (float)m.cols;
+    const float step = mu.lr * sqrtf(ratio > 1.f ? ratio : 1.f);
+    const float* X = m.X1;
+    for (int i = blockIdx.x * kAdamThreads + threadIdx.x; i < n; i += gridDim.x * kAdamThreads) {
+      const int row = i / m.cols, col = i - row * m.cols;
+      const float x = X[tr ? (int64_t)col * k + row : (int64_t)row * k + col];
+      const float p = m.p[i] - step * x;
+      m.p[i] = p;
+      if (shadows) write_shadow(mu.s, mu.sh, (int)(m.off + i), p);
+    }
+  }
 }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
@@ -451,6 +638,62 @@ cudaError_t launch_adam(const AdamArgs& a0, cudaStream_t st, const Trace* tr) {
                              dim3(kAdamThreads), 0, st, a);
   if (e != cudaSuccess) return e;
   if (tr) tr->mark(ST_ADAM, st);
+  return cudaSuccess;
+}
+
+cudaError_t launch_muon(const MuonArgs& mu, const AdamArgs& a0, cudaStream_t st,
+                        const Trace* tr) {
+  AdamArgs a = a0;
+  if (a.nsq <= 0) {   // no squared-norm partials supplied: compute them
+    const int nb = blocks_for((a.P + 3) / 4, kNormThreads, kNormBlocks);
+    cudaError_t e = launch_pdl(sqnorm_kernel, dim3(nb), dim3(kNormThreads), 0, st, a.g, a.P,
+                               const_cast<double*>(a.sq_part));
+    if (e != cudaSuccess) return e;
+    if (tr) tr->mark(ST_SQNORM, st);
+    a.nsq = nb;
+  }
+  cudaError_t e = launch_pdl(muon_prep_kernel, dim3(kMuonPrepBlocks), dim3(kAdamThreads), 0, st,
+                             mu, a);
+  if (e != cudaSuccess) return e;
+  if (tr) tr->mark(ST_MUON, st);
+  // Adam on the biases and log-std; it also advances the step counter
+  a.vectors_only = 1;
+  e = launch_pdl(adam_kernel, dim3(4), dim3(kAdamThreads), 0, st, a);
+  if (e != cudaSuccess) return e;
+  if (tr) tr->mark(ST_ADAM, st);
+  e = launch_pdl(muon_norm_kernel, dim3(1), dim3(32), 0, st, mu);
+  if (e != cudaSuccess) return e;
+  if (tr) tr->mark(ST_MUON, st);
+  NsStage sg{};
+  int ntile[3][3];   // [stage][matrix]
+  for (int m = 0; m < 3; ++m) {
+    const int r = std::min(mu.m[m].rows, mu.m[m].cols), k = std::max(mu.m[m].rows, mu.m[m].cols);
+    const int tr_ = (r + kNsTile - 1) / kNsTile, tk = (k + kNsTile - 1) / kNsTile;
+    ntile[0][m] = tr_ * tr_;
+    ntile[1][m] = tr_ * tr_;
+    ntile[2][m] = tr_ * tk;
+  }
+  const float* cur[3] = {mu.m[0].X0, mu.m[1].X0, mu.m[2].X0};
+  for (int it = 0; it < 5; ++it) {
+    for (int stage = 0; stage < 3; ++stage) {
+      sg.stage = stage;
+      sg.first = it == 0;
+      sg.tiles[0] = 0;
+      for (int m = 0; m < 3; ++m) {
+        sg.src[m] = cur[m];
+        sg.dst[m] = cur[m] == mu.m[m].X0 ? mu.m[m].X1 : mu.m[m].X0;
+        sg.tiles[m + 1] = sg.tiles[m] + ntile[stage][m];
+      }
+      e = launch_pdl(ns_stage_kernel, dim3(sg.tiles[3]), dim3(kNsThreads), 0, st, mu, sg);
+      if (e != cudaSuccess) return e;
+      if (tr) tr->mark(ST_MUON, st);
+    }
+    for (int m = 0; m < 3; ++m) cur[m] = sg.dst[m];
+  }
+  e = launch_pdl(muon_apply_kernel, dim3(blocks_for(mu.m[1].rows * mu.m[1].cols, kAdamThreads, 152)),
+                 dim3(kAdamThreads), 0, st, mu);
+  if (e != cudaSuccess) return e;
+  if (tr) tr->mark(ST_MUON, st);
   return cudaSuccess;
 }
 
