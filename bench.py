@@ -175,6 +175,8 @@ def _stage_work(stage: str, w, mb: int):
 # --advantages: 0 GAE once per update over the rollout; 1 per minibatch of
 # environment segments from fresh values (GAE); 2 the same with V-trace
 ADV_MODES = {"global": 0, "fresh_gae": 1, "vtrace": 2}
+# --optimizer: Adam on every parameter (default) or Muon on the weight matrices
+OPTIMIZERS = {"adam": 0, "muon": 1}
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
@@ -192,10 +194,36 @@ NCU_TRAFFIC = {
 }
 
 
+# fp32 FMA peak of the CUDA cores (no measured figure exists for it):
+# 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz (the recipe's unit counts and
+# maximum SM clock)
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def _muon_step_flops(w):
+    """Newton-Schulz FLOPs of one Muon step: five iterations of X X^T
+    (2 r^2 k), A A (2 r^3) and B X (2 r^2 k) per weight matrix."""
+    D, H1, H2, C = w.obs_dim, w.h1, w.h2, w.out_cols
+    tot = 0
+    for rows, cols in ((H1, D), (H2, H1), (C, H2)):
+        r, k = min(rows, cols), max(rows, cols)
+        tot += 5 * (4 * r * r * k + 2 * r ** 3)
+    return tot
+
+
 def _roofline(stage, w, mb, ms_total, launches, hbm_peak, tf_peak, peak_src):
     """Roofline entry of one stage: bound = the larger of its tensor-time and
     HBM-time floors at the measured peaks; achieved = algorithmic work per
     launch / mean launch duration."""
+    if stage == "muon":   # 18 launches per optimizer step, fp32 CUDA-core products
+        steps = launches / 18
+        achieved = _muon_step_flops(w) * steps / (ms_total / 1e3) / 1e12
+        return {"bound": "alu", "kernel": stage, "achieved": round(achieved, 3),
+                "peak": round(FP32_ALU_TFLOPS, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / FP32_ALU_TFLOPS, 4), "traffic": None,
+                "peak_kind": "fp32 FMA, derived (152 SMs x 128 lanes x 2 x 2.07 GHz)",
+                "per_launch_us": round(ms_total / launches * 1e3, 2),
+                "algorithmic_per_launch": {"flop": _muon_step_flops(w) / 18, "bytes": None}}
     work = _stage_work(stage, w, mb)
     if work is None:
         return None
@@ -235,7 +263,8 @@ def run_ours(args, world, rank, local):
     big = w.B * w.obs_dim > 2e8
     ro = synth.rollout(w, seed=rank, with_obs=not big)
     p0 = synth.init_params(w)
-    ctx = P.Context(P.config_from_workload(w, adv_mode=ADV_MODES[args.advantages]), p0)
+    ctx = P.Context(P.config_from_workload(w, adv_mode=ADV_MODES[args.advantages],
+                                           optimizer=OPTIMIZERS[args.optimizer]), p0)
     stream = torch.cuda.Stream()
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
     if big:
@@ -348,7 +377,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
-        cpu = _cpu_baseline(w, ADV_MODES[args.advantages])
+        cpu = _cpu_baseline(w, ADV_MODES[args.advantages], OPTIMIZERS[args.optimizer])
 
     out = {
         "metric": "PPO update samples/s (GAE+clipped loss fwd/bwd+Adam); GAE GB/s vs HBM peak",
@@ -357,7 +386,7 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded mulberry32 rollout with the workload's shapes and value "
                 "distributions; random-init weights)",
-        "config": {"workload": _workload_str(w, args.advantages),
+        "config": {"workload": _workload_str(w, args.advantages, args.optimizer),
                    "global_batch": world * B, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (256 MB write)",
                    "timing": "CUDA events per update on the launching stream, mean over steps"},
@@ -482,7 +511,7 @@ def _cpu_sample(w):
     return w.scaled(T=w.T, N=n, minibatches=w.minibatches, epochs=w.epochs)
 
 
-def _oracle_update(ws, seed=0, adv_mode=0):
+def _oracle_update(ws, seed=0, adv_mode=0, optimizer=0):
     import oracle
     from policy_rl_gb300 import synth
     ro = synth.rollout(ws, seed=seed)
@@ -490,23 +519,23 @@ def _oracle_update(ws, seed=0, adv_mode=0):
     net = oracle.Net(ws.obs_dim, ws.h1, ws.h2, ws.act, ws.heads, ws.n_gauss)
     hp = oracle.Hyper(gamma=ws.gamma, lam=ws.lam, clip=ws.clip, vf_coef=ws.vf_coef,
                       ent_coef=ws.ent_coef, lr=ws.lr, max_grad_norm=ws.max_grad_norm, seed=1234,
-                      adv_mode=adv_mode)
+                      adv_mode=adv_mode, optimizer=optimizer)
     t0 = time.perf_counter()
     oracle.update(net, hp, ws.T, ws.N, ws.epochs, ws.minibatches, ro.obs, ro.act_disc,
                   ro.act_cont, ro.logp_old, ro.val, ro.rew, ro.done, ro.boot, p0)
     return time.perf_counter() - t0
 
 
-def _cpu_baseline(w, adv_mode=0):
+def _cpu_baseline(w, adv_mode=0, optimizer=0):
     ws = _cpu_sample(w)
-    t = _oracle_update(ws, adv_mode=adv_mode)
+    t = _oracle_update(ws, adv_mode=adv_mode, optimizer=optimizer)
     return {"value": round(ws.B / t, 1), "unit": "samples/s", "cores": 1, "kind": "oracle",
             "sample": f"whole update of a T={ws.T} x N={ws.N} slice ({ws.B} samples) of the "
                       f"{w.name} workload, {ws.epochs} epochs x {ws.minibatches} minibatches; "
                       f"plain C fp64, single thread ({t:.2f} s)"}
 
 
-def _workload_str(w, advantages="global") -> str:
+def _workload_str(w, advantages="global", optimizer="adam") -> str:
     mb = w.B // w.minibatches
     s = (f"{w.name}: T={w.T} N={w.N} obs={w.obs_dim} MLP {w.obs_dim}-{w.h1}-{w.h2} "
          f"{'tanh' if w.act == 0 else 'relu'} heads {list(w.heads)}+V epochs={w.epochs} "
@@ -514,6 +543,8 @@ def _workload_str(w, advantages="global") -> str:
     if advantages != "global":
         s += (f" advantages={advantages} (per minibatch of {w.N // w.minibatches} env segments, "
               f"from fresh values)")
+    if optimizer != "adam":
+        s += f" optimizer={optimizer}"
     return s
 
 
@@ -524,16 +555,18 @@ def run_reference(args, world, rank):
     from policy_rl_gb300 import synth
     w = synth.WORKLOADS[args.workload]
     am = ADV_MODES[args.advantages]
+    om = OPTIMIZERS[args.optimizer]
     n = max(8, w.minibatches)    # powers of two: whole env segments per minibatch
     probe = w.scaled(T=16, N=n, minibatches=w.minibatches, epochs=w.epochs)
-    per_sample = _oracle_update(probe, adv_mode=am) / probe.B
+    per_sample = _oracle_update(probe, adv_mode=am, optimizer=om) / probe.B
     budget = 120.0 / (args.steps + args.warmup)
     while n < 1024 and 16 * (2 * n) * per_sample <= budget:
         n *= 2
     ws = w.scaled(T=16, N=n, minibatches=w.minibatches, epochs=w.epochs)
     for i in range(args.warmup):
-        _oracle_update(ws, seed=i, adv_mode=am)
-    times = [_oracle_update(ws, seed=args.warmup + i, adv_mode=am) for i in range(args.steps)]
+        _oracle_update(ws, seed=i, adv_mode=am, optimizer=om)
+    times = [_oracle_update(ws, seed=args.warmup + i, adv_mode=am, optimizer=om)
+             for i in range(args.steps)]
     t = float(np.mean(times))
     v = ws.B / t
     sample = (f"whole update of a T={ws.T} x N={ws.N} slice ({ws.B} samples) of the {w.name} "
@@ -545,7 +578,8 @@ def run_reference(args, world, rank):
         "value": round(v, 2), "unit": "samples/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": _workload_str(w, args.advantages), "global_batch": world * w.B,
+        "config": {"workload": _workload_str(w, args.advantages, args.optimizer),
+                   "global_batch": world * w.B,
                    "parallelism": "host cores (rank 0)",
                    "sample": f"oracle on a {ws.B}-sample slice per step (T={ws.T} x N={ws.N})"},
         "cpu_baseline": {"value": round(v, 2), "unit": "samples/s", "cores": 1,
@@ -566,6 +600,8 @@ def main():
     ap.add_argument("--advantages", default="global", choices=sorted(ADV_MODES),
                     help="global: GAE once per update (default); fresh_gae / vtrace: per "
                          "minibatch of env segments from fresh values")
+    ap.add_argument("--optimizer", default="adam", choices=sorted(OPTIMIZERS),
+                    help="adam (default) or muon (Newton-Schulz on the weight matrices)")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     ap.add_argument("--skip-gae-stress", action="store_true")
     ap.add_argument("--skip-adam-stress", action="store_true")

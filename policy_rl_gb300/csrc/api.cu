@@ -1419,7 +1419,8 @@ ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
   TRY(check_update_args(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
                         minibatches, stats));
   if (!h_stage_ms || !h_stage_launches || st == nullptr) return PPO_ERR_INVALID;
-  const size_t need = 8 + 3 * 4 + 20 * (size_t)epochs * minibatches;
+  // launches per minibatch: at most 7 per-stage kernels + 20 of a Muon step
+  const size_t need = 8 + 3 * 4 + 40 * (size_t)epochs * minibatches;
   while (c->prof_events.size() < need) {
     cudaEvent_t e;
     PPO_CUDA(cudaEventCreate(&e));

@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(AdamArgs a) {
 // products are latency-bound).
 constexpr float kNsA = 3.4445f, kNsB = -4.7750f, kNsC = 2.0315f;
 constexpr int kNsTile = 32;
+constexpr int kNsChunk = 128;   // reduction elements staged per round (all loads in flight)
 constexpr int kNsThreads = 256;
 
 // Momentum update of the matrices and the Frobenius partials of u:
@@ -430,7 +431,7 @@ struct NsStage {
 
 __global__ void __launch_bounds__(kNsThreads) ns_stage_kernel(MuonArgs mu, NsStage st) {
   pdl_wait();
-  __shared__ float Ps[kNsTile][kNsTile + 1], Qs[kNsTile][kNsTile + 1];
+  __shared__ float Ps[kNsTile][kNsChunk + 1], Qs[kNsTile][kNsChunk + 1];
   const int b = blockIdx.x;
   const int mtx = b < st.tiles[1] ? 0 : (b < st.tiles[2] ? 1 : 2);
   const MuonMat& m = mu.m[mtx];
@@ -460,16 +461,26 @@ __global__ void __launch_bounds__(kNsThreads) ns_stage_kernel(MuonArgs mu, NsSta
   // each thread: a 2 x 2 block of the 32 x 32 tile
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
   float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-  for (int q0 = 0; q0 < K; q0 += kNsTile) {
-    for (int e = threadIdx.x; e < kNsTile * kNsTile; e += kNsThreads) {
-      const int rr = e / kNsTile, qc = e % kNsTile;
+  constexpr int kPer = kNsTile * kNsChunk / kNsThreads;   // elements per thread per operand
+  for (int q0 = 0; q0 < K; q0 += kNsChunk) {
+    float pv[kPer], qv[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {   // every load of the round before any store
+      const int e = threadIdx.x + u * kNsThreads;
+      const int rr = e / kNsChunk, qc = e % kNsChunk;
       const int q = q0 + qc;
-      Ps[rr][qc] = (i0 + rr < Mo && q < K) ? P[(int64_t)(i0 + rr) * pi + (int64_t)q * pq] : 0.f;
-      Qs[rr][qc] = (j0 + rr < No && q < K) ? Q[(int64_t)(j0 + rr) * qj + (int64_t)q * qq] : 0.f;
+      pv[u] = (i0 + rr < Mo && q < K) ? P[(int64_t)(i0 + rr) * pi + (int64_t)q * pq] : 0.f;
+      qv[u] = (j0 + rr < No && q < K) ? Q[(int64_t)(j0 + rr) * qj + (int64_t)q * qq] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = threadIdx.x + u * kNsThreads;
+      Ps[e / kNsChunk][e % kNsChunk] = pv[u];
+      Qs[e / kNsChunk][e % kNsChunk] = qv[u];
     }
     __syncthreads();
 #pragma unroll 8
-    for (int qc = 0; qc < kNsTile; ++qc) {
+    for (int qc = 0; qc < kNsChunk; ++qc) {
       const float p0 = Ps[2 * ty][qc], p1 = Ps[2 * ty + 1][qc];
       const float q0v = Qs[2 * tx][qc], q1v = Qs[2 * tx + 1][qc];
       acc[0][0] = fmaf(p0, q0v, acc[0][0]);
