@@ -440,6 +440,27 @@ def _gae_stress(stream, hbm_peak):
             gbs = bpe * T * N / t / 1e9
             res[name] = {"ms": round(t * 1e3, 4), "GB_per_s": round(gbs, 1),
                          "frac_of_hbm": round(gbs / hbm_peak, 4), "bytes_per_elem": bpe}
+        # the same scan through ppo_segment_advantage (all N environments as
+        # segments, values given, V-trace ratios off), with moments + normalise
+        envs = torch.arange(N, dtype=torch.int32, device="cuda")
+        swork = torch.empty(P.ppo_segment_advantage_workspace_bytes(), dtype=torch.uint8,
+                            device="cuda")
+        for _ in range(3):
+            P.ppo_segment_advantage(rew, done, boot, envs, val, None, 0.997, 0.95, adv, ret,
+                                    adv_norm=advn, stats=st, work=swork, stream=stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(10)]
+        for s0, e0 in evs:
+            s0.record(stream)
+            P.ppo_segment_advantage(rew, done, boot, envs, val, None, 0.997, 0.95, adv, ret,
+                                    adv_norm=advn, stats=st, work=swork, stream=stream)
+            e0.record(stream)
+        stream.synchronize()
+        t = float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
+        gbs = 28 * T * N / t / 1e9
+        res["segments+moments+normalise"] = {"ms": round(t * 1e3, 4), "GB_per_s": round(gbs, 1),
+                                             "frac_of_hbm": round(gbs / hbm_peak, 4),
+                                             "bytes_per_elem": 28}
     return {"workload": "gae_stress: T=1024 N=65536 fp32 (inputs > L2)", **res}
 
 

@@ -19,7 +19,9 @@
 //    final merge grow with the block count).  GAE needs only the value column (NCOL = 1); V-trace needs
 //    every column to form the log-probability of the taken action and the
 //    ratio pi/mu = exp(logp - logp_old).
-//  B the segment scan: one warp per segment; the recursion is affine in
+//  B the segment scan (from 16,384 segments: one thread per segment, a
+//    coalesced backward walk like the GAE kernel); otherwise one warp per
+//    segment, for latency: the recursion is affine in
 //    A_{t+1} (A_t = b_t + a_t A_{t+1}), so each lane composes the maps of a
 //    run of kRun steps, a suffix scan over the lanes composes the runs, and
 //    each lane then replays its steps from the exact incoming value.  Windows
@@ -225,6 +227,56 @@ __device__ __forceinline__ void seg_prefetch(const FreshAdvArgs& a, int64_t e, i
   }
 }
 
+// Many segments (a whole rollout's worth): one thread per segment walks the
+// horizon backwards like the GAE kernel, so that a warp reads 32 consecutive
+// segments of one time step (coalesced on the [T][ns] arrays, and on the
+// [T][N] rollout arrays when the segments are consecutive environments).
+constexpr int kSegPerThreadFrom = 16384;
+constexpr int kSegU = 16;   // steps whose loads are in flight together
+
+__device__ __forceinline__ void thread_segment(const FreshAdvArgs& a, int j, LaneSums& acc) {
+  const int T = a.T, ns = a.ns;
+  const int64_t N = a.N;
+  int64_t e = __ldg(a.envs + j);
+  e = e < 0 ? 0 : (e >= N ? N - 1 : e);
+  const bool vtrace = a.ratio != nullptr;
+  float A = 0.f;
+  float v_next = __ldg(a.boot + e);
+  for (int t_hi = T; t_hi > 0; t_hi -= kSegU) {
+    float r[kSegU], d[kSegU], v[kSegU], rho[kSegU];
+#pragma unroll
+    for (int q = 0; q < kSegU; ++q) {
+      const int t = t_hi - 1 - q;
+      r[q] = d[q] = v[q] = 0.f;
+      rho[q] = 1.f;
+      if (t >= 0) {
+        r[q] = __ldcs(a.rew + (int64_t)t * N + e);
+        d[q] = __ldcs(a.done + (int64_t)t * N + e);
+        v[q] = a.val[(int64_t)t * ns + j];
+        if (vtrace) rho[q] = a.ratio[(int64_t)t * ns + j];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kSegU; ++q) {
+      const int t = t_hi - 1 - q;
+      if (t >= 0) {
+        const float alive = d[q] != 0.f ? 0.f : 1.f;
+        float w = 1.f, c = a.lambda;
+        if (vtrace) {
+          w = fminf(a.rho_clip, rho[q]);
+          c = a.lambda * fminf(a.c_clip, rho[q]);
+        }
+        A = w * (r[q] + a.gamma * alive * v_next - v[q]) + a.gamma * alive * c * A;
+        const int64_t k = (int64_t)t * ns + j;
+        a.adv[k] = A;
+        a.ret[k] = A + v[q];
+        acc.add(A);
+        v_next = v[q];
+      }
+    }
+  }
+}
+
 // Phase B for segment j: the scan over the horizon, accumulating this lane's
 // advantages into its sums.  pre: the segment's prefetched last window.
 __device__ __forceinline__ void fresh_segment(const FreshAdvArgs& a, int j, int lane,
@@ -327,7 +379,8 @@ fresh_adv_kernel(FreshAdvArgs a) {
   const int j0 = blockIdx.x * kFreshWarps + warp;
   // the first segment's rollout inputs: its environment index now, the rest
   // after phase A, so that their latency hides behind phase A and the barrier
-  const int64_t e0 = j0 < a.ns ? (int64_t)__ldg(a.envs + j0) : 0;
+  const bool warp_path = a.ns < kSegPerThreadFrom;
+  const int64_t e0 = warp_path && j0 < a.ns ? (int64_t)__ldg(a.envs + j0) : 0;
   SegPre pre;
   if (a.head) {
     const HeadSrc hs{a.H2, a.h2_bf16, a.W3, a.b3, a.s.H2, a.s.C};
@@ -336,15 +389,20 @@ fresh_adv_kernel(FreshAdvArgs a) {
     for (int64_t row = (int64_t)blockIdx.x * kFreshThreads + threadIdx.x; row < rows;
          row += stride)
       eval_row<NCOL>(a, hs, w3t, row);
-    if (j0 < a.ns) seg_prefetch(a, e0, lane, pre);
+    if (warp_path && j0 < a.ns) seg_prefetch(a, e0, lane, pre);
     if (!grid_barrier(a.bar, ++k, a.err, a.timeout_ns, &s_abort)) return;
-  } else if (j0 < a.ns) {
+  } else if (warp_path && j0 < a.ns) {
     seg_prefetch(a, e0, lane, pre);
   }
   LaneSums acc{0.f, 0.f, 0.f, 0.f};
-  for (int j = j0; j < a.ns; j += nwarps) {
-    if (j != j0) seg_prefetch(a, __ldg(a.envs + j), lane, pre);
-    fresh_segment(a, j, lane, pre, acc);
+  if (a.ns >= kSegPerThreadFrom) {
+    for (int j = blockIdx.x * kFreshThreads + threadIdx.x; j < a.ns; j += gridDim.x * kFreshThreads)
+      thread_segment(a, j, acc);
+  } else {
+    for (int j = j0; j < a.ns; j += nwarps) {
+      if (j != j0) seg_prefetch(a, __ldg(a.envs + j), lane, pre);
+      fresh_segment(a, j, lane, pre, acc);
+    }
   }
   const MomF wm = mom_warp(acc.moments());
   if (lane == 0) s_mom[warp] = wm;
@@ -443,7 +501,8 @@ cudaError_t launch_fresh_adv(const FreshAdvArgs& a, int num_sms, cudaStream_t st
   const int64_t rows = (int64_t)a.T * a.ns;
   // enough blocks for one row per thread in phase A (or for the normalisation)
   // and one warp per segment in phase B
-  int64_t want = (a.ns + kFreshWarps - 1) / kFreshWarps;
+  int64_t want = a.ns >= kSegPerThreadFrom ? (a.ns + kFreshThreads - 1) / kFreshThreads
+                                           : (a.ns + kFreshWarps - 1) / kFreshWarps;
   const int64_t per_rows = a.head ? (rows + kFreshThreads - 1) / kFreshThreads
                                   : (rows + 8 * kFreshThreads - 1) / (8 * kFreshThreads);
   if (per_rows > want) want = per_rows;

@@ -63,6 +63,8 @@ CASES = [
     (1, 5, 3, True, (1.0, 1.0), 0.3),             # one step
     (200, 40, 17, True, (2.0, 0.5), 1.0),         # every step terminal
     (129, 33, 33, True, (1.0, 1.0), 0.0),         # a window of a single step
+    (64, 32768, 32768, True, (1.0, 1.0), 0.01),   # thread-per-segment scan (>= 16,384)
+    (37, 20000, 16384, False, (1.0, 1.0), 0.05),  # its threshold, ragged T
 ]
 
 
