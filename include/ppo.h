@@ -338,6 +338,10 @@ ppo_status ppo_muon_step(ppo_ctx *ctx, float lr, float *d_grad_norm, cudaStream_
  * GAE (gamma, lambda) over the [T,N] rollout, advantage statistics over all
  * T*N entries, then for e in [0, epochs): permutation of epoch e (seed), and
  * for m in [0, minibatches): loss+gradient of minibatch m, clip, Adam(lr).
+ * With adv_mode 1/2 (ppo_config) the minibatches are environment segments
+ * whose advantages are recomputed from fresh values before each loss (GAE
+ * or V-trace; d_val is then unused); with optimizer 1 the step is Muon on
+ * the weight matrices and Adam(lr) on the biases and log-std.
  * d_obs..d_boot as above (d_val, d_rew, d_done [T,N]; d_boot [N]).
  * d_stats (nullable): fp32 [epochs*minibatches][6] minibatch stats.
  * T*N must be divisible by minibatches; T*N <= max_batch; epochs <=
