@@ -45,6 +45,12 @@ class _Net(ctypes.Structure):
                 ("head_n", ctypes.c_int32 * 8), ("n_gauss", ctypes.c_int32)]
 
 
+class _Rnn(ctypes.Structure):
+    _fields_ = [("obs_dim", ctypes.c_int32), ("hidden", ctypes.c_int32), ("layers", ctypes.c_int32),
+                ("n_heads", ctypes.c_int32), ("head_n", ctypes.c_int32 * 8),
+                ("n_gauss", ctypes.c_int32)]
+
+
 class _LossCfg(ctypes.Structure):
     _fields_ = [("clip", ctypes.c_double), ("vf_coef", ctypes.c_double),
                 ("ent_coef", ctypes.c_double), ("bf16_operands", ctypes.c_int)]
@@ -113,6 +119,14 @@ def lib():
         L.orc_newton_schulz5.argtypes = [_I64, _I64, _P, ctypes.c_int, _P]
         L.orc_muon.argtypes = [ctypes.POINTER(_Net), _P, _P, _P, _P, _P, _I64, _D, _D, _D, _D, _D,
                                _D]
+        L.orc_rnn_num_params.argtypes = [ctypes.POINTER(_Rnn)]
+        L.orc_rnn_num_params.restype = _I64
+        L.orc_rnn_forward.argtypes = [ctypes.POINTER(_Rnn), _P, _I64, _I64, _I64, _P, _P, _P, _P,
+                                      _P, _P, _P, _P, _P]
+        L.orc_rnn_loss_grad.argtypes = [ctypes.POINTER(_Rnn), ctypes.POINTER(_LossCfg), _P, _I64,
+                                        _I64, _I64, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _D,
+                                        _D, _P, _P, _P, _P, _P]
+        L.orc_rnn_loss_grad.restype = _D
         L.orc_update.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_Hyper), _I64, _I64, _I64, _I64,
                                  _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                  ctypes.POINTER(_I64), _P, _P, _P]
@@ -152,6 +166,30 @@ class Net:
     def num_params(self) -> int:
         D, H1, H2, C = self.obs_dim, self.h1, self.h2, self.out_cols
         return H1 * D + H1 + H2 * H1 + H2 + C * H2 + C + self.n_gauss
+
+
+@dataclass
+class Rnn:
+    """Recurrent policy: bias-free encoder D -> hidden, `layers` MinGRU layers,
+    bias-free decoder to the head columns (logits, Gaussian means, value)."""
+    obs_dim: int
+    hidden: int = 128
+    layers: int = 4
+    heads: tuple = (3, 2, 2)
+    n_gauss: int = 0
+
+    def c(self) -> _Rnn:
+        hn = (ctypes.c_int32 * 8)(*(list(self.heads) + [0] * (8 - len(self.heads))))
+        return _Rnn(self.obs_dim, self.hidden, self.layers, len(self.heads), hn, self.n_gauss)
+
+    @property
+    def out_cols(self) -> int:
+        return int(sum(self.heads)) + self.n_gauss + 1
+
+    @property
+    def num_params(self) -> int:
+        D, H, L, C = self.obs_dim, self.hidden, self.layers, self.out_cols
+        return H * D + L * (2 * H * H + 2 * H) + C * H + self.n_gauss
 
 
 @dataclass
@@ -301,6 +339,41 @@ def policy_act(net: Net, params, obs, seed: int, draw0: int = 0, bf16_operands=F
                          seed & 0xFFFFFFFF, int(draw0), _ptr(act), _ptr(actc), _ptr(logp),
                          _ptr(val))
     return act[:, :NH], actc[:, :G], logp, val
+
+
+def rnn_forward(rnn: Rnn, params, obs, done, h0, n: int = 0):
+    """Head outputs [T][C] of segment n; obs rows t*N + n, done [T][N], h0 [L][H]."""
+    done = _as(done, np.float32)
+    T, N = done.shape
+    out = np.empty((T, rnn.out_cols), np.float64)
+    cn = rnn.c()
+    lib().orc_rnn_forward(ctypes.byref(cn), _ptr(_as(params, np.float64)), T, N, n,
+                          _ptr(_as(obs, np.float32)), _ptr(done), _ptr(_as(h0, np.float64)),
+                          _ptr(out), None, None, None, None, None)
+    return out
+
+
+def rnn_loss_grad(rnn: Rnn, params, envs, obs, act_disc, act_cont, logp_old, adv, ret, done, h0,
+                  clip=0.2, vf_coef=0.5, ent_coef=0.01, normalize=False, adv_mean=0.0,
+                  adv_std=1.0):
+    """Loss and BPTT gradient of the segments envs; returns (loss, grad, stats6, scale6).
+    obs [T*N][D] (row t*N + n), adv / ret [T*N], done [T][N], h0 [N][L][H]."""
+    done = _as(done, np.float32)
+    T, N = done.shape
+    envs = _as(envs, np.int32)
+    grad = np.empty(rnn.num_params, np.float64)
+    st = np.empty(6, np.float64)
+    sc = np.empty(6, np.float64)
+    act_cont = _as(act_cont if act_cont is not None else np.zeros(1), np.float32)
+    cfg = _LossCfg(clip, vf_coef, ent_coef, 0)
+    cn = rnn.c()
+    loss = lib().orc_rnn_loss_grad(
+        ctypes.byref(cn), ctypes.byref(cfg), _ptr(_as(params, np.float64)), T, N, envs.size,
+        _ptr(envs), _ptr(_as(obs, np.float32)), _ptr(_as(act_disc, np.int32)), _ptr(act_cont),
+        _ptr(_as(logp_old, np.float32)), _ptr(_as(adv, np.float64)), _ptr(_as(ret, np.float64)),
+        int(bool(normalize)), adv_mean, adv_std, _ptr(done), _ptr(_as(h0, np.float64)),
+        _ptr(grad), _ptr(st), _ptr(sc))
+    return loss, grad, st, sc
 
 
 def moments(x):

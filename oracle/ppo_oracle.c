@@ -323,6 +323,63 @@ void orc_policy_logp(const orc_net *net, const double *params, int64_t n, const 
     free(logprob);
 }
 
+/* Per-row loss terms and dL/dz of one row of head outputs z (the body of
+ * orc_loss_grad's row loop, also used by the recurrent policy):
+ *   ratio = exp(logp - logp_old), pg = -min(ratio A, clip(ratio) A),
+ *   vl = (V - R)^2, total = pg + c_v vl - c_e H, clipfrac, approx_kl;
+ * dz gets dL/dz (with the 1/mb of the mean), glogstd accumulates the row's
+ * log-std gradient, terms = {total, pg, vl, H, clipfrac, kl}. */
+static void orc_ppo_row(const orc_net *net, const orc_loss_cfg *cfg, const double *logstd,
+                        const double *z, const int32_t *act, const float *actc,
+                        double logp_old, double A, double R, double inv_mb, double *logprob,
+                        double *dz, double *glogstd, double terms[6])
+{
+    const int64_t NH = net->n_heads, G = net->n_gauss, C = orc_out_cols(net);
+    /* log-probability and entropy of the taken action */
+    double logp, ent, head_ent[8];
+    orc_row_policy(net, logstd, z, act, actc, logprob, head_ent, &logp, &ent);
+    const double value = z[C - 1];
+
+    const double log_ratio = logp - logp_old;
+    const double ratio = exp(log_ratio);
+    const double lo = 1.0 - cfg->clip, hi = 1.0 + cfg->clip;
+    const double clipped = ratio < lo ? lo : (ratio > hi ? hi : ratio);
+    const double s1 = ratio * A, s2 = clipped * A;
+    const double pg = -(s1 < s2 ? s1 : s2);
+    const double vl = (value - R) * (value - R);
+    terms[0] = pg + cfg->vf_coef * vl - cfg->ent_coef * ent;
+    terms[1] = pg;
+    terms[2] = vl;
+    terms[3] = ent;
+    terms[4] = fabs(ratio - 1.0) > cfg->clip ? 1.0 : 0.0;
+    terms[5] = (ratio - 1.0) - log_ratio;
+
+    /* dL/dlogp: the unclipped term is active when s1 <= s2 */
+    const double g_logp = (s1 <= s2) ? -A * ratio * inv_mb : 0.0;
+    const double g_ent = -cfg->ent_coef * inv_mb;
+
+    int64_t off = 0;
+    for (int64_t h = 0; h < NH; ++h) {
+        int64_t n = net->head_n[h];
+        int64_t a = act[h];
+        for (int64_t k = 0; k < n; ++k) {
+            double p = exp(logprob[off + k]);
+            double dlogp_dz = (k == a ? 1.0 : 0.0) - p;
+            double dent_dz = -p * (logprob[off + k] + head_ent[h]);
+            dz[off + k] = g_logp * dlogp_dz + g_ent * dent_dz;
+        }
+        off += n;
+    }
+    for (int64_t g = 0; g < G; ++g) {
+        double mu = z[off + g], s = logstd[g];
+        double a = (double)actc[g];
+        double var = exp(2.0 * s);
+        dz[off + g] = g_logp * (a - mu) / var;
+        glogstd[g] += g_logp * ((a - mu) * (a - mu) / var - 1.0) + g_ent * 1.0;
+    }
+    dz[C - 1] = cfg->vf_coef * 2.0 * (value - R) * inv_mb;
+}
+
 /* ------------------------------------------------------------------------ */
 /* "Teaching Mario to speedrun", sec. 6 "Don't move too far at once":
  *   ratio  = new_prob(action) / old_prob(action)
@@ -374,52 +431,12 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
         const float *x = obs + row * D;
         orc_forward_full(net, &w, x, pre1, h1, pre2, h2, z, bf16);
 
-        /* log-probability and entropy of the taken action */
-        double logp, ent, head_ent[8];
-        orc_row_policy(net, w.logstd, z, act_disc + row * NH, act_cont + row * G, logprob,
-                       head_ent, &logp, &ent);
-        const double value = z[C - 1];
-
         double A = adv[row];
         if (normalize) A = (A - adv_mean) / (adv_std + 1e-8);
-        const double R = ret[row];
-        const double log_ratio = logp - (double)logp_old[row];
-        const double ratio = exp(log_ratio);
-        const double lo = 1.0 - cfg->clip, hi = 1.0 + cfg->clip;
-        const double clipped = ratio < lo ? lo : (ratio > hi ? hi : ratio);
-        const double s1 = ratio * A, s2 = clipped * A;
-        const double pg = -(s1 < s2 ? s1 : s2);
-        const double vl = (value - R) * (value - R);
-        const double total = pg + cfg->vf_coef * vl - cfg->ent_coef * ent;
-        const double clipfrac = fabs(ratio - 1.0) > cfg->clip ? 1.0 : 0.0;
-        const double kl = (ratio - 1.0) - log_ratio;
-        const double terms[6] = {total, pg, vl, ent, clipfrac, kl};
+        double terms[6];
+        orc_ppo_row(net, cfg, w.logstd, z, act_disc + row * NH, act_cont + row * G,
+                    (double)logp_old[row], A, ret[row], inv_mb, logprob, dz, glogstd, terms);
         for (int q = 0; q < 6; ++q) { sum[q] += terms[q]; asum[q] += fabs(terms[q]); }
-
-        /* dL/dlogp: the unclipped term is active when s1 <= s2 */
-        const double g_logp = (s1 <= s2) ? -A * ratio * inv_mb : 0.0;
-        const double g_ent = -cfg->ent_coef * inv_mb;
-
-        int64_t off = 0;
-        for (int64_t h = 0; h < NH; ++h) {
-            int64_t n = net->head_n[h];
-            int64_t a = act_disc[row * NH + h];
-            for (int64_t k = 0; k < n; ++k) {
-                double p = exp(logprob[off + k]);
-                double dlogp_dz = (k == a ? 1.0 : 0.0) - p;
-                double dent_dz = -p * (logprob[off + k] + head_ent[h]);
-                dz[off + k] = g_logp * dlogp_dz + g_ent * dent_dz;
-            }
-            off += n;
-        }
-        for (int64_t g = 0; g < G; ++g) {
-            double mu = z[off + g], s = w.logstd[g];
-            double a = (double)act_cont[row * G + g];
-            double var = exp(2.0 * s);
-            dz[off + g] = g_logp * (a - mu) / var;
-            glogstd[g] += g_logp * ((a - mu) * (a - mu) / var - 1.0) + g_ent * 1.0;
-        }
-        dz[C - 1] = cfg->vf_coef * 2.0 * (value - R) * inv_mb;
 
         /* backward through z = W3 h2 + b3 (bias gradients take the
          * unrounded signal; GEMM operands are rounded in bf16-operand mode) */
@@ -620,6 +637,198 @@ void orc_policy_act(const orc_net *net, int bf16, const double *params, int64_t 
     }
     free(buf);
     free(wr);
+}
+
+/* ------------------------------------------------------------------------ */
+/* "Teaching Mario to speedrun", sec. 8 "The Puffer net, and the trainer":
+ * PufferLib 5.0's policy is a bias-free linear encoder (observation -> H),
+ * four MinGRU layers, and one matrix from the hidden state to every head's
+ * logits plus the value.  The MinGRU's gates depend only on its input; its
+ * state carries across horizons and clears when an episode ends.  The pages
+ * give no equations; the MinGRU is the minimal GRU of Feng et al. 2024 ("Were
+ * RNNs All We Needed?"), layer input u, state h:
+ *   z_t = sigmoid(W_z u_t + b_z),  h~_t = W_h u_t + b_h,
+ *   h_t = (1 - z_t) h_{t-1} + z_t h~_t,
+ * layer l + 1 reading layer l's h (no residual, no normalisation: the pages
+ * name none).  A terminal at step t - 1 (the episode ended there) clears the
+ * state entering step t; h0 is the state carried into the segment.
+ * Parameter layout: W_enc[H][D]; per layer W_z[H][H], b_z[H], W_h[H][H],
+ * b_h[H]; W_dec[C][H]; logstd[G]. */
+int64_t orc_rnn_out_cols(const orc_rnn *r)
+{
+    int64_t c = 0;
+    for (int h = 0; h < r->n_heads; ++h) c += r->head_n[h];
+    return c + r->n_gauss + 1;
+}
+
+int64_t orc_rnn_num_params(const orc_rnn *r)
+{
+    const int64_t D = r->obs_dim, H = r->hidden, L = r->layers, C = orc_rnn_out_cols(r);
+    return H * D + L * (2 * H * H + 2 * H) + C * H + r->n_gauss;
+}
+
+/* the head layout of the recurrent policy as an orc_net (for orc_ppo_row) */
+static orc_net orc_rnn_heads(const orc_rnn *r)
+{
+    orc_net n;
+    memset(&n, 0, sizeof n);
+    n.obs_dim = r->obs_dim;
+    n.h1 = r->hidden;
+    n.h2 = r->hidden;
+    n.n_heads = r->n_heads;
+    for (int h = 0; h < 8; ++h) n.head_n[h] = r->head_n[h];
+    n.n_gauss = r->n_gauss;
+    return n;
+}
+
+static double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* Forward of one segment (env n, steps 0..T-1).  obs rows t*N + n, done
+ * [T][N], h0 [L][H].  zout [T][C]; when non-NULL, per step and layer
+ * [T][L][H]: the layer input u, the gate z, the candidate h~, the masked
+ * previous state hp and the new state h. */
+void orc_rnn_forward(const orc_rnn *r, const double *params, int64_t T, int64_t N, int64_t n,
+                     const float *obs, const float *done, const double *h0, double *zout,
+                     double *su, double *sz, double *sht, double *shp, double *sh)
+{
+    const int64_t D = r->obs_dim, H = r->hidden, L = r->layers, C = orc_rnn_out_cols(r);
+    const double *Wenc = params;
+    const double *Wdec = params + H * D + L * (2 * H * H + 2 * H);
+    double *state = (double *)malloc(sizeof(double) * (size_t)(L * H));
+    double *u = (double *)malloc(sizeof(double) * (size_t)H);
+    double *hn = (double *)malloc(sizeof(double) * (size_t)H);
+    memcpy(state, h0, sizeof(double) * (size_t)(L * H));
+    for (int64_t t = 0; t < T; ++t) {
+        const float *x = obs + (t * N + n) * D;
+        const double mask = (t > 0 && done[(t - 1) * N + n] != 0.0f) ? 0.0 : 1.0;
+        for (int64_t i = 0; i < H; ++i) {
+            double e = 0.0;
+            for (int64_t k = 0; k < D; ++k) e += Wenc[i * D + k] * (double)x[k];
+            u[i] = e;
+        }
+        for (int64_t l = 0; l < L; ++l) {
+            const double *Wz = params + H * D + l * (2 * H * H + 2 * H);
+            const double *bz = Wz + H * H, *Wh = bz + H, *bh = Wh + H * H;
+            for (int64_t i = 0; i < H; ++i) {
+                double pz = bz[i], ph = bh[i];
+                for (int64_t k = 0; k < H; ++k) {
+                    pz += Wz[i * H + k] * u[k];
+                    ph += Wh[i * H + k] * u[k];
+                }
+                const double z = orc_sigmoid(pz);
+                const double hp = mask * state[l * H + i];
+                hn[i] = (1.0 - z) * hp + z * ph;
+                const int64_t o = (t * L + l) * H + i;
+                if (su) { su[o] = u[i]; sz[o] = z; sht[o] = ph; shp[o] = hp; sh[o] = hn[i]; }
+            }
+            memcpy(state + l * H, hn, sizeof(double) * (size_t)H);
+            memcpy(u, hn, sizeof(double) * (size_t)H);
+        }
+        for (int64_t c = 0; c < C; ++c) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < H; ++k) acc += Wdec[c * H + k] * u[k];
+            zout[t * C + c] = acc;
+        }
+    }
+    free(state); free(u); free(hn);
+}
+
+/* Loss and gradient of a minibatch of environment segments envs[0..ns)
+ * (rows t*N + envs[j], t < T), with backpropagation through time inside each
+ * segment (h0, carried in from the previous horizon, is a constant).  The
+ * per-row loss is orc_loss_grad's (orc_ppo_row), with advantages optionally
+ * normalised by (adv_mean, adv_std); adv, ret [T*N]; h0 [N][L][H].
+ * grad overwritten; stats6 / scale6 as in orc_loss_grad. */
+double orc_rnn_loss_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double *params,
+                         int64_t T, int64_t N, int64_t ns, const int32_t *envs,
+                         const float *obs, const int32_t *act_disc, const float *act_cont,
+                         const float *logp_old, const double *adv, const double *ret,
+                         int normalize, double adv_mean, double adv_std, const float *done,
+                         const double *h0, double *grad, double *stats6, double *scale6)
+{
+    const int64_t D = r->obs_dim, H = r->hidden, L = r->layers, C = orc_rnn_out_cols(r);
+    const int64_t NH = r->n_heads, G = r->n_gauss, P = orc_rnn_num_params(r);
+    const orc_net heads = orc_rnn_heads(r);
+    const double *Wdec = params + H * D + L * (2 * H * H + 2 * H);
+    const double *logstd = Wdec + C * H;
+    memset(grad, 0, sizeof(double) * (size_t)P);
+    double *gWenc = grad;
+    double *gWdec = grad + (Wdec - params), *glogstd = grad + (logstd - params);
+    const int64_t TLH = T * L * H;
+    double *su = (double *)malloc(sizeof(double) * (size_t)TLH);
+    double *sz = (double *)malloc(sizeof(double) * (size_t)TLH);
+    double *sht = (double *)malloc(sizeof(double) * (size_t)TLH);
+    double *shp = (double *)malloc(sizeof(double) * (size_t)TLH);
+    double *sh = (double *)malloc(sizeof(double) * (size_t)TLH);
+    double *zout = (double *)malloc(sizeof(double) * (size_t)(T * C));
+    double *logprob = (double *)malloc(sizeof(double) * (size_t)C);
+    double *dz = (double *)malloc(sizeof(double) * (size_t)C);
+    double *dnext = (double *)malloc(sizeof(double) * (size_t)(L * H));
+    double *din = (double *)malloc(sizeof(double) * (size_t)H);
+    double *du = (double *)malloc(sizeof(double) * (size_t)H);
+    double sum[6] = {0, 0, 0, 0, 0, 0}, asum[6] = {0, 0, 0, 0, 0, 0};
+    const double inv_mb = 1.0 / (double)(T * ns);
+
+    for (int64_t j = 0; j < ns; ++j) {
+        const int64_t n = envs[j];
+        orc_rnn_forward(r, params, T, N, n, obs, done, h0 + n * L * H, zout, su, sz, sht, shp,
+                        sh);
+        memset(dnext, 0, sizeof(double) * (size_t)(L * H));
+        for (int64_t t = T - 1; t >= 0; --t) {
+            const int64_t row = t * N + n;
+            double A = adv[row];
+            if (normalize) A = (A - adv_mean) / (adv_std + 1e-8);
+            double terms[6];
+            orc_ppo_row(&heads, cfg, logstd, zout + t * C, act_disc + row * NH,
+                        act_cont + row * G, (double)logp_old[row], A, ret[row], inv_mb,
+                        logprob, dz, glogstd, terms);
+            for (int q = 0; q < 6; ++q) { sum[q] += terms[q]; asum[q] += fabs(terms[q]); }
+            /* decoder: z = W_dec h^{L-1}_t */
+            const double *htop = sh + (t * L + (L - 1)) * H;
+            for (int64_t k = 0; k < H; ++k) din[k] = 0.0;
+            for (int64_t c = 0; c < C; ++c)
+                for (int64_t k = 0; k < H; ++k) {
+                    gWdec[c * H + k] += dz[c] * htop[k];
+                    din[k] += dz[c] * Wdec[c * H + k];
+                }
+            /* layers, top to bottom: h = (1 - z) hp + z h~ */
+            const double mask = (t > 0 && done[(t - 1) * N + n] != 0.0f) ? 0.0 : 1.0;
+            for (int64_t l = L - 1; l >= 0; --l) {
+                const double *Wz = params + H * D + l * (2 * H * H + 2 * H);
+                const double *Wh = Wz + H * H + H;
+                double *gWz = grad + (Wz - params), *gbz = gWz + H * H;
+                double *gWh = gbz + H, *gbh = gWh + H * H;
+                const int64_t o = (t * L + l) * H;
+                for (int64_t k = 0; k < H; ++k) du[k] = 0.0;
+                for (int64_t i = 0; i < H; ++i) {
+                    const double dh = din[i] + dnext[l * H + i];
+                    const double z = sz[o + i];
+                    const double dpz = dh * (sht[o + i] - shp[o + i]) * z * (1.0 - z);
+                    const double dht = dh * z;
+                    dnext[l * H + i] = dh * (1.0 - z) * mask;   /* into h_{t-1} */
+                    gbz[i] += dpz;
+                    gbh[i] += dht;
+                    for (int64_t k = 0; k < H; ++k) {
+                        gWz[i * H + k] += dpz * su[o + k];
+                        gWh[i * H + k] += dht * su[o + k];
+                        du[k] += Wz[i * H + k] * dpz + Wh[i * H + k] * dht;
+                    }
+                }
+                memcpy(din, du, sizeof(double) * (size_t)H);
+            }
+            /* encoder: u^0 = W_enc x */
+            const float *x = obs + row * D;
+            for (int64_t i = 0; i < H; ++i)
+                for (int64_t k = 0; k < D; ++k) gWenc[i * D + k] += din[i] * (double)x[k];
+        }
+    }
+    for (int q = 0; q < 6; ++q) {
+        if (stats6) stats6[q] = sum[q] * inv_mb;
+        if (scale6) scale6[q] = asum[q] * inv_mb;
+    }
+    free(su); free(sz); free(sht); free(shp); free(sh); free(zout); free(logprob); free(dz);
+    free(dnext); free(din); free(du);
+    return sum[0] * inv_mb;
 }
 
 /* ------------------------------------------------------------------------ */

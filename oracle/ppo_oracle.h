@@ -147,6 +147,26 @@ void orc_policy_act(const orc_net *net, int bf16, const double *params, int64_t 
                     const float *obs, uint32_t seed, uint64_t draw0, int32_t *act,
                     double *actc, double *logp, double *value);
 
+/* Recurrent policy (see ppo_oracle.c): bias-free encoder, `layers` MinGRU
+ * layers of width `hidden`, bias-free decoder to the head columns. */
+typedef struct {
+    int32_t obs_dim, hidden, layers;
+    int32_t n_heads;
+    int32_t head_n[8];
+    int32_t n_gauss;
+} orc_rnn;
+int64_t orc_rnn_out_cols(const orc_rnn *r);
+int64_t orc_rnn_num_params(const orc_rnn *r);
+void orc_rnn_forward(const orc_rnn *r, const double *params, int64_t T, int64_t N, int64_t n,
+                     const float *obs, const float *done, const double *h0, double *zout,
+                     double *su, double *sz, double *sht, double *shp, double *sh);
+double orc_rnn_loss_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double *params,
+                         int64_t T, int64_t N, int64_t ns, const int32_t *envs,
+                         const float *obs, const int32_t *act_disc, const float *act_cont,
+                         const float *logp_old, const double *adv, const double *ret,
+                         int normalize, double adv_mean, double adv_std, const float *done,
+                         const double *h0, double *grad, double *stats6, double *scale6);
+
 /* L2 norm of g; if max_norm > 0, g *= min(1, max_norm/(norm + 1e-6)).
  * Returns the norm before clipping. */
 double orc_clip_grad_norm(int64_t P, double *g, double max_norm);
