@@ -333,6 +333,44 @@ ppo_status ppo_adam_step(ppo_ctx *ctx, float lr, float *d_grad_norm, cudaStream_
  * increments the step counter; d_grad_norm as in ppo_adam_step. */
 ppo_status ppo_muon_step(ppo_ctx *ctx, float lr, float *d_grad_norm, cudaStream_t stream);
 
+/* ---- Recurrent (MinGRU) policy ------------------------------------------------
+ * "Teaching Mario to speedrun", sec. 8 "The Puffer net, and the trainer":
+ * bias-free encoder (obs_dim -> hidden), `layers` MinGRU layers, one decoder
+ * matrix to every head's logits, the Gaussian means and the value.  MinGRU
+ * (Feng et al. 2024, "Were RNNs All We Needed?"), layer input u, state h:
+ *   z = sigmoid(W_z u + b_z),  h~ = W_h u + b_h,  h_t = (1 - z) h_{t-1} + z h~;
+ * the state entering step t is cleared when the episode ended at step t - 1
+ * (d_done[t-1][n] != 0).  Parameter layout (fp32): W_enc[hidden][obs_dim];
+ * per layer W_z[hidden][hidden], b_z[hidden], W_h[hidden][hidden],
+ * b_h[hidden]; W_dec[C][hidden]; logstd[n_gauss]. */
+typedef struct {
+    int32_t obs_dim, hidden, layers;  /* hidden 1..256, layers 1..8             */
+    int32_t n_heads;
+    int32_t head_n[PPO_MAX_HEADS];
+    int32_t n_gauss;                  /* 0..4; C = sum(head_n) + n_gauss + 1 <= 32 */
+    float clip, vf_coef, ent_coef;
+} ppo_rnn_config;
+
+ppo_status ppo_rnn_param_count(const ppo_rnn_config *cfg, int64_t *n);
+ppo_status ppo_rnn_workspace_bytes(const ppo_rnn_config *cfg, int64_t T, int64_t ns,
+                                   size_t *bytes);
+/* Loss (sec. 6, as ppo_minibatch_loss_grad) and gradient of a minibatch of
+ * environment segments d_envs[0..ns) (rows t*N + d_envs[j], t < T), with
+ * backpropagation through time inside each segment; d_h0 (fp32 [N][layers]
+ * [hidden]) is the state carried into the horizon, a constant of the loss.
+ * d_obs [T*N][obs_dim], d_act_disc [T*N][n_heads], d_act_cont [T*N][n_gauss],
+ * d_logp_old, d_adv, d_ret [T*N], d_adv_stats nullable ({mean, std}: the
+ * advantage used is (adv - mean)/(std + 1e-8)), d_done [T][N].  d_grad
+ * (param_count floats) is overwritten; d_stats6 as in
+ * ppo_minibatch_loss_grad.  fp32 CUDA-core kernels; deterministic. */
+ppo_status ppo_rnn_loss_grad(const ppo_rnn_config *cfg, const float *d_params, int64_t T,
+                             int64_t N, const int32_t *d_envs, int64_t ns, const float *d_obs,
+                             const int32_t *d_act_disc, const float *d_act_cont,
+                             const float *d_logp_old, const float *d_adv, const float *d_ret,
+                             const float *d_adv_stats, const float *d_done, const float *d_h0,
+                             float *d_grad, float *d_stats6, void *d_work, size_t work_bytes,
+                             cudaStream_t stream);
+
 /* ---- Whole update -------------------------------------------------------------
  * "Teaching Mario to speedrun", sec. 6 "The whole algorithm", steps 2-3:
  * GAE (gamma, lambda) over the [T,N] rollout, advantage statistics over all

@@ -12,13 +12,14 @@ import ctypes
 from dataclasses import dataclass
 
 from . import _abi
-from ._abi import PpoConfig, PpoError
+from ._abi import PpoConfig, PpoError, RnnConfig
 
 __all__ = [
     "PpoConfig", "PpoError", "Context", "make_config", "ppo_param_count", "ppo_gae",
     "ppo_gae_workspace_bytes", "ppo_gae_noalloc", "ppo_minibatch_perm", "ppo_perm_workspace_bytes",
     "ppo_segment_advantage", "ppo_segment_advantage_workspace_bytes",
-    "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_muon_step",
+    "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_muon_step", "RnnConfig",
+    "make_rnn_config", "ppo_rnn_param_count", "ppo_rnn_workspace_bytes", "ppo_rnn_loss_grad",
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
     "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "library_path",
@@ -143,6 +144,38 @@ def ppo_minibatch_perm(seed, epoch, B, perm, work, stream=None) -> None:
     wb = work.numel() * work.element_size()
     _abi.check(_lib().ppo_minibatch_perm(seed & 0xFFFFFFFF, epoch, B, _ptr(perm), _ptr(work), wb,
                                          _stream(stream)), "ppo_minibatch_perm")
+
+
+def make_rnn_config(obs_dim, hidden=128, layers=4, heads=(3, 2, 2), n_gauss=0, clip=0.2,
+                    vf_coef=0.5, ent_coef=0.01) -> RnnConfig:
+    hn = (ctypes.c_int32 * _abi.MAX_HEADS)(*(list(heads) + [0] * (_abi.MAX_HEADS - len(heads))))
+    return RnnConfig(obs_dim, hidden, layers, len(heads), hn, n_gauss, clip, vf_coef, ent_coef)
+
+
+def ppo_rnn_param_count(cfg: RnnConfig) -> int:
+    n = ctypes.c_int64()
+    _abi.check(_lib().ppo_rnn_param_count(ctypes.byref(cfg), ctypes.byref(n)),
+               "ppo_rnn_param_count")
+    return n.value
+
+
+def ppo_rnn_workspace_bytes(cfg: RnnConfig, T: int, ns: int) -> int:
+    n = ctypes.c_size_t()
+    _abi.check(_lib().ppo_rnn_workspace_bytes(ctypes.byref(cfg), T, ns, ctypes.byref(n)),
+               "ppo_rnn_workspace_bytes")
+    return n.value
+
+
+def ppo_rnn_loss_grad(cfg: RnnConfig, params, envs, obs, act_disc, act_cont, logp_old, adv, ret,
+                      done, h0, grad, adv_stats=None, stats6=None, work=None, stream=None) -> None:
+    """Loss and BPTT gradient of the recurrent policy over the segments envs (see ppo.h)."""
+    T, N = done.shape
+    wb = work.numel() * work.element_size() if work is not None else 0
+    _abi.check(_lib().ppo_rnn_loss_grad(
+        ctypes.byref(cfg), _ptr(params), T, N, _ptr(envs), envs.numel(), _ptr(obs),
+        _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(adv), _ptr(ret), _ptr(adv_stats),
+        _ptr(done), _ptr(h0), _ptr(grad), _ptr(stats6), _ptr(work), wb, _stream(stream)),
+        "ppo_rnn_loss_grad")
 
 
 # ---- context ------------------------------------------------------------------

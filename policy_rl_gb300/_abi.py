@@ -19,7 +19,8 @@ SYMBOLS = (
     "ppo_params_changed", "ppo_get_step", "ppo_gae_workspace_bytes", "ppo_gae",
     "ppo_gae_noalloc", "ppo_segment_advantage_workspace_bytes", "ppo_segment_advantage",
     "ppo_perm_workspace_bytes", "ppo_minibatch_perm", "ppo_minibatch_loss_grad",
-    "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_adam_step", "ppo_muon_step", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
+    "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_adam_step", "ppo_muon_step",
+    "ppo_rnn_param_count", "ppo_rnn_workspace_bytes", "ppo_rnn_loss_grad", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
     "ppo_sync_status",
 )
 NUM_STAGES = 34
@@ -49,6 +50,15 @@ class PpoConfig(ctypes.Structure):
         ("adv_mode", ctypes.c_int32), ("vtrace_rho_clip", ctypes.c_float),
         ("vtrace_c_clip", ctypes.c_float), ("optimizer", ctypes.c_int32),
         ("muon_lr", ctypes.c_float), ("muon_beta", ctypes.c_float),
+    ]
+
+
+class RnnConfig(ctypes.Structure):
+    _fields_ = [
+        ("obs_dim", ctypes.c_int32), ("hidden", ctypes.c_int32), ("layers", ctypes.c_int32),
+        ("n_heads", ctypes.c_int32), ("head_n", ctypes.c_int32 * MAX_HEADS),
+        ("n_gauss", ctypes.c_int32), ("clip", ctypes.c_float), ("vf_coef", ctypes.c_float),
+        ("ent_coef", ctypes.c_float),
     ]
 
 
@@ -97,6 +107,11 @@ def load(path: str = LIB_PATH):
         "ppo_policy_act": ([_P, _P, _I64, u32, ctypes.c_uint64, _P, _P, _P, _P, _P], ctypes.c_int),
         "ppo_adam_step": ([_P, _F, _P, _P], ctypes.c_int),
         "ppo_muon_step": ([_P, _F, _P, _P], ctypes.c_int),
+        "ppo_rnn_param_count": ([ctypes.POINTER(RnnConfig), ctypes.POINTER(_I64)], ctypes.c_int),
+        "ppo_rnn_workspace_bytes": ([ctypes.POINTER(RnnConfig), _I64, _I64, ctypes.POINTER(_SZ)],
+                                    ctypes.c_int),
+        "ppo_rnn_loss_grad": ([ctypes.POINTER(RnnConfig), _P, _I64, _I64, _P, _I64, _P, _P, _P, _P,
+                               _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
         "ppo_update": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F, _F,
                         u32, _P, _P], ctypes.c_int),
         "ppo_update_host": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F,

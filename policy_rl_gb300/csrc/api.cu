@@ -1217,6 +1217,96 @@ ppo_status ppo_policy_act(ppo_ctx* c, const float* obs, int64_t N, uint32_t seed
   return PPO_OK;
 }
 
+static ppo_status rnn_check(const ppo_rnn_config* r, NetShape* s, int64_t* P) {
+  if (!r) return PPO_ERR_INVALID;
+  if (r->obs_dim < 1 || r->hidden < 1 || r->layers < 1) return PPO_ERR_INVALID;
+  if (r->n_heads < 0 || r->n_heads > PPO_MAX_HEADS || r->n_gauss < 0 || r->n_gauss > 4)
+    return PPO_ERR_INVALID;
+  if (r->hidden > 256 || r->layers > 8) return PPO_ERR_UNSUPPORTED;
+  std::memset(s, 0, sizeof(*s));
+  int C = 0;
+  for (int h = 0; h < r->n_heads; ++h) {
+    if (r->head_n[h] < 1) return PPO_ERR_INVALID;
+    s->head_n[h] = r->head_n[h];
+    C += r->head_n[h];
+  }
+  C += r->n_gauss + 1;
+  if (C > 32) return PPO_ERR_UNSUPPORTED;
+  s->NH = r->n_heads;
+  s->G = r->n_gauss;
+  s->C = C;
+  s->CP = 32;
+  s->D = s->Dp = r->obs_dim;
+  s->H1 = s->H2 = r->hidden;
+  const int64_t D = r->obs_dim, H = r->hidden, L = r->layers;
+  *P = H * D + L * (2 * H * H + 2 * H) + (int64_t)C * H + r->n_gauss;
+  return PPO_OK;
+}
+
+ppo_status ppo_rnn_param_count(const ppo_rnn_config* cfg, int64_t* n) {
+  if (!n) return PPO_ERR_INVALID;
+  NetShape s;
+  return rnn_check(cfg, &s, n);
+}
+
+ppo_status ppo_rnn_workspace_bytes(const ppo_rnn_config* cfg, int64_t T, int64_t ns,
+                                   size_t* bytes) {
+  NetShape s;
+  int64_t P;
+  TRY(rnn_check(cfg, &s, &P));
+  if (!bytes || T < 1 || ns < 1) return PPO_ERR_INVALID;
+  *bytes = sizeof(float) * rnn_workspace_floats(cfg->obs_dim, cfg->hidden, cfg->layers, T * ns);
+  return PPO_OK;
+}
+
+ppo_status ppo_rnn_loss_grad(const ppo_rnn_config* cfg, const float* params, int64_t T,
+                             int64_t N, const int32_t* envs, int64_t ns, const float* obs,
+                             const int32_t* act, const float* actc, const float* logp_old,
+                             const float* adv, const float* ret, const float* adv_stats,
+                             const float* done, const float* h0, float* grad, float* stats6,
+                             void* work, size_t work_bytes, cudaStream_t st) {
+  NetShape s;
+  int64_t P;
+  TRY(rnn_check(cfg, &s, &P));
+  if (!params || !envs || !obs || !logp_old || !adv || !ret || !done || !h0 || !grad || !work)
+    return PPO_ERR_INVALID;
+  if ((s.NH > 0 && !act) || (s.G > 0 && !actc)) return PPO_ERR_INVALID;
+  if (T < 1 || N < 1 || ns < 1 || T * N >= (1ll << 31) || T * ns >= (1ll << 31))
+    return PPO_ERR_INVALID;
+  size_t need = 0;
+  TRY(ppo_rnn_workspace_bytes(cfg, T, ns, &need));
+  if (work_bytes < need) return PPO_ERR_INVALID;
+  const void* ps[] = {params, envs, obs, act, actc, logp_old, adv, ret, adv_stats, done, h0,
+                      grad, stats6, work};
+  for (const void* p : ps)
+    if (p && !al16(p)) return PPO_ERR_ALIGN;
+  RnnLaunch a{};
+  a.s = s;
+  a.lc = LossCoef{cfg->clip, cfg->vf_coef, cfg->ent_coef};
+  a.T = (int)T;
+  a.ns = (int)ns;
+  a.D = cfg->obs_dim;
+  a.H = cfg->hidden;
+  a.L = cfg->layers;
+  a.N = N;
+  a.params = params;
+  a.envs = envs;
+  a.obs = obs;
+  a.act = act;
+  a.actc = actc;
+  a.logp_old = logp_old;
+  a.adv = adv;
+  a.ret = ret;
+  a.adv_stats = adv_stats;
+  a.done = done;
+  a.h0 = h0;
+  a.grad = grad;
+  a.stats6 = stats6;
+  a.work = static_cast<float*>(work);
+  PPO_CUDA(launch_rnn_loss_grad(a, st));
+  return PPO_OK;
+}
+
 ppo_status ppo_segment_advantage_workspace_bytes(size_t* bytes) {
   if (!bytes) return PPO_ERR_INVALID;
   *bytes = 16 + sizeof(float) * 3 * (size_t)kFreshMaxGrid;

@@ -331,4 +331,31 @@ struct PolicyActArgs {
 cudaError_t policy_act_prepare();
 cudaError_t launch_policy_act(const PolicyActArgs& a, cudaStream_t st);
 
+// Loss and gradient of the recurrent MinGRU policy over a minibatch of
+// environment segments (rnn.cu).  params / grad in the recurrent layout:
+// W_enc[H][D], per layer W_z[H][H], b_z[H], W_h[H][H], b_h[H], W_dec[C][H],
+// logstd[G].  s carries the head layout (NH, head_n, G, C).
+struct RnnLaunch {
+  NetShape s;
+  LossCoef lc;
+  int T, ns, D, H, L;
+  int64_t N;
+  const float* params;
+  const int32_t* envs;      // [ns]
+  const float* obs;         // [T*N][D]
+  const int32_t* act;       // [T*N][NH]
+  const float* actc;        // [T*N][G]
+  const float* logp_old;    // [T*N]
+  const float* adv;         // [T*N]
+  const float* ret;         // [T*N]
+  const float* adv_stats;   // [2] or nullptr
+  const float* done;        // [T][N]
+  const float* h0;          // [N][L][H]
+  float* grad;
+  float* stats6;            // [6] or nullptr
+  float* work;              // rnn_workspace_floats(D, H, L, T*ns)
+};
+size_t rnn_workspace_floats(int D, int H, int L, int64_t rows);
+cudaError_t launch_rnn_loss_grad(const RnnLaunch& a, cudaStream_t st);
+
 }  // namespace ppo
