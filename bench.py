@@ -370,6 +370,10 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.skip_adam_stress:
         adam = _adam_stress(stream, hbm_peak)
 
+    rnn = None
+    if rank == 0 and not args.skip_rnn:
+        rnn = _rnn_minibatch(stream)
+
     # rollout side: one policy step (forward + sampling) of the workload's N agents
     act_step = None
     if rank == 0 and not args.skip_policy_act:
@@ -401,6 +405,7 @@ def run_ours(args, world, rank, local):
         "gae_stress": gae,
         "adam_stress": adam,
         "policy_act": act_step,
+        "rnn_minibatch": rnn,
         "cpu_baseline": cpu,
         "clocks": clk,
     }
@@ -526,6 +531,52 @@ def _policy_act_step(ctx, w, obs_d, stream, reps=50):
                     + f"; median of {reps} steps, inputs resident, no L2 flush"}
 
 
+def _rnn_minibatch(stream, reps=10):
+    """ppo_rnn_loss_grad on a Mario-like minibatch with the pages' recurrent
+    policy: 256 environment segments x T=128 (32,768 rows), 64-d observations,
+    encoder to 128, four MinGRU layers, heads [9,2,2,2] + value."""
+    import torch
+    import policy_rl_gb300 as P
+    T, N, ns, D, H, L = 128, 2048, 256, 64, 128, 4
+    heads = (9, 2, 2, 2)
+    cfg = P.make_rnn_config(D, H, L, heads)
+    n = P.ppo_rnn_param_count(cfg)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    with torch.cuda.stream(stream):
+        params = torch.randn(n, device="cuda", generator=g) * 0.05
+        obs = torch.randn(T * N, D, device="cuda", generator=g)
+        act = torch.stack([torch.randint(0, k, (T * N,), device="cuda", generator=g)
+                           for k in heads], 1).int().contiguous()
+        lp = torch.full((T * N,), -3.0, device="cuda")
+        adv = torch.randn(T * N, device="cuda", generator=g)
+        ret = torch.randn(T * N, device="cuda", generator=g)
+        done = (torch.rand(T, N, device="cuda", generator=g) < 0.004).float()
+        h0 = torch.zeros(N, L, H, device="cuda")
+        envs = torch.arange(ns, dtype=torch.int32, device="cuda")
+        grad = torch.empty(n, device="cuda")
+        work = torch.empty(P.ppo_rnn_workspace_bytes(cfg, T, ns), dtype=torch.uint8,
+                           device="cuda")
+        run = lambda: P.ppo_rnn_loss_grad(cfg, params, envs, obs, act, None, lp, adv, ret, done,
+                                          h0, grad, work=work, stream=stream)
+        for _ in range(3):
+            run()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for s0, e0 in evs:
+            s0.record(stream)
+            run()
+            e0.record(stream)
+        stream.synchronize()
+    t = float(np.median([a.elapsed_time(b) for a, b in evs])) / 1e3
+    rows = T * ns
+    flops = rows * (2 * D * H + L * 8 * H * H + 2 * 16 * H) * 3   # forward + backward (~2x)
+    return {"rows": rows, "ms_per_minibatch": round(t * 1e3, 3),
+            "samples_per_s": round(rows / t, 1), "approx_TFLOPs": round(flops / t / 1e12, 3),
+            "note": "ppo_rnn_loss_grad, fp32 CUDA-core kernels (correctness-first); "
+                    f"median of {reps}"}
+
+
 def _cpu_sample(w):
     n = max(1, 8192 // w.T)
     n = max(n - n % w.minibatches, w.minibatches)   # whole segments per minibatch
@@ -627,6 +678,7 @@ def main():
     ap.add_argument("--skip-gae-stress", action="store_true")
     ap.add_argument("--skip-adam-stress", action="store_true")
     ap.add_argument("--skip-policy-act", action="store_true")
+    ap.add_argument("--skip-rnn", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = _dist()
