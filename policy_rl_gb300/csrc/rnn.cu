@@ -10,7 +10,8 @@
 // backpropagation through time inside each segment.
 //
 // fp32 throughout (correctness-first version): the products are a generic
-// tiled GEMM; the recurrence runs one thread per (segment, unit) walking
+// tiled GEMM (split-K with fixed-order partial sums for the weight and bias
+// gradients, whose reduction runs over all rows); the recurrence runs one thread per (segment, unit) walking
 // time forward (and backward for the gradient); the loss is the MLP path's
 // per-row epilogue (tc::row_loss_seg) after a thread-per-row decoder.
 #include <utility>
@@ -27,21 +28,27 @@ constexpr int kGThreads = 256;
 
 // C[m][n] (+)= sum_k A(m, k) B(n, k) (+ bias[n]) with A(m, k) = A[m sam + k sak],
 // B(n, k) = B[n sbn + k sbk]; each output summed over k in order by one thread.
+// Split-K (gridDim.z > 1): block z sums k in [z kc, (z + 1) kc) into the
+// partial C + z M ldc (no bias, no accumulation); split_reduce_kernel then
+// adds the partials in split order.
 __global__ void __launch_bounds__(kGThreads)
 sgemm_kernel(int M, int N, int K, const float* __restrict__ A, int64_t sam, int64_t sak,
              const float* __restrict__ B, int64_t sbn, int64_t sbk, const float* bias,
-             float* C, int64_t ldc, int accumulate) {
+             float* C, int64_t ldc, int accumulate, int kc) {
   __shared__ float As[kT][kT + 1], Bs[kT][kT + 1];
   const int m0 = blockIdx.y * kT, n0 = blockIdx.x * kT;
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  const int kb = blockIdx.z * kc;
+  const int ke = kb + kc < K ? kb + kc : K;
+  if (gridDim.z > 1) C += (int64_t)blockIdx.z * M * ldc;
   float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-  for (int k0 = 0; k0 < K; k0 += kT) {
+  for (int k0 = kb; k0 < ke; k0 += kT) {
     for (int e = threadIdx.x; e < kT * kT; e += kGThreads) {
       const int r = e / kT, c = e % kT;
-      As[r][c] = (m0 + r < M && k0 + c < K) ? A[(int64_t)(m0 + r) * sam + (int64_t)(k0 + c) * sak]
-                                            : 0.f;
-      Bs[r][c] = (n0 + r < N && k0 + c < K) ? B[(int64_t)(n0 + r) * sbn + (int64_t)(k0 + c) * sbk]
-                                            : 0.f;
+      As[r][c] = (m0 + r < M && k0 + c < ke) ? A[(int64_t)(m0 + r) * sam + (int64_t)(k0 + c) * sak]
+                                             : 0.f;
+      Bs[r][c] = (n0 + r < N && k0 + c < ke) ? B[(int64_t)(n0 + r) * sbn + (int64_t)(k0 + c) * sbk]
+                                             : 0.f;
     }
     __syncthreads();
 #pragma unroll 8
@@ -61,11 +68,25 @@ sgemm_kernel(int M, int N, int K, const float* __restrict__ A, int64_t sam, int6
     for (int v = 0; v < 2; ++v) {
       const int m = m0 + 2 * ty + u, n = n0 + 2 * tx + v;
       if (m < M && n < N) {
-        float y = acc[u][v] + (bias ? bias[n] : 0.f);
-        if (accumulate) y += C[(int64_t)m * ldc + n];
+        float y = acc[u][v];
+        if (gridDim.z == 1) {
+          y += bias ? bias[n] : 0.f;
+          if (accumulate) y += C[(int64_t)m * ldc + n];
+        }
         C[(int64_t)m * ldc + n] = y;
       }
     }
+}
+
+// C[m][n] = sum over splits of part[s][m][n] (split order).
+__global__ void split_reduce_kernel(int M, int N, int splits, const float* __restrict__ part,
+                                    float* __restrict__ C, int64_t ldc) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)M * N) return;
+  const int m = (int)(i / N), n = (int)(i - (int64_t)m * N);
+  float y = 0.f;
+  for (int sp = 0; sp < splits; ++sp) y += part[((int64_t)sp * M + m) * N + n];
+  C[(int64_t)m * ldc + n] = y;
 }
 
 cudaError_t sgemm(int M, int N, int K, const float* A, int64_t sam, int64_t sak, const float* B,
@@ -74,7 +95,28 @@ cudaError_t sgemm(int M, int N, int K, const float* A, int64_t sam, int64_t sak,
   if (M <= 0 || N <= 0) return cudaSuccess;
   const dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT);
   sgemm_kernel<<<grid, kGThreads, 0, st>>>(M, N, K, A, sam, sak, B, sbn, sbk, bias, C, ldc,
-                                            accumulate);
+                                            accumulate, K);
+  return cudaGetLastError();
+}
+
+// Weight-gradient form: a long reduction (K = rows) over few output tiles,
+// split into kSplitK ranges written to `part` ([kSplitK][M][N]) and summed in
+// split order into C.
+constexpr int kSplitK = 32;
+cudaError_t sgemm_splitk(int M, int N, int K, const float* A, int64_t sam, int64_t sak,
+                         const float* B, int64_t sbn, int64_t sbk, float* C, int64_t ldc,
+                         float* part, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  int kc = (K + kSplitK - 1) / kSplitK;
+  kc = (kc + kT - 1) / kT * kT;
+  const int splits = (K + kc - 1) / kc;
+  const dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT, splits);
+  sgemm_kernel<<<grid, kGThreads, 0, st>>>(M, N, K, A, sam, sak, B, sbn, sbk, nullptr, part, N,
+                                            0, kc);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t n = (int64_t)M * N;
+  split_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(M, N, splits, part, C, ldc);
   return cudaGetLastError();
 }
 
@@ -145,16 +187,6 @@ __global__ void rnn_bwd_scan_kernel(RnnDims d, const float* __restrict__ done,
     dPH[o] = dh * z;
     dnext = dh * (1.f - z) * mask;
   }
-}
-
-// Column sums of A [rows][H] (bias gradients), rows in order.
-__global__ void rnn_colsum_kernel(int64_t rows, int H, const float* __restrict__ A,
-                                  float* __restrict__ out) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= H) return;
-  float s = 0.f;
-  for (int64_t r = 0; r < rows; ++r) s += A[r * H + i];
-  out[i] = s;
 }
 
 constexpr int kLossThreads = 128;
@@ -241,9 +273,12 @@ __global__ void rnn_finalize_kernel(int nblocks, int64_t rows, int G,
 }  // namespace
 
 size_t rnn_workspace_floats(int D, int H, int L, int64_t rows) {
-  // X, per layer (U, Zg, HT, HP), top state, dz, dIn, dPZ, dPH, dU, loss partials
+  // X, per layer (U, Zg, HT, HP), top state, dz, dIn, dPZ, dPH, dU, loss
+  // partials, split-K partials of the largest weight gradient, the constant 1
+  const size_t wmax = (size_t)H * (D > H ? (D > 32 ? D : 32) : (H > 32 ? H : 32));
   return (size_t)rows * D + (size_t)L * 4 * rows * H + (size_t)rows * H + (size_t)rows * 32 +
-         4 * (size_t)rows * H + 10 * ((size_t)(rows + kLossThreads - 1) / kLossThreads) + 64;
+         4 * (size_t)rows * H + 10 * ((size_t)(rows + kLossThreads - 1) / kLossThreads) + 64 +
+         (size_t)kSplitK * wmax + 4;
 }
 
 cudaError_t launch_rnn_loss_grad(const RnnLaunch& a, cudaStream_t st) {
@@ -262,7 +297,10 @@ cudaError_t launch_rnn_loss_grad(const RnnLaunch& a, cudaStream_t st) {
   float* dPZ = w;          w += rows * H;
   float* dPH = w;          w += rows * H;
   float* dU = w;           w += rows * H;
-  float* part = w;
+  float* part = w;         w += 10 * ((rows + kLossThreads - 1) / kLossThreads) + 64;
+  const size_t wmax = (size_t)H * (D > H ? (D > 32 ? D : 32) : (H > 32 ? H : 32));
+  float* kpart = w;        w += (size_t)kSplitK * wmax;
+  float* one = w;          // the constant 1 (column sums as a product with ones)
   const float* P = a.params;
   const int64_t oLayer0 = (int64_t)H * D, per = 2 * (int64_t)H * H + 2 * H;
   const float* Wenc = P;
@@ -272,6 +310,8 @@ cudaError_t launch_rnn_loss_grad(const RnnLaunch& a, cudaStream_t st) {
   const int thr = 256;
   cudaError_t e;
 #define RNN_TRY(x) do { if ((e = (x)) != cudaSuccess) return e; } while (0)
+  const float kOne = 1.f;
+  RNN_TRY(cudaMemcpyAsync(one, &kOne, sizeof(float), cudaMemcpyHostToDevice, st));
   rnn_gather_kernel<<<(unsigned)((rows * D + thr - 1) / thr), thr, 0, st>>>(d, a.obs, a.envs, X);
   RNN_TRY(cudaGetLastError());
   // encoder: U0 = X W_enc^T
@@ -298,7 +338,7 @@ cudaError_t launch_rnn_loss_grad(const RnnLaunch& a, cudaStream_t st) {
   RNN_TRY(cudaGetLastError());
   float* gWdec = G + oLayer0 + L * per;
   // gW_dec[c][k] = sum_r dz[r][c] Htop[r][k];  dIn = dz W_dec
-  RNN_TRY(sgemm(C, H, (int)rows, dz, 1, 32, Htop, 1, H, nullptr, gWdec, H, 0, st));
+  RNN_TRY(sgemm_splitk(C, H, (int)rows, dz, 1, 32, Htop, 1, H, gWdec, H, kpart, st));
   RNN_TRY(sgemm((int)rows, H, C, dz, 32, 1, Wdec, 1, H, nullptr, dIn, H, 0, st));
   for (int l = L - 1; l >= 0; --l) {
     const float* Wz = P + oLayer0 + l * per;
@@ -311,18 +351,18 @@ cudaError_t launch_rnn_loss_grad(const RnnLaunch& a, cudaStream_t st) {
                                                HPv + (size_t)l * rows * H, dIn, dPZ, dPH);
     RNN_TRY(cudaGetLastError());
     // weight and bias gradients
-    RNN_TRY(sgemm(H, H, (int)rows, dPZ, 1, H, Ul, 1, H, nullptr, gWz, H, 0, st));
-    RNN_TRY(sgemm(H, H, (int)rows, dPH, 1, H, Ul, 1, H, nullptr, gWh, H, 0, st));
-    rnn_colsum_kernel<<<(H + 127) / 128, 128, 0, st>>>(rows, H, dPZ, gbz);
-    rnn_colsum_kernel<<<(H + 127) / 128, 128, 0, st>>>(rows, H, dPH, gbh);
-    RNN_TRY(cudaGetLastError());
+    RNN_TRY(sgemm_splitk(H, H, (int)rows, dPZ, 1, H, Ul, 1, H, gWz, H, kpart, st));
+    RNN_TRY(sgemm_splitk(H, H, (int)rows, dPH, 1, H, Ul, 1, H, gWh, H, kpart, st));
+    // bias gradients: column sums, i.e. the product with a column of ones
+    RNN_TRY(sgemm_splitk(H, 1, (int)rows, dPZ, 1, H, one, 0, 0, gbz, 1, kpart, st));
+    RNN_TRY(sgemm_splitk(H, 1, (int)rows, dPH, 1, H, one, 0, 0, gbh, 1, kpart, st));
     // input gradient: dU = dPZ W_z + dPH W_h -> the layer below
     RNN_TRY(sgemm((int)rows, H, H, dPZ, H, 1, Wz, 1, H, nullptr, dU, H, 0, st));
     RNN_TRY(sgemm((int)rows, H, H, dPH, H, 1, Wh, 1, H, nullptr, dU, H, 1, st));
     std::swap(dIn, dU);
   }
   // encoder gradient: gW_enc[i][k] = sum_r dU0[r][i] X[r][k]
-  RNN_TRY(sgemm(H, D, (int)rows, dIn, 1, H, X, 1, D, nullptr, G, D, 0, st));
+  RNN_TRY(sgemm_splitk(H, D, (int)rows, dIn, 1, H, X, 1, D, G, D, kpart, st));
   rnn_finalize_kernel<<<1, 32, 0, st>>>(lblocks, rows, a.s.G, part, a.stats6,
                                         G + (logstd - P));
   RNN_TRY(cudaGetLastError());
