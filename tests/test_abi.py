@@ -53,3 +53,31 @@ def test_host_side_argument_checks(lib):
     p = ctypes.c_void_p(0x1004)
     assert L.ppo_gae(p, p, p, p, 4, 4, 0.99, 0.95, p, p, None, None, None, 0, None) == 2
     assert L.ppo_minibatch_perm(0, 0, 16, p, p, 1 << 20, None) == 2
+
+
+def test_recurrent_and_new_host_side_checks(lib):
+    import oracle
+    from policy_rl_gb300 import _abi, make_config, make_rnn_config
+    L = _abi.load()
+    n = ctypes.c_int64()
+    # recurrent policy: the parameter count equals the oracle's layout
+    for D, H, Ly, heads, G in ((3, 4, 2, (3, 2), 1), (64, 128, 4, (9, 2, 2, 2), 0)):
+        cfg = make_rnn_config(D, H, Ly, heads, G)
+        assert L.ppo_rnn_param_count(ctypes.byref(cfg), ctypes.byref(n)) == 0
+        assert n.value == oracle.Rnn(D, H, Ly, heads, G).num_params
+    assert L.ppo_rnn_param_count(ctypes.byref(make_rnn_config(3, 0, 2)), ctypes.byref(n)) == 1
+    assert L.ppo_rnn_param_count(ctypes.byref(make_rnn_config(3, 512, 2)), ctypes.byref(n)) == 4
+    assert L.ppo_rnn_param_count(ctypes.byref(make_rnn_config(3, 8, 9)), ctypes.byref(n)) == 4
+    assert L.ppo_rnn_param_count(ctypes.byref(make_rnn_config(3, 8, 2, heads=(30, 3))),
+                                 ctypes.byref(n)) == 4
+    sz = ctypes.c_size_t()
+    cfg = make_rnn_config(3, 4, 2, (3, 2), 1)
+    assert L.ppo_rnn_workspace_bytes(ctypes.byref(cfg), 0, 2, ctypes.byref(sz)) == 1
+    assert L.ppo_rnn_workspace_bytes(ctypes.byref(cfg), 6, 2, ctypes.byref(sz)) == 0
+    assert sz.value > 0
+    # invalid modes of the learner config
+    bad = make_config(32, 64, 64, precision=0, adv_mode=3)
+    assert L.ppo_param_count(ctypes.byref(bad), ctypes.byref(n)) == 1
+    bad = make_config(32, 64, 64, precision=0, optimizer=2)
+    assert L.ppo_param_count(ctypes.byref(bad), ctypes.byref(n)) == 1
+    assert L.ppo_segment_advantage_workspace_bytes(ctypes.byref(sz)) == 0 and sz.value >= 16
