@@ -7,6 +7,13 @@
  *   GAE -> advantage normalisation -> for each epoch, a shuffled set of
  *   minibatches -> MLP actor-critic forward, clipped surrogate + value +
  *   entropy loss, backward -> gradient-norm clip -> Adam.
+ * and, from sec. 8 (PufferLib 5.0) and the rollout side of sec. 6-7:
+ *   advantages per minibatch of environment segments from fresh values
+ *   (GAE or V-trace: ppo_segment_advantage, ppo_minibatch_loss_grad_fresh,
+ *   ppo_config.adv_mode), the Muon optimizer (ppo_muon_step,
+ *   ppo_config.optimizer), the rollout-side policy step with sampling
+ *   (ppo_policy_act), and the loss and gradient of the recurrent MinGRU
+ *   policy (ppo_rnn_loss_grad).
  *
  * Conventions shared by every entry point
  *  - Pointers named d_* are DEVICE pointers on the current CUDA device;
