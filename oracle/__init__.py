@@ -127,6 +127,9 @@ def lib():
                                         _I64, _I64, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _D,
                                         _D, _P, _P, _P, _P, _P]
         L.orc_rnn_loss_grad.restype = _D
+        L.orc_rnn_update.argtypes = [ctypes.POINTER(_Rnn), ctypes.POINTER(_Hyper), _I64, _I64, _I64,
+                                     _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                     ctypes.POINTER(_I64), _P]
         L.orc_update.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_Hyper), _I64, _I64, _I64, _I64,
                                  _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                  ctypes.POINTER(_I64), _P, _P, _P]
@@ -374,6 +377,26 @@ def rnn_loss_grad(rnn: Rnn, params, envs, obs, act_disc, act_cont, logp_old, adv
         int(bool(normalize)), adv_mean, adv_std, _ptr(done), _ptr(_as(h0, np.float64)),
         _ptr(grad), _ptr(st), _ptr(sc))
     return loss, grad, st, sc
+
+
+def rnn_update(rnn: Rnn, hp, T, N, epochs, minibatches, obs, act_disc, act_cont, logp_old, val,
+               rew, done, boot, h0, params, m=None, v=None, step=0):
+    """One recurrent-policy update; returns (params, m, v, step, stats [E*M][6])."""
+    P = rnn.num_params
+    params = _as(params, np.float64).copy()
+    m = np.zeros(P) if m is None else _as(m, np.float64).copy()
+    v = np.zeros(P) if v is None else _as(v, np.float64).copy()
+    stats = np.empty((epochs * minibatches, 6), np.float64)
+    st = _I64(step)
+    arrs = [_as(obs, np.float32), _as(act_disc, np.int32),
+            _as(act_cont if act_cont is not None else np.zeros(1), np.float32),
+            _as(logp_old, np.float32), _as(val, np.float32), _as(rew, np.float32),
+            _as(done, np.float32), _as(boot, np.float32), _as(h0, np.float64)]
+    cn, ch = rnn.c(), hp.c()
+    lib().orc_rnn_update(ctypes.byref(cn), ctypes.byref(ch), T, N, epochs, minibatches,
+                         *[_ptr(a) for a in arrs], _ptr(params), _ptr(m), _ptr(v),
+                         ctypes.byref(st), _ptr(stats))
+    return params, m, v, st.value, stats
 
 
 def moments(x):

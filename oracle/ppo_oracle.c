@@ -964,6 +964,44 @@ void orc_muon(const orc_net *net, double *params, const double *g, double *mom,
     free(is_mat);
 }
 
+/* One update of the recurrent policy ("Teaching Mario to speedrun", sec. 6
+ * "The whole algorithm" with sec. 8's policy): GAE over the stored values,
+ * advantage statistics over all T*N entries, then per epoch the mulberry32
+ * permutation of the N environments (orc_perm) and per minibatch the segments
+ * envs perm[k*ns .. (k+1)*ns) (ns = N / minibatches): orc_rnn_loss_grad
+ * (normalised advantages, carried state h0), gradient-norm clip, Adam.
+ * params, m, v updated in place; *step incremented per minibatch; stats
+ * (epochs*minibatches*6) nullable. */
+void orc_rnn_update(const orc_rnn *r, const orc_hyper *hp, int64_t T, int64_t N, int64_t epochs,
+                    int64_t minibatches, const float *obs, const int32_t *act_disc,
+                    const float *act_cont, const float *logp_old, const float *val,
+                    const float *rew, const float *done, const float *boot, const double *h0,
+                    double *params, double *m, double *v, int64_t *step, double *stats)
+{
+    const int64_t B = T * N, ns = N / minibatches, P = orc_rnn_num_params(r);
+    double *adv = (double *)malloc(sizeof(double) * (size_t)B);
+    double *ret = (double *)malloc(sizeof(double) * (size_t)B);
+    int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
+    double *grad = (double *)malloc(sizeof(double) * (size_t)P);
+    orc_gae(T, N, rew, val, done, boot, hp->gamma, hp->lambda, adv, ret);
+    double mean, sd;
+    orc_moments(B, adv, &mean, &sd);
+    const orc_loss_cfg lc = {hp->clip, hp->vf_coef, hp->ent_coef, 0};
+    for (int64_t e = 0; e < epochs; ++e) {
+        orc_perm(hp->seed, e, N, perm);
+        for (int64_t k = 0; k < minibatches; ++k) {
+            double tmp[6];
+            double *st = stats ? stats + (e * minibatches + k) * 6 : tmp;
+            orc_rnn_loss_grad(r, &lc, params, T, N, ns, perm + k * ns, obs, act_disc, act_cont,
+                              logp_old, adv, ret, 1, mean, sd, done, h0, grad, st, NULL);
+            orc_clip_grad_norm(P, grad, hp->max_grad_norm);
+            *step += 1;
+            orc_adam(P, params, grad, m, v, *step, hp->lr, hp->beta1, hp->beta2, hp->adam_eps);
+        }
+    }
+    free(adv); free(ret); free(perm); free(grad);
+}
+
 /* ------------------------------------------------------------------------ */
 /* "Teaching Mario to speedrun", sec. 6 "The whole algorithm": judge with GAE,
  * then learn for a few epochs over shuffled minibatches, one backward pass

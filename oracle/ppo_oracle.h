@@ -213,6 +213,15 @@ void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
                 double *params, double *m, double *v, double *mom, int64_t *step,
                 double *stats, double *adv_out, double *ret_out);
 
+/* One update of the recurrent policy: GAE, global advantage statistics, per
+ * epoch an environment permutation and minibatches of whole segments with
+ * orc_rnn_loss_grad, clip and Adam (see ppo_oracle.c).  h0 [N][layers][hidden]. */
+void orc_rnn_update(const orc_rnn *r, const orc_hyper *hp, int64_t T, int64_t N, int64_t epochs,
+                    int64_t minibatches, const float *obs, const int32_t *act_disc,
+                    const float *act_cont, const float *logp_old, const float *val,
+                    const float *rew, const float *done, const float *boot, const double *h0,
+                    double *params, double *m, double *v, int64_t *step, double *stats);
+
 #ifdef __cplusplus
 }
 #endif

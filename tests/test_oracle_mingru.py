@@ -162,3 +162,33 @@ def test_terminal_cuts_the_past():
     z2 = oracle.rnn_forward(rnn, p, obs2, done, h0[0] + 1.0)
     np.testing.assert_array_equal(z[4:], z2[4:])
     assert not np.allclose(z[:4], z2[:4])
+
+
+def test_rnn_update_is_the_composition():
+    rnn = oracle.Rnn(obs_dim=3, hidden=4, layers=2, heads=(3, 2), n_gauss=1)
+    T, N, E, M = 5, 8, 2, 2
+    p, obs, act, actc, lp, _, _, done, h0 = _data(rnn, T, N, 11)
+    rng = np.random.default_rng(12)
+    val = rng.normal(size=(T, N)).astype(np.float32)
+    rew = rng.normal(size=(T, N)).astype(np.float32)
+    boot = rng.normal(size=N).astype(np.float32)
+    hp = oracle.Hyper(lr=1e-3, seed=21)
+    q, m, v, step, stats = oracle.rnn_update(rnn, hp, T, N, E, M, obs, act, actc, lp, val, rew,
+                                             done, boot, h0, p)
+    adv, ret = oracle.gae(rew, val, done, boot, hp.gamma, hp.lam)
+    mean, sd = oracle.moments(adv)
+    r, mr, vr = p.copy(), np.zeros(p.size), np.zeros(p.size)
+    ns = N // M
+    k = 0
+    for e in range(E):
+        perm = oracle.perm(hp.seed, e, N)
+        for j in range(M):
+            _, g, st, _ = oracle.rnn_loss_grad(rnn, r, perm[j * ns:(j + 1) * ns], obs, act, actc,
+                                               lp, adv.ravel(), ret.ravel(), done, h0,
+                                               normalize=True, adv_mean=mean, adv_std=sd)
+            np.testing.assert_allclose(stats[k], st, rtol=1e-12, atol=1e-14)
+            _, g = oracle.clip_grad_norm(g, hp.max_grad_norm)
+            k += 1
+            r, mr, vr = oracle.adam(r, g, mr, vr, k, hp.lr)
+    assert step == E * M
+    np.testing.assert_allclose(q, r, rtol=1e-12, atol=1e-14)
