@@ -2,23 +2,29 @@
 """PPO learner-update benchmark on GB300.
 
 One step = one whole PPO update ("Teaching Mario to speedrun", sec. 6 "The
-whole algorithm", judge + learn) over a synthetic rollout of the Mario-like
-workload: T=128 steps x N=2048 envs, obs 64-d, MLP 64-256-256 tanh, heads
-[9,2,2,2] + value, 4 epochs x 8 minibatches, bf16 tensor-core GEMMs with fp32
-master weights and Adam.  Metric: samples/s = T*N / update time.
+whole algorithm", judge + learn) over a synthetic rollout.  The default
+workload is the large-batch one: T=64 steps x N=65536 envs, obs 128-d, MLP
+128-512-512 tanh, heads [9,2,2,2] + value, 4 epochs x 16 minibatches of
+262,144 rows, bf16 tensor-core GEMMs with fp32 master weights and Adam.
+Metric: samples/s = T*N / update time.
 
 Output: one JSON line on rank 0.  `value` is device time with the rollout
 resident in HBM (L2 flushed between steps by writing 256 MB); `e2e` goes
 through ppo_update_host from pinned host buffers (H2D of the rollout and D2H
 of the statistics inside the timed region).  `roofline` is the kernel stage
 with the largest share of a profiled update (CUDA events between kernels);
-`gae_stress` is the GAE scan's bandwidth at T=1024 x N=65536; `cpu_baseline`
-is the plain-C oracle on a bounded sample of the same workload.
+`gemm_all` aggregates the tensor-core GEMM stages.  `mario` repeats the
+measurement on the Mario-like workload (T=128 x N=2048, 64-256-256, 4 x 8
+minibatches), a launch- and latency-bound case.  `gae_stress` is the GAE
+scan's bandwidth at T=1024 x N=65536, `adam_stress` Adam over 67 M
+parameters; `cpu_baseline` is the plain-C oracle on a bounded slice of the
+headline workload (all host cores, and one core).
 
 --impl reference times the oracle itself (the CPU reference implementation)
-on a bounded sample per step.  Multi-GPU (torchrun): every rank runs an
-independent replica on its own GPU; value sums the samples of all ranks over
-the slowest rank's time (weak scaling, no data-path collective).
+on a bounded slice per step.  --drive runs plain driver loops for profilers.
+Multi-GPU (torchrun): every rank runs an independent replica on its own GPU;
+value sums the samples of all ranks over the slowest rank's time (weak
+scaling, no data-path collective).
 """
 from __future__ import annotations
 
@@ -180,9 +186,8 @@ OPTIMIZERS = {"adam": 0, "muon": 1}
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of the current kernels, cold caches (profiles/gemm_minibatch_*.md,
-# profiles/reduce_adam_mario.md);
-# stages without such a capture report null.
+# ncu capture of the current kernels, cold caches; stages without such a
+# capture report null.
 NCU_TRAFFIC = {
     ("mario", "fwd1_gemm"): 4.254e6, ("mario", "fwd2_gemm"): 16.936e6,
     ("mario", "head_loss_gemm"): 17.769e6, ("mario", "dact2_gemm"): 21.041e6,
@@ -247,14 +252,15 @@ def _roofline(stage, w, mb, ms_total, launches, hbm_peak, tf_peak, peak_src):
             "tensor_TFLOPs": round(flops / per_launch_s / 1e12, 2) if flops else None}
 
 
-def run_ours(args, world, rank, local):
+def _measure(w, args, world, rank, local, stream, peaks, adv_mode=0, optimizer=0):
+    """Device-timed and end-to-end updates of workload w, a profiled update
+    (per-kernel time), the dominant kernel's roofline and the aggregate of
+    the tensor-core GEMM stages.  Returns (summary, ctx, obs on the device)."""
     import torch
     import policy_rl_gb300 as P
     from policy_rl_gb300 import synth
 
-    torch.cuda.set_device(local)
-    hbm_peak, tf_burst, tf_sust, peak_src = _peaks()
-    w = synth.WORKLOADS[args.workload]
+    hbm_peak, tf_burst, tf_sust, peak_src = peaks
     B, E, M = w.B, w.epochs, w.minibatches
     mb = B // M
     # observations of the large workloads (> 2e8 values) are drawn on the device
@@ -263,9 +269,7 @@ def run_ours(args, world, rank, local):
     big = w.B * w.obs_dim > 2e8
     ro = synth.rollout(w, seed=rank, with_obs=not big)
     p0 = synth.init_params(w)
-    ctx = P.Context(P.config_from_workload(w, adv_mode=ADV_MODES[args.advantages],
-                                           optimizer=OPTIMIZERS[args.optimizer]), p0)
-    stream = torch.cuda.Stream()
+    ctx = P.Context(P.config_from_workload(w, adv_mode=adv_mode, optimizer=optimizer), p0)
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
     if big:
         g = torch.Generator(device="cuda")
@@ -339,7 +343,7 @@ def run_ours(args, world, rank, local):
     gemm_all = ({"ms_per_update": round(g_ms, 4),
                  "TFLOPs": round(g_flop / (g_ms / 1e3) / 1e12, 2),
                  "frac_of_bf16_sustained": round(g_flop / (g_ms / 1e3) / 1e12 / tf_sust, 4)}
-                if g_ms > 0 else None)
+                if g_ms > 0 and w.precision == "bf16" else None)
     stages = {k: {"ms": round(t, 4), "launches": c, "share": round(t / total_ms, 4)}
               for k, (t, c) in sorted(prof_all.items(), key=lambda kv: -kv[1][0])}
 
@@ -351,15 +355,62 @@ def run_ours(args, world, rank, local):
     host_stats = torch.zeros(E * M, 6).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_args)
     d2h = host_stats.numel() * 4
+    e2e_steps = max(3, min(args.steps, int(math.ceil(4000.0 / max(ms, 1e-3)))))
     with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup)):
+        for _ in range(max(1, min(args.warmup, 3))):
             P.ppo_update_host(ctx.handle, *host_args, *hp, stats=host_stats, stream=stream)
         _barrier(world)
         t0 = time.perf_counter()
-        for _ in range(args.steps):   # (the host->device copies pass through L2 anyway)
+        for _ in range(e2e_steps):   # (the host->device copies pass through L2 anyway)
             P.ppo_update_host(ctx.handle, *host_args, *hp, stats=host_stats, stream=stream)
         t1 = time.perf_counter()
-    e2e_s = _max_over_ranks((t1 - t0) / args.steps, world)
+    e2e_s = _max_over_ranks((t1 - t0) / e2e_steps, world)
+    del host_obs, host_args
+    summary = {
+        "workload": _workload_str(w, _name(ADV_MODES, adv_mode), _name(OPTIMIZERS, optimizer)),
+        "value": round(value, 1), "ms_per_step": round(ms, 4),
+        "e2e": {"value": round(world * B / e2e_s, 1), "unit": "samples/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "ppo_update_host (pinned host rollout -> device, stats -> host)"},
+        "roofline": roof, "gemm_all": gemm_all, "stages": stages,
+        "profiled_update_ms": round(total_ms, 4),
+        "launches_per_update": launches_per_update, "clocks": clk,
+    }
+    return summary, ctx, obs_d
+
+
+def _name(table, v):
+    return {x: k for k, x in table.items()}[v]
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from policy_rl_gb300 import synth
+
+    torch.cuda.set_device(local)
+    peaks = _peaks()
+    hbm_peak = peaks[0]
+    stream = torch.cuda.Stream()
+    w = synth.WORKLOADS[args.workload]
+    am, om = ADV_MODES[args.advantages], OPTIMIZERS[args.optimizer]
+    head, ctx, obs_d = _measure(w, args, world, rank, local, stream, peaks, am, om)
+
+    # rollout side: one policy step (forward + sampling) of the workload's N agents
+    act_step = None
+    if rank == 0 and not args.skip_policy_act:
+        act_step = _policy_act_step(ctx, w, obs_d, stream)
+    ctx.close()
+    del obs_d
+    torch.cuda.empty_cache()
+
+    # the Mario-like update (T=128 x N=2048) as a second, launch-bound workload
+    mario = None
+    if args.workload != "mario" and not args.skip_mario:
+        m, mctx, _ = _measure(synth.WORKLOADS["mario"], args, world, rank, local, stream, peaks,
+                              am, om)
+        mctx.close()
+        mario = {k: m[k] for k in ("workload", "value", "ms_per_step", "e2e", "roofline",
+                                   "gemm_all", "stages", "profiled_update_ms")}
 
     # GAE bandwidth stress (T=1024, N=65536): scan alone, and with moments + normalise
     gae = None
@@ -374,42 +425,35 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.skip_rnn:
         rnn = _rnn_minibatch(stream)
 
-    # rollout side: one policy step (forward + sampling) of the workload's N agents
-    act_step = None
-    if rank == 0 and not args.skip_policy_act:
-        act_step = _policy_act_step(ctx, w, obs_d, stream)
-
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
-        cpu = _cpu_baseline(w, ADV_MODES[args.advantages], OPTIMIZERS[args.optimizer])
+        cpu = _cpu_baseline(w, am, om)
 
     out = {
         "metric": "PPO update samples/s (GAE+clipped loss fwd/bwd+Adam); GAE GB/s vs HBM peak",
-        "value": round(value, 1), "unit": "samples/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "value": head["value"], "unit": "samples/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.precision == "bf16" else "f32",
         "data": "synthetic (seeded mulberry32 rollout with the workload's shapes and value "
                 "distributions; random-init weights)",
-        "config": {"workload": _workload_str(w, args.advantages, args.optimizer),
-                   "global_batch": world * B, "parallelism": f"replicas x{world}",
+        "config": {"workload": head["workload"],
+                   "global_batch": world * w.B, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (256 MB write)",
                    "timing": "CUDA events per update on the launching stream, mean over steps"},
-        "gpu_launches": launches_per_update * args.steps,
-        "e2e": {"value": round(world * B / e2e_s, 1), "unit": "samples/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "ppo_update_host (pinned host rollout -> device, stats -> host)"},
-        "roofline": roof,
-        "gemm_all": gemm_all,
-        "stages": stages,
-        "profiled_update_ms": round(total_ms, 4),
+        "gpu_launches": head["launches_per_update"] * args.steps,
+        "e2e": head["e2e"],
+        "roofline": head["roofline"],
+        "gemm_all": head["gemm_all"],
+        "stages": head["stages"],
+        "profiled_update_ms": head["profiled_update_ms"],
+        "mario": mario,
         "gae_stress": gae,
         "adam_stress": adam,
         "policy_act": act_step,
         "rnn_minibatch": rnn,
         "cpu_baseline": cpu,
-        "clocks": clk,
+        "clocks": head["clocks"],
     }
-    ctx.close()
     return out
 
 
@@ -577,12 +621,6 @@ def _rnn_minibatch(stream, reps=10):
                     f"median of {reps}"}
 
 
-def _cpu_sample(w):
-    n = max(1, 8192 // w.T)
-    n = max(n - n % w.minibatches, w.minibatches)   # whole segments per minibatch
-    return w.scaled(T=w.T, N=n, minibatches=w.minibatches, epochs=w.epochs)
-
-
 def _oracle_update(ws, seed=0, adv_mode=0, optimizer=0):
     import oracle
     from policy_rl_gb300 import synth
@@ -598,13 +636,44 @@ def _oracle_update(ws, seed=0, adv_mode=0, optimizer=0):
     return time.perf_counter() - t0
 
 
+def _slice(w, n):
+    """The workload with N reduced to n environments (whole env segments per
+    minibatch; the horizon, network, epochs and minibatches unchanged)."""
+    n = max(n - n % w.minibatches, w.minibatches)
+    return w.scaled(T=w.T, N=n, minibatches=w.minibatches, epochs=w.epochs)
+
+
+def _sized_slice(w, budget_s, adv_mode, optimizer, max_n=None):
+    """A slice of w whose oracle update takes about budget_s seconds (probe
+    on the smallest slice, then scale N)."""
+    probe = _slice(w, w.minibatches)
+    per_sample = _oracle_update(probe, adv_mode=adv_mode, optimizer=optimizer) / probe.B
+    n = int(budget_s / (per_sample * w.T))
+    n = max(w.minibatches, min(n, max_n or w.N, w.N))
+    return _slice(w, n)
+
+
 def _cpu_baseline(w, adv_mode=0, optimizer=0):
-    ws = _cpu_sample(w)
+    """The oracle (plain C fp64) on a bounded slice of the same workload: all
+    host cores (OpenMP over the minibatch rows), and one core on a smaller
+    slice."""
+    import oracle
+    cores = oracle.threads()
+    ws = _sized_slice(w, 15.0, adv_mode, optimizer)
     t = _oracle_update(ws, adv_mode=adv_mode, optimizer=optimizer)
-    return {"value": round(ws.B / t, 1), "unit": "samples/s", "cores": 1, "kind": "oracle",
+    oracle.set_threads(1)
+    try:
+        w1 = _sized_slice(w, 5.0, adv_mode, optimizer)
+        t1 = _oracle_update(w1, adv_mode=adv_mode, optimizer=optimizer)
+    finally:
+        oracle.set_threads(cores)
+    return {"value": round(ws.B / t, 1), "unit": "samples/s", "cores": cores, "kind": "oracle",
             "sample": f"whole update of a T={ws.T} x N={ws.N} slice ({ws.B} samples) of the "
                       f"{w.name} workload, {ws.epochs} epochs x {ws.minibatches} minibatches; "
-                      f"plain C fp64, single thread ({t:.2f} s)"}
+                      f"plain C fp64, OpenMP over minibatch rows on {cores} threads ({t:.2f} s)",
+            "single_thread": {"value": round(w1.B / t1, 1), "unit": "samples/s", "cores": 1,
+                              "sample": f"T={w1.T} x N={w1.N} slice ({w1.B} samples), "
+                                        f"{t1:.2f} s"}}
 
 
 def _workload_str(w, advantages="global", optimizer="adam") -> str:
@@ -621,29 +690,25 @@ def _workload_str(w, advantages="global", optimizer="adam") -> str:
 
 
 def run_reference(args, world, rank):
-    """The oracle timed on the host cores, one bounded sample per step.  The
-    sample (a T=16 x N slice of the workload) is sized so that the whole
-    run (warm-up + timed steps) takes about two minutes."""
+    """The oracle timed on the host cores (OpenMP over minibatch rows), one
+    bounded slice of the workload per step, sized so that the whole run
+    (warm-up + timed steps) takes about two minutes."""
+    import oracle
     from policy_rl_gb300 import synth
     w = synth.WORKLOADS[args.workload]
     am = ADV_MODES[args.advantages]
     om = OPTIMIZERS[args.optimizer]
-    n = max(8, w.minibatches)    # powers of two: whole env segments per minibatch
-    probe = w.scaled(T=16, N=n, minibatches=w.minibatches, epochs=w.epochs)
-    per_sample = _oracle_update(probe, adv_mode=am, optimizer=om) / probe.B
-    budget = 120.0 / (args.steps + args.warmup)
-    while n < 1024 and 16 * (2 * n) * per_sample <= budget:
-        n *= 2
-    ws = w.scaled(T=16, N=n, minibatches=w.minibatches, epochs=w.epochs)
+    ws = _sized_slice(w, 120.0 / (args.steps + args.warmup), am, om)
     for i in range(args.warmup):
         _oracle_update(ws, seed=i, adv_mode=am, optimizer=om)
     times = [_oracle_update(ws, seed=args.warmup + i, adv_mode=am, optimizer=om)
              for i in range(args.steps)]
     t = float(np.mean(times))
     v = ws.B / t
+    cores = oracle.threads()
     sample = (f"whole update of a T={ws.T} x N={ws.N} slice ({ws.B} samples) of the {w.name} "
               f"workload, {ws.epochs} epochs x {ws.minibatches} minibatches, per step; plain C "
-              f"fp64, single thread")
+              f"fp64, OpenMP over minibatch rows on {cores} threads")
     return {
         "impl": "reference",
         "metric": "PPO update samples/s (GAE+clipped loss fwd/bwd+Adam); GAE GB/s vs HBM peak",
@@ -654,11 +719,71 @@ def run_reference(args, world, rank):
                    "global_batch": world * w.B,
                    "parallelism": "host cores (rank 0)",
                    "sample": f"oracle on a {ws.B}-sample slice per step (T={ws.T} x N={ws.N})"},
-        "cpu_baseline": {"value": round(v, 2), "unit": "samples/s", "cores": 1,
+        "cpu_baseline": {"value": round(v, 2), "unit": "samples/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 2), "unit": "samples/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+
+
+def run_drive(args):
+    """Plain driver loops for profilers (ncu launch lists and captures): no
+    timing, no JSON line.
+      minibatch: ppo_minibatch_loss_grad + ppo_adam_step, --reps times, on one
+                 minibatch of --workload (random advantages, returns, indices);
+      update:    ppo_update of --workload, --reps times;
+      gae:       ppo_gae with moments + normalisation, T=--gae-T x N=--gae-N;
+      adam:      ppo_adam_step over the 67.2 M parameters of a 65536-1024-64
+                 fp32 network (1 GB of optimiser state)."""
+    import torch
+    import policy_rl_gb300 as P
+    from policy_rl_gb300 import synth
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    if args.drive in ("minibatch", "update"):
+        w = synth.WORKLOADS[args.workload]
+        B, mb = w.B, w.B // w.minibatches
+        big = B * w.obs_dim > 2e8
+        ro = synth.rollout(w, with_obs=not big)
+        ctx = P.Context(P.config_from_workload(w), synth.init_params(w))
+        d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+        obs = torch.randn(B, w.obs_dim, device="cuda", generator=g) if big else d(ro.obs)
+        if args.drive == "minibatch":
+            adv = torch.randn(B, device="cuda", generator=g)
+            ret = torch.randn(B, device="cuda", generator=g)
+            idx = torch.randperm(B, device="cuda", generator=g)[:mb].to(torch.int32)
+            a = [obs, d(ro.act_disc), d(ro.act_cont), d(ro.logp_old), adv, ret, idx]
+            for _ in range(args.reps):
+                ctx.minibatch_loss_grad(*a)
+                ctx.adam_step(w.lr)
+        else:
+            a = [obs] + [d(x) for x in (ro.act_disc, ro.act_cont, ro.logp_old, ro.val, ro.rew,
+                                        ro.done, ro.boot)]
+            for _ in range(args.reps):
+                ctx.update(*a, w.epochs, w.minibatches, w.gamma, w.lam, w.lr, 1234)
+        ctx.sync_status()
+        ctx.close()
+    elif args.drive == "gae":
+        T, N = args.gae_T, args.gae_N
+        rew = torch.randn(T, N, device="cuda", generator=g)
+        val = torch.randn(T, N, device="cuda", generator=g)
+        done = (torch.rand(T, N, device="cuda", generator=g) < 0.001).float()
+        boot = torch.randn(N, device="cuda", generator=g)
+        adv, ret, advn = (torch.empty(T, N, device="cuda") for _ in range(3))
+        st = torch.empty(4, device="cuda")
+        work = torch.empty(P.ppo_gae_workspace_bytes(T, N), dtype=torch.uint8, device="cuda")
+        for _ in range(args.reps):
+            P.ppo_gae(rew, val, done, boot, 0.997, 0.95, adv, ret, advn, st, work)
+    elif args.drive == "adam":
+        cfg = P.make_config(65536, 1024, 64, heads=(2,), precision=0, max_batch=1,
+                            max_minibatch=1, max_epochs=1)
+        ctx = P.Context(cfg)
+        ctx.grad.normal_(generator=g)
+        for _ in range(args.reps):
+            ctx.adam_step(1e-4)
+        ctx.sync_status()
+        ctx.close()
+    torch.cuda.synchronize()
 
 
 def main():
@@ -667,7 +792,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mario",
+    ap.add_argument("--workload", default="large",
                     choices=["tiny", "mario", "ddnet", "large"])
     ap.add_argument("--advantages", default="global", choices=sorted(ADV_MODES),
                     help="global: GAE once per update (default); fresh_gae / vtrace: per "
@@ -679,7 +804,17 @@ def main():
     ap.add_argument("--skip-adam-stress", action="store_true")
     ap.add_argument("--skip-policy-act", action="store_true")
     ap.add_argument("--skip-rnn", action="store_true")
+    ap.add_argument("--skip-mario", action="store_true",
+                    help="omit the Mario-like update measured beside the headline workload")
+    ap.add_argument("--drive", choices=["minibatch", "update", "gae", "adam"],
+                    help="plain driver loop for profilers (no timing, no JSON line)")
+    ap.add_argument("--reps", type=int, default=3, help="--drive: repetitions")
+    ap.add_argument("--gae-T", type=int, default=1024, help="--drive gae: horizon")
+    ap.add_argument("--gae-N", type=int, default=65536, help="--drive gae: environments")
     args = ap.parse_args()
+    if args.drive:
+        run_drive(args)
+        return
     args.warmup = max(args.warmup, 3)
     world, rank, local = _dist()
     if args.impl == "reference":

@@ -179,7 +179,8 @@ ppo_status ppo_get_step(ppo_ctx *ctx, int64_t *step);
  *         T*N entries.
  * d_work: device scratch of ppo_gae_workspace_bytes(T, N) bytes (may be NULL
  * when both d_adv_norm and d_stats are NULL).  Outputs may not alias inputs.
- * T, N >= 1; T*N < 2^31. */
+ * T, N >= 1; T*N < 2^31; T <= 2^19 (the per-warp moment counts, at most
+ * 32*T, stay exact in fp32; PPO_ERR_UNSUPPORTED above). */
 ppo_status ppo_gae_workspace_bytes(int64_t T, int64_t N, size_t *bytes);
 ppo_status ppo_gae(const float *d_rew, const float *d_val, const float *d_done,
                    const float *d_boot, int64_t T, int64_t N, float gamma, float lambda,
@@ -195,7 +196,10 @@ ppo_status ppo_gae(const float *d_rew, const float *d_val, const float *d_done,
  * (about 193 KB, held on every GPU that loads the library until exit), so
  * N must be at most 1,048,576 (PPO_ERR_UNSUPPORTED otherwise).  The first
  * call on a device looks that array's address up (cudaGetSymbolAddress with
- * the device current): make it before any stream capture.  All calls share
+ * the device current): make it before any stream capture.  The look-up is
+ * repeated when another CUDA context has become current on the device (after
+ * cudaDeviceReset, say); the first call after such a change must also come
+ * before any stream capture.  All calls share
  * the array: calls that may overlap on the GPU (unordered streams, several
  * host threads) race and must be serialised by the caller.  Never calls
  * cudaMalloc or cudaFree. */
@@ -442,6 +446,33 @@ ppo_status ppo_update_profile(ppo_ctx *ctx, const float *d_obs, const int32_t *d
 /* Synchronises `stream` and returns any error latched on the device since
  * the last call (PPO_ERR_TIMEOUT if a bounded wait gave up), clearing it. */
 ppo_status ppo_sync_status(ppo_ctx *ctx, cudaStream_t stream);
+
+/* ---- Inspection and failure handling ----------------------------------------
+ * Step trace of the whole update ("Teaching Mario to speedrun", sec. 6 "The
+ * whole algorithm": one backward pass and one optimizer step per minibatch).
+ * With a trace set, ppo_update records for minibatch step j (j = e *
+ * minibatches + m, the first max_steps steps of each update) into
+ * d_trace + j*4*P (P = ppo_param_count) four fp32 vectors of P values:
+ *   [0] the parameters before the step, [1] Adam's m and [2] Adam's v before
+ *   the step, [3] the assembled gradient of the step's minibatch (before the
+ *   gradient-norm clip).
+ * The copies are device-to-device on the update's stream, inside its graph;
+ * the kernels and their results are unchanged.  d_trace (DEVICE, 16-byte
+ * aligned, max_steps*4*P floats, owned by the caller, kept until the trace is
+ * cleared or the context destroyed); d_trace NULL with max_steps 0 clears it.
+ * The next ppo_update re-captures its graph. */
+ppo_status ppo_set_step_trace(ppo_ctx *ctx, float *d_trace, int64_t max_steps);
+
+/* Limit, in nanoseconds of the GPU's global timer, of the bounded grid-barrier
+ * waits of the cooperative kernels (gradient assembly + Adam inside
+ * ppo_update; the fresh-advantage kernel).  A wait that runs past it latches
+ * PPO_ERR_TIMEOUT (returned by the next ppo_sync_status); the kernel then
+ * skips the rest of its work and returns (these kernels hold no asynchronous
+ * copies or tensor memory).  The results of an update that timed out are
+ * undefined; the next update starts from cleared barrier counters.  0
+ * restores the default (2 s).  The tensor-core kernels' pipeline waits keep
+ * their own 2 s limit.  The next ppo_update re-captures its graph. */
+ppo_status ppo_set_wait_limit(ppo_ctx *ctx, uint64_t limit_ns);
 
 #ifdef __cplusplus
 }

@@ -32,11 +32,23 @@ def build(force: bool = False) -> str:
     newest = max(os.path.getmtime(_SRC), os.path.getmtime(hdr))
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".{os.getpid()}.tmp"
-        subprocess.check_call(
-            ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-Wall", "-shared", "-fPIC",
-             _SRC, "-o", tmp, "-lm"])
+        base = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-Wall", "-shared", "-fPIC"]
+        # OpenMP (row loops of the minibatch gradient) when the compiler has it
+        if subprocess.call(base + ["-fopenmp", _SRC, "-o", tmp, "-lm"],
+                           stderr=subprocess.DEVNULL) != 0:
+            subprocess.check_call(base + [_SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
+
+
+def threads() -> int:
+    """Threads of the oracle's OpenMP row loops (1 without OpenMP)."""
+    return int(lib().orc_threads())
+
+
+def set_threads(n: int) -> None:
+    """Thread count of the oracle's OpenMP row loops."""
+    lib().orc_set_threads(int(n))
 
 
 class _Net(ctypes.Structure):
@@ -127,9 +139,13 @@ def lib():
                                         _I64, _I64, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _D,
                                         _D, _P, _P, _P, _P, _P]
         L.orc_rnn_loss_grad.restype = _D
+        L.orc_rnn_update.restype = ctypes.c_int
         L.orc_rnn_update.argtypes = [ctypes.POINTER(_Rnn), ctypes.POINTER(_Hyper), _I64, _I64, _I64,
                                      _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                      ctypes.POINTER(_I64), _P]
+        L.orc_threads.argtypes = []
+        L.orc_threads.restype = ctypes.c_int
+        L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_update.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_Hyper), _I64, _I64, _I64, _I64,
                                  _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                  ctypes.POINTER(_I64), _P, _P, _P]
@@ -393,6 +409,8 @@ def rnn_update(rnn: Rnn, hp, T, N, epochs, minibatches, obs, act_disc, act_cont,
             _as(logp_old, np.float32), _as(val, np.float32), _as(rew, np.float32),
             _as(done, np.float32), _as(boot, np.float32), _as(h0, np.float64)]
     cn, ch = rnn.c(), hp.c()
+    if minibatches < 1 or N % minibatches:
+        raise ValueError("minibatches must be >= 1 and divide N (whole segments)")
     lib().orc_rnn_update(ctypes.byref(cn), ctypes.byref(ch), T, N, epochs, minibatches,
                          *[_ptr(a) for a in arrs], _ptr(params), _ptr(m), _ptr(v),
                          ctypes.byref(st), _ptr(stats))

@@ -11,6 +11,9 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ------------------------------------------------------------------------ */
 /* "PlayTrain", Appendix F.2 listing "seeded RNG" (mulberry32).
@@ -311,16 +314,25 @@ void orc_policy_logp(const orc_net *net, const double *params, int64_t n, const 
 {
     const int64_t C = orc_out_cols(net);
     orc_views w = orc_split(net, params);
-    double *z = (double *)malloc(sizeof(double) * (size_t)C);
-    double *logprob = (double *)malloc(sizeof(double) * (size_t)C);
-    double head_ent[8];
-    for (int64_t r = 0; r < n; ++r) {
-        orc_forward(net, params, obs + r * net->obs_dim, z);
-        orc_row_policy(net, w.logstd, z, act_disc + r * net->n_heads,
-                       act_cont + r * net->n_gauss, logprob, head_ent, &logp[r], &ent[r]);
+    /* rows are independent: with OpenMP each thread takes a share of them */
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+    {
+        double *z = (double *)malloc(sizeof(double) * (size_t)C);
+        double *logprob = (double *)malloc(sizeof(double) * (size_t)C);
+        double head_ent[8];
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+        for (int64_t r = 0; r < n; ++r) {
+            orc_forward(net, params, obs + r * net->obs_dim, z);
+            orc_row_policy(net, w.logstd, z, act_disc + r * net->n_heads,
+                           act_cont + r * net->n_gauss, logprob, head_ent, &logp[r], &ent[r]);
+        }
+        free(z);
+        free(logprob);
     }
-    free(z);
-    free(logprob);
 }
 
 /* Per-row loss terms and dL/dz of one row of head outputs z (the body of
@@ -380,6 +392,75 @@ static void orc_ppo_row(const orc_net *net, const orc_loss_cfg *cfg, const doubl
     dz[C - 1] = cfg->vf_coef * 2.0 * (value - R) * inv_mb;
 }
 
+/* Forward, loss terms and backward of one row; accumulates the row's
+ * gradient into grad (layout of the flat parameter vector) and returns its
+ * loss terms in terms[6].  buf holds 6 H + 3 C doubles of scratch. */
+static void orc_row_grad(const orc_net *net, const orc_loss_cfg *cfg, const orc_views *w,
+                         const float *x, const int32_t *act, const float *actc,
+                         double logp_old, double A, double R, double inv_mb, double *buf,
+                         double *grad, double terms[6])
+{
+    const int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
+    const int bf16 = cfg->bf16_operands;
+    double *gW1 = grad, *gb1 = gW1 + H1 * D, *gW2 = gb1 + H1, *gb2 = gW2 + H2 * H1;
+    double *gW3 = gb2 + H2, *gb3 = gW3 + C * H2, *glogstd = gb3 + C;
+    double *pre1 = buf, *h1 = pre1 + H1, *dh1 = h1 + H1;
+    double *pre2 = dh1 + H1, *h2 = pre2 + H2, *dh2 = h2 + H2;
+    double *z = dh2 + H2, *logprob = z + C, *dz = logprob + C;
+
+    orc_forward_full(net, w, x, pre1, h1, pre2, h2, z, bf16);
+    orc_ppo_row(net, cfg, w->logstd, z, act, actc, logp_old, A, R, inv_mb, logprob, dz, glogstd,
+                terms);
+
+    /* backward through z = W3 h2 + b3 (bias gradients take the unrounded
+     * signal; GEMM operands are rounded in bf16-operand mode) */
+    for (int64_t j = 0; j < H2; ++j) dh2[j] = 0.0;
+    for (int64_t c = 0; c < C; ++c) {
+        gb3[c] += dz[c];
+        const double dzc = orc_rnd(bf16, dz[c]);
+        for (int64_t j = 0; j < H2; ++j) {
+            gW3[c * H2 + j] += dzc * h2[j];
+            dh2[j] += dzc * w->W3[c * H2 + j];
+        }
+    }
+    /* through h2 = act(W2 h1 + b2) */
+    for (int64_t k = 0; k < H1; ++k) dh1[k] = 0.0;
+    for (int64_t j = 0; j < H2; ++j) {
+        double dpre = dh2[j] * orc_act_grad(net->act, pre2[j], h2[j]);
+        gb2[j] += dpre;
+        dpre = orc_rnd(bf16, dpre);
+        for (int64_t k = 0; k < H1; ++k) {
+            gW2[j * H1 + k] += dpre * h1[k];
+            dh1[k] += dpre * w->W2[j * H1 + k];
+        }
+    }
+    /* through h1 = act(W1 x + b1) */
+    for (int64_t j = 0; j < H1; ++j) {
+        double dpre = dh1[j] * orc_act_grad(net->act, pre1[j], h1[j]);
+        gb1[j] += dpre;
+        dpre = orc_rnd(bf16, dpre);
+        for (int64_t k = 0; k < D; ++k) gW1[j * D + k] += dpre * orc_rnd(bf16, (double)x[k]);
+    }
+}
+
+int orc_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* "Teaching Mario to speedrun", sec. 6 "Don't move too far at once":
  *   ratio  = new_prob(action) / old_prob(action)
@@ -394,7 +475,12 @@ static void orc_ppo_row(const orc_net *net, const orc_loss_cfg *cfg, const doubl
  * and entropy 1/2 + ln(2 pi)/2 + s.
  * Gradient of the log-probability w.r.t. head logits: 1[k == a] - p_k
  * (sec. 5, "the gradient of log probs[action]").  The clipped branch, where
- * min() picks the clipped term, has zero gradient w.r.t. the ratio. */
+ * min() picks the clipped term, has zero gradient w.r.t. the ratio.
+ *
+ * The gradient is a sum over rows.  With OpenMP the rows are cut into one
+ * contiguous range per thread, each thread sums its range into its own
+ * gradient, and the per-thread sums are added in thread order (deterministic
+ * for a given thread count). */
 double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *params,
                      int64_t mb, const int32_t *idx,
                      const float *obs, const int32_t *act_disc, const float *act_cont,
@@ -405,76 +491,53 @@ double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *
     const int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
     const int64_t NH = net->n_heads, G = net->n_gauss;
     const int64_t P = orc_num_params(net);
-    const int bf16 = cfg->bf16_operands;
-    double *wr = orc_gemm_weights(net, params, bf16);
-    orc_views w = orc_split(net, bf16 ? wr : params);
-
-    memset(grad, 0, sizeof(double) * (size_t)P);
-    double *gW1 = grad, *gb1 = gW1 + H1 * D, *gW2 = gb1 + H1, *gb2 = gW2 + H2 * H1;
-    double *gW3 = gb2 + H2, *gb3 = gW3 + C * H2, *glogstd = gb3 + C;
-
-    double *pre1 = (double *)malloc(sizeof(double) * (size_t)H1);
-    double *h1 = (double *)malloc(sizeof(double) * (size_t)H1);
-    double *pre2 = (double *)malloc(sizeof(double) * (size_t)H2);
-    double *h2 = (double *)malloc(sizeof(double) * (size_t)H2);
-    double *z = (double *)malloc(sizeof(double) * (size_t)C);
-    double *logprob = (double *)malloc(sizeof(double) * (size_t)C);
-    double *dz = (double *)malloc(sizeof(double) * (size_t)C);
-    double *dh2 = (double *)malloc(sizeof(double) * (size_t)H2);
-    double *dh1 = (double *)malloc(sizeof(double) * (size_t)H1);
-
-    double sum[6] = {0, 0, 0, 0, 0, 0}, asum[6] = {0, 0, 0, 0, 0, 0};
+    double *wr = orc_gemm_weights(net, params, cfg->bf16_operands);
+    const orc_views w = orc_split(net, cfg->bf16_operands ? wr : params);
     const double inv_mb = 1.0 / (double)mb;
 
-    for (int64_t r = 0; r < mb; ++r) {
-        const int64_t row = idx[r];
-        const float *x = obs + row * D;
-        orc_forward_full(net, &w, x, pre1, h1, pre2, h2, z, bf16);
+    int nt = orc_threads();
+    if (nt > mb) nt = (int)(mb > 0 ? mb : 1);
+    double *acc = (double *)calloc((size_t)nt * (size_t)P, sizeof(double));
+    double *tsum = (double *)calloc((size_t)nt * 12, sizeof(double));
 
-        double A = adv[row];
-        if (normalize) A = (A - adv_mean) / (adv_std + 1e-8);
-        double terms[6];
-        orc_ppo_row(net, cfg, w.logstd, z, act_disc + row * NH, act_cont + row * G,
-                    (double)logp_old[row], A, ret[row], inv_mb, logprob, dz, glogstd, terms);
-        for (int q = 0; q < 6; ++q) { sum[q] += terms[q]; asum[q] += fabs(terms[q]); }
-
-        /* backward through z = W3 h2 + b3 (bias gradients take the
-         * unrounded signal; GEMM operands are rounded in bf16-operand mode) */
-        for (int64_t j = 0; j < H2; ++j) dh2[j] = 0.0;
-        for (int64_t c = 0; c < C; ++c) {
-            gb3[c] += dz[c];
-            const double dzc = orc_rnd(bf16, dz[c]);
-            for (int64_t j = 0; j < H2; ++j) {
-                gW3[c * H2 + j] += dzc * h2[j];
-                dh2[j] += dzc * w.W3[c * H2 + j];
-            }
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+#ifdef _OPENMP
+        const int t = omp_get_thread_num();
+#else
+        const int t = 0;
+#endif
+        const int64_t r0 = mb * t / nt, r1 = mb * (t + 1) / nt;
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(3 * H1 + 3 * H2 + 3 * C));
+        double *g = acc + (size_t)t * (size_t)P;
+        double *sum = tsum + 12 * t, *asum = sum + 6;
+        for (int64_t r = r0; r < r1; ++r) {
+            const int64_t row = idx[r];
+            double A = adv[row];
+            if (normalize) A = (A - adv_mean) / (adv_std + 1e-8);
+            double terms[6];
+            orc_row_grad(net, cfg, &w, obs + row * D, act_disc + row * NH, act_cont + row * G,
+                         (double)logp_old[row], A, ret[row], inv_mb, buf, g, terms);
+            for (int q = 0; q < 6; ++q) { sum[q] += terms[q]; asum[q] += fabs(terms[q]); }
         }
-        /* through h2 = act(W2 h1 + b2) */
-        for (int64_t k = 0; k < H1; ++k) dh1[k] = 0.0;
-        for (int64_t j = 0; j < H2; ++j) {
-            double dpre = dh2[j] * orc_act_grad(net->act, pre2[j], h2[j]);
-            gb2[j] += dpre;
-            dpre = orc_rnd(bf16, dpre);
-            for (int64_t k = 0; k < H1; ++k) {
-                gW2[j * H1 + k] += dpre * h1[k];
-                dh1[k] += dpre * w.W2[j * H1 + k];
-            }
-        }
-        /* through h1 = act(W1 x + b1) */
-        for (int64_t j = 0; j < H1; ++j) {
-            double dpre = dh1[j] * orc_act_grad(net->act, pre1[j], h1[j]);
-            gb1[j] += dpre;
-            dpre = orc_rnd(bf16, dpre);
-            for (int64_t k = 0; k < D; ++k) gW1[j * D + k] += dpre * orc_rnd(bf16, (double)x[k]);
-        }
+        free(buf);
     }
 
+    memset(grad, 0, sizeof(double) * (size_t)P);
+    double sum[6] = {0, 0, 0, 0, 0, 0}, asum[6] = {0, 0, 0, 0, 0, 0};
+    for (int t = 0; t < nt; ++t) {
+        const double *g = acc + (size_t)t * (size_t)P;
+        for (int64_t i = 0; i < P; ++i) grad[i] += g[i];
+        for (int q = 0; q < 6; ++q) { sum[q] += tsum[12 * t + q]; asum[q] += tsum[12 * t + 6 + q]; }
+    }
     for (int q = 0; q < 6; ++q) {
         if (stats6) stats6[q] = sum[q] * inv_mb;
         if (scale6) scale6[q] = asum[q] * inv_mb;
     }
-    free(pre1); free(h1); free(pre2); free(h2); free(z); free(logprob);
-    free(dz); free(dh2); free(dh1);
+    free(acc);
+    free(tsum);
     free(wr);
     return sum[0] * inv_mb;
 }
@@ -493,22 +556,31 @@ void orc_fresh_values(const orc_net *net, int bf16, const double *params, int64_
     const int64_t H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
     double *wr = orc_gemm_weights(net, params, bf16);
     orc_views w = orc_split(net, bf16 ? wr : params);
-    double *buf = (double *)malloc(sizeof(double) * (size_t)(2 * H1 + 2 * H2 + 2 * C));
-    double *pre1 = buf, *h1 = pre1 + H1, *pre2 = h1 + H1, *h2 = pre2 + H2, *z = h2 + H2;
-    double *logprob = z + C;
-    double head_ent[8];
-    for (int64_t r = 0; r < n; ++r) {
-        const int64_t row = idx[r];
-        orc_forward_full(net, &w, obs + row * net->obs_dim, pre1, h1, pre2, h2, z, bf16);
-        val[r] = z[C - 1];
-        if (ratio) {
-            double logp, ent;
-            orc_row_policy(net, w.logstd, z, act_disc + row * net->n_heads,
-                           act_cont + row * net->n_gauss, logprob, head_ent, &logp, &ent);
-            ratio[r] = exp(logp - (double)logp_old[row]);
+    /* rows are independent: with OpenMP each thread takes a share of them */
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+    {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(2 * H1 + 2 * H2 + 2 * C));
+        double *pre1 = buf, *h1 = pre1 + H1, *pre2 = h1 + H1, *h2 = pre2 + H2, *z = h2 + H2;
+        double *logprob = z + C;
+        double head_ent[8];
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+        for (int64_t r = 0; r < n; ++r) {
+            const int64_t row = idx[r];
+            orc_forward_full(net, &w, obs + row * net->obs_dim, pre1, h1, pre2, h2, z, bf16);
+            val[r] = z[C - 1];
+            if (ratio) {
+                double logp, ent;
+                orc_row_policy(net, w.logstd, z, act_disc + row * net->n_heads,
+                               act_cont + row * net->n_gauss, logprob, head_ent, &logp, &ent);
+                ratio[r] = exp(logp - (double)logp_old[row]);
+            }
         }
+        free(buf);
     }
-    free(buf);
     free(wr);
 }
 
@@ -971,13 +1043,16 @@ void orc_muon(const orc_net *net, double *params, const double *g, double *mom,
  * envs perm[k*ns .. (k+1)*ns) (ns = N / minibatches): orc_rnn_loss_grad
  * (normalised advantages, carried state h0), gradient-norm clip, Adam.
  * params, m, v updated in place; *step incremented per minibatch; stats
- * (epochs*minibatches*6) nullable. */
-void orc_rnn_update(const orc_rnn *r, const orc_hyper *hp, int64_t T, int64_t N, int64_t epochs,
-                    int64_t minibatches, const float *obs, const int32_t *act_disc,
-                    const float *act_cont, const float *logp_old, const float *val,
-                    const float *rew, const float *done, const float *boot, const double *h0,
-                    double *params, double *m, double *v, int64_t *step, double *stats)
+ * (epochs*minibatches*6) nullable.  Returns -1 (and changes nothing) unless
+ * minibatches >= 1 divides N. */
+int orc_rnn_update(const orc_rnn *r, const orc_hyper *hp, int64_t T, int64_t N, int64_t epochs,
+                   int64_t minibatches, const float *obs, const int32_t *act_disc,
+                   const float *act_cont, const float *logp_old, const float *val,
+                   const float *rew, const float *done, const float *boot, const double *h0,
+                   double *params, double *m, double *v, int64_t *step, double *stats)
 {
+    /* every minibatch takes N / minibatches whole segments: no remainder */
+    if (minibatches < 1 || N % minibatches != 0) return -1;
     const int64_t B = T * N, ns = N / minibatches, P = orc_rnn_num_params(r);
     double *adv = (double *)malloc(sizeof(double) * (size_t)B);
     double *ret = (double *)malloc(sizeof(double) * (size_t)B);
@@ -1000,6 +1075,7 @@ void orc_rnn_update(const orc_rnn *r, const orc_hyper *hp, int64_t T, int64_t N,
         }
     }
     free(adv); free(ret); free(perm); free(grad);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */

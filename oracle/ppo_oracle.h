@@ -110,6 +110,11 @@ typedef struct {
  * scale6 = mean |per-row term| of the same six quantities (may be NULL);
  *          used by tests to form absolute tolerances for near-zero means.
  * Returns the loss. */
+/* Number of threads the OpenMP row loops use (1 when built without OpenMP). */
+int orc_threads(void);
+/* Sets the thread count of those loops (no effect without OpenMP). */
+void orc_set_threads(int n);
+
 double orc_loss_grad(const orc_net *net, const orc_loss_cfg *cfg, const double *params,
                      int64_t mb, const int32_t *idx,
                      const float *obs, const int32_t *act_disc, const float *act_cont,
@@ -215,12 +220,13 @@ void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
 
 /* One update of the recurrent policy: GAE, global advantage statistics, per
  * epoch an environment permutation and minibatches of whole segments with
- * orc_rnn_loss_grad, clip and Adam (see ppo_oracle.c).  h0 [N][layers][hidden]. */
-void orc_rnn_update(const orc_rnn *r, const orc_hyper *hp, int64_t T, int64_t N, int64_t epochs,
-                    int64_t minibatches, const float *obs, const int32_t *act_disc,
-                    const float *act_cont, const float *logp_old, const float *val,
-                    const float *rew, const float *done, const float *boot, const double *h0,
-                    double *params, double *m, double *v, int64_t *step, double *stats);
+ * orc_rnn_loss_grad, clip and Adam (see ppo_oracle.c).  h0 [N][layers][hidden].
+ * Returns -1 unless minibatches >= 1 divides N. */
+int orc_rnn_update(const orc_rnn *r, const orc_hyper *hp, int64_t T, int64_t N, int64_t epochs,
+                   int64_t minibatches, const float *obs, const int32_t *act_disc,
+                   const float *act_cont, const float *logp_old, const float *val,
+                   const float *rew, const float *done, const float *boot, const double *h0,
+                   double *params, double *m, double *v, int64_t *step, double *stats);
 
 #ifdef __cplusplus
 }

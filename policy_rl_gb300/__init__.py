@@ -22,7 +22,8 @@ __all__ = [
     "make_rnn_config", "ppo_rnn_param_count", "ppo_rnn_workspace_bytes", "ppo_rnn_loss_grad",
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
-    "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "library_path",
+    "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "ppo_set_step_trace",
+    "ppo_set_wait_limit", "library_path",
 ]
 
 
@@ -293,6 +294,16 @@ def ppo_sync_status(ctx, stream=None) -> None:
     _abi.check(_lib().ppo_sync_status(ctx, _stream(stream)), "ppo_sync_status")
 
 
+def ppo_set_step_trace(ctx, trace=None, max_steps: int = 0) -> None:
+    """Per-step copies of params, m, v and the gradient inside ppo_update (see ppo.h)."""
+    _abi.check(_lib().ppo_set_step_trace(ctx, _ptr(trace), max_steps), "ppo_set_step_trace")
+
+
+def ppo_set_wait_limit(ctx, limit_ns: int = 0) -> None:
+    """Limit of the cooperative kernels' grid-barrier waits (0: the 2 s default)."""
+    _abi.check(_lib().ppo_set_wait_limit(ctx, int(limit_ns)), "ppo_set_wait_limit")
+
+
 class Context:
     """Owns one ppo_ctx (parameters, gradient, Adam state, workspaces)."""
 
@@ -345,3 +356,9 @@ class Context:
 
     def step(self) -> int:
         return ppo_get_step(self.handle)
+
+    def set_step_trace(self, trace=None, max_steps: int = 0):
+        return ppo_set_step_trace(self.handle, trace, max_steps)
+
+    def set_wait_limit(self, limit_ns: int = 0):
+        return ppo_set_wait_limit(self.handle, limit_ns)

@@ -21,7 +21,7 @@ SYMBOLS = (
     "ppo_perm_workspace_bytes", "ppo_minibatch_perm", "ppo_minibatch_loss_grad",
     "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_adam_step", "ppo_muon_step",
     "ppo_rnn_param_count", "ppo_rnn_workspace_bytes", "ppo_rnn_loss_grad", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
-    "ppo_sync_status",
+    "ppo_sync_status", "ppo_set_step_trace", "ppo_set_wait_limit",
 )
 NUM_STAGES = 34
 NUM_KERNEL_STAGES = 25
@@ -120,6 +120,8 @@ def load(path: str = LIB_PATH):
         "ppo_update_profile": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F,
                                 _F, _F, u32, _P, _P, _P, _P], ctypes.c_int),
         "ppo_sync_status": ([_P, _P], ctypes.c_int),
+        "ppo_set_step_trace": ([_P, _P, _I64], ctypes.c_int),
+        "ppo_set_wait_limit": ([_P, ctypes.c_uint64], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)

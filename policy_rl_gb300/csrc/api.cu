@@ -95,6 +95,13 @@ struct ppo_ctx {
   int32_t* perm = nullptr;
   void* perm_work = nullptr;
 
+  // step trace (ppo_set_step_trace): per minibatch step, params, m, v before
+  // the step and the assembled gradient after it, [trace_cap][4][P] fp32
+  float* trace = nullptr;
+  int64_t trace_cap = 0;
+  // limit of the cooperative kernels' grid-barrier waits (ppo_set_wait_limit)
+  uint64_t wait_ns = kTimeoutNs;
+
   // host-update staging (allocated on first ppo_update_host)
   float *st_obs = nullptr, *st_actc = nullptr, *st_logp = nullptr, *st_val = nullptr,
         *st_rew = nullptr, *st_done = nullptr, *st_boot = nullptr, *st_stats = nullptr;
@@ -380,7 +387,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     f.part = c->fpart;
     f.bar = c->fbar;
     f.err = c->err;
-    f.timeout_ns = kTimeoutNs;
+    f.timeout_ns = c->wait_ns;
     cudaError_t e = launch_fresh_adv(f, c->num_sms, st);
     if (e == cudaSuccess) c->tr.mark(ST_FRESH_ADV, st);
     return e;
@@ -556,7 +563,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
   }
   if (adam) {   // gradient assembly, clip and Adam in one cooperative launch
     ra.sq_part = c->sq;
-    PPO_CUDA(launch_reduce_adam(ra, *adam, c->rbar, c->err, kTimeoutNs, c->num_sms, st));
+    PPO_CUDA(launch_reduce_adam(ra, *adam, c->rbar, c->err, c->wait_ns, c->num_sms, st));
     c->tr.mark(ST_REDUCE_ADAM, st);
     return PPO_OK;
   }
@@ -740,6 +747,22 @@ ppo_status enqueue_minibatch_mk(ppo_ctx* c, const float* obs, const __nv_bfloat1
   return PPO_OK;
 }
 
+// Step trace of minibatch step j: params, m, v before the step (after == 0),
+// the assembled (unclipped) gradient after it (after == 1).
+cudaError_t trace_step(ppo_ctx* c, int64_t j, int after, cudaStream_t st) {
+  if (!c->trace || j >= c->trace_cap) return cudaSuccess;
+  const int64_t P = c->s.P;
+  float* slot = c->trace + j * 4 * P;
+  const size_t bytes = sizeof(float) * (size_t)P;
+  if (after) return cudaMemcpyAsync(slot + 3 * P, c->grad, bytes, cudaMemcpyDeviceToDevice, st);
+  const float* src[3] = {c->params, c->m, c->v};
+  for (int i = 0; i < 3; ++i) {
+    cudaError_t e = cudaMemcpyAsync(slot + i * P, src[i], bytes, cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, const float* actc,
                           const float* logp_old, const float* val, const float* rew,
                           const float* done, const float* boot, int64_t T, int64_t N,
@@ -754,8 +777,11 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
     // environments with the mulberry32 rule, minibatch k takes N/M of them
     const int ns = (int)(N / minibatches);
     if (parts & 1) {
+      // barrier and Adam completion counters start at zero (also after a
+      // launch that gave up on a bounded wait)
       PPO_CUDA(cudaMemsetAsync(c->rbar, 0, sizeof(unsigned), st));
       PPO_CUDA(cudaMemsetAsync(c->fbar, 0, sizeof(unsigned), st));
+      PPO_CUDA(cudaMemsetAsync(c->done_ctr, 0, sizeof(unsigned), st));
       PPO_CUDA(launch_perm(seed, 0, epochs, N, c->perm, c->perm_work, st, &c->tr));
     }
     if (!(parts & 2)) return PPO_OK;
@@ -779,14 +805,18 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
         const AdamArgs aa = make_adam_args(c, lr, nullptr, 0);
         const FreshSpec fs{rew, done, boot, perm_e + (int64_t)k * ns, (int)T, ns, N, gamma,
                            lambda, c->cfg.adv_mode == 2};
+        const int64_t j = (int64_t)e * minibatches + k;
+        PPO_CUDA(trace_step(c, j, 0, st));
         if (c->cfg.optimizer == 1) {
           int nsq = 0;
           TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, nullptr, nullptr, nullptr,
                                 B, mb, nullptr, st6, st, &nsq, &mr, nullptr, &fs));
+          PPO_CUDA(trace_step(c, j, 1, st));
           TRY(enqueue_muon(c, lr, nullptr, st, nsq));
         } else {
           TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, nullptr, nullptr, nullptr,
                                 B, mb, nullptr, st6, st, nullptr, &mr, &aa, &fs));
+          PPO_CUDA(trace_step(c, j, 1, st));
         }
       }
     }
@@ -798,6 +828,7 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
       PPO_CUDA(cudaMemsetAsync(c->gbar, 0, 2 * sizeof(unsigned), st));
     else
       PPO_CUDA(cudaMemsetAsync(c->rbar, 0, sizeof(unsigned), st));
+    PPO_CUDA(cudaMemsetAsync(c->done_ctr, 0, sizeof(unsigned), st));
     PPO_CUDA(launch_gae(rew, val, done, boot, (int)T, (int)N, gamma, lambda, c->adv, c->ret,
                         c->gae_part, gae_num_blocks((int)N), st));
     c->tr.mark(ST_GAE, st);
@@ -824,9 +855,12 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
     for (int k = 0; k < minibatches; ++k) {
       const int32_t* idx = perm_e + (int64_t)k * mb;
       float* st6 = stats ? stats + ((int64_t)e * minibatches + k) * 6 : nullptr;
+      const int64_t j = (int64_t)e * minibatches + k;
+      PPO_CUDA(trace_step(c, j, 0, st));
       if (c->use_mk) {
         TRY(enqueue_minibatch_mk(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
                                  c->advstats, st6, 1, lr, st));
+        PPO_CUDA(trace_step(c, j, 1, st));
       } else {
         const int64_t r0 = (int64_t)k * mb;
         const MbRows mr{static_cast<uint8_t*>(ep.X) + r0 * xrow, ep.act + r0 * NH,
@@ -836,10 +870,12 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
           int nsq = 0;
           TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
                                 c->advstats, st6, st, &nsq, &mr));
+          PPO_CUDA(trace_step(c, j, 1, st));
           TRY(enqueue_muon(c, lr, nullptr, st, nsq));
         } else {
           TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
                                 c->advstats, st6, st, nullptr, &mr, &aa));
+          PPO_CUDA(trace_step(c, j, 1, st));
         }
       }
     }
@@ -1072,6 +1108,7 @@ ppo_status ppo_get_step(ppo_ctx* c, int64_t* step) {
 
 ppo_status ppo_gae_workspace_bytes(int64_t T, int64_t N, size_t* bytes) {
   if (!bytes || T < 1 || N < 1 || T * N >= (1ll << 31)) return PPO_ERR_INVALID;
+  if (T > kGaeMaxT) return PPO_ERR_UNSUPPORTED;
   *bytes = (size_t)round_up(24 * (int64_t)gae_num_blocks((int)N), 256) + 256;
   return PPO_OK;
 }
@@ -1082,6 +1119,7 @@ ppo_status ppo_gae(const float* rew, const float* val, const float* done, const 
                    cudaStream_t st) {
   if (!rew || !val || !done || !boot || !adv || !ret) return PPO_ERR_INVALID;
   if (T < 1 || N < 1 || T * N >= (1ll << 31)) return PPO_ERR_INVALID;
+  if (T > kGaeMaxT) return PPO_ERR_UNSUPPORTED;
   const void* ps[] = {rew, val, done, boot, adv, ret, adv_norm, stats, work};
   for (const void* p : ps)
     if (p && !al16(p)) return PPO_ERR_ALIGN;
@@ -1271,6 +1309,7 @@ ppo_status ppo_rnn_loss_grad(const ppo_rnn_config* cfg, const float* params, int
   if (!params || !envs || !obs || !logp_old || !adv || !ret || !done || !h0 || !grad || !work)
     return PPO_ERR_INVALID;
   if ((s.NH > 0 && !act) || (s.G > 0 && !actc)) return PPO_ERR_INVALID;
+  if (T > kGaeMaxT) return PPO_ERR_UNSUPPORTED;
   if (T < 1 || N < 1 || ns < 1 || T * N >= (1ll << 31) || T * ns >= (1ll << 31))
     return PPO_ERR_INVALID;
   size_t need = 0;
@@ -1320,6 +1359,7 @@ ppo_status ppo_segment_advantage(const float* rew, const float* done, const floa
                                  float* adv_norm, float* stats, void* work, size_t work_bytes,
                                  cudaStream_t st) {
   if (!rew || !done || !boot || !envs || !val || !adv || !ret || !work) return PPO_ERR_INVALID;
+  if (T > kGaeMaxT) return PPO_ERR_UNSUPPORTED;
   if (T < 1 || N < 1 || ns < 1 || T * N >= (1ll << 31) || T * ns >= (1ll << 31))
     return PPO_ERR_INVALID;
   size_t need = 0;
@@ -1382,6 +1422,7 @@ static ppo_status check_update_args(ppo_ctx* c, const float* obs, const int32_t*
                                     const float* stats) {
   if (!c || !val || !rew || !done || !boot) return PPO_ERR_INVALID;
   if (T < 1 || N < 1 || epochs < 1 || minibatches < 1) return PPO_ERR_INVALID;
+  if (T > kGaeMaxT) return PPO_ERR_UNSUPPORTED;
   const int64_t B = T * N;
   if (B > c->bmax || epochs > c->emax || B % minibatches != 0) return PPO_ERR_INVALID;
   if (c->cfg.adv_mode != 0 && N % minibatches != 0) return PPO_ERR_INVALID;
@@ -1575,6 +1616,7 @@ ppo_status ppo_update_host(ppo_ctx* c, const float* h_obs, const int32_t* h_act,
     return PPO_ERR_INVALID;
   if ((c->s.NH > 0 && !h_act) || (c->s.G > 0 && !h_actc)) return PPO_ERR_INVALID;
   if (T < 1 || N < 1 || epochs < 1 || minibatches < 1) return PPO_ERR_INVALID;
+  if (T > kGaeMaxT) return PPO_ERR_UNSUPPORTED;
   const int64_t B = T * N;
   if (B > c->bmax) return PPO_ERR_INVALID;
   const NetShape& s = c->s;
@@ -1621,6 +1663,22 @@ ppo_status ppo_update_host(ppo_ctx* c, const float* h_obs, const int32_t* h_act,
     PPO_CUDA(cudaMemcpyAsync(h_stats, c->st_stats, sizeof(float) * nstats,
                              cudaMemcpyDeviceToHost, st));
   PPO_CUDA(cudaStreamSynchronize(st));
+  return PPO_OK;
+}
+
+ppo_status ppo_set_step_trace(ppo_ctx* c, float* d_trace, int64_t max_steps) {
+  if (!c || max_steps < 0 || (d_trace == nullptr) != (max_steps == 0)) return PPO_ERR_INVALID;
+  if (d_trace && !al16(d_trace)) return PPO_ERR_ALIGN;
+  c->trace = d_trace;
+  c->trace_cap = max_steps;
+  c->gvalid = false;   // the cached update graph does not hold the copies
+  return PPO_OK;
+}
+
+ppo_status ppo_set_wait_limit(ppo_ctx* c, uint64_t limit_ns) {
+  if (!c) return PPO_ERR_INVALID;
+  c->wait_ns = limit_ns == 0 ? kTimeoutNs : limit_ns;
+  c->gvalid = false;   // the limit is a kernel argument inside the cached graph
   return PPO_OK;
 }
 

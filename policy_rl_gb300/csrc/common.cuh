@@ -228,6 +228,9 @@ struct Trace {
 
 // ---------------------------------------------------------------------------
 // Host-side launchers (defined in the .cu files).
+// Longest horizon the GAE kernels accept: a warp's moment count (at most
+// 32 * T) must stay exact in fp32 (below 2^24).
+constexpr int64_t kGaeMaxT = 1 << 19;
 cudaError_t launch_gae(const float* rew, const float* val, const float* done, const float* boot,
                        int T, int N, float gamma, float lambda, float* adv, float* ret,
                        double* partials, int num_partial_blocks, cudaStream_t st);

@@ -13,10 +13,15 @@
 // library holds it (kNoAllocScratchBytes) until the process exits.  Host code
 // cannot use the array's name as a device address, so the first call on each
 // device looks the address up with cudaGetSymbolAddress (with that device
-// current) and caches it; that first call should therefore come before any
-// stream capture.  All calls share the array: calls that overlap on the GPU
+// current) and caches it together with the device's current CUDA context;
+// that first call should therefore come before any stream capture.  A later
+// call that finds another context current on the device (the old one was
+// destroyed, e.g. by cudaDeviceReset, and the module loaded again) repeats
+// the look-up.  All calls share the array: calls that overlap on the GPU
 // (different streams without ordering, or different host threads) race on
 // it.  Each call overwrites every partial it reads, so nothing needs clearing.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -35,20 +40,37 @@ static __device__ __align__(256) unsigned char g_gae_scratch[kNoAllocScratchByte
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
 
-// Device address of g_gae_scratch on the current device (looked up once).
+// Device address of g_gae_scratch on the current device: looked up on the
+// first call, and again whenever the device's current context has changed.
 ppo_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PPO_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return PPO_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (g_ctx_get_current == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      cudaGetLastError();
+      return PPO_ERR_CUDA;
+    }
+    g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  }
+  CUcontext cur = nullptr;
+  if (g_ctx_get_current(&cur) != CUDA_SUCCESS || cur == nullptr) return PPO_ERR_CUDA;
+  if (g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != cur) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_gae_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return PPO_ERR_CUDA;
     }
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = cur;
   }
   *out = g_scratch_addr[dev];
   return PPO_OK;
@@ -65,6 +87,7 @@ extern "C" ppo_status ppo_gae_noalloc(const float* rew, const float* val, const 
   if (!rew || !val || !done || !boot || !adv || !ret) return PPO_ERR_INVALID;
   if (T < 1 || N < 1 || T * N >= (1ll << 31)) return PPO_ERR_INVALID;
   if (N > kNoAllocMaxN) return PPO_ERR_UNSUPPORTED;   // beyond the fixed scratch
+  if (T > ppo::kGaeMaxT) return PPO_ERR_UNSUPPORTED;
   const void* ps[] = {rew, val, done, boot, adv, ret, adv_norm, stats};
   for (const void* p : ps)
     if (p && !al16(p)) return PPO_ERR_ALIGN;

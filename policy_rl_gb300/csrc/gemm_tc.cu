@@ -54,17 +54,11 @@ struct Cfg {
   // backward-data kernels keep two TMA-loaded activation tiles (aux), which
   // also stage their output; forward kernels stage their output per warp
   static constexpr int AUX_SLOT = EPI == EPI_DACT ? BM * BN * 2 : 0;
-#ifndef PPO_DACT_AUX_SLOTS
-#define PPO_DACT_AUX_SLOTS 2
-#endif
-#ifndef PPO_DACT_STAGES
-#define PPO_DACT_STAGES 4
-#endif
-  static constexpr int NAUX = EPI == EPI_DACT ? PPO_DACT_AUX_SLOTS : 2;
+  static constexpr int NAUX = 2;
   // per-warp output staging: 64-column blocks of 32 rows (4 KB); a warp takes
   // 64 columns of a 256-column tile (16 epilogue warps) or half a 128-column one
   static constexpr int STG_WARP = EPI == EPI_BIAS_ACT ? 4096 : 0;
-  static constexpr int S = EPI == EPI_DACT ? PPO_DACT_STAGES
+  static constexpr int S = EPI == EPI_DACT ? 4
                          : EPI == EPI_BIAS_ACT ? (BN >= 256 ? 3 : 5)
                                                : (BN >= 128 ? 6 : 8);
   static constexpr int A_BYTES = BM * BK * 2;

@@ -26,6 +26,9 @@ namespace {
 constexpr int kT = 32;          // GEMM tile
 constexpr int kGThreads = 256;
 
+// Writes the constant 1 read by the bias-gradient products.
+__global__ void rnn_set_one_kernel(float* one) { *one = 1.f; }
+
 // C[m][n] (+)= sum_k A(m, k) B(n, k) (+ bias[n]) with A(m, k) = A[m sam + k sak],
 // B(n, k) = B[n sbn + k sbk]; each output summed over k in order by one thread.
 // Split-K (gridDim.z > 1): block z sums k in [z kc, (z + 1) kc) into the
@@ -310,8 +313,10 @@ cudaError_t launch_rnn_loss_grad(const RnnLaunch& a, cudaStream_t st) {
   const int thr = 256;
   cudaError_t e;
 #define RNN_TRY(x) do { if ((e = (x)) != cudaSuccess) return e; } while (0)
-  const float kOne = 1.f;
-  RNN_TRY(cudaMemcpyAsync(one, &kOne, sizeof(float), cudaMemcpyHostToDevice, st));
+  // the constant 1 the bias-gradient products read, written on the stream
+  // (no host memory involved, so the call can be captured)
+  rnn_set_one_kernel<<<1, 1, 0, st>>>(one);
+  RNN_TRY(cudaGetLastError());
   rnn_gather_kernel<<<(unsigned)((rows * D + thr - 1) / thr), thr, 0, st>>>(d, a.obs, a.envs, X);
   RNN_TRY(cudaGetLastError());
   // encoder: U0 = X W_enc^T
