@@ -463,12 +463,14 @@ ppo_status ppo_sync_status(ppo_ctx *ctx, cudaStream_t stream);
  * The next ppo_update re-captures its graph. */
 ppo_status ppo_set_step_trace(ppo_ctx *ctx, float *d_trace, int64_t max_steps);
 
-/* Limit, in nanoseconds of the GPU's global timer, of the bounded grid-barrier
- * waits of the cooperative kernels (gradient assembly + Adam inside
- * ppo_update; the fresh-advantage kernel).  A wait that runs past it latches
- * PPO_ERR_TIMEOUT (returned by the next ppo_sync_status); the kernel then
- * skips the rest of its work and returns (these kernels hold no asynchronous
- * copies or tensor memory).  The results of an update that timed out are
+/* Limit, in nanoseconds of the GPU's global timer, of the bounded waits of
+ * the cooperative kernels for one another's blocks: the grid barrier of
+ * gradient assembly + Adam inside ppo_update, those of the fresh-advantage
+ * kernel, and the weight-gradient kernel's wait for the other blocks of its
+ * output tile (taken after its own copies have completed and its tensor
+ * memory is freed).  A wait that runs past it latches PPO_ERR_TIMEOUT
+ * (returned by the next ppo_sync_status); the kernel then skips the rest of
+ * its work and returns, with no asynchronous copy or tensor memory held.  The results of an update that timed out are
  * undefined; the next update starts from cleared barrier counters.  0
  * restores the default (2 s).  The tensor-core kernels' pipeline waits keep
  * their own 2 s limit.  The next ppo_update re-captures its graph. */

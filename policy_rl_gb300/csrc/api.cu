@@ -59,6 +59,7 @@ struct ppo_ctx {
   unsigned* done_ctr = nullptr;
   int* err = nullptr;
   double* sq = nullptr;
+  unsigned* wctr = nullptr;   // weight-gradient tile counters [2][kWgradMaxTiles]
   Shadows sh{};
 
   // minibatch workspace
@@ -399,6 +400,8 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
   ra.grad = c->grad;
   ra.stats6 = stats6;
   ra.sq_part = nsq_out ? c->sq : nullptr;   // fused squared-norm partials for Adam
+  ra.weights_done = 0;
+  ra.nsq_pre = 0;
 
   if (c->bf16) {
     auto* X = static_cast<__nv_bfloat16*>(mr.X);
@@ -494,20 +497,36 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     PPO_CUDA(tc_gemm_dact(g5, H1, s.H1, s.act, dP1, s.H1, c->cs1, c->err, kTimeoutNs, ns, st, &n1));
     c->tr.mark(ST_DACT1, st);
     }
-    // weight gradients, split over the minibatch rows
+    // weight gradients, split over the minibatch rows; the kernel also sums
+    // the split partials into the flat gradient (dW3 from its transpose) and
+    // writes the squared-norm partials of those entries to sq[0 .. wg_grid)
     const WgradPlan wp = wgrad_plan(s, mb, ns);
-    WGradRegion regs[3] = {{dP2, s.H2, s.H2, H1, s.H1, s.H1, wp.kt[0], c->pW2},
-                           {dP1, s.H1, s.H1, X, s.Dp, s.Dp, wp.kt[1], c->pW1},
-                           {H2, s.H2, s.H2, dZ, c->lddz, 64, wp.kt[2], c->pW3}};
-    PPO_CUDA(tc_wgrad(regs, 3, M, 8192, 1024, c->err, kTimeoutNs, ns, st));
-    c->tr.mark(ST_WGRAD, st);
-    ra.pW1 = c->pW1; ra.s1 = tc_wgrad_splits(M, regs[1].kt_per_split); ra.ld1 = s.Dp;
-    ra.pW2 = c->pW2; ra.s2 = tc_wgrad_splits(M, regs[0].kt_per_split);
-    ra.pW3t = c->pW3; ra.s3 = tc_wgrad_splits(M, regs[2].kt_per_split); ra.ld3 = 64;
+    float* G = c->grad;
+    WGradRegion regs[3] = {
+        {dP2, s.H2, s.H2, H1, s.H1, s.H1, wp.kt[0], c->pW2, {G + s.oW2, s.H2, s.H1, s.H1, 1}},
+        {dP1, s.H1, s.H1, X, s.Dp, s.Dp, wp.kt[1], c->pW1, {G + s.oW1, s.H1, s.D, s.D, 1}},
+        {H2, s.H2, s.H2, dZ, c->lddz, 64, wp.kt[2], c->pW3, {G + s.oW3, s.H2, s.C, 1, s.H2}}};
+    // ... and the bias / log-std / statistic entries from the epilogues'
+    // per-CTA partial rows, so that its squared-norm partials cover the
+    // whole gradient and the optimizer follows directly
     ra.pb1 = c->cs1; ra.nb1 = n1;
     ra.pb2 = c->cs2; ra.nb2 = n2;
     ra.pb3 = c->cs3; ra.nb3 = n3; ra.ldb3 = s.CP;
     ra.ploss = c->lossp; ra.nl = n3;
+    if (!pre)   // standalone call: the tile counters start at zero (also after a timeout)
+      PPO_CUDA(cudaMemsetAsync(c->wctr, 0, 2 * kWgradMaxTiles * sizeof(unsigned), st));
+    int wg_grid = 0;
+    PPO_CUDA(tc_wgrad(regs, 3, M, 8192, 1024, c->err, kTimeoutNs, ns, st, c->wctr, c->sq,
+                      &wg_grid, c->wait_ns, &ra));
+    c->tr.mark(ST_WGRAD, st);
+    if (adam) {   // clip + Adam (its norm from the weight-gradient kernel's partials)
+      AdamArgs aa = *adam;
+      aa.sq_part = c->sq;
+      aa.nsq = wg_grid;
+      PPO_CUDA(launch_adam(aa, st, &c->tr));
+    }
+    if (nsq_out) *nsq_out = wg_grid;
+    return PPO_OK;
   } else {
     auto* X = static_cast<float*>(mr.X);
     auto* H1 = static_cast<float*>(c->H1);
@@ -562,14 +581,14 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
     ra.ploss = c->lossp; ra.nl = n3;
   }
   if (adam) {   // gradient assembly, clip and Adam in one cooperative launch
-    ra.sq_part = c->sq;
+    ra.sq_part = c->sq + ra.nsq_pre;
     PPO_CUDA(launch_reduce_adam(ra, *adam, c->rbar, c->err, c->wait_ns, c->num_sms, st));
     c->tr.mark(ST_REDUCE_ADAM, st);
     return PPO_OK;
   }
   PPO_CUDA(launch_reduce(ra, st));
   c->tr.mark(ST_REDUCE, st);
-  if (nsq_out) *nsq_out = reduce_blocks(s);
+  if (nsq_out) *nsq_out = ra.nsq_pre + reduce_launch_blocks(ra);
   return PPO_OK;
 }
 
@@ -782,6 +801,7 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
       PPO_CUDA(cudaMemsetAsync(c->rbar, 0, sizeof(unsigned), st));
       PPO_CUDA(cudaMemsetAsync(c->fbar, 0, sizeof(unsigned), st));
       PPO_CUDA(cudaMemsetAsync(c->done_ctr, 0, sizeof(unsigned), st));
+      PPO_CUDA(cudaMemsetAsync(c->wctr, 0, 2 * kWgradMaxTiles * sizeof(unsigned), st));
       PPO_CUDA(launch_perm(seed, 0, epochs, N, c->perm, c->perm_work, st, &c->tr));
     }
     if (!(parts & 2)) return PPO_OK;
@@ -829,6 +849,7 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
     else
       PPO_CUDA(cudaMemsetAsync(c->rbar, 0, sizeof(unsigned), st));
     PPO_CUDA(cudaMemsetAsync(c->done_ctr, 0, sizeof(unsigned), st));
+    PPO_CUDA(cudaMemsetAsync(c->wctr, 0, 2 * kWgradMaxTiles * sizeof(unsigned), st));
     PPO_CUDA(launch_gae(rew, val, done, boot, (int)T, (int)N, gamma, lambda, c->adv, c->ret,
                         c->gae_part, gae_num_blocks((int)N), st));
     c->tr.mark(ST_GAE, st);
@@ -966,7 +987,9 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
   A(c->phase_ns, kMkPhases);
   A(c->done_ctr, 1);
   A(c->err, 1);
-  A(c->sq, std::max(4096, reduce_blocks(s)));
+  // squared-norm partials: the weight-gradient kernel's (<= SMs), then the reduce's
+  A(c->sq, std::max(4096, reduce_blocks(s)) + c->num_sms);
+  A(c->wctr, 2 * kWgradMaxTiles);
   A(c->rbar, 1);
   A(c->fbar, 1);
   A(c->fpart, 3 * (int64_t)kFreshMaxGrid);

@@ -42,9 +42,40 @@ struct TcParams {
   uint64_t timeout_ns;
 };
 
+// Gradient assembly from the split-K and per-CTA partials (optim.cu, and the
+// weight-gradient kernel's vector tasks).
+struct ReduceArgs {
+  NetShape s;
+  const float* pW1; int s1; int ld1;    // [s1][H1][ld1]
+  const float* pW2; int s2;             // [s2][H2][H1]
+  const float* pW3t; int s3; int ld3;   // [s3][H2][ld3]  (dW3 transposed)
+  const float* pb1; int nb1;            // [nb1][H1]
+  const float* pb2; int nb2;            // [nb2][H2]
+  const float* pb3; int nb3; int ldb3;  // [nb3][ldb3]
+  const float* ploss; int nl;           // [nl][kLossPartials]
+  float inv_mb;
+  float* grad;                          // [P]
+  double* sq_part;                      // nullable: per-block sum of squares of grad
+  float* stats6;                        // nullable
+  int weights_done;                     // the weight entries of grad are already assembled
+                                        // (by the weight-gradient kernel): biases, log-std
+                                        // and statistics only
+  int nsq_pre;                          // squared-norm partials of the same gradient stored
+                                        // just before sq_part (by that kernel)
+};
+
 struct WRegion {
   int M, N, bn, tiles_m, tiles_n, splits, kt_per_split, k_tiles, unit_begin;
   float* part;  // [splits][M][N]
+};
+
+// Where the assembled gradient of a weight-gradient region goes: element
+// (m, n) of the region's product, m < rows and n < cols, is written to
+// dst[m * ldm + n * ldn].
+struct WFinal {
+  float* dst;
+  int rows, cols;
+  int64_t ldm, ldn;
 };
 
 struct WParams {
@@ -53,6 +84,18 @@ struct WParams {
   uint32_t mn_lbo, mn_sbo;
   int* err;
   uint64_t timeout_ns;
+  // in-kernel assembly (fixup != 0): the CTAs of one output tile meet at a
+  // per-tile counter and each sums a slice of the tile over the splits
+  int fixup;
+  WFinal f[3];
+  int tile_begin[3];   // first tile index of each region
+  unsigned* tile_ctr;  // [2][tiles] arrival / completion counters, zero between launches
+  double* sq_part;     // [gridDim.x] per-CTA sums of squares of the entries it wrote
+  uint64_t tile_wait_ns;   // limit of the wait for a tile's other CTAs (no copies in flight)
+  // the bias / log-std / statistic entries (nvt > 0): ra's vector tasks, one
+  // warp each, summed into the same per-CTA squared-norm partials
+  ReduceArgs ra;
+  int nvt;
 };
 
 // One weight-gradient product P[M][N] = sum_r U[r][0..M) (x) V[r][0..N),
@@ -64,7 +107,12 @@ struct WGradRegion {
   int ldv, N;
   int kt_per_split;   // 64-row k-tiles per split
   float* part;        // [splits][M][N] fp32
+  WFinal fin;         // in-kernel assembly target (fin.dst == nullptr: partials only)
 };
+
+// Largest tile count of a tc_wgrad call with in-kernel assembly (size of the
+// counter array: 2 * kWgradMaxTiles unsigned).
+constexpr int kWgradMaxTiles = 256;
 
 cudaError_t tc_prepare();
 int tc_pick_bn(int N);
@@ -81,9 +129,19 @@ cudaError_t tc_gemm_loss(const GemmOperands& g, const NetShape& s, LossCoef lc, 
                          float inv_mb, const float* b3, const float* logstd, __nv_bfloat16* dz,
                          int lddz, float* colsum_part, float* loss_part, int* err,
                          uint64_t timeout_ns, int num_sms, cudaStream_t st, int* grid_out);
+// Weight gradients of up to three regions.  With tile_ctr and sq_part given
+// (and every region's fin.dst set), the kernel is launched cooperatively and
+// also sums the split partials into the final gradient (fixed split order)
+// and writes per-CTA squared-norm partials sq_part[0 .. *grid_out).
+// timeout_ns bounds the TMA/MMA pipeline waits, tile_wait_ns (0: timeout_ns)
+// the wait of a CTA for the other CTAs of its tile.  With `vectors` (and the
+// assembly on), the kernel also runs that gradient's bias / log-std /
+// statistic sums, so that sq_part covers the whole gradient.
 cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lbo,
                      uint32_t mn_sbo, int* err, uint64_t timeout_ns, int num_sms,
-                     cudaStream_t st);
+                     cudaStream_t st, unsigned* tile_ctr = nullptr, double* sq_part = nullptr,
+                     int* grid_out = nullptr, uint64_t tile_wait_ns = 0,
+                     const ReduceArgs* vectors = nullptr);
 
 // ---- fp32 CUDA-core path ----------------------------------------------------
 // Generic-stride GEMM: C(m,n) = sum_k A(m,k) B(n,k) with
@@ -111,21 +169,8 @@ cudaError_t simt_head_loss(const NetShape& s, LossCoef lc, LossRows rows, float 
 int simt_head_blocks(int mb);
 
 // ---- reduction and optimizer --------------------------------------------------
-struct ReduceArgs {
-  NetShape s;
-  const float* pW1; int s1; int ld1;    // [s1][H1][ld1]
-  const float* pW2; int s2;             // [s2][H2][H1]
-  const float* pW3t; int s3; int ld3;   // [s3][H2][ld3]  (dW3 transposed)
-  const float* pb1; int nb1;            // [nb1][H1]
-  const float* pb2; int nb2;            // [nb2][H2]
-  const float* pb3; int nb3; int ldb3;  // [nb3][ldb3]
-  const float* ploss; int nl;           // [nl][kLossPartials]
-  float inv_mb;
-  float* grad;                          // [P]
-  double* sq_part;                      // nullable: per-block sum of squares of grad
-  float* stats6;                        // nullable
-};
-int reduce_blocks(const NetShape& s);
+int reduce_blocks(const NetShape& s);            // every entry: weights, biases, statistics
+int reduce_launch_blocks(const ReduceArgs& a);    // blocks of one launch (and its sq partials)
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st);
 
 struct Shadows {

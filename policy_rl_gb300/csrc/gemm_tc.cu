@@ -18,7 +18,12 @@
 //  * tc_wgrad_kernel: weight gradients dW = dPre^T X with K = minibatch rows.
 //    Both operands are read MN-major straight from the row-major activation
 //    buffers; K is split across CTAs and every split writes its own fp32
-//    partial tile, reduced later in a fixed order (deterministic, no atomics).
+//    partial tile.  In the learner step the launch is cooperative and the
+//    kernel assembles the gradient itself: the CTAs of an output tile meet at
+//    a per-tile counter and each sums a slice of the tile's rows over the
+//    splits in split order (deterministic, no float atomics), then runs a
+//    share of the bias / log-std / statistic sums and writes its part of the
+//    squared gradient norm.
 //
 // Every wait on an mbarrier is bounded (globaltimer); on expiry the kernel
 // latches kDevTimeout, stops issuing work, drains what it has in flight and
@@ -27,6 +32,7 @@
 
 #include "common.cuh"
 #include "gemm.h"
+#include "reduce.cuh"
 #include "tc_ptx.cuh"
 #include "tc_tile.cuh"
 
@@ -364,6 +370,115 @@ __device__ __forceinline__ void decode_unit(const WParams& p, int u, int& reg, i
   kt1 = min(R.k_tiles, kt0 + R.kt_per_split);
 }
 
+// Sum of the n <= kWgMaxSplits split partials q[0], q[st], ... (four
+// consecutive columns each) in split order; the loads of 16 splits are issued
+// before their adds.  L2 loads: the partials were written by other CTAs of
+// this launch.
+constexpr int kWgMaxSplits = 64;
+__device__ __forceinline__ float4 split_sum4_cg(const float* q, int64_t st, int n) {
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < n; s0 += 16) {
+    float4 x[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      x[j] = s0 + j < n ? __ldcg(reinterpret_cast<const float4*>(q + (s0 + j) * st))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (s0 + j < n) {
+        v.x += x[j].x;
+        v.y += x[j].y;
+        v.z += x[j].z;
+        v.w += x[j].w;
+      }
+  }
+  return v;
+}
+
+// In-kernel assembly of the weight gradient (cooperative launch: every CTA
+// is resident).  Each CTA first arrives on the counter of every output tile
+// it stored a split partial of; then, per unit, it waits (bounded) until all
+// splits of the tile have arrived and sums its share of the tile's rows --
+// split s of S takes rows [128 s / S, 128 (s + 1) / S) -- over the splits in
+// split order, writing the final gradient entries and the sum of their
+// squares (per CTA, fixed order) for the clip norm.  The last CTA of a tile to
+// finish clears its counters for the next launch.  On a timeout (or an
+// earlier abort of this CTA) it latches the error and writes no gradient.
+__device__ __noinline__ void wgrad_fixup(const WParams& p, bool aborted) {
+  __shared__ int s_ok;
+  __shared__ double s_sq[kThreads / kWarp];
+  double sq = 0.0;
+  if (!aborted) {
+    if (threadIdx.x == 0) {
+      __threadfence();
+      for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+        int reg, tm, tn, kt0, kt1, split;
+        decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
+        atomicAdd(p.tile_ctr + p.tile_begin[reg] + tm * p.r[reg].tiles_n + tn, 1u);
+      }
+    }
+    // the bias / log-std / statistic sums (their partial rows come from the
+    // kernels before this one), while the tiles' other CTAs finish
+    constexpr int kFixWarps = kThreads / kWarp;
+    for (int e = blockIdx.x * kFixWarps + (int)(threadIdx.x / kWarp); e < p.nvt;
+         e += gridDim.x * kFixWarps)
+      sq += reduce_vector_task(p.ra, e);
+    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+      int reg, tm, tn, kt0, kt1, split;
+      decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
+      const WRegion& R = p.r[reg];
+      const int t = p.tile_begin[reg] + tm * R.tiles_n + tn;
+      if (threadIdx.x == 0) {
+        int ok = 1;
+        if (ld_acquire_gpu(p.tile_ctr + t) < (unsigned)R.splits) {
+          const uint64_t t0 = ptx::globaltimer();
+          while (ld_acquire_gpu(p.tile_ctr + t) < (unsigned)R.splits) {
+            if (ptx::globaltimer() - t0 > p.tile_wait_ns) {
+              atomicOr(p.err, kDevTimeout);
+              ok = 0;
+              break;
+            }
+          }
+        }
+        s_ok = ok;
+      }
+      __syncthreads();
+      if (!s_ok) break;
+      const WFinal& F = p.f[reg];
+      const int r0 = BM * split / R.splits, r1 = BM * (split + 1) / R.splits;
+      const int q4 = R.bn / 4;   // four columns per work item
+      const int n_it = (r1 - r0) * q4;
+      const int64_t pst = (int64_t)R.M * R.N;
+      for (int e = threadIdx.x; e < n_it; e += kThreads) {
+        const int m = tm * BM + r0 + e / q4, n = tn * R.bn + 4 * (e % q4);
+        const float4 v = split_sum4_cg(R.part + (int64_t)m * R.N + n, pst, R.splits);
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (m < F.rows && n + j < F.cols) {
+            F.dst[m * F.ldm + (n + j) * F.ldn] = vv[j];
+            sq += (double)(vv[j] * vv[j]);
+          }
+      }
+      __syncthreads();
+      if (threadIdx.x == 0 &&
+          atomicAdd(p.tile_ctr + kWgradMaxTiles + t, 1u) == (unsigned)R.splits - 1) {
+        p.tile_ctr[t] = 0u;   // every CTA of the tile has passed its wait
+        p.tile_ctr[kWgradMaxTiles + t] = 0u;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  if (threadIdx.x % kWarp == 0) s_sq[threadIdx.x / kWarp] = sq;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < kThreads / kWarp; ++w) tot += s_sq[w];
+    p.sq_part[blockIdx.x] = tot;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant__ CUtensorMap tmV0,
                 const __grid_constant__ CUtensorMap tmU1, const __grid_constant__ CUtensorMap tmV1,
@@ -510,7 +625,13 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
       mbar_arrive(cb.tempty(acc));
       ++tc;
     }
-    if (lane == 0) bulk_wait0();   // this warp's stores are complete before the CTA exits
+    if (lane == 0) {
+      bulk_wait0();   // this warp's stores are complete before the CTA exits
+      if (p.fixup) {  // ... and visible to the other CTAs' loads of the tile
+        fence_proxy_async_global();
+        __threadfence();
+      }
+    }
   }
   __syncthreads();
   if (*abort_flag) {
@@ -529,6 +650,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem, W_TMEM_COLS);
   }
+  if (p.fixup) wgrad_fixup(p, *abort_flag != 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -730,7 +852,8 @@ cudaError_t tc_gemm_loss(const GemmOperands& g, const NetShape& s, LossCoef lc, 
 
 cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lbo,
                      uint32_t mn_sbo, int* err, uint64_t timeout_ns, int num_sms,
-                     cudaStream_t st) {
+                     cudaStream_t st, unsigned* tile_ctr, double* sq_part, int* grid_out,
+                     uint64_t tile_wait_ns, const ReduceArgs* vectors) {
   if (nreg < 1 || nreg > 3) return cudaErrorInvalidValue;
   CUtensorMap tu[3], tv[3], tp[3];
   WParams p{};
@@ -739,7 +862,15 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
   p.timeout_ns = timeout_ns;
   p.mn_lbo = mn_lbo;
   p.mn_sbo = mn_sbo;
-  int unit = 0;
+  p.fixup = tile_ctr != nullptr && sq_part != nullptr;
+  p.tile_ctr = tile_ctr;
+  p.sq_part = sq_part;
+  p.tile_wait_ns = tile_wait_ns ? tile_wait_ns : timeout_ns;
+  if (p.fixup && vectors) {
+    p.ra = *vectors;
+    p.nvt = reduce_vector_tasks(vectors->s);
+  }
+  int unit = 0, tiles = 0;
   for (int r = 0; r < nreg; ++r) {
     const WGradRegion& G = regs[r];
     if (G.M % BM != 0 || G.N % 64 != 0 || G.M > G.ldu || G.N > G.ldv) return cudaErrorInvalidValue;
@@ -761,7 +892,14 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
     R.unit_begin = unit;
     R.part = G.part;
     unit += R.tiles_m * R.tiles_n * R.splits;
+    if (p.fixup) {
+      if (G.fin.dst == nullptr || R.splits > kWgMaxSplits) return cudaErrorInvalidValue;
+      p.f[r] = G.fin;
+      p.tile_begin[r] = tiles;
+    }
+    tiles += R.tiles_m * R.tiles_n;
   }
+  if (p.fixup && tiles > kWgradMaxTiles) return cudaErrorInvalidValue;
   for (int r = nreg; r < 3; ++r) {
     tu[r] = tu[0];
     tv[r] = tv[0];
@@ -769,8 +907,28 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
   }
   p.total_units = unit;
   const int grid = unit < num_sms ? unit : num_sms;
-  return launch_pdl(tc_wgrad_kernel, dim3(grid), dim3(kThreads), W_SMEM, st, tu[0], tv[0], tu[1],
-                    tv[1], tu[2], tv[2], tp[0], tp[1], tp[2], p);
+  if (grid_out) *grid_out = grid;
+  if (!p.fixup)
+    return launch_pdl(tc_wgrad_kernel, dim3(grid), dim3(kThreads), W_SMEM, st, tu[0], tv[0],
+                      tu[1], tv[1], tu[2], tv[2], tp[0], tp[1], tp[2], p);
+  // cooperative: the CTAs of a tile wait for one another (one CTA per SM,
+  // grid <= SMs, so the launch is always resident); programmatic
+  // serialization lets its prologue overlap the previous kernel's tail (the
+  // kernel waits for that kernel's results before its first load)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = W_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, tc_wgrad_kernel, tu[0], tv[0], tu[1], tv[1], tu[2], tv[2],
+                            tp[0], tp[1], tp[2], p);
 }
 
 int tc_wgrad_bn(int N) { return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64); }

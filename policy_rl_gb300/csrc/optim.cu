@@ -11,6 +11,7 @@
 
 #include "common.cuh"
 #include "gemm.h"
+#include "reduce.cuh"
 #include "tc_ptx.cuh"
 
 namespace ppo {
@@ -28,25 +29,6 @@ constexpr int kAdamThreads = 256;
 // Every block also writes the sum of squares of the gradient entries it
 // produced (fixed order), for the clip norm.
 constexpr int kRedWarps = kRedThreads / kWarp;
-
-// Lane l sums rows l, l+32, ... in order (eight loads in flight per lane), then
-// a fixed xor-shuffle tree.
-__device__ __forceinline__ float warp_rows_sum(const float* base, int rows, int64_t stride) {
-  const int lane = threadIdx.x % kWarp;
-  float v = 0.f;
-  for (int b0 = lane; b0 < rows; b0 += 8 * kWarp) {
-    float x[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int b = b0 + u * kWarp;
-      x[u] = b < rows ? base[(int64_t)b * stride] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (b0 + u * kWarp < rows) v += x[u];
-  }
-  return warp_sum(v);
-}
 
 // Sum of n <= kMaxSplits split-K partials q[0], q[st], ... in split order, with
 // every load issued before the first add (one memory latency, not n).
@@ -97,37 +79,8 @@ __device__ __forceinline__ void reduce_block(const ReduceArgs& a, int vb, int we
       sq = (double)(v * v);
     }
   } else {
-    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int e = (vb - weight_blocks) * kRedWarps + warp;
-    const int nb = s.H1 + s.H2 + s.C + s.G;
-    if (e < nb) {
-      float v;
-      int i;
-      if (e < s.H1) {
-        i = (int)s.ob1 + e;
-        v = warp_rows_sum(a.pb1 + e, a.nb1, s.H1);
-      } else if (e < s.H1 + s.H2) {
-        const int j = e - s.H1;
-        i = (int)s.ob2 + j;
-        v = warp_rows_sum(a.pb2 + j, a.nb2, s.H2);
-      } else if (e < s.H1 + s.H2 + s.C) {
-        const int c = e - s.H1 - s.H2;
-        i = (int)s.ob3 + c;
-        v = warp_rows_sum(a.pb3 + c, a.nb3, a.ldb3);
-      } else {
-        const int g = e - s.H1 - s.H2 - s.C;
-        i = (int)s.ologstd + g;
-        v = warp_rows_sum(a.ploss + 6 + g, a.nl, kLossPartials);
-      }
-      if (lane == 0) {
-        a.grad[i] = v;
-        sq = (double)(v * v);
-      }
-    } else if (e < nb + 6) {
-      const int q = e - nb;
-      const float v = warp_rows_sum(a.ploss + q, a.nl, kLossPartials);
-      if (lane == 0 && a.stats6 != nullptr) a.stats6[q] = v * a.inv_mb;
-    }
+    const int warp = threadIdx.x / kWarp;
+    sq = reduce_vector_task(a, (vb - weight_blocks) * kRedWarps + warp);
   }
   if (a.sq_part != nullptr) {
 #pragma unroll
@@ -565,7 +518,7 @@ reduce_adam_kernel(ReduceArgs ra, AdamArgs aa, int weight_blocks, int nvb, unsig
   }
   __syncthreads();
   if (s_abort) return;
-  aa.nsq = nvb;
+  aa.nsq = ra.nsq_pre + nvb;   // the weight-gradient kernel's partials come first
   adam_body(aa, blockIdx.x, gridDim.x, bar);
 }
 
@@ -590,14 +543,24 @@ static int reduce_weight_blocks(const NetShape& s) {
   return (int)((nW + kRedThreads - 1) / kRedThreads);
 }
 
-int reduce_blocks(const NetShape& s) {
-  const int nb = s.H1 + s.H2 + s.C + s.G + 6;
-  return reduce_weight_blocks(s) + (nb + kRedWarps - 1) / kRedWarps;
+static int reduce_vector_blocks(const NetShape& s) {
+  return (reduce_vector_tasks(s) + kRedWarps - 1) / kRedWarps;
+}
+
+int reduce_blocks(const NetShape& s) { return reduce_weight_blocks(s) + reduce_vector_blocks(s); }
+
+// blocks of one reduce launch: the weight blocks only when the weight
+// entries are not yet assembled
+static int reduce_weight_blocks(const ReduceArgs& a) {
+  return a.weights_done ? 0 : reduce_weight_blocks(a.s);
+}
+int reduce_launch_blocks(const ReduceArgs& a) {
+  return reduce_weight_blocks(a) + reduce_vector_blocks(a.s);
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
-  return launch_pdl(reduce_kernel, dim3(reduce_blocks(a.s)), dim3(kRedThreads), 0, st, a,
-                    reduce_weight_blocks(a.s));
+  return launch_pdl(reduce_kernel, dim3(reduce_launch_blocks(a)), dim3(kRedThreads), 0, st, a,
+                    reduce_weight_blocks(a));
 }
 
 int g_reduce_adam_blocks_per_sm = 0;
@@ -614,11 +577,12 @@ cudaError_t reduce_adam_prepare() {
 cudaError_t launch_reduce_adam(const ReduceArgs& ra, const AdamArgs& aa, unsigned* bar, int* err,
                                uint64_t limit_ns, int num_sms, cudaStream_t st) {
   if (g_reduce_adam_blocks_per_sm <= 0) return cudaErrorInitializationError;
-  const int nvb = reduce_blocks(ra.s);
+  const int nvb = reduce_launch_blocks(ra);
   // up to 4 resident blocks per SM: one virtual block of reduce work each at
-  // the usual sizes (one block per SM measured slower: serial reduce work)
+  // the usual sizes (one block per SM measured slower: serial reduce work);
+  // at least one block per SM for the Adam pass
   int grid = num_sms * (g_reduce_adam_blocks_per_sm < 4 ? g_reduce_adam_blocks_per_sm : 4);
-  if (grid > nvb) grid = nvb;
+  if (grid > nvb) grid = nvb > num_sms ? nvb : num_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kRedThreads);
@@ -631,7 +595,7 @@ cudaError_t launch_reduce_adam(const ReduceArgs& ra, const AdamArgs& aa, unsigne
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, reduce_adam_kernel, ra, aa, reduce_weight_blocks(ra.s), nvb, bar,
+  return cudaLaunchKernelEx(&cfg, reduce_adam_kernel, ra, aa, reduce_weight_blocks(ra), nvb, bar,
                             err, limit_ns);
 }
 

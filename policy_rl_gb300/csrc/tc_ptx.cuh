@@ -96,6 +96,16 @@ __device__ __forceinline__ void bulk_wait0() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// orders this thread's completed async-proxy (TMA) global writes with its
+// later generic-proxy operations
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void prefetch_tmap(const void* p) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)p) : "memory");
 }
