@@ -446,10 +446,31 @@ fresh_adv_kernel(FreshAdvArgs a) {
   __syncthreads();
   pdl_trigger();
   if (a.adv_norm) {
+    // float4 groups, four groups per thread in flight, then the rows % 4
+    // tail (all scalar when a pointer is not 16-byte aligned: a minibatch's
+    // rows inside the update start at k * T * ns)
     const float mean = s_stats[0], inv = 1.f / (s_stats[1] + 1e-8f);
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.adv) |
+                       reinterpret_cast<uintptr_t>(a.adv_norm)) & 15u) == 0;
+    const int64_t n4 = vec ? rows / 4 : 0;
+    const float4* a4 = reinterpret_cast<const float4*>(a.adv);
+    float4* o4 = reinterpret_cast<float4*>(a.adv_norm);
+    const int64_t tid = (int64_t)blockIdx.x * kFreshThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kFreshThreads;
-    for (int64_t i = (int64_t)blockIdx.x * kFreshThreads + threadIdx.x; i < rows; i += stride)
-      a.adv_norm[i] = (a.adv[i] - mean) * inv;
+    auto nrm = [&](float4 v) {
+      return make_float4((v.x - mean) * inv, (v.y - mean) * inv, (v.z - mean) * inv,
+                         (v.w - mean) * inv);
+    };
+    int64_t i = tid;
+    for (; i + 3 * stride < n4; i += 4 * stride) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcs(a4 + i + u * stride);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) __stcs(o4 + i + u * stride, nrm(v[u]));
+    }
+    for (; i < n4; i += stride) __stcs(o4 + i, nrm(__ldcs(a4 + i)));
+    for (int64_t k = n4 * 4 + tid; k < rows; k += stride) a.adv_norm[k] = (a.adv[k] - mean) * inv;
   }
   // the last block out resets the barrier counter for the next launch
   if (threadIdx.x == 0) {
