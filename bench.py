@@ -22,9 +22,12 @@ headline workload (all host cores, and one core).
 
 --impl reference times the oracle itself (the CPU reference implementation)
 on a bounded slice per step.  --drive runs plain driver loops for profilers.
-Multi-GPU (torchrun): every rank runs an independent replica on its own GPU;
-value sums the samples of all ranks over the slowest rank's time (weak
-scaling, no data-path collective).
+Multi-GPU (torchrun): one data-parallel update over the ranks, each rank
+holding its own N environments (weak scaling): shard GAE, the advantage
+moments all-gathered, per-rank minibatch slices, the flat gradient
+all-reduced over NCCL before every optimizer step; value sums the samples
+of all ranks over the slowest rank's time.  (With --advantages other than
+global the ranks run independent replicas.)
 """
 from __future__ import annotations
 
@@ -270,6 +273,11 @@ def _measure(w, args, world, rank, local, stream, peaks, adv_mode=0, optimizer=0
     ro = synth.rollout(w, seed=rank, with_obs=not big)
     p0 = synth.init_params(w)
     ctx = P.Context(P.config_from_workload(w, adv_mode=adv_mode, optimizer=optimizer), p0)
+    # N > 1 ranks: one data-parallel update over the ranks' environment shards
+    # (each rank its own N envs; the gradient all-reduced over NCCL every step)
+    dp = world > 1 and adv_mode == 0
+    if dp:
+        ctx.set_collective(world, rank, P.TorchCollective())
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
     if big:
         g = torch.Generator(device="cuda")
@@ -314,9 +322,14 @@ def _measure(w, args, world, rank, local, stream, peaks, adv_mode=0, optimizer=0
     ms = _max_over_ranks(float(np.mean(step_ms)), world)
     value = world * B / (ms / 1e3)
 
-    # one profiled update: per-kernel device time, launches
+    # one profiled update: per-kernel device time, launches (the single-rank
+    # update: the same kernels, without the collectives)
+    if dp:
+        ctx.set_collective(1, 0)
     with torch.cuda.stream(stream):
         prof = P.ppo_update_profile(ctx.handle, *args_dev, *hp, stats=stats, stream=stream)
+    if dp:
+        ctx.set_collective(world, rank, ctx._collective)
     kern = {k: v for k, v in prof.items() if not k.startswith("phase:")}
     phases = {k: v for k, v in prof.items() if k.startswith("phase:")}
     launches_per_update = sum(c for _, c in kern.values())
@@ -375,6 +388,9 @@ def _measure(w, args, world, rank, local, stream, peaks, adv_mode=0, optimizer=0
         "roofline": roof, "gemm_all": gemm_all, "stages": stages,
         "profiled_update_ms": round(total_ms, 4),
         "launches_per_update": launches_per_update, "clocks": clk,
+        "parallelism": (f"data-parallel x{world}: env shards, shard moments all-gathered, "
+                        f"gradient all-reduced (NCCL) every minibatch" if dp
+                        else f"replicas x{world}"),
     }
     return summary, ctx, obs_d
 
@@ -437,7 +453,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded mulberry32 rollout with the workload's shapes and value "
                 "distributions; random-init weights)",
         "config": {"workload": head["workload"],
-                   "global_batch": world * w.B, "parallelism": f"replicas x{world}",
+                   "global_batch": world * w.B, "parallelism": head["parallelism"],
                    "l2": "flushed between timed steps (256 MB write)",
                    "timing": "CUDA events per update on the launching stream, mean over steps"},
         "gpu_launches": head["launches_per_update"] * args.steps,

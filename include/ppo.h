@@ -447,6 +447,43 @@ ppo_status ppo_update_profile(ppo_ctx *ctx, const float *d_obs, const int32_t *d
  * the last call (PPO_ERR_TIMEOUT if a bounded wait gave up), clearing it. */
 ppo_status ppo_sync_status(ppo_ctx *ctx, cudaStream_t stream);
 
+/* ---- Data-parallel learner ---------------------------------------------------
+ * "PlayTrain", App. C.3 (the learner trained data-parallel over GPUs with DDP,
+ * Table 8 "2 DDP + 2 inference GPUs"), applied to the update of sec. 6 of
+ * "Teaching Mario to speedrun".  With world > 1, each of `world` processes
+ * (one GPU each) calls ppo_update on its own shard of environments -- the
+ * [T, N_r] rollout of its N_r envs, the same T, epochs, minibatches and
+ * seed on every rank, the same N_r on every rank -- and the update becomes:
+ *   GAE on the shard; the shard's advantage moments (count, mean, M2) in
+ *   fp64, all-gathered, merged in a fixed order into the global mean and
+ *   std (every rank the same values); per epoch the shard's own
+ *   permutation by the single-GPU rule (seed, epoch, B_r = T*N_r); minibatch
+ *   m is the union of the ranks' m-th slices, so the loss of rank r's rows
+ *   is scaled by 1/(world * B_r/minibatches); after gradient assembly the
+ *   flat gradient (and the minibatch statistics) are sum-all-reduced, and
+ *   every rank takes the same clip + optimizer step.
+ * The library issues its collectives through `fn`, called on the host while
+ * the update is enqueued, in the same order on every rank:
+ *   op PPO_COLL_ALLREDUCE_SUM_F32: d_buf fp32 [count], summed in place over
+ *     the ranks;
+ *   op PPO_COLL_ALLGATHER_F64: d_buf fp64 [world][count], this rank's count
+ *     values at d_buf + rank*count on entry, every rank's on return;
+ * each enqueued on `stream` (device pointers, stream order); fn returns 0 on
+ * success (anything else: the update returns PPO_ERR_CUDA).  The Python
+ * binding supplies one over torch.distributed.  With world > 1 ppo_update is
+ * enqueued directly rather than from a cached CUDA graph; the fresh-advantage
+ * modes (adv_mode 1, 2), the persistent minibatch kernel and
+ * ppo_update_profile return PPO_ERR_UNSUPPORTED.  world == 1 (the default)
+ * restores the single-GPU update; fn may then be NULL. */
+typedef enum {
+    PPO_COLL_ALLREDUCE_SUM_F32 = 0,
+    PPO_COLL_ALLGATHER_F64 = 1
+} ppo_collective_op;
+typedef int (*ppo_collective_fn)(void *user, int32_t op, void *d_buf, int64_t count,
+                                 cudaStream_t stream);
+ppo_status ppo_set_collective(ppo_ctx *ctx, int32_t world, int32_t rank, ppo_collective_fn fn,
+                              void *user);
+
 /* ---- Inspection and failure handling ----------------------------------------
  * Step trace of the whole update ("Teaching Mario to speedrun", sec. 6 "The
  * whole algorithm": one backward pass and one optimizer step per minibatch).

@@ -143,6 +143,12 @@ def lib():
         L.orc_rnn_update.argtypes = [ctypes.POINTER(_Rnn), ctypes.POINTER(_Hyper), _I64, _I64, _I64,
                                      _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                      ctypes.POINTER(_I64), _P]
+        L.orc_moments3.argtypes = [_I64, _P, _P]
+        L.orc_moments_merge.argtypes = [_P, _P, _P]
+        L.orc_update_sharded.restype = ctypes.c_int
+        L.orc_update_sharded.argtypes = [ctypes.POINTER(_Net), ctypes.POINTER(_Hyper), _I64, _I64,
+                                         _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                         _P, _P, _P, ctypes.POINTER(_I64), _P]
         L.orc_threads.argtypes = []
         L.orc_threads.restype = ctypes.c_int
         L.orc_set_threads.argtypes = [ctypes.c_int]
@@ -424,6 +430,23 @@ def moments(x):
     return m.value, s.value
 
 
+def moments3(x):
+    """(count, mean, M2) of x (two-pass)."""
+    x = _as(x, np.float64).ravel()
+    out = np.empty(3, np.float64)
+    lib().orc_moments3(x.size, _ptr(x), _ptr(out))
+    return out
+
+
+def moments_merge(a, b):
+    """Pairwise merge of two (count, mean, M2) triples."""
+    a = _as(a, np.float64)
+    b = _as(b, np.float64)
+    out = np.empty(3, np.float64)
+    lib().orc_moments_merge(_ptr(a), _ptr(b), _ptr(out))
+    return out
+
+
 def normalize(x, mean, std):
     x = _as(x, np.float64)
     out = np.empty_like(x)
@@ -561,3 +584,27 @@ def update(net: Net, hp: Hyper, T, N, epochs, minibatches, obs, act_disc, act_co
                      *[_ptr(a) for a in arrs], _ptr(params), _ptr(m), _ptr(v), _ptr(mom),
                      ctypes.byref(st), _ptr(stats), _ptr(adv), _ptr(ret))
     return UpdateResult(params, m, v, mom, st.value, stats, adv.reshape(T, N), ret.reshape(T, N))
+
+
+def update_sharded(net: Net, hp: Hyper, world, T, N, epochs, minibatches, obs, act_disc,
+                   act_cont, logp_old, val, rew, done, boot, params, m=None, v=None, step=0,
+                   mom=None) -> UpdateResult:
+    """The update data-parallel over `world` env shards of the [T][N] rollout
+    (one process; see orc_update_sharded)."""
+    P = net.num_params
+    params = _as(params, np.float64).copy()
+    m = np.zeros(P) if m is None else _as(m, np.float64).copy()
+    v = np.zeros(P) if v is None else _as(v, np.float64).copy()
+    mom = np.zeros(P) if mom is None else _as(mom, np.float64).copy()
+    stats = np.empty((epochs * minibatches, 6), np.float64)
+    st = _I64(step)
+    arrs = [_as(obs, np.float32), _as(act_disc, np.int32),
+            _as(act_cont if act_cont is not None else np.zeros(1), np.float32),
+            _as(logp_old, np.float32), _as(val, np.float32), _as(rew, np.float32),
+            _as(done, np.float32), _as(boot, np.float32)]
+    cn, ch = net.c(), hp.c()
+    if lib().orc_update_sharded(ctypes.byref(cn), ctypes.byref(ch), world, T, N, epochs,
+                                minibatches, *[_ptr(a) for a in arrs], _ptr(params), _ptr(m),
+                                _ptr(v), _ptr(mom), ctypes.byref(st), _ptr(stats)) != 0:
+        raise ValueError("world must divide N and minibatches must divide T*N/world")
+    return UpdateResult(params, m, v, mom, st.value, stats, None, None)

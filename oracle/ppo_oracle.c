@@ -116,6 +116,36 @@ void orc_moments(int64_t n, const double *x, double *mean, double *std_unbiased)
     *std_unbiased = (n > 1) ? sqrt(ss / (double)(n - 1)) : 0.0;
 }
 
+/* (count, mean, M2) of x[0..n), M2 the sum of squared deviations from the
+ * mean, by the two-pass definition. */
+void orc_moments3(int64_t n, const double *x, double out[3])
+{
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s += x[i];
+    const double mu = (n > 0) ? s / (double)n : 0.0;
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; ++i) ss += (x[i] - mu) * (x[i] - mu);
+    out[0] = (double)n;
+    out[1] = mu;
+    out[2] = ss;
+}
+
+/* The (count, mean, M2) of the union of two sets from theirs (Chan, Golub
+ * and LeVeque's pairwise combination): with d = mean_b - mean_a,
+ *   n = n_a + n_b,  mean = mean_a + d n_b / n,  M2 = M2_a + M2_b + d^2 n_a n_b / n.
+ * out may alias a or b. */
+void orc_moments_merge(const double a[3], const double b[3], double out[3])
+{
+    if (a[0] == 0.0) { out[0] = b[0]; out[1] = b[1]; out[2] = b[2]; return; }
+    if (b[0] == 0.0) { out[0] = a[0]; out[1] = a[1]; out[2] = a[2]; return; }
+    const double n = a[0] + b[0], d = b[1] - a[1];
+    const double mean = a[1] + d * (b[0] / n);
+    const double m2 = a[2] + b[2] + d * d * (a[0] * b[0] / n);
+    out[0] = n;
+    out[1] = mean;
+    out[2] = m2;
+}
+
 void orc_normalize(int64_t n, const double *x, double mean, double std_, double *out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = (x[i] - mean) / (std_ + 1e-8);
@@ -1151,4 +1181,95 @@ void orc_update(const orc_net *net, const orc_hyper *hp, int64_t T, int64_t N,
     if (adv_out) memcpy(adv_out, adv, sizeof(double) * (size_t)B);
     if (ret_out) memcpy(ret_out, ret, sizeof(double) * (size_t)B);
     free(adv); free(ret); free(perm); free(grad);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The update of "Teaching Mario to speedrun", sec. 6, data-parallel over
+ * `world` learners ("PlayTrain", App. C.3: the learner trained with DDP on
+ * several GPUs), emulated in one process.  The rollout [T][N] is split by
+ * environment: rank r holds envs [r Nr, (r + 1) Nr), Nr = N / world.  Each
+ * rank runs GAE on its shard; the advantage statistics are those of all T*N
+ * advantages, from the shards' (count, mean, M2) merged in rank order; per
+ * epoch every rank permutes its own Br = T*Nr rows with orc_perm(seed, e, Br)
+ * and minibatch k is the union of the ranks' k-th slices of Br/minibatches
+ * rows.  The minibatch loss is the mean over that union, so its gradient is
+ * the mean over the ranks of each rank's own minibatch gradient (equal
+ * slice sizes); then clip and the optimizer, as in orc_update.  Returns -1
+ * (changing nothing) unless world divides N and minibatches divides Br. */
+int orc_update_sharded(const orc_net *net, const orc_hyper *hp, int64_t world, int64_t T,
+                       int64_t N, int64_t epochs, int64_t minibatches, const float *obs,
+                       const int32_t *act_disc, const float *act_cont, const float *logp_old,
+                       const float *val, const float *rew, const float *done, const float *boot,
+                       double *params, double *m, double *v, double *mom, int64_t *step,
+                       double *stats)
+{
+    if (world < 1 || N % world != 0 || minibatches < 1) return -1;
+    const int64_t Nr = N / world, Br = T * Nr;
+    if (Br % minibatches != 0) return -1;
+    const int64_t mbr = Br / minibatches, P = orc_num_params(net);
+    double *adv = (double *)malloc(sizeof(double) * (size_t)(T * N));
+    double *ret = (double *)malloc(sizeof(double) * (size_t)(T * N));
+    float *sr = (float *)malloc(sizeof(float) * (size_t)Br);
+    float *sv = (float *)malloc(sizeof(float) * (size_t)Br);
+    float *sd = (float *)malloc(sizeof(float) * (size_t)Br);
+    double *sa = (double *)malloc(sizeof(double) * (size_t)Br);
+    double *sret = (double *)malloc(sizeof(double) * (size_t)Br);
+    int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * (size_t)Br);
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)mbr);
+    double *g = (double *)malloc(sizeof(double) * (size_t)P);
+    double *gsum = (double *)malloc(sizeof(double) * (size_t)P);
+
+    /* judge: GAE per shard, statistics of the union */
+    double tot[3] = {0.0, 0.0, 0.0};
+    for (int64_t r = 0; r < world; ++r) {
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t j = 0; j < Nr; ++j) {
+                const int64_t gi = t * N + r * Nr + j;
+                sr[t * Nr + j] = rew[gi];
+                sv[t * Nr + j] = val[gi];
+                sd[t * Nr + j] = done[gi];
+            }
+        orc_gae(T, Nr, sr, sv, sd, boot + r * Nr, hp->gamma, hp->lambda, sa, sret);
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t j = 0; j < Nr; ++j) {
+                adv[t * N + r * Nr + j] = sa[t * Nr + j];
+                ret[t * N + r * Nr + j] = sret[t * Nr + j];
+            }
+        double mr[3];
+        orc_moments3(Br, sa, mr);
+        orc_moments_merge(tot, mr, tot);
+    }
+    const double mean = tot[1];
+    const double sdv = tot[0] > 1.0 ? sqrt(tot[2] / (tot[0] - 1.0)) : 0.0;
+
+    /* learn */
+    const orc_loss_cfg lc = {hp->clip, hp->vf_coef, hp->ent_coef, hp->bf16_operands};
+    for (int64_t e = 0; e < epochs; ++e) {
+        orc_perm(hp->seed, e, Br, perm);   /* every rank: the same rule over its Br rows */
+        for (int64_t k = 0; k < minibatches; ++k) {
+            double st[6] = {0, 0, 0, 0, 0, 0};
+            memset(gsum, 0, sizeof(double) * (size_t)P);
+            for (int64_t r = 0; r < world; ++r) {
+                for (int64_t i = 0; i < mbr; ++i) {
+                    const int64_t b = perm[k * mbr + i];   /* local row t * Nr + j */
+                    idx[i] = (int32_t)((b / Nr) * N + r * Nr + b % Nr);
+                }
+                double st_r[6];
+                orc_loss_grad(net, &lc, params, mbr, idx, obs, act_disc, act_cont, logp_old,
+                              adv, ret, 1, mean, sdv, g, st_r, NULL);
+                for (int64_t i = 0; i < P; ++i) gsum[i] += g[i];
+                for (int q = 0; q < 6; ++q) st[q] += st_r[q];
+            }
+            for (int64_t i = 0; i < P; ++i) gsum[i] /= (double)world;
+            if (stats)
+                for (int q = 0; q < 6; ++q)
+                    stats[(e * minibatches + k) * 6 + q] = st[q] / (double)world;
+            orc_clip_grad_norm(P, gsum, hp->max_grad_norm);
+            *step += 1;
+            orc_optimize(net, hp, P, params, gsum, m, v, mom, *step);
+        }
+    }
+    free(adv); free(ret); free(sr); free(sv); free(sd); free(sa); free(sret);
+    free(perm); free(idx); free(g); free(gsum);
+    return 0;
 }

@@ -57,6 +57,10 @@ void orc_segment_advantage(int64_t T, int64_t N, const float *rew, const float *
 void orc_moments(int64_t n, const double *x, double *mean, double *std_unbiased);
 
 /* out[i] = (x[i] - mean) / (std + 1e-8) */
+/* (count, mean, M2) of x[0..n) (two-pass), and the pairwise merge of two
+ * such triples (Chan, Golub and LeVeque); out may alias a or b. */
+void orc_moments3(int64_t n, const double *x, double out[3]);
+void orc_moments_merge(const double a[3], const double b[3], double out[3]);
 void orc_normalize(int64_t n, const double *x, double mean, double std_, double *out);
 
 /* Minibatch permutation of epoch `epoch`: key i = mulberry32 draw number
@@ -227,6 +231,19 @@ int orc_rnn_update(const orc_rnn *r, const orc_hyper *hp, int64_t T, int64_t N, 
                    const float *act_cont, const float *logp_old, const float *val,
                    const float *rew, const float *done, const float *boot, const double *h0,
                    double *params, double *m, double *v, int64_t *step, double *stats);
+
+/* The update data-parallel over `world` ranks, emulated in one process: rank
+ * r holds envs [r N/world, (r+1) N/world) of the [T][N] rollout; shard GAE,
+ * statistics from the merged shard moments, per-rank permutations of the
+ * shard's rows, minibatch k = the union of the ranks' k-th slices, gradient
+ * = mean over the ranks (see ppo_oracle.c).  Returns -1 unless world divides
+ * N and minibatches divides T*N/world. */
+int orc_update_sharded(const orc_net *net, const orc_hyper *hp, int64_t world, int64_t T,
+                       int64_t N, int64_t epochs, int64_t minibatches, const float *obs,
+                       const int32_t *act_disc, const float *act_cont, const float *logp_old,
+                       const float *val, const float *rew, const float *done, const float *boot,
+                       double *params, double *m, double *v, double *mom, int64_t *step,
+                       double *stats);
 
 #ifdef __cplusplus
 }

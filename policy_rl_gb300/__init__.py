@@ -23,7 +23,7 @@ __all__ = [
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
     "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "ppo_set_step_trace",
-    "ppo_set_wait_limit", "library_path",
+    "ppo_set_wait_limit", "ppo_set_collective", "TorchCollective", "library_path",
 ]
 
 
@@ -294,6 +294,63 @@ def ppo_sync_status(ctx, stream=None) -> None:
     _abi.check(_lib().ppo_sync_status(ctx, _stream(stream)), "ppo_sync_status")
 
 
+def ppo_set_collective(ctx, world: int, rank: int, fn=None, user=None) -> None:
+    """Registers the collective of the data-parallel update (see ppo.h); fn is
+    an _abi.COLLECTIVE_FN (e.g. TorchCollective(...).fn)."""
+    cfn = fn if fn is not None else ctypes.cast(None, _abi.COLLECTIVE_FN)
+    _abi.check(_lib().ppo_set_collective(ctx, world, rank, cfn, user), "ppo_set_collective")
+
+
+class TorchCollective:
+    """The library's collective over torch.distributed: an in-place sum
+    all-reduce of fp32 buffers and an all-gather of fp64 buffers, issued on
+    the stream the library passes (so that they are ordered with its
+    kernels).  device: "cuda" (NCCL; buffers are device pointers) or "cpu"
+    (gloo; host pointers).  Keep the object alive while the context uses it."""
+
+    def __init__(self, group=None, device: str = "cuda"):
+        self.group = group
+        self.device = device
+        self.fn = _abi.COLLECTIVE_FN(self._call)
+        self.error = None
+
+    def _view(self, ptr: int, n: int, fp64: bool):
+        import torch
+        if self.device == "cuda":
+            return torch.as_tensor(_DevArray(ptr, n, "<f8" if fp64 else "<f4"), device="cuda")
+        import numpy as np
+        ct = ctypes.c_double if fp64 else ctypes.c_float
+        return torch.from_numpy(np.ctypeslib.as_array((ct * n).from_address(ptr)))
+
+    def _call(self, user, op, buf, count, stream):
+        try:
+            import contextlib
+            import torch
+            import torch.distributed as dist
+            world = dist.get_world_size(self.group)
+            rank = dist.get_rank(self.group)
+            # the library's stream (the legacy default stream arrives as NULL)
+            if self.device != "cuda":
+                ctxm = contextlib.nullcontext()
+            else:
+                ctxm = torch.cuda.stream(torch.cuda.ExternalStream(stream) if stream
+                                         else torch.cuda.default_stream())
+            with ctxm:
+                if op == _abi.COLL_ALLREDUCE_SUM_F32:
+                    dist.all_reduce(self._view(buf, count, False), group=self.group)
+                elif op == _abi.COLL_ALLGATHER_F64:
+                    t = self._view(buf, world * count, True)
+                    parts = list(t.split(count))
+                    mine = parts[rank].clone()
+                    dist.all_gather(parts, mine, group=self.group)
+                else:
+                    return 1
+            return 0
+        except Exception as e:   # reported to the library as a failed collective
+            self.error = e
+            return 1
+
+
 def ppo_set_step_trace(ctx, trace=None, max_steps: int = 0) -> None:
     """Per-step copies of params, m, v and the gradient inside ppo_update (see ppo.h)."""
     _abi.check(_lib().ppo_set_step_trace(ctx, _ptr(trace), max_steps), "ppo_set_step_trace")
@@ -362,3 +419,10 @@ class Context:
 
     def set_wait_limit(self, limit_ns: int = 0):
         return ppo_set_wait_limit(self.handle, limit_ns)
+
+    def set_collective(self, world: int, rank: int, collective=None):
+        """Data-parallel update over `world` ranks (collective: a
+        TorchCollective, or None with world == 1)."""
+        self._collective = collective   # kept alive with the context
+        return ppo_set_collective(self.handle, world, rank,
+                                  collective.fn if collective is not None else None)

@@ -21,7 +21,7 @@ SYMBOLS = (
     "ppo_perm_workspace_bytes", "ppo_minibatch_perm", "ppo_minibatch_loss_grad",
     "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_adam_step", "ppo_muon_step",
     "ppo_rnn_param_count", "ppo_rnn_workspace_bytes", "ppo_rnn_loss_grad", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
-    "ppo_sync_status", "ppo_set_step_trace", "ppo_set_wait_limit",
+    "ppo_sync_status", "ppo_set_collective", "ppo_set_step_trace", "ppo_set_wait_limit",
 )
 NUM_STAGES = 34
 NUM_KERNEL_STAGES = 25
@@ -64,6 +64,12 @@ class RnnConfig(ctypes.Structure):
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
+
+# ppo_collective_fn: int (*)(void* user, int32_t op, void* d_buf, int64_t count, cudaStream_t)
+COLLECTIVE_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                 ctypes.c_int64, ctypes.c_void_p)
+COLL_ALLREDUCE_SUM_F32 = 0
+COLL_ALLGATHER_F64 = 1
 _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 _lib = None
@@ -120,6 +126,7 @@ def load(path: str = LIB_PATH):
         "ppo_update_profile": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F,
                                 _F, _F, u32, _P, _P, _P, _P], ctypes.c_int),
         "ppo_sync_status": ([_P, _P], ctypes.c_int),
+        "ppo_set_collective": ([_P, i32, i32, COLLECTIVE_FN, _P], ctypes.c_int),
         "ppo_set_step_trace": ([_P, _P, _I64], ctypes.c_int),
         "ppo_set_wait_limit": ([_P, ctypes.c_uint64], ctypes.c_int),
     }

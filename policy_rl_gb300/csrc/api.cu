@@ -102,6 +102,13 @@ struct ppo_ctx {
   int64_t trace_cap = 0;
   // limit of the cooperative kernels' grid-barrier waits (ppo_set_wait_limit)
   uint64_t wait_ns = kTimeoutNs;
+  // data-parallel learner (ppo_set_collective): this rank of `world`, the
+  // caller's collective, the gathered shard moments [world][3]
+  int world = 1, rank = 0;
+  ppo_collective_fn coll = nullptr;
+  void* coll_user = nullptr;
+  double* mom_all = nullptr;
+  int mom_cap = 0;
 
   // host-update staging (allocated on first ppo_update_host)
   float *st_obs = nullptr, *st_actc = nullptr, *st_logp = nullptr, *st_val = nullptr,
@@ -339,7 +346,8 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
                              const float* adv, const float* ret, const int32_t* idx, int64_t B,
                              int64_t mb, const float* adv_stats, float* stats6, cudaStream_t st,
                              int* nsq_out = nullptr, const MbRows* pre = nullptr,
-                             const AdamArgs* adam = nullptr, const FreshSpec* fr = nullptr) {
+                             const AdamArgs* adam = nullptr, const FreshSpec* fr = nullptr,
+                             int64_t mb_global = 0) {
   const NetShape& s = c->s;
   MbRows mr{c->X, c->act_mb, c->actc_mb, c->logp_mb, c->adv_mb, c->ret_mb};
   if (pre) {
@@ -352,7 +360,9 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
 
   LossRows rows{mr.act, mr.actc, mr.logp, mr.adv, mr.ret};
   LossCoef lc{c->cfg.clip, c->cfg.vf_coef, c->cfg.ent_coef};
-  const float inv_mb = 1.0f / (float)mb;
+  // the loss is a mean over the minibatch: over all ranks' rows when the
+  // minibatch is the union of the ranks' slices (data-parallel update)
+  const float inv_mb = 1.0f / (float)(mb_global > 0 ? mb_global : mb);
   const float* P = c->params;
   const int M = (int)mb;
   // advantages from the values (and ratios) of the forward pass just run;
@@ -766,6 +776,10 @@ ppo_status enqueue_minibatch_mk(ppo_ctx* c, const float* obs, const __nv_bfloat1
   return PPO_OK;
 }
 
+ppo_status collective(ppo_ctx* c, int32_t op, void* buf, int64_t count, cudaStream_t st) {
+  return c->coll(c->coll_user, op, buf, count, st) == 0 ? PPO_OK : PPO_ERR_CUDA;
+}
+
 // Step trace of minibatch step j: params, m, v before the step (after == 0),
 // the assembled (unclipped) gradient after it (after == 1).
 cudaError_t trace_step(ppo_ctx* c, int64_t j, int after, cudaStream_t st) {
@@ -853,7 +867,16 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
     PPO_CUDA(launch_gae(rew, val, done, boot, (int)T, (int)N, gamma, lambda, c->adv, c->ret,
                         c->gae_part, gae_num_blocks((int)N), st));
     c->tr.mark(ST_GAE, st);
-    PPO_CUDA(launch_gae_finalize(c->gae_part, gae_num_blocks((int)N), c->advstats, st));
+    if (c->world > 1) {
+      // this shard's (count, mean, M2), every rank's gathered, merged in a
+      // fixed order: the same global statistics on every rank
+      PPO_CUDA(launch_gae_moments(c->gae_part, gae_num_blocks((int)N), c->mom_all + 3 * c->rank,
+                                  st));
+      TRY(collective(c, PPO_COLL_ALLGATHER_F64, c->mom_all, 3, st));
+      PPO_CUDA(launch_gae_finalize(c->mom_all, c->world, c->advstats, st));
+    } else {
+      PPO_CUDA(launch_gae_finalize(c->gae_part, gae_num_blocks((int)N), c->advstats, st));
+    }
     c->tr.mark(ST_GAE_FINALIZE, st);
     PPO_CUDA(launch_perm(seed, 0, epochs, B, c->perm, c->perm_work, st, &c->tr));
   }
@@ -882,6 +905,23 @@ ppo_status enqueue_update(ppo_ctx* c, const float* obs, const int32_t* act, cons
         TRY(enqueue_minibatch_mk(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
                                  c->advstats, st6, 1, lr, st));
         PPO_CUDA(trace_step(c, j, 1, st));
+      } else if (c->world > 1) {
+        // data-parallel step: this rank's slice of minibatch k, scaled for the
+        // union of the ranks' slices; the gradient (and the statistics) summed
+        // over the ranks before the optimizer, which recomputes the norm
+        const int64_t r0 = (int64_t)k * mb;
+        const MbRows mr{static_cast<uint8_t*>(ep.X) + r0 * xrow, ep.act + r0 * NH,
+                        ep.actc + r0 * G, ep.logp + r0, ep.adv + r0, ep.ret + r0};
+        TRY(enqueue_minibatch(c, obs, packed, act, actc, logp_old, c->adv, c->ret, idx, B, mb,
+                              c->advstats, st6, st, nullptr, &mr, nullptr, nullptr,
+                              mb * c->world));
+        TRY(collective(c, PPO_COLL_ALLREDUCE_SUM_F32, c->grad, c->s.P, st));
+        if (st6) TRY(collective(c, PPO_COLL_ALLREDUCE_SUM_F32, st6, 6, st));
+        PPO_CUDA(trace_step(c, j, 1, st));
+        if (c->cfg.optimizer == 1)
+          TRY(enqueue_muon(c, lr, nullptr, st, 0));
+        else
+          TRY(enqueue_adam(c, lr, nullptr, st, 0));
       } else {
         const int64_t r0 = (int64_t)k * mb;
         const MbRows mr{static_cast<uint8_t*>(ep.X) + r0 * xrow, ep.act + r0 * NH,
@@ -1450,6 +1490,7 @@ static ppo_status check_update_args(ppo_ctx* c, const float* obs, const int32_t*
   if (B > c->bmax || epochs > c->emax || B % minibatches != 0) return PPO_ERR_INVALID;
   if (c->cfg.adv_mode != 0 && N % minibatches != 0) return PPO_ERR_INVALID;
   if (c->cfg.adv_mode != 0 && c->s.H2 > 512) return PPO_ERR_UNSUPPORTED;
+  if (c->world > 1 && (c->cfg.adv_mode != 0 || c->use_mk)) return PPO_ERR_UNSUPPORTED;
   const int64_t mb = B / minibatches;
   if (mb > c->mbmax || !obs || !logp_old || (c->s.NH > 0 && !act) || (c->s.G > 0 && !actc))
     return PPO_ERR_INVALID;
@@ -1473,8 +1514,9 @@ ppo_status run_update(ppo_ctx* c, const float* obs, const int32_t* act, const fl
                         minibatches, stats));
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   PPO_CUDA(cudaStreamIsCapturing(st, &cs));
-  if (st == nullptr || cs != cudaStreamCaptureStatusNone) {
-    // legacy stream cannot be captured; inside a caller's capture, just enqueue
+  if (st == nullptr || cs != cudaStreamCaptureStatusNone || c->world > 1) {
+    // legacy stream cannot be captured; inside a caller's capture, or with
+    // the caller's collectives in the update, just enqueue
     TRY(enqueue_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
                        minibatches, gamma, lambda, lr, seed, stats, st, 1));
     if (wait_before_part2) PPO_CUDA(cudaStreamWaitEvent(st, wait_before_part2, 0));
@@ -1573,6 +1615,7 @@ ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
   TRY(check_update_args(c, obs, act, actc, logp_old, val, rew, done, boot, T, N, epochs,
                         minibatches, stats));
   if (!h_stage_ms || !h_stage_launches || st == nullptr) return PPO_ERR_INVALID;
+  if (c->world > 1) return PPO_ERR_UNSUPPORTED;
   // launches per minibatch: at most 7 per-stage kernels + 20 of a Muon step
   const size_t need = 8 + 3 * 4 + 40 * (size_t)epochs * minibatches;
   while (c->prof_events.size() < need) {
@@ -1686,6 +1729,24 @@ ppo_status ppo_update_host(ppo_ctx* c, const float* h_obs, const int32_t* h_act,
     PPO_CUDA(cudaMemcpyAsync(h_stats, c->st_stats, sizeof(float) * nstats,
                              cudaMemcpyDeviceToHost, st));
   PPO_CUDA(cudaStreamSynchronize(st));
+  return PPO_OK;
+}
+
+ppo_status ppo_set_collective(ppo_ctx* c, int32_t world, int32_t rank, ppo_collective_fn fn,
+                              void* user) {
+  if (!c || world < 1 || rank < 0 || rank >= world || (world > 1 && !fn))
+    return PPO_ERR_INVALID;
+  if (world > 1 && (c->cfg.adv_mode != 0 || c->use_mk)) return PPO_ERR_UNSUPPORTED;
+  if (world > c->mom_cap) {
+    ppo_status r = c->alloc_n(&c->mom_all, 3 * (int64_t)world);
+    if (r != PPO_OK) return r;
+    c->mom_cap = world;
+  }
+  c->world = world;
+  c->rank = rank;
+  c->coll = fn;
+  c->coll_user = user;
+  c->gvalid = false;
   return PPO_OK;
 }
 

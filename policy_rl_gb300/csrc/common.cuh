@@ -237,6 +237,11 @@ cudaError_t launch_gae(const float* rew, const float* val, const float* done, co
 int gae_num_blocks(int N);
 cudaError_t launch_gae_finalize(const double* partials, int nblocks, float* stats,
                                 cudaStream_t st);
+// The merged (count, mean, M2) of the per-block moments, fp64 triple[3] (a
+// shard's moments, merged with other ranks' by launch_gae_finalize over the
+// gathered triples).
+cudaError_t launch_gae_moments(const double* partials, int nblocks, double* triple,
+                               cudaStream_t st);
 cudaError_t launch_normalize(const float* adv, const float* stats, float* out, int64_t n,
                              cudaStream_t st);
 

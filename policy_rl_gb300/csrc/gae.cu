@@ -169,10 +169,13 @@ gae_kernel(const float* __restrict__ rew, const float* __restrict__ val,
 }
 
 // One block merges the per-block moments in a fixed order and writes
-// {mean, unbiased std} as fp32.
+// {mean, unbiased std} as fp32 (kTriple: the merged (count, mean, M2) in fp64
+// instead, for a merge with other ranks' shards).
 constexpr int kFinThreads = 256;
+template <bool kTriple>
 __global__ void __launch_bounds__(kFinThreads)
-gae_finalize_kernel(const double* __restrict__ partials, int nblocks, float* __restrict__ stats) {
+gae_finalize_kernel(const double* __restrict__ partials, int nblocks, float* __restrict__ stats,
+                    double* __restrict__ triple) {
   Moments m{0.0, 0.0, 0.0};
   for (int b = threadIdx.x; b < nblocks; b += kFinThreads) {
     Moments p{partials[3 * b], partials[3 * b + 1], partials[3 * b + 2]};
@@ -186,8 +189,14 @@ gae_finalize_kernel(const double* __restrict__ partials, int nblocks, float* __r
   if (threadIdx.x == 0) {
     Moments b = wm[0];
     for (int k = 1; k < kFinThreads / kWarp; ++k) b = merge(b, wm[k]);
-    stats[0] = (float)b.mean;
-    stats[1] = (float)(b.n > 1.0 ? sqrt(b.m2 / (b.n - 1.0)) : 0.0);
+    if constexpr (kTriple) {
+      triple[0] = b.n;
+      triple[1] = b.mean;
+      triple[2] = b.m2;
+    } else {
+      stats[0] = (float)b.mean;
+      stats[1] = (float)(b.n > 1.0 ? sqrt(b.m2 / (b.n - 1.0)) : 0.0);
+    }
   }
 }
 
@@ -245,7 +254,13 @@ cudaError_t launch_gae(const float* rew, const float* val, const float* done, co
 
 cudaError_t launch_gae_finalize(const double* partials, int nblocks, float* stats,
                                 cudaStream_t st) {
-  gae_finalize_kernel<<<1, kFinThreads, 0, st>>>(partials, nblocks, stats);
+  gae_finalize_kernel<false><<<1, kFinThreads, 0, st>>>(partials, nblocks, stats, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gae_moments(const double* partials, int nblocks, double* triple,
+                               cudaStream_t st) {
+  gae_finalize_kernel<true><<<1, kFinThreads, 0, st>>>(partials, nblocks, nullptr, triple);
   return cudaGetLastError();
 }
 
