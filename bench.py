@@ -591,7 +591,7 @@ def _policy_act_step(ctx, w, obs_d, stream, reps=50):
                     + f"; median of {reps} steps, inputs resident, no L2 flush"}
 
 
-def _rnn_minibatch(stream, reps=10):
+def _rnn_minibatch(stream, reps=10, warm=3):
     """ppo_rnn_loss_grad on a Mario-like minibatch with the pages' recurrent
     policy: 256 environment segments x T=128 (32,768 rows), 64-d observations,
     encoder to 128, four MinGRU layers, heads [9,2,2,2] + value."""
@@ -619,7 +619,7 @@ def _rnn_minibatch(stream, reps=10):
                            device="cuda")
         run = lambda: P.ppo_rnn_loss_grad(cfg, params, envs, obs, act, None, lp, adv, ret, done,
                                           h0, grad, work=work, stream=stream)
-        for _ in range(3):
+        for _ in range(warm):
             run()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(reps)]
@@ -750,7 +750,9 @@ def run_drive(args):
       update:    ppo_update of --workload, --reps times;
       gae:       ppo_gae with moments + normalisation, T=--gae-T x N=--gae-N;
       adam:      ppo_adam_step over the 67.2 M parameters of a 65536-1024-64
-                 fp32 network (1 GB of optimiser state)."""
+                 fp32 network (1 GB of optimiser state);
+      rnn:       ppo_rnn_loss_grad on the Mario-like recurrent minibatch;
+      muon:      ppo_muon_step on the network of --workload."""
     import torch
     import policy_rl_gb300 as P
     from policy_rl_gb300 import synth
@@ -790,6 +792,16 @@ def run_drive(args):
         work = torch.empty(P.ppo_gae_workspace_bytes(T, N), dtype=torch.uint8, device="cuda")
         for _ in range(args.reps):
             P.ppo_gae(rew, val, done, boot, 0.997, 0.95, adv, ret, advn, st, work)
+    elif args.drive == "rnn":
+        _rnn_minibatch(torch.cuda.current_stream(), reps=args.reps, warm=0)
+    elif args.drive == "muon":
+        w = synth.WORKLOADS[args.workload]
+        ctx = P.Context(P.config_from_workload(w, optimizer=1), synth.init_params(w))
+        ctx.grad.normal_(generator=g)
+        for _ in range(args.reps):
+            ctx.muon_step(w.lr)
+        ctx.sync_status()
+        ctx.close()
     elif args.drive == "adam":
         cfg = P.make_config(65536, 1024, 64, heads=(2,), precision=0, max_batch=1,
                             max_minibatch=1, max_epochs=1)
@@ -822,7 +834,7 @@ def main():
     ap.add_argument("--skip-rnn", action="store_true")
     ap.add_argument("--skip-mario", action="store_true",
                     help="omit the Mario-like update measured beside the headline workload")
-    ap.add_argument("--drive", choices=["minibatch", "update", "gae", "adam"],
+    ap.add_argument("--drive", choices=["minibatch", "update", "gae", "adam", "rnn", "muon"],
                     help="plain driver loop for profilers (no timing, no JSON line)")
     ap.add_argument("--reps", type=int, default=3, help="--drive: repetitions")
     ap.add_argument("--gae-T", type=int, default=1024, help="--drive gae: horizon")

@@ -380,7 +380,7 @@ def rnn_forward(rnn: Rnn, params, obs, done, h0, n: int = 0):
 
 def rnn_loss_grad(rnn: Rnn, params, envs, obs, act_disc, act_cont, logp_old, adv, ret, done, h0,
                   clip=0.2, vf_coef=0.5, ent_coef=0.01, normalize=False, adv_mean=0.0,
-                  adv_std=1.0):
+                  adv_std=1.0, bf16_operands=False):
     """Loss and BPTT gradient of the segments envs; returns (loss, grad, stats6, scale6).
     obs [T*N][D] (row t*N + n), adv / ret [T*N], done [T][N], h0 [N][L][H]."""
     done = _as(done, np.float32)
@@ -390,7 +390,7 @@ def rnn_loss_grad(rnn: Rnn, params, envs, obs, act_disc, act_cont, logp_old, adv
     st = np.empty(6, np.float64)
     sc = np.empty(6, np.float64)
     act_cont = _as(act_cont if act_cont is not None else np.zeros(1), np.float32)
-    cfg = _LossCfg(clip, vf_coef, ent_coef, 0)
+    cfg = _LossCfg(clip, vf_coef, ent_coef, int(bool(bf16_operands)))
     cn = rnn.c()
     loss = lib().orc_rnn_loss_grad(
         ctypes.byref(cn), ctypes.byref(cfg), _ptr(_as(params, np.float64)), T, N, envs.size,

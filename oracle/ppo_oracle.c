@@ -785,13 +785,44 @@ static orc_net orc_rnn_heads(const orc_rnn *r)
 
 static double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
+/* bf16-operand mode of the recurrent policy (the reading of the MLP's mode
+ * applied to its products): the GEMMs read bf16-rounded weights (W_enc,
+ * W_z, W_h, W_dec) and bf16 operands -- the observation, every layer input
+ * u (the encoder's output and each layer's new state as the next layer's or
+ * the decoder's input), and in the backward pass dL/dz, the pre-activation
+ * gradients dpz, dph and the input gradients du -- and the products that are
+ * stored between kernels are rounded when stored: u, the pre-activations
+ * pz, ph (bias added first), du.  The recurrence itself (z, the state h,
+ * dL/dh) and the bias gradients stay unrounded.  Identity when off. */
+static double *orc_rnn_gemm_weights(const orc_rnn *r, const double *params, int bf16)
+{
+    if (!bf16) return NULL;
+    const int64_t D = r->obs_dim, H = r->hidden, L = r->layers, C = orc_rnn_out_cols(r);
+    const int64_t P = orc_rnn_num_params(r), per = 2 * H * H + 2 * H;
+    double *wr = (double *)malloc(sizeof(double) * (size_t)P);
+    memcpy(wr, params, sizeof(double) * (size_t)P);
+    for (int64_t i = 0; i < H * D; ++i) wr[i] = orc_bf16(params[i]);
+    for (int64_t l = 0; l < L; ++l) {
+        const int64_t oz = H * D + l * per, oh = oz + H * H + H;
+        for (int64_t i = 0; i < H * H; ++i) {
+            wr[oz + i] = orc_bf16(params[oz + i]);
+            wr[oh + i] = orc_bf16(params[oh + i]);
+        }
+    }
+    const int64_t od = H * D + L * per;
+    for (int64_t i = 0; i < C * H; ++i) wr[od + i] = orc_bf16(params[od + i]);
+    return wr;
+}
+
 /* Forward of one segment (env n, steps 0..T-1).  obs rows t*N + n, done
  * [T][N], h0 [L][H].  zout [T][C]; when non-NULL, per step and layer
  * [T][L][H]: the layer input u, the gate z, the candidate h~, the masked
- * previous state hp and the new state h. */
-void orc_rnn_forward(const orc_rnn *r, const double *params, int64_t T, int64_t N, int64_t n,
-                     const float *obs, const float *done, const double *h0, double *zout,
-                     double *su, double *sz, double *sht, double *shp, double *sh)
+ * previous state hp and the new state h.  bf16: the operand rounding above
+ * (params must then hold the rounded weights, see orc_rnn_gemm_weights). */
+static void orc_rnn_forward_mode(const orc_rnn *r, const double *params, int64_t T, int64_t N,
+                                 int64_t n, const float *obs, const float *done, const double *h0,
+                                 int bf16, double *zout, double *su, double *sz, double *sht,
+                                 double *shp, double *sh)
 {
     const int64_t D = r->obs_dim, H = r->hidden, L = r->layers, C = orc_rnn_out_cols(r);
     const double *Wenc = params;
@@ -805,8 +836,8 @@ void orc_rnn_forward(const orc_rnn *r, const double *params, int64_t T, int64_t 
         const double mask = (t > 0 && done[(t - 1) * N + n] != 0.0f) ? 0.0 : 1.0;
         for (int64_t i = 0; i < H; ++i) {
             double e = 0.0;
-            for (int64_t k = 0; k < D; ++k) e += Wenc[i * D + k] * (double)x[k];
-            u[i] = e;
+            for (int64_t k = 0; k < D; ++k) e += Wenc[i * D + k] * orc_rnd(bf16, (double)x[k]);
+            u[i] = orc_rnd(bf16, e);
         }
         for (int64_t l = 0; l < L; ++l) {
             const double *Wz = params + H * D + l * (2 * H * H + 2 * H);
@@ -817,6 +848,8 @@ void orc_rnn_forward(const orc_rnn *r, const double *params, int64_t T, int64_t 
                     pz += Wz[i * H + k] * u[k];
                     ph += Wh[i * H + k] * u[k];
                 }
+                pz = orc_rnd(bf16, pz);
+                ph = orc_rnd(bf16, ph);
                 const double z = orc_sigmoid(pz);
                 const double hp = mask * state[l * H + i];
                 hn[i] = (1.0 - z) * hp + z * ph;
@@ -824,7 +857,7 @@ void orc_rnn_forward(const orc_rnn *r, const double *params, int64_t T, int64_t 
                 if (su) { su[o] = u[i]; sz[o] = z; sht[o] = ph; shp[o] = hp; sh[o] = hn[i]; }
             }
             memcpy(state + l * H, hn, sizeof(double) * (size_t)H);
-            memcpy(u, hn, sizeof(double) * (size_t)H);
+            for (int64_t i = 0; i < H; ++i) u[i] = orc_rnd(bf16, hn[i]);
         }
         for (int64_t c = 0; c < C; ++c) {
             double acc = 0.0;
@@ -833,6 +866,13 @@ void orc_rnn_forward(const orc_rnn *r, const double *params, int64_t T, int64_t 
         }
     }
     free(state); free(u); free(hn);
+}
+
+void orc_rnn_forward(const orc_rnn *r, const double *params, int64_t T, int64_t N, int64_t n,
+                     const float *obs, const float *done, const double *h0, double *zout,
+                     double *su, double *sz, double *sht, double *shp, double *sh)
+{
+    orc_rnn_forward_mode(r, params, T, N, n, obs, done, h0, 0, zout, su, sz, sht, shp, sh);
 }
 
 /* Loss and gradient of a minibatch of environment segments envs[0..ns)
@@ -851,11 +891,14 @@ double orc_rnn_loss_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double
     const int64_t D = r->obs_dim, H = r->hidden, L = r->layers, C = orc_rnn_out_cols(r);
     const int64_t NH = r->n_heads, G = r->n_gauss, P = orc_rnn_num_params(r);
     const orc_net heads = orc_rnn_heads(r);
-    const double *Wdec = params + H * D + L * (2 * H * H + 2 * H);
-    const double *logstd = Wdec + C * H;
+    const int bf16 = cfg->bf16_operands;
+    double *wr = orc_rnn_gemm_weights(r, params, bf16);
+    const double *pw = bf16 ? wr : params;   /* the weights the products read */
+    const double *Wdec = pw + H * D + L * (2 * H * H + 2 * H);
+    const double *logstd = params + (Wdec - pw) + C * H;
     memset(grad, 0, sizeof(double) * (size_t)P);
     double *gWenc = grad;
-    double *gWdec = grad + (Wdec - params), *glogstd = grad + (logstd - params);
+    double *gWdec = grad + (Wdec - pw), *glogstd = grad + (logstd - params);
     const int64_t TLH = T * L * H;
     double *su = (double *)malloc(sizeof(double) * (size_t)TLH);
     double *sz = (double *)malloc(sizeof(double) * (size_t)TLH);
@@ -873,8 +916,8 @@ double orc_rnn_loss_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double
 
     for (int64_t j = 0; j < ns; ++j) {
         const int64_t n = envs[j];
-        orc_rnn_forward(r, params, T, N, n, obs, done, h0 + n * L * H, zout, su, sz, sht, shp,
-                        sh);
+        orc_rnn_forward_mode(r, pw, T, N, n, obs, done, h0 + n * L * H, bf16, zout, su, sz, sht,
+                             shp, sh);
         memset(dnext, 0, sizeof(double) * (size_t)(L * H));
         for (int64_t t = T - 1; t >= 0; --t) {
             const int64_t row = t * N + n;
@@ -885,20 +928,23 @@ double orc_rnn_loss_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double
                         act_cont + row * G, (double)logp_old[row], A, ret[row], inv_mb,
                         logprob, dz, glogstd, terms);
             for (int q = 0; q < 6; ++q) { sum[q] += terms[q]; asum[q] += fabs(terms[q]); }
-            /* decoder: z = W_dec h^{L-1}_t */
+            /* decoder: z = W_dec u^L_t (u^L the top state, as an operand) */
             const double *htop = sh + (t * L + (L - 1)) * H;
             for (int64_t k = 0; k < H; ++k) din[k] = 0.0;
-            for (int64_t c = 0; c < C; ++c)
+            for (int64_t c = 0; c < C; ++c) {
+                const double dzc = orc_rnd(bf16, dz[c]);
                 for (int64_t k = 0; k < H; ++k) {
-                    gWdec[c * H + k] += dz[c] * htop[k];
-                    din[k] += dz[c] * Wdec[c * H + k];
+                    gWdec[c * H + k] += dzc * orc_rnd(bf16, htop[k]);
+                    din[k] += dzc * Wdec[c * H + k];
                 }
+            }
+            for (int64_t k = 0; k < H; ++k) din[k] = orc_rnd(bf16, din[k]);
             /* layers, top to bottom: h = (1 - z) hp + z h~ */
             const double mask = (t > 0 && done[(t - 1) * N + n] != 0.0f) ? 0.0 : 1.0;
             for (int64_t l = L - 1; l >= 0; --l) {
-                const double *Wz = params + H * D + l * (2 * H * H + 2 * H);
+                const double *Wz = pw + H * D + l * (2 * H * H + 2 * H);
                 const double *Wh = Wz + H * H + H;
-                double *gWz = grad + (Wz - params), *gbz = gWz + H * H;
+                double *gWz = grad + (Wz - pw), *gbz = gWz + H * H;
                 double *gWh = gbz + H, *gbh = gWh + H * H;
                 const int64_t o = (t * L + l) * H;
                 for (int64_t k = 0; k < H; ++k) du[k] = 0.0;
@@ -910,18 +956,20 @@ double orc_rnn_loss_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double
                     dnext[l * H + i] = dh * (1.0 - z) * mask;   /* into h_{t-1} */
                     gbz[i] += dpz;
                     gbh[i] += dht;
+                    const double dpzr = orc_rnd(bf16, dpz), dhtr = orc_rnd(bf16, dht);
                     for (int64_t k = 0; k < H; ++k) {
-                        gWz[i * H + k] += dpz * su[o + k];
-                        gWh[i * H + k] += dht * su[o + k];
-                        du[k] += Wz[i * H + k] * dpz + Wh[i * H + k] * dht;
+                        gWz[i * H + k] += dpzr * su[o + k];
+                        gWh[i * H + k] += dhtr * su[o + k];
+                        du[k] += Wz[i * H + k] * dpzr + Wh[i * H + k] * dhtr;
                     }
                 }
-                memcpy(din, du, sizeof(double) * (size_t)H);
+                for (int64_t k = 0; k < H; ++k) din[k] = orc_rnd(bf16, du[k]);
             }
             /* encoder: u^0 = W_enc x */
             const float *x = obs + row * D;
             for (int64_t i = 0; i < H; ++i)
-                for (int64_t k = 0; k < D; ++k) gWenc[i * D + k] += din[i] * (double)x[k];
+                for (int64_t k = 0; k < D; ++k)
+                    gWenc[i * D + k] += din[i] * orc_rnd(bf16, (double)x[k]);
         }
     }
     for (int q = 0; q < 6; ++q) {
@@ -930,6 +978,7 @@ double orc_rnn_loss_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double
     }
     free(su); free(sz); free(sht); free(shp); free(sh); free(zout); free(logprob); free(dz);
     free(dnext); free(din); free(du);
+    free(wr);
     return sum[0] * inv_mb;
 }
 
@@ -1091,7 +1140,7 @@ int orc_rnn_update(const orc_rnn *r, const orc_hyper *hp, int64_t T, int64_t N, 
     orc_gae(T, N, rew, val, done, boot, hp->gamma, hp->lambda, adv, ret);
     double mean, sd;
     orc_moments(B, adv, &mean, &sd);
-    const orc_loss_cfg lc = {hp->clip, hp->vf_coef, hp->ent_coef, 0};
+    const orc_loss_cfg lc = {hp->clip, hp->vf_coef, hp->ent_coef, hp->bf16_operands};
     for (int64_t e = 0; e < epochs; ++e) {
         orc_perm(hp->seed, e, N, perm);
         for (int64_t k = 0; k < minibatches; ++k) {

@@ -192,3 +192,55 @@ def test_rnn_update_is_the_composition():
             r, mr, vr = oracle.adam(r, g, mr, vr, k, hp.lr)
     assert step == E * M
     np.testing.assert_allclose(q, r, rtol=1e-12, atol=1e-14)
+
+
+# ---- bf16-operand mode of the recurrent policy ----------------------------------
+def test_rnn_bf16_mode_is_exact_on_representable_operands():
+    """Saturated gates (b_z = 40: z = 1 exactly in fp64), dyadic weights and
+    observations, no entropy term, zero advantages and a dyadic value error:
+    every stored product and backpropagated value is bf16-exact, so the
+    bf16-operand mode equals the fp64 mode bit for bit (it rounds nothing
+    that was not rounded and drops no term)."""
+    rnn = oracle.Rnn(obs_dim=3, hidden=4, layers=2, heads=(2,), n_gauss=0)
+    rng = np.random.default_rng(7)
+    T, N = 4, 2
+    p = rng.integers(-2, 3, rnn.num_params) / 8.0
+    D, H, L = rnn.obs_dim, rnn.hidden, rnn.layers
+    per = 2 * H * H + 2 * H
+    for l in range(L):
+        p[H * D + l * per + H * H:H * D + l * per + H * H + H] = 40.0   # b_z
+    obs = rng.integers(-2, 3, (T * N, D)).astype(np.float32)
+    act = np.zeros((T * N, 1), np.int32)
+    lp = np.zeros(T * N, np.float32)
+    adv = np.zeros(T * N)
+    done = np.zeros((T, N), np.float32)
+    h0 = np.zeros((N, L, H))
+    envs = np.arange(N, dtype=np.int32)
+    # V from the fp64 forward, so that V - R is a small dyadic
+    z = np.stack([oracle.rnn_forward(rnn, p, obs, done, h0[n], n) for n in range(N)],
+                 axis=1)                                       # [T][N][C]
+    ret = (z[..., -1].reshape(-1) - rng.integers(-2, 3, T * N) / 4.0)
+    kw = dict(clip=0.2, vf_coef=0.5, ent_coef=0.0)
+    l0, g0, _, _ = oracle.rnn_loss_grad(rnn, p, envs, obs, act, None, lp, adv, ret, done, h0, **kw)
+    l1, g1, _, _ = oracle.rnn_loss_grad(rnn, p, envs, obs, act, None, lp, adv, ret, done, h0,
+                                        bf16_operands=True, **kw)
+    assert l0 == l1
+    np.testing.assert_array_equal(g0, g1)
+    assert np.abs(g0).sum() > 0
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_rnn_bf16_mode_is_close_to_fp64(seed):
+    rnn = oracle.Rnn(obs_dim=16, hidden=32, layers=3, heads=(9, 2), n_gauss=1)
+    T, N = 16, 4
+    p, obs, act, actc, lp, adv, ret, done, h0 = _data(rnn, T, N, seed, p_done=0.1)
+    p *= 0.4
+    envs = np.arange(N, dtype=np.int32)
+    kw = dict(clip=10.0)
+    _, g0, s0, _ = oracle.rnn_loss_grad(rnn, p, envs, obs, act, actc, lp, adv, ret, done, h0,
+                                        **kw)
+    _, g1, s1, _ = oracle.rnn_loss_grad(rnn, p, envs, obs, act, actc, lp, adv, ret, done, h0,
+                                        bf16_operands=True, **kw)
+    assert np.linalg.norm(g1 - g0) / np.linalg.norm(g0) < 2e-2
+    assert np.linalg.norm(g1 - g0) > 0          # the mode does round something
+    np.testing.assert_allclose(s1, s0, rtol=2e-2, atol=1e-6)
