@@ -437,9 +437,11 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.skip_adam_stress:
         adam = _adam_stress(stream, hbm_peak)
 
-    rnn = None
+    rnn = rnn_upd = None
     if rank == 0 and not args.skip_rnn:
-        rnn = _rnn_minibatch(stream)
+        rnn = {"bf16": _rnn_minibatch(stream, precision=1),
+               "fp32": _rnn_minibatch(stream, precision=0)}
+        rnn_upd = _rnn_update(stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -467,6 +469,7 @@ def run_ours(args, world, rank, local):
         "adam_stress": adam,
         "policy_act": act_step,
         "rnn_minibatch": rnn,
+        "rnn_update": rnn_upd,
         "cpu_baseline": cpu,
         "clocks": head["clocks"],
     }
@@ -591,7 +594,31 @@ def _policy_act_step(ctx, w, obs_d, stream, reps=50):
                     + f"; median of {reps} steps, inputs resident, no L2 flush"}
 
 
-def _rnn_minibatch(stream, reps=10, warm=3):
+def _rnn_inputs(T, N, D, H, L, heads, precision, gen_seed=0):
+    import torch
+    import policy_rl_gb300 as P
+    cfg = P.make_rnn_config(D, H, L, heads, precision=precision)
+    n = P.ppo_rnn_param_count(cfg)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(gen_seed)
+    d = {
+        "params": torch.randn(n, device="cuda", generator=g) * 0.05,
+        "obs": torch.randn(T * N, D, device="cuda", generator=g),
+        "act": torch.stack([torch.randint(0, k, (T * N,), device="cuda", generator=g)
+                            for k in heads], 1).int().contiguous(),
+        "lp": torch.full((T * N,), -3.0, device="cuda"),
+        "adv": torch.randn(T * N, device="cuda", generator=g),
+        "ret": torch.randn(T * N, device="cuda", generator=g),
+        "val": torch.randn(T, N, device="cuda", generator=g),
+        "rew": (torch.rand(T, N, device="cuda", generator=g) < 0.02).float(),
+        "done": (torch.rand(T, N, device="cuda", generator=g) < 0.004).float(),
+        "boot": torch.randn(N, device="cuda", generator=g),
+        "h0": torch.zeros(N, L, H, device="cuda"),
+    }
+    return cfg, n, d
+
+
+def _rnn_minibatch(stream, reps=10, warm=3, precision=1):
     """ppo_rnn_loss_grad on a Mario-like minibatch with the pages' recurrent
     policy: 256 environment segments x T=128 (32,768 rows), 64-d observations,
     encoder to 128, four MinGRU layers, heads [9,2,2,2] + value."""
@@ -599,26 +626,15 @@ def _rnn_minibatch(stream, reps=10, warm=3):
     import policy_rl_gb300 as P
     T, N, ns, D, H, L = 128, 2048, 256, 64, 128, 4
     heads = (9, 2, 2, 2)
-    cfg = P.make_rnn_config(D, H, L, heads)
-    n = P.ppo_rnn_param_count(cfg)
-    g = torch.Generator(device="cuda")
-    g.manual_seed(0)
     with torch.cuda.stream(stream):
-        params = torch.randn(n, device="cuda", generator=g) * 0.05
-        obs = torch.randn(T * N, D, device="cuda", generator=g)
-        act = torch.stack([torch.randint(0, k, (T * N,), device="cuda", generator=g)
-                           for k in heads], 1).int().contiguous()
-        lp = torch.full((T * N,), -3.0, device="cuda")
-        adv = torch.randn(T * N, device="cuda", generator=g)
-        ret = torch.randn(T * N, device="cuda", generator=g)
-        done = (torch.rand(T, N, device="cuda", generator=g) < 0.004).float()
-        h0 = torch.zeros(N, L, H, device="cuda")
+        cfg, n, d = _rnn_inputs(T, N, D, H, L, heads, precision)
         envs = torch.arange(ns, dtype=torch.int32, device="cuda")
         grad = torch.empty(n, device="cuda")
         work = torch.empty(P.ppo_rnn_workspace_bytes(cfg, T, ns), dtype=torch.uint8,
                            device="cuda")
-        run = lambda: P.ppo_rnn_loss_grad(cfg, params, envs, obs, act, None, lp, adv, ret, done,
-                                          h0, grad, work=work, stream=stream)
+        run = lambda: P.ppo_rnn_loss_grad(cfg, d["params"], envs, d["obs"], d["act"], None,
+                                          d["lp"], d["adv"], d["ret"], d["done"], d["h0"], grad,
+                                          work=work, stream=stream)
         for _ in range(warm):
             run()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -630,11 +646,44 @@ def _rnn_minibatch(stream, reps=10, warm=3):
         stream.synchronize()
     t = float(np.median([a.elapsed_time(b) for a, b in evs])) / 1e3
     rows = T * ns
-    flops = rows * (2 * D * H + L * 8 * H * H + 2 * 16 * H) * 3   # forward + backward (~2x)
-    return {"rows": rows, "ms_per_minibatch": round(t * 1e3, 3),
-            "samples_per_s": round(rows / t, 1), "approx_TFLOPs": round(flops / t / 1e12, 3),
-            "note": "ppo_rnn_loss_grad, fp32 CUDA-core kernels (correctness-first); "
-                    f"median of {reps}"}
+    # products of one minibatch: forward (encoder, 2 per layer, decoder) and
+    # backward (input and weight gradients)
+    flops = rows * 2 * (D * H + L * 2 * H * H + 16 * H) * 3
+    out = {"rows": rows, "ms_per_minibatch": round(t * 1e3, 3),
+           "samples_per_s": round(rows / t, 1), "TFLOPs": round(flops / t / 1e12, 3),
+           "note": ("ppo_rnn_loss_grad, bf16 tcgen05 products, fp32 scans" if precision
+                    else "ppo_rnn_loss_grad, fp32 CUDA-core kernels") + f"; median of {reps}"}
+    return out
+
+
+def _rnn_update(stream, reps=5):
+    """ppo_rnn_update of the Mario-like recurrent workload: T=128 x N=2048,
+    4 epochs x 8 minibatches of 256 segments, bf16 products."""
+    import torch
+    import policy_rl_gb300 as P
+    T, N, D, H, L, E, M = 128, 2048, 64, 128, 4, 4, 8
+    heads = (9, 2, 2, 2)
+    with torch.cuda.stream(stream):
+        cfg, n, d = _rnn_inputs(T, N, D, H, L, heads, 1)
+        ctx = P.RnnContext(cfg, d["params"].cpu().numpy(), max_T=T, max_N=N, max_epochs=E)
+        run = lambda: ctx.update(d["obs"], d["act"], None, d["lp"], d["val"], d["rew"],
+                                 d["done"], d["boot"], d["h0"], E, M, 0.99, 0.95, 2.5e-4, 7,
+                                 stream=stream)
+        run()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for s0, e0 in evs:
+            s0.record(stream)
+            run()
+            e0.record(stream)
+        stream.synchronize()
+        ctx.sync_status(stream)
+        ctx.close()
+    t = float(np.median([a.elapsed_time(b) for a, b in evs])) / 1e3
+    return {"workload": f"recurrent Mario-like: T={T} N={N} obs={D} MinGRU {L}x{H} heads "
+                        f"{list(heads)}+V epochs={E} minibatches={M}",
+            "ms_per_update": round(t * 1e3, 3), "samples_per_s": round(T * N / t, 1),
+            "note": f"ppo_rnn_update, bf16 tcgen05 products; median of {reps}"}
 
 
 def _oracle_update(ws, seed=0, adv_mode=0, optimizer=0):
@@ -751,7 +800,8 @@ def run_drive(args):
       gae:       ppo_gae with moments + normalisation, T=--gae-T x N=--gae-N;
       adam:      ppo_adam_step over the 67.2 M parameters of a 65536-1024-64
                  fp32 network (1 GB of optimiser state);
-      rnn:       ppo_rnn_loss_grad on the Mario-like recurrent minibatch;
+      rnn:       ppo_rnn_loss_grad on the Mario-like recurrent minibatch (bf16);
+      rnn_update: ppo_rnn_update of the Mario-like recurrent workload;
       muon:      ppo_muon_step on the network of --workload."""
     import torch
     import policy_rl_gb300 as P
@@ -794,6 +844,8 @@ def run_drive(args):
             P.ppo_gae(rew, val, done, boot, 0.997, 0.95, adv, ret, advn, st, work)
     elif args.drive == "rnn":
         _rnn_minibatch(torch.cuda.current_stream(), reps=args.reps, warm=0)
+    elif args.drive == "rnn_update":
+        _rnn_update(torch.cuda.current_stream(), reps=args.reps)
     elif args.drive == "muon":
         w = synth.WORKLOADS[args.workload]
         ctx = P.Context(P.config_from_workload(w, optimizer=1), synth.init_params(w))
@@ -834,7 +886,8 @@ def main():
     ap.add_argument("--skip-rnn", action="store_true")
     ap.add_argument("--skip-mario", action="store_true",
                     help="omit the Mario-like update measured beside the headline workload")
-    ap.add_argument("--drive", choices=["minibatch", "update", "gae", "adam", "rnn", "muon"],
+    ap.add_argument("--drive", choices=["minibatch", "update", "gae", "adam", "rnn",
+                                        "rnn_update", "muon"],
                     help="plain driver loop for profilers (no timing, no JSON line)")
     ap.add_argument("--reps", type=int, default=3, help="--drive: repetitions")
     ap.add_argument("--gae-T", type=int, default=1024, help="--drive gae: horizon")

@@ -360,6 +360,12 @@ typedef struct {
     int32_t head_n[PPO_MAX_HEADS];
     int32_t n_gauss;                  /* 0..4; C = sum(head_n) + n_gauss + 1 <= 32 */
     float clip, vf_coef, ent_coef;
+    int32_t precision;                /* 0 = fp32 CUDA-core products,
+                                         1 = bf16 tensor-core (tcgen05) products,
+                                             fp32 accumulate; hidden 128 or 256 */
+    /* the update (ppo_rnn_update): gradient-norm clip and Adam */
+    float max_grad_norm;
+    double beta1, beta2, adam_eps;
 } ppo_rnn_config;
 
 ppo_status ppo_rnn_param_count(const ppo_rnn_config *cfg, int64_t *n);
@@ -373,7 +379,14 @@ ppo_status ppo_rnn_workspace_bytes(const ppo_rnn_config *cfg, int64_t T, int64_t
  * d_logp_old, d_adv, d_ret [T*N], d_adv_stats nullable ({mean, std}: the
  * advantage used is (adv - mean)/(std + 1e-8)), d_done [T][N].  d_grad
  * (param_count floats) is overwritten; d_stats6 as in
- * ppo_minibatch_loss_grad.  fp32 CUDA-core kernels; deterministic. */
+ * ppo_minibatch_loss_grad.  precision 0: fp32 CUDA-core kernels; precision
+ * 1: the products (encoder, gate and candidate pre-activations, input
+ * gradients, weight gradients) on the tensor cores with bf16 operands -- the
+ * weights, the observations, each layer's input, the stored pre-activations,
+ * dL/dz, the pre-activation and input gradients -- and fp32 accumulation;
+ * the recurrence, the loss and the bias gradients in fp32.  In precision 1
+ * the first int32 of d_work is set nonzero if a bounded device wait of the
+ * call gave up (the outputs are then unspecified).  Deterministic. */
 ppo_status ppo_rnn_loss_grad(const ppo_rnn_config *cfg, const float *d_params, int64_t T,
                              int64_t N, const int32_t *d_envs, int64_t ns, const float *d_obs,
                              const int32_t *d_act_disc, const float *d_act_cont,
@@ -381,6 +394,37 @@ ppo_status ppo_rnn_loss_grad(const ppo_rnn_config *cfg, const float *d_params, i
                              const float *d_adv_stats, const float *d_done, const float *d_h0,
                              float *d_grad, float *d_stats6, void *d_work, size_t work_bytes,
                              cudaStream_t stream);
+
+/* Update of the recurrent policy ("Teaching Mario to speedrun", sec. 6 "The
+ * whole algorithm" with sec. 8's policy and its carried state).  The context
+ * owns the parameters (fp32, layout above), the gradient, Adam's m and v and
+ * the workspaces for rollouts of up to max_T steps x max_N environments and
+ * max_epochs epochs.  ppo_rnn_update: GAE (gamma, lambda, terminals as in
+ * ppo_gae) over d_val/d_rew/d_done [T][N] and d_boot [N]; the statistics of
+ * all T*N advantages; per epoch e the mulberry32 permutation of the N
+ * environments (the rule of ppo_minibatch_perm, B = N); per minibatch k the
+ * segments perm_e[k*ns .. (k+1)*ns), ns = N / minibatches, with the loss and
+ * gradient of ppo_rnn_loss_grad (normalised advantages, d_h0 [N][layers]
+ * [hidden] the state carried into the horizon), the gradient-norm clip
+ * (max_grad_norm) and Adam (lr, beta1, beta2, adam_eps of the config).
+ * d_obs [T*N][obs_dim], d_act_disc [T*N][n_heads], d_act_cont [T*N][n_gauss]
+ * (NULL if n_gauss == 0), d_logp_old [T*N]; d_stats (nullable) fp32
+ * [epochs*minibatches][6].  minibatches must divide N.  Asynchronous on
+ * `stream`; ppo_rnn_sync_status synchronises it and returns PPO_ERR_TIMEOUT
+ * once if a bounded device wait gave up since the last call. */
+typedef struct ppo_rnn_ctx ppo_rnn_ctx;
+ppo_status ppo_rnn_create(const ppo_rnn_config *cfg, const float *h_init_params, int64_t max_T,
+                          int64_t max_N, int32_t max_epochs, ppo_rnn_ctx **out);
+ppo_status ppo_rnn_destroy(ppo_rnn_ctx *ctx);
+ppo_status ppo_rnn_buffers(ppo_rnn_ctx *ctx, float **d_params, float **d_grad, float **d_m,
+                           float **d_v);
+ppo_status ppo_rnn_update(ppo_rnn_ctx *ctx, const float *d_obs, const int32_t *d_act_disc,
+                          const float *d_act_cont, const float *d_logp_old, const float *d_val,
+                          const float *d_rew, const float *d_done, const float *d_boot,
+                          const float *d_h0, int64_t T, int64_t N, int32_t epochs,
+                          int32_t minibatches, float gamma, float lambda, float lr, uint32_t seed,
+                          float *d_stats, cudaStream_t stream);
+ppo_status ppo_rnn_sync_status(ppo_rnn_ctx *ctx, cudaStream_t stream);
 
 /* ---- Whole update -------------------------------------------------------------
  * "Teaching Mario to speedrun", sec. 6 "The whole algorithm", steps 2-3:

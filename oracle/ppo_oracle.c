@@ -881,6 +881,88 @@ void orc_rnn_forward(const orc_rnn *r, const double *params, int64_t T, int64_t 
  * per-row loss is orc_loss_grad's (orc_ppo_row), with advantages optionally
  * normalised by (adv_mean, adv_std); adv, ret [T*N]; h0 [N][L][H].
  * grad overwritten; stats6 / scale6 as in orc_loss_grad. */
+/* One segment's contribution (env n) to the recurrent policy's loss and
+ * gradient: forward, per-row loss, backpropagation through time.  Adds into
+ * grad (layout of the parameters) and the loss-term sums; buf holds the
+ * segment's scratch (see orc_rnn_loss_grad). */
+static void orc_rnn_segment_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double *params,
+                                 const double *pw, int64_t T, int64_t N, int64_t n,
+                                 const float *obs, const int32_t *act_disc,
+                                 const float *act_cont, const float *logp_old, const double *adv,
+                                 const double *ret, int normalize, double adv_mean,
+                                 double adv_std, const float *done, const double *h0,
+                                 double inv_mb, double *buf, double *grad, double sum[6],
+                                 double asum[6])
+{
+    const int64_t D = r->obs_dim, H = r->hidden, L = r->layers, C = orc_rnn_out_cols(r);
+    const int64_t NH = r->n_heads, G = r->n_gauss;
+    const orc_net heads = orc_rnn_heads(r);
+    const int bf16 = cfg->bf16_operands;
+    const double *Wdec = pw + H * D + L * (2 * H * H + 2 * H);
+    const double *logstd = params + (Wdec - pw) + C * H;
+    double *gWenc = grad;
+    double *gWdec = grad + (Wdec - pw), *glogstd = grad + (logstd - params);
+    const int64_t TLH = T * L * H;
+    double *su = buf, *sz = su + TLH, *sht = sz + TLH, *shp = sht + TLH, *sh = shp + TLH;
+    double *zout = sh + TLH, *logprob = zout + T * C, *dz = logprob + C, *dnext = dz + C;
+    double *din = dnext + L * H, *du = din + H;
+    orc_rnn_forward_mode(r, pw, T, N, n, obs, done, h0 + n * L * H, bf16, zout, su, sz, sht,
+                         shp, sh);
+    memset(dnext, 0, sizeof(double) * (size_t)(L * H));
+    for (int64_t t = T - 1; t >= 0; --t) {
+        const int64_t row = t * N + n;
+        double A = adv[row];
+        if (normalize) A = (A - adv_mean) / (adv_std + 1e-8);
+        double terms[6];
+        orc_ppo_row(&heads, cfg, logstd, zout + t * C, act_disc + row * NH,
+                    act_cont + row * G, (double)logp_old[row], A, ret[row], inv_mb,
+                    logprob, dz, glogstd, terms);
+        for (int q = 0; q < 6; ++q) { sum[q] += terms[q]; asum[q] += fabs(terms[q]); }
+        /* decoder: z = W_dec u^L_t (u^L the top state, as an operand) */
+        const double *htop = sh + (t * L + (L - 1)) * H;
+        for (int64_t k = 0; k < H; ++k) din[k] = 0.0;
+        for (int64_t c = 0; c < C; ++c) {
+            const double dzc = orc_rnd(bf16, dz[c]);
+            for (int64_t k = 0; k < H; ++k) {
+                gWdec[c * H + k] += dzc * orc_rnd(bf16, htop[k]);
+                din[k] += dzc * Wdec[c * H + k];
+            }
+        }
+        for (int64_t k = 0; k < H; ++k) din[k] = orc_rnd(bf16, din[k]);
+        /* layers, top to bottom: h = (1 - z) hp + z h~ */
+        const double mask = (t > 0 && done[(t - 1) * N + n] != 0.0f) ? 0.0 : 1.0;
+        for (int64_t l = L - 1; l >= 0; --l) {
+            const double *Wz = pw + H * D + l * (2 * H * H + 2 * H);
+            const double *Wh = Wz + H * H + H;
+            double *gWz = grad + (Wz - pw), *gbz = gWz + H * H;
+            double *gWh = gbz + H, *gbh = gWh + H * H;
+            const int64_t o = (t * L + l) * H;
+            for (int64_t k = 0; k < H; ++k) du[k] = 0.0;
+            for (int64_t i = 0; i < H; ++i) {
+                const double dh = din[i] + dnext[l * H + i];
+                const double z = sz[o + i];
+                const double dpz = dh * (sht[o + i] - shp[o + i]) * z * (1.0 - z);
+                const double dht = dh * z;
+                dnext[l * H + i] = dh * (1.0 - z) * mask;   /* into h_{t-1} */
+                gbz[i] += dpz;
+                gbh[i] += dht;
+                const double dpzr = orc_rnd(bf16, dpz), dhtr = orc_rnd(bf16, dht);
+                for (int64_t k = 0; k < H; ++k) {
+                    gWz[i * H + k] += dpzr * su[o + k];
+                    gWh[i * H + k] += dhtr * su[o + k];
+                    du[k] += Wz[i * H + k] * dpzr + Wh[i * H + k] * dhtr;
+                }
+            }
+            for (int64_t k = 0; k < H; ++k) din[k] = orc_rnd(bf16, du[k]);
+        }
+        /* encoder: u^0 = W_enc x */
+        const float *x = obs + row * D;
+        for (int64_t i = 0; i < H; ++i)
+            for (int64_t k = 0; k < D; ++k)
+                gWenc[i * D + k] += din[i] * orc_rnd(bf16, (double)x[k]);
+    }
+}
+
 double orc_rnn_loss_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double *params,
                          int64_t T, int64_t N, int64_t ns, const int32_t *envs,
                          const float *obs, const int32_t *act_disc, const float *act_cont,
@@ -888,96 +970,48 @@ double orc_rnn_loss_grad(const orc_rnn *r, const orc_loss_cfg *cfg, const double
                          int normalize, double adv_mean, double adv_std, const float *done,
                          const double *h0, double *grad, double *stats6, double *scale6)
 {
-    const int64_t D = r->obs_dim, H = r->hidden, L = r->layers, C = orc_rnn_out_cols(r);
-    const int64_t NH = r->n_heads, G = r->n_gauss, P = orc_rnn_num_params(r);
-    const orc_net heads = orc_rnn_heads(r);
-    const int bf16 = cfg->bf16_operands;
-    double *wr = orc_rnn_gemm_weights(r, params, bf16);
-    const double *pw = bf16 ? wr : params;   /* the weights the products read */
-    const double *Wdec = pw + H * D + L * (2 * H * H + 2 * H);
-    const double *logstd = params + (Wdec - pw) + C * H;
-    memset(grad, 0, sizeof(double) * (size_t)P);
-    double *gWenc = grad;
-    double *gWdec = grad + (Wdec - pw), *glogstd = grad + (logstd - params);
-    const int64_t TLH = T * L * H;
-    double *su = (double *)malloc(sizeof(double) * (size_t)TLH);
-    double *sz = (double *)malloc(sizeof(double) * (size_t)TLH);
-    double *sht = (double *)malloc(sizeof(double) * (size_t)TLH);
-    double *shp = (double *)malloc(sizeof(double) * (size_t)TLH);
-    double *sh = (double *)malloc(sizeof(double) * (size_t)TLH);
-    double *zout = (double *)malloc(sizeof(double) * (size_t)(T * C));
-    double *logprob = (double *)malloc(sizeof(double) * (size_t)C);
-    double *dz = (double *)malloc(sizeof(double) * (size_t)C);
-    double *dnext = (double *)malloc(sizeof(double) * (size_t)(L * H));
-    double *din = (double *)malloc(sizeof(double) * (size_t)H);
-    double *du = (double *)malloc(sizeof(double) * (size_t)H);
-    double sum[6] = {0, 0, 0, 0, 0, 0}, asum[6] = {0, 0, 0, 0, 0, 0};
+    const int64_t H = r->hidden, L = r->layers, C = orc_rnn_out_cols(r);
+    const int64_t P = orc_rnn_num_params(r);
+    double *wr = orc_rnn_gemm_weights(r, params, cfg->bf16_operands);
+    const double *pw = cfg->bf16_operands ? wr : params;   /* the weights the products read */
     const double inv_mb = 1.0 / (double)(T * ns);
-
-    for (int64_t j = 0; j < ns; ++j) {
-        const int64_t n = envs[j];
-        orc_rnn_forward_mode(r, pw, T, N, n, obs, done, h0 + n * L * H, bf16, zout, su, sz, sht,
-                             shp, sh);
-        memset(dnext, 0, sizeof(double) * (size_t)(L * H));
-        for (int64_t t = T - 1; t >= 0; --t) {
-            const int64_t row = t * N + n;
-            double A = adv[row];
-            if (normalize) A = (A - adv_mean) / (adv_std + 1e-8);
-            double terms[6];
-            orc_ppo_row(&heads, cfg, logstd, zout + t * C, act_disc + row * NH,
-                        act_cont + row * G, (double)logp_old[row], A, ret[row], inv_mb,
-                        logprob, dz, glogstd, terms);
-            for (int q = 0; q < 6; ++q) { sum[q] += terms[q]; asum[q] += fabs(terms[q]); }
-            /* decoder: z = W_dec u^L_t (u^L the top state, as an operand) */
-            const double *htop = sh + (t * L + (L - 1)) * H;
-            for (int64_t k = 0; k < H; ++k) din[k] = 0.0;
-            for (int64_t c = 0; c < C; ++c) {
-                const double dzc = orc_rnd(bf16, dz[c]);
-                for (int64_t k = 0; k < H; ++k) {
-                    gWdec[c * H + k] += dzc * orc_rnd(bf16, htop[k]);
-                    din[k] += dzc * Wdec[c * H + k];
-                }
-            }
-            for (int64_t k = 0; k < H; ++k) din[k] = orc_rnd(bf16, din[k]);
-            /* layers, top to bottom: h = (1 - z) hp + z h~ */
-            const double mask = (t > 0 && done[(t - 1) * N + n] != 0.0f) ? 0.0 : 1.0;
-            for (int64_t l = L - 1; l >= 0; --l) {
-                const double *Wz = pw + H * D + l * (2 * H * H + 2 * H);
-                const double *Wh = Wz + H * H + H;
-                double *gWz = grad + (Wz - pw), *gbz = gWz + H * H;
-                double *gWh = gbz + H, *gbh = gWh + H * H;
-                const int64_t o = (t * L + l) * H;
-                for (int64_t k = 0; k < H; ++k) du[k] = 0.0;
-                for (int64_t i = 0; i < H; ++i) {
-                    const double dh = din[i] + dnext[l * H + i];
-                    const double z = sz[o + i];
-                    const double dpz = dh * (sht[o + i] - shp[o + i]) * z * (1.0 - z);
-                    const double dht = dh * z;
-                    dnext[l * H + i] = dh * (1.0 - z) * mask;   /* into h_{t-1} */
-                    gbz[i] += dpz;
-                    gbh[i] += dht;
-                    const double dpzr = orc_rnd(bf16, dpz), dhtr = orc_rnd(bf16, dht);
-                    for (int64_t k = 0; k < H; ++k) {
-                        gWz[i * H + k] += dpzr * su[o + k];
-                        gWh[i * H + k] += dhtr * su[o + k];
-                        du[k] += Wz[i * H + k] * dpzr + Wh[i * H + k] * dhtr;
-                    }
-                }
-                for (int64_t k = 0; k < H; ++k) din[k] = orc_rnd(bf16, du[k]);
-            }
-            /* encoder: u^0 = W_enc x */
-            const float *x = obs + row * D;
-            for (int64_t i = 0; i < H; ++i)
-                for (int64_t k = 0; k < D; ++k)
-                    gWenc[i * D + k] += din[i] * orc_rnd(bf16, (double)x[k]);
+    const int64_t nbuf = 5 * T * L * H + T * C + 2 * C + L * H + 2 * H;
+    /* segments are independent: with OpenMP each thread takes a contiguous
+     * range of them into its own gradient, summed in thread order */
+    int nt = orc_threads();
+    if (nt > ns) nt = (int)(ns > 0 ? ns : 1);
+    double *acc = (double *)calloc((size_t)nt * (size_t)P, sizeof(double));
+    double *tsum = (double *)calloc((size_t)nt * 12, sizeof(double));
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+#ifdef _OPENMP
+        const int th = omp_get_thread_num();
+#else
+        const int th = 0;
+#endif
+        double *buf = (double *)malloc(sizeof(double) * (size_t)nbuf);
+        for (int64_t j = ns * th / nt; j < ns * (th + 1) / nt; ++j) {
+            const int64_t n = envs[j];
+            orc_rnn_segment_grad(r, cfg, params, pw, T, N, n, obs, act_disc, act_cont, logp_old,
+                                 adv, ret, normalize, adv_mean, adv_std, done, h0, inv_mb, buf,
+                                 acc + (size_t)th * (size_t)P, tsum + 12 * th, tsum + 12 * th + 6);
         }
+        free(buf);
+    }
+    memset(grad, 0, sizeof(double) * (size_t)P);
+    double sum[6] = {0, 0, 0, 0, 0, 0}, asum[6] = {0, 0, 0, 0, 0, 0};
+    for (int th = 0; th < nt; ++th) {
+        for (int64_t i = 0; i < P; ++i) grad[i] += acc[(size_t)th * (size_t)P + i];
+        for (int q = 0; q < 6; ++q) { sum[q] += tsum[12 * th + q]; asum[q] += tsum[12 * th + 6 + q]; }
     }
     for (int q = 0; q < 6; ++q) {
         if (stats6) stats6[q] = sum[q] * inv_mb;
         if (scale6) scale6[q] = asum[q] * inv_mb;
     }
-    free(su); free(sz); free(sht); free(shp); free(sh); free(zout); free(logprob); free(dz);
-    free(dnext); free(din); free(du);
+    free(acc);
+    free(tsum);
     free(wr);
     return sum[0] * inv_mb;
 }

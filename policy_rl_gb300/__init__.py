@@ -23,7 +23,8 @@ __all__ = [
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
     "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "ppo_set_step_trace",
-    "ppo_set_wait_limit", "ppo_set_collective", "TorchCollective", "library_path",
+    "ppo_set_wait_limit", "ppo_set_collective", "TorchCollective", "RnnContext",
+    "library_path",
 ]
 
 
@@ -148,9 +149,11 @@ def ppo_minibatch_perm(seed, epoch, B, perm, work, stream=None) -> None:
 
 
 def make_rnn_config(obs_dim, hidden=128, layers=4, heads=(3, 2, 2), n_gauss=0, clip=0.2,
-                    vf_coef=0.5, ent_coef=0.01) -> RnnConfig:
+                    vf_coef=0.5, ent_coef=0.01, precision=0, max_grad_norm=0.5, beta1=0.9,
+                    beta2=0.999, adam_eps=1e-8) -> RnnConfig:
     hn = (ctypes.c_int32 * _abi.MAX_HEADS)(*(list(heads) + [0] * (_abi.MAX_HEADS - len(heads))))
-    return RnnConfig(obs_dim, hidden, layers, len(heads), hn, n_gauss, clip, vf_coef, ent_coef)
+    return RnnConfig(obs_dim, hidden, layers, len(heads), hn, n_gauss, clip, vf_coef, ent_coef,
+                     precision, max_grad_norm, beta1, beta2, adam_eps)
 
 
 def ppo_rnn_param_count(cfg: RnnConfig) -> int:
@@ -177,6 +180,49 @@ def ppo_rnn_loss_grad(cfg: RnnConfig, params, envs, obs, act_disc, act_cont, log
         _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(adv), _ptr(ret), _ptr(adv_stats),
         _ptr(done), _ptr(h0), _ptr(grad), _ptr(stats6), _ptr(work), wb, _stream(stream)),
         "ppo_rnn_loss_grad")
+
+
+class RnnContext:
+    """Owns one ppo_rnn_ctx: the recurrent policy's parameters, gradient, Adam
+    state and update workspaces (see ppo.h, ppo_rnn_update)."""
+
+    def __init__(self, cfg: RnnConfig, init_params=None, max_T=1, max_N=1, max_epochs=1):
+        import numpy as np
+        self.cfg = cfg
+        self.n_params = ppo_rnn_param_count(cfg)
+        h = ctypes.c_void_p()
+        ip = None if init_params is None else np.ascontiguousarray(init_params, np.float32)
+        _abi.check(_lib().ppo_rnn_create(ctypes.byref(cfg), _ptr(ip), max_T, max_N, max_epochs,
+                                         ctypes.byref(h)), "ppo_rnn_create")
+        self.handle = h
+        ps = [ctypes.c_void_p() for _ in range(4)]
+        _abi.check(_lib().ppo_rnn_buffers(h, *[ctypes.byref(p) for p in ps]), "ppo_rnn_buffers")
+        import torch
+        self.params, self.grad, self.adam_m, self.adam_v = (
+            torch.as_tensor(_DevArray(p.value, self.n_params), device="cuda") for p in ps)
+
+    def update(self, obs, act_disc, act_cont, logp_old, val, rew, done, boot, h0, epochs,
+               minibatches, gamma, lam, lr, seed, stats=None, stream=None):
+        T, N = val.shape
+        _abi.check(_lib().ppo_rnn_update(
+            self.handle, _ptr(obs), _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(val),
+            _ptr(rew), _ptr(done), _ptr(boot), _ptr(h0), T, N, epochs, minibatches, gamma, lam,
+            lr, seed & 0xFFFFFFFF, _ptr(stats), _stream(stream)), "ppo_rnn_update")
+
+    def sync_status(self, stream=None):
+        _abi.check(_lib().ppo_rnn_sync_status(self.handle, _stream(stream)),
+                   "ppo_rnn_sync_status")
+
+    def close(self):
+        if self.handle is not None:
+            _lib().ppo_rnn_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # ---- context ------------------------------------------------------------------

@@ -20,7 +20,8 @@ SYMBOLS = (
     "ppo_gae_noalloc", "ppo_segment_advantage_workspace_bytes", "ppo_segment_advantage",
     "ppo_perm_workspace_bytes", "ppo_minibatch_perm", "ppo_minibatch_loss_grad",
     "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_adam_step", "ppo_muon_step",
-    "ppo_rnn_param_count", "ppo_rnn_workspace_bytes", "ppo_rnn_loss_grad", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
+    "ppo_rnn_param_count", "ppo_rnn_workspace_bytes", "ppo_rnn_loss_grad", "ppo_rnn_create",
+    "ppo_rnn_destroy", "ppo_rnn_buffers", "ppo_rnn_update", "ppo_rnn_sync_status", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
     "ppo_sync_status", "ppo_set_collective", "ppo_set_step_trace", "ppo_set_wait_limit",
 )
 NUM_STAGES = 34
@@ -58,7 +59,9 @@ class RnnConfig(ctypes.Structure):
         ("obs_dim", ctypes.c_int32), ("hidden", ctypes.c_int32), ("layers", ctypes.c_int32),
         ("n_heads", ctypes.c_int32), ("head_n", ctypes.c_int32 * MAX_HEADS),
         ("n_gauss", ctypes.c_int32), ("clip", ctypes.c_float), ("vf_coef", ctypes.c_float),
-        ("ent_coef", ctypes.c_float),
+        ("ent_coef", ctypes.c_float), ("precision", ctypes.c_int32),
+        ("max_grad_norm", ctypes.c_float), ("beta1", ctypes.c_double),
+        ("beta2", ctypes.c_double), ("adam_eps", ctypes.c_double),
     ]
 
 
@@ -118,6 +121,14 @@ def load(path: str = LIB_PATH):
                                     ctypes.c_int),
         "ppo_rnn_loss_grad": ([ctypes.POINTER(RnnConfig), _P, _I64, _I64, _P, _I64, _P, _P, _P, _P,
                                _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
+        "ppo_rnn_create": ([ctypes.POINTER(RnnConfig), _P, _I64, _I64, i32, ctypes.POINTER(_P)],
+                           ctypes.c_int),
+        "ppo_rnn_destroy": ([_P], ctypes.c_int),
+        "ppo_rnn_buffers": ([_P, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
+                             ctypes.POINTER(_P)], ctypes.c_int),
+        "ppo_rnn_update": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F,
+                            _F, u32, _P, _P], ctypes.c_int),
+        "ppo_rnn_sync_status": ([_P, _P], ctypes.c_int),
         "ppo_update": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F, _F,
                         u32, _P, _P], ctypes.c_int),
         "ppo_update_host": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F,

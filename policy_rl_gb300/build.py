@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libppo_gb300.so")
-SOURCES = ["api.cu", "gae.cu", "gae_noalloc.cu", "perm.cu", "gather.cu", "gemm_tc.cu", "hl2.cu", "fmlp.cu", "mk.cu", "gemm_simt.cu", "optim.cu", "fresh.cu", "act.cu", "rnn.cu"]
+SOURCES = ["api.cu", "gae.cu", "gae_noalloc.cu", "perm.cu", "gather.cu", "gemm_tc.cu", "hl2.cu", "fmlp.cu", "mk.cu", "gemm_simt.cu", "optim.cu", "fresh.cu", "act.cu", "rnn.cu", "rnn_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -219,38 +219,17 @@ int wgrad_kt_per_split(const NetShape& s, int64_t mb, int num_sms) {
   return per;
 }
 
-// Split plan of the standalone weight-gradient kernel (256/128/64-column
-// tiles).  At large minibatches the kernel streams its operands (each unit
-// reads (128 + bn) features of every row in its k-range) and the tensor pipe
-// is not the limit, so units are balanced by the bytes they load: a region of
-// bn-column tiles gets q / (128 + bn) k-tiles per unit.  q is the smallest
-// budget whose units fit in one wave of num_sms CTAs (a second, partial wave
-// would double the kernel's time); every unit covers at least 4 k-tiles.
+// Split plan of the weight-gradient kernel for the MLP's three products:
+// W2 (H2 x H1), W1 (H1 x Dp), W3 (H2 x 64); see tc_wgrad_plan.
 struct WgradPlan {
   int kt[3];   // k-tiles per unit: W2 (H2 x H1), W1 (H1 x Dp), W3 (H2 x 64)
 };
 
 WgradPlan wgrad_plan(const NetShape& s, int64_t mb, int num_sms) {
-  const int64_t kt = (mb + 63) / 64;
   const int regs[3][2] = {{s.H2, s.H1}, {s.H1, s.Dp}, {s.H2, 64}};
-  double total = 0;
-  for (const auto& r : regs)
-    total += (double)(r[0] / 128) * (r[1] / tc_wgrad_bn(r[1])) * (128 + tc_wgrad_bn(r[1])) * kt;
-  int64_t q = (int64_t)std::ceil(total / num_sms);
   WgradPlan P{};
-  for (;; q += (q + 15) / 16) {
-    int64_t units = 0;
-    for (int i = 0; i < 3; ++i) {
-      const int bn = tc_wgrad_bn(regs[i][1]);
-      int64_t kp = q / (128 + bn);
-      if (kp < 4) kp = 4;
-      if ((kt + kp - 1) / kp > kMaxSplit) kp = (kt + kMaxSplit - 1) / kMaxSplit;
-      if (kp > kt) kp = kt;
-      P.kt[i] = (int)kp;
-      units += (int64_t)(regs[i][0] / 128) * (regs[i][1] / bn) * ((kt + kp - 1) / kp);
-    }
-    if (units <= num_sms || q >= 1024 * kt) return P;
-  }
+  tc_wgrad_plan(regs, 3, mb, num_sms, kMaxSplit, P.kt);
+  return P;
 }
 
 ppo_status check_minibatch_args(ppo_ctx* c, const float* obs, const int32_t* act,
@@ -1324,6 +1303,8 @@ static ppo_status rnn_check(const ppo_rnn_config* r, NetShape* s, int64_t* P) {
   if (r->n_heads < 0 || r->n_heads > PPO_MAX_HEADS || r->n_gauss < 0 || r->n_gauss > 4)
     return PPO_ERR_INVALID;
   if (r->hidden > 256 || r->layers > 8) return PPO_ERR_UNSUPPORTED;
+  if (r->precision != 0 && r->precision != 1) return PPO_ERR_INVALID;
+  if (r->precision == 1 && !rnn_tc_supported(r->obs_dim, r->hidden)) return PPO_ERR_UNSUPPORTED;
   std::memset(s, 0, sizeof(*s));
   int C = 0;
   for (int h = 0; h < r->n_heads; ++h) {
@@ -1356,6 +1337,13 @@ ppo_status ppo_rnn_workspace_bytes(const ppo_rnn_config* cfg, int64_t T, int64_t
   int64_t P;
   TRY(rnn_check(cfg, &s, &P));
   if (!bytes || T < 1 || ns < 1) return PPO_ERR_INVALID;
+  if (cfg->precision == 1) {
+    int dev = 0, nsm = 1;
+    PPO_CUDA(cudaGetDevice(&dev));
+    PPO_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+    *bytes = rnn_tc_workspace_bytes(cfg->obs_dim, cfg->hidden, cfg->layers, T, ns, nsm);
+    return PPO_OK;
+  }
   *bytes = sizeof(float) * rnn_workspace_floats(cfg->obs_dim, cfg->hidden, cfg->layers, T * ns);
   return PPO_OK;
 }
@@ -1405,6 +1393,14 @@ ppo_status ppo_rnn_loss_grad(const ppo_rnn_config* cfg, const float* params, int
   a.grad = grad;
   a.stats6 = stats6;
   a.work = static_cast<float*>(work);
+  if (cfg->precision == 1) {
+    int dev = 0, nsm = 1;
+    PPO_CUDA(cudaGetDevice(&dev));
+    PPO_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+    PPO_CUDA(tc_prepare());
+    PPO_CUDA(launch_rnn_loss_grad_tc(a, nsm, st, nullptr));
+    return PPO_OK;
+  }
   PPO_CUDA(launch_rnn_loss_grad(a, st));
   return PPO_OK;
 }
@@ -1774,6 +1770,235 @@ ppo_status ppo_sync_status(ppo_ctx* c, cudaStream_t st) {
   if (e != 0) {
     PPO_CUDA(cudaMemset(c->err, 0, sizeof(int)));
     return PPO_ERR_TIMEOUT;
+  }
+  return PPO_OK;
+}
+
+}  // extern "C"
+
+// =============================================================================
+// Recurrent-policy update ("Teaching Mario to speedrun", sec. 6 "The whole
+// algorithm" with sec. 8's MinGRU policy): GAE over the stored values, the
+// advantage statistics over all T*N entries, then per epoch the mulberry32
+// permutation of the N environments and per minibatch the BPTT loss and
+// gradient of its N/minibatches whole segments, clip and Adam.
+struct ppo_rnn_ctx {
+  ppo_rnn_config cfg;
+  NetShape s;
+  int64_t P = 0, max_T = 0, max_N = 0;
+  int max_epochs = 0, num_sms = 1;
+  std::vector<void*> allocs;
+  float *params = nullptr, *grad = nullptr, *m = nullptr, *v = nullptr;
+  int64_t* step = nullptr;
+  double* beta_pow = nullptr;
+  unsigned* done_ctr = nullptr;
+  double* sq = nullptr;
+  float *adv = nullptr, *ret = nullptr, *advstats = nullptr;
+  double* gae_part = nullptr;
+  int32_t* perm = nullptr;
+  void* perm_work = nullptr;
+  void* work = nullptr;
+  size_t work_bytes = 0;
+  int* err = nullptr;   // error word of the bounded device waits (tensor-core path)
+
+  ppo_status alloc(void** p, size_t bytes) {
+    void* q = nullptr;
+    if (bytes == 0) bytes = 16;
+    if (cudaMalloc(&q, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return PPO_ERR_NOMEM;
+    }
+    if (cudaMemset(q, 0, bytes) != cudaSuccess) {
+      cudaFree(q);
+      return PPO_ERR_CUDA;
+    }
+    allocs.push_back(q);
+    *p = q;
+    return PPO_OK;
+  }
+  template <class T>
+  ppo_status alloc_n(T** p, int64_t n) {
+    return alloc(reinterpret_cast<void**>(p), (size_t)n * sizeof(T));
+  }
+  ~ppo_rnn_ctx() {
+    for (void* p : allocs) cudaFree(p);
+  }
+};
+
+extern "C" {
+
+ppo_status ppo_rnn_create(const ppo_rnn_config* cfg, const float* h_init_params, int64_t max_T,
+                          int64_t max_N, int32_t max_epochs, ppo_rnn_ctx** out) {
+  if (!out) return PPO_ERR_INVALID;
+  *out = nullptr;
+  NetShape s;
+  int64_t P;
+  TRY(rnn_check(cfg, &s, &P));
+  if (max_T < 1 || max_N < 1 || max_epochs < 1 || max_T * max_N >= (1ll << 31))
+    return PPO_ERR_INVALID;
+  if (max_T > kGaeMaxT) return PPO_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PPO_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return PPO_ERR_CUDA;
+  if (major != 10 || minor != 3) return PPO_ERR_UNSUPPORTED;
+  ppo_rnn_ctx* c = new (std::nothrow) ppo_rnn_ctx();
+  if (!c) return PPO_ERR_NOMEM;
+  c->cfg = *cfg;
+  c->s = s;
+  c->P = P;
+  c->max_T = max_T;
+  c->max_N = max_N;
+  c->max_epochs = max_epochs;
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (c->num_sms < 1) c->num_sms = 1;
+  auto fail = [&](ppo_status st) {
+    delete c;
+    return st;
+  };
+  ppo_status r;
+#define A(ptr, n) \
+  if ((r = c->alloc_n(&(ptr), (n))) != PPO_OK) return fail(r);
+  A(c->params, P);
+  A(c->grad, P);
+  A(c->m, P);
+  A(c->v, P);
+  A(c->step, 1);
+  A(c->beta_pow, 4);
+  A(c->done_ctr, 1);
+  A(c->sq, 4096);
+  A(c->err, 1);
+  const int64_t B = max_T * max_N;
+  A(c->adv, B);
+  A(c->ret, B);
+  A(c->advstats, 4);
+  A(c->gae_part, 3 * (int64_t)gae_num_blocks((int)max_N));
+  A(c->perm, max_N * max_epochs);
+#undef A
+  if ((r = c->alloc(&c->perm_work, perm_workspace_bytes(max_N, max_epochs))) != PPO_OK)
+    return fail(r);
+  // the loss workspace for the largest minibatch (all N environments)
+  if ((r = ppo_rnn_workspace_bytes(cfg, max_T, max_N, &c->work_bytes)) != PPO_OK) return fail(r);
+  if ((r = c->alloc(&c->work, c->work_bytes)) != PPO_OK) return fail(r);
+  if (cfg->precision == 1 && tc_prepare() != cudaSuccess) return fail(PPO_ERR_CUDA);
+  if (h_init_params &&
+      cudaMemcpy(c->params, h_init_params, sizeof(float) * P, cudaMemcpyHostToDevice) !=
+          cudaSuccess)
+    return fail(PPO_ERR_CUDA);
+  const double one[4] = {1.0, 1.0, 1.0 / (1.0 - cfg->beta1), 1.0 / (1.0 - cfg->beta2)};
+  if (cudaMemcpy(c->beta_pow, one, sizeof one, cudaMemcpyHostToDevice) != cudaSuccess)
+    return fail(PPO_ERR_CUDA);
+  if (cudaDeviceSynchronize() != cudaSuccess) return fail(PPO_ERR_CUDA);
+  *out = c;
+  return PPO_OK;
+}
+
+ppo_status ppo_rnn_destroy(ppo_rnn_ctx* c) {
+  if (!c) return PPO_ERR_INVALID;
+  cudaDeviceSynchronize();
+  delete c;
+  return PPO_OK;
+}
+
+ppo_status ppo_rnn_buffers(ppo_rnn_ctx* c, float** d_params, float** d_grad, float** d_m,
+                           float** d_v) {
+  if (!c) return PPO_ERR_INVALID;
+  if (d_params) *d_params = c->params;
+  if (d_grad) *d_grad = c->grad;
+  if (d_m) *d_m = c->m;
+  if (d_v) *d_v = c->v;
+  return PPO_OK;
+}
+
+ppo_status ppo_rnn_update(ppo_rnn_ctx* c, const float* obs, const int32_t* act, const float* actc,
+                          const float* logp_old, const float* val, const float* rew,
+                          const float* done, const float* boot, const float* h0, int64_t T,
+                          int64_t N, int32_t epochs, int32_t minibatches, float gamma,
+                          float lambda, float lr, uint32_t seed, float* stats, cudaStream_t st) {
+  if (!c || !obs || !logp_old || !val || !rew || !done || !boot || !h0) return PPO_ERR_INVALID;
+  if ((c->s.NH > 0 && !act) || (c->s.G > 0 && !actc)) return PPO_ERR_INVALID;
+  if (T < 1 || N < 1 || epochs < 1 || minibatches < 1) return PPO_ERR_INVALID;
+  if (T > c->max_T || N > c->max_N || epochs > c->max_epochs || N % minibatches != 0)
+    return PPO_ERR_INVALID;
+  const void* ps[] = {obs, act, actc, logp_old, val, rew, done, boot, h0, stats};
+  for (const void* p : ps)
+    if (p && !al16(p)) return PPO_ERR_ALIGN;
+  const int64_t ns = N / minibatches;
+  // judge: GAE, statistics of all T*N advantages; the environment permutations
+  PPO_CUDA(cudaMemsetAsync(c->done_ctr, 0, sizeof(unsigned), st));
+  const int nb = gae_num_blocks((int)N);
+  PPO_CUDA(launch_gae(rew, val, done, boot, (int)T, (int)N, gamma, lambda, c->adv, c->ret,
+                      c->gae_part, nb, st));
+  PPO_CUDA(launch_gae_finalize(c->gae_part, nb, c->advstats, st));
+  PPO_CUDA(launch_perm(seed, 0, epochs, N, c->perm, c->perm_work, st, nullptr));
+  // learn
+  RnnLaunch a{};
+  a.s = c->s;
+  a.lc = LossCoef{c->cfg.clip, c->cfg.vf_coef, c->cfg.ent_coef};
+  a.T = (int)T;
+  a.ns = (int)ns;
+  a.D = c->cfg.obs_dim;
+  a.H = c->cfg.hidden;
+  a.L = c->cfg.layers;
+  a.N = N;
+  a.params = c->params;
+  a.obs = obs;
+  a.act = act;
+  a.actc = actc;
+  a.logp_old = logp_old;
+  a.adv = c->adv;
+  a.ret = c->ret;
+  a.adv_stats = c->advstats;
+  a.done = done;
+  a.h0 = h0;
+  a.grad = c->grad;
+  a.work = static_cast<float*>(c->work);
+  a.err = c->err;
+  AdamArgs aa{};
+  aa.p = c->params;
+  aa.g = c->grad;
+  aa.m = c->m;
+  aa.v = c->v;
+  aa.P = c->P;
+  aa.sq_part = c->sq;
+  aa.nsq = 0;   // the norm pass runs before Adam
+  aa.max_norm = c->cfg.max_grad_norm;
+  aa.lr = lr;
+  aa.b1 = c->cfg.beta1;
+  aa.b2 = c->cfg.beta2;
+  aa.eps = (float)c->cfg.adam_eps;
+  aa.omb1 = (float)(1.0 - c->cfg.beta1);
+  aa.omb2 = (float)(1.0 - c->cfg.beta2);
+  aa.step = c->step;
+  aa.beta_pow = c->beta_pow;
+  aa.done_ctr = c->done_ctr;
+  aa.s = c->s;   // no bf16 shadows: the loss builds its operand forms each minibatch
+  for (int e = 0; e < epochs; ++e) {
+    for (int k = 0; k < minibatches; ++k) {
+      a.envs = c->perm + (int64_t)e * N + (int64_t)k * ns;
+      a.stats6 = stats ? stats + ((int64_t)e * minibatches + k) * 6 : nullptr;
+      if (c->cfg.precision == 1)
+        PPO_CUDA(launch_rnn_loss_grad_tc(a, c->num_sms, st, nullptr));
+      else
+        PPO_CUDA(launch_rnn_loss_grad(a, st));
+      PPO_CUDA(launch_adam(aa, st));
+    }
+  }
+  return PPO_OK;
+}
+
+ppo_status ppo_rnn_sync_status(ppo_rnn_ctx* c, cudaStream_t st) {
+  if (!c) return PPO_ERR_INVALID;
+  PPO_CUDA(cudaStreamSynchronize(st));
+  if (c->cfg.precision == 1) {
+    int e = 0;
+    PPO_CUDA(cudaMemcpy(&e, c->err, sizeof(int), cudaMemcpyDeviceToHost));
+    if (e != 0) {
+      PPO_CUDA(cudaMemset(c->err, 0, sizeof(int)));
+      return PPO_ERR_TIMEOUT;
+    }
   }
   return PPO_OK;
 }

@@ -362,6 +362,8 @@ struct RnnLaunch {
   float* grad;
   float* stats6;            // [6] or nullptr
   float* work;              // rnn_workspace_floats(D, H, L, T*ns)
+  int* err;                 // tensor-core path: error word of bounded waits (nullptr:
+                            // the workspace's own, cleared at the call's start)
 };
 size_t rnn_workspace_floats(int D, int H, int L, int64_t rows);
 cudaError_t launch_rnn_loss_grad(const RnnLaunch& a, cudaStream_t st);

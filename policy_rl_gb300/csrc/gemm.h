@@ -111,13 +111,28 @@ struct WGradRegion {
 };
 
 // Largest tile count of a tc_wgrad call with in-kernel assembly (size of the
-// counter array: 2 * kWgradMaxTiles unsigned).
+// counter array: 2 * kWgradMaxTiles unsigned), and the most K-splits of a
+// product in one call.
 constexpr int kWgradMaxTiles = 256;
+constexpr int kMaxWgSplit = 64;
+
+// Loss and BPTT gradient of the recurrent policy on the tensor cores
+// (rnn_tc.cu): hidden 128 or 256; the workspace holds an error word at its
+// start (nonzero after a bounded device wait gave up), *err_out points to it.
+struct RnnLaunch;
+bool rnn_tc_supported(int D, int H);
+size_t rnn_tc_workspace_bytes(int D, int H, int L, int64_t T, int64_t ns, int num_sms);
+cudaError_t launch_rnn_loss_grad_tc(const RnnLaunch& a, int num_sms, cudaStream_t st,
+                                    int** err_out);
 
 cudaError_t tc_prepare();
 int tc_pick_bn(int N);
 int tc_wgrad_splits(int rows, int kt_per_split);
 int tc_wgrad_bn(int N);   // column width of the weight-gradient tiles of an N-column product
+// K-split plan of up to three products mn[i] = {M, N} over `rows` rows: kt[i]
+// 64-row k-tiles per unit, all units in one wave of num_sms CTAs when possible.
+void tc_wgrad_plan(const int (*mn)[2], int nreg, int64_t rows, int num_sms, int max_split,
+                   int* kt);
 
 cudaError_t tc_gemm_bias_act(const GemmOperands& g, const float* bias, int act,
                              __nv_bfloat16* out, int ldo, int* err, uint64_t timeout_ns,

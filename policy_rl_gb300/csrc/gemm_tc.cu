@@ -30,6 +30,8 @@
 // releases its TMEM before returning.
 #include <cudaTypedefs.h>
 
+#include <cmath>
+
 #include "common.cuh"
 #include "gemm.h"
 #include "reduce.cuh"
@@ -147,7 +149,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   pdl_wait();      // inputs are written by the previous kernel of the chain
   pdl_trigger();
   if (EPI != EPI_DACT) {  // the bias, read by every epilogue thread, staged once
-    for (int i = threadIdx.x; i < p.N; i += NT) bias_s[i] = p.bias[i];
+    for (int i = threadIdx.x; i < p.N; i += NT) bias_s[i] = p.bias ? p.bias[i] : 0.f;
     __syncthreads();      // reached by every thread of the block (before the role split)
   }
 
@@ -932,6 +934,36 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
 }
 
 int tc_wgrad_bn(int N) { return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64); }
+
+// At large minibatches the kernel streams its operands (each unit reads
+// (128 + bn) features of every row in its k-range) and the tensor pipe is not
+// the limit, so units are balanced by the bytes they load: a region of
+// bn-column tiles gets q / (128 + bn) k-tiles per unit.  q is the smallest
+// budget whose units fit in one wave of num_sms CTAs (a second, partial wave
+// would double the kernel's time); every unit covers at least 4 k-tiles and a
+// region is split at most max_split times.
+void tc_wgrad_plan(const int (*mn)[2], int nreg, int64_t rows, int num_sms, int max_split,
+                   int* kt) {
+  const int64_t k_tiles = (rows + BK - 1) / BK;
+  double total = 0;
+  for (int i = 0; i < nreg; ++i) {
+    const int bn = tc_wgrad_bn(mn[i][1]);
+    total += (double)(mn[i][0] / BM) * (mn[i][1] / bn) * (BM + bn) * k_tiles;
+  }
+  for (int64_t q = (int64_t)std::ceil(total / num_sms);; q += (q + 15) / 16) {
+    int64_t units = 0;
+    for (int i = 0; i < nreg; ++i) {
+      const int bn = tc_wgrad_bn(mn[i][1]);
+      int64_t kp = q / (BM + bn);
+      if (kp < 4) kp = 4;
+      if ((k_tiles + kp - 1) / kp > max_split) kp = (k_tiles + max_split - 1) / max_split;
+      if (kp > k_tiles) kp = k_tiles;
+      kt[i] = (int)kp;
+      units += (int64_t)(mn[i][0] / BM) * (mn[i][1] / bn) * ((k_tiles + kp - 1) / kp);
+    }
+    if (units <= num_sms || q >= 1024 * k_tiles) return;
+  }
+}
 
 int tc_wgrad_splits(int rows, int kt_per_split) {
   const int k_tiles = (rows + BK - 1) / BK;

@@ -125,7 +125,7 @@ __device__ __forceinline__ void epi_elem_tile(uint32_t taddr, int row, bool rok,
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float x = v[j] + bias_s[col0 + j];
-        v[j] = act == 0 ? tanh_fast(x) : fmaxf(x, 0.f);
+        v[j] = act == 0 ? tanh_fast(x) : (act == 1 ? fmaxf(x, 0.f) : x);
       }
       if (rok) store_bf16x32(out + (int64_t)row * ldo + col0, v);
     } else {
@@ -192,7 +192,8 @@ __device__ __forceinline__ void put_row_chunks(uint8_t* row, int r, int c16, con
   }
 }
 
-// act(acc + bias) for one 32-column chunk (bias read as float4 from shared memory)
+// act(acc + bias) for one 32-column chunk (bias read as float4 from shared
+// memory); act 0 tanh, 1 ReLU, 2 identity (a plain product)
 __device__ __forceinline__ void act_bias_chunk(const uint32_t (&r)[32], const float* bias, int act,
                                                float (&v)[32]) {
   const float4* b4 = reinterpret_cast<const float4*>(bias);   // 16-byte aligned
@@ -203,7 +204,7 @@ __device__ __forceinline__ void act_bias_chunk(const uint32_t (&r)[32], const fl
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float x = __uint_as_float(r[4 * j4 + e]) + bb[e];
-      v[4 * j4 + e] = act == 0 ? tanh_fast(x) : fmaxf(x, 0.f);
+      v[4 * j4 + e] = act == 0 ? tanh_fast(x) : (act == 1 ? fmaxf(x, 0.f) : x);
     }
   }
 }
