@@ -129,8 +129,10 @@ def lib():
         L.orc_policy_act.argtypes = [ctypes.POINTER(_Net), ctypes.c_int, _P, _I64, _P, ctypes.c_uint32,
                                      ctypes.c_uint64, _P, _P, _P, _P]
         L.orc_newton_schulz5.argtypes = [_I64, _I64, _P, ctypes.c_int, _P]
+        L.orc_newton_schulz5_bf16.argtypes = [_I64, _I64, _P, ctypes.c_int, _P]
         L.orc_muon.argtypes = [ctypes.POINTER(_Net), _P, _P, _P, _P, _P, _I64, _D, _D, _D, _D, _D,
                                _D]
+        L.orc_muon_bf16.argtypes = L.orc_muon.argtypes
         L.orc_rnn_num_params.argtypes = [ctypes.POINTER(_Rnn)]
         L.orc_rnn_num_params.restype = _I64
         L.orc_rnn_forward.argtypes = [ctypes.POINTER(_Rnn), _P, _I64, _I64, _I64, _P, _P, _P, _P,
@@ -532,22 +534,24 @@ def adam(p, g, m, v, step, lr, beta1=0.9, beta2=0.999, eps=1e-8):
     return p, m, v
 
 
-def newton_schulz5(G, steps: int = 5):
-    """Muon's quintic Newton-Schulz orthogonalisation of a matrix (fp64)."""
+def newton_schulz5(G, steps: int = 5, bf16: bool = False):
+    """Muon's quintic Newton-Schulz orthogonalisation of a matrix (fp64; bf16:
+    X, A, B stored as bf16)."""
     G = _as(G, np.float64)
     rows, cols = G.shape
     out = np.empty_like(G)
-    lib().orc_newton_schulz5(rows, cols, _ptr(G), steps, _ptr(out))
+    fn = lib().orc_newton_schulz5_bf16 if bf16 else lib().orc_newton_schulz5
+    fn(rows, cols, _ptr(G), steps, _ptr(out))
     return out
 
 
 def muon(net: Net, p, g, mom, m, v, step, muon_lr=0.02, muon_beta=0.95, lr=2.5e-4,
-         beta1=0.9, beta2=0.999, eps=1e-8):
+         beta1=0.9, beta2=0.999, eps=1e-8, bf16=False):
     """One Muon step (matrices) + Adam (vectors); returns (p, mom, m, v)."""
     p, mom, m, v = (_as(x, np.float64).copy() for x in (p, mom, m, v))
     g = _as(g, np.float64)
     cn = net.c()
-    lib().orc_muon(ctypes.byref(cn), _ptr(p), _ptr(g), _ptr(mom), _ptr(m), _ptr(v), step, muon_lr,
+    (lib().orc_muon_bf16 if bf16 else lib().orc_muon)(ctypes.byref(cn), _ptr(p), _ptr(g), _ptr(mom), _ptr(m), _ptr(v), step, muon_lr,
                    muon_beta, lr, beta1, beta2, eps)
     return p, mom, m, v
 

@@ -1061,7 +1061,12 @@ void orc_adam(int64_t P, double *p, const double *g, double *m, double *v, int64
  *     A = X X^T,  B = b A + c A A,  X = a X + B X,
  *   with (a, b, c) = (3.4445, -4.7750, 2.0315); transposed back.
  * The write-up runs the iteration in bf16; here it is fp64. */
-void orc_newton_schulz5(int64_t rows, int64_t cols, const double *G, int steps, double *out)
+/* bf16 mode (the write-up's precision): X, A and B are stored as bf16 --
+ * the normalised input, each product A = X X^T, B = b A + c A A and
+ * X = a X + B X rounded once computed (sums in fp64 of the rounded values).
+ * Identity when off. */
+static void orc_newton_schulz5_mode(int64_t rows, int64_t cols, const double *G, int steps,
+                                    int bf16, double *out)
 {
     const double ca = 3.4445, cb = -4.7750, cc = 2.0315;
     const int tr = rows > cols;
@@ -1075,25 +1080,25 @@ void orc_newton_schulz5(int64_t rows, int64_t cols, const double *G, int steps, 
     const double inv = 1.0 / (sqrt(ss) + 1e-7);
     for (int64_t i = 0; i < r; ++i)
         for (int64_t j = 0; j < k; ++j)
-            X[i * k + j] = (tr ? G[j * cols + i] : G[i * cols + j]) * inv;
+            X[i * k + j] = orc_rnd(bf16, (tr ? G[j * cols + i] : G[i * cols + j]) * inv);
     for (int s = 0; s < steps; ++s) {
         for (int64_t i = 0; i < r; ++i)
             for (int64_t j = 0; j < r; ++j) {
                 double t = 0.0;
                 for (int64_t q = 0; q < k; ++q) t += X[i * k + q] * X[j * k + q];
-                A[i * r + j] = t;
+                A[i * r + j] = orc_rnd(bf16, t);
             }
         for (int64_t i = 0; i < r; ++i)
             for (int64_t j = 0; j < r; ++j) {
                 double t = 0.0;
                 for (int64_t q = 0; q < r; ++q) t += A[i * r + q] * A[q * r + j];
-                B[i * r + j] = cb * A[i * r + j] + cc * t;
+                B[i * r + j] = orc_rnd(bf16, cb * A[i * r + j] + cc * t);
             }
         for (int64_t i = 0; i < r; ++i)
             for (int64_t j = 0; j < k; ++j) {
                 double t = 0.0;
                 for (int64_t q = 0; q < r; ++q) t += B[i * r + q] * X[q * k + j];
-                Xn[i * k + j] = ca * X[i * k + j] + t;
+                Xn[i * k + j] = orc_rnd(bf16, ca * X[i * k + j] + t);
             }
         memcpy(X, Xn, sizeof(double) * (size_t)(r * k));
     }
@@ -1105,6 +1110,16 @@ void orc_newton_schulz5(int64_t rows, int64_t cols, const double *G, int steps, 
     free(X); free(Xn); free(A); free(B);
 }
 
+void orc_newton_schulz5(int64_t rows, int64_t cols, const double *G, int steps, double *out)
+{
+    orc_newton_schulz5_mode(rows, cols, G, steps, 0, out);
+}
+
+void orc_newton_schulz5_bf16(int64_t rows, int64_t cols, const double *G, int steps, double *out)
+{
+    orc_newton_schulz5_mode(rows, cols, G, steps, 1, out);
+}
+
 /* One Muon step of the MLP's parameters (write-up's update with Nesterov
  * momentum): for each weight matrix W1, W2, W3 (rows x cols)
  *   mom = beta mom + g;  u = g + beta mom;
@@ -1113,9 +1128,10 @@ void orc_newton_schulz5(int64_t rows, int64_t cols, const double *G, int steps, 
  * for the biases and the log-std (orc_adam's update, this `step`).  mom
  * covers the whole parameter vector (only the matrix entries are used);
  * adam_m, adam_v likewise (only the vector entries). */
-void orc_muon(const orc_net *net, double *params, const double *g, double *mom,
-              double *adam_m, double *adam_v, int64_t step, double muon_lr, double muon_beta,
-              double lr, double beta1, double beta2, double eps)
+static void orc_muon_mode(const orc_net *net, double *params, const double *g, double *mom,
+                          double *adam_m, double *adam_v, int64_t step, double muon_lr,
+                          double muon_beta, double lr, double beta1, double beta2, double eps,
+                          int bf16)
 {
     const int64_t D = net->obs_dim, H1 = net->h1, H2 = net->h2, C = orc_out_cols(net);
     const int64_t P = orc_num_params(net);
@@ -1132,7 +1148,7 @@ void orc_muon(const orc_net *net, double *params, const double *g, double *mom,
             u[i] = g[o + i] + muon_beta * mom[o + i];
             is_mat[o + i] = 1;
         }
-        orc_newton_schulz5(rows[mtx], cols[mtx], u, 5, x);
+        orc_newton_schulz5_mode(rows[mtx], cols[mtx], u, 5, bf16, x);
         const double ratio = (double)rows[mtx] / (double)cols[mtx];
         const double scale = sqrt(ratio > 1.0 ? ratio : 1.0);
         for (int64_t i = 0; i < n; ++i) params[o + i] -= muon_lr * scale * x[i];
@@ -1147,6 +1163,22 @@ void orc_muon(const orc_net *net, double *params, const double *g, double *mom,
         params[i] -= lr * (adam_m[i] / bc1) / (sqrt(adam_v[i] / bc2) + eps);
     }
     free(is_mat);
+}
+
+void orc_muon(const orc_net *net, double *params, const double *g, double *mom,
+              double *adam_m, double *adam_v, int64_t step, double muon_lr, double muon_beta,
+              double lr, double beta1, double beta2, double eps)
+{
+    orc_muon_mode(net, params, g, mom, adam_m, adam_v, step, muon_lr, muon_beta, lr, beta1,
+                  beta2, eps, 0);
+}
+
+void orc_muon_bf16(const orc_net *net, double *params, const double *g, double *mom,
+                   double *adam_m, double *adam_v, int64_t step, double muon_lr,
+                   double muon_beta, double lr, double beta1, double beta2, double eps)
+{
+    orc_muon_mode(net, params, g, mom, adam_m, adam_v, step, muon_lr, muon_beta, lr, beta1,
+                  beta2, eps, 1);
 }
 
 /* One update of the recurrent policy ("Teaching Mario to speedrun", sec. 6
@@ -1201,8 +1233,8 @@ static void orc_optimize(const orc_net *net, const orc_hyper *hp, int64_t P, dou
                          const double *grad, double *m, double *v, double *mom, int64_t step)
 {
     if (hp->optimizer == 1)
-        orc_muon(net, params, grad, mom, m, v, step, hp->muon_lr, hp->muon_beta, hp->lr,
-                 hp->beta1, hp->beta2, hp->adam_eps);
+        orc_muon_mode(net, params, grad, mom, m, v, step, hp->muon_lr, hp->muon_beta, hp->lr,
+                      hp->beta1, hp->beta2, hp->adam_eps, hp->bf16_operands);
     else
         orc_adam(P, params, grad, m, v, step, hp->lr, hp->beta1, hp->beta2, hp->adam_eps);
 }

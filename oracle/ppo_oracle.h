@@ -189,9 +189,16 @@ void orc_adam(int64_t P, double *p, const double *g, double *m, double *v, int64
  * iterations), and one Muon step of the MLP (matrices W1..W3 by Muon with
  * Nesterov momentum mom, biases and log-std by Adam).  See ppo_oracle.c. */
 void orc_newton_schulz5(int64_t rows, int64_t cols, const double *G, int steps, double *out);
+/* The same with X, A, B stored as bf16 (each product rounded once computed). */
+void orc_newton_schulz5_bf16(int64_t rows, int64_t cols, const double *G, int steps,
+                             double *out);
 void orc_muon(const orc_net *net, double *params, const double *g, double *mom,
               double *adam_m, double *adam_v, int64_t step, double muon_lr, double muon_beta,
               double lr, double beta1, double beta2, double eps);
+/* orc_muon with the bf16 Newton-Schulz iteration (orc_newton_schulz5_bf16). */
+void orc_muon_bf16(const orc_net *net, double *params, const double *g, double *mom,
+                   double *adam_m, double *adam_v, int64_t step, double muon_lr,
+                   double muon_beta, double lr, double beta1, double beta2, double eps);
 
 typedef struct {
     double gamma, lambda, clip, vf_coef, ent_coef;

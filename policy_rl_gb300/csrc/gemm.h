@@ -40,6 +40,7 @@ struct TcParams {
   int lddz;
   int* err;
   uint64_t timeout_ns;
+  float alpha, beta;   // act 3 of the aux-tile epilogue: out = alpha aux + beta acc
 };
 
 // Gradient assembly from the split-K and per-CTA partials (optim.cu, and the
@@ -140,6 +141,11 @@ cudaError_t tc_gemm_bias_act(const GemmOperands& g, const float* bias, int act,
 cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ldaux, int act,
                          __nv_bfloat16* out, int ldo, float* colsum_part, int* err,
                          uint64_t timeout_ns, int num_sms, cudaStream_t st, int* grid_out);
+// out = alpha * aux + beta * (A B^T), bf16, aux and out [M][N] (N a multiple
+// of 128): the aux-tile kernel with its act' replaced by the sum.
+cudaError_t tc_gemm_axpby(const GemmOperands& g, const __nv_bfloat16* aux, int ldaux, float alpha,
+                          float beta, __nv_bfloat16* out, int ldo, int* err, uint64_t timeout_ns,
+                          int num_sms, cudaStream_t st);
 cudaError_t tc_gemm_loss(const GemmOperands& g, const NetShape& s, LossCoef lc, LossRows rows,
                          float inv_mb, const float* b3, const float* logstd, __nv_bfloat16* dz,
                          int lddz, float* colsum_part, float* loss_part, int* err,

@@ -265,7 +265,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!wait_bar(smem_u32(&xbar[xs]), (tc / C::NAUX) & 1, g)) break;
         uint8_t* slot = auxs + xs * C::AUX_SLOT;
         epi_dact_smem_tile<BN, EW>(taddr, q * 32 + lane, rok, tn * BN, h, p.act, slot,
-                                   cs + q * kColsumCap, lane);
+                                   cs + q * kColsumCap, lane, p.alpha, p.beta);
         tc_fence_before();
         mbar_arrive(cb.tempty(acc));
         fence_proxy_async_smem();
@@ -827,6 +827,25 @@ cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ld
   // 128 columns, so that 4 stages and two activation tiles fit
   if (g.N % 128 == 0) return launch_tc<128, EPI_DACT>(g, p, num_sms, st, grid_out);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_gemm_axpby(const GemmOperands& g, const __nv_bfloat16* aux, int ldaux, float alpha,
+                          float beta, __nv_bfloat16* out, int ldo, int* err, uint64_t timeout_ns,
+                          int num_sms, cudaStream_t st) {
+  if (g.N % 128 != 0) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.aux = aux;
+  p.ldaux = ldaux;
+  p.act = 3;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.out = out;
+  p.ldo = ldo;
+  p.colsum_part = nullptr;
+  p.epi_n = 0;   // no column sums
+  p.err = err;
+  p.timeout_ns = timeout_ns;
+  return launch_tc<128, EPI_DACT>(g, p, num_sms, st, nullptr);
 }
 
 cudaError_t tc_gemm_loss(const GemmOperands& g, const NetShape& s, LossCoef lc, LossRows rows,

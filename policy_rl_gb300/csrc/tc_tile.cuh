@@ -215,10 +215,13 @@ __device__ __forceinline__ void act_bias_chunk(const uint32_t (&r)[32], const fl
 // r*128 + ((c ^ (r & 7)) * 16)).  out = acc * act'(aux) is written back in
 // place (same thread, same bytes) for a TMA store of the tile; per-warp column
 // sums of out go to cs_q (rows >= M count as zero).
+// act == 3 instead: out = alpha * aux + beta * acc, no column sums (a
+// product added to a multiple of a tile of the same shape).
 template <int BN, int EW>
 __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool rok, int col_tile,
                                                    int h, int act, uint8_t* aux, float* cs_q,
-                                                   int lane) {
+                                                   int lane, float alpha = 0.f,
+                                                   float beta = 0.f) {
   constexpr int PART = BN / (EW / 4);
   tmem_chunks<PART / 32>(taddr, h * PART, [&](const uint32_t (&r)[32], int c0) {
     float v[32];
@@ -234,15 +237,22 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool 
       for (int hh = 0; hh < 4; ++hh) {
         const float2 hv = unpack_bf16x2(w4[hh]);
         const int j = 8 * i + 2 * hh;
-        const float d0 = act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
-        const float d1 = act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
-        v[j] = rok ? v[j] * d0 : 0.f;
-        v[j + 1] = rok ? v[j + 1] * d1 : 0.f;
+        if (act == 3) {
+          v[j] = rok ? alpha * hv.x + beta * v[j] : 0.f;
+          v[j + 1] = rok ? alpha * hv.y + beta * v[j + 1] : 0.f;
+        } else {
+          const float d0 = act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
+          const float d1 = act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
+          v[j] = rok ? v[j] * d0 : 0.f;
+          v[j + 1] = rok ? v[j + 1] * d1 : 0.f;
+        }
       }
     }
     put_row_chunks(blk, rl, c16, v);
-    const float colsum = warp_reduce_scatter32(v);
-    cs_q[col_tile + c0 + lane] += colsum;
+    if (act != 3) {
+      const float colsum = warp_reduce_scatter32(v);
+      cs_q[col_tile + c0 + lane] += colsum;
+    }
   });
 }
 

@@ -133,3 +133,28 @@ def test_update_with_muon_is_the_composition():
     np.testing.assert_allclose(res.params, q, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(res.mom, mo, rtol=1e-12, atol=1e-13)
     assert res.step == step
+
+
+# ---- bf16 Newton-Schulz (the write-up's precision) --------------------------------
+@pytest.mark.parametrize("shape", [(64, 256), (256, 256), (16, 256), (512, 1397)])
+def test_newton_schulz_bf16_is_close_to_fp64_and_rounds(shape):
+    rng = np.random.default_rng(sum(shape))
+    G = rng.standard_normal(shape)
+    x64 = oracle.newton_schulz5(G)
+    x16 = oracle.newton_schulz5(G, bf16=True)
+    err = np.linalg.norm(x16 - x64) / np.linalg.norm(x64)
+    assert err < 2e-2, err
+    assert err > 0
+    # every entry of the result is a bf16 value
+    assert all(oracle.round_bf16(v) == v for v in x16.ravel()[:2000])
+
+
+def test_newton_schulz_bf16_transposes_exactly_and_keeps_singular_values_in_band():
+    rng = np.random.default_rng(3)
+    G = rng.standard_normal((48, 200))
+    x = oracle.newton_schulz5(G, bf16=True)
+    np.testing.assert_array_equal(oracle.newton_schulz5(G.T.copy(), bf16=True), x.T)
+    s = np.linalg.svd(x, compute_uv=False)
+    # the quintic's five iterations take every singular value into a band
+    # around 1 (the write-up's (a, b, c) do not converge to exactly 1)
+    assert s.min() > 0.5 and s.max() < 1.3, (s.min(), s.max())
