@@ -223,15 +223,21 @@ def _roofline(stage, w, mb, ms_total, launches, hbm_peak, tf_peak, peak_src):
     """Roofline entry of one stage: bound = the larger of its tensor-time and
     HBM-time floors at the measured peaks; achieved = algorithmic work per
     launch / mean launch duration."""
-    if stage == "muon":   # 18 launches per optimizer step, fp32 CUDA-core products
-        steps = launches / 18
+    if stage == "muon":   # one optimizer step per minibatch
+        steps = w.epochs * w.minibatches
         achieved = _muon_step_flops(w) * steps / (ms_total / 1e3) / 1e12
+        if w.precision == "bf16":   # bf16 tensor-core Newton-Schulz products
+            return {"bound": "tensor", "kernel": stage, "achieved": round(achieved, 3),
+                    "peak": tf_peak, "unit": "TFLOP/s", "frac": round(achieved / tf_peak, 5),
+                    "traffic": None, "peak_kind": f"bf16 sustained ({peak_src})",
+                    "ms_per_optimizer_step": round(ms_total / steps, 4),
+                    "algorithmic_per_step": {"flop": _muon_step_flops(w), "bytes": None}}
         return {"bound": "alu", "kernel": stage, "achieved": round(achieved, 3),
                 "peak": round(FP32_ALU_TFLOPS, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / FP32_ALU_TFLOPS, 4), "traffic": None,
                 "peak_kind": "fp32 FMA, derived (152 SMs x 128 lanes x 2 x 2.07 GHz)",
-                "per_launch_us": round(ms_total / launches * 1e3, 2),
-                "algorithmic_per_launch": {"flop": _muon_step_flops(w) / 18, "bytes": None}}
+                "ms_per_optimizer_step": round(ms_total / steps, 4),
+                "algorithmic_per_step": {"flop": _muon_step_flops(w), "bytes": None}}
     work = _stage_work(stage, w, mb)
     if work is None:
         return None

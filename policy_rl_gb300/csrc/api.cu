@@ -74,6 +74,8 @@ struct ppo_ctx {
   float* mom = nullptr;
   float *ns_ws[3][4] = {};                      // per matrix: X0, X1 [r][k], A, B [r][r]
   float *mpart = nullptr, *minv = nullptr;
+  MuonTc mtc{};                                 // bf16 contexts: tensor-core Newton-Schulz
+  bool has_mtc = false;
   unsigned* fbar = nullptr;                     // grid-barrier counter of that kernel
   void* X = nullptr;
   // one epoch of minibatch rows gathered in permutation order (ppo_update)
@@ -149,6 +151,13 @@ struct ppo_ctx {
     return alloc(reinterpret_cast<void**>(p), (size_t)n * sizeof(T));
   }
   ~ppo_ctx() {
+    if (has_mtc) {
+      for (int i = 0; i < 3; ++i) {
+        if (mtc.side[i]) cudaStreamDestroy(mtc.side[i]);
+        if (mtc.join[i]) cudaEventDestroy(mtc.join[i]);
+      }
+      if (mtc.fork) cudaEventDestroy(mtc.fork);
+    }
     if (gexec) cudaGraphExecDestroy(gexec);
     if (gexec_pre) cudaGraphExecDestroy(gexec_pre);
     if (cev) cudaEventDestroy(cev);
@@ -636,7 +645,7 @@ MuonArgs make_muon_args(ppo_ctx* c) {
 ppo_status enqueue_muon(ppo_ctx* c, float lr, float* grad_norm_out, cudaStream_t st, int nsq) {
   if (!c->mom) return PPO_ERR_INVALID;   // context created with optimizer 0
   const AdamArgs a = make_adam_args(c, lr, grad_norm_out, nsq);
-  PPO_CUDA(launch_muon(make_muon_args(c), a, st, &c->tr));
+  PPO_CUDA(launch_muon(make_muon_args(c), a, st, &c->tr, c->has_mtc ? &c->mtc : nullptr));
   return PPO_OK;
 }
 
@@ -1025,6 +1034,30 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
       A(c->ns_ws[m][1], nr * nk);
       A(c->ns_ws[m][2], nr * nr);
       A(c->ns_ws[m][3], nr * nr);
+      if (c->bf16) {   // tensor-core iteration: bf16 X, X2, XT, A, B padded to 128
+        MuonTcMat& q = c->mtc.m[m];
+        q.r = (int)nr;
+        q.k = (int)nk;
+        q.rp = (int)round_up(nr, 128);
+        q.kp = (int)round_up(nk, 128);
+        A(q.X, (int64_t)q.rp * q.kp);
+        A(q.X2, (int64_t)q.rp * q.kp);
+        A(q.XT, (int64_t)q.kp * q.rp);
+        A(q.A, (int64_t)q.rp * q.rp);
+        A(q.B, (int64_t)q.rp * q.rp);
+      }
+    }
+    if (c->bf16) {
+      c->has_mtc = true;
+      for (int i = 0; i < 3; ++i) {
+        if (cudaStreamCreateWithFlags(&c->mtc.side[i], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&c->mtc.join[i], cudaEventDisableTiming) != cudaSuccess)
+          return fail(PPO_ERR_CUDA);
+      }
+      if (cudaEventCreateWithFlags(&c->mtc.fork, cudaEventDisableTiming) != cudaSuccess)
+        return fail(PPO_ERR_CUDA);
+      c->mtc.err = c->err;
+      c->mtc.num_sms = c->num_sms;
     }
   }
   if (c->bf16) {

@@ -244,9 +244,28 @@ struct MuonArgs {
 };
 // Clip (coefficient from a's squared-norm partials, computed by launch_muon
 // when a.nsq == 0), Muon on the three weight matrices, Adam (a) on the
-// biases and log-std, bf16 shadows refreshed.
+// biases and log-std, bf16 shadows refreshed.  With tc, the Newton-Schulz
+// products run on the tensor cores with bf16 X, A, B (see MuonTc).
+struct MuonTc;
 cudaError_t launch_muon(const MuonArgs& mu, const AdamArgs& a, cudaStream_t st,
-                        const Trace* tr = nullptr);
+                        const Trace* tr = nullptr, const MuonTc* tc = nullptr);
+
+// Tensor-core Newton-Schulz of one matrix: r x k (r <= k) zero-padded to
+// rp x kp (multiples of 128); bf16 X, X2 [rp][kp] (ping-pong), XT [kp][rp]
+// (X transposed), A, B [rp][rp].  The padding stays zero.
+struct MuonTcMat {
+  int r, k, rp, kp;
+  __nv_bfloat16 *X, *X2, *XT, *A, *B;
+};
+// The three matrices' iterations run concurrently on side streams (forked
+// from and joined back to the caller's stream with the events).
+struct MuonTc {
+  MuonTcMat m[3];
+  cudaStream_t side[3];
+  cudaEvent_t fork, join[3];
+  int* err;
+  int num_sms;
+};
 // Gradient assembly + clip + Adam in one cooperative launch (optim.cu); *bar
 // is a zeroed grid-barrier counter (cleared again by the kernel).
 cudaError_t reduce_adam_prepare();

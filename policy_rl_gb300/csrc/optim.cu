@@ -8,6 +8,7 @@
 // writes p, m, v and the bf16 weight shadows the tensor-core GEMMs read,
 // one coalesced grid-stride pass.
 #include <algorithm>
+#include <utility>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -616,8 +617,115 @@ cudaError_t launch_adam(const AdamArgs& a0, cudaStream_t st, const Trace* tr) {
   return cudaSuccess;
 }
 
+namespace {
+
+// X (bf16) = X0 * inv for the tensor-core iteration, and its transpose; the
+// padded rows and columns are never written (zero from allocation).
+__global__ void __launch_bounds__(kAdamThreads)
+muon_pack_kernel(MuonArgs mu, MuonTcMat t0, MuonTcMat t1, MuonTcMat t2) {
+  pdl_wait();
+  pdl_trigger();
+  const MuonTcMat tm[3] = {t0, t1, t2};
+  for (int mtx = 0; mtx < 3; ++mtx) {
+    const MuonTcMat& t = tm[mtx];
+    const float s = mu.inv[mtx];
+    const float* X0 = mu.m[mtx].X0;   // [r][k]
+    for (int e = blockIdx.x * kAdamThreads + threadIdx.x; e < t.r * t.k;
+         e += gridDim.x * kAdamThreads) {
+      const int i = e / t.k, j = e - i * t.k;
+      const __nv_bfloat16 v = __float2bfloat16_rn(X0[e] * s);
+      t.X[(int64_t)i * t.kp + j] = v;
+      t.XT[(int64_t)j * t.rp + i] = v;
+    }
+  }
+}
+
+// XT [kp][rp] = X^T of X [rp][kp] (32 x 32 tiles through shared memory).
+__global__ void muon_transpose_kernel(const __nv_bfloat16* __restrict__ X,
+                                      __nv_bfloat16* __restrict__ XT, int rp, int kp) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int bx = blockIdx.x * 32, by = blockIdx.y * 32;   // column block of X, row block
+  pdl_wait();
+  pdl_trigger();
+  for (int y = threadIdx.y; y < 32; y += blockDim.y) {
+    const int i = by + y, j = bx + threadIdx.x;
+    if (i < rp && j < kp) tile[y][threadIdx.x] = X[(int64_t)i * kp + j];
+  }
+  __syncthreads();
+  for (int y = threadIdx.y; y < 32; y += blockDim.y) {
+    const int j = bx + y, i = by + threadIdx.x;
+    if (i < rp && j < kp) XT[(int64_t)j * rp + i] = tile[threadIdx.x][y];
+  }
+}
+
+// W -= lr sqrt(max(1, rows/cols)) X with the final bf16 X of the tensor-core
+// iteration ([rp][kp], transposed back when tall), bf16 shadows refreshed.
+__global__ void __launch_bounds__(kAdamThreads)
+muon_apply_tc_kernel(MuonArgs mu, const __nv_bfloat16* X0, const __nv_bfloat16* X1,
+                     const __nv_bfloat16* X2, int kp0, int kp1, int kp2) {
+  pdl_wait();
+  pdl_trigger();
+  const bool shadows = mu.sh.W1s != nullptr;
+  const __nv_bfloat16* Xs[3] = {X0, X1, X2};
+  const int kps[3] = {kp0, kp1, kp2};
+  for (int mtx = 0; mtx < 3; ++mtx) {
+    const MuonMat& m = mu.m[mtx];
+    const int n = m.rows * m.cols;
+    const bool tr = m.rows > m.cols;
+    const float ratio = (float)m.rows / (float)m.cols;
+    const float step = mu.lr * sqrtf(ratio > 1.f ? ratio : 1.f);
+    for (int i = blockIdx.x * kAdamThreads + threadIdx.x; i < n; i += gridDim.x * kAdamThreads) {
+      const int row = i / m.cols, col = i - row * m.cols;
+      const float x = __bfloat162float(
+          Xs[mtx][tr ? (int64_t)col * kps[mtx] + row : (int64_t)row * kps[mtx] + col]);
+      const float p = m.p[i] - step * x;
+      m.p[i] = p;
+      if (shadows) write_shadow(mu.s, mu.sh, (int)(m.off + i), p);
+    }
+  }
+}
+
+}  // namespace
+
+// Five Newton-Schulz iterations of the three matrices on the tensor cores,
+// each matrix's chain on its own side stream:
+//   A = X X^T;  B = b A + c A A (A symmetric: A A = A A^T);  X2 = a X + B X
+//   (B X = B (X^T)^T, the transpose held in XT);  XT = X2^T;  swap X, X2.
+static cudaError_t muon_tc_iterations(const MuonTc& t, cudaStream_t st, __nv_bfloat16** final) {
+  cudaError_t e = cudaEventRecord(t.fork, st);
+  if (e != cudaSuccess) return e;
+  for (int m = 0; m < 3; ++m) {
+    const MuonTcMat& q = t.m[m];
+    cudaStream_t s = t.side[m];
+    if ((e = cudaStreamWaitEvent(s, t.fork, 0)) != cudaSuccess) return e;
+    __nv_bfloat16 *X = q.X, *X2 = q.X2;
+    for (int it = 0; it < 5; ++it) {
+      const uint64_t to = 2000000000ull;
+      e = tc_gemm_bias_act(GemmOperands{X, q.kp, X, q.kp, q.rp, q.rp, q.kp}, nullptr, 2, q.A,
+                           q.rp, t.err, to, t.num_sms, s);
+      if (e == cudaSuccess)
+        e = tc_gemm_axpby(GemmOperands{q.A, q.rp, q.A, q.rp, q.rp, q.rp, q.rp}, q.A, q.rp,
+                          kNsB, kNsC, q.B, q.rp, t.err, to, t.num_sms, s);
+      if (e == cudaSuccess)
+        e = tc_gemm_axpby(GemmOperands{q.B, q.rp, q.XT, q.rp, q.rp, q.kp, q.rp}, X, q.kp, kNsA,
+                          1.f, X2, q.kp, t.err, to, t.num_sms, s);
+      if (e != cudaSuccess) return e;
+      if (it < 4) {   // the last iterate is not transposed: apply reads X
+        const dim3 grid((unsigned)(q.kp / 32), (unsigned)(q.rp / 32));
+        e = launch_pdl(muon_transpose_kernel, grid, dim3(32, 8), 0, s, X2, q.XT, q.rp, q.kp);
+        if (e != cudaSuccess) return e;
+      }
+      std::swap(X, X2);
+    }
+    final[m] = X;
+    if ((e = cudaEventRecord(t.join[m], s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(st, t.join[m], 0)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_muon(const MuonArgs& mu, const AdamArgs& a0, cudaStream_t st,
-                        const Trace* tr) {
+                        const Trace* tr, const MuonTc* tc) {
   AdamArgs a = a0;
   if (a.nsq <= 0) {   // no squared-norm partials supplied: compute them
     const int nb = blocks_for((a.P + 3) / 4, kNormThreads, kNormBlocks);
@@ -639,6 +747,23 @@ cudaError_t launch_muon(const MuonArgs& mu, const AdamArgs& a0, cudaStream_t st,
   e = launch_pdl(muon_norm_kernel, dim3(1), dim3(32), 0, st, mu);
   if (e != cudaSuccess) return e;
   if (tr) tr->mark(ST_MUON, st);
+  if (tc) {
+    e = launch_pdl(muon_pack_kernel, dim3(152), dim3(kAdamThreads), 0, st, mu, tc->m[0],
+                   tc->m[1], tc->m[2]);
+    if (e != cudaSuccess) return e;
+    if (tr) tr->mark(ST_MUON, st);
+    __nv_bfloat16* fin[3];
+    if ((e = muon_tc_iterations(*tc, st, fin)) != cudaSuccess) return e;
+    if (tr) tr->mark(ST_MUON, st);
+    e = launch_pdl(muon_apply_tc_kernel,
+                   dim3(blocks_for(mu.m[1].rows * mu.m[1].cols, kAdamThreads, 152)),
+                   dim3(kAdamThreads), 0, st, mu, (const __nv_bfloat16*)fin[0],
+                   (const __nv_bfloat16*)fin[1], (const __nv_bfloat16*)fin[2], tc->m[0].kp,
+                   tc->m[1].kp, tc->m[2].kp);
+    if (e != cudaSuccess) return e;
+    if (tr) tr->mark(ST_MUON, st);
+    return cudaSuccess;
+  }
   NsStage sg{};
   int ntile[3][3];   // [stage][matrix]
   for (int m = 0; m < 3; ++m) {

@@ -3,10 +3,13 @@
 "Teaching Mario to speedrun", sec. 8 and "puff-rs" (Muon, five Newton-Schulz
 iterations per weight matrix); definition from Muon's published write-up.
 - one to three steps on identical gradients: the parameter change of the
-  weight matrices normwise within 1e-4 of the fp64 oracle (fp32 products;
-  the quintic iteration amplifies rounding by at most a^5 ~ 480 on the
-  smallest singular directions), momentum buffers within 1e-6, Adam on the
-  biases / log-std as in test_gpu_update (1e-6), gradient norm 1e-5;
+  weight matrices normwise within 1e-4 of the fp64 oracle in fp32 contexts
+  (fp32 CUDA-core products; the quintic iteration amplifies rounding by at
+  most a^5 ~ 480 on the smallest singular directions), and within 2e-2 of
+  the oracle's bf16 Newton-Schulz in bf16 contexts (tensor-core products
+  with X, A, B stored as bf16, as in the write-up); momentum buffers within
+  1e-6, Adam on the biases / log-std as in test_gpu_update (1e-6), gradient
+  norm 1e-5;
 - shapes: wide, tall (transposed) and square matrices up to 512 x 1397;
 - whole update with Muon: parameter change against the oracle's trajectory
   (fp32 1e-3, bf16 0.1 as for Adam), bit-identical replays.
@@ -48,16 +51,18 @@ def test_muon_steps_match_oracle(wname, prec):
         ctx.muon_step(lr, grad_norm=gn)
         ctx.sync_status()
         norm, gc = oracle.clip_grad_norm(g.astype(np.float64), w.max_grad_norm)
-        p, mom, m, v = oracle.muon(net, p, gc, mom, m, v, step, 0.02, 0.95, lr)
+        p, mom, m, v = oracle.muon(net, p, gc, mom, m, v, step, 0.02, 0.95, lr,
+                                   bf16=prec == "bf16")
         assert abs(host(gn)[0] - norm) <= 1e-5 * norm
     assert ctx.step() == 3
     got = host(ctx.params).astype(np.float64)
+    tol = 1e-4 if prec == "fp32" else 2e-2
     for name, sl in param_slices(w).items():
         if sl.stop == sl.start:
             continue
         if name.startswith("W"):
             e = normwise(got[sl] - p0[sl], p[sl] - p0[sl])
-            assert e <= 1e-4, (name, e)
+            assert e <= tol, (name, e)
         else:
             np.testing.assert_allclose(got[sl], p[sl], rtol=1e-6, atol=1e-7)
     ctx.close()
