@@ -192,13 +192,12 @@ OPTIMIZERS = {"adam": 0, "muon": 1}
 # ncu capture of the current kernels, cold caches; stages without such a
 # capture report null.
 NCU_TRAFFIC = {
-    ("mario", "fwd1_gemm"): 4.254e6, ("mario", "fwd2_gemm"): 16.936e6,
-    ("mario", "head_loss_gemm"): 17.769e6, ("mario", "dact2_gemm"): 21.041e6,
-    ("mario", "dact1_gemm"): 33.731e6, ("mario", "wgrad_gemm"): 77.725e6,
-    ("mario", "grad_reduce_adam"): 13.008e6,
-    ("large", "fwd1_gemm"): 274.744e6, ("large", "fwd2_gemm"): 489.007e6,
-    ("large", "head_loss_gemm"): 284.109e6, ("large", "dact2_gemm"): 526.100e6,
-    ("large", "dact1_gemm"): 773.235e6, ("large", "wgrad_gemm"): 1191.282e6,
+    ("mario", "fwd1_gemm"): 4.26e6, ("mario", "fwd2_gemm"): 16.94e6,
+    ("mario", "head_loss_gemm"): 17.77e6, ("mario", "dact2_gemm"): 21.05e6,
+    ("mario", "dact1_gemm"): 33.73e6, ("mario", "wgrad_gemm"): 76.20e6,
+    ("large", "fwd1_gemm"): 273.29e6, ("large", "fwd2_gemm"): 485.66e6,
+    ("large", "head_loss_gemm"): 281.18e6, ("large", "dact2_gemm"): 522.56e6,
+    ("large", "dact1_gemm"): 769.47e6, ("large", "wgrad_gemm"): 1191.22e6,
 }
 
 
@@ -816,6 +815,8 @@ def run_drive(args):
     g.manual_seed(0)
     if args.drive in ("minibatch", "update"):
         w = synth.WORKLOADS[args.workload]
+        if args.drive_T:   # a shorter horizon: one minibatch of the same width
+            w = w.scaled(T=args.drive_T, minibatches=max(1, w.minibatches * args.drive_T // w.T))
         B, mb = w.B, w.B // w.minibatches
         big = B * w.obs_dim > 2e8
         ro = synth.rollout(w, with_obs=not big)
@@ -896,6 +897,9 @@ def main():
                                         "rnn_update", "muon"],
                     help="plain driver loop for profilers (no timing, no JSON line)")
     ap.add_argument("--reps", type=int, default=3, help="--drive: repetitions")
+    ap.add_argument("--drive-T", type=int, default=0,
+                    help="--drive minibatch/update: horizon of a smaller rollout of the workload "
+                         "(minibatch size kept)")
     ap.add_argument("--gae-T", type=int, default=1024, help="--drive gae: horizon")
     ap.add_argument("--gae-N", type=int, default=65536, help="--drive gae: environments")
     args = ap.parse_args()
