@@ -450,14 +450,40 @@ ppo_status ppo_update(ppo_ctx *ctx, const float *d_obs, const int32_t *d_act_dis
 
 /* Same update, from HOST arrays (ideally pinned): copies the rollout into
  * context-owned device buffers, runs ppo_update, copies the stats back into
- * h_stats (nullable, fp32 [epochs*minibatches][6]) and synchronises
- * `stream`.  h_act_cont may be NULL if n_gauss == 0. */
+ * h_stats (nullable, fp32 [epochs*minibatches][6]) and returns when all of
+ * it is done.  h_act_cont may be NULL if n_gauss == 0.  Waits first for any
+ * ppo_update_host_async still in flight. */
 ppo_status ppo_update_host(ppo_ctx *ctx, const float *h_obs, const int32_t *h_act_disc,
                            const float *h_act_cont, const float *h_logp_old, const float *h_val,
                            const float *h_rew, const float *h_done, const float *h_boot,
                            int64_t T, int64_t N, int32_t epochs, int32_t minibatches,
                            float gamma, float lambda, float lr, uint32_t seed, float *h_stats,
                            cudaStream_t stream);
+
+/* Pipelined form of ppo_update_host: enqueues the copies, the update and the
+ * stats copy-back and returns without waiting for them, so that the copies
+ * of one call run on the copy engines while the previous call's update
+ * computes.  The context stages rollouts in two device slots, used in turn.
+ * Before enqueueing, a call waits on the host until the call two before it
+ * (the last user of its slot) has completed: on return from call k, the
+ * update of call k-2 is done, its h_stats written and its host arrays no
+ * longer read.  The arrays of calls k-1 and k must stay unchanged, and their
+ * h_stats unread, until a later call returns or ppo_host_wait does.
+ * The copies overlap compute only from page-locked host memory (pageable
+ * arrays still give correct results, without the overlap).  Successive
+ * calls belong on one stream; a call on another stream first waits for the
+ * calls in flight.  Arguments and errors as ppo_update_host; on an error
+ * nothing of the call is enqueued except possibly its copies. */
+ppo_status ppo_update_host_async(ppo_ctx *ctx, const float *h_obs, const int32_t *h_act_disc,
+                                 const float *h_act_cont, const float *h_logp_old,
+                                 const float *h_val, const float *h_rew, const float *h_done,
+                                 const float *h_boot, int64_t T, int64_t N, int32_t epochs,
+                                 int32_t minibatches, float gamma, float lambda, float lr,
+                                 uint32_t seed, float *h_stats, cudaStream_t stream);
+
+/* Waits until every ppo_update_host_async of the context has completed
+ * (updates done, stats on the host, host arrays free). */
+ppo_status ppo_host_wait(ppo_ctx *ctx);
 
 /* ---- Profiling -----------------------------------------------------------------
  * The library's kernels, by stage; one stage entry is one kernel launch.

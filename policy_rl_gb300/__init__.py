@@ -22,6 +22,7 @@ __all__ = [
     "make_rnn_config", "ppo_rnn_param_count", "ppo_rnn_workspace_bytes", "ppo_rnn_loss_grad",
     "ppo_create", "ppo_destroy", "ppo_buffers", "ppo_params_changed", "ppo_get_step",
     "ppo_minibatch_loss_grad", "ppo_adam_step", "ppo_update", "ppo_update_host",
+    "ppo_update_host_async", "ppo_host_wait",
     "ppo_sync_status", "ppo_stage_name", "ppo_update_profile", "ppo_set_step_trace",
     "ppo_set_wait_limit", "ppo_set_collective", "TorchCollective", "RnnContext",
     "library_path",
@@ -319,6 +320,19 @@ def ppo_update_host(ctx, obs, act_disc, act_cont, logp_old, val, rew, done, boot
         _ptr(stats), _stream(stream)), "ppo_update_host")
 
 
+def ppo_update_host_async(ctx, obs, act_disc, act_cont, logp_old, val, rew, done, boot, epochs,
+                          minibatches, gamma, lam, lr, seed, stats=None, stream=None) -> None:
+    T, N = val.shape
+    _abi.check(_lib().ppo_update_host_async(
+        ctx, _ptr(obs), _ptr(act_disc), _ptr(act_cont), _ptr(logp_old), _ptr(val), _ptr(rew),
+        _ptr(done), _ptr(boot), T, N, epochs, minibatches, gamma, lam, lr, seed & 0xFFFFFFFF,
+        _ptr(stats), _stream(stream)), "ppo_update_host_async")
+
+
+def ppo_host_wait(ctx) -> None:
+    _abi.check(_lib().ppo_host_wait(ctx), "ppo_host_wait")
+
+
 def ppo_stage_name(stage: int) -> str:
     return _lib().ppo_stage_name(stage).decode()
 
@@ -447,6 +461,12 @@ class Context:
 
     def update_host(self, *a, **k):
         return ppo_update_host(self.handle, *a, **k)
+
+    def update_host_async(self, *a, **k):
+        return ppo_update_host_async(self.handle, *a, **k)
+
+    def host_wait(self):
+        return ppo_host_wait(self.handle)
 
     def update_profile(self, *a, **k):
         return ppo_update_profile(self.handle, *a, **k)

@@ -21,8 +21,10 @@ SYMBOLS = (
     "ppo_perm_workspace_bytes", "ppo_minibatch_perm", "ppo_minibatch_loss_grad",
     "ppo_minibatch_loss_grad_fresh", "ppo_policy_act", "ppo_adam_step", "ppo_muon_step",
     "ppo_rnn_param_count", "ppo_rnn_workspace_bytes", "ppo_rnn_loss_grad", "ppo_rnn_create",
-    "ppo_rnn_destroy", "ppo_rnn_buffers", "ppo_rnn_update", "ppo_rnn_sync_status", "ppo_update", "ppo_update_host", "ppo_stage_name", "ppo_update_profile",
-    "ppo_sync_status", "ppo_set_collective", "ppo_set_step_trace", "ppo_set_wait_limit",
+    "ppo_rnn_destroy", "ppo_rnn_buffers", "ppo_rnn_update", "ppo_rnn_sync_status", "ppo_update",
+    "ppo_update_host", "ppo_update_host_async", "ppo_host_wait", "ppo_stage_name",
+    "ppo_update_profile", "ppo_sync_status", "ppo_set_collective", "ppo_set_step_trace",
+    "ppo_set_wait_limit",
 )
 NUM_STAGES = 34
 NUM_KERNEL_STAGES = 25
@@ -133,6 +135,9 @@ def load(path: str = LIB_PATH):
                         u32, _P, _P], ctypes.c_int),
         "ppo_update_host": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F, _F,
                              _F, u32, _P, _P], ctypes.c_int),
+        "ppo_update_host_async": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32,
+                                   _F, _F, _F, u32, _P, _P], ctypes.c_int),
+        "ppo_host_wait": ([_P], ctypes.c_int),
         "ppo_stage_name": ([i32], ctypes.c_char_p),
         "ppo_update_profile": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, i32, i32, _F,
                                 _F, _F, u32, _P, _P, _P, _P], ctypes.c_int),

@@ -40,6 +40,41 @@ struct UpdateKey {
   bool operator==(const UpdateKey& o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
 };
 
+// one cached update: part 1 (GAE, moments, permutations) and part 2 (the
+// rest) as two executable graphs, so that a host update can make part 2 wait
+// for its observation copy
+struct GraphEntry {
+  UpdateKey key{};
+  cudaGraphExec_t pre = nullptr, main = nullptr;
+  uint64_t used = 0;
+  bool valid = false;
+  void reset() {
+    // an executable graph still in flight is released when it completes
+    if (pre) cudaGraphExecDestroy(pre);
+    if (main) cudaGraphExecDestroy(main);
+    pre = main = nullptr;
+    valid = false;
+  }
+};
+constexpr int kGraphCache = 4;
+
+// device copy of one host rollout and the events that order its use:
+// gae_in (values, rewards, dones, bootstrap) copied, rest (observations,
+// actions, old log-probs) copied, freed (the update that read it and its
+// stats copy-back done)
+struct HostSlot {
+  float *obs = nullptr, *actc = nullptr, *logp = nullptr, *val = nullptr, *rew = nullptr,
+        *done = nullptr, *boot = nullptr;
+  int32_t* act = nullptr;
+  cudaEvent_t gae_in = nullptr, rest = nullptr, freed = nullptr;
+  bool used = false;   // freed has been recorded at least once
+  void destroy_events() {
+    for (cudaEvent_t e : {gae_in, rest, freed})
+      if (e) cudaEventDestroy(e);
+    gae_in = rest = freed = nullptr;
+  }
+};
+
 }  // namespace
 
 struct ppo_ctx {
@@ -112,24 +147,30 @@ struct ppo_ctx {
   double* mom_all = nullptr;
   int mom_cap = 0;
 
-  // host-update staging (allocated on first ppo_update_host)
-  float *st_obs = nullptr, *st_actc = nullptr, *st_logp = nullptr, *st_val = nullptr,
-        *st_rew = nullptr, *st_done = nullptr, *st_boot = nullptr, *st_stats = nullptr;
-  int32_t* st_act = nullptr;
+  // host-update staging (allocated on first ppo_update_host[_async]): two
+  // slots, so that the copies of one call run while the previous call's
+  // update still reads the other slot
+  HostSlot hs[2];
+  float* st_stats = nullptr;
   int64_t st_stats_cap = 0;
+  int hs_next = 0;                  // slot of the next host update
+  cudaStream_t hs_stream = nullptr; // the stream of the host updates in flight
+  int hs_inflight = 0;              // host updates enqueued and not yet waited for
 
   // kernel-boundary trace hook (profiling) and its events
   Trace tr;
   std::vector<cudaEvent_t> prof_events;
   std::vector<int> prof_stages;
 
-  // graph cache of the last ppo_update
-  cudaGraphExec_t gexec = nullptr;        // the update after GAE and the permutation
-  cudaGraphExec_t gexec_pre = nullptr;    // GAE, advantage moments, permutations
-  cudaStream_t cst = nullptr;             // ppo_update_host: rollout copies that GAE does not read
-  cudaEvent_t cev = nullptr;
-  UpdateKey gkey{};
-  bool gvalid = false;
+  // graph cache of ppo_update, least recently used entry replaced: one
+  // entry per argument set (the two host staging slots are two)
+  GraphEntry gc[kGraphCache];
+  uint64_t gclock = 0;
+  cudaStream_t cst = nullptr;             // host updates: the rollout copies
+
+  void invalidate_graphs() {
+    for (GraphEntry& g : gc) g.reset();
+  }
 
   ppo_status alloc(void** p, size_t bytes) {
     void* q = nullptr;
@@ -158,9 +199,8 @@ struct ppo_ctx {
       }
       if (mtc.fork) cudaEventDestroy(mtc.fork);
     }
-    if (gexec) cudaGraphExecDestroy(gexec);
-    if (gexec_pre) cudaGraphExecDestroy(gexec_pre);
-    if (cev) cudaEventDestroy(cev);
+    invalidate_graphs();
+    for (HostSlot& h : hs) h.destroy_events();
     if (cst) cudaStreamDestroy(cst);
     for (cudaEvent_t e : prof_events) cudaEventDestroy(e);
     for (void* p : allocs) cudaFree(p);
@@ -1565,15 +1605,14 @@ ppo_status run_update(ppo_ctx* c, const float* obs, const int32_t* act, const fl
   key.seed = seed;
   key.stats = stats;
   key.stream = st;
-  if (!c->gvalid || !(key == c->gkey)) {
-    for (cudaGraphExec_t* g : {&c->gexec_pre, &c->gexec})
-      if (*g) {
-        cudaGraphExecDestroy(*g);
-        *g = nullptr;
-      }
-    c->gvalid = false;
-    // two graphs: part 1 (GAE, moments, permutations) and part 2 (the rest),
-    // so that ppo_update_host can wait for the observation copy in between
+  GraphEntry* g = nullptr;
+  for (GraphEntry& e : c->gc)
+    if (e.valid && e.key == key) g = &e;
+  if (!g) {
+    g = &c->gc[0];
+    for (GraphEntry& e : c->gc)
+      if (!e.valid || e.used < g->used) g = &e;
+    g->reset();
     for (int part = 1; part <= 2; ++part) {
       PPO_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
       ppo_status r = enqueue_update(c, obs, act, actc, logp_old, val, rew, done, boot, T, N,
@@ -1585,16 +1624,20 @@ ppo_status run_update(ppo_ctx* c, const float* obs, const int32_t* act, const fl
         return r;
       }
       if (e != cudaSuccess) return PPO_ERR_CUDA;
-      e = cudaGraphInstantiate(part == 1 ? &c->gexec_pre : &c->gexec, graph, 0);
+      e = cudaGraphInstantiate(part == 1 ? &g->pre : &g->main, graph, 0);
       cudaGraphDestroy(graph);
-      if (e != cudaSuccess) return PPO_ERR_CUDA;
+      if (e != cudaSuccess) {
+        g->reset();
+        return PPO_ERR_CUDA;
+      }
     }
-    c->gkey = key;
-    c->gvalid = true;
+    g->key = key;
+    g->valid = true;
   }
-  PPO_CUDA(cudaGraphLaunch(c->gexec_pre, st));
+  g->used = ++c->gclock;
+  PPO_CUDA(cudaGraphLaunch(g->pre, st));
   if (wait_before_part2) PPO_CUDA(cudaStreamWaitEvent(st, wait_before_part2, 0));
-  PPO_CUDA(cudaGraphLaunch(c->gexec, st));
+  PPO_CUDA(cudaGraphLaunch(g->main, st));
   return PPO_OK;
 }
 }  // namespace
@@ -1701,12 +1744,28 @@ ppo_status ppo_update_profile(ppo_ctx* c, const float* obs, const int32_t* act,
   return PPO_OK;
 }
 
-ppo_status ppo_update_host(ppo_ctx* c, const float* h_obs, const int32_t* h_act,
-                           const float* h_actc, const float* h_logp_old, const float* h_val,
-                           const float* h_rew, const float* h_done, const float* h_boot,
-                           int64_t T, int64_t N, int32_t epochs, int32_t minibatches,
-                           float gamma, float lambda, float lr, uint32_t seed, float* h_stats,
-                           cudaStream_t st) {
+}  // extern "C"
+
+namespace {
+// waits (host) for every host update in flight
+ppo_status host_wait_all(ppo_ctx* c) {
+  if (c->hs_inflight > 0) {
+    for (HostSlot& h : c->hs)
+      if (h.used) PPO_CUDA(cudaEventSynchronize(h.freed));
+    PPO_CUDA(cudaStreamSynchronize(c->cst));
+    c->hs_inflight = 0;
+  }
+  return PPO_OK;
+}
+
+// ppo_update_host / ppo_update_host_async: stage the rollout in the next
+// slot on the copy stream and enqueue the update and the stats copy-back on
+// `st`; returns once everything is enqueued
+ppo_status host_update(ppo_ctx* c, const float* h_obs, const int32_t* h_act,
+                       const float* h_actc, const float* h_logp_old, const float* h_val,
+                       const float* h_rew, const float* h_done, const float* h_boot, int64_t T,
+                       int64_t N, int32_t epochs, int32_t minibatches, float gamma,
+                       float lambda, float lr, uint32_t seed, float* h_stats, cudaStream_t st) {
   if (!c || !h_obs || !h_logp_old || !h_val || !h_rew || !h_done || !h_boot)
     return PPO_ERR_INVALID;
   if ((c->s.NH > 0 && !h_act) || (c->s.G > 0 && !h_actc)) return PPO_ERR_INVALID;
@@ -1716,49 +1775,92 @@ ppo_status ppo_update_host(ppo_ctx* c, const float* h_obs, const int32_t* h_act,
   if (B > c->bmax) return PPO_ERR_INVALID;
   const NetShape& s = c->s;
   ppo_status r;
-  if (!c->st_obs) {
+  if (!c->cst) PPO_CUDA(cudaStreamCreateWithFlags(&c->cst, cudaStreamNonBlocking));
+  HostSlot& h = c->hs[c->hs_next];
+  if (!h.obs) {
     const int64_t Bm = c->bmax;
-    if ((r = c->alloc_n(&c->st_obs, Bm * s.D)) != PPO_OK) return r;
-    if ((r = c->alloc_n(&c->st_act, Bm * (s.NH > 0 ? s.NH : 1))) != PPO_OK) return r;
-    if ((r = c->alloc_n(&c->st_actc, Bm * (s.G > 0 ? s.G : 1))) != PPO_OK) return r;
-    if ((r = c->alloc_n(&c->st_logp, Bm)) != PPO_OK) return r;
-    if ((r = c->alloc_n(&c->st_val, Bm)) != PPO_OK) return r;
-    if ((r = c->alloc_n(&c->st_rew, Bm)) != PPO_OK) return r;
-    if ((r = c->alloc_n(&c->st_done, Bm)) != PPO_OK) return r;
-    if ((r = c->alloc_n(&c->st_boot, Bm)) != PPO_OK) return r;
+    if ((r = c->alloc_n(&h.obs, Bm * s.D)) != PPO_OK) return r;
+    if ((r = c->alloc_n(&h.act, Bm * (s.NH > 0 ? s.NH : 1))) != PPO_OK) return r;
+    if ((r = c->alloc_n(&h.actc, Bm * (s.G > 0 ? s.G : 1))) != PPO_OK) return r;
+    if ((r = c->alloc_n(&h.logp, Bm)) != PPO_OK) return r;
+    if ((r = c->alloc_n(&h.val, Bm)) != PPO_OK) return r;
+    if ((r = c->alloc_n(&h.rew, Bm)) != PPO_OK) return r;
+    if ((r = c->alloc_n(&h.done, Bm)) != PPO_OK) return r;
+    if ((r = c->alloc_n(&h.boot, Bm)) != PPO_OK) return r;
+    for (cudaEvent_t* e : {&h.gae_in, &h.rest, &h.freed})
+      PPO_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
   }
   const int64_t nstats = (int64_t)epochs * minibatches * 6;
   if (h_stats && nstats > c->st_stats_cap) {
+    TRY(host_wait_all(c));   // earlier updates may still write the old buffer
     if ((r = c->alloc_n(&c->st_stats, nstats)) != PPO_OK) return r;
     c->st_stats_cap = nstats;
   }
-  if (!c->cst) {
-    PPO_CUDA(cudaStreamCreateWithFlags(&c->cst, cudaStreamNonBlocking));
-    PPO_CUDA(cudaEventCreateWithFlags(&c->cev, cudaEventDisableTiming));
-  }
-  auto h2d = [&](void* d, const void* h, size_t bytes, cudaStream_t s2) {
-    return cudaMemcpyAsync(d, h, bytes, cudaMemcpyHostToDevice, s2);
+  TRY(check_update_args(c, h.obs, h.act, h.actc, h.logp, h.val, h.rew, h.done, h.boot, T, N,
+                        epochs, minibatches, h_stats ? c->st_stats : nullptr));
+  // the context's buffers are ordered by one stream: a switch waits first
+  if (c->hs_inflight > 0 && st != c->hs_stream) TRY(host_wait_all(c));
+  // the call two before this one used this slot: wait until its update and
+  // stats copy-back are done, so that on return its results are on the host
+  // and its host buffers are no longer read
+  if (h.used) PPO_CUDA(cudaEventSynchronize(h.freed));
+  auto h2d = [&](void* d, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(d, src, bytes, cudaMemcpyHostToDevice, c->cst);
   };
-  // GAE's inputs on `stream`; observations, actions and logp_old on a second
-  // stream, copied while GAE and the permutation run (the previous call ended
-  // with a stream synchronisation, so nothing still reads these buffers)
-  PPO_CUDA(h2d(c->st_val, h_val, sizeof(float) * B, st));
-  PPO_CUDA(h2d(c->st_rew, h_rew, sizeof(float) * B, st));
-  PPO_CUDA(h2d(c->st_done, h_done, sizeof(float) * B, st));
-  PPO_CUDA(h2d(c->st_boot, h_boot, sizeof(float) * N, st));
-  PPO_CUDA(h2d(c->st_obs, h_obs, sizeof(float) * B * s.D, c->cst));
-  if (s.NH > 0) PPO_CUDA(h2d(c->st_act, h_act, sizeof(int32_t) * B * s.NH, c->cst));
-  if (s.G > 0) PPO_CUDA(h2d(c->st_actc, h_actc, sizeof(float) * B * s.G, c->cst));
-  PPO_CUDA(h2d(c->st_logp, h_logp_old, sizeof(float) * B, c->cst));
-  PPO_CUDA(cudaEventRecord(c->cev, c->cst));
-  TRY(run_update(c, c->st_obs, c->st_act, c->st_actc, c->st_logp, c->st_val, c->st_rew,
-                 c->st_done, c->st_boot, T, N, epochs, minibatches, gamma, lambda, lr, seed,
-                 h_stats ? c->st_stats : nullptr, st, c->cev));
+  // GAE's inputs first: part 1 (GAE, moments, permutations) starts as soon
+  // as they are in, while observations, actions and old log-probs follow
+  PPO_CUDA(h2d(h.val, h_val, sizeof(float) * B));
+  PPO_CUDA(h2d(h.rew, h_rew, sizeof(float) * B));
+  PPO_CUDA(h2d(h.done, h_done, sizeof(float) * B));
+  PPO_CUDA(h2d(h.boot, h_boot, sizeof(float) * N));
+  PPO_CUDA(cudaEventRecord(h.gae_in, c->cst));
+  PPO_CUDA(h2d(h.obs, h_obs, sizeof(float) * B * s.D));
+  if (s.NH > 0) PPO_CUDA(h2d(h.act, h_act, sizeof(int32_t) * B * s.NH));
+  if (s.G > 0) PPO_CUDA(h2d(h.actc, h_actc, sizeof(float) * B * s.G));
+  PPO_CUDA(h2d(h.logp, h_logp_old, sizeof(float) * B));
+  PPO_CUDA(cudaEventRecord(h.rest, c->cst));
+  PPO_CUDA(cudaStreamWaitEvent(st, h.gae_in, 0));
+  TRY(run_update(c, h.obs, h.act, h.actc, h.logp, h.val, h.rew, h.done, h.boot, T, N, epochs,
+                 minibatches, gamma, lambda, lr, seed, h_stats ? c->st_stats : nullptr, st,
+                 h.rest));
   if (h_stats)
     PPO_CUDA(cudaMemcpyAsync(h_stats, c->st_stats, sizeof(float) * nstats,
                              cudaMemcpyDeviceToHost, st));
-  PPO_CUDA(cudaStreamSynchronize(st));
+  PPO_CUDA(cudaEventRecord(h.freed, st));
+  h.used = true;
+  c->hs_next ^= 1;
+  c->hs_stream = st;
+  ++c->hs_inflight;
   return PPO_OK;
+}
+}  // namespace
+
+extern "C" {
+
+ppo_status ppo_update_host(ppo_ctx* c, const float* h_obs, const int32_t* h_act,
+                           const float* h_actc, const float* h_logp_old, const float* h_val,
+                           const float* h_rew, const float* h_done, const float* h_boot,
+                           int64_t T, int64_t N, int32_t epochs, int32_t minibatches,
+                           float gamma, float lambda, float lr, uint32_t seed, float* h_stats,
+                           cudaStream_t st) {
+  TRY(host_update(c, h_obs, h_act, h_actc, h_logp_old, h_val, h_rew, h_done, h_boot, T, N,
+                  epochs, minibatches, gamma, lambda, lr, seed, h_stats, st));
+  return host_wait_all(c);
+}
+
+ppo_status ppo_update_host_async(ppo_ctx* c, const float* h_obs, const int32_t* h_act,
+                                 const float* h_actc, const float* h_logp_old,
+                                 const float* h_val, const float* h_rew, const float* h_done,
+                                 const float* h_boot, int64_t T, int64_t N, int32_t epochs,
+                                 int32_t minibatches, float gamma, float lambda, float lr,
+                                 uint32_t seed, float* h_stats, cudaStream_t st) {
+  return host_update(c, h_obs, h_act, h_actc, h_logp_old, h_val, h_rew, h_done, h_boot, T, N,
+                     epochs, minibatches, gamma, lambda, lr, seed, h_stats, st);
+}
+
+ppo_status ppo_host_wait(ppo_ctx* c) {
+  if (!c) return PPO_ERR_INVALID;
+  return host_wait_all(c);
 }
 
 ppo_status ppo_set_collective(ppo_ctx* c, int32_t world, int32_t rank, ppo_collective_fn fn,
@@ -1775,7 +1877,7 @@ ppo_status ppo_set_collective(ppo_ctx* c, int32_t world, int32_t rank, ppo_colle
   c->rank = rank;
   c->coll = fn;
   c->coll_user = user;
-  c->gvalid = false;
+  c->invalidate_graphs();
   return PPO_OK;
 }
 
@@ -1784,14 +1886,14 @@ ppo_status ppo_set_step_trace(ppo_ctx* c, float* d_trace, int64_t max_steps) {
   if (d_trace && !al16(d_trace)) return PPO_ERR_ALIGN;
   c->trace = d_trace;
   c->trace_cap = max_steps;
-  c->gvalid = false;   // the cached update graph does not hold the copies
+  c->invalidate_graphs();   // the cached update graphs do not hold the copies
   return PPO_OK;
 }
 
 ppo_status ppo_set_wait_limit(ppo_ctx* c, uint64_t limit_ns) {
   if (!c) return PPO_ERR_INVALID;
   c->wait_ns = limit_ns == 0 ? kTimeoutNs : limit_ns;
-  c->gvalid = false;   // the limit is a kernel argument inside the cached graph
+  c->invalidate_graphs();   // the limit is a kernel argument inside the cached graphs
   return PPO_OK;
 }
 

@@ -119,3 +119,53 @@ def test_update_replays_graph_and_is_deterministic():
         finals.append(host(ctx.params).copy())
         ctx.close()
     assert np.array_equal(finals[0], finals[1])
+
+
+@pytest.mark.parametrize("prec", ["fp32", "bf16"])
+def test_pipelined_host_updates_match_synchronous(prec):
+    """ppo_update_host_async over five distinct pinned rollouts (both staging
+    slots used more than once) gives the same bits as five ppo_update_host
+    calls: parameters, optimizer step count and every call's statistics.  On
+    return from call k the statistics of call k-2 are already on the host."""
+    import torch
+    import policy_rl_gb300 as P
+    w = dataclasses.replace(synth.WORKLOADS["mario"].scaled(T=16, N=256, epochs=2,
+                                                            minibatches=4), precision=prec)
+    p0 = synth.init_params(w, seed=2)
+    E, M, K = w.epochs, w.minibatches, 5
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    rolls = []
+    for k in range(K):
+        ro = synth.rollout(w, seed=20 + k)
+        rolls.append([pin(x) for x in (ro.obs, ro.act_disc, ro.act_cont, ro.logp_old, ro.val,
+                                       ro.rew, ro.done, ro.boot)])
+    hp = (E, M, w.gamma, w.lam, w.lr)
+    stream = torch.cuda.Stream()
+    ref = P.Context(P.config_from_workload(w), p0)
+    ref_stats = []
+    for k in range(K):
+        st = torch.zeros(E * M, 6).pin_memory()
+        ref.update_host(*rolls[k], *hp, 100 + k, stats=st, stream=stream)
+        ref_stats.append(st.numpy().copy())
+    ref_p = host(ref.params).copy()
+    ref.close()
+    assert np.all(np.isfinite(ref_p)) and np.all(np.isfinite(np.stack(ref_stats)))
+
+    ctx = P.Context(P.config_from_workload(w), p0)
+    stats = [torch.full((E * M, 6), float("nan")).pin_memory() for _ in range(K)]
+    for k in range(K):
+        ctx.update_host_async(*rolls[k], *hp, 100 + k, stats=stats[k], stream=stream)
+        if k >= 2:
+            np.testing.assert_array_equal(stats[k - 2].numpy(), ref_stats[k - 2])
+    ctx.host_wait()
+    for k in range(K):
+        np.testing.assert_array_equal(stats[k].numpy(), ref_stats[k])
+    np.testing.assert_array_equal(host(ctx.params), ref_p)
+    assert ctx.step() == K * E * M
+    # a synchronous call after pipelined ones, and a call on another stream,
+    # continue the same trajectory
+    ctx.update_host_async(*rolls[0], *hp, 7, stream=torch.cuda.Stream())
+    ctx.update_host(*rolls[1], *hp, 8, stream=stream)
+    ctx.sync_status()
+    assert ctx.step() == (K + 2) * E * M
+    ctx.close()
