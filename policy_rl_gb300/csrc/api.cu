@@ -179,7 +179,10 @@ struct ppo_ctx {
       cudaGetLastError();
       return PPO_ERR_NOMEM;
     }
-    if (cudaMemset(q, 0, bytes) != cudaSuccess) {
+    // zeroed on the legacy stream, which the library's non-blocking streams
+    // do not wait for: finish it before any of them writes the buffer
+    if (cudaMemset(q, 0, bytes) != cudaSuccess ||
+        cudaStreamSynchronize(cudaStreamLegacy) != cudaSuccess) {
       cudaFree(q);
       return PPO_ERR_CUDA;
     }
@@ -1943,7 +1946,10 @@ struct ppo_rnn_ctx {
       cudaGetLastError();
       return PPO_ERR_NOMEM;
     }
-    if (cudaMemset(q, 0, bytes) != cudaSuccess) {
+    // zeroed on the legacy stream, which the library's non-blocking streams
+    // do not wait for: finish it before any of them writes the buffer
+    if (cudaMemset(q, 0, bytes) != cudaSuccess ||
+        cudaStreamSynchronize(cudaStreamLegacy) != cudaSuccess) {
       cudaFree(q);
       return PPO_ERR_CUDA;
     }

@@ -47,36 +47,57 @@ using namespace tc;
 
 constexpr int kThreads = 192;
 
+// the bias of a forward product launched without one
+__device__ __align__(16) float g_zero_bias[kColsumCap];
+
 // Epilogue warps: 16 for the element-wise epilogues of 256-column tiles (four
-// per TMEM lane quarter, each taking 64 of the tile's columns -- one TMA store
-// block; measured faster than 8), 8 otherwise (two per lane quarter).  The
-// per-row loss epilogue runs two groups of four warps on alternate tiles (one
-// accumulator each; its 168 registers per thread leave no room for more).
+// per TMEM lane quarter, each taking 64 of the tile's columns; measured faster
+// than 8), 8 otherwise (two per lane quarter).  The per-row loss epilogue runs
+// two groups of four warps on alternate tiles, one accumulator each (a third
+// group would cap the registers at 128 per thread and spill: measured slower).
 template <int BN, int EPI>
-__host__ __device__ constexpr int epi_warps() { return (EPI != EPI_LOSS && BN >= 256) ? 16 : 8; }
+__host__ __device__ constexpr int epi_warps() { return BN >= 256 && EPI != EPI_LOSS ? 16 : 8; }
+// TMEM accumulators: one per loss group, otherwise a double buffer
+template <int BN, int EPI>
+__host__ __device__ constexpr int n_acc() { return EPI == EPI_LOSS ? epi_warps<BN, EPI>() / 4 : 2; }
 template <int BN, int EPI>
 __host__ __device__ constexpr int gemm_threads() { return 2 * kWarp + kWarp * epi_warps<BN, EPI>(); }
 
+template <int EPI>
+__host__ __device__ constexpr bool is_dact() { return EPI == EPI_DACT || EPI == EPI_DACT_K1; }
+
 template <int BN, int EPI>
 struct Cfg {
-  // backward-data kernels keep two TMA-loaded activation tiles (aux), which
-  // also stage their output; forward kernels stage their output per warp
-  static constexpr int AUX_SLOT = EPI == EPI_DACT ? BM * BN * 2 : 0;
-  static constexpr int NAUX = 2;
-  // per-warp output staging: 64-column blocks of 32 rows (4 KB); a warp takes
-  // 64 columns of a 256-column tile (16 epilogue warps) or half a 128-column one
-  static constexpr int STG_WARP = EPI == EPI_BIAS_ACT ? 4096 : 0;
+  // backward-data kernels keep NAUX TMA-loaded activation tiles (aux), which
+  // also stage their output (four when the product has one k-tile, so that
+  // the loads run several tiles ahead of the epilogue); forward kernels stage
+  // their output per warp
+  static constexpr int AUX_SLOT = is_dact<EPI>() ? BM * BN * 2 : 0;
+  static constexpr int NAUX = EPI == EPI_DACT_K1 ? 4 : 2;
+  // per-warp output staging of the forward kernels: one 32-row x 32-column
+  // bf16 chunk (2 KB, 64-byte swizzle), stored by TMA before the next chunk
+  // is written, so that the ring gets the shared memory: 4 stages of 48 KB
+  // at BN = 256
+  static constexpr int STG_WARP = EPI == EPI_BIAS_ACT ? 2048 : 0;
   static constexpr int S = EPI == EPI_DACT ? 4
-                         : EPI == EPI_BIAS_ACT ? (BN >= 256 ? 3 : 5)
+                         : EPI == EPI_DACT_K1 ? 2
+                         : EPI == EPI_BIAS_ACT ? (BN >= 256 ? 4 : 6)
                                                : (BN >= 128 ? 6 : 8);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
-  static constexpr int CTRL = 512;
+  static constexpr int ACC_COLS = n_acc<BN, EPI>() * BN;
+  static constexpr int TMEM_COLS = ACC_COLS <= 32 ? 32 : (ACC_COLS <= 64 ? 64 : (ACC_COLS <= 128 ? 128 : (ACC_COLS <= 256 ? 256 : 512)));
+  // barriers, TMEM slot, flags (<= 244 bytes for S <= 8)
+  static constexpr int CTRL = EPI == EPI_LOSS ? 512 : 256;
+  // column sums, loss partials (one row per group and lane quarter) and the
+  // staged bias: not in the forward kernels (their bias is read through the
+  // read-only cache)
+  static constexpr size_t EXTRA =
+      EPI == EPI_BIAS_ACT ? 0 : 4 * kColsumCap * 4 + 12 * kLossPartials * 4 + kColsumCap * 4;
   static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + NAUX * (size_t)AUX_SLOT +
-                                 epi_warps<BN, EPI>() * (size_t)STG_WARP + CTRL + 4 * kColsumCap * 4 +
-                                 8 * kLossPartials * 4 + kColsumCap * 4;
+                                 epi_warps<BN, EPI>() * (size_t)STG_WARP + CTRL + EXTRA;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 
@@ -99,13 +120,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint8_t* stgs = auxs + C::NAUX * (size_t)C::AUX_SLOT;  // [EW warps][STG_WARP] (BIAS_ACT only)
   uint8_t* ctrl = stgs + EW * (size_t)C::STG_WARP;
   Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), S};
-  uint64_t* xbar = reinterpret_cast<uint64_t*>(ctrl) + Ctrl::count(S);  // aux full[2], empty[2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 4);
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(ctrl) + Ctrl::count(S);  // aux full[NAUX], empty[NAUX]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 2 * C::NAUX);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);  // issued, consumed, aux issued
   float* cs = reinterpret_cast<float*>(ctrl + C::CTRL);                      // [4][kColsumCap]
-  float* lp = cs + 4 * kColsumCap;                                           // [8][kLossPartials]
-  float* bias_s = lp + 8 * kLossPartials;                                    // [kColsumCap]
+  float* lp = cs + 4 * kColsumCap;                                           // [12][kLossPartials]
+  float* bias_s = lp + 12 * kLossPartials;                                   // [kColsumCap]
 
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   auto sA = [&](int s) { return base + (uint32_t)(s * C::STAGE); };
@@ -116,14 +137,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(cb.full(s), 1);
       mbar_init(cb.empty(s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < n_acc<BN, EPI>(); ++a) {
       mbar_init(cb.tfull(a), 1);
       mbar_init(cb.tempty(a), (EPI == EPI_LOSS ? 4 : EW) * kWarp);
     }
     mbar_init(cb.drain(), 1);
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < C::NAUX; ++a) {
       mbar_init(smem_u32(&xbar[a]), 1);
-      mbar_init(smem_u32(&xbar[2 + a]), EW * kWarp);
+      mbar_init(smem_u32(&xbar[C::NAUX + a]), EW * kWarp);
     }
     *abort_flag = 0;
     cnt[0] = 0;
@@ -132,12 +153,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     fence_mbar_init();
   }
   if (EPI != EPI_BIAS_ACT)
-    for (int i = threadIdx.x; i < 4 * kColsumCap + 8 * kLossPartials; i += NT) cs[i] = 0.f;
+    for (int i = threadIdx.x; i < 4 * kColsumCap + 12 * kLossPartials; i += NT) cs[i] = 0.f;
   if (warp == 1) tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (EPI == EPI_DACT) prefetch_tmap(&tmX);
+    if (is_dact<EPI>()) prefetch_tmap(&tmX);
     if (EPI != EPI_LOSS) prefetch_tmap(&tmO);
   }
   tc_fence_before();
@@ -148,7 +169,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int total = p.tiles_m * p.tiles_n;
   pdl_wait();      // inputs are written by the previous kernel of the chain
   pdl_trigger();
-  if (EPI != EPI_DACT) {  // the bias, read by every epilogue thread, staged once
+  if (EPI == EPI_LOSS) {  // the bias, read by every epilogue thread, staged once
     for (int i = threadIdx.x; i < p.N; i += NT) bias_s[i] = p.bias ? p.bias[i] : 0.f;
     __syncthreads();      // reached by every thread of the block (before the role split)
   }
@@ -160,11 +181,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t lt = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++lt) {
         const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
-        if constexpr (EPI == EPI_DACT) {
-          // this tile's activation operand, one slot of two, ahead of its k-loop
+        // the streamed operands of this CTA's next tile (activation rows, and
+        // the act' tile) into L2 one tile ahead, so that the ring's loads wait
+        // for L2 rather than DRAM (not for the loss kernel, whose per-row
+        // epilogue sets its pace)
+        if (EPI != EPI_LOSS && tile + (int)gridDim.x < total) {
+          const int nt = tile + (int)gridDim.x;
+          const int tmn = nt / p.tiles_n;
+          for (int kt = 0; kt < p.k_tiles; ++kt) tma_prefetch_2d(&tmA, kt * BK, tmn * BM);
+          if constexpr (is_dact<EPI>())
+            for (int j = 0; j < BN / 64; ++j)
+              tma_prefetch_2d(&tmX, (nt % p.tiles_n) * BN + 64 * j, tmn * BM);
+        }
+        if constexpr (is_dact<EPI>()) {
+          // this tile's activation operand, one slot of NAUX, ahead of its k-loop
           const int xs = lt % C::NAUX;
           const uint32_t xu = lt / C::NAUX;
-          if (!wait_bar(smem_u32(&xbar[2 + xs]), (xu & 1) ^ 1, g)) { ok = false; break; }
+          if (!wait_bar(smem_u32(&xbar[C::NAUX + xs]), (xu & 1) ^ 1, g)) { ok = false; break; }
           mbar_arrive_expect_tx(smem_u32(&xbar[xs]), C::AUX_SLOT);
           for (int j = 0; j < BN / 64; ++j)
             tma_load_2d(smem_u32(auxs) + (uint32_t)(xs * C::AUX_SLOT + j * 16384), &tmX,
@@ -197,8 +230,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t it = 0, tc = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const int acc = tc & 1;
-        const uint32_t use = tc >> 1;
+        const int acc = (int)(tc % n_acc<BN, EPI>());
+        const uint32_t use = tc / n_acc<BN, EPI>();
         if (!wait_bar(cb.tempty(acc), (use & 1) ^ 1, g)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * BN);
@@ -223,21 +256,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
   } else if constexpr (EPI == EPI_LOSS) {
-    // two groups of four warps (lane quarter q = warp % 4) take alternate
-    // tiles, i.e. the tiles of accumulator grp; column sums of group 1 sit
-    // 256 floats after group 0's in each quarter's slot
+    // groups of four warps (lane quarter q = warp % 4) take rotating tiles,
+    // i.e. the tiles of accumulator grp; column sums of group grp sit 64
+    // floats after those of group grp - 1 in each quarter's slot.  The row
+    // inputs are loaded before the wait for the accumulator.
     const int q = warp & 3;
     const int grp = (warp - 2) / 4;
     const HeadMasks hm = head_masks(p.shape);
     uint32_t i = 0;
-    for (int tile = blockIdx.x + grp * gridDim.x; tile < total; tile += 2 * gridDim.x, ++i) {
-      if (!wait_bar(cb.tfull(grp), i & 1, g)) break;
-      tc_fence_after();
+    constexpr int NA = n_acc<BN, EPI>();
+    for (int tile = blockIdx.x + grp * gridDim.x; tile < total; tile += NA * gridDim.x, ++i) {
       const int tm = tile / p.tiles_n;
       const int row = tm * BM + q * 32 + lane;
+      RowIn in;
+      load_row_in(in, row, row < p.M, p.shape, p.rows);
+      if (!wait_bar(cb.tfull(grp), i & 1, g)) break;
+      tc_fence_after();
       const uint32_t taddr = tmem + (uint32_t)(grp * BN) + ((uint32_t)(q * 32) << 16);
-      epi_loss_tile<BN>(taddr, row, row < p.M, p.shape, hm, p.lc, p.inv_mb, p.rows, p.logstd,
-                        bias_s, p.dz, p.lddz, cs + q * kColsumCap + grp * 256,
+      epi_loss_tile<BN>(taddr, row, row < p.M, p.shape, hm, p.lc, p.inv_mb, in, p.logstd,
+                        bias_s, p.dz, p.lddz, cs + q * kColsumCap + grp * 64,
                         lp + (grp * 4 + q) * kLossPartials, lane);
       tc_fence_before();
       mbar_arrive(cb.tempty(grp));
@@ -258,8 +295,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t taddr = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       constexpr int PART = BN / (EW / 4);   // columns of this warp: [h*PART, (h+1)*PART)
       static_assert(PART == 64, "one 64-column TMA store block per epilogue warp");
-      if constexpr (EPI == EPI_DACT) {
-        // tile tc uses aux slot tc & 1 (same tile order as the producer); the
+      if constexpr (is_dact<EPI>()) {
+        // tile tc uses aux slot tc % NAUX (same tile order as the producer); the
         // result overwrites the warp's rows of the slot and leaves by TMA
         const int xs = tc % C::NAUX;
         if (!wait_bar(smem_u32(&xbar[xs]), (tc / C::NAUX) & 1, g)) break;
@@ -270,34 +307,52 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         mbar_arrive(cb.tempty(acc));
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && tm * BM + q * 32 < p.M) {   // rows of the box exist
+        // With two slots the slot is released as soon as its stores have read
+        // it; with more, a tile releases the previous tile's slot, so that the
+        // warp does not wait for its own stores
+        constexpr bool kDefer = C::NAUX >= 3;
+        if (lane == 0) {
+          if (tm * BM + q * 32 < p.M) {   // rows of the box exist
 #pragma unroll
-          for (int b = 0; b < PART / 64; ++b) {
-            const int cb64 = (h * PART) / 64 + b;
-            tma_store_2d(&tmO, smem_u32(slot + cb64 * 16384 + q * 4096), tn * BN + cb64 * 64,
-                         tm * BM + q * 32);
+            for (int b = 0; b < PART / 64; ++b) {
+              const int cb64 = (h * PART) / 64 + b;
+              tma_store_2d(&tmO, smem_u32(slot + cb64 * 16384 + q * 4096), tn * BN + cb64 * 64,
+                           tm * BM + q * 32);
+            }
+            bulk_commit();
+            if constexpr (kDefer) bulk_wait_read1();
+            else bulk_wait_read0();
+          } else {
+            bulk_wait_read0();
           }
-          bulk_commit();
-          bulk_wait_read0();   // the slot is refilled by the producer after this
         }
         __syncwarp();
-        mbar_arrive(smem_u32(&xbar[2 + xs]));
+        if constexpr (kDefer) {
+          if (tc > 0) mbar_arrive(smem_u32(&xbar[C::NAUX + (tc - 1) % C::NAUX]));
+        } else {
+          mbar_arrive(smem_u32(&xbar[C::NAUX + xs]));
+        }
       } else {
+        // 32-column chunks through the warp's 2 KB staging buffer: each waits
+        // until the previous chunk's store has read the buffer
         uint8_t* stg = stgs + (warp - 2) * C::STG_WARP;
-        if (lane == 0) bulk_wait_read0();   // the previous tile's stores have left stg
-        __syncwarp();
-        epi_act_stage_tile<BN, EW>(taddr, tn * BN, h, p.act, bias_s, stg, lane);
+        const float* bias = (p.bias ? p.bias : g_zero_bias) + tn * BN;
+        const bool rows_exist = tm * BM + q * 32 < p.M;
+        tmem_chunks<PART / 32>(taddr, h * PART, [&](const uint32_t (&r)[32], int c0) {
+          float v[32];
+          act_bias_chunk_ldg(r, bias + c0, p.act, v);
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+          put_row_chunks_sw64(stg + lane * 64, lane, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && rows_exist) {
+            tma_store_2d(&tmO, smem_u32(stg), tn * BN + c0, tm * BM + q * 32);
+            bulk_commit();
+          }
+        });
         tc_fence_before();
         mbar_arrive(cb.tempty(acc));
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && tm * BM + q * 32 < p.M) {   // rows of the box exist
-#pragma unroll
-          for (int b = 0; b < PART / 64; ++b)
-            tma_store_2d(&tmO, smem_u32(stg + b * 4096), tn * BN + h * PART + b * 64,
-                         tm * BM + q * 32);
-          bulk_commit();
-        }
       }
       ++tc;
     }
@@ -311,7 +366,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t issued = cnt[0], consumed = cnt[1];
       for (uint32_t it = consumed; it < issued; ++it)
         drain_wait(cb.full(it % S), (it / S) & 1, p.timeout_ns);
-      const uint32_t xi = cnt[2];   // the last two activation-tile loads
+      const uint32_t xi = cnt[2];   // the last NAUX activation-tile loads
       for (uint32_t l = xi >= (uint32_t)C::NAUX ? xi - C::NAUX : 0; l < xi; ++l)
         drain_wait(smem_u32(&xbar[l % C::NAUX]), (l / C::NAUX) & 1, p.timeout_ns);
     }
@@ -333,11 +388,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       };
       for (int c = et; c < p.epi_n; c += EW * kWarp)
         p.colsum_part[(int64_t)blockIdx.x * p.epi_n + c] =
-            EPI == EPI_LOSS ? quad(cs, c) + quad(cs + 256, c) : quad(cs, c);
+            EPI == EPI_LOSS ? (quad(cs, c) + quad(cs + 64, c)) + quad(cs + 128, c) : quad(cs, c);
       if constexpr (EPI == EPI_LOSS) {
         if (et < kLossPartials) {
           float t = 0.f;
-          for (int k = 0; k < 8; ++k) t += lp[k * kLossPartials + et];
+          for (int k = 0; k < 12; ++k) t += lp[k * kLossPartials + et];
           p.loss_part[(int64_t)blockIdx.x * kLossPartials + et] = t;
         }
       }
@@ -356,6 +411,7 @@ constexpr int W_STAGE = W_A_BYTES + W_B_BYTES;
 constexpr int W_STG = 2 * 4096;   // per epilogue warp: two 32 x 32 fp32 store boxes
 constexpr size_t W_SMEM = 1024 + (size_t)WS * W_STAGE + 4 * W_STG + 512;
 constexpr int W_TMEM_COLS = 512;
+constexpr int kWPrefetch = WS;   // L2 prefetch distance of the streamed operands (k-tiles)
 
 __device__ __forceinline__ void decode_unit(const WParams& p, int u, int& reg, int& tm, int& tn,
                                             int& kt0, int& kt1, int& split) {
@@ -539,6 +595,12 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
         for (int kt = kt0; kt < kt1; ++kt) {
           const int s = it % WS;
           const uint32_t r = it / WS;
+          // both operands stream from DRAM: bring the rows kWPrefetch k-tiles
+          // beyond the ring into L2 before their loads are issued
+          if (kt + kWPrefetch < kt1) {
+            tma_prefetch_3d(tu, 0, (kt + kWPrefetch) * BK, tm * (BM / 64));
+            tma_prefetch_3d(tv, 0, (kt + kWPrefetch) * BK, tn * (bn / 64));
+          }
           if (!wait_bar(cb.empty(s), (r & 1) ^ 1, g)) { ok = false; break; }
           mbar_arrive_expect_tx(cb.full(s), bytes);
           // one 3-D box per operand: 64 rows x {2, bn/64} blocks of 64 features
@@ -672,7 +734,8 @@ cudaError_t get_encode() {
 
 // bf16 row-major [rows][cols] (row pitch ld elements), box = box_cols x box_rows
 cudaError_t make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
-                      int box_cols, int box_rows) {
+                      int box_cols, int box_rows,
+                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -680,9 +743,8 @@ cudaError_t make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t ro
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -730,12 +792,16 @@ cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream
   if (e != cudaSuccess) return e;
   tx = ta;
   to = ta;
-  if (EPI == EPI_DACT) {   // activation operand [M][N], 128-row x 64-column boxes
+  if (is_dact<EPI>()) {   // activation operand [M][N], 128-row x 64-column boxes
     e = make_tmap(&tx, p.aux, g.N, g.M, p.ldaux, 64, BM);
     if (e != cudaSuccess) return e;
   }
-  if (EPI != EPI_LOSS) {   // output [M][N] (row pitch ldo), 32-row x 64-column boxes
+  if (is_dact<EPI>()) {   // output [M][N] (row pitch ldo), 32-row x 64-column boxes
     e = make_tmap(&to, p.out, g.N, g.M, p.ldo, 64, 32);
+    if (e != cudaSuccess) return e;
+  }
+  if (EPI == EPI_BIAS_ACT) {   // output, 32-row x 32-column boxes, 64-byte swizzle
+    e = make_tmap(&to, p.out, g.N, g.M, p.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (e != cudaSuccess) return e;
   }
   p.M = g.M;
@@ -768,7 +834,7 @@ cudaError_t tc_prepare() {
   if (e != cudaSuccess) return e;
   const cudaError_t errs[] = {
       set_smem_attr<256, EPI_BIAS_ACT>(), set_smem_attr<128, EPI_BIAS_ACT>(),
-      set_smem_attr<128, EPI_DACT>(),
+      set_smem_attr<128, EPI_DACT>(),     set_smem_attr<128, EPI_DACT_K1>(),
       set_smem_attr<16, EPI_LOSS>(),      set_smem_attr<32, EPI_LOSS>(),
       cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)W_SMEM)};
@@ -824,9 +890,11 @@ cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ld
   p.epi_n = g.N;
   p.err = err;
   p.timeout_ns = timeout_ns;
-  // 128 columns, so that 4 stages and two activation tiles fit
-  if (g.N % 128 == 0) return launch_tc<128, EPI_DACT>(g, p, num_sms, st, grid_out);
-  return cudaErrorInvalidValue;
+  // 128 columns, so that 4 stages and two activation tiles fit (2 stages and
+  // four activation tiles for a single k-tile)
+  if (g.N % 128 != 0) return cudaErrorInvalidValue;
+  if (g.K <= BK) return launch_tc<128, EPI_DACT_K1>(g, p, num_sms, st, grid_out);
+  return launch_tc<128, EPI_DACT>(g, p, num_sms, st, grid_out);
 }
 
 cudaError_t tc_gemm_axpby(const GemmOperands& g, const __nv_bfloat16* aux, int ldaux, float alpha,
@@ -845,6 +913,7 @@ cudaError_t tc_gemm_axpby(const GemmOperands& g, const __nv_bfloat16* aux, int l
   p.epi_n = 0;   // no column sums
   p.err = err;
   p.timeout_ns = timeout_ns;
+  if (g.K <= BK) return launch_tc<128, EPI_DACT_K1>(g, p, num_sms, st, nullptr);
   return launch_tc<128, EPI_DACT>(g, p, num_sms, st, nullptr);
 }
 

@@ -519,11 +519,13 @@ mk_kernel(const __grid_constant__ MkMaps maps, const MkParams p) {
           float* cs_q = cs + q * kColsumCap;
           if (m->epi == EPI_LOSS) {
             if (h == 0) {
+              RowIn in;
+              load_row_in(in, row, rok, p.s, p.rows);
               if (m->BN == 16)
-                epi_loss_tile<16>(taddr, row, rok, p.s, head_masks(p.s), p.lc, p.inv_mb, p.rows, p.logstd, bias_s,
+                epi_loss_tile<16>(taddr, row, rok, p.s, head_masks(p.s), p.lc, p.inv_mb, in, p.logstd, bias_s,
                                   p.dz, p.lddz, cs_q, lp + q * kLossPartials, lane);
               else
-                epi_loss_tile<32>(taddr, row, rok, p.s, head_masks(p.s), p.lc, p.inv_mb, p.rows, p.logstd, bias_s,
+                epi_loss_tile<32>(taddr, row, rok, p.s, head_masks(p.s), p.lc, p.inv_mb, in, p.logstd, bias_s,
                                   p.dz, p.lddz, cs_q, lp + q * kLossPartials, lane);
             }
           } else if (m->epi == EPI_BIAS_ACT) {

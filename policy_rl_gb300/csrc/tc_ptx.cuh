@@ -52,6 +52,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// 2-D tiled prefetch of a box into L2 (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   (uint64_t)tmap),
+               "r"(x), "r"(y)
+               : "memory");
+}
+// 3-D tiled prefetch of a box into L2
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   (uint64_t)tmap),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 // 3-D tiled TMA load (x innermost), completing on an mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z,
                                             uint32_t bar) {

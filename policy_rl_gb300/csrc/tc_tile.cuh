@@ -16,7 +16,9 @@ constexpr int BM = 128;
 constexpr int BK = 64;          // 64 bf16 = 128 bytes = one swizzle atom row
 constexpr int kColsumCap = 512;
 
-enum Epi { EPI_BIAS_ACT = 0, EPI_DACT = 1, EPI_LOSS = 2 };
+// EPI_DACT_K1: EPI_DACT for products with a single k-tile (K <= 64), whose
+// pace is set by the activation tiles rather than by the operand ring
+enum Epi { EPI_BIAS_ACT = 0, EPI_DACT = 1, EPI_LOSS = 2, EPI_DACT_K1 = 3 };
 
 struct Guard {
   volatile int* abort;
@@ -70,11 +72,12 @@ struct Ctrl {
   int S;
   __device__ uint32_t full(int s) const { return smem_u32(&bars[s]); }
   __device__ uint32_t empty(int s) const { return smem_u32(&bars[S + s]); }
+  // up to three TMEM accumulators (full / empty each)
   __device__ uint32_t tfull(int a) const { return smem_u32(&bars[2 * S + a]); }
-  __device__ uint32_t tempty(int a) const { return smem_u32(&bars[2 * S + 2 + a]); }
-  __device__ uint32_t drain() const { return smem_u32(&bars[2 * S + 4]); }
-  __device__ uint32_t epi() const { return smem_u32(&bars[2 * S + 5]); }
-  __host__ __device__ static constexpr int count(int S) { return 2 * S + 6; }
+  __device__ uint32_t tempty(int a) const { return smem_u32(&bars[2 * S + 3 + a]); }
+  __device__ uint32_t drain() const { return smem_u32(&bars[2 * S + 6]); }
+  __device__ uint32_t epi() const { return smem_u32(&bars[2 * S + 7]); }
+  __host__ __device__ static constexpr int count(int S) { return 2 * S + 8; }
 };
 
 // Element-wise epilogue of one 128 x BN tile for one epilogue warp: TMEM lane
@@ -189,6 +192,37 @@ __device__ __forceinline__ void put_row_chunks(uint8_t* row, int r, int c16, con
     o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
     o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
     *reinterpret_cast<uint4*>(row + (((c16 + i) ^ (r & 7)) << 4)) = o;
+  }
+}
+
+// 32 values -> one 64-byte bf16 row of a 64-byte-swizzled 32-column tile
+// (16-byte chunk c of row r at (c ^ ((r >> 1) & 3)) * 16)
+__device__ __forceinline__ void put_row_chunks_sw64(uint8_t* row, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 o;
+    o.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    o.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    *reinterpret_cast<uint4*>(row + ((i ^ ((r >> 1) & 3)) << 4)) = o;
+  }
+}
+
+// act(acc + bias) for one 32-column chunk, the bias read as float4 through the
+// read-only cache (16-byte aligned); act 0 tanh, 1 ReLU, 2 identity
+__device__ __forceinline__ void act_bias_chunk_ldg(const uint32_t (&r)[32], const float* bias,
+                                                   int act, float (&v)[32]) {
+  const float4* b4 = reinterpret_cast<const float4*>(bias);
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) {
+    const float4 b = __ldg(b4 + j4);
+    const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = __uint_as_float(r[4 * j4 + e]) + bb[e];
+      v[4 * j4 + e] = act == 0 ? tanh_fast(x) : (act == 1 ? fmaxf(x, 0.f) : x);
+    }
   }
 }
 
@@ -432,6 +466,59 @@ __device__ __forceinline__ void row_loss_seg(const HeadMasks& hm, const LossCoef
 // Per-row loss of one 128 x BN head tile (BN = CP columns), thread = row:
 // z = TMEM accumulator + b3, then d(loss)/dz, the loss terms and dlogstd in
 // registers (all zero for rows >= M).
+// The per-row inputs of the loss that do not depend on the head product:
+// loaded before the epilogue waits for the accumulator, so that their latency
+// overlaps the wait.
+struct RowIn {
+  int av[PPO_MAX_HEADS];
+  float ac[4];
+  float logp_old, adv, ret;
+};
+
+__device__ __forceinline__ void load_row_in(RowIn& in, int row, bool rok, const NetShape& s,
+                                            const LossRows& rows) {
+#pragma unroll
+  for (int h = 0; h < PPO_MAX_HEADS; ++h) in.av[h] = rok && h < s.NH ? rows.act[(int64_t)row * s.NH + h] : 0;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) in.ac[g] = rok && g < s.G ? rows.actc[(int64_t)row * s.G + g] : 0.f;
+  in.logp_old = rok ? rows.logp_old[row] : 0.f;
+  in.adv = rok ? rows.adv[row] : 0.f;
+  in.ret = rok ? rows.ret[row] : 0.f;
+}
+
+// loss_row_regs with the row inputs already in registers
+template <int BN>
+__device__ __forceinline__ void loss_row_in(uint32_t taddr, bool rok, const NetShape& s,
+                                            const HeadMasks& hm, const LossCoef& lc, float inv_mb,
+                                            const RowIn& in, const float* logstd,
+                                            const float* bias_s, float (&dzr)[32], float (&t6)[6],
+                                            float (&dls)[4]) {
+  float v[32];
+  if constexpr (BN == 16) tmem_ld16(taddr, v);
+  else tmem_ld32(taddr, v);
+  float z[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    z[j] = (j < BN && j < s.C) ? v[j] + bias_s[j] : 0.f;
+    dzr[j] = 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < 6; ++k) t6[k] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) dls[k] = 0.f;
+  if (rok) {
+    uint32_t amask = 0u;
+    int off = 0;
+#pragma unroll
+    for (int h = 0; h < PPO_MAX_HEADS; ++h) {
+      if (h < s.NH) amask |= 1u << (off + in.av[h]);
+      off += h < s.NH ? s.head_n[h] : 0;
+    }
+    row_loss_seg<BN>(hm, lc, inv_mb, z, amask, in.ac, logstd, in.logp_old, in.adv, in.ret, dzr,
+                     t6, dls);
+  }
+}
+
 template <int BN>
 __device__ __forceinline__ void loss_row_regs(uint32_t taddr, int row, bool rok,
                                               const NetShape& s, const HeadMasks& hm,
@@ -493,12 +580,12 @@ __device__ __forceinline__ void loss_warp_reduce(float (&dzr)[32], const float (
 template <int BN>
 __device__ __forceinline__ void epi_loss_tile(uint32_t taddr, int row, bool rok, const NetShape& s,
                                               const HeadMasks& hm, const LossCoef& lc,
-                                              float inv_mb, const LossRows& rows,
+                                              float inv_mb, const RowIn& in,
                                               const float* logstd, const float* bias_s,
                                               __nv_bfloat16* dz, int lddz, float* cs_q,
                                               float* lp_q, int lane) {
   float dzr[32], t6[6], dls[4];
-  loss_row_regs<BN>(taddr, row, rok, s, hm, lc, inv_mb, rows, logstd, bias_s, dzr, t6, dls);
+  loss_row_in<BN>(taddr, rok, s, hm, lc, inv_mb, in, logstd, bias_s, dzr, t6, dls);
   if (rok) {
     uint4* d = reinterpret_cast<uint4*>(dz + (int64_t)row * lddz);
 #pragma unroll
