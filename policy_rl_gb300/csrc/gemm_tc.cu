@@ -73,13 +73,13 @@ struct Cfg {
   // the loads run several tiles ahead of the epilogue); forward kernels stage
   // their output per warp
   static constexpr int AUX_SLOT = is_dact<EPI>() ? BM * BN * 2 : 0;
-  static constexpr int NAUX = EPI == EPI_DACT_K1 ? 4 : 2;
+  static constexpr int NAUX = EPI == EPI_DACT_K1 ? 5 : 2;
   // per-warp output staging of the forward kernels: one 32-row x 32-column
   // bf16 chunk (2 KB, 64-byte swizzle), stored by TMA before the next chunk
   // is written, so that the ring gets the shared memory: 4 stages of 48 KB
   // at BN = 256
   static constexpr int STG_WARP = EPI == EPI_BIAS_ACT ? 2048 : 0;
-  static constexpr int S = EPI == EPI_DACT ? 4
+  static constexpr int S = EPI == EPI_DACT ? 5
                          : EPI == EPI_DACT_K1 ? 2
                          : EPI == EPI_BIAS_ACT ? (BN >= 256 ? 4 : 6)
                                                : (BN >= 128 ? 6 : 8);
@@ -91,10 +91,11 @@ struct Cfg {
   // barriers, TMEM slot, flags (<= 244 bytes for S <= 8)
   static constexpr int CTRL = EPI == EPI_LOSS ? 512 : 256;
   // column sums, loss partials (one row per group and lane quarter) and the
-  // staged bias: not in the forward kernels (their bias is read through the
-  // read-only cache)
+  // staged bias of the loss kernel (the forward kernels read their bias
+  // through the read-only cache; the backward-data kernels keep their column
+  // sums in registers)
   static constexpr size_t EXTRA =
-      EPI == EPI_BIAS_ACT ? 0 : 4 * kColsumCap * 4 + 12 * kLossPartials * 4 + kColsumCap * 4;
+      EPI == EPI_LOSS ? 4 * kColsumCap * 4 + 12 * kLossPartials * 4 + kColsumCap * 4 : 0;
   static constexpr size_t SMEM = 1024 + (size_t)S * STAGE + NAUX * (size_t)AUX_SLOT +
                                  epi_warps<BN, EPI>() * (size_t)STG_WARP + CTRL + EXTRA;
   static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -130,6 +131,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   auto sA = [&](int s) { return base + (uint32_t)(s * C::STAGE); };
+  // backward-data column sums of this epilogue warp (see epi_dact_smem_tile_r)
+  constexpr int NTC = kColsumCap / BN;
+  float csr[is_dact<EPI>() ? 2 * NTC : 1];
+#pragma unroll
+  for (int j = 0; j < (is_dact<EPI>() ? 2 * NTC : 1); ++j) csr[j] = 0.f;
   auto sB = [&](int s) { return base + (uint32_t)(s * C::STAGE + C::A_BYTES); };
 
   if (threadIdx.x == 0) {
@@ -152,7 +158,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     cnt[2] = 0;
     fence_mbar_init();
   }
-  if (EPI != EPI_BIAS_ACT)
+  if (EPI == EPI_LOSS)
     for (int i = threadIdx.x; i < 4 * kColsumCap + 12 * kLossPartials; i += NT) cs[i] = 0.f;
   if (warp == 1) tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
@@ -301,8 +307,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int xs = tc % C::NAUX;
         if (!wait_bar(smem_u32(&xbar[xs]), (tc / C::NAUX) & 1, g)) break;
         uint8_t* slot = auxs + xs * C::AUX_SLOT;
-        epi_dact_smem_tile<BN, EW>(taddr, q * 32 + lane, rok, tn * BN, h, p.act, slot,
-                                   cs + q * kColsumCap, lane, p.alpha, p.beta);
+        epi_dact_smem_tile_r<BN, EW, NTC>(taddr, q * 32 + lane, rok, tn, h, p.act, slot, csr, lane,
+                                          p.alpha, p.beta);
         tc_fence_before();
         mbar_arrive(cb.tempty(acc));
         fence_proxy_async_smem();
@@ -380,7 +386,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  if constexpr (EPI != EPI_BIAS_ACT) {
+  if constexpr (is_dact<EPI>()) {
+    // every stage has been released: the first ones take the per-quarter
+    // column sums [4][kColsumCap], summed in quarter order as in the loss
+    static_assert((size_t)C::S * C::STAGE >= 4 * kColsumCap * 4, "column-sum scratch");
+    float* scr = reinterpret_cast<float*>(gbase);
+    if (warp >= 2) {
+      const int q = warp & 3, h = (warp - 2) / 4;
+#pragma unroll
+      for (int t = 0; t < NTC; ++t)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2)
+          scr[q * kColsumCap + t * BN + h * 64 + k2 * 32 + lane] = csr[2 * t + k2];
+    }
+    __syncthreads();
+    if (warp >= 2) {
+      const int et = threadIdx.x - 2 * kWarp;
+      for (int c = et; c < p.epi_n; c += EW * kWarp)
+        p.colsum_part[(int64_t)blockIdx.x * p.epi_n + c] =
+            ((scr[c] + scr[kColsumCap + c]) + scr[2 * kColsumCap + c]) + scr[3 * kColsumCap + c];
+    }
+  }
+  if constexpr (EPI == EPI_LOSS) {
     if (warp >= 2) {
       const int et = threadIdx.x - 2 * kWarp;
       auto quad = [&](const float* b, int c) {
@@ -388,13 +415,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       };
       for (int c = et; c < p.epi_n; c += EW * kWarp)
         p.colsum_part[(int64_t)blockIdx.x * p.epi_n + c] =
-            EPI == EPI_LOSS ? (quad(cs, c) + quad(cs + 64, c)) + quad(cs + 128, c) : quad(cs, c);
-      if constexpr (EPI == EPI_LOSS) {
-        if (et < kLossPartials) {
-          float t = 0.f;
-          for (int k = 0; k < 12; ++k) t += lp[k * kLossPartials + et];
-          p.loss_part[(int64_t)blockIdx.x * kLossPartials + et] = t;
-        }
+            (quad(cs, c) + quad(cs + 64, c)) + quad(cs + 128, c);
+      if (et < kLossPartials) {
+        float t = 0.f;
+        for (int k = 0; k < 12; ++k) t += lp[k * kLossPartials + et];
+        p.loss_part[(int64_t)blockIdx.x * kLossPartials + et] = t;
       }
     }
   }

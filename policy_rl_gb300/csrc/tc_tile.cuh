@@ -290,6 +290,53 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool 
   });
 }
 
+// The same with the column sums kept in registers: lane j of the warp holds
+// column tn * BN + h * 64 + 32 k + j of column tile tn in csr[2 tn + k] (NT
+// column tiles at most; the warp's part is 64 columns).
+template <int BN, int EW, int NT>
+__device__ __forceinline__ void epi_dact_smem_tile_r(uint32_t taddr, int rl, bool rok, int tn,
+                                                     int h, int act, uint8_t* aux,
+                                                     float (&csr)[NT * 2], int lane,
+                                                     float alpha = 0.f, float beta = 0.f) {
+  constexpr int PART = BN / (EW / 4);
+  tmem_chunks<PART / 32>(taddr, h * PART, [&](const uint32_t (&r)[32], int c0) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    uint8_t* blk = aux + (c0 / 64) * 16384 + rl * 128;
+    const int c16 = (c0 % 64) / 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a4 = *reinterpret_cast<const uint4*>(blk + (((c16 + i) ^ (rl & 7)) << 4));
+      const uint32_t w4[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        const float2 hv = unpack_bf16x2(w4[hh]);
+        const int j = 8 * i + 2 * hh;
+        if (act == 3) {
+          v[j] = rok ? alpha * hv.x + beta * v[j] : 0.f;
+          v[j + 1] = rok ? alpha * hv.y + beta * v[j + 1] : 0.f;
+        } else {
+          const float d0 = act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
+          const float d1 = act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
+          v[j] = rok ? v[j] * d0 : 0.f;
+          v[j + 1] = rok ? v[j + 1] * d1 : 0.f;
+        }
+      }
+    }
+    put_row_chunks(blk, rl, c16, v);
+    if (act != 3) {
+      const float colsum = warp_reduce_scatter32(v);
+      const int kk = (c0 - h * PART) >> 5;   // chunk of the warp's 64 columns
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2)
+          if (tn == t && kk == k2) csr[2 * t + k2] += colsum;
+    }
+  });
+}
+
 // Forward epilogue, out = act(acc + bias), for one epilogue warp: its 32 rows
 // (lane = row) and columns [h*PART, (h+1)*PART) of the tile go to the warp's
 // staging buffer stg as PART/64 blocks of 32 rows x 128 bytes in the 128-byte
