@@ -56,7 +56,7 @@ __device__ __align__(16) float g_zero_bias[kColsumCap];
 // two groups of four warps on alternate tiles, one accumulator each (a third
 // group would cap the registers at 128 per thread and spill: measured slower).
 template <int BN, int EPI>
-__host__ __device__ constexpr int epi_warps() { return BN >= 256 && EPI != EPI_LOSS ? 16 : 8; }
+__host__ __device__ constexpr int epi_warps() { return BN >= 256 && EPI == EPI_BIAS_ACT ? 16 : 8; }
 // TMEM accumulators: one per loss group, otherwise a double buffer
 template <int BN, int EPI>
 __host__ __device__ constexpr int n_acc() { return EPI == EPI_LOSS ? epi_warps<BN, EPI>() / 4 : 2; }
@@ -73,13 +73,17 @@ struct Cfg {
   // the loads run several tiles ahead of the epilogue); forward kernels stage
   // their output per warp
   static constexpr int AUX_SLOT = is_dact<EPI>() ? BM * BN * 2 : 0;
-  static constexpr int NAUX = EPI == EPI_DACT_K1 ? 5 : 2;
+  // 256-column backward data: one activation tile, each epilogue warp
+  // reloading its own rows of it for its next tile as soon as its stores have
+  // read them (the operand ring takes the rest of the shared memory)
+  static constexpr bool WARP_AUX = EPI == EPI_DACT && BN >= 256;
+  static constexpr int NAUX = EPI == EPI_DACT_K1 ? 5 : (WARP_AUX ? 1 : 2);
   // per-warp output staging of the forward kernels: one 32-row x 32-column
   // bf16 chunk (2 KB, 64-byte swizzle), stored by TMA before the next chunk
   // is written, so that the ring gets the shared memory: 4 stages of 48 KB
   // at BN = 256
   static constexpr int STG_WARP = EPI == EPI_BIAS_ACT ? 2048 : 0;
-  static constexpr int S = EPI == EPI_DACT ? 5
+  static constexpr int S = EPI == EPI_DACT ? (BN >= 256 ? 3 : 5)
                          : EPI == EPI_DACT_K1 ? 2
                          : EPI == EPI_BIAS_ACT ? (BN >= 256 ? 4 : 6)
                                                : (BN >= 128 ? 6 : 8);
@@ -121,8 +125,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint8_t* stgs = auxs + C::NAUX * (size_t)C::AUX_SLOT;  // [EW warps][STG_WARP] (BIAS_ACT only)
   uint8_t* ctrl = stgs + EW * (size_t)C::STG_WARP;
   Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), S};
-  uint64_t* xbar = reinterpret_cast<uint64_t*>(ctrl) + Ctrl::count(S);  // aux full[NAUX], empty[NAUX]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 2 * C::NAUX);
+  // aux full[NAUX], empty[NAUX]; with WARP_AUX one barrier per epilogue warp
+  constexpr int XB = C::WARP_AUX ? EW : 2 * C::NAUX;
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(ctrl) + Ctrl::count(S);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + XB);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);  // issued, consumed, aux issued
   float* cs = reinterpret_cast<float*>(ctrl + C::CTRL);                      // [4][kColsumCap]
@@ -133,9 +139,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   auto sA = [&](int s) { return base + (uint32_t)(s * C::STAGE); };
   // backward-data column sums of this epilogue warp (see epi_dact_smem_tile_r)
   constexpr int NTC = kColsumCap / BN;
-  float csr[is_dact<EPI>() ? 2 * NTC : 1];
+  constexpr int PART = BN / (EW / 4);   // columns of an epilogue warp
+  constexpr int CPW = PART / 32;
+  static_assert(EPI == EPI_LOSS || PART % 64 == 0, "whole 64-column blocks per epilogue warp");
+  float csr[is_dact<EPI>() ? NTC * CPW : 1];
 #pragma unroll
-  for (int j = 0; j < (is_dact<EPI>() ? 2 * NTC : 1); ++j) csr[j] = 0.f;
+  for (int j = 0; j < (is_dact<EPI>() ? NTC * CPW : 1); ++j) csr[j] = 0.f;
   auto sB = [&](int s) { return base + (uint32_t)(s * C::STAGE + C::A_BYTES); };
 
   if (threadIdx.x == 0) {
@@ -148,9 +157,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(cb.tempty(a), (EPI == EPI_LOSS ? 4 : EW) * kWarp);
     }
     mbar_init(cb.drain(), 1);
-    for (int a = 0; a < C::NAUX; ++a) {
-      mbar_init(smem_u32(&xbar[a]), 1);
-      mbar_init(smem_u32(&xbar[C::NAUX + a]), EW * kWarp);
+    if constexpr (C::WARP_AUX) {
+      for (int w = 0; w < EW; ++w) mbar_init(smem_u32(&xbar[w]), 1);
+    } else {
+      for (int a = 0; a < C::NAUX; ++a) {
+        mbar_init(smem_u32(&xbar[a]), 1);
+        mbar_init(smem_u32(&xbar[C::NAUX + a]), EW * kWarp);
+      }
     }
     *abort_flag = 0;
     cnt[0] = 0;
@@ -195,11 +208,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const int nt = tile + (int)gridDim.x;
           const int tmn = nt / p.tiles_n;
           for (int kt = 0; kt < p.k_tiles; ++kt) tma_prefetch_2d(&tmA, kt * BK, tmn * BM);
-          if constexpr (is_dact<EPI>())
+          if constexpr (is_dact<EPI>())   // (the per-warp map's boxes are 32 rows high)
             for (int j = 0; j < BN / 64; ++j)
-              tma_prefetch_2d(&tmX, (nt % p.tiles_n) * BN + 64 * j, tmn * BM);
+              for (int r0 = 0; r0 < BM; r0 += C::WARP_AUX ? 32 : BM)
+                tma_prefetch_2d(&tmX, (nt % p.tiles_n) * BN + 64 * j, tmn * BM + r0);
         }
-        if constexpr (is_dact<EPI>()) {
+        if constexpr (is_dact<EPI>() && !C::WARP_AUX) {
           // this tile's activation operand, one slot of NAUX, ahead of its k-loop
           const int xs = lt % C::NAUX;
           const uint32_t xu = lt / C::NAUX;
@@ -290,6 +304,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int q = warp & 3;
     const int h = (warp - 2) / 4;
     uint32_t tc = 0;
+    // WARP_AUX: this warp's rows of the activation tile, [PART/64 blocks of 32
+    // rows x 64 columns] at auxs + block * 16384 + q * 4096, loaded by lane 0
+    const uint32_t wb = smem_u32(&xbar[C::WARP_AUX ? warp - 2 : 0]);
+    uint32_t xi = 0;   // WARP_AUX loads issued by this warp
+    auto load_part = [&](int t) {
+      const int tm = t / p.tiles_n, tn = t % p.tiles_n;
+      mbar_arrive_expect_tx(wb, (uint32_t)(PART / 64) * 4096u);
+#pragma unroll
+      for (int b = 0; b < PART / 64; ++b) {
+        const int cb64 = (h * PART) / 64 + b;
+        tma_load_2d(smem_u32(auxs + cb64 * 16384 + q * 4096), &tmX, tn * BN + cb64 * 64,
+                    tm * BM + q * 32, wb);
+      }
+      ++xi;
+    };
+    if constexpr (C::WARP_AUX)
+      if (lane == 0 && (int)blockIdx.x < total) load_part(blockIdx.x);
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const int acc = tc & 1;
       const uint32_t use = tc >> 1;
@@ -299,9 +330,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int row = tm * BM + q * 32 + lane;
       const bool rok = row < p.M;
       const uint32_t taddr = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      constexpr int PART = BN / (EW / 4);   // columns of this warp: [h*PART, (h+1)*PART)
-      static_assert(PART == 64, "one 64-column TMA store block per epilogue warp");
-      if constexpr (is_dact<EPI>()) {
+      if constexpr (C::WARP_AUX) {
+        if (!wait_bar(wb, tc & 1, g)) break;
+        epi_dact_smem_tile_r<BN, EW, NTC>(taddr, q * 32 + lane, rok, tn, h, p.act, auxs, csr,
+                                          lane, p.alpha, p.beta);
+        tc_fence_before();
+        mbar_arrive(cb.tempty(acc));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (tm * BM + q * 32 < p.M) {   // rows of the box exist
+#pragma unroll
+            for (int b = 0; b < PART / 64; ++b) {
+              const int cb64 = (h * PART) / 64 + b;
+              tma_store_2d(&tmO, smem_u32(auxs + cb64 * 16384 + q * 4096), tn * BN + cb64 * 64,
+                           tm * BM + q * 32);
+            }
+            bulk_commit();
+          }
+          bulk_wait_read0();   // the rows are reloaded for the next tile
+          if (tile + (int)gridDim.x < total) load_part(tile + gridDim.x);
+        }
+        __syncwarp();
+      } else if constexpr (is_dact<EPI>()) {
         // tile tc uses aux slot tc % NAUX (same tile order as the producer); the
         // result overwrites the warp's rows of the slot and leaves by TMA
         const int xs = tc % C::NAUX;
@@ -362,6 +413,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       ++tc;
     }
+    if constexpr (C::WARP_AUX)   // a load issued for a tile this warp did not reach
+      if (lane == 0 && xi > tc) drain_wait(wb, (xi - 1) & 1, p.timeout_ns);
     if (lane == 0) bulk_wait0();   // this warp's stores are complete before the CTA exits
   }
 
@@ -396,8 +449,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
       for (int t = 0; t < NTC; ++t)
 #pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2)
-          scr[q * kColsumCap + t * BN + h * 64 + k2 * 32 + lane] = csr[2 * t + k2];
+        for (int k2 = 0; k2 < CPW; ++k2)
+          scr[q * kColsumCap + t * BN + h * PART + k2 * 32 + lane] = csr[CPW * t + k2];
     }
     __syncthreads();
     if (warp >= 2) {
@@ -817,8 +870,8 @@ cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream
   if (e != cudaSuccess) return e;
   tx = ta;
   to = ta;
-  if (is_dact<EPI>()) {   // activation operand [M][N], 128-row x 64-column boxes
-    e = make_tmap(&tx, p.aux, g.N, g.M, p.ldaux, 64, BM);
+  if (is_dact<EPI>()) {   // activation operand [M][N], 128-row (per-warp: 32-row) x 64-column boxes
+    e = make_tmap(&tx, p.aux, g.N, g.M, p.ldaux, 64, Cfg<BN, EPI>::WARP_AUX ? 32 : BM);
     if (e != cudaSuccess) return e;
   }
   if (is_dact<EPI>()) {   // output [M][N] (row pitch ldo), 32-row x 64-column boxes
@@ -860,6 +913,7 @@ cudaError_t tc_prepare() {
   const cudaError_t errs[] = {
       set_smem_attr<256, EPI_BIAS_ACT>(), set_smem_attr<128, EPI_BIAS_ACT>(),
       set_smem_attr<128, EPI_DACT>(),     set_smem_attr<128, EPI_DACT_K1>(),
+      set_smem_attr<256, EPI_DACT>(),
       set_smem_attr<16, EPI_LOSS>(),      set_smem_attr<32, EPI_LOSS>(),
       cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)W_SMEM)};
@@ -919,6 +973,7 @@ cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ld
   // four activation tiles for a single k-tile)
   if (g.N % 128 != 0) return cudaErrorInvalidValue;
   if (g.K <= BK) return launch_tc<128, EPI_DACT_K1>(g, p, num_sms, st, grid_out);
+  if (g.N % 256 == 0) return launch_tc<256, EPI_DACT>(g, p, num_sms, st, grid_out);
   return launch_tc<128, EPI_DACT>(g, p, num_sms, st, grid_out);
 }
 
@@ -939,6 +994,7 @@ cudaError_t tc_gemm_axpby(const GemmOperands& g, const __nv_bfloat16* aux, int l
   p.err = err;
   p.timeout_ns = timeout_ns;
   if (g.K <= BK) return launch_tc<128, EPI_DACT_K1>(g, p, num_sms, st, nullptr);
+  if (g.N % 256 == 0) return launch_tc<256, EPI_DACT>(g, p, num_sms, st, nullptr);
   return launch_tc<128, EPI_DACT>(g, p, num_sms, st, nullptr);
 }
 

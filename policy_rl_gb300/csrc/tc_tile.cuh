@@ -291,13 +291,14 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool 
 }
 
 // The same with the column sums kept in registers: lane j of the warp holds
-// column tn * BN + h * 64 + 32 k + j of column tile tn in csr[2 tn + k] (NT
-// column tiles at most; the warp's part is 64 columns).
+// column tn * BN + h * PART + 32 k + j of column tile tn in csr[CPW tn + k]
+// (NT column tiles at most; the warp's part is PART = 32 CPW columns).
 template <int BN, int EW, int NT>
 __device__ __forceinline__ void epi_dact_smem_tile_r(uint32_t taddr, int rl, bool rok, int tn,
                                                      int h, int act, uint8_t* aux,
-                                                     float (&csr)[NT * 2], int lane,
-                                                     float alpha = 0.f, float beta = 0.f) {
+                                                     float (&csr)[NT * (BN / (EW / 4) / 32)],
+                                                     int lane, float alpha = 0.f,
+                                                     float beta = 0.f) {
   constexpr int PART = BN / (EW / 4);
   tmem_chunks<PART / 32>(taddr, h * PART, [&](const uint32_t (&r)[32], int c0) {
     float v[32];
@@ -327,12 +328,13 @@ __device__ __forceinline__ void epi_dact_smem_tile_r(uint32_t taddr, int rl, boo
     put_row_chunks(blk, rl, c16, v);
     if (act != 3) {
       const float colsum = warp_reduce_scatter32(v);
-      const int kk = (c0 - h * PART) >> 5;   // chunk of the warp's 64 columns
+      constexpr int CPW = PART / 32;
+      const int kk = (c0 - h * PART) >> 5;   // chunk of the warp's PART columns
 #pragma unroll
       for (int t = 0; t < NT; ++t)
 #pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2)
-          if (tn == t && kk == k2) csr[2 * t + k2] += colsum;
+        for (int k2 = 0; k2 < CPW; ++k2)
+          if (tn == t && kk == k2) csr[CPW * t + k2] += colsum;
     }
   });
 }
