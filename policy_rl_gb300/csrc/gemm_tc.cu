@@ -481,15 +481,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // ---------------------------------------------------------------------------
 // Weight-gradient kernel: P[M][N] = sum_rows U[row][m] * V[row][n] over a
 // K-split of the minibatch rows; both operands MN-major in shared memory.
+// Output tiles are WBM = 256 rows (two 128-row MMAs sharing each B tile, two
+// TMEM accumulators) x bn <= 256 columns: per k-tile an SM takes in 64 KB for
+// 256 x 256 x 64 products.  A tile's lower half may lie beyond M (M a
+// multiple of 128): its A blocks are zero-filled and its MMAs and stores
+// skipped.
+constexpr int WBM = 256;
 constexpr int WBN = 256;
-constexpr int WS = 4;
-constexpr int W_A_BYTES = BM * BK * 2;   // 2 blocks of 64 features x 64 rows
+constexpr int WS = 3;
+constexpr int W_A_BYTES = WBM * BK * 2;  // 4 blocks of 64 features x 64 rows
 constexpr int W_B_BYTES = WBN * BK * 2;  // up to 4 blocks
 constexpr int W_STAGE = W_A_BYTES + W_B_BYTES;
 constexpr int W_STG = 2 * 4096;   // per epilogue warp: two 32 x 32 fp32 store boxes
 constexpr size_t W_SMEM = 1024 + (size_t)WS * W_STAGE + 4 * W_STG + 512;
+static_assert(W_SMEM <= 232448, "shared memory per CTA");
 constexpr int W_TMEM_COLS = 512;
-constexpr int kWPrefetch = WS;   // L2 prefetch distance of the streamed operands (k-tiles)
+constexpr int kWPrefetch = WS + 1;   // L2 prefetch distance of the streamed operands (k-tiles)
 
 __device__ __forceinline__ void decode_unit(const WParams& p, int u, int& reg, int& tm, int& tn,
                                             int& kt0, int& kt1, int& split) {
@@ -535,7 +542,7 @@ __device__ __forceinline__ float4 split_sum4_cg(const float* q, int64_t st, int 
 // is resident).  Each CTA first arrives on the counter of every output tile
 // it stored a split partial of; then, per unit, it waits (bounded) until all
 // splits of the tile have arrived and sums its share of the tile's rows --
-// split s of S takes rows [128 s / S, 128 (s + 1) / S) -- over the splits in
+// split s of S takes rows [256 s / S, 256 (s + 1) / S) below M -- over the splits in
 // split order, writing the final gradient entries and the sum of their
 // squares (per CTA, fixed order) for the clip norm.  The last CTA of a tile to
 // finish clears its counters for the next launch.  On a timeout (or an
@@ -581,12 +588,13 @@ __device__ __noinline__ void wgrad_fixup(const WParams& p, bool aborted) {
       __syncthreads();
       if (!s_ok) break;
       const WFinal& F = p.f[reg];
-      const int r0 = BM * split / R.splits, r1 = BM * (split + 1) / R.splits;
+      const int r0 = WBM * split / R.splits, r1 = WBM * (split + 1) / R.splits;
       const int q4 = R.bn / 4;   // four columns per work item
       const int n_it = (r1 - r0) * q4;
       const int64_t pst = (int64_t)R.M * R.N;
       for (int e = threadIdx.x; e < n_it; e += kThreads) {
-        const int m = tm * BM + r0 + e / q4, n = tn * R.bn + 4 * (e % q4);
+        const int m = tm * WBM + r0 + e / q4, n = tn * R.bn + 4 * (e % q4);
+        if (m >= R.M) break;   // (e grows with m)
         const float4 v = split_sum4_cg(R.part + (int64_t)m * R.N + n, pst, R.splits);
         const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -640,10 +648,8 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
       mbar_init(cb.full(s), 1);
       mbar_init(cb.empty(s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(cb.tfull(a), 1);
-      mbar_init(cb.tempty(a), 128);
-    }
+    mbar_init(cb.tfull(0), 1);
+    mbar_init(cb.tempty(0), 128);
     mbar_init(cb.drain(), 1);
     *abort_flag = 0;
     cnt[0] = 0;
@@ -669,20 +675,21 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
         const int bn = p.r[reg].bn;
         const CUtensorMap* tu = reg == 0 ? &tmU0 : (reg == 1 ? &tmU1 : &tmU2);
         const CUtensorMap* tv = reg == 0 ? &tmV0 : (reg == 1 ? &tmV1 : &tmV2);
-        const uint32_t bytes = (uint32_t)(BM + bn) * BK * 2;
+        const uint32_t bytes = (uint32_t)(WBM + bn) * BK * 2;
         for (int kt = kt0; kt < kt1; ++kt) {
           const int s = it % WS;
           const uint32_t r = it / WS;
           // both operands stream from DRAM: bring the rows kWPrefetch k-tiles
           // beyond the ring into L2 before their loads are issued
           if (kt + kWPrefetch < kt1) {
-            tma_prefetch_3d(tu, 0, (kt + kWPrefetch) * BK, tm * (BM / 64));
+            tma_prefetch_3d(tu, 0, (kt + kWPrefetch) * BK, tm * (WBM / 64));
             tma_prefetch_3d(tv, 0, (kt + kWPrefetch) * BK, tn * (bn / 64));
           }
           if (!wait_bar(cb.empty(s), (r & 1) ^ 1, g)) { ok = false; break; }
           mbar_arrive_expect_tx(cb.full(s), bytes);
-          // one 3-D box per operand: 64 rows x {2, bn/64} blocks of 64 features
-          tma_load_3d(sA(s), tu, 0, kt * BK, tm * (BM / 64), cb.full(s));
+          // one 3-D box per operand: 64 rows x {4, bn/64} blocks of 64 features
+          // (blocks beyond M read as zeros)
+          tma_load_3d(sA(s), tu, 0, kt * BK, tm * (WBM / 64), cb.full(s));
           tma_load_3d(sB(s), tv, 0, kt * BK, tn * (bn / 64), cb.full(s));
           ++it;
           cnt[0] = it;
@@ -702,12 +709,13 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
         int reg, tm, tn, kt0, kt1, split;
         decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
-        const uint32_t idesc = idesc_bf16(BM, p.r[reg].bn, true, true);
-        const int acc = tc & 1;
-        const uint32_t use = tc >> 1;
-        if (!wait_bar(cb.tempty(acc), (use & 1) ^ 1, g)) break;
+        const int bn = p.r[reg].bn;
+        const uint32_t idesc = idesc_bf16(BM, bn, true, true);
+        const bool lower = tm * WBM + BM < p.r[reg].M;   // the tile's rows 128..255 exist
+        // one unit at a time: the accumulators [rows 0..127 | rows 128..255]
+        // take 2 bn <= 512 TMEM columns
+        if (!wait_bar(cb.tempty(0), (tc & 1) ^ 1, g)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(acc * WBN);
         for (int kt = kt0; kt < kt1; ++kt) {
           const int s = it % WS;
           const uint32_t r = it / WS;
@@ -715,16 +723,20 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t da = sdesc_sw128(sA(s) + kk * 2048, p.mn_lbo, p.mn_sbo);
+            const uint32_t accf = (kt != kt0 || kk != 0) ? 1u : 0u;
             const uint64_t db = sdesc_sw128(sB(s) + kk * 2048, p.mn_lbo, p.mn_sbo);
-            tc_mma_bf16(d, da, db, idesc, (kt != kt0 || kk != 0) ? 1u : 0u);
+            tc_mma_bf16(tmem, sdesc_sw128(sA(s) + kk * 2048, p.mn_lbo, p.mn_sbo), db, idesc, accf);
+            if (lower)   // A's features 128..255: two 64-feature blocks further on
+              tc_mma_bf16(tmem + (uint32_t)bn,
+                          sdesc_sw128(sA(s) + 2 * (64 * BK * 2) + kk * 2048, p.mn_lbo, p.mn_sbo),
+                          db, idesc, accf);
           }
           tc_commit(cb.empty(s));
           ++it;
           cnt[1] = it;
         }
         if (!ok) break;
-        tc_commit(cb.tfull(acc));
+        tc_commit(cb.tfull(0));
         ++tc;
       }
     }
@@ -735,36 +747,38 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
       int reg, tm, tn, kt0, kt1, split;
       decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
       const WRegion& R = p.r[reg];
-      const int acc = tc & 1;
-      const uint32_t use = tc >> 1;
-      if (!wait_bar(cb.tfull(acc), use & 1, g)) break;
+      if (!wait_bar(cb.tfull(0), tc & 1, g)) break;
       tc_fence_after();
       // fp32 partial tile -> this split's slice of the partial buffer, 32
       // columns at a time through two 32 x 32 staging boxes per warp (128-byte
-      // swizzle: float4 c of row r at ((c ^ (r & 7)) * 16)) and TMA stores
+      // swizzle: float4 c of row r at ((c ^ (r & 7)) * 16)) and TMA stores;
+      // half hf = rows 128 hf .. 128 hf + 127 of the tile
       const CUtensorMap* tp = reg == 0 ? &tmP0 : (reg == 1 ? &tmP1 : &tmP2);
-      const uint32_t taddr = tmem + (uint32_t)(acc * WBN) + ((uint32_t)(q * 32) << 16);
       uint8_t* mystg = wstg + (warp - 2) * W_STG;
+      for (int hf = 0; hf < 2; ++hf) {
+        if (tm * WBM + hf * BM >= R.M) break;
+        const uint32_t taddr = tmem + (uint32_t)(hf * R.bn) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < R.bn; c0 += 32, ++sc) {
-        float v[32];
-        tmem_ld32(taddr + (uint32_t)c0, v);
-        uint8_t* buf = mystg + (sc & 1) * 4096;
-        if (lane == 0) bulk_wait_read1();   // the store that used buf last has read it
-        __syncwarp();
+        for (int c0 = 0; c0 < R.bn; c0 += 32, ++sc) {
+          float v[32];
+          tmem_ld32(taddr + (uint32_t)c0, v);
+          uint8_t* buf = mystg + (sc & 1) * 4096;
+          if (lane == 0) bulk_wait_read1();   // the store that used buf last has read it
+          __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
-              make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(tp, smem_u32(buf), tn * R.bn + c0, tm * BM + q * 32, split);
-          bulk_commit();
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(tp, smem_u32(buf), tn * R.bn + c0, tm * WBM + hf * BM + q * 32, split);
+            bulk_commit();
+          }
         }
       }
       tc_fence_before();
-      mbar_arrive(cb.tempty(acc));
+      mbar_arrive(cb.tempty(0));
       ++tc;
     }
     if (lane == 0) {
@@ -1047,13 +1061,13 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
     if (G.M % BM != 0 || G.N % 64 != 0 || G.M > G.ldu || G.N > G.ldv) return cudaErrorInvalidValue;
     WRegion& R = p.r[r];
     R.bn = tc_wgrad_bn(G.N);
-    cudaError_t e = make_tmap_blocks(&tu[r], G.U, rows, G.ldu, G.M / 64, BK, BM / 64);
+    cudaError_t e = make_tmap_blocks(&tu[r], G.U, rows, G.ldu, G.M / 64, BK, WBM / 64);
     if (e != cudaSuccess) return e;
     e = make_tmap_blocks(&tv[r], G.V, rows, G.ldv, G.N / 64, BK, R.bn / 64);
     if (e != cudaSuccess) return e;
     R.M = G.M;
     R.N = G.N;
-    R.tiles_m = G.M / BM;
+    R.tiles_m = (G.M + WBM - 1) / WBM;
     R.tiles_n = G.N / R.bn;
     R.k_tiles = (rows + BK - 1) / BK;
     R.kt_per_split = G.kt_per_split;
@@ -1117,18 +1131,18 @@ void tc_wgrad_plan(const int (*mn)[2], int nreg, int64_t rows, int num_sms, int 
   double total = 0;
   for (int i = 0; i < nreg; ++i) {
     const int bn = tc_wgrad_bn(mn[i][1]);
-    total += (double)(mn[i][0] / BM) * (mn[i][1] / bn) * (BM + bn) * k_tiles;
+    total += (double)((mn[i][0] + WBM - 1) / WBM) * (mn[i][1] / bn) * (WBM + bn) * k_tiles;
   }
   for (int64_t q = (int64_t)std::ceil(total / num_sms);; q += (q + 15) / 16) {
     int64_t units = 0;
     for (int i = 0; i < nreg; ++i) {
       const int bn = tc_wgrad_bn(mn[i][1]);
-      int64_t kp = q / (BM + bn);
+      int64_t kp = q / (WBM + bn);
       if (kp < 4) kp = 4;
       if ((k_tiles + kp - 1) / kp > max_split) kp = (k_tiles + max_split - 1) / max_split;
       if (kp > k_tiles) kp = k_tiles;
       kt[i] = (int)kp;
-      units += (int64_t)(mn[i][0] / BM) * (mn[i][1] / bn) * ((k_tiles + kp - 1) / kp);
+      units += (int64_t)((mn[i][0] + WBM - 1) / WBM) * (mn[i][1] / bn) * ((k_tiles + kp - 1) / kp);
     }
     if (units <= num_sms || q >= 1024 * k_tiles) return;
   }
