@@ -41,6 +41,9 @@ struct TcParams {
   int* err;
   uint64_t timeout_ns;
   float alpha, beta;   // act 3 of the aux-tile epilogue: out = alpha aux + beta acc
+  int layout9222;      // loss epilogue: the 9-2-2-2 head layout (compile-time masks)
+  const __nv_bfloat16* a_rows;   // A [M][lda] (the producer's L2 prefetch of whole rows)
+  int lda;
 };
 
 // Gradient assembly from the split-K and per-CTA partials (optim.cu, and the

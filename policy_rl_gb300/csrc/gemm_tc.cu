@@ -91,7 +91,7 @@ struct Cfg {
   static constexpr int S = EPI == EPI_DACT ? (BN >= 256 ? 3 : 5)
                          : EPI == EPI_DACT_K1 ? 2
                          : EPI == EPI_BIAS_ACT ? (BN >= 256 ? 4 : 6)
-                                               : (BN >= 128 ? 6 : 8);
+                                               : 10;   // loss: H2 rows stream through 10 stages
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
@@ -111,6 +111,35 @@ struct Cfg {
 };
 
 
+
+// The loss epilogue's tile loop: groups of four warps (lane quarter q =
+// warp % 4) take rotating tiles, i.e. the tiles of accumulator grp; column
+// sums of group grp sit 64 floats after those of group grp - 1 in each
+// quarter's slot.  The row inputs are loaded before the wait for the
+// accumulator.  Inlined once with run-time head masks and once with the
+// compile-time masks of the common layout.
+template <int BN, int NA>
+__device__ __forceinline__ void loss_epilogue(const TcParams& p, const HeadMasks hm, const Ctrl& cb,
+                                              const Guard& g, uint32_t tmem, int total, float* cs,
+                                              float* lp, const float* bias_s, int warp, int lane) {
+  const int q = warp & 3;
+  const int grp = (warp - 2) / 4;
+  uint32_t i = 0;
+  for (int tile = blockIdx.x + grp * gridDim.x; tile < total; tile += NA * gridDim.x, ++i) {
+    const int tm = tile / p.tiles_n;
+    const int row = tm * BM + q * 32 + lane;
+    RowIn in;
+    load_row_in(in, row, row < p.M, p.shape, p.rows);
+    if (!wait_bar(cb.tfull(grp), i & 1, g)) break;
+    tc_fence_after();
+    const uint32_t taddr = tmem + (uint32_t)(grp * BN) + ((uint32_t)(q * 32) << 16);
+    epi_loss_tile<BN>(taddr, row, row < p.M, p.shape, hm, p.lc, p.inv_mb, in, p.logstd, bias_s,
+                      p.dz, p.lddz, cs + q * kColsumCap + grp * 64,
+                      lp + (grp * 4 + q) * kLossPartials, lane);
+    tc_fence_before();
+    mbar_arrive(cb.tempty(grp));
+  }
+}
 
 // ---------------------------------------------------------------------------
 template <int BN, int EPI>
@@ -207,12 +236,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
         // the streamed operands of this CTA's next tile (activation rows, and
         // the act' tile) into L2 one tile ahead, so that the ring's loads wait
-        // for L2 rather than DRAM (not for the loss kernel, whose per-row
-        // epilogue sets its pace)
-        if (EPI != EPI_LOSS && tile + (int)gridDim.x < total) {
+        // for L2 rather than DRAM
+        if (tile + (int)gridDim.x < total) {
           const int nt = tile + (int)gridDim.x;
           const int tmn = nt / p.tiles_n;
-          for (int kt = 0; kt < p.k_tiles; ++kt) tma_prefetch_2d(&tmA, kt * BK, tmn * BM);
+          // A's rows are contiguous in memory: one linear prefetch of them (the
+          // k-tile boxes would visit the region in 128-byte column strips)
+          const int rows = min(BM, p.M - tmn * BM);
+          if (rows > 0)
+            bulk_prefetch_l2(p.a_rows + (int64_t)tmn * BM * p.lda,
+                             (uint32_t)rows * (uint32_t)p.lda * 2u);
           if constexpr (is_dact<EPI>())   // (the per-warp map's boxes are 32 rows high)
             for (int j = 0; j < BN / 64; ++j)
               for (int r0 = 0; r0 < BM; r0 += C::WARP_AUX ? 32 : BM)
@@ -285,25 +318,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // i.e. the tiles of accumulator grp; column sums of group grp sit 64
     // floats after those of group grp - 1 in each quarter's slot.  The row
     // inputs are loaded before the wait for the accumulator.
-    const int q = warp & 3;
-    const int grp = (warp - 2) / 4;
-    const HeadMasks hm = head_masks(p.shape);
-    uint32_t i = 0;
-    constexpr int NA = n_acc<BN, EPI>();
-    for (int tile = blockIdx.x + grp * gridDim.x; tile < total; tile += NA * gridDim.x, ++i) {
-      const int tm = tile / p.tiles_n;
-      const int row = tm * BM + q * 32 + lane;
-      RowIn in;
-      load_row_in(in, row, row < p.M, p.shape, p.rows);
-      if (!wait_bar(cb.tfull(grp), i & 1, g)) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem + (uint32_t)(grp * BN) + ((uint32_t)(q * 32) << 16);
-      epi_loss_tile<BN>(taddr, row, row < p.M, p.shape, hm, p.lc, p.inv_mb, in, p.logstd,
-                        bias_s, p.dz, p.lddz, cs + q * kColsumCap + grp * 64,
-                        lp + (grp * 4 + q) * kLossPartials, lane);
-      tc_fence_before();
-      mbar_arrive(cb.tempty(grp));
-    }
+    if (p.layout9222)
+      loss_epilogue<BN, n_acc<BN, EPI>()>(p, kMasks9222, cb, g, tmem, total, cs, lp, bias_s, warp,
+                                         lane);
+    else
+      loss_epilogue<BN, n_acc<BN, EPI>()>(p, head_masks(p.shape), cb, g, tmem, total, cs, lp,
+                                         bias_s, warp, lane);
   } else {
     // epilogue warps 2..2+EW: TMEM lane quarter q = warp % 4, column part h
     const int q = warp & 3;
@@ -917,6 +937,8 @@ cudaError_t launch_tc(const GemmOperands& g, TcParams p, int num_sms, cudaStream
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
+  p.a_rows = g.A;
+  p.lda = g.lda;
   p.tiles_m = (g.M + BM - 1) / BM;
   p.tiles_n = g.N / BN;
   p.k_tiles = (g.K + BK - 1) / BK;
@@ -1046,6 +1068,7 @@ cudaError_t tc_gemm_loss(const GemmOperands& g, const NetShape& s, LossCoef lc, 
   p.lddz = lddz;
   p.colsum_part = colsum_part;
   p.loss_part = loss_part;
+  p.layout9222 = is_layout_9222(s) ? 1 : 0;
   p.epi_n = g.N;
   p.err = err;
   p.timeout_ns = timeout_ns;

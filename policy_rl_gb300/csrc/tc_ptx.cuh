@@ -59,6 +59,11 @@ __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) 
                "r"(x), "r"(y)
                : "memory");
 }
+// contiguous bytes into L2 (bytes a multiple of 16, address 16-byte aligned)
+__device__ __forceinline__ void bulk_prefetch_l2(const void* addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)addr), "r"(bytes)
+               : "memory");
+}
 // 3-D tiled prefetch of a box into L2
 __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(

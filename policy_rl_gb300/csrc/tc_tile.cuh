@@ -379,7 +379,7 @@ struct HeadMasks {
   int g0, vcol, G;
 };
 
-__device__ __forceinline__ HeadMasks head_masks(const NetShape& s) {
+__host__ __device__ constexpr HeadMasks head_masks(const NetShape& s) {
   HeadMasks m{0u, 0u, 0u, 0u, 0, s.C - 1, s.G};
   int off = 0;
   for (int h = 0; h < s.NH; ++h) {
@@ -392,6 +392,33 @@ __device__ __forceinline__ HeadMasks head_masks(const NetShape& s) {
   m.g0 = off;
   m.gm = s.G > 0 ? ((1u << s.G) - 1u) << off : 0u;
   return m;
+}
+
+// Four discrete heads of 9, 2, 2 and 2 actions and the value column (16
+// columns, no Gaussian dimensions): with its masks as compile-time constants
+// the compiler resolves every per-column test of the loss, and the running
+// scans become straight-line per-head code (measured 6x faster than with
+// run-time masks).  Every other layout takes the run-time masks.
+__host__ __device__ constexpr NetShape shape_9222() {
+  NetShape s{};
+  s.NH = 4;
+  s.head_n[0] = 9;
+  s.head_n[1] = 2;
+  s.head_n[2] = 2;
+  s.head_n[3] = 2;
+  s.G = 0;
+  s.C = 16;
+  s.CP = 16;
+  return s;
+}
+constexpr HeadMasks kMasks9222 = head_masks(shape_9222());
+static_assert(kMasks9222.hs == 0x2A01u && kMasks9222.he == 0x5500u && kMasks9222.hd == 0x7FFFu &&
+                  kMasks9222.gm == 0u && kMasks9222.g0 == 15 && kMasks9222.vcol == 15 &&
+                  kMasks9222.G == 0,
+              "head masks of the 9-2-2-2 layout");
+__host__ __device__ inline bool is_layout_9222(const NetShape& s) {
+  return s.NH == 4 && s.head_n[0] == 9 && s.head_n[1] == 2 && s.head_n[2] == 2 &&
+         s.head_n[3] == 2 && s.G == 0 && s.C == 16 && s.CP == 16;
 }
 
 // Per-row PPO loss and d(loss)/dz for one row of head outputs z (CP columns),
