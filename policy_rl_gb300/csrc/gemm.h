@@ -85,7 +85,6 @@ struct WFinal {
 struct WParams {
   WRegion r[3];
   int nreg, total_units;
-  int wbm, ws;   // output tile rows (128 or 256) and ring stages
   uint32_t mn_lbo, mn_sbo;
   int* err;
   uint64_t timeout_ns;

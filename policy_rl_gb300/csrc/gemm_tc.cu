@@ -47,9 +47,8 @@ using namespace tc;
 
 constexpr int kThreads = 192;
 
-// minibatch rows from which the configurations for tall minibatches are used
-// (256-row weight-gradient tiles, the single-k-tile backward-data kernel):
-// they trade latency for bandwidth, which short minibatches cannot afford
+// minibatch rows from which the single-k-tile backward-data kernel is used: it
+// trades latency for bandwidth, which short minibatches cannot afford
 constexpr int64_t kTallRows = 65536;
 
 // the bias of a forward product launched without one
@@ -506,22 +505,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // ---------------------------------------------------------------------------
 // Weight-gradient kernel: P[M][N] = sum_rows U[row][m] * V[row][n] over a
 // K-split of the minibatch rows; both operands MN-major in shared memory.
-// Output tiles are wbm x bn (bn <= 256): with tall minibatches (long K
-// ranges per unit) wbm = 256 -- two 128-row MMAs share each B tile, one
-// accumulator pair [rows 0..127 | 128..255] in TMEM, 3 stages of 64 KB: per
-// k-tile an SM takes in 64 KB for 256 x 256 x 64 products; otherwise wbm =
-// 128 with a double-buffered accumulator (the next unit's MMAs overlap the
-// previous unit's epilogue, which matters when units are short) and 4 stages
-// of 48 KB.  A 256-row tile's lower half may lie beyond M (M a multiple of
-// 128): its A blocks are zero-filled and its MMAs and stores skipped.
+// Output tiles are WBM = 256 rows x bn <= 256 columns: two 128-row MMAs share
+// each B tile, one accumulator pair [rows 0..127 | 128..255] in TMEM, 3
+// stages of 64 KB -- per k-tile an SM takes in 64 KB for 256 x 256 x 64
+// products (measured against 128-row tiles with a double-buffered
+// accumulator: 212 vs 238 us per large-batch minibatch, 116 vs 172 us per
+// DDNet-like one, 32 vs 30 us per Mario-like one).  A tile's lower half may
+// lie beyond M (M a multiple of 128): its A blocks are zero-filled and its
+// MMAs and stores skipped.
+constexpr int WBM = 256;
 constexpr int WBN = 256;
-constexpr int WS_MAX = 4;
-constexpr int W_RING = 196608;   // 3 x 64 KB or 4 x 48 KB
+constexpr int WS = 3;
+constexpr int W_STAGE = (WBM + WBN) * BK * 2;   // A: 4 blocks of 64 features x 64 rows, B: up to 4
 constexpr int W_STG = 2 * 4096;   // per epilogue warp: two 32 x 32 fp32 store boxes
-constexpr size_t W_SMEM = 1024 + (size_t)W_RING + 4 * W_STG + 512;
+constexpr size_t W_SMEM = 1024 + (size_t)WS * W_STAGE + 4 * W_STG + 512;
 static_assert(W_SMEM + 64 <= 232448, "shared memory per CTA");
 constexpr int W_TMEM_COLS = 512;
-__host__ __device__ constexpr int wgrad_wbm(int64_t rows) { return rows >= kTallRows ? 256 : 128; }
 
 __device__ __forceinline__ void decode_unit(const WParams& p, int u, int& reg, int& tm, int& tn,
                                             int& kt0, int& kt1, int& split) {
@@ -567,7 +566,7 @@ __device__ __forceinline__ float4 split_sum4_cg(const float* q, int64_t st, int 
 // is resident).  Each CTA first arrives on the counter of every output tile
 // it stored a split partial of; then, per unit, it waits (bounded) until all
 // splits of the tile have arrived and sums its share of the tile's rows --
-// split s of S takes rows [wbm s / S, wbm (s + 1) / S) below M -- over the splits in
+// split s of S takes rows [256 s / S, 256 (s + 1) / S) below M -- over the splits in
 // split order, writing the final gradient entries and the sum of their
 // squares (per CTA, fixed order) for the clip norm.  The last CTA of a tile to
 // finish clears its counters for the next launch.  On a timeout (or an
@@ -613,12 +612,12 @@ __device__ __noinline__ void wgrad_fixup(const WParams& p, bool aborted) {
       __syncthreads();
       if (!s_ok) break;
       const WFinal& F = p.f[reg];
-      const int r0 = p.wbm * split / R.splits, r1 = p.wbm * (split + 1) / R.splits;
+      const int r0 = WBM * split / R.splits, r1 = WBM * (split + 1) / R.splits;
       const int q4 = R.bn / 4;   // four columns per work item
       const int n_it = (r1 - r0) * q4;
       const int64_t pst = (int64_t)R.M * R.N;
       for (int e = threadIdx.x; e < n_it; e += kThreads) {
-        const int m = tm * p.wbm + r0 + e / q4, n = tn * R.bn + 4 * (e % q4);
+        const int m = tm * WBM + r0 + e / q4, n = tn * R.bn + 4 * (e % q4);
         if (m >= R.M) break;   // (e grows with m)
         const float4 v = split_sum4_cg(R.part + (int64_t)m * R.N + n, pst, R.splits);
         const float vv[4] = {v.x, v.y, v.z, v.w};
@@ -658,29 +657,23 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  uint8_t* wstg = gbase + (size_t)W_RING;   // [4 warps][2][32 rows x 128 B]
+  uint8_t* wstg = gbase + (size_t)WS * W_STAGE;   // [4 warps][2][32 rows x 128 B]
   uint8_t* ctrl = wstg + 4 * W_STG;
-  Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), WS_MAX};
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * Ctrl::count(WS_MAX));
-  const int WS = p.ws;                          // stages of this launch
-  const int W_STAGE = (p.wbm + WBN) * BK * 2;   // A (wbm / 64 blocks) + B (up to 4 blocks)
-  const int nacc = p.wbm == 256 ? 1 : 2;        // accumulators of wbm x WBN in TMEM
-  const int kWPrefetch = WS + 1;                // L2 prefetch distance (k-tiles)
+  Ctrl cb{reinterpret_cast<uint64_t*>(ctrl), WS};
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(ctrl + 8 * Ctrl::count(WS));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   auto sA = [&](int s) { return base + (uint32_t)(s * W_STAGE); };
-  auto sB = [&](int s) { return base + (uint32_t)(s * W_STAGE + p.wbm * BK * 2); };
+  auto sB = [&](int s) { return base + (uint32_t)(s * W_STAGE + WBM * BK * 2); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < WS_MAX; ++s) {
+    for (int s = 0; s < WS; ++s) {
       mbar_init(cb.full(s), 1);
       mbar_init(cb.empty(s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(cb.tfull(a), 1);
-      mbar_init(cb.tempty(a), 128);
-    }
+    mbar_init(cb.tfull(0), 1);
+    mbar_init(cb.tempty(0), 128);
     mbar_init(cb.drain(), 1);
     *abort_flag = 0;
     cnt[0] = 0;
@@ -699,8 +692,8 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
   if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
-      int ws_s = 0;          // stage of `it` (it % WS) and its phase parity ((it / WS) & 1),
-      uint32_t ws_ph = 0;    // kept as counters: WS is a launch parameter
+      int ws_s = 0;          // stage of `it` (it % WS) and its phase parity ((it / WS) & 1)
+      uint32_t ws_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
         int reg, tm, tn, kt0, kt1, split;
@@ -708,21 +701,15 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
         const int bn = p.r[reg].bn;
         const CUtensorMap* tu = reg == 0 ? &tmU0 : (reg == 1 ? &tmU1 : &tmU2);
         const CUtensorMap* tv = reg == 0 ? &tmV0 : (reg == 1 ? &tmV1 : &tmV2);
-        const uint32_t bytes = (uint32_t)(p.wbm + bn) * BK * 2;
+        const uint32_t bytes = (uint32_t)(WBM + bn) * BK * 2;
         for (int kt = kt0; kt < kt1; ++kt) {
           const int s = ws_s;
           const uint32_t r = ws_ph;
-          // both operands stream from DRAM: bring the rows kWPrefetch k-tiles
-          // beyond the ring into L2 before their loads are issued
-          if (p.wbm == 128 && kt + kWPrefetch < kt1) {   // (256-row tiles: measured no gain)
-            tma_prefetch_3d(tu, 0, (kt + kWPrefetch) * BK, tm * (p.wbm / 64));
-            tma_prefetch_3d(tv, 0, (kt + kWPrefetch) * BK, tn * (bn / 64));
-          }
           if (!wait_bar(cb.empty(s), (r & 1) ^ 1, g)) { ok = false; break; }
           mbar_arrive_expect_tx(cb.full(s), bytes);
-          // one 3-D box per operand: 64 rows x {wbm/64, bn/64} blocks of 64
-          // features (blocks beyond M read as zeros)
-          tma_load_3d(sA(s), tu, 0, kt * BK, tm * (p.wbm / 64), cb.full(s));
+          // one 3-D box per operand: 64 rows x {4, bn/64} blocks of 64 features
+          // (blocks beyond M read as zeros)
+          tma_load_3d(sA(s), tu, 0, kt * BK, tm * (WBM / 64), cb.full(s));
           tma_load_3d(sB(s), tv, 0, kt * BK, tn * (bn / 64), cb.full(s));
           ++it;
           cnt[0] = it;
@@ -746,11 +733,11 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
         decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
         const int bn = p.r[reg].bn;
         const uint32_t idesc = idesc_bf16(BM, bn, true, true);
-        // wbm = 256: the tile's rows 128..255 exist, in the second accumulator
-        const bool lower = p.wbm == 256 && tm * 256 + BM < p.r[reg].M;
-        const int acc = (int)(tc % nacc);
-        const uint32_t d = tmem + (uint32_t)(acc * WBN);
-        if (!wait_bar(cb.tempty(acc), ((tc / nacc) & 1) ^ 1, g)) break;
+        const bool lower = tm * WBM + BM < p.r[reg].M;   // the tile's rows 128..255 exist
+        // one unit at a time: the accumulators [rows 0..127 | rows 128..255]
+        // take 2 bn <= 512 TMEM columns
+        const uint32_t d = tmem;
+        if (!wait_bar(cb.tempty(0), (tc & 1) ^ 1, g)) break;
         tc_fence_after();
         for (int kt = kt0; kt < kt1; ++kt) {
           const int s = ws_s;
@@ -772,7 +759,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
           if (++ws_s == WS) { ws_s = 0; ws_ph ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(cb.tfull(acc));
+        tc_commit(cb.tfull(0));
         ++tc;
       }
     }
@@ -783,8 +770,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
       int reg, tm, tn, kt0, kt1, split;
       decode_unit(p, u, reg, tm, tn, kt0, kt1, split);
       const WRegion& R = p.r[reg];
-      const int acc = (int)(tc % nacc);
-      if (!wait_bar(cb.tfull(acc), (tc / nacc) & 1, g)) break;
+      if (!wait_bar(cb.tfull(0), tc & 1, g)) break;
       tc_fence_after();
       // fp32 partial tile -> this split's slice of the partial buffer, 32
       // columns at a time through two 32 x 32 staging boxes per warp (128-byte
@@ -792,10 +778,9 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
       // half hf = rows 128 hf .. 128 hf + 127 of the tile
       const CUtensorMap* tp = reg == 0 ? &tmP0 : (reg == 1 ? &tmP1 : &tmP2);
       uint8_t* mystg = wstg + (warp - 2) * W_STG;
-      for (int hf = 0; hf < p.wbm / BM; ++hf) {
-        if (tm * p.wbm + hf * BM >= R.M) break;
-        const uint32_t taddr =
-            tmem + (uint32_t)(acc * WBN + hf * R.bn) + ((uint32_t)(q * 32) << 16);
+      for (int hf = 0; hf < WBM / BM; ++hf) {
+        if (tm * WBM + hf * BM >= R.M) break;
+        const uint32_t taddr = tmem + (uint32_t)(hf * R.bn) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
         for (int c0 = 0; c0 < R.bn; c0 += 32, ++sc) {
           float v[32];
@@ -810,13 +795,13 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmU0, const __grid_constant_
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(tp, smem_u32(buf), tn * R.bn + c0, tm * p.wbm + hf * BM + q * 32, split);
+            tma_store_3d(tp, smem_u32(buf), tn * R.bn + c0, tm * WBM + hf * BM + q * 32, split);
             bulk_commit();
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(cb.tempty(acc));
+      mbar_arrive(cb.tempty(0));
       ++tc;
     }
     if (lane == 0) {
@@ -1085,8 +1070,6 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
   CUtensorMap tu[3], tv[3], tp[3];
   WParams p{};
   p.nreg = nreg;
-  p.wbm = wgrad_wbm(rows);
-  p.ws = W_RING / ((p.wbm + WBN) * BK * 2);
   p.err = err;
   p.timeout_ns = timeout_ns;
   p.mn_lbo = mn_lbo;
@@ -1105,13 +1088,13 @@ cudaError_t tc_wgrad(const WGradRegion* regs, int nreg, int rows, uint32_t mn_lb
     if (G.M % BM != 0 || G.N % 64 != 0 || G.M > G.ldu || G.N > G.ldv) return cudaErrorInvalidValue;
     WRegion& R = p.r[r];
     R.bn = tc_wgrad_bn(G.N);
-    cudaError_t e = make_tmap_blocks(&tu[r], G.U, rows, G.ldu, G.M / 64, BK, p.wbm / 64);
+    cudaError_t e = make_tmap_blocks(&tu[r], G.U, rows, G.ldu, G.M / 64, BK, WBM / 64);
     if (e != cudaSuccess) return e;
     e = make_tmap_blocks(&tv[r], G.V, rows, G.ldv, G.N / 64, BK, R.bn / 64);
     if (e != cudaSuccess) return e;
     R.M = G.M;
     R.N = G.N;
-    R.tiles_m = (G.M + p.wbm - 1) / p.wbm;
+    R.tiles_m = (G.M + WBM - 1) / WBM;
     R.tiles_n = G.N / R.bn;
     R.k_tiles = (rows + BK - 1) / BK;
     R.kt_per_split = G.kt_per_split;
@@ -1172,7 +1155,7 @@ int tc_wgrad_bn(int N) { return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64); 
 void tc_wgrad_plan(const int (*mn)[2], int nreg, int64_t rows, int num_sms, int max_split,
                    int* kt) {
   const int64_t k_tiles = (rows + BK - 1) / BK;
-  const int wbm = wgrad_wbm(rows);
+  constexpr int wbm = WBM;
   double total = 0;
   for (int i = 0; i < nreg; ++i) {
     const int bn = tc_wgrad_bn(mn[i][1]);
