@@ -994,6 +994,13 @@ cudaError_t tc_gemm_bias_act(const GemmOperands& g, const float* bias, int act,
   return cudaErrorInvalidValue;
 }
 
+// 256-column backward-data tiles halve the re-reads of the row operand but
+// also the number of tiles: used when every SM still gets one (a chain of
+// small products, e.g. Newton-Schulz on 256 x 256 matrices, keeps 128 columns)
+bool wide_dact(const GemmOperands& g, int num_sms) {
+  return g.N % 256 == 0 && (int64_t)((g.M + BM - 1) / BM) * (g.N / 256) >= num_sms;
+}
+
 cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ldaux, int act,
                          __nv_bfloat16* out, int ldo, float* colsum_part, int* err,
                          uint64_t timeout_ns, int num_sms, cudaStream_t st, int* grid_out) {
@@ -1013,7 +1020,7 @@ cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ld
   if (g.N % 128 != 0) return cudaErrorInvalidValue;
   // (the single-k-tile configuration pays off on tall minibatches only)
   if (g.K <= BK && g.M >= kTallRows) return launch_tc<128, EPI_DACT_K1>(g, p, num_sms, st, grid_out);
-  if (g.N % 256 == 0) return launch_tc<256, EPI_DACT>(g, p, num_sms, st, grid_out);
+  if (wide_dact(g, num_sms)) return launch_tc<256, EPI_DACT>(g, p, num_sms, st, grid_out);
   return launch_tc<128, EPI_DACT>(g, p, num_sms, st, grid_out);
 }
 
@@ -1034,7 +1041,7 @@ cudaError_t tc_gemm_axpby(const GemmOperands& g, const __nv_bfloat16* aux, int l
   p.err = err;
   p.timeout_ns = timeout_ns;
   if (g.K <= BK && g.M >= kTallRows) return launch_tc<128, EPI_DACT_K1>(g, p, num_sms, st, nullptr);
-  if (g.N % 256 == 0) return launch_tc<256, EPI_DACT>(g, p, num_sms, st, nullptr);
+  if (wide_dact(g, num_sms)) return launch_tc<256, EPI_DACT>(g, p, num_sms, st, nullptr);
   return launch_tc<128, EPI_DACT>(g, p, num_sms, st, nullptr);
 }
 
