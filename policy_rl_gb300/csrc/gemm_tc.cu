@@ -995,10 +995,10 @@ cudaError_t tc_gemm_bias_act(const GemmOperands& g, const float* bias, int act,
 }
 
 // 256-column backward-data tiles halve the re-reads of the row operand but
-// also the number of tiles: used when every SM still gets one (a chain of
+// also the number of tiles: used when every SM still gets two (a chain of
 // small products, e.g. Newton-Schulz on 256 x 256 matrices, keeps 128 columns)
 bool wide_dact(const GemmOperands& g, int num_sms) {
-  return g.N % 256 == 0 && (int64_t)((g.M + BM - 1) / BM) * (g.N / 256) >= num_sms;
+  return g.N % 256 == 0 && (int64_t)((g.M + BM - 1) / BM) * (g.N / 256) >= 2 * num_sms;
 }
 
 cudaError_t tc_gemm_dact(const GemmOperands& g, const __nv_bfloat16* aux, int ldaux, int act,
