@@ -195,11 +195,11 @@ OPTIMIZERS = {"adam": 0, "muon": 1}
 # capture report null.
 NCU_TRAFFIC = {
     ("mario", "fwd1_gemm"): 4.26e6, ("mario", "fwd2_gemm"): 16.94e6,
-    ("mario", "head_loss_gemm"): 17.78e6, ("mario", "dact2_gemm"): 21.06e6,
-    ("mario", "dact1_gemm"): 33.74e6, ("mario", "wgrad_gemm"): 76.00e6,
-    ("large", "fwd1_gemm"): 279.68e6, ("large", "fwd2_gemm"): 488.11e6,
-    ("large", "head_loss_gemm"): 280.99e6, ("large", "dact2_gemm"): 518.45e6,
-    ("large", "dact1_gemm"): 832.47e6, ("large", "wgrad_gemm"): 1192.68e6,
+    ("mario", "head_loss_gemm"): 17.78e6, ("mario", "dact2_gemm"): 21.05e6,
+    ("mario", "dact1_gemm"): 33.73e6, ("mario", "wgrad_gemm"): 76.15e6,
+    ("large", "fwd1_gemm"): 279.80e6, ("large", "fwd2_gemm"): 487.82e6,
+    ("large", "head_loss_gemm"): 280.92e6, ("large", "dact2_gemm"): 518.69e6,
+    ("large", "dact1_gemm"): 835.31e6, ("large", "wgrad_gemm"): 1190.63e6,
 }
 
 
