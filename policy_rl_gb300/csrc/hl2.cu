@@ -54,8 +54,13 @@ constexpr int kOffLp = kOffCs3 + 4 * 32 * 4;      // [4][kLossPartials]
 constexpr int kOffB3 = kOffLp + 4 * kLossPartials * 4;
 constexpr int kSmemBytes = 1024 + kOffB3 + 32 * 4;
 
+// H2 blocks (128 rows x 64 columns, 16 KB) have a full and an empty barrier
+// each: slot hb * 4 + kb holds block kb of the tile in buffer hb.  A dP2
+// half releases its blocks as soon as its stores have read them, so the next
+// tile's blocks load while the rest of the current tile is processed.
+constexpr int kSlots = 8;
 enum Bar : int {
-  B_HS_FULL = 0, B_HS_FULL1, B_HS_EMPTY, B_HS_EMPTY1, B_W3_FULL, B_W3T_FULL, B_W3T_EMPTY, B_ZFULL, B_DZ_RDY,
+  B_HSF = 0, B_HSE = kSlots, B_W3_FULL = 2 * kSlots, B_W3T_FULL, B_W3T_EMPTY, B_ZFULL, B_DZ_RDY,
   B_P0, B_P1, B_RA_FREE, B_RB_FREE, B_DRAIN, B_COUNT
 };
 
@@ -74,6 +79,17 @@ struct HParams {
   float *cs2, *cs3, *lossp;   // per-CTA partial rows
   int* err;
   uint64_t timeout_ns;
+  int layout9222;   // the 9-2-2-2 head layout: compile-time masks in the loss
+};
+
+// head masks of the loss: the compile-time ones of the common layout, or the
+// run-time ones of the shape (two instantiations of the loss loop)
+struct FixedMasks {
+  __device__ static constexpr HeadMasks get() { return kMasks9222; }
+};
+struct ShapeMasks {
+  HeadMasks m;
+  __device__ HeadMasks get() const { return m; }
 };
 
 template <int H2, int CP>
@@ -101,9 +117,9 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
 
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   if (threadIdx.x == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_HS_FULL + b), 1);
-      mbar_init(bar(B_HS_EMPTY + b), kHGrp);
+    for (int b = 0; b < kSlots; ++b) {
+      mbar_init(bar(B_HSF + b), 1);
+      mbar_init(bar(B_HSE + b), kHGrp);
     }
     mbar_init(bar(B_W3_FULL), 1);
     mbar_init(bar(B_W3T_FULL), 1);
@@ -144,17 +160,21 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
       mbar_arrive_expect_tx(bar(B_W3_FULL), (uint32_t)(CP * H2 * 2));
       tma_load_3d(base + kOffW3, &maps.w3, 0, 0, 0, bar(B_W3_FULL));
       uint32_t t = 0, wl = 0;
+      uint32_t nblk = 0;   // H2 blocks issued
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++t) {
-        // H2 tile into buffer t % NBUF, once that buffer's previous tile has been
-        // stored out of it
+        // the tile's H2 blocks into buffer t % NBUF, each once that slot's
+        // block of the previous tile has been stored out of it
         const int hb = t % NBUF;
         const uint32_t hu = t / NBUF;
-        if (hu > 0 && !wait_bar(bar(B_HS_EMPTY + hb), (hu - 1) & 1, g)) break;
-        mbar_arrive_expect_tx(bar(B_HS_FULL + hb), (uint32_t)(NB * kBlk));
-        for (int kb = 0; kb < NB; ++kb)
-          tma_load_2d(base + kOffHS + (hb * 4 + kb) * kBlk, &maps.h2, kb * 64, tile * 128,
-                      bar(B_HS_FULL + hb));
-        cnt[0] = t + 1;
+        for (int kb = 0; kb < NB && ok; ++kb) {
+          const int slot = hb * 4 + kb;
+          if (hu > 0 && !wait_bar(bar(B_HSE + slot), (hu - 1) & 1, g)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(B_HSF + slot), (uint32_t)kBlk);
+          tma_load_2d(base + kOffHS + slot * kBlk, &maps.h2, kb * 64, tile * 128,
+                      bar(B_HSF + slot));
+          cnt[0] = ++nblk;
+        }
+        if (!ok) break;
         // W3^T, one box per dP2 half (the buffer is free once the half's MMA is done)
         for (int hf = 0; hf < NH && ok; ++hf, ++wl) {
           if (wl > 0 && !wait_bar(bar(B_W3T_EMPTY), (wl - 1) & 1, g)) { ok = false; break; }
@@ -173,15 +193,17 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
         const uint32_t ph = t & 1, pph = (t - 1) & 1;
         // Z = H2 W3^T into RA[0, CP): RA free once the previous tile drained it
         const int hb = t % NBUF;
-        if (!wait_bar(bar(B_HS_FULL + hb), (t / NBUF) & 1, g)) break;
         if (t > 0 && !wait_bar(bar(B_RA_FREE), pph, g)) break;
-        tc_fence_after();
         const uint32_t idz = idesc_bf16(128, CP, false, false);
-        for (int kb = 0; kb < NB; ++kb)
+        for (int kb = 0; kb < NB && ok; ++kb) {   // block by block as they land
+          if (!wait_bar(bar(B_HSF + hb * 4 + kb), (t / NBUF) & 1, g)) { ok = false; break; }
+          tc_fence_after();
           for (int kk = 0; kk < 4; ++kk)
             tc_mma_bf16(RA, sdesc_sw128(base + kOffHS + (hb * 4 + kb) * kBlk + kk * 32, 16, 1024),
                         sdesc_sw128(base + kOffW3 + kb * CP * 128 + kk * 32, 16, 1024), idz,
                         (kb | kk) ? 1u : 0u);
+        }
+        if (!ok) break;
         tc_commit(bar(B_ZFULL));
         // dP2 halves = dz W3 (K = CP): half 0 -> RB, half 1 -> RA (Z drained by then)
         if (!wait_bar(bar(B_DZ_RDY), ph, g)) break;
@@ -206,7 +228,6 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
     const int q = warp & 3;
     const bool loss_grp = warp < 6;
     const int rl = q * 32 + lane;
-    const HeadMasks hm = head_masks(p.shape);
     const uint32_t lanes = (uint32_t)(q * 32) << 16;
     const uint32_t RA = tmem + lanes, RB = tmem + 256 + lanes;
     auto store_rows = [&](const CUtensorMap* m, const uint8_t* tile_base, int blk0, int nblk,
@@ -224,6 +245,8 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
       if (lane == 0) bulk_wait_read0();
       __syncwarp();
     };
+    auto run = [&](auto masks) {
+    const HeadMasks hm = masks.get();
     uint32_t t = 0;
     for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++t) {
       const uint32_t ph = t & 1;
@@ -234,12 +257,14 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
       const bool rok = row < p.M;
       if (loss_grp) {
         // loss on Z (one row per thread) -> dz tile.  ZFULL(t) is committed after
-        // the dP2 products of tile t-1, which read the dz tile: it is free.
+        // the dP2 products of tile t-1, which read the dz tile: it is free.  The
+        // row inputs are loaded before the wait.
+        RowIn in;
+        load_row_in(in, row, rok, p.shape, p.rows);
         if (!wait_bar(bar(B_ZFULL), ph, g)) break;
         tc_fence_after();
         float dzr[32], t6[6], dls[4];
-        loss_row_regs<CP>(RA, row, rok, p.shape, hm, p.lc, p.inv_mb, p.rows, p.logstd, b3s, dzr,
-                          t6, dls);
+        loss_row_in<CP>(RA, rok, p.shape, hm, p.lc, p.inv_mb, in, p.logstd, b3s, dzr, t6, dls);
         uint8_t* drow = DZ + rl * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -269,21 +294,28 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
           tc_fence_before();
           store_rows(&maps.dp2, hs, hf * 4, HN / 64, row0);
           mbar_arrive(bar(hf == 0 ? B_RB_FREE : B_RA_FREE));
+          stores_read();   // the half's blocks are reloaded after this
+          for (int j = 0; j < HN / 64; ++j) mbar_arrive(bar(B_HSE + hb * 4 + hf * 4 + j));
         }
         if (!ok) break;
-        stores_read();   // this buffer is reloaded after this
-        mbar_arrive(bar(B_HS_EMPTY + hb));
       }
     }
+    };
+    if (loss_grp && p.layout9222)
+      run(FixedMasks{});
+    else
+      run(ShapeMasks{head_masks(p.shape)});
     if (lane == 0) bulk_wait0();
   }
 
   __syncthreads();
   if (*abort_flag) {
-    if (threadIdx.x == 0) {   // loads in flight: the last H2 tiles and W3^T box
+    if (threadIdx.x == 0) {   // loads in flight: the last H2 blocks and W3^T box
       const uint32_t hl = cnt[0], wl = cnt[1];
-      for (uint32_t l = hl >= (uint32_t)NBUF ? hl - NBUF : 0; l < hl; ++l)
-        drain_wait(bar(B_HS_FULL + l % NBUF), (l / NBUF) & 1, p.timeout_ns);
+      for (uint32_t l = hl >= (uint32_t)(NBUF * NB) ? hl - NBUF * NB : 0; l < hl; ++l) {
+        const uint32_t tl = l / NB;   // the block's tile (in this CTA's order) and slot
+        drain_wait(bar(B_HSF + (tl % NBUF) * 4 + l % NB), (tl / NBUF) & 1, p.timeout_ns);
+      }
       if (wl > 0) drain_wait(bar(B_W3T_FULL), (wl - 1) & 1, p.timeout_ns);
       drain_wait(bar(B_W3_FULL), 0, p.timeout_ns);
     }
@@ -364,6 +396,7 @@ cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int*
   p.lossp = f.lossp;
   p.err = f.err;
   p.timeout_ns = f.timeout_ns;
+  p.layout9222 = is_layout_9222(s) ? 1 : 0;
   const int grid = p.tiles < num_sms ? p.tiles : num_sms;
   if (grid_out) *grid_out = grid;
   const bool c32 = s.CP == 32;
