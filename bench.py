@@ -160,7 +160,7 @@ def _stage_work(stage: str, w, mb: int):
         "dact1_gemm": (2 * mb * H1 * H2, a * (H2 + 2 * H1)),
         "wgrad_gemm": (2 * mb * (H2 * H1 + H1 * D + C * H2), a * (H2 + H1 + H1 + Dp + H2 + 64)),
         # fused variants: head + loss + dP2 (H2 read once); the whole fwd / loss / bwd-data
-        "head_loss_dact2": (4 * mb * C * H2, a * (2 * H2 + 64) + mb * (4 * len(w.heads) + 12)),
+        "head_loss_dact2": (4 * mb * C * H2, a * (2 * H2 + CP) + mb * (4 * len(w.heads) + 12)),
         "fused_mlp": (2 * mb * (H1 * D + H2 * H1 + 2 * C * H2 + H1 * H2),
                       a * (Dp + 2 * H1 + 2 * H2 + 64) + mb * (4 * len(w.heads) + 12)),
     }
@@ -200,6 +200,7 @@ NCU_TRAFFIC = {
     ("large", "fwd1_gemm"): 279.80e6, ("large", "fwd2_gemm"): 487.82e6,
     ("large", "head_loss_gemm"): 280.92e6, ("large", "dact2_gemm"): 518.69e6,
     ("large", "dact1_gemm"): 835.31e6, ("large", "wgrad_gemm"): 1190.63e6,
+    ("large", "head_loss_dact2"): 497.02e6,
 }
 
 

@@ -1032,7 +1032,8 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
               cfg->optimizer == 0;   // the persistent kernel runs Adam itself
   c->use_fmlp = c->bf16 && !c->use_mk && cfg->fused_mlp != 0 && cfg->adv_mode == 0 &&
                 fmlp_supported(s);
-  c->use_hl2 = c->bf16 && !c->use_mk && cfg->fused_loss != 0 && hl2_supported(s);
+  c->use_hl2 = c->bf16 && !c->use_mk &&
+               (cfg->fused_loss > 0 ? hl2_supported(s) : cfg->fused_loss == 0 && hl2_preferred(s));
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (c->num_sms < 1) c->num_sms = 1;
   c->mbmax = cfg->max_minibatch;

@@ -306,8 +306,10 @@ cudaError_t mk_prepare();
 int mk_grid(int num_sms);
 int mk_wgrad_bn(int N);
 cudaError_t mk_launch(const MkLaunch& L, cudaStream_t st);
+// bf16 row-major [rows][ld]: box = box_cols x box_rows, swizzled in rows of
+// swizzle_bytes (128, 64 or 32; the box's row must fit in it)
 cudaError_t tc_make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
-                         int box_cols, int box_rows);
+                         int box_cols, int box_rows, int swizzle_bytes = 128);
 // [rows][ld] bf16 viewed as 64-column blocks: box = 64 x box_rows x box_blk,
 // landing as box_blk consecutive [box_rows][64] swizzled blocks
 cudaError_t tc_make_tmap_blocks(CUtensorMap* m, const void* base, int64_t rows, int64_t ld,
@@ -349,6 +351,8 @@ struct HeadLossDact {
   uint64_t timeout_ns;
 };
 bool hl2_supported(const NetShape& s);
+// shapes where the fused kernel beats the two-kernel path (H2 = 512, CP = 16)
+bool hl2_preferred(const NetShape& s);
 cudaError_t hl2_prepare();
 cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int* grid_out);
 

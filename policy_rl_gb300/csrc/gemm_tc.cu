@@ -962,8 +962,14 @@ cudaError_t tc_prepare() {
 }
 
 cudaError_t tc_make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
-                         int box_cols, int box_rows) {
-  return make_tmap(m, base, cols, rows, ld, box_cols, box_rows);
+                         int box_cols, int box_rows, int swizzle_bytes) {
+  if (box_cols * 2 > swizzle_bytes) return cudaErrorInvalidValue;
+  const CUtensorMapSwizzle swz = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                       : CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swz == CU_TENSOR_MAP_SWIZZLE_NONE) return cudaErrorInvalidValue;
+  return make_tmap(m, base, cols, rows, ld, box_cols, box_rows, swz);
 }
 
 cudaError_t tc_make_tmap_blocks(CUtensorMap* m, const void* base, int64_t rows, int64_t ld,

@@ -18,7 +18,8 @@
 //
 // Roles: warp 0 TMA, warp 1 MMA, warps 2..5 the loss and warps 6..9 the dP2
 // epilogue (TMEM lane quarter q = warp % 4 in each group), so that the loss of
-// one tile overlaps the dP2 epilogue of the previous one.  TMEM: R_A = columns [0, 256) holds Z (first
+// one tile overlaps the dP2 epilogue of the previous one.  With H2 = 512 only
+// one tile fits and the loss warps then work on dP2 as well.  TMEM: R_A = columns [0, 256) holds Z (first
 // CP columns) and then the second 256-column half of dP2 (H2 = 512); R_B =
 // [256, 512) holds the first half of dP2.  Every wait is bounded.
 #include <cuda.h>
@@ -128,8 +129,8 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
     mbar_init(bar(B_DZ_RDY), kHGrp);
     mbar_init(bar(B_P0), 1);
     mbar_init(bar(B_P1), 1);
-    mbar_init(bar(B_RA_FREE), kHGrp);
-    mbar_init(bar(B_RB_FREE), kHGrp);
+    mbar_init(bar(B_RA_FREE), NBUF == 1 ? 2 * kHGrp : kHGrp);
+    mbar_init(bar(B_RB_FREE), NBUF == 1 ? 2 * kHGrp : kHGrp);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     cnt[0] = 0;
@@ -283,19 +284,25 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
         stores_read();   // the dz tile is rewritten with the next tile
         mbar_arrive(bar(B_DZ_RDY));
         if (NH == 1) mbar_arrive(bar(B_RA_FREE));   // RA held only Z
-      } else {
-        // dP2 halves, in place in HS, stored (one warp per quarter: all columns)
+      }
+      if (!loss_grp || NBUF == 1) {
+        // dP2 halves, in place in HS, stored.  With one H2 buffer the loss group
+        // has nothing to overlap and joins in: each of the GW warps takes the
+        // rows of its lane quarter and CB of the half's 64-column blocks.
+        constexpr int GW = NBUF == 1 ? 8 : 4;
+        constexpr int CB = HN / 64 / (GW / 4);
+        const int gi = NBUF == 1 && !loss_grp ? 1 : 0;
         bool ok = true;
         for (int hf = 0; hf < NH; ++hf) {
           if (!wait_bar(bar(hf == 0 ? B_P0 : B_P1), ph, g)) { ok = false; break; }
           tc_fence_after();
-          epi_dact_smem_tile<HN, 4>(hf == 0 ? RB : RA, rl, rok, hf * 256, 0, p.act,
-                                    hs + hf * 4 * kBlk, cs2 + q * kH2Max, lane);
+          epi_dact_smem_tile<HN, GW>(hf == 0 ? RB : RA, rl, rok, hf * 256, gi, p.act,
+                                     hs + hf * 4 * kBlk, cs2 + q * kH2Max, lane);
           tc_fence_before();
-          store_rows(&maps.dp2, hs, hf * 4, HN / 64, row0);
+          store_rows(&maps.dp2, hs, hf * 4 + gi * CB, CB, row0);
           mbar_arrive(bar(hf == 0 ? B_RB_FREE : B_RA_FREE));
-          stores_read();   // the half's blocks are reloaded after this
-          for (int j = 0; j < HN / 64; ++j) mbar_arrive(bar(B_HSE + hb * 4 + hf * 4 + j));
+          stores_read();   // the blocks are reloaded after this
+          for (int j = 0; j < CB; ++j) mbar_arrive(bar(B_HSE + hb * 4 + hf * 4 + gi * CB + j));
         }
         if (!ok) break;
       }
@@ -342,6 +349,286 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// H2 = 512, CP = 16: a tile's dP2 in four 128-column quarters, so that the
+// next tile's head product and loss overlap this tile's dP2 epilogue.
+//
+// H2 streams through a ring of kQR 64-column blocks (16 KB each) instead of
+// one tile buffer: the next tile's blocks land in slots as the current
+// tile's quarters are stored out of theirs, and its head product Z runs
+// block by block as they land.  TMEM: three rotating 128-column dP2 quarter
+// buffers in columns [0, 384) and Z in [384, 400).  W3^T (512 x 16) and the
+// dz tile (128 x 16) sit in 32-byte swizzled rows, W3 in 64-column blocks.
+// Roles: warp 0 TMA, warp 1 MMA, warps 2..9 the dP2 epilogue (warps 2..5 the
+// first 64 columns of each quarter, warps 6..9 the second; TMEM lane quarter
+// q = warp % 4).  Warps 2..5 also run each tile's loss before its quarters.
+// A block's slot is handed back once the TMA store of its dP2 has read it:
+// each epilogue warp checks that for its previous store half-way through its
+// next block, so no warp waits on a store it has just issued.  The loss
+// warps keep their loss sums and dz column sums in registers across tiles.
+constexpr int kQR = 11;                              // ring slots
+constexpr int kQH2 = 512, kQCP = 16;
+constexpr int kQOffW3 = kQR * kBlk;                  // W3: 8 blocks of [16][64]
+constexpr int kQOffW3T = kQOffW3 + kQCP * kQH2 * 2;  // W3^T [512][16]
+constexpr int kQOffDZ = kQOffW3T + kQH2 * kQCP * 2;  // dz [128][16]
+constexpr int kQOffCtrl = kQOffDZ + 128 * kQCP * 2;
+constexpr int kQOffCs2 = kQOffCtrl + kCtrlBytes;     // [4][512]
+constexpr int kQOffCs3 = kQOffCs2 + 4 * kQH2 * 4;    // [4][32]
+constexpr int kQOffLp = kQOffCs3 + 4 * 32 * 4;       // [4][kLossPartials]
+constexpr int kQOffB3 = kQOffLp + 4 * kLossPartials * 4;
+constexpr int kQSmemBytes = 1024 + kQOffB3 + 32 * 4;
+static_assert(kQSmemBytes <= 232448, "shared memory of the quarter kernel");
+constexpr uint32_t kQTZ = 384;   // TMEM column of Z
+
+enum QBar : int {
+  Q_FULL = 0, Q_EMPTY = kQR, Q_W3 = 2 * kQR, Q_W3T, Q_ZFULL, Q_ZFREE, Q_DZRDY, Q_DZFREE,
+  Q_QFULL, Q_QFREE = Q_QFULL + 3, Q_DRAIN = Q_QFREE + 3, Q_COUNT
+};
+static_assert(Q_COUNT * 8 + 32 <= kCtrlBytes, "barrier block");
+
+template <class Masks>
+__global__ void __launch_bounds__(kHThreads, 1)
+hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gb = smem_raw + (base - raw);
+  uint8_t* ring = gb;
+  uint8_t* DZ = gb + kQOffDZ;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gb + kQOffCtrl);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + Q_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);   // H2 blocks issued
+  float* cs2 = reinterpret_cast<float*>(gb + kQOffCs2);
+  float* cs3 = reinterpret_cast<float*>(gb + kQOffCs3);
+  float* lp = reinterpret_cast<float*>(gb + kQOffLp);
+  float* b3s = reinterpret_cast<float*>(gb + kQOffB3);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kQR; ++b) {
+      mbar_init(bar(Q_FULL + b), 1);
+      mbar_init(bar(Q_EMPTY + b), kHGrp);   // the four warps storing the block
+    }
+    mbar_init(bar(Q_W3), 1);
+    mbar_init(bar(Q_W3T), 1);
+    mbar_init(bar(Q_ZFULL), 1);
+    mbar_init(bar(Q_ZFREE), kHGrp);
+    mbar_init(bar(Q_DZRDY), kHGrp);
+    mbar_init(bar(Q_DZFREE), 1);
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(bar(Q_QFULL + b), 1);
+      mbar_init(bar(Q_QFREE + b), kHEpi);
+    }
+    mbar_init(bar(Q_DRAIN), 1);
+    *abort_flag = 0;
+    cnt[0] = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < (kQOffB3 - kQOffCs2) / 4; i += kHThreads) cs2[i] = 0.f;
+  if (warp == 1) tmem_alloc(smem_u32(tslot), 512);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.h2);
+    prefetch_tmap(&maps.w3);
+    prefetch_tmap(&maps.w3t);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const Guard g{abort_flag, p.err, p.timeout_ns};
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i < 32; i += kHThreads) b3s[i] = i < p.shape.C ? p.b3[i] : 0.f;
+  __syncthreads();   // reached by every thread of the block (before the role split)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(bar(Q_W3), (uint32_t)(kQCP * kQH2 * 2));
+      tma_load_3d(base + kQOffW3, &maps.w3, 0, 0, 0, bar(Q_W3));
+      mbar_arrive_expect_tx(bar(Q_W3T), (uint32_t)(kQH2 * kQCP * 2));
+      tma_load_2d(base + kQOffW3T, &maps.w3t, 0, 0, bar(Q_W3T));
+      tma_load_2d(base + kQOffW3T + 256 * kQCP * 2, &maps.w3t, 0, 256, bar(Q_W3T));
+      uint32_t n = 0, slot = 0, use = 0;   // blocks issued; ring position of the next
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < kQH2 / 64; ++kb) {
+          if (use > 0 && !wait_bar(bar(Q_EMPTY + slot), (use - 1) & 1, g)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(Q_FULL + slot), (uint32_t)kBlk);
+          tma_load_2d(base + slot * kBlk, &maps.h2, kb * 64, tile * 128, bar(Q_FULL + slot));
+          cnt[0] = ++n;
+          if (++slot == kQR) { slot = 0; ++use; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = wait_bar(bar(Q_W3), 0, g) && wait_bar(bar(Q_W3T), 0, g);
+      uint32_t slot = 0, use = 0, qb = 0, qu = 0, t = 0;
+      const uint32_t idz = idesc_bf16(128, kQCP, false, false);
+      const uint32_t idq = idesc_bf16(128, 128, false, false);
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++t) {
+        // Z = H2 W3^T into [kQTZ, kQTZ + 16), block by block as they land,
+        // once the loss of the previous tile has read Z
+        if (t > 0 && !wait_bar(bar(Q_ZFREE), (t - 1) & 1, g)) break;
+        for (int kb = 0; kb < kQH2 / 64 && ok; ++kb) {
+          if (!wait_bar(bar(Q_FULL + slot), use & 1, g)) { ok = false; break; }
+          tc_fence_after();
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(tmem + kQTZ, sdesc_sw128(base + slot * kBlk + kk * 32, 16, 1024),
+                        sdesc_sw128(base + kQOffW3 + kb * kQCP * 128 + kk * 32, 16, 1024), idz,
+                        (kb | kk) ? 1u : 0u);
+          if (++slot == kQR) { slot = 0; ++use; }
+        }
+        if (!ok) break;
+        tc_commit(bar(Q_ZFULL));
+        // dP2 quarters = dz W3^T[rows of the quarter] (K = 16), each into the
+        // next free quarter buffer
+        if (!wait_bar(bar(Q_DZRDY), t & 1, g)) break;
+        for (int j = 0; j < 4 && ok; ++j) {
+          if (qu > 0 && !wait_bar(bar(Q_QFREE + qb), (qu - 1) & 1, g)) { ok = false; break; }
+          tc_fence_after();
+          tc_mma_bf16(tmem + qb * 128, sdesc_sw32(base + kQOffDZ, 256),
+                      sdesc_sw32(base + kQOffW3T + j * 128 * kQCP * 2, 256), idq, 0u);
+          tc_commit(bar(Q_QFULL + qb));
+          if (++qb == 3) { qb = 0; ++qu; }
+        }
+        if (!ok) break;
+        tc_commit(bar(Q_DZFREE));   // the dz tile has been read
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int gi = warp < 6 ? 0 : 1;   // which 64 columns of each quarter
+    const bool loss_w = gi == 0;
+    const int rl = q * 32 + lane;
+    const uint32_t lanes = (uint32_t)(q * 32) << 16;
+    const HeadMasks hm = masks.get();
+    uint32_t ts = 0, n0 = 0, qb = 0, qu = 0, t = 0;   // ring slot and number of the tile's block 0
+    int pend = -1;                            // slot of this warp's last dP2 store
+    // the slot of the previous dP2 store goes back once this warp's stores
+    // (that one, and the dz tile's for the loss warps) have read shared memory
+    auto release = [&]() {
+      if (pend >= 0) {
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        mbar_arrive(bar(Q_EMPTY + pend));
+        pend = -1;
+      }
+    };
+    float adz[32], at6[6], adl[4];   // loss warps: sums over their rows of all tiles
+#pragma unroll
+    for (int k = 0; k < 32; ++k) adz[k] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 6; ++k) at6[k] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) adl[k] = 0.f;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++t) {
+      const int row0 = tile * 128;
+      const int row = row0 + rl;
+      const bool rok = row < p.M;
+      const bool box_ok = row0 + q * 32 < p.M;   // boxes wholly below the last row are skipped
+      if (loss_w) {
+        RowIn in;
+        load_row_in(in, row, rok, p.shape, p.rows);
+        if (!wait_bar(bar(Q_ZFULL), t & 1, g)) break;
+        tc_fence_after();
+        float dzr[32], t6[6], dls[4];
+        loss_row_in<kQCP>(tmem + lanes + kQTZ, rok, p.shape, hm, p.lc, p.inv_mb, in, p.logstd,
+                          b3s, dzr, t6, dls);
+        tc_fence_before();
+        mbar_arrive(bar(Q_ZFREE));
+        // the dz tile is free once the previous tile's quarter products have
+        // read it (its store was checked by this warp's later stores)
+        if (t > 0 && !wait_bar(bar(Q_DZFREE), (t - 1) & 1, g)) break;
+        uint8_t* drow = DZ + rl * 32;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          uint4 u;
+          u.x = pack_bf16x2(dzr[8 * i + 0], dzr[8 * i + 1]);
+          u.y = pack_bf16x2(dzr[8 * i + 2], dzr[8 * i + 3]);
+          u.z = pack_bf16x2(dzr[8 * i + 4], dzr[8 * i + 5]);
+          u.w = pack_bf16x2(dzr[8 * i + 6], dzr[8 * i + 7]);
+          *reinterpret_cast<uint4*>(drow + ((i ^ ((rl >> 2) & 1)) << 4)) = u;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(Q_DZRDY));
+        __syncwarp();
+        if (lane == 0) {
+          if (box_ok) tma_store_2d(&maps.dz, smem_u32(DZ + q * 1024), 0, row0 + q * 32);
+          bulk_commit();
+        }
+#pragma unroll
+        for (int k = 0; k < kQCP; ++k) adz[k] += dzr[k];
+#pragma unroll
+        for (int k = 0; k < 6; ++k) at6[k] += t6[k];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) adl[k] += dls[k];
+      }
+      bool ok = true;
+      for (int j = 0; j < 4; ++j) {
+        const int kb = 2 * j + gi;
+        const int slot = ts + kb < kQR ? ts + kb : ts + kb - kQR;
+        uint8_t* blk = ring + slot * kBlk;
+        // the block's TMA load (complete: the quarter product ran after the
+        // head product read it) and the quarter's accumulator
+        if (!wait_bar(bar(Q_FULL + slot), ((n0 + kb) / kQR) & 1, g) ||
+            !wait_bar(bar(Q_QFULL + qb), qu & 1, g)) { ok = false; break; }
+        tc_fence_after();
+        epi_dact_block(tmem + lanes + qb * 128 + gi * 64, rl, rok, p.act, blk,
+                       cs2 + q * kQH2 + kb * 64, lane, release);
+        tc_fence_before();
+        mbar_arrive(bar(Q_QFREE + qb));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (box_ok) tma_store_2d(&maps.dp2, smem_u32(blk + q * 4096), kb * 64, row0 + q * 32);
+          bulk_commit();
+        }
+        pend = slot;
+        if (++qb == 3) { qb = 0; ++qu; }
+      }
+      if (!ok) break;
+      ts = ts + 8 < kQR ? ts + 8 : ts + 8 - kQR;
+      n0 += 8;
+    }
+    if (loss_w) loss_warp_reduce(adz, at6, adl, cs3 + q * 32, lp + q * kLossPartials, lane);
+    if (lane == 0) bulk_wait0();
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {   // loads in flight: the last kQR H2 blocks, W3, W3^T
+      const uint32_t n = cnt[0];
+      for (uint32_t l = n >= (uint32_t)kQR ? n - kQR : 0; l < n; ++l)
+        drain_wait(bar(Q_FULL + l % kQR), (l / kQR) & 1, p.timeout_ns);
+      drain_wait(bar(Q_W3), 0, p.timeout_ns);
+      drain_wait(bar(Q_W3T), 0, p.timeout_ns);
+    }
+    if (warp == 1 && lane == 0) {
+      tc_commit(bar(Q_DRAIN));
+      drain_wait(bar(Q_DRAIN), 0, p.timeout_ns);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (warp >= 2) {
+    const int et = threadIdx.x - 2 * kWarp;
+    auto quad = [&](const float* b, int ld, int c) {
+      return ((b[c] + b[ld + c]) + b[2 * ld + c]) + b[3 * ld + c];
+    };
+    for (int c = et; c < kQH2; c += kHEpi)
+      p.cs2[(int64_t)blockIdx.x * kQH2 + c] = quad(cs2, kQH2, c);
+    if (et < kQCP) p.cs3[(int64_t)blockIdx.x * kQCP + et] = quad(cs3, 32, et);
+    if (et < kLossPartials)
+      p.lossp[(int64_t)blockIdx.x * kLossPartials + et] = quad(lp, kLossPartials, et);
+  }
+}
+
 template <int H2, int CP>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(hl2_kernel<H2, CP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -353,15 +640,30 @@ cudaError_t launch_t(const HMaps& m, const HParams& p, int grid, cudaStream_t st
   return launch_pdl(hl2_kernel<H2, CP>, dim3(grid), dim3(kHThreads), (size_t)kSmemBytes, st, m, p);
 }
 
+template <class Masks>
+cudaError_t launch_q(const HMaps& m, const HParams& p, Masks masks, int grid, cudaStream_t st) {
+  return launch_pdl(hlq_kernel<Masks>, dim3(grid), dim3(kHThreads), (size_t)kQSmemBytes, st, m, p,
+                    masks);
+}
+
 }  // namespace
 
 bool hl2_supported(const NetShape& s) {
   return (s.H2 == 128 || s.H2 == 256 || s.H2 == 512) && (s.CP == 16 || s.CP == 32) && s.G <= 4;
 }
 
+bool hl2_preferred(const NetShape& s) {
+  return hl2_supported(s) && s.H2 == kQH2 && s.CP == kQCP;
+}
+
 cudaError_t hl2_prepare() {
-  const cudaError_t errs[] = {set_attr<128, 16>(), set_attr<128, 32>(), set_attr<256, 16>(),
-                              set_attr<256, 32>(), set_attr<512, 16>(), set_attr<512, 32>()};
+  const cudaError_t errs[] = {
+      set_attr<128, 16>(), set_attr<128, 32>(), set_attr<256, 16>(), set_attr<256, 32>(),
+      set_attr<512, 16>(), set_attr<512, 32>(),
+      cudaFuncSetAttribute(hlq_kernel<FixedMasks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kQSmemBytes),
+      cudaFuncSetAttribute(hlq_kernel<ShapeMasks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kQSmemBytes)};
   for (cudaError_t e : errs)
     if (e != cudaSuccess) return e;
   return cudaSuccess;
@@ -370,16 +672,24 @@ cudaError_t hl2_prepare() {
 cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int* grid_out) {
   const NetShape& s = f.s;
   if (!hl2_supported(s) || f.M < 1) return cudaErrorInvalidValue;
+  // H2 = 512 with 16 head columns: the quarter kernel (W3^T and dz in 32-byte rows)
+  const bool quarters = s.H2 == kQH2 && s.CP == kQCP;
   HMaps m;
   cudaError_t e;
   if ((e = tc_make_tmap(&m.h2, f.H2, s.H2, f.M, s.H2, 64, 128)) != cudaSuccess) return e;
   if ((e = tc_make_tmap_blocks(&m.w3, f.W3s, s.CP, s.H2, s.H2 / 64, s.CP, s.H2 / 64)) !=
       cudaSuccess)
     return e;
-  if ((e = tc_make_tmap(&m.w3t, f.W3Ts, 64, s.H2, f.ld3t, 64, s.H2 > 256 ? 256 : s.H2)) !=
-      cudaSuccess)
-    return e;
-  if ((e = tc_make_tmap(&m.dz, f.dZ, 64, f.M, f.lddz, 64, 32)) != cudaSuccess) return e;
+  if (quarters) {
+    if ((e = tc_make_tmap(&m.w3t, f.W3Ts, kQCP, s.H2, f.ld3t, kQCP, 256, 32)) != cudaSuccess)
+      return e;
+    if ((e = tc_make_tmap(&m.dz, f.dZ, kQCP, f.M, f.lddz, kQCP, 32, 32)) != cudaSuccess) return e;
+  } else {
+    if ((e = tc_make_tmap(&m.w3t, f.W3Ts, 64, s.H2, f.ld3t, 64, s.H2 > 256 ? 256 : s.H2)) !=
+        cudaSuccess)
+      return e;
+    if ((e = tc_make_tmap(&m.dz, f.dZ, 64, f.M, f.lddz, 64, 32)) != cudaSuccess) return e;
+  }
   if ((e = tc_make_tmap(&m.dp2, f.dP2, s.H2, f.M, s.H2, 64, 32)) != cudaSuccess) return e;
   HParams p{};
   p.M = f.M;
@@ -399,6 +709,9 @@ cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int*
   p.layout9222 = is_layout_9222(s) ? 1 : 0;
   const int grid = p.tiles < num_sms ? p.tiles : num_sms;
   if (grid_out) *grid_out = grid;
+  if (quarters)
+    return p.layout9222 ? launch_q(m, p, FixedMasks{}, grid, st)
+                        : launch_q(m, p, ShapeMasks{head_masks(s)}, grid, st);
   const bool c32 = s.CP == 32;
   switch (s.H2) {
     case 128: return c32 ? launch_t<128, 32>(m, p, grid, st) : launch_t<128, 16>(m, p, grid, st);

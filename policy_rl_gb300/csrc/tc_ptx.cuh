@@ -180,6 +180,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same for K-major operands in 32-byte swizzled rows (16 bf16 of K per
+// row, 8-row atoms of 256 bytes; swizzle mode 6): one MMA's K = 16 spans the
+// row, so the leading byte offset is unused and sbo = 256 for packed rows.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
+}
+
 // 32 lanes x 32 consecutive fp32 columns: thread t of the warp receives row
 // (lane base + t), columns [col, col+32).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {

@@ -290,6 +290,39 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool 
   });
 }
 
+// dP = acc * act'(H) for one warp's 32 rows (rl = row in the tile) of one
+// 64-column block: acc in TMEM columns [taddr, taddr + 64) of the warp's lane
+// quarter, H in `blk` (128 rows x 128 bytes, 128-byte swizzle), overwritten
+// in place by dP (bf16); the block's column sums are added to cs[0, 64).
+// mid() runs between the two 32-column chunks.
+template <class Mid>
+__device__ __forceinline__ void epi_dact_block(uint32_t taddr, int rl, bool rok, int act,
+                                               uint8_t* blk, float* cs, int lane, Mid&& mid) {
+  uint8_t* row = blk + rl * 128;
+  tmem_chunks<2>(taddr, 0, [&](const uint32_t (&r)[32], int c0) {
+    float v[32];
+    const int c16 = c0 / 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a4 = *reinterpret_cast<const uint4*>(row + (((c16 + i) ^ (rl & 7)) << 4));
+      const uint32_t w4[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        const float2 hv = unpack_bf16x2(w4[hh]);
+        const int j = 8 * i + 2 * hh;
+        const float d0 = act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
+        const float d1 = act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
+        v[j] = rok ? __uint_as_float(r[j]) * d0 : 0.f;
+        v[j + 1] = rok ? __uint_as_float(r[j + 1]) * d1 : 0.f;
+      }
+    }
+    put_row_chunks(row, rl, c16, v);
+    const float colsum = warp_reduce_scatter32(v);
+    cs[c0 + lane] += colsum;
+    if (c0 == 0) mid();
+  });
+}
+
 // The same with the column sums kept in registers: lane j of the warp holds
 // column tn * BN + h * PART + 32 k + j of column tile tn in csr[CPW tn + k]
 // (NT column tiles at most; the warp's part is PART = 32 CPW columns).
