@@ -357,8 +357,10 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
 // one tile buffer: the next tile's blocks land in slots as the current
 // tile's quarters are stored out of theirs, and its head product Z runs
 // block by block as they land.  TMEM: three rotating 128-column dP2 quarter
-// buffers in columns [0, 384) and Z in [384, 400).  W3^T (512 x 16) and the
-// dz tile (128 x 16) sit in 32-byte swizzled rows, W3 in 64-column blocks.
+// buffers in columns [0, 384) and Z in [384, 400).  W3 sits in 64-column
+// blocks of its 16 rows and is the B operand of both products: K-major for
+// Z = H2 W3^T, MN-major for dz W3.  The dz tile (128 x 16) is kept in
+// 32-byte swizzled rows.
 // Roles: warp 0 TMA, warp 1 MMA, warps 2..9 the dP2 epilogue (warps 2..5 the
 // first 64 columns of each quarter, warps 6..9 the second; TMEM lane quarter
 // q = warp % 4).  Warps 2..5 also run each tile's loss before its quarters.
@@ -366,11 +368,10 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
 // each epilogue warp checks that for its previous store half-way through its
 // next block, so no warp waits on a store it has just issued.  The loss
 // warps keep their loss sums and dz column sums in registers across tiles.
-constexpr int kQR = 11;                              // ring slots
+constexpr int kQR = 12;                              // ring slots
 constexpr int kQH2 = 512, kQCP = 16;
 constexpr int kQOffW3 = kQR * kBlk;                  // W3: 8 blocks of [16][64]
-constexpr int kQOffW3T = kQOffW3 + kQCP * kQH2 * 2;  // W3^T [512][16]
-constexpr int kQOffDZ = kQOffW3T + kQH2 * kQCP * 2;  // dz [128][16]
+constexpr int kQOffDZ = kQOffW3 + kQCP * kQH2 * 2;   // dz [128][16]
 constexpr int kQOffCtrl = kQOffDZ + 128 * kQCP * 2;
 constexpr int kQOffCs2 = kQOffCtrl + kCtrlBytes;     // [4][512]
 constexpr int kQOffCs3 = kQOffCs2 + 4 * kQH2 * 4;    // [4][32]
@@ -381,7 +382,7 @@ static_assert(kQSmemBytes <= 232448, "shared memory of the quarter kernel");
 constexpr uint32_t kQTZ = 384;   // TMEM column of Z
 
 enum QBar : int {
-  Q_FULL = 0, Q_EMPTY = kQR, Q_W3 = 2 * kQR, Q_W3T, Q_ZFULL, Q_ZFREE, Q_DZRDY, Q_DZFREE,
+  Q_FULL = 0, Q_EMPTY = kQR, Q_W3 = 2 * kQR, Q_ZFULL, Q_ZFREE, Q_DZRDY, Q_DZFREE,
   Q_QFULL, Q_QFREE = Q_QFULL + 3, Q_DRAIN = Q_QFREE + 3, Q_COUNT
 };
 static_assert(Q_COUNT * 8 + 32 <= kCtrlBytes, "barrier block");
@@ -412,7 +413,6 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
       mbar_init(bar(Q_EMPTY + b), kHGrp);   // the four warps storing the block
     }
     mbar_init(bar(Q_W3), 1);
-    mbar_init(bar(Q_W3T), 1);
     mbar_init(bar(Q_ZFULL), 1);
     mbar_init(bar(Q_ZFREE), kHGrp);
     mbar_init(bar(Q_DZRDY), kHGrp);
@@ -431,7 +431,6 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.h2);
     prefetch_tmap(&maps.w3);
-    prefetch_tmap(&maps.w3t);
   }
   tc_fence_before();
   __syncthreads();
@@ -448,9 +447,6 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
       bool ok = true;
       mbar_arrive_expect_tx(bar(Q_W3), (uint32_t)(kQCP * kQH2 * 2));
       tma_load_3d(base + kQOffW3, &maps.w3, 0, 0, 0, bar(Q_W3));
-      mbar_arrive_expect_tx(bar(Q_W3T), (uint32_t)(kQH2 * kQCP * 2));
-      tma_load_2d(base + kQOffW3T, &maps.w3t, 0, 0, bar(Q_W3T));
-      tma_load_2d(base + kQOffW3T + 256 * kQCP * 2, &maps.w3t, 0, 256, bar(Q_W3T));
       uint32_t n = 0, slot = 0, use = 0;   // blocks issued; ring position of the next
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
         for (int kb = 0; kb < kQH2 / 64; ++kb) {
@@ -464,10 +460,10 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = wait_bar(bar(Q_W3), 0, g) && wait_bar(bar(Q_W3T), 0, g);
+      bool ok = wait_bar(bar(Q_W3), 0, g);
       uint32_t slot = 0, use = 0, qb = 0, qu = 0, t = 0;
       const uint32_t idz = idesc_bf16(128, kQCP, false, false);
-      const uint32_t idq = idesc_bf16(128, 128, false, false);
+      const uint32_t idq = idesc_bf16(128, 128, false, true);   // B = W3, MN-major
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++t) {
         // Z = H2 W3^T into [kQTZ, kQTZ + 16), block by block as they land,
         // once the loss of the previous tile has read Z
@@ -483,14 +479,17 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
         }
         if (!ok) break;
         tc_commit(bar(Q_ZFULL));
-        // dP2 quarters = dz W3^T[rows of the quarter] (K = 16), each into the
-        // next free quarter buffer
+        // dP2 quarters = dz W3[:, columns of the quarter] (K = 16), each into
+        // the next free quarter buffer; B spans two 64-column blocks of W3
+        // (leading byte offset: one block) and its 16 rows (stride byte
+        // offset: 8 rows of 128 bytes)
         if (!wait_bar(bar(Q_DZRDY), t & 1, g)) break;
         for (int j = 0; j < 4 && ok; ++j) {
           if (qu > 0 && !wait_bar(bar(Q_QFREE + qb), (qu - 1) & 1, g)) { ok = false; break; }
           tc_fence_after();
           tc_mma_bf16(tmem + qb * 128, sdesc_sw32(base + kQOffDZ, 256),
-                      sdesc_sw32(base + kQOffW3T + j * 128 * kQCP * 2, 256), idq, 0u);
+                      sdesc_sw128(base + kQOffW3 + 2 * j * kQCP * 128, kQCP * 128, 1024), idq,
+                      0u);
           tc_commit(bar(Q_QFULL + qb));
           if (++qb == 3) { qb = 0; ++qu; }
         }
@@ -524,14 +523,16 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
     for (int k = 0; k < 6; ++k) at6[k] = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) adl[k] = 0.f;
+    // loss warps: the per-row inputs of the loss, loaded one tile ahead (their
+    // latency then overlaps this tile's quarters)
+    RowIn in;
+    if (loss_w) load_row_in(in, blockIdx.x * 128 + rl, blockIdx.x * 128 + rl < p.M, p.shape, p.rows);
     for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++t) {
       const int row0 = tile * 128;
       const int row = row0 + rl;
       const bool rok = row < p.M;
       const bool box_ok = row0 + q * 32 < p.M;   // boxes wholly below the last row are skipped
       if (loss_w) {
-        RowIn in;
-        load_row_in(in, row, rok, p.shape, p.rows);
         if (!wait_bar(bar(Q_ZFULL), t & 1, g)) break;
         tc_fence_after();
         float dzr[32], t6[6], dls[4];
@@ -565,6 +566,8 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
         for (int k = 0; k < 6; ++k) at6[k] += t6[k];
 #pragma unroll
         for (int k = 0; k < 4; ++k) adl[k] += dls[k];
+        const int nrow = row + (int)gridDim.x * 128;
+        if (tile + (int)gridDim.x < p.tiles) load_row_in(in, nrow, nrow < p.M, p.shape, p.rows);
       }
       bool ok = true;
       for (int j = 0; j < 4; ++j) {
@@ -599,12 +602,11 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
 
   __syncthreads();
   if (*abort_flag) {
-    if (threadIdx.x == 0) {   // loads in flight: the last kQR H2 blocks, W3, W3^T
+    if (threadIdx.x == 0) {   // loads in flight: the last kQR H2 blocks and W3
       const uint32_t n = cnt[0];
       for (uint32_t l = n >= (uint32_t)kQR ? n - kQR : 0; l < n; ++l)
         drain_wait(bar(Q_FULL + l % kQR), (l / kQR) & 1, p.timeout_ns);
       drain_wait(bar(Q_W3), 0, p.timeout_ns);
-      drain_wait(bar(Q_W3T), 0, p.timeout_ns);
     }
     if (warp == 1 && lane == 0) {
       tc_commit(bar(Q_DRAIN));
@@ -672,7 +674,7 @@ cudaError_t hl2_prepare() {
 cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int* grid_out) {
   const NetShape& s = f.s;
   if (!hl2_supported(s) || f.M < 1) return cudaErrorInvalidValue;
-  // H2 = 512 with 16 head columns: the quarter kernel (W3^T and dz in 32-byte rows)
+  // H2 = 512 with 16 head columns: the quarter kernel (dz in 32-byte rows)
   const bool quarters = s.H2 == kQH2 && s.CP == kQCP;
   HMaps m;
   cudaError_t e;
@@ -680,9 +682,8 @@ cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int*
   if ((e = tc_make_tmap_blocks(&m.w3, f.W3s, s.CP, s.H2, s.H2 / 64, s.CP, s.H2 / 64)) !=
       cudaSuccess)
     return e;
-  if (quarters) {
-    if ((e = tc_make_tmap(&m.w3t, f.W3Ts, kQCP, s.H2, f.ld3t, kQCP, 256, 32)) != cudaSuccess)
-      return e;
+  if (quarters) {   // (no W3^T map: the kernel reads W3 for both products)
+    m.w3t = m.w3;
     if ((e = tc_make_tmap(&m.dz, f.dZ, kQCP, f.M, f.lddz, kQCP, 32, 32)) != cudaSuccess) return e;
   } else {
     if ((e = tc_make_tmap(&m.w3t, f.W3Ts, 64, s.H2, f.ld3t, 64, s.H2 > 256 ? 256 : s.H2)) !=
