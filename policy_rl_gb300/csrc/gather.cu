@@ -38,17 +38,10 @@ pack_kernel(const float* __restrict__ obs, int64_t B, int D, int Dp,
 }
 
 constexpr int kGatherThreads = 256;
+constexpr int kGatherRows = 4;   // rows per thread: four independent loads in flight
 
-// One thread per 8-element chunk of a row (bf16 output) or per element (fp32
-// output); the thread holding chunk 0 of a row also copies the row's side data.
-__global__ void __launch_bounds__(kGatherThreads)
-gather_kernel(NetShape s, GatherArgs a, int per_row) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t t = (int64_t)blockIdx.x * kGatherThreads + threadIdx.x;
-  const int64_t r = t / per_row;
-  const int c = (int)(t - r * per_row);
-  if (r >= a.mb) return;
+// Source row of minibatch row r, clamped into the batch.
+__device__ __forceinline__ int64_t gather_src(const GatherArgs& a, int64_t r) {
   int64_t src;
   if (a.seg_envs) {
     const int64_t per = (int64_t)a.seg_T * a.seg_ns;
@@ -62,48 +55,96 @@ gather_kernel(NetShape s, GatherArgs a, int per_row) {
   } else {
     src = __ldg(a.idx + r);
   }
-  src = src < 0 ? 0 : (src >= a.B ? a.B - 1 : src);   // never read outside the batch
-  if (a.obs_bf16) {
-    const uint4* in = reinterpret_cast<const uint4*>(a.obs_bf16 + src * s.Dp);
-    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.X) + r * s.Dp)[c] = __ldg(in + c);
-  } else if (a.x_bf16) {
-    const float* in = a.obs_f32 + src * s.D;
-    float f[8];
+  return src < 0 ? 0 : (src >= a.B ? a.B - 1 : src);   // never read outside the batch
+}
+
+// One thread per 8-element chunk (bf16 output) or element (fp32 output) of
+// kGatherRows consecutive minibatch rows, all loads issued before any store;
+// the threads holding chunks 0 .. kGatherRows-1 also copy the rows' side data.
+// MODE: 0 packed bf16 observations, 1 fp32 observations to bf16, 2 fp32.
+template <int MODE>
+__global__ void __launch_bounds__(kGatherThreads)
+gather_kernel(NetShape s, GatherArgs a, int per_row) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t t = (int64_t)blockIdx.x * kGatherThreads + threadIdx.x;
+  const int64_t grp = t / per_row;
+  const int c = (int)(t - grp * per_row);
+  const int64_t r0 = grp * kGatherRows;
+  if (r0 >= a.mb) return;
+  const int nr = a.mb - r0 < kGatherRows ? (int)(a.mb - r0) : kGatherRows;
+  int64_t src[kGatherRows];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) f[j] = (8 * c + j < s.D) ? __ldg(in + 8 * c + j) : 0.f;
-    uint4 o;
-    o.x = pack_bf16x2(f[0], f[1]);
-    o.y = pack_bf16x2(f[2], f[3]);
-    o.z = pack_bf16x2(f[4], f[5]);
-    o.w = pack_bf16x2(f[6], f[7]);
-    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.X) + r * s.Dp)[c] = o;
+  for (int k = 0; k < kGatherRows; ++k) src[k] = k < nr ? gather_src(a, r0 + k) : 0;
+  if constexpr (MODE == 0) {
+    uint4 x[kGatherRows];
+#pragma unroll
+    for (int k = 0; k < kGatherRows; ++k)
+      if (k < nr) x[k] = __ldg(reinterpret_cast<const uint4*>(a.obs_bf16 + src[k] * s.Dp) + c);
+#pragma unroll
+    for (int k = 0; k < kGatherRows; ++k)
+      if (k < nr)
+        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.X) + (r0 + k) * s.Dp)[c] = x[k];
+  } else if constexpr (MODE == 1) {
+    float f[kGatherRows][8];
+#pragma unroll
+    for (int k = 0; k < kGatherRows; ++k) {
+      const float* in = a.obs_f32 + src[k] * s.D;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[k][j] = (k < nr && 8 * c + j < s.D) ? __ldg(in + 8 * c + j) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kGatherRows; ++k) {
+      if (k >= nr) continue;
+      uint4 o;
+      o.x = pack_bf16x2(f[k][0], f[k][1]);
+      o.y = pack_bf16x2(f[k][2], f[k][3]);
+      o.z = pack_bf16x2(f[k][4], f[k][5]);
+      o.w = pack_bf16x2(f[k][6], f[k][7]);
+      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.X) + (r0 + k) * s.Dp)[c] = o;
+    }
   } else {
-    static_cast<float*>(a.X)[r * s.D + c] = __ldg(a.obs_f32 + src * s.D + c);
+    float x[kGatherRows];
+#pragma unroll
+    for (int k = 0; k < kGatherRows; ++k) x[k] = k < nr ? __ldg(a.obs_f32 + src[k] * s.D + c) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kGatherRows; ++k)
+      if (k < nr) static_cast<float*>(a.X)[(r0 + k) * s.D + c] = x[k];
   }
-  if (c != 0) return;
-  // side data: every load is issued before any store
-  int32_t act[PPO_MAX_HEADS];
-  float actc[4];
-  for (int h = 0; h < s.NH; ++h) act[h] = __ldg(a.act + src * s.NH + h);
-  for (int g = 0; g < s.G; ++g) actc[g] = __ldg(a.actc + src * s.G + g);
-  const float lp = __ldg(a.logp_old + src);
-  float A = 0.f, R = 0.f;
-  if (a.adv) {   // no advantages when they are computed per minibatch later
-    A = __ldg(a.adv + src);
-    R = __ldg(a.ret + src);
-    if (a.adv_stats) A = (A - __ldg(a.adv_stats)) / (__ldg(a.adv_stats + 1) + 1e-8f);
-  }
-  for (int h = 0; h < s.NH; ++h) {
-    // an out-of-range action is clamped into its head so the loss never
-    // indexes outside the head's logits
-    const int n = s.head_n[h];
-    a.act_mb[r * s.NH + h] = act[h] < 0 ? 0 : (act[h] >= n ? n - 1 : act[h]);
-  }
-  for (int g = 0; g < s.G; ++g) a.actc_mb[r * s.G + g] = actc[g];
-  a.logp_mb[r] = lp;
-  if (a.adv) {
-    a.adv_mb[r] = A;
-    a.ret_mb[r] = R;
+  // side data: thread c copies that of row r0 + c (rows taken in turn if a
+  // row has fewer than kGatherRows threads), every load before any store
+  for (int k = c; k < nr; k += per_row) {
+    const int64_t sr = k == 0 ? src[0] : (k == 1 ? src[1] : (k == 2 ? src[2] : src[3]));
+    const int64_t r = r0 + k;
+    int32_t act[PPO_MAX_HEADS];
+    float actc[4];
+#pragma unroll
+    for (int h = 0; h < PPO_MAX_HEADS; ++h) act[h] = h < s.NH ? __ldg(a.act + sr * s.NH + h) : 0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) actc[g] = g < s.G ? __ldg(a.actc + sr * s.G + g) : 0.f;
+    const float lp = __ldg(a.logp_old + sr);
+    float A = 0.f, R = 0.f;
+    if (a.adv) {   // no advantages when they are computed per minibatch later
+      A = __ldg(a.adv + sr);
+      R = __ldg(a.ret + sr);
+      if (a.adv_stats) A = (A - __ldg(a.adv_stats)) / (__ldg(a.adv_stats + 1) + 1e-8f);
+    }
+#pragma unroll
+    for (int h = 0; h < PPO_MAX_HEADS; ++h) {
+      // an out-of-range action is clamped into its head so the loss never
+      // indexes outside the head's logits
+      if (h >= s.NH) break;
+      const int n = s.head_n[h];
+      a.act_mb[r * s.NH + h] = act[h] < 0 ? 0 : (act[h] >= n ? n - 1 : act[h]);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (g < s.G) a.actc_mb[r * s.G + g] = actc[g];
+    a.logp_mb[r] = lp;
+    if (a.adv) {
+      a.adv_mb[r] = A;
+      a.ret_mb[r] = R;
+    }
   }
 }
 
@@ -121,9 +162,15 @@ cudaError_t launch_pack_obs(const float* obs, int64_t B, int D, int Dp, __nv_bfl
 
 cudaError_t launch_gather(const NetShape& s, const GatherArgs& a, cudaStream_t st) {
   const int per_row = (a.obs_bf16 || a.x_bf16) ? s.Dp / 8 : s.D;
-  const int64_t threads = a.mb * per_row;
+  const int64_t threads = (a.mb + kGatherRows - 1) / kGatherRows * per_row;
   const int64_t blocks = (threads + kGatherThreads - 1) / kGatherThreads;
-  return launch_pdl(gather_kernel, dim3((unsigned)blocks), dim3(kGatherThreads), 0, st, s, a,
+  if (a.obs_bf16)
+    return launch_pdl(gather_kernel<0>, dim3((unsigned)blocks), dim3(kGatherThreads), 0, st, s, a,
+                      per_row);
+  if (a.x_bf16)
+    return launch_pdl(gather_kernel<1>, dim3((unsigned)blocks), dim3(kGatherThreads), 0, st, s, a,
+                      per_row);
+  return launch_pdl(gather_kernel<2>, dim3((unsigned)blocks), dim3(kGatherThreads), 0, st, s, a,
                     per_row);
 }
 
