@@ -197,10 +197,11 @@ NCU_TRAFFIC = {
     ("mario", "fwd1_gemm"): 4.26e6, ("mario", "fwd2_gemm"): 16.94e6,
     ("mario", "head_loss_gemm"): 17.78e6, ("mario", "dact2_gemm"): 21.05e6,
     ("mario", "dact1_gemm"): 33.73e6, ("mario", "wgrad_gemm"): 76.15e6,
-    ("large", "fwd1_gemm"): 279.80e6, ("large", "fwd2_gemm"): 487.82e6,
+    ("large", "fwd1_gemm"): 279.56e6, ("large", "fwd2_gemm"): 487.96e6,
+    ("large", "head_loss_dact2"): 495.39e6, ("large", "dact1_gemm"): 837.59e6,
+    ("large", "wgrad_gemm"): 1192.21e6,
+    # the two-kernel head + loss / dP2 path (fused_loss = -1), earlier capture
     ("large", "head_loss_gemm"): 280.92e6, ("large", "dact2_gemm"): 518.69e6,
-    ("large", "dact1_gemm"): 835.31e6, ("large", "wgrad_gemm"): 1190.63e6,
-    ("large", "head_loss_dact2"): 497.02e6,
 }
 
 

@@ -579,8 +579,8 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
         if (!wait_bar(bar(Q_FULL + slot), ((n0 + kb) / kQR) & 1, g) ||
             !wait_bar(bar(Q_QFULL + qb), qu & 1, g)) { ok = false; break; }
         tc_fence_after();
-        epi_dact_block(tmem + lanes + qb * 128 + gi * 64, rl, rok, p.act, blk,
-                       cs2 + q * kQH2 + kb * 64, lane, release);
+        epi_dact_block(tmem + lanes + qb * 128 + gi * 64, rl, p.act, blk, cs2 + q * kQH2 + kb * 64,
+                       lane, release);
         tc_fence_before();
         mbar_arrive(bar(Q_QFREE + qb));
         fence_proxy_async_smem();

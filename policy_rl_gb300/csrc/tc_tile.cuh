@@ -294,10 +294,12 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool 
 // 64-column block: acc in TMEM columns [taddr, taddr + 64) of the warp's lane
 // quarter, H in `blk` (128 rows x 128 bytes, 128-byte swizzle), overwritten
 // in place by dP (bf16); the block's column sums are added to cs[0, 64).
+// Rows past the last one need no masking: their H rows are TMA zero fill and
+// their accumulator rows are zero (a zero dz row), so dP is zero there.
 // mid() runs between the two 32-column chunks.
 template <class Mid>
-__device__ __forceinline__ void epi_dact_block(uint32_t taddr, int rl, bool rok, int act,
-                                               uint8_t* blk, float* cs, int lane, Mid&& mid) {
+__device__ __forceinline__ void epi_dact_block(uint32_t taddr, int rl, int act, uint8_t* blk,
+                                               float* cs, int lane, Mid&& mid) {
   uint8_t* row = blk + rl * 128;
   tmem_chunks<2>(taddr, 0, [&](const uint32_t (&r)[32], int c0) {
     float v[32];
@@ -312,8 +314,8 @@ __device__ __forceinline__ void epi_dact_block(uint32_t taddr, int rl, bool rok,
         const int j = 8 * i + 2 * hh;
         const float d0 = act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
         const float d1 = act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
-        v[j] = rok ? __uint_as_float(r[j]) * d0 : 0.f;
-        v[j + 1] = rok ? __uint_as_float(r[j + 1]) * d1 : 0.f;
+        v[j] = __uint_as_float(r[j]) * d0;
+        v[j + 1] = __uint_as_float(r[j + 1]) * d1;
       }
     }
     put_row_chunks(row, rl, c16, v);
