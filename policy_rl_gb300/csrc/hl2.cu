@@ -360,7 +360,9 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
 // buffers in columns [0, 384) and Z in [384, 400).  W3 sits in 64-column
 // blocks of its 16 rows and is the B operand of both products: K-major for
 // Z = H2 W3^T, MN-major for dz W3.  The dz tile (128 x 16) is kept in
-// 32-byte swizzled rows.
+// 32-byte swizzled rows, with a negated copy that is the A operand of the
+// dP2 product: the epilogue then forms dP2 with two packed fp32-pair
+// instructions per pair of columns.
 // Roles: warp 0 TMA, warp 1 MMA, warps 2..9 the dP2 epilogue (warps 2..5 the
 // first 64 columns of each quarter, warps 6..9 the second; TMEM lane quarter
 // q = warp % 4).  Warps 2..5 also run each tile's loss before its quarters.
@@ -371,8 +373,9 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
 constexpr int kQR = 12;                              // ring slots
 constexpr int kQH2 = 512, kQCP = 16;
 constexpr int kQOffW3 = kQR * kBlk;                  // W3: 8 blocks of [16][64]
-constexpr int kQOffDZ = kQOffW3 + kQCP * kQH2 * 2;   // dz [128][16]
-constexpr int kQOffCtrl = kQOffDZ + 128 * kQCP * 2;
+constexpr int kQOffDZ = kQOffW3 + kQCP * kQH2 * 2;   // dz [128][16] (stored out)
+constexpr int kQOffNDZ = kQOffDZ + 128 * kQCP * 2;   // -dz, the A operand of the dP2 product
+constexpr int kQOffCtrl = kQOffNDZ + 128 * kQCP * 2;
 constexpr int kQOffCs2 = kQOffCtrl + kCtrlBytes;     // [4][512]
 constexpr int kQOffCs3 = kQOffCs2 + 4 * kQH2 * 4;    // [4][32]
 constexpr int kQOffLp = kQOffCs3 + 4 * 32 * 4;       // [4][kLossPartials]
@@ -487,7 +490,7 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
         for (int j = 0; j < 4 && ok; ++j) {
           if (qu > 0 && !wait_bar(bar(Q_QFREE + qb), (qu - 1) & 1, g)) { ok = false; break; }
           tc_fence_after();
-          tc_mma_bf16(tmem + qb * 128, sdesc_sw32(base + kQOffDZ, 256),
+          tc_mma_bf16(tmem + qb * 128, sdesc_sw32(base + kQOffNDZ, 256),
                       sdesc_sw128(base + kQOffW3 + 2 * j * kQCP * 128, kQCP * 128, 1024), idq,
                       0u);
           tc_commit(bar(Q_QFULL + qb));
@@ -551,7 +554,11 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
           u.y = pack_bf16x2(dzr[8 * i + 2], dzr[8 * i + 3]);
           u.z = pack_bf16x2(dzr[8 * i + 4], dzr[8 * i + 5]);
           u.w = pack_bf16x2(dzr[8 * i + 6], dzr[8 * i + 7]);
-          *reinterpret_cast<uint4*>(drow + ((i ^ ((rl >> 2) & 1)) << 4)) = u;
+          const int off = (i ^ ((rl >> 2) & 1)) << 4;
+          *reinterpret_cast<uint4*>(drow + off) = u;
+          constexpr uint32_t kSign = 0x80008000u;   // -dz: both bf16 sign bits flipped
+          *reinterpret_cast<uint4*>(drow + (kQOffNDZ - kQOffDZ) + off) =
+              make_uint4(u.x ^ kSign, u.y ^ kSign, u.z ^ kSign, u.w ^ kSign);
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(Q_DZRDY));

@@ -290,13 +290,15 @@ __device__ __forceinline__ void epi_dact_smem_tile(uint32_t taddr, int rl, bool 
   });
 }
 
-// dP = acc * act'(H) for one warp's 32 rows (rl = row in the tile) of one
-// 64-column block: acc in TMEM columns [taddr, taddr + 64) of the warp's lane
-// quarter, H in `blk` (128 rows x 128 bytes, 128-byte swizzle), overwritten
-// in place by dP (bf16); the block's column sums are added to cs[0, 64).
-// Rows past the last one need no masking: their H rows are TMA zero fill and
-// their accumulator rows are zero (a zero dz row), so dP is zero there.
-// mid() runs between the two 32-column chunks.
+// dP = a * act'(H) for one warp's 32 rows (rl = row in the tile) of one
+// 64-column block, from the NEGATED accumulator -a in TMEM columns
+// [taddr, taddr + 64) of the warp's lane quarter (the product was run with
+// -dz): for tanh, dP = (-a) * (H^2 - 1) in packed fp32 pairs, which rounds
+// exactly as a * (1 - H^2) does.  H is in `blk` (128 rows x 128 bytes,
+// 128-byte swizzle), overwritten in place by dP (bf16); the block's column
+// sums are added to cs[0, 64).  Rows past the last one need no masking:
+// their H rows are TMA zero fill and their accumulator rows are zero (a zero
+// dz row), so dP is zero there.  mid() runs between the two 32-column chunks.
 template <class Mid>
 __device__ __forceinline__ void epi_dact_block(uint32_t taddr, int rl, int act, uint8_t* blk,
                                                float* cs, int lane, Mid&& mid) {
@@ -311,11 +313,17 @@ __device__ __forceinline__ void epi_dact_block(uint32_t taddr, int rl, int act, 
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {
         const float2 hv = unpack_bf16x2(w4[hh]);
-        const int j = 8 * i + 2 * hh;
-        const float d0 = act == 0 ? 1.f - hv.x * hv.x : (hv.x > 0.f ? 1.f : 0.f);
-        const float d1 = act == 0 ? 1.f - hv.y * hv.y : (hv.y > 0.f ? 1.f : 0.f);
-        v[j] = __uint_as_float(r[j]) * d0;
-        v[j + 1] = __uint_as_float(r[j + 1]) * d1;
+        const float2 na = make_float2(__uint_as_float(r[8 * i + 2 * hh]),
+                                      __uint_as_float(r[8 * i + 2 * hh + 1]));
+        float2 dp;
+        if (act == 0) {
+          dp = fmul2(na, ffma2(hv, hv, make_float2(-1.f, -1.f)));
+        } else {
+          dp.x = hv.x > 0.f ? -na.x : 0.f;
+          dp.y = hv.y > 0.f ? -na.y : 0.f;
+        }
+        v[8 * i + 2 * hh] = dp.x;
+        v[8 * i + 2 * hh + 1] = dp.y;
       }
     }
     put_row_chunks(row, rl, c16, v);
