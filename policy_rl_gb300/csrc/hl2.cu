@@ -5,23 +5,30 @@
 //   dP2 = (dz W3) * act'(H2)                            (N = H2, K = CP)
 //
 // "Teaching Mario to speedrun", sec. 6 (loss_pi, loss_V, entropy and
-// loss.backward() through the policy/value head).  The tile's H2 (up to
-// 128 x 512 bf16 = 128 KB) is loaded once by TMA and stays in shared memory:
-// it is the A operand of the head product and the activation operand of
-// act'(H2), and dP2 is written back over it in place and leaves by TMA
-// stores.  For H2 <= 256 two tiles fit, so the next tile's H2 is loaded while
-// the current one is processed.  dz goes to a 128 x 64 shared tile (the A operand of dz W3, K = CP)
-// and to HBM for the weight gradient of W3.  W3 is resident for the whole
-// kernel; W3^T streams in 256-row boxes.  Compared with a head+loss kernel
-// followed by a separate backward-data kernel this reads H2 once instead of
-// twice and drops the dz round trip and one launch.
+// loss.backward() through the policy/value head).  Each tile of H2 is loaded
+// once by TMA: it is the A operand of the head product and the activation
+// operand of act'(H2), and dP2 is written back over it in place and leaves by
+// TMA stores.  dz stays in shared memory as the A operand of dz W3 (K = CP)
+// and goes to HBM for the weight gradient of W3.  Compared with a head+loss
+// kernel followed by a separate backward-data kernel this reads H2 once
+// instead of twice and drops the dz round trip and one launch.
 //
-// Roles: warp 0 TMA, warp 1 MMA, warps 2..5 the loss and warps 6..9 the dP2
-// epilogue (TMEM lane quarter q = warp % 4 in each group), so that the loss of
-// one tile overlaps the dP2 epilogue of the previous one.  With H2 = 512 only
-// one tile fits and the loss warps then work on dP2 as well.  TMEM: R_A = columns [0, 256) holds Z (first
-// CP columns) and then the second 256-column half of dP2 (H2 = 512); R_B =
-// [256, 512) holds the first half of dP2.  Every wait is bounded.
+// Two kernels:
+//  - hlq_kernel (H2 = 512, CP = 16; below): H2 streams through a ring of
+//    64-column blocks and dP2 comes in 128-column quarters, so that the next
+//    tile's head product and loss overlap this tile's epilogue.
+//  - hl2_kernel (the other shapes): the whole tile stays in shared memory.
+//    For H2 <= 256 two tiles fit, so the next tile's H2 is loaded while the
+//    current one is processed.  dz goes to a 128 x 64 shared tile; W3 is
+//    resident for the whole kernel and W3^T streams in 256-row boxes.
+//    Roles: warp 0 TMA, warp 1 MMA, warps 2..5 the loss and warps 6..9 the
+//    dP2 epilogue (TMEM lane quarter q = warp % 4 in each group), so that the
+//    loss of one tile overlaps the dP2 epilogue of the previous one.  With
+//    H2 = 512 only one tile fits and the loss warps then work on dP2 as well.
+//    TMEM: R_A = columns [0, 256) holds Z (first CP columns) and then the
+//    second 256-column half of dP2 (H2 = 512); R_B = [256, 512) holds the
+//    first half of dP2.
+// Every wait is bounded.
 #include <cuda.h>
 
 #include "common.cuh"
