@@ -106,8 +106,8 @@ typedef struct {
                                     that reads each tile of H2 once, or as two
                                     kernels.  -1: two kernels; 0 (default):
                                     one kernel where it is the faster choice
-                                    (H2 = 512 with at most 16 head columns),
-                                    else two; 1: one kernel wherever it
+                                    (H2 = 256 or 512 with at most 16 head
+                                    columns), else two; 1: one kernel wherever it
                                     applies (H2 in {128, 256, 512}, at most 32
                                     head columns).  Same results up to fp32
                                     summation order.                         */

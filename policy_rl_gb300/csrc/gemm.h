@@ -351,7 +351,7 @@ struct HeadLossDact {
   uint64_t timeout_ns;
 };
 bool hl2_supported(const NetShape& s);
-// shapes where the fused kernel beats the two-kernel path (H2 = 512, CP = 16)
+// shapes where the fused kernel beats the two-kernel path (H2 = 256 or 512, CP = 16)
 bool hl2_preferred(const NetShape& s);
 cudaError_t hl2_prepare();
 cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int* grid_out);

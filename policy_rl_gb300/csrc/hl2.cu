@@ -14,7 +14,7 @@
 // instead of twice and drops the dz round trip and one launch.
 //
 // Two kernels:
-//  - hlq_kernel (H2 = 512, CP = 16; below): H2 streams through a ring of
+//  - hlq_kernel (H2 = 256 or 512, CP = 16; below): H2 streams through a ring of
 //    64-column blocks and dP2 comes in 128-column quarters, so that the next
 //    tile's head product and loss overlap this tile's epilogue.
 //  - hl2_kernel (the other shapes): the whole tile stays in shared memory.
@@ -357,8 +357,9 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// H2 = 512, CP = 16: a tile's dP2 in four 128-column quarters, so that the
-// next tile's head product and loss overlap this tile's dP2 epilogue.
+// H2 = 256 or 512, CP = 16: a tile's dP2 in 128-column quarters (two or
+// four), so that the next tile's head product and loss overlap this tile's
+// dP2 epilogue.
 //
 // H2 streams through a ring of kQR 64-column blocks (16 KB each) instead of
 // one tile buffer: the next tile's blocks land in slots as the current
@@ -377,18 +378,22 @@ hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
 // each epilogue warp checks that for its previous store half-way through its
 // next block, so no warp waits on a store it has just issued.  The loss
 // warps keep their loss sums and dz column sums in registers across tiles.
-constexpr int kQR = 12;                              // ring slots
-constexpr int kQH2 = 512, kQCP = 16;
-constexpr int kQOffW3 = kQR * kBlk;                  // W3: 8 blocks of [16][64]
-constexpr int kQOffDZ = kQOffW3 + kQCP * kQH2 * 2;   // dz [128][16] (stored out)
-constexpr int kQOffNDZ = kQOffDZ + 128 * kQCP * 2;   // -dz, the A operand of the dP2 product
-constexpr int kQOffCtrl = kQOffNDZ + 128 * kQCP * 2;
-constexpr int kQOffCs2 = kQOffCtrl + kCtrlBytes;     // [4][512]
-constexpr int kQOffCs3 = kQOffCs2 + 4 * kQH2 * 4;    // [4][32]
-constexpr int kQOffLp = kQOffCs3 + 4 * 32 * 4;       // [4][kLossPartials]
-constexpr int kQOffB3 = kQOffLp + 4 * kLossPartials * 4;
-constexpr int kQSmemBytes = 1024 + kQOffB3 + 32 * 4;
-static_assert(kQSmemBytes <= 232448, "shared memory of the quarter kernel");
+constexpr int kQR = 12;   // ring slots
+constexpr int kQCP = 16;
+// shared-memory layout for H2 = QH2 (256 or 512) columns
+template <int QH2>
+struct QL {
+  static constexpr int W3 = kQR * kBlk;             // W3: QH2/64 blocks of [16][64]
+  static constexpr int DZ = W3 + kQCP * QH2 * 2;    // dz [128][16] (stored out)
+  static constexpr int NDZ = DZ + 128 * kQCP * 2;   // -dz, the A operand of the dP2 product
+  static constexpr int Ctrl = NDZ + 128 * kQCP * 2;
+  static constexpr int Cs2 = Ctrl + kCtrlBytes;     // [4][QH2]
+  static constexpr int Cs3 = Cs2 + 4 * QH2 * 4;     // [4][32]
+  static constexpr int Lp = Cs3 + 4 * 32 * 4;       // [4][kLossPartials]
+  static constexpr int B3 = Lp + 4 * kLossPartials * 4;
+  static constexpr int Smem = 1024 + B3 + 32 * 4;
+  static_assert(Smem <= 232448, "shared memory of the quarter kernel");
+};
 constexpr uint32_t kQTZ = 384;   // TMEM column of Z
 
 enum QBar : int {
@@ -397,23 +402,26 @@ enum QBar : int {
 };
 static_assert(Q_COUNT * 8 + 32 <= kCtrlBytes, "barrier block");
 
-template <class Masks>
+template <int QH2, class Masks>
 __global__ void __launch_bounds__(kHThreads, 1)
 hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
+  using L = QL<QH2>;
+  constexpr int NB = QH2 / 64;    // H2 blocks per tile
+  constexpr int NQ = QH2 / 128;   // dP2 quarters per tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (base - raw);
   uint8_t* ring = gb;
-  uint8_t* DZ = gb + kQOffDZ;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gb + kQOffCtrl);
+  uint8_t* DZ = gb + L::DZ;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gb + L::Ctrl);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + Q_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);   // H2 blocks issued
-  float* cs2 = reinterpret_cast<float*>(gb + kQOffCs2);
-  float* cs3 = reinterpret_cast<float*>(gb + kQOffCs3);
-  float* lp = reinterpret_cast<float*>(gb + kQOffLp);
-  float* b3s = reinterpret_cast<float*>(gb + kQOffB3);
+  float* cs2 = reinterpret_cast<float*>(gb + L::Cs2);
+  float* cs3 = reinterpret_cast<float*>(gb + L::Cs3);
+  float* lp = reinterpret_cast<float*>(gb + L::Lp);
+  float* b3s = reinterpret_cast<float*>(gb + L::B3);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -436,7 +444,7 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
     cnt[0] = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < (kQOffB3 - kQOffCs2) / 4; i += kHThreads) cs2[i] = 0.f;
+  for (int i = threadIdx.x; i < (L::B3 - L::Cs2) / 4; i += kHThreads) cs2[i] = 0.f;
   if (warp == 1) tmem_alloc(smem_u32(tslot), 512);
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.h2);
@@ -455,11 +463,11 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      mbar_arrive_expect_tx(bar(Q_W3), (uint32_t)(kQCP * kQH2 * 2));
-      tma_load_3d(base + kQOffW3, &maps.w3, 0, 0, 0, bar(Q_W3));
+      mbar_arrive_expect_tx(bar(Q_W3), (uint32_t)(kQCP * QH2 * 2));
+      tma_load_3d(base + L::W3, &maps.w3, 0, 0, 0, bar(Q_W3));
       uint32_t n = 0, slot = 0, use = 0;   // blocks issued; ring position of the next
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-        for (int kb = 0; kb < kQH2 / 64; ++kb) {
+        for (int kb = 0; kb < NB; ++kb) {
           if (use > 0 && !wait_bar(bar(Q_EMPTY + slot), (use - 1) & 1, g)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(Q_FULL + slot), (uint32_t)kBlk);
           tma_load_2d(base + slot * kBlk, &maps.h2, kb * 64, tile * 128, bar(Q_FULL + slot));
@@ -478,12 +486,12 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
         // Z = H2 W3^T into [kQTZ, kQTZ + 16), block by block as they land,
         // once the loss of the previous tile has read Z
         if (t > 0 && !wait_bar(bar(Q_ZFREE), (t - 1) & 1, g)) break;
-        for (int kb = 0; kb < kQH2 / 64 && ok; ++kb) {
+        for (int kb = 0; kb < NB && ok; ++kb) {
           if (!wait_bar(bar(Q_FULL + slot), use & 1, g)) { ok = false; break; }
           tc_fence_after();
           for (int kk = 0; kk < 4; ++kk)
             tc_mma_bf16(tmem + kQTZ, sdesc_sw128(base + slot * kBlk + kk * 32, 16, 1024),
-                        sdesc_sw128(base + kQOffW3 + kb * kQCP * 128 + kk * 32, 16, 1024), idz,
+                        sdesc_sw128(base + L::W3 + kb * kQCP * 128 + kk * 32, 16, 1024), idz,
                         (kb | kk) ? 1u : 0u);
           if (++slot == kQR) { slot = 0; ++use; }
         }
@@ -494,11 +502,11 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
         // (leading byte offset: one block) and its 16 rows (stride byte
         // offset: 8 rows of 128 bytes)
         if (!wait_bar(bar(Q_DZRDY), t & 1, g)) break;
-        for (int j = 0; j < 4 && ok; ++j) {
+        for (int j = 0; j < NQ && ok; ++j) {
           if (qu > 0 && !wait_bar(bar(Q_QFREE + qb), (qu - 1) & 1, g)) { ok = false; break; }
           tc_fence_after();
-          tc_mma_bf16(tmem + qb * 128, sdesc_sw32(base + kQOffNDZ, 256),
-                      sdesc_sw128(base + kQOffW3 + 2 * j * kQCP * 128, kQCP * 128, 1024), idq,
+          tc_mma_bf16(tmem + qb * 128, sdesc_sw32(base + L::NDZ, 256),
+                      sdesc_sw128(base + L::W3 + 2 * j * kQCP * 128, kQCP * 128, 1024), idq,
                       0u);
           tc_commit(bar(Q_QFULL + qb));
           if (++qb == 3) { qb = 0; ++qu; }
@@ -564,7 +572,7 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
           const int off = (i ^ ((rl >> 2) & 1)) << 4;
           *reinterpret_cast<uint4*>(drow + off) = u;
           constexpr uint32_t kSign = 0x80008000u;   // -dz: both bf16 sign bits flipped
-          *reinterpret_cast<uint4*>(drow + (kQOffNDZ - kQOffDZ) + off) =
+          *reinterpret_cast<uint4*>(drow + (L::NDZ - L::DZ) + off) =
               make_uint4(u.x ^ kSign, u.y ^ kSign, u.z ^ kSign, u.w ^ kSign);
         }
         fence_proxy_async_smem();
@@ -584,7 +592,7 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
         if (tile + (int)gridDim.x < p.tiles) load_row_in(in, nrow, nrow < p.M, p.shape, p.rows);
       }
       bool ok = true;
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < NQ; ++j) {
         const int kb = 2 * j + gi;
         const int slot = ts + kb < kQR ? ts + kb : ts + kb - kQR;
         uint8_t* blk = ring + slot * kBlk;
@@ -593,7 +601,7 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
         if (!wait_bar(bar(Q_FULL + slot), ((n0 + kb) / kQR) & 1, g) ||
             !wait_bar(bar(Q_QFULL + qb), qu & 1, g)) { ok = false; break; }
         tc_fence_after();
-        epi_dact_block(tmem + lanes + qb * 128 + gi * 64, rl, p.act, blk, cs2 + q * kQH2 + kb * 64,
+        epi_dact_block(tmem + lanes + qb * 128 + gi * 64, rl, p.act, blk, cs2 + q * QH2 + kb * 64,
                        lane, release);
         tc_fence_before();
         mbar_arrive(bar(Q_QFREE + qb));
@@ -607,8 +615,8 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
         if (++qb == 3) { qb = 0; ++qu; }
       }
       if (!ok) break;
-      ts = ts + 8 < kQR ? ts + 8 : ts + 8 - kQR;
-      n0 += 8;
+      ts = ts + NB < kQR ? ts + NB : ts + NB - kQR;
+      n0 += NB;
     }
     if (loss_w) loss_warp_reduce(adz, at6, adl, cs3 + q * 32, lp + q * kLossPartials, lane);
     if (lane == 0) bulk_wait0();
@@ -637,8 +645,8 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
     auto quad = [&](const float* b, int ld, int c) {
       return ((b[c] + b[ld + c]) + b[2 * ld + c]) + b[3 * ld + c];
     };
-    for (int c = et; c < kQH2; c += kHEpi)
-      p.cs2[(int64_t)blockIdx.x * kQH2 + c] = quad(cs2, kQH2, c);
+    for (int c = et; c < QH2; c += kHEpi)
+      p.cs2[(int64_t)blockIdx.x * QH2 + c] = quad(cs2, QH2, c);
     if (et < kQCP) p.cs3[(int64_t)blockIdx.x * kQCP + et] = quad(cs3, 32, et);
     if (et < kLossPartials)
       p.lossp[(int64_t)blockIdx.x * kLossPartials + et] = quad(lp, kLossPartials, et);
@@ -656,11 +664,20 @@ cudaError_t launch_t(const HMaps& m, const HParams& p, int grid, cudaStream_t st
   return launch_pdl(hl2_kernel<H2, CP>, dim3(grid), dim3(kHThreads), (size_t)kSmemBytes, st, m, p);
 }
 
-template <class Masks>
+template <int QH2, class Masks>
 cudaError_t launch_q(const HMaps& m, const HParams& p, Masks masks, int grid, cudaStream_t st) {
-  return launch_pdl(hlq_kernel<Masks>, dim3(grid), dim3(kHThreads), (size_t)kQSmemBytes, st, m, p,
-                    masks);
+  return launch_pdl(hlq_kernel<QH2, Masks>, dim3(grid), dim3(kHThreads), (size_t)QL<QH2>::Smem, st,
+                    m, p, masks);
 }
+
+template <int QH2, class Masks>
+cudaError_t set_attr_q() {
+  return cudaFuncSetAttribute(hlq_kernel<QH2, Masks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              QL<QH2>::Smem);
+}
+
+// the quarter kernel's shapes: H2 = 256 or 512 with 16 head columns
+bool quarter_shape(const NetShape& s) { return (s.H2 == 256 || s.H2 == 512) && s.CP == kQCP; }
 
 }  // namespace
 
@@ -669,17 +686,15 @@ bool hl2_supported(const NetShape& s) {
 }
 
 bool hl2_preferred(const NetShape& s) {
-  return hl2_supported(s) && s.H2 == kQH2 && s.CP == kQCP;
+  return hl2_supported(s) && quarter_shape(s);
 }
 
 cudaError_t hl2_prepare() {
   const cudaError_t errs[] = {
       set_attr<128, 16>(), set_attr<128, 32>(), set_attr<256, 16>(), set_attr<256, 32>(),
       set_attr<512, 16>(), set_attr<512, 32>(),
-      cudaFuncSetAttribute(hlq_kernel<FixedMasks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kQSmemBytes),
-      cudaFuncSetAttribute(hlq_kernel<ShapeMasks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kQSmemBytes)};
+      set_attr_q<256, FixedMasks>(), set_attr_q<256, ShapeMasks>(),
+      set_attr_q<512, FixedMasks>(), set_attr_q<512, ShapeMasks>()};
   for (cudaError_t e : errs)
     if (e != cudaSuccess) return e;
   return cudaSuccess;
@@ -689,7 +704,7 @@ cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int*
   const NetShape& s = f.s;
   if (!hl2_supported(s) || f.M < 1) return cudaErrorInvalidValue;
   // H2 = 512 with 16 head columns: the quarter kernel (dz in 32-byte rows)
-  const bool quarters = s.H2 == kQH2 && s.CP == kQCP;
+  const bool quarters = quarter_shape(s);
   HMaps m;
   cudaError_t e;
   if ((e = tc_make_tmap(&m.h2, f.H2, s.H2, f.M, s.H2, 64, 128)) != cudaSuccess) return e;
@@ -725,8 +740,10 @@ cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int*
   const int grid = p.tiles < num_sms ? p.tiles : num_sms;
   if (grid_out) *grid_out = grid;
   if (quarters)
-    return p.layout9222 ? launch_q(m, p, FixedMasks{}, grid, st)
-                        : launch_q(m, p, ShapeMasks{head_masks(s)}, grid, st);
+    return s.H2 == 512 ? (p.layout9222 ? launch_q<512>(m, p, FixedMasks{}, grid, st)
+                                       : launch_q<512>(m, p, ShapeMasks{head_masks(s)}, grid, st))
+                       : (p.layout9222 ? launch_q<256>(m, p, FixedMasks{}, grid, st)
+                                       : launch_q<256>(m, p, ShapeMasks{head_masks(s)}, grid, st));
   const bool c32 = s.CP == 32;
   switch (s.H2) {
     case 128: return c32 ? launch_t<128, 32>(m, p, grid, st) : launch_t<128, 16>(m, p, grid, st);

@@ -69,7 +69,7 @@ def mode_kwargs(mode):
     """Context options of the bf16 minibatch paths: forward, loss and
     backward-data fused in one kernel (where the network fits it); one kernel
     per GEMM stage; the same with head + loss and layer-2 backward-data in one
-    kernel (the default where H2 = 512 with 16 head columns); and the
+    kernel (the default where H2 = 256 or 512 with 16 head columns); and the
     persistent cooperative kernel."""
     return {"fused": {"fused_mlp": 1}, "per_stage": {"fused_loss": -1},
             "fused_loss": {"fused_loss": 1},
