@@ -841,7 +841,8 @@ def run_drive(args):
         B, mb = w.B, w.B // w.minibatches
         big = B * w.obs_dim > 2e8
         ro = synth.rollout(w, with_obs=not big)
-        ctx = P.Context(P.config_from_workload(w), synth.init_params(w))
+        ctx = P.Context(P.config_from_workload(w, fused_loss=args.fused_loss),
+                        synth.init_params(w))
         d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
         obs = torch.randn(B, w.obs_dim, device="cuda", generator=g) if big else d(ro.obs)
         if args.drive == "minibatch":
@@ -918,6 +919,9 @@ def main():
                                         "rnn_update", "muon"],
                     help="plain driver loop for profilers (no timing, no JSON line)")
     ap.add_argument("--reps", type=int, default=3, help="--drive: repetitions")
+    ap.add_argument("--fused-loss", type=int, default=0, choices=[-1, 0, 1],
+                    help="--drive minibatch/update: the context's fused_loss (-1 two kernels, "
+                         "0 the library's choice, 1 fused wherever it applies)")
     ap.add_argument("--drive-T", type=int, default=0,
                     help="--drive minibatch/update: horizon of a smaller rollout of the workload "
                          "(minibatch size kept)")
