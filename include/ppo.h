@@ -104,12 +104,10 @@ typedef struct {
     int32_t fused_loss;          /* bf16 mode: head + loss and
                                     dP2 = (dz W3) * act'(H2) as one kernel
                                     that reads each tile of H2 once, or as two
-                                    kernels.  -1: two kernels; 0 (default):
-                                    one kernel where it is the faster choice
-                                    (H2 = 256 or 512 with at most 16 head
-                                    columns), else two; 1: one kernel wherever it
-                                    applies (H2 in {128, 256, 512}, at most 32
-                                    head columns).  Same results up to fp32
+                                    kernels.  -1: two kernels; 0 (default) or
+                                    1: one kernel where it applies (H2 = 256
+                                    or 512 with at most 16 head columns), two
+                                    elsewhere.  Same results up to fp32
                                     summation order.                         */
     int32_t adv_mode;            /* advantages of ppo_update:
                                     0 (default) GAE once per update over the

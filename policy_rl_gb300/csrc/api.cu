@@ -462,9 +462,7 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
       f.W1s = c->sh.W1s;
       f.W2s = c->sh.W2s;
       f.W3s = c->sh.W3s;
-      f.W3Ts = c->sh.W3Ts;
       f.W2Ts = c->sh.W2Ts;
-      f.ld3t = c->sh.ld3t;
       f.b1 = P + s.ob1;
       f.b2 = P + s.ob2;
       f.b3 = P + s.ob3;
@@ -503,8 +501,6 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
       f.M = M;
       f.H2 = H2;
       f.W3s = c->sh.W3s;
-      f.W3Ts = c->sh.W3Ts;
-      f.ld3t = c->sh.ld3t;
       f.b3 = P + s.ob3;
       f.logstd = P + s.ologstd;
       f.dZ = dZ;
@@ -1032,8 +1028,7 @@ ppo_status ppo_create(const ppo_config* cfg, const float* h_init_params, ppo_ctx
               cfg->optimizer == 0;   // the persistent kernel runs Adam itself
   c->use_fmlp = c->bf16 && !c->use_mk && cfg->fused_mlp != 0 && cfg->adv_mode == 0 &&
                 fmlp_supported(s);
-  c->use_hl2 = c->bf16 && !c->use_mk &&
-               (cfg->fused_loss > 0 ? hl2_supported(s) : cfg->fused_loss == 0 && hl2_preferred(s));
+  c->use_hl2 = c->bf16 && !c->use_mk && cfg->fused_loss >= 0 && hl2_supported(s);
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (c->num_sms < 1) c->num_sms = 1;
   c->mbmax = cfg->max_minibatch;

@@ -338,8 +338,7 @@ struct FusedMlp {
 struct HeadLossDact {
   NetShape s;
   int M;
-  const __nv_bfloat16 *H2, *W3s, *W3Ts;
-  int ld3t;
+  const __nv_bfloat16 *H2, *W3s;
   const float *b3, *logstd;
   __nv_bfloat16 *dZ, *dP2;
   int lddz;
@@ -350,9 +349,8 @@ struct HeadLossDact {
   int* err;
   uint64_t timeout_ns;
 };
+// shapes of the fused kernel: H2 = 256 or 512 with 16 head columns
 bool hl2_supported(const NetShape& s);
-// shapes where the fused kernel beats the two-kernel path (H2 = 256 or 512, CP = 16)
-bool hl2_preferred(const NetShape& s);
 cudaError_t hl2_prepare();
 cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int* grid_out);
 

@@ -11,24 +11,8 @@
 // TMA stores.  dz stays in shared memory as the A operand of dz W3 (K = CP)
 // and goes to HBM for the weight gradient of W3.  Compared with a head+loss
 // kernel followed by a separate backward-data kernel this reads H2 once
-// instead of twice and drops the dz round trip and one launch.
-//
-// Two kernels:
-//  - hlq_kernel (H2 = 256 or 512, CP = 16; below): H2 streams through a ring of
-//    64-column blocks and dP2 comes in 128-column quarters, so that the next
-//    tile's head product and loss overlap this tile's epilogue.
-//  - hl2_kernel (the other shapes): the whole tile stays in shared memory.
-//    For H2 <= 256 two tiles fit, so the next tile's H2 is loaded while the
-//    current one is processed.  dz goes to a 128 x 64 shared tile; W3 is
-//    resident for the whole kernel and W3^T streams in 256-row boxes.
-//    Roles: warp 0 TMA, warp 1 MMA, warps 2..5 the loss and warps 6..9 the
-//    dP2 epilogue (TMEM lane quarter q = warp % 4 in each group), so that the
-//    loss of one tile overlaps the dP2 epilogue of the previous one.  With
-//    H2 = 512 only one tile fits and the loss warps then work on dP2 as well.
-//    TMEM: R_A = columns [0, 256) holds Z (first CP columns) and then the
-//    second 256-column half of dP2 (H2 = 512); R_B = [256, 512) holds the
-//    first half of dP2.
-// Every wait is bounded.
+// instead of twice and drops the dz round trip and one launch.  Shapes:
+// H2 = 256 or 512 with CP = 16 head columns.  Every wait is bounded.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -48,33 +32,11 @@ constexpr int kHThreads = kHWarps * kWarp;
 constexpr int kHEpi = 8 * kWarp;
 constexpr int kHGrp = 4 * kWarp;   // one epilogue group
 constexpr int kBlk = 128 * 128;   // 128 rows x 64 bf16 columns (16 KB)
-constexpr int kH2Max = 512;
-
-constexpr int kOffHS = 0;                         // H2 / dP2 tile: up to 8 blocks
-constexpr int kOffW3 = kOffHS + 8 * kBlk;         // W3 [CP][H2] as H2/64 blocks of CP rows
-constexpr int kOffW3T = kOffW3 + 32 * 1024;       // one [<= 256][64] box of W3^T
-constexpr int kOffDZ = kOffW3T + 32 * 1024;       // dz tile, 128 rows x 64 columns
-constexpr int kOffCtrl = kOffDZ + kBlk;
 constexpr int kCtrlBytes = 512;
-constexpr int kOffCs2 = kOffCtrl + kCtrlBytes;    // [4][kH2Max]
-constexpr int kOffCs3 = kOffCs2 + 4 * kH2Max * 4; // [4][32]
-constexpr int kOffLp = kOffCs3 + 4 * 32 * 4;      // [4][kLossPartials]
-constexpr int kOffB3 = kOffLp + 4 * kLossPartials * 4;
-constexpr int kSmemBytes = 1024 + kOffB3 + 32 * 4;
-
-// H2 blocks (128 rows x 64 columns, 16 KB) have a full and an empty barrier
-// each: slot hb * 4 + kb holds block kb of the tile in buffer hb.  A dP2
-// half releases its blocks as soon as its stores have read them, so the next
-// tile's blocks load while the rest of the current tile is processed.
-constexpr int kSlots = 8;
-enum Bar : int {
-  B_HSF = 0, B_HSE = kSlots, B_W3_FULL = 2 * kSlots, B_W3T_FULL, B_W3T_EMPTY, B_ZFULL, B_DZ_RDY,
-  B_P0, B_P1, B_RA_FREE, B_RB_FREE, B_DRAIN, B_COUNT
-};
 
 struct HMaps {
-  CUtensorMap h2, w3, w3t;   // loads
-  CUtensorMap dz, dp2;       // stores (32-row x 64-column boxes)
+  CUtensorMap h2, w3;   // loads
+  CUtensorMap dz, dp2;  // stores (32-row boxes)
 };
 
 struct HParams {
@@ -99,262 +61,6 @@ struct ShapeMasks {
   HeadMasks m;
   __device__ HeadMasks get() const { return m; }
 };
-
-template <int H2, int CP>
-__global__ void __launch_bounds__(kHThreads, 1)
-hl2_kernel(const __grid_constant__ HMaps maps, const HParams p) {
-  constexpr int NH = H2 > 256 ? 2 : 1;        // dP2 halves of <= 256 columns
-  constexpr int HN = H2 > 256 ? 256 : H2;     // columns per half
-  constexpr int NB = H2 / 64;                 // 64-column blocks of H2
-  constexpr int NBUF = H2 <= 256 ? 2 : 1;     // H2 tiles in shared memory (next one prefetched)
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gb = smem_raw + (base - raw);
-  uint8_t* HS = gb + kOffHS;
-  uint8_t* DZ = gb + kOffDZ;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gb + kOffCtrl);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + B_COUNT);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-  volatile uint32_t* cnt = reinterpret_cast<volatile uint32_t*>(tslot + 2);  // HS loads, W3T loads, W3T consumed
-  float* cs2 = reinterpret_cast<float*>(gb + kOffCs2);
-  float* cs3 = reinterpret_cast<float*>(gb + kOffCs3);
-  float* lp = reinterpret_cast<float*>(gb + kOffLp);
-  float* b3s = reinterpret_cast<float*>(gb + kOffB3);
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
-
-  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-  if (threadIdx.x == 0) {
-    for (int b = 0; b < kSlots; ++b) {
-      mbar_init(bar(B_HSF + b), 1);
-      mbar_init(bar(B_HSE + b), kHGrp);
-    }
-    mbar_init(bar(B_W3_FULL), 1);
-    mbar_init(bar(B_W3T_FULL), 1);
-    mbar_init(bar(B_W3T_EMPTY), 1);
-    mbar_init(bar(B_ZFULL), 1);
-    mbar_init(bar(B_DZ_RDY), kHGrp);
-    mbar_init(bar(B_P0), 1);
-    mbar_init(bar(B_P1), 1);
-    mbar_init(bar(B_RA_FREE), NBUF == 1 ? 2 * kHGrp : kHGrp);
-    mbar_init(bar(B_RB_FREE), NBUF == 1 ? 2 * kHGrp : kHGrp);
-    mbar_init(bar(B_DRAIN), 1);
-    *abort_flag = 0;
-    cnt[0] = 0;
-    cnt[1] = 0;
-    cnt[2] = 0;
-    fence_mbar_init();
-  }
-  for (int i = threadIdx.x; i < (kOffB3 - kOffCs2) / 4; i += kHThreads) cs2[i] = 0.f;
-  if (warp == 1) tmem_alloc(smem_u32(tslot), 512);
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&maps.h2);
-    prefetch_tmap(&maps.w3);
-    prefetch_tmap(&maps.w3t);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-  const Guard g{abort_flag, p.err, p.timeout_ns};
-  pdl_wait();
-  pdl_trigger();
-  for (int i = threadIdx.x; i < 32; i += kHThreads) b3s[i] = i < p.shape.C ? p.b3[i] : 0.f;
-  __syncthreads();   // reached by every thread of the block (before the role split)
-
-  if (warp == 0) {
-    if (lane == 0) {
-      bool ok = true;
-      mbar_arrive_expect_tx(bar(B_W3_FULL), (uint32_t)(CP * H2 * 2));
-      tma_load_3d(base + kOffW3, &maps.w3, 0, 0, 0, bar(B_W3_FULL));
-      uint32_t t = 0, wl = 0;
-      uint32_t nblk = 0;   // H2 blocks issued
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++t) {
-        // the tile's H2 blocks into buffer t % NBUF, each once that slot's
-        // block of the previous tile has been stored out of it
-        const int hb = t % NBUF;
-        const uint32_t hu = t / NBUF;
-        for (int kb = 0; kb < NB && ok; ++kb) {
-          const int slot = hb * 4 + kb;
-          if (hu > 0 && !wait_bar(bar(B_HSE + slot), (hu - 1) & 1, g)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(B_HSF + slot), (uint32_t)kBlk);
-          tma_load_2d(base + kOffHS + slot * kBlk, &maps.h2, kb * 64, tile * 128,
-                      bar(B_HSF + slot));
-          cnt[0] = ++nblk;
-        }
-        if (!ok) break;
-        // W3^T, one box per dP2 half (the buffer is free once the half's MMA is done)
-        for (int hf = 0; hf < NH && ok; ++hf, ++wl) {
-          if (wl > 0 && !wait_bar(bar(B_W3T_EMPTY), (wl - 1) & 1, g)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(B_W3T_FULL), (uint32_t)(HN * 128));
-          tma_load_2d(base + kOffW3T, &maps.w3t, 0, hf * 256, bar(B_W3T_FULL));
-          cnt[1] = wl + 1;
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t RA = tmem, RB = tmem + 256;
-      uint32_t t = 0, wl = 0;
-      bool ok = wait_bar(bar(B_W3_FULL), 0, g);
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++t) {
-        const uint32_t ph = t & 1, pph = (t - 1) & 1;
-        // Z = H2 W3^T into RA[0, CP): RA free once the previous tile drained it
-        const int hb = t % NBUF;
-        if (t > 0 && !wait_bar(bar(B_RA_FREE), pph, g)) break;
-        const uint32_t idz = idesc_bf16(128, CP, false, false);
-        for (int kb = 0; kb < NB && ok; ++kb) {   // block by block as they land
-          if (!wait_bar(bar(B_HSF + hb * 4 + kb), (t / NBUF) & 1, g)) { ok = false; break; }
-          tc_fence_after();
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(RA, sdesc_sw128(base + kOffHS + (hb * 4 + kb) * kBlk + kk * 32, 16, 1024),
-                        sdesc_sw128(base + kOffW3 + kb * CP * 128 + kk * 32, 16, 1024), idz,
-                        (kb | kk) ? 1u : 0u);
-        }
-        if (!ok) break;
-        tc_commit(bar(B_ZFULL));
-        // dP2 halves = dz W3 (K = CP): half 0 -> RB, half 1 -> RA (Z drained by then)
-        if (!wait_bar(bar(B_DZ_RDY), ph, g)) break;
-        const uint32_t idp = idesc_bf16(128, HN, false, false);
-        for (int hf = 0; hf < NH && ok; ++hf, ++wl) {
-          if (!wait_bar(bar(B_W3T_FULL), wl & 1, g)) { ok = false; break; }
-          if (hf == 0 && t > 0 && !wait_bar(bar(B_RB_FREE), pph, g)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t d = hf == 0 ? RB : RA;
-          for (int kk = 0; kk < CP / 16; ++kk)
-            tc_mma_bf16(d, sdesc_sw128(base + kOffDZ + kk * 32, 16, 1024),
-                        sdesc_sw128(base + kOffW3T + kk * 32, 16, 1024), idp, kk ? 1u : 0u);
-          tc_commit(bar(B_W3T_EMPTY));
-          tc_commit(bar(hf == 0 ? B_P0 : B_P1));
-          cnt[2] = wl + 1;
-        }
-      }
-    }
-  } else {
-    // two epilogue groups of four warps (TMEM lane quarter q = warp % 4 each):
-    // warps 2..5 run the loss of tile t+1 while warps 6..9 finish dP2 of tile t
-    const int q = warp & 3;
-    const bool loss_grp = warp < 6;
-    const int rl = q * 32 + lane;
-    const uint32_t lanes = (uint32_t)(q * 32) << 16;
-    const uint32_t RA = tmem + lanes, RB = tmem + 256 + lanes;
-    auto store_rows = [&](const CUtensorMap* m, const uint8_t* tile_base, int blk0, int nblk,
-                          int row0) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && row0 + q * 32 < p.M) {   // boxes wholly below the last row are skipped
-        for (int b = blk0; b < blk0 + nblk; ++b)
-          tma_store_2d(m, smem_u32(tile_base + b * kBlk + q * 4096), b * 64, row0 + q * 32);
-        bulk_commit();
-      }
-      __syncwarp();
-    };
-    auto stores_read = [&]() {
-      if (lane == 0) bulk_wait_read0();
-      __syncwarp();
-    };
-    auto run = [&](auto masks) {
-    const HeadMasks hm = masks.get();
-    uint32_t t = 0;
-    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++t) {
-      const uint32_t ph = t & 1;
-      const int hb = t % NBUF;
-      uint8_t* hs = HS + hb * 4 * kBlk;
-      const int row0 = tile * 128;
-      const int row = row0 + rl;
-      const bool rok = row < p.M;
-      if (loss_grp) {
-        // loss on Z (one row per thread) -> dz tile.  ZFULL(t) is committed after
-        // the dP2 products of tile t-1, which read the dz tile: it is free.  The
-        // row inputs are loaded before the wait.
-        RowIn in;
-        load_row_in(in, row, rok, p.shape, p.rows);
-        if (!wait_bar(bar(B_ZFULL), ph, g)) break;
-        tc_fence_after();
-        float dzr[32], t6[6], dls[4];
-        loss_row_in<CP>(RA, rok, p.shape, hm, p.lc, p.inv_mb, in, p.logstd, b3s, dzr, t6, dls);
-        uint8_t* drow = DZ + rl * 128;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint4 u = make_uint4(0u, 0u, 0u, 0u);
-          if (i < CP / 8) {
-            u.x = pack_bf16x2(dzr[8 * i + 0], dzr[8 * i + 1]);
-            u.y = pack_bf16x2(dzr[8 * i + 2], dzr[8 * i + 3]);
-            u.z = pack_bf16x2(dzr[8 * i + 4], dzr[8 * i + 5]);
-            u.w = pack_bf16x2(dzr[8 * i + 6], dzr[8 * i + 7]);
-          }
-          *reinterpret_cast<uint4*>(drow + ((i ^ (rl & 7)) << 4)) = u;
-        }
-        loss_warp_reduce(dzr, t6, dls, cs3 + q * 32, lp + q * kLossPartials, lane);
-        tc_fence_before();
-        store_rows(&maps.dz, DZ, 0, 1, row0);
-        stores_read();   // the dz tile is rewritten with the next tile
-        mbar_arrive(bar(B_DZ_RDY));
-        if (NH == 1) mbar_arrive(bar(B_RA_FREE));   // RA held only Z
-      }
-      if (!loss_grp || NBUF == 1) {
-        // dP2 halves, in place in HS, stored.  With one H2 buffer the loss group
-        // has nothing to overlap and joins in: each of the GW warps takes the
-        // rows of its lane quarter and CB of the half's 64-column blocks.
-        constexpr int GW = NBUF == 1 ? 8 : 4;
-        constexpr int CB = HN / 64 / (GW / 4);
-        const int gi = NBUF == 1 && !loss_grp ? 1 : 0;
-        bool ok = true;
-        for (int hf = 0; hf < NH; ++hf) {
-          if (!wait_bar(bar(hf == 0 ? B_P0 : B_P1), ph, g)) { ok = false; break; }
-          tc_fence_after();
-          epi_dact_smem_tile<HN, GW>(hf == 0 ? RB : RA, rl, rok, hf * 256, gi, p.act,
-                                     hs + hf * 4 * kBlk, cs2 + q * kH2Max, lane);
-          tc_fence_before();
-          store_rows(&maps.dp2, hs, hf * 4 + gi * CB, CB, row0);
-          mbar_arrive(bar(hf == 0 ? B_RB_FREE : B_RA_FREE));
-          stores_read();   // the blocks are reloaded after this
-          for (int j = 0; j < CB; ++j) mbar_arrive(bar(B_HSE + hb * 4 + hf * 4 + gi * CB + j));
-        }
-        if (!ok) break;
-      }
-    }
-    };
-    if (loss_grp && p.layout9222)
-      run(FixedMasks{});
-    else
-      run(ShapeMasks{head_masks(p.shape)});
-    if (lane == 0) bulk_wait0();
-  }
-
-  __syncthreads();
-  if (*abort_flag) {
-    if (threadIdx.x == 0) {   // loads in flight: the last H2 blocks and W3^T box
-      const uint32_t hl = cnt[0], wl = cnt[1];
-      for (uint32_t l = hl >= (uint32_t)(NBUF * NB) ? hl - NBUF * NB : 0; l < hl; ++l) {
-        const uint32_t tl = l / NB;   // the block's tile (in this CTA's order) and slot
-        drain_wait(bar(B_HSF + (tl % NBUF) * 4 + l % NB), (tl / NBUF) & 1, p.timeout_ns);
-      }
-      if (wl > 0) drain_wait(bar(B_W3T_FULL), (wl - 1) & 1, p.timeout_ns);
-      drain_wait(bar(B_W3_FULL), 0, p.timeout_ns);
-    }
-    if (warp == 1 && lane == 0) {
-      tc_commit(bar(B_DRAIN));
-      drain_wait(bar(B_DRAIN), 0, p.timeout_ns);
-    }
-    __syncthreads();
-  }
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-  if (warp >= 2) {
-    const int et = threadIdx.x - 2 * kWarp;
-    auto quad = [&](const float* b, int ld, int c) {
-      return ((b[c] + b[ld + c]) + b[2 * ld + c]) + b[3 * ld + c];
-    };
-    for (int c = et; c < H2; c += kHEpi)
-      p.cs2[(int64_t)blockIdx.x * H2 + c] = quad(cs2, kH2Max, c);
-    if (et < CP) p.cs3[(int64_t)blockIdx.x * CP + et] = quad(cs3, 32, et);
-    if (et < kLossPartials)
-      p.lossp[(int64_t)blockIdx.x * kLossPartials + et] = quad(lp, kLossPartials, et);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // H2 = 256 or 512, CP = 16: a tile's dP2 in 128-column quarters (two or
@@ -653,17 +359,6 @@ hlq_kernel(const __grid_constant__ HMaps maps, const HParams p, Masks masks) {
   }
 }
 
-template <int H2, int CP>
-cudaError_t set_attr() {
-  return cudaFuncSetAttribute(hl2_kernel<H2, CP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemBytes);
-}
-
-template <int H2, int CP>
-cudaError_t launch_t(const HMaps& m, const HParams& p, int grid, cudaStream_t st) {
-  return launch_pdl(hl2_kernel<H2, CP>, dim3(grid), dim3(kHThreads), (size_t)kSmemBytes, st, m, p);
-}
-
 template <int QH2, class Masks>
 cudaError_t launch_q(const HMaps& m, const HParams& p, Masks masks, int grid, cudaStream_t st) {
   return launch_pdl(hlq_kernel<QH2, Masks>, dim3(grid), dim3(kHThreads), (size_t)QL<QH2>::Smem, st,
@@ -676,25 +371,16 @@ cudaError_t set_attr_q() {
                               QL<QH2>::Smem);
 }
 
-// the quarter kernel's shapes: H2 = 256 or 512 with 16 head columns
-bool quarter_shape(const NetShape& s) { return (s.H2 == 256 || s.H2 == 512) && s.CP == kQCP; }
 
 }  // namespace
 
 bool hl2_supported(const NetShape& s) {
-  return (s.H2 == 128 || s.H2 == 256 || s.H2 == 512) && (s.CP == 16 || s.CP == 32) && s.G <= 4;
-}
-
-bool hl2_preferred(const NetShape& s) {
-  return hl2_supported(s) && quarter_shape(s);
+  return (s.H2 == 256 || s.H2 == 512) && s.CP == kQCP && s.G <= 4;
 }
 
 cudaError_t hl2_prepare() {
-  const cudaError_t errs[] = {
-      set_attr<128, 16>(), set_attr<128, 32>(), set_attr<256, 16>(), set_attr<256, 32>(),
-      set_attr<512, 16>(), set_attr<512, 32>(),
-      set_attr_q<256, FixedMasks>(), set_attr_q<256, ShapeMasks>(),
-      set_attr_q<512, FixedMasks>(), set_attr_q<512, ShapeMasks>()};
+  const cudaError_t errs[] = {set_attr_q<256, FixedMasks>(), set_attr_q<256, ShapeMasks>(),
+                              set_attr_q<512, FixedMasks>(), set_attr_q<512, ShapeMasks>()};
   for (cudaError_t e : errs)
     if (e != cudaSuccess) return e;
   return cudaSuccess;
@@ -703,23 +389,14 @@ cudaError_t hl2_prepare() {
 cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int* grid_out) {
   const NetShape& s = f.s;
   if (!hl2_supported(s) || f.M < 1) return cudaErrorInvalidValue;
-  // H2 = 512 with 16 head columns: the quarter kernel (dz in 32-byte rows)
-  const bool quarters = quarter_shape(s);
   HMaps m;
   cudaError_t e;
   if ((e = tc_make_tmap(&m.h2, f.H2, s.H2, f.M, s.H2, 64, 128)) != cudaSuccess) return e;
+  // W3 as H2/64 blocks of its 16 rows: the B operand of both products
   if ((e = tc_make_tmap_blocks(&m.w3, f.W3s, s.CP, s.H2, s.H2 / 64, s.CP, s.H2 / 64)) !=
       cudaSuccess)
     return e;
-  if (quarters) {   // (no W3^T map: the kernel reads W3 for both products)
-    m.w3t = m.w3;
-    if ((e = tc_make_tmap(&m.dz, f.dZ, kQCP, f.M, f.lddz, kQCP, 32, 32)) != cudaSuccess) return e;
-  } else {
-    if ((e = tc_make_tmap(&m.w3t, f.W3Ts, 64, s.H2, f.ld3t, 64, s.H2 > 256 ? 256 : s.H2)) !=
-        cudaSuccess)
-      return e;
-    if ((e = tc_make_tmap(&m.dz, f.dZ, 64, f.M, f.lddz, 64, 32)) != cudaSuccess) return e;
-  }
+  if ((e = tc_make_tmap(&m.dz, f.dZ, kQCP, f.M, f.lddz, kQCP, 32, 32)) != cudaSuccess) return e;
   if ((e = tc_make_tmap(&m.dp2, f.dP2, s.H2, f.M, s.H2, 64, 32)) != cudaSuccess) return e;
   HParams p{};
   p.M = f.M;
@@ -739,17 +416,10 @@ cudaError_t hl2_launch(const HeadLossDact& f, int num_sms, cudaStream_t st, int*
   p.layout9222 = is_layout_9222(s) ? 1 : 0;
   const int grid = p.tiles < num_sms ? p.tiles : num_sms;
   if (grid_out) *grid_out = grid;
-  if (quarters)
-    return s.H2 == 512 ? (p.layout9222 ? launch_q<512>(m, p, FixedMasks{}, grid, st)
-                                       : launch_q<512>(m, p, ShapeMasks{head_masks(s)}, grid, st))
-                       : (p.layout9222 ? launch_q<256>(m, p, FixedMasks{}, grid, st)
-                                       : launch_q<256>(m, p, ShapeMasks{head_masks(s)}, grid, st));
-  const bool c32 = s.CP == 32;
-  switch (s.H2) {
-    case 128: return c32 ? launch_t<128, 32>(m, p, grid, st) : launch_t<128, 16>(m, p, grid, st);
-    case 256: return c32 ? launch_t<256, 32>(m, p, grid, st) : launch_t<256, 16>(m, p, grid, st);
-    default: return c32 ? launch_t<512, 32>(m, p, grid, st) : launch_t<512, 16>(m, p, grid, st);
-  }
+  return s.H2 == 512 ? (p.layout9222 ? launch_q<512>(m, p, FixedMasks{}, grid, st)
+                                     : launch_q<512>(m, p, ShapeMasks{head_masks(s)}, grid, st))
+                     : (p.layout9222 ? launch_q<256>(m, p, FixedMasks{}, grid, st)
+                                     : launch_q<256>(m, p, ShapeMasks{head_masks(s)}, grid, st));
 }
 
 }  // namespace ppo
