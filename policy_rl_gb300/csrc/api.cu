@@ -462,7 +462,9 @@ ppo_status enqueue_minibatch(ppo_ctx* c, const float* obs, const __nv_bfloat16* 
       f.W1s = c->sh.W1s;
       f.W2s = c->sh.W2s;
       f.W3s = c->sh.W3s;
+      f.W3Ts = c->sh.W3Ts;
       f.W2Ts = c->sh.W2Ts;
+      f.ld3t = c->sh.ld3t;
       f.b1 = P + s.ob1;
       f.b2 = P + s.ob2;
       f.b3 = P + s.ob3;

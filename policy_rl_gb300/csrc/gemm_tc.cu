@@ -851,6 +851,8 @@ cudaError_t get_encode() {
 cudaError_t make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
                       int box_cols, int box_rows,
                       CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  // a missing operand is an error here, never a tensor map over address 0
+  if (base == nullptr || cols < 1 || rows < 1 || ld < 1) return cudaErrorInvalidValue;
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -869,6 +871,7 @@ cudaError_t make_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t ro
 // fp32 split-K partials [splits][rows][cols] as 32-column x 32-row x 1-split boxes
 cudaError_t make_tmap_partials(CUtensorMap* m, const float* base, int64_t cols, int64_t rows,
                                int64_t splits) {
+  if (base == nullptr || cols < 1 || rows < 1 || splits < 1) return cudaErrorInvalidValue;
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)splits};
@@ -884,6 +887,7 @@ cudaError_t make_tmap_partials(CUtensorMap* m, const float* base, int64_t cols, 
 
 cudaError_t make_tmap_blocks(CUtensorMap* m, const void* base, int64_t rows, int64_t ld, int nblk,
                              int box_rows, int box_blk) {
+  if (base == nullptr || rows < 1 || nblk < 1 || ld < 1) return cudaErrorInvalidValue;
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)nblk};
